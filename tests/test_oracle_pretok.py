@@ -18,6 +18,8 @@ from exact_bpe_tokenization_gb300 import synth
 ALPHABETS = {
     1: ["a", "s", "1", " ", "\t", "\n", "\r", "'", ".", "é"],
     2: ["a", "B", "1", " ", "\n", "'", ".", "か", "́", "\U0001F642"],
+    # o200k contractions, case and marks together
+    3: ["s", "T", "'", "a", "か", "́", " ", ".", "E", "r"],
 }
 HAVE_REGEX = importlib.util.find_spec("regex") is not None
 
@@ -34,12 +36,12 @@ def oracle_pieces_batch(o, strings):
     return out
 
 
-@pytest.mark.parametrize("family", [1, 2])
-def test_brute_force_matcher_short_strings(family, masks):
+@pytest.mark.parametrize("family,alphabet", [(1, 1), (2, 2), (2, 3)])
+def test_brute_force_matcher_short_strings(family, alphabet, masks):
     """Independent AST backtracking matcher: every string of length <= 4 and
     a seeded sample of 3000 strings of length 5-8."""
     ast = brute.family_ast(family, masks)
-    alpha = ALPHABETS[family]
+    alpha = ALPHABETS[alphabet]
     strings = list(brute.all_strings(alpha, 4))
     rng = random.Random(family)
     strings += ["".join(rng.choice(alpha) for _ in range(rng.randint(5, 8))) for _ in range(3000)]
@@ -49,14 +51,14 @@ def test_brute_force_matcher_short_strings(family, masks):
 
 
 @pytest.mark.skipif(not HAVE_REGEX, reason="regex engine not installed")
-@pytest.mark.parametrize("family", [1, 2])
-def test_regex_engine_all_strings_up_to_6(family):
+@pytest.mark.parametrize("family,alphabet", [(1, 1), (2, 2), (2, 3)])
+def test_regex_engine_all_strings_up_to_6(family, alphabet):
     """Library run: the regex engine on every string of length <= 6 over the
     reduced alphabet (1,111,110 strings), fed to the oracle as one batch of
     tiny requests."""
     import regex
     pat = regex.compile(brute.REGEX_PATTERNS[family])
-    strings = list(brute.all_strings(ALPHABETS[family], 6))
+    strings = list(brute.all_strings(ALPHABETS[alphabet], 6))
     got = oracle_pieces_batch(oracle.pretokenizer(family), strings)
     bad = [s for s, g in zip(strings, got) if g != pat.findall(s)]
     assert not bad, [repr(s) for s in bad[:10]]
@@ -145,6 +147,10 @@ def test_o200k_case_contraction_marks():
     assert pt.pieces("..́a") == ["..́", "a"]           # after two others a mark stays "other"
     assert pt.pieces(" .́a") == [" .́", "a"]
     assert pt.pieces("́.́..") == ["́", ".́", ".."]
+    # contraction chain: letters used up by a contraction do not take another
+    assert pt.pieces("a'd'd") == ["a'd", "'d"]
+    assert pt.pieces("a'd'd'd") == ["a'd", "'d'd"]
+    assert pt.pieces("s'rE") == ["s'rE"]
 
 
 def test_request_boundaries_cut_runs():
