@@ -1,0 +1,584 @@
+// tt_api.cu - the C ABI of the exact BPE tokenizer (include/toktier.h):
+// handle creation (vocabulary validation and device table build), per-stream
+// workspaces, kernel sequencing (direct launches or a captured CUDA graph per
+// stream and capacity bucket), status, the pre-tokenizer test hook and
+// per-kernel timing.
+//
+// Design notes (TokTier: Exact Stateful CPU+GPU Tokenization for Agentic LLM
+// Serving, §4.3): piece counts, dispatch lists and output lengths stay in
+// device memory; kernel geometry depends on buffer capacity, not on counts,
+// so the whole bytes-to-IDs chain can be captured once per size bucket and
+// replayed with new buffers.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/toktier.h"
+#include "tt_common.cuh"
+#include "tt_kernels.h"
+#include "tt_char_classes.inc"   // TT_CLASS_RANGES, TT_CLASS_RANGE_COUNT, TT_CLASS_DIGEST (generated)
+
+using namespace tt;
+
+namespace {
+
+constexpr int N_KERNELS = 7;
+const char *KERNEL_NAMES[N_KERNELS] = {"k_prepass", "k_tilescan", "k_pretok", "k_bpe_small",
+                                       "k_bpe_long", "k_ids", "k_req"};
+
+struct Workspace {
+  Work W{};
+  void *mem = nullptr;
+  size_t mem_bytes = 0;
+  int64_t cap_bytes = 0, cap_reqs = 0;
+  cudaGraphExec_t graph = nullptr;
+  // device staging for tt_encode_host (bytes, offsets, ids, id offsets)
+  void *stage = nullptr;
+  size_t stage_bytes = 0;
+  std::vector<int64_t> h_offs;     // rebased host offsets
+};
+
+struct Pending { int kernel; cudaEvent_t a, b; };
+
+uint64_t next_pow2(uint64_t x) {
+  uint64_t p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+struct tt_tokenizer {
+  int family = 0;
+  int device = 0;
+  Tables T{};
+  std::vector<void *> dev_allocs;
+  DevStatus *d_status = nullptr;
+  std::mutex mu;
+  std::map<cudaStream_t, Workspace *> ws;
+  std::atomic<int64_t> launches{0};
+  bool profiling = false;
+  std::vector<Pending> pending;
+  std::vector<cudaEvent_t> event_pool;
+  double prof_ms[N_KERNELS] = {0};
+  int64_t prof_n[N_KERNELS] = {0};
+  bool graphs_enabled = true;
+};
+
+#define TT_CUDA(call)                                                   \
+  do {                                                                  \
+    cudaError_t e_ = (call);                                            \
+    if (e_ != cudaSuccess) {                                            \
+      fprintf(stderr, "toktier: %s failed: %s\n", #call, cudaGetErrorString(e_)); \
+      return TT_ERR_CUDA;                                               \
+    }                                                                   \
+  } while (0)
+
+static tt_status upload(tt_tokenizer *h, const void *src, size_t bytes, void **dst) {
+  void *p = nullptr;
+  if (cudaMalloc(&p, bytes ? bytes : 16) != cudaSuccess) return TT_ERR_OOM;
+  h->dev_allocs.push_back(p);
+  if (bytes) TT_CUDA(cudaMemcpy(p, src, bytes, cudaMemcpyHostToDevice));
+  *dst = p;
+  return TT_OK;
+}
+
+// raw kind of a code point from the probed property mask
+// (bits: L Lu Ll Lt Lm Lo M N \s)
+static uint8_t kind_from_mask(uint32_t m) {
+  if (m & 0x100) return K_WS;
+  if (m & 0x080) return K_NUM;
+  if (m & (0x002 | 0x008)) return K_LU;
+  if (m & 0x004) return K_LL;
+  if (m & (0x010 | 0x020)) return K_LB;
+  if (m & 0x040) return K_MARK;
+  return K_OTHER;
+}
+
+static tt_status build_class_tables(tt_tokenizer *h) {
+  std::vector<uint8_t> kind(0x110000, K_OTHER);
+  for (int i = 0; i < TT_CLASS_RANGE_COUNT; ++i)
+    for (uint32_t c = TT_CLASS_RANGES[i][0]; c <= TT_CLASS_RANGES[i][1]; ++c) kind[c] = kind_from_mask(TT_CLASS_RANGES[i][2]);
+  std::vector<uint16_t> stage1(0x110000 / 256);
+  std::vector<uint8_t> stage2;
+  std::map<std::string, int> seen;
+  for (int blk = 0; blk < 0x110000 / 256; ++blk) {
+    std::string key(reinterpret_cast<const char *>(&kind[blk * 256]), 256);
+    auto it = seen.find(key);
+    int idx;
+    if (it == seen.end()) {
+      idx = (int)seen.size();
+      seen.emplace(key, idx);
+      stage2.insert(stage2.end(), kind.begin() + blk * 256, kind.begin() + blk * 256 + 256);
+    } else {
+      idx = it->second;
+    }
+    stage1[blk] = (uint16_t)idx;
+  }
+  void *p1, *p2;
+  tt_status s;
+  if ((s = upload(h, stage1.data(), stage1.size() * 2, &p1)) != TT_OK) return s;
+  if ((s = upload(h, stage2.data(), stage2.size(), &p2)) != TT_OK) return s;
+  h->T.cls1 = (const uint16_t *)p1;
+  h->T.cls2 = (const uint8_t *)p2;
+  return TT_OK;
+}
+
+extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, const uint8_t *vocab_bytes,
+                               const int64_t *vocab_offsets, int64_t n_vocab, int32_t pattern_family,
+                               tt_tokenizer **out) {
+  if (!out) return TT_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (pattern_family != TT_FAMILY_CL100K_STYLE && pattern_family != TT_FAMILY_O200K_STYLE) return TT_ERR_BAD_FAMILY;
+  if (!vocab_offsets || n_vocab < 256 || n_vocab > (1 << MAX_VOCAB_BITS) || n_merges < 0 ||
+      n_merges > (1 << MAX_RANK_BITS) - 1 || (n_merges > 0 && !merge_pairs))
+    return n_vocab > (1 << MAX_VOCAB_BITS) || n_merges > (1 << MAX_RANK_BITS) - 1 ? TT_ERR_BAD_VOCAB : TT_ERR_INVALID_ARG;
+  // ---- vocabulary
+  const int64_t vbase = vocab_offsets[0];
+  if (vbase < 0) return TT_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < n_vocab; ++i) {
+    const int64_t len = vocab_offsets[i + 1] - vocab_offsets[i];
+    if (len < 1 || len > 4095) return TT_ERR_BAD_VOCAB;
+  }
+  const int64_t vtotal = vocab_offsets[n_vocab] - vbase;
+  if (vtotal > INT32_MAX || (vtotal > 0 && !vocab_bytes)) return TT_ERR_BAD_VOCAB;
+  std::unordered_map<std::string, int32_t> index;
+  index.reserve((size_t)n_vocab * 2);
+  int max_len = 0;
+  for (int64_t i = 0; i < n_vocab; ++i) {
+    const int64_t len = vocab_offsets[i + 1] - vocab_offsets[i];
+    std::string key(reinterpret_cast<const char *>(vocab_bytes + vocab_offsets[i]), (size_t)len);
+    if (!index.emplace(std::move(key), (int32_t)i).second) return TT_ERR_BAD_VOCAB;   // duplicate string
+    if (len > max_len) max_len = (int)len;
+  }
+  std::vector<int32_t> byte_id(256);
+  for (int b = 0; b < 256; ++b) {
+    auto it = index.find(std::string(1, (char)b));
+    if (it == index.end()) return TT_ERR_BAD_VOCAB;
+    byte_id[b] = it->second;
+  }
+  // ---- merges: operands, results, duplicates, well-ordering
+  std::vector<int32_t> result((size_t)n_merges);
+  std::vector<int64_t> creator((size_t)n_vocab, -1);
+  std::unordered_map<uint64_t, int64_t> pairs;
+  pairs.reserve((size_t)n_merges * 2);
+  for (int64_t k = 0; k < n_merges; ++k) {
+    const int32_t l = merge_pairs[2 * k], r = merge_pairs[2 * k + 1];
+    if (l < 0 || r < 0 || l >= n_vocab || r >= n_vocab) return TT_ERR_BAD_VOCAB;
+    std::string cat(reinterpret_cast<const char *>(vocab_bytes + vocab_offsets[l]),
+                    (size_t)(vocab_offsets[l + 1] - vocab_offsets[l]));
+    cat.append(reinterpret_cast<const char *>(vocab_bytes + vocab_offsets[r]),
+               (size_t)(vocab_offsets[r + 1] - vocab_offsets[r]));
+    auto it = index.find(cat);
+    if (it == index.end()) return TT_ERR_BAD_VOCAB;
+    result[k] = it->second;
+    if (!pairs.emplace(pair_key((uint32_t)l, (uint32_t)r), k).second) return TT_ERR_BAD_VOCAB;
+    if (creator[result[k]] >= 0) return TT_ERR_BAD_VOCAB;                 // two merges, one result
+    creator[result[k]] = k;
+  }
+  for (int64_t k = 0; k < n_merges; ++k) {
+    const int32_t ops[2] = {merge_pairs[2 * k], merge_pairs[2 * k + 1]};
+    for (int32_t x : ops)
+      if (creator[x] >= k) return TT_ERR_BAD_VOCAB;                        // used before it is made
+  }
+
+  tt_tokenizer *h = new tt_tokenizer();
+  h->family = pattern_family;
+  cudaGetDevice(&h->device);
+  tt_status s;
+  auto fail = [&](tt_status st) { tt_destroy(h); return st; };
+  if (pretok_configure() != cudaSuccess) return fail(TT_ERR_CUDA);
+  // ---- pair table
+  const uint64_t pcap = next_pow2((uint64_t)std::max<int64_t>(2 * n_merges, 1024));
+  std::vector<uint64_t> ptab(pcap, PAIR_EMPTY);
+  for (int64_t k = 0; k < n_merges; ++k) {
+    const uint32_t l = (uint32_t)merge_pairs[2 * k], r = (uint32_t)merge_pairs[2 * k + 1];
+    uint64_t sl = pair_hash(l, r) & (pcap - 1);
+    while (ptab[sl] != PAIR_EMPTY) sl = (sl + 1) & (pcap - 1);
+    ptab[sl] = (pair_key(l, r) << MAX_RANK_BITS) | (uint64_t)k;
+  }
+  // ---- vocab table
+  const uint64_t vcap = next_pow2((uint64_t)std::max<int64_t>(2 * n_vocab, 1024));
+  std::vector<uint64_t> vtab(vcap, 0);
+  for (int64_t i = 0; i < n_vocab; ++i) {
+    const int len = (int)(vocab_offsets[i + 1] - vocab_offsets[i]);
+    const uint64_t hh = hash_bytes(vocab_bytes + vocab_offsets[i], len);
+    uint64_t sl = hh & (vcap - 1);
+    while (vtab[sl] != 0) sl = (sl + 1) & (vcap - 1);
+    vtab[sl] = ((uint64_t)vocab_fp(hh) << 32) | ((uint64_t)len << 20) | (uint64_t)i;
+  }
+  std::vector<int32_t> voff32((size_t)n_vocab + 1);
+  for (int64_t i = 0; i <= n_vocab; ++i) voff32[i] = (int32_t)(vocab_offsets[i] - vbase);
+  void *p;
+  if ((s = upload(h, ptab.data(), ptab.size() * 8, &p)) != TT_OK) return fail(s);
+  h->T.pair_tab = (const uint64_t *)p;
+  h->T.pair_mask = (uint32_t)(pcap - 1);
+  if ((s = upload(h, result.data(), result.size() * 4, &p)) != TT_OK) return fail(s);
+  h->T.merge_result = (const int32_t *)p;
+  if ((s = upload(h, vtab.data(), vtab.size() * 8, &p)) != TT_OK) return fail(s);
+  h->T.vocab_tab = (const uint64_t *)p;
+  h->T.vocab_mask = (uint32_t)(vcap - 1);
+  if ((s = upload(h, vocab_bytes + vbase, (size_t)vtotal, &p)) != TT_OK) return fail(s);
+  h->T.vbytes = (const uint8_t *)p;
+  if ((s = upload(h, voff32.data(), voff32.size() * 4, &p)) != TT_OK) return fail(s);
+  h->T.voff = (const int32_t *)p;
+  if ((s = upload(h, byte_id.data(), 256 * 4, &p)) != TT_OK) return fail(s);
+  h->T.byte_id = (const int32_t *)p;
+  h->T.max_tok_len = max_len;
+  h->T.family = pattern_family;
+  if ((s = build_class_tables(h)) != TT_OK) return fail(s);
+  DevStatus init = {0, 0, ~0ull};
+  if ((s = upload(h, &init, sizeof(init), &p)) != TT_OK) return fail(s);
+  h->d_status = (DevStatus *)p;
+  const char *env = getenv("TOKTIER_NO_GRAPHS");
+  if (env && env[0] == '1') h->graphs_enabled = false;
+  *out = h;
+  return TT_OK;
+}
+
+static void free_workspace(Workspace *w) {
+  if (!w) return;
+  if (w->graph) cudaGraphExecDestroy(w->graph);
+  if (w->mem) cudaFree(w->mem);
+  if (w->stage) cudaFree(w->stage);
+  delete w;
+}
+
+extern "C" void tt_destroy(tt_tokenizer *h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  for (auto &kv : h->ws) free_workspace(kv.second);
+  for (auto &pd : h->pending) { cudaEventDestroy(pd.a); cudaEventDestroy(pd.b); }
+  for (cudaEvent_t e : h->event_pool) cudaEventDestroy(e);
+  for (void *p : h->dev_allocs) cudaFree(p);
+  delete h;
+}
+
+// Carve the workspace of one capacity bucket out of one allocation.
+static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_reqs, Workspace **out) {
+  Workspace *w = new Workspace();
+  w->cap_bytes = cap_bytes;
+  w->cap_reqs = cap_reqs;
+  const int64_t tiles = (cap_bytes + TILE - 1) / TILE + 1;
+  const int64_t chunks = (cap_bytes + 1 + IDS_CHUNK - 1) / IDS_CHUNK + 2;
+  struct Item { void **dst; size_t bytes; };
+  Work &W = w->W;
+  std::vector<Item> items = {
+      {(void **)&W.s1_sum, sizeof(int2) * tiles},       {(void **)&W.s1_carry, sizeof(int2) * tiles},
+      {(void **)&W.rq_sum, 2 * (size_t)tiles},          {(void **)&W.rq_carry, 2 * (size_t)tiles},
+      {(void **)&W.s2_agg, sizeof(S2) * tiles},         {(void **)&W.s2_inc, sizeof(S2) * tiles},
+      {(void **)&W.s2_flag, 4 * (size_t)tiles},         {(void **)&W.cnt_agg, 4 * (size_t)tiles},
+      {(void **)&W.cnt_inc, 4 * (size_t)tiles},         {(void **)&W.cnt_flag, 4 * (size_t)tiles},
+      {(void **)&W.ids_agg, 4 * (size_t)chunks},        {(void **)&W.ids_inc, 4 * (size_t)chunks},
+      {(void **)&W.ids_flag, 4 * (size_t)chunks},       {(void **)&W.counters, 4 * 16},
+      {(void **)&W.piece_start, 4 * (size_t)(cap_bytes + 2)}, {(void **)&W.n_ids, 4 * (size_t)(cap_bytes + 1)},
+      {(void **)&W.id_off, 4 * (size_t)(cap_bytes + 2)},      {(void **)&W.scratch, 4 * (size_t)(cap_bytes + 1)},
+      {(void **)&W.tmp_a, 4 * (size_t)(cap_bytes + 1)},       {(void **)&W.tmp_b, 4 * (size_t)(cap_bytes + 1)},
+      {(void **)&W.long_list, 4 * (size_t)(cap_bytes / (SMALL_MAX + 1) + 2)},
+      {(void **)&W.bad, (size_t)cap_reqs + 1},          {(void **)&W.bad_pre, 4 * (size_t)(cap_reqs + 2)},
+      {(void **)&W.args, sizeof(CallArgs)},
+  };
+  size_t total = 0;
+  for (auto &it : items) total += (it.bytes + 255) & ~(size_t)255;
+  if (cudaMalloc(&w->mem, total) != cudaSuccess) { delete w; return TT_ERR_OOM; }
+  w->mem_bytes = total;
+  size_t off = 0;
+  for (auto &it : items) {
+    *it.dst = (char *)w->mem + off;
+    off += (it.bytes + 255) & ~(size_t)255;
+  }
+  W.cap_bytes = cap_bytes;
+  W.cap_reqs = cap_reqs;
+  W.cap_tiles = (int32_t)tiles;
+  W.spin_limit = 1 << 22;
+  W.status = h->d_status;
+  if (cudaMemset(w->mem, 0, total) != cudaSuccess) { free_workspace(w); return TT_ERR_CUDA; }
+  *out = w;
+  return TT_OK;
+}
+
+// The workspace of `stream`, grown to hold (bytes, reqs).  Caller holds h->mu.
+// Capacities are powers of two (>= 64 KiB, >= 64 requests) so that a stream
+// sees few distinct buckets; growing drops the old bucket and its graph.
+static tt_status get_workspace(tt_tokenizer *h, cudaStream_t stream, int64_t bytes, int64_t reqs, Workspace **out) {
+  int64_t cb = (int64_t)next_pow2((uint64_t)std::max<int64_t>(bytes, 1 << 16));
+  int64_t cr = (int64_t)next_pow2((uint64_t)std::max<int64_t>(reqs, 64));
+  auto it = h->ws.find(stream);
+  if (it != h->ws.end()) {
+    Workspace *old = it->second;
+    if (old->cap_bytes >= cb && old->cap_reqs >= cr) {
+      *out = old;
+      return TT_OK;
+    }
+    cb = std::max(cb, old->cap_bytes);
+    cr = std::max(cr, old->cap_reqs);
+    cudaStreamSynchronize(stream);
+    free_workspace(old);
+    h->ws.erase(it);
+  }
+  Workspace *w;
+  tt_status s = make_workspace(h, cb, cr, &w);
+  if (s != TT_OK) return s;
+  h->ws[stream] = w;
+  *out = w;
+  return TT_OK;
+}
+
+static cudaEvent_t pool_event(tt_tokenizer *h) {
+  if (!h->event_pool.empty()) {
+    cudaEvent_t e = h->event_pool.back();
+    h->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// grid sizes, all from capacity
+static int grid_tiles(const Workspace *w) { return (int)((w->cap_bytes + TILE - 1) / TILE); }
+static int grid_chunks(const Workspace *w) { return (int)((w->cap_bytes + 1 + IDS_CHUNK - 1) / IDS_CHUNK); }
+static int grid_reqs(const Workspace *w) { return (int)((w->cap_reqs + 1 + 255) / 256); }
+static int grid_small(const Workspace *w) {
+  const int64_t g = (w->cap_bytes / 4 + BPE_SMALL_THREADS - 1) / BPE_SMALL_THREADS;
+  return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 8);
+}
+static int grid_long(const Workspace *w) { return 152 * 2; }
+
+// Enqueue the kernels of one encode on `stream` (eager; optionally timed).
+static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stream, bool timed) {
+  const Tables &T = h->T;
+  const Work &W = w->W;
+  TT_CUDA(cudaMemsetAsync(W.counters, 0, 4 * 16, stream));
+  TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)w->cap_reqs + 1, stream));
+  for (int kidx = 0; kidx < N_KERNELS; ++kidx) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (timed) { a = pool_event(h); b = pool_event(h); cudaEventRecord(a, stream); }
+    switch (kidx) {
+      case 0: launch_prepass(T, W, grid_tiles(w), stream); break;
+      case 1: launch_tilescan(T, W, stream); break;
+      case 2: launch_pretok(T, W, grid_tiles(w), stream); break;
+      case 3: launch_bpe_small(T, W, grid_small(w), stream); break;
+      case 4: launch_bpe_long(T, W, grid_long(w), stream); break;
+      case 5: launch_ids(T, W, grid_chunks(w), stream); break;
+      case 6: launch_req(T, W, grid_reqs(w), stream); break;
+    }
+    if (timed) { cudaEventRecord(b, stream); h->pending.push_back({kidx, a, b}); }
+  }
+  TT_CUDA(cudaGetLastError());
+  h->launches += N_KERNELS;
+  return TT_OK;
+}
+
+static tt_status check_batch_args(tt_tokenizer *h, const void *d_utf8, const int64_t *offs, int64_t n,
+                                  const void *out_ids, const int64_t *out_offs) {
+  if (!h || n < 0 || !offs || !out_offs) return TT_ERR_INVALID_ARG;
+  if (n > 0 && (!d_utf8 || !out_ids)) return TT_ERR_INVALID_ARG;
+  return TT_OK;
+}
+
+extern "C" tt_status tt_encode_batch_bounded(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
+                                             int64_t n_requests, int64_t max_total_bytes, int32_t *d_out_ids,
+                                             int64_t *d_out_id_offsets, tt_stream_t stream_) {
+  tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets);
+  if (s != TT_OK) return s;
+  if (max_total_bytes < 0 || max_total_bytes >= INT32_MAX - 64) return TT_ERR_CAPACITY;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (n_requests == 0) {
+    TT_CUDA(cudaMemsetAsync(d_out_id_offsets, 0, sizeof(int64_t), stream));
+    return TT_OK;
+  }
+  std::lock_guard<std::mutex> lock(h->mu);
+  Workspace *w;
+  if ((s = get_workspace(h, stream, max_total_bytes, n_requests, &w)) != TT_OK) return s;
+  CallArgs args = {d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, nullptr, nullptr};
+  TT_CUDA(cudaMemcpyAsync(w->W.args, &args, sizeof(args), cudaMemcpyHostToDevice, stream));
+  if (h->profiling || !h->graphs_enabled) return enqueue_encode(h, w, stream, h->profiling);
+  if (!w->graph) {
+    cudaGraph_t g;
+    TT_CUDA(cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal));
+    tt_status es = enqueue_encode(h, w, stream, false);
+    cudaError_t ce = cudaStreamEndCapture(stream, &g);
+    h->launches -= N_KERNELS;   // captured, not launched
+    if (es != TT_OK) return es;
+    TT_CUDA(ce);
+    cudaError_t ie = cudaGraphInstantiate(&w->graph, g, 0);
+    cudaGraphDestroy(g);
+    TT_CUDA(ie);
+  }
+  TT_CUDA(cudaGraphLaunch(w->graph, stream));
+  h->launches += N_KERNELS;
+  return TT_OK;
+}
+
+extern "C" tt_status tt_encode_batch(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
+                                     int64_t n_requests, int32_t *d_out_ids, int64_t *d_out_id_offsets,
+                                     tt_stream_t stream_) {
+  tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets);
+  if (s != TT_OK) return s;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (n_requests == 0) {
+    TT_CUDA(cudaMemsetAsync(d_out_id_offsets, 0, sizeof(int64_t), stream));
+    return TT_OK;
+  }
+  int64_t ends[2];
+  TT_CUDA(cudaMemcpyAsync(&ends[0], d_byte_offsets, 8, cudaMemcpyDeviceToHost, stream));
+  TT_CUDA(cudaMemcpyAsync(&ends[1], d_byte_offsets + n_requests, 8, cudaMemcpyDeviceToHost, stream));
+  TT_CUDA(cudaStreamSynchronize(stream));
+  if (ends[0] < 0 || ends[1] < ends[0]) return TT_ERR_INVALID_ARG;
+  return tt_encode_batch_bounded(h, d_utf8, d_byte_offsets, n_requests, ends[1] - ends[0], d_out_ids,
+                                 d_out_id_offsets, stream_);
+}
+
+extern "C" tt_status tt_get_status(tt_tokenizer *h, tt_stream_t stream, int64_t *bad_request) {
+  if (!h) return TT_ERR_INVALID_ARG;
+  TT_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  DevStatus st;
+  TT_CUDA(cudaMemcpy(&st, h->d_status, sizeof(st), cudaMemcpyDeviceToHost));
+  DevStatus init = {0, 0, ~0ull};
+  TT_CUDA(cudaMemcpy(h->d_status, &init, sizeof(init), cudaMemcpyHostToDevice));
+  if (bad_request) *bad_request = st.code == ST_INVALID_UTF8 && st.bad_request != ~0ull ? (int64_t)st.bad_request : -1;
+  return (tt_status)st.code;
+}
+
+extern "C" tt_status tt_encode_host(tt_tokenizer *h, const uint8_t *utf8, const int64_t *byte_offsets,
+                                    int64_t n_requests, int32_t *out_ids, int64_t out_capacity,
+                                    int64_t *out_id_offsets, tt_stream_t stream_) {
+  if (!h || n_requests < 0 || !byte_offsets || !out_id_offsets || out_capacity < 0) return TT_ERR_INVALID_ARG;
+  if (n_requests == 0) { out_id_offsets[0] = 0; return TT_OK; }
+  const int64_t b0 = byte_offsets[0], b1 = byte_offsets[n_requests];
+  if (b0 < 0 || b1 < b0 || (b1 > b0 && (!utf8 || !out_ids))) return TT_ERR_INVALID_ARG;
+  for (int64_t r = 0; r < n_requests; ++r)
+    if (byte_offsets[r] > byte_offsets[r + 1]) return TT_ERR_INVALID_ARG;
+  const int64_t total = b1 - b0;
+  if (total >= INT32_MAX - 64) return TT_ERR_CAPACITY;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  const size_t in_b = ((size_t)total + 16 + 255) & ~(size_t)255;
+  const size_t off_b = ((size_t)(n_requests + 1) * 8 + 255) & ~(size_t)255;
+  const size_t out_b = ((size_t)total + 1) * 4;
+  uint8_t *d_in;
+  int64_t *d_offs, *d_out_offs;
+  int32_t *d_out;
+  {
+    std::lock_guard<std::mutex> lock(h->mu);
+    Workspace *w;
+    tt_status s = get_workspace(h, stream, total, n_requests, &w);
+    if (s != TT_OK) return s;
+    const size_t need = in_b + 2 * off_b + out_b;
+    if (w->stage_bytes < need) {
+      if (w->stage) { cudaStreamSynchronize(stream); cudaFree(w->stage); w->stage = nullptr; w->stage_bytes = 0; }
+      const size_t sz = next_pow2(need);
+      if (cudaMalloc(&w->stage, sz) != cudaSuccess) return TT_ERR_OOM;
+      w->stage_bytes = sz;
+    }
+    char *cur = (char *)w->stage;
+    d_in = (uint8_t *)cur;
+    d_offs = (int64_t *)(cur + in_b);
+    d_out_offs = (int64_t *)(cur + in_b + off_b);
+    d_out = (int32_t *)(cur + in_b + 2 * off_b);
+    w->h_offs.resize((size_t)n_requests + 1);
+    for (int64_t r = 0; r <= n_requests; ++r) w->h_offs[r] = byte_offsets[r] - b0;
+    if (total) TT_CUDA(cudaMemcpyAsync(d_in, utf8 + b0, (size_t)total, cudaMemcpyHostToDevice, stream));
+    TT_CUDA(cudaMemcpyAsync(d_offs, w->h_offs.data(), (size_t)(n_requests + 1) * 8, cudaMemcpyHostToDevice, stream));
+  }
+  tt_status s = tt_encode_batch_bounded(h, d_in, d_offs, n_requests, total, d_out, d_out_offs, stream_);
+  if (s != TT_OK) return s;
+  TT_CUDA(cudaMemcpyAsync(out_id_offsets, d_out_offs, (size_t)(n_requests + 1) * 8, cudaMemcpyDeviceToHost, stream));
+  TT_CUDA(cudaStreamSynchronize(stream));
+  const int64_t ntok = out_id_offsets[n_requests];
+  if (ntok > out_capacity) return TT_ERR_CAPACITY;
+  if (ntok) TT_CUDA(cudaMemcpyAsync(out_ids, d_out, (size_t)ntok * 4, cudaMemcpyDeviceToHost, stream));
+  return tt_get_status(h, stream_, nullptr);
+}
+
+extern "C" tt_status tt_pretokenize_batch(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
+                                          int64_t n_requests, int64_t *d_piece_starts, int64_t *d_piece_offsets,
+                                          tt_stream_t stream_) {
+  tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_piece_starts, d_piece_offsets);
+  if (s != TT_OK) return s;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (n_requests == 0) {
+    TT_CUDA(cudaMemsetAsync(d_piece_offsets, 0, sizeof(int64_t), stream));
+    return TT_OK;
+  }
+  int64_t ends[2];
+  TT_CUDA(cudaMemcpyAsync(&ends[0], d_byte_offsets, 8, cudaMemcpyDeviceToHost, stream));
+  TT_CUDA(cudaMemcpyAsync(&ends[1], d_byte_offsets + n_requests, 8, cudaMemcpyDeviceToHost, stream));
+  TT_CUDA(cudaStreamSynchronize(stream));
+  if (ends[0] < 0 || ends[1] < ends[0]) return TT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(h->mu);
+  Workspace *w;
+  if ((s = get_workspace(h, stream, ends[1] - ends[0], n_requests, &w)) != TT_OK) return s;
+  CallArgs args = {d_utf8, d_byte_offsets, n_requests, nullptr, nullptr, d_piece_starts, d_piece_offsets};
+  TT_CUDA(cudaMemcpyAsync(w->W.args, &args, sizeof(args), cudaMemcpyHostToDevice, stream));
+  const Work &W = w->W;
+  TT_CUDA(cudaMemsetAsync(W.counters, 0, 4 * 16, stream));
+  TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)w->cap_reqs + 1, stream));
+  launch_prepass(h->T, W, grid_tiles(w), stream);
+  launch_tilescan(h->T, W, stream);
+  launch_pretok(h->T, W, grid_tiles(w), stream);
+  launch_hook_pre(W, stream);
+  launch_hook_pieces(W, grid_small(w), stream);
+  launch_hook_offsets(W, grid_reqs(w), stream);
+  TT_CUDA(cudaGetLastError());
+  h->launches += 6;
+  return TT_OK;
+}
+
+extern "C" const char *tt_status_string(tt_status s) {
+  switch (s) {
+    case TT_OK: return "ok";
+    case TT_ERR_INVALID_ARG: return "invalid argument";
+    case TT_ERR_BAD_VOCAB: return "vocabulary or merge list rejected";
+    case TT_ERR_BAD_FAMILY: return "unknown pattern family";
+    case TT_ERR_INVALID_UTF8: return "a request is not valid UTF-8";
+    case TT_ERR_CAPACITY: return "batch exceeds a stated bound";
+    case TT_ERR_OOM: return "out of memory";
+    case TT_ERR_CUDA: return "CUDA runtime error";
+    case TT_ERR_TIMEOUT: return "bounded device wait ran out";
+  }
+  return "unknown status";
+}
+
+extern "C" void tt_profile(tt_tokenizer *h, int enable) {
+  if (!h) return;
+  std::lock_guard<std::mutex> lock(h->mu);
+  h->profiling = enable != 0;
+}
+
+extern "C" int tt_profile_read(tt_tokenizer *h, const char **names, double *ms, int64_t *launches, int cap) {
+  if (!h) return 0;
+  std::lock_guard<std::mutex> lock(h->mu);
+  for (auto &pd : h->pending) {
+    cudaEventSynchronize(pd.b);
+    float t = 0.f;
+    cudaEventElapsedTime(&t, pd.a, pd.b);
+    h->prof_ms[pd.kernel] += t;
+    h->prof_n[pd.kernel] += 1;
+    h->event_pool.push_back(pd.a);
+    h->event_pool.push_back(pd.b);
+  }
+  h->pending.clear();
+  int n = 0;
+  for (int k = 0; k < N_KERNELS && n < cap; ++k, ++n) {
+    if (names) names[n] = KERNEL_NAMES[k];
+    if (ms) ms[n] = h->prof_ms[k];
+    if (launches) launches[n] = h->prof_n[k];
+    h->prof_ms[k] = 0;
+    h->prof_n[k] = 0;
+  }
+  return n;
+}
+
+extern "C" int64_t tt_launch_count(tt_tokenizer *h) { return h ? h->launches.load() : 0; }
+
+extern "C" const char *tt_table_digest(void) { return TT_CLASS_DIGEST; }

@@ -1,0 +1,308 @@
+// tt_common.cuh - device-side definitions shared by the kernels of the exact
+// BPE tokenizer: sizes, tables, hashing, status reporting, block scans and
+// decoupled look-back.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "tt_rules.cuh"
+
+namespace tt {
+
+// ------------------------------------------------------------ geometry
+// Pre-tokenizer tiles: one CTA of 256 threads reads a 4096-byte window, one
+// 16-byte vector per thread: 48 bytes before the tile (lookback and the
+// shifted scan entry points), the 4016-byte tile, 32 bytes after it.
+constexpr int PT_THREADS = 256;
+constexpr int WIN = 4096;
+constexpr int HALO_L = 48;
+constexpr int HALO_R = 32;
+constexpr int TILE = WIN - HALO_L - HALO_R;  // 4016 = 16 * 251
+constexpr int S1_SHIFT = 32;                 // mark-resolution scan enters at tile start - 32
+constexpr int S2_SHIFT = 16;                 // forward scan enters at tile start - 16
+static_assert(TILE % 16 == 0, "tile must keep 16-byte alignment");
+
+// BPE execution units by piece length (bytes)
+constexpr int SMALL_MAX = 32;                // thread per piece, state in registers / local
+constexpr int IDS_CHUNK = 2048;              // pieces per CTA in the ID scatter
+
+// status codes (mirror include/toktier.h)
+enum : int { ST_OK = 0, ST_INVALID_ARG = 1, ST_INVALID_UTF8 = 4, ST_CAPACITY = 5, ST_TIMEOUT = 8 };
+
+struct DevStatus {
+  int code;                       // first error recorded (0 = none)
+  int pad;
+  unsigned long long bad_request; // lowest rejected request index (~0 = none)
+};
+
+__device__ __forceinline__ void set_status(DevStatus *st, int code) { atomicCAS(&st->code, 0, code); }
+
+// ------------------------------------------------------------ tables
+// pair table entry: left << 44 | right << 24 | rank ; empty = ~0
+// vocab table entry: fp << 32 | len << 20 | id ; empty = 0
+constexpr uint64_t PAIR_EMPTY = ~0ull;
+constexpr int MAX_VOCAB_BITS = 20;
+constexpr int MAX_RANK_BITS = 24;
+
+struct Tables {
+  const uint16_t *cls1;       // code point >> 8 -> block index
+  const uint8_t *cls2;        // block * 256 + (cp & 255) -> raw kind (K_*)
+  const uint64_t *pair_tab;
+  uint32_t pair_mask;
+  const int32_t *merge_result;
+  const uint64_t *vocab_tab;
+  uint32_t vocab_mask;
+  const uint8_t *vbytes;
+  const int32_t *voff;
+  const int32_t *byte_id;     // [256]
+  int32_t max_tok_len;
+  int32_t family;
+};
+
+TT_HD uint64_t mix64(uint64_t x) {
+  x ^= x >> 33; x *= 0xff51afd7ed558ccdull;
+  x ^= x >> 33; x *= 0xc4ceb9fe1a85ec53ull;
+  x ^= x >> 33;
+  return x;
+}
+TT_HD uint64_t pair_hash(uint32_t l, uint32_t r) { return mix64(((uint64_t)l << 32) | r); }
+TT_HD uint64_t pair_key(uint32_t l, uint32_t r) { return ((uint64_t)l << MAX_VOCAB_BITS) | r; }
+
+// hash of a byte string, 8 bytes at a time (little-endian words, zero padded)
+struct ByteHash {
+  uint64_t h;
+  TT_HD void init(int len) { h = 0x9E3779B97F4A7C15ull ^ (uint64_t)len; }
+  TT_HD void word(uint64_t w) { h = (h ^ w) * 0xff51afd7ed558ccdull; h ^= h >> 32; }
+  TT_HD uint64_t fin() const { return mix64(h); }
+};
+TT_HD uint64_t hash_bytes(const uint8_t *b, int len) {
+  ByteHash bh; bh.init(len);
+  for (int i = 0; i < len; i += 8) {
+    uint64_t w = 0;
+    for (int k = 0; k < 8 && i + k < len; ++k) w |= (uint64_t)b[i + k] << (8 * k);
+    bh.word(w);
+  }
+  return bh.fin();
+}
+TT_HD uint32_t vocab_fp(uint64_t h) { uint32_t f = (uint32_t)(h >> 32); return f ? f : 1u; }
+
+#if defined(__CUDACC__)
+// rank of the pair (l, r), or -1
+__device__ __forceinline__ int pair_rank(const Tables &T, int l, int r) {
+  const uint64_t key = pair_key((uint32_t)l, (uint32_t)r);
+  uint32_t s = (uint32_t)pair_hash((uint32_t)l, (uint32_t)r) & T.pair_mask;
+  for (;;) {
+    const uint64_t e = __ldg(&T.pair_tab[s]);
+    if (e == PAIR_EMPTY) return -1;
+    if ((e >> MAX_RANK_BITS) == key) return (int)(e & ((1u << MAX_RANK_BITS) - 1));
+    s = (s + 1) & T.pair_mask;
+  }
+}
+
+// ------------------------------------------------------------ memory order
+__device__ __forceinline__ int ld_acquire(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int *p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// copy a trivially copyable struct through L2 (bypassing L1)
+template <typename T>
+__device__ __forceinline__ T ld_cg(const T *p) {
+  static_assert(sizeof(T) % 4 == 0, "words");
+  T out;
+  uint32_t *o = reinterpret_cast<uint32_t *>(&out);
+  const uint32_t *i = reinterpret_cast<const uint32_t *>(p);
+#pragma unroll
+  for (int k = 0; k < (int)(sizeof(T) / 4); ++k) o[k] = __ldcg(i + k);
+  return out;
+}
+
+template <typename T>
+__device__ __forceinline__ T shfl_up_t(T v, int d) {
+  static_assert(sizeof(T) % 4 == 0, "words");
+  uint32_t w[sizeof(T) / 4];
+  memcpy(w, &v, sizeof(T));
+#pragma unroll
+  for (int k = 0; k < (int)(sizeof(T) / 4); ++k) w[k] = __shfl_up_sync(0xffffffffu, w[k], d);
+  memcpy(&v, w, sizeof(T));
+  return v;
+}
+template <typename T>
+__device__ __forceinline__ T shfl_down_t(T v, int d) {
+  uint32_t w[sizeof(T) / 4];
+  memcpy(w, &v, sizeof(T));
+#pragma unroll
+  for (int k = 0; k < (int)(sizeof(T) / 4); ++k) w[k] = __shfl_down_sync(0xffffffffu, w[k], d);
+  memcpy(&v, w, sizeof(T));
+  return v;
+}
+template <typename T>
+__device__ __forceinline__ T shfl_idx_t(T v, int src) {
+  uint32_t w[sizeof(T) / 4];
+  memcpy(w, &v, sizeof(T));
+#pragma unroll
+  for (int k = 0; k < (int)(sizeof(T) / 4); ++k) w[k] = __shfl_sync(0xffffffffu, w[k], src);
+  memcpy(&v, w, sizeof(T));
+  return v;
+}
+
+// Block-wide exclusive scan in thread order (NT threads, NT % 32 == 0).
+// op(a, b) = "a then b".  Returns the exclusive prefix of this thread;
+// *total receives the combination over all threads.  smem: NT/32 slots.
+template <int NT, typename T, typename Op>
+__device__ T block_exclusive_scan(T v, Op op, T identity, T *smem, T *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    T y = shfl_up_t(inc, d);
+    if (lane >= d) inc = op(y, inc);
+  }
+  if (lane == 31) smem[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    T w = lane < NT / 32 ? smem[lane] : identity;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      T y = shfl_up_t(w, d);
+      if (lane >= d) w = op(y, w);
+    }
+    if (lane < NT / 32) smem[lane] = w;       // inclusive over warps
+  }
+  __syncthreads();
+  T warp_prefix = warp == 0 ? identity : smem[warp - 1];
+  T excl_in_warp = shfl_up_t(inc, 1);
+  if (lane == 0) excl_in_warp = identity;
+  T r = op(warp_prefix, excl_in_warp);
+  if (total) *total = smem[NT / 32 - 1];
+  __syncthreads();
+  return r;
+}
+
+// Block-wide exclusive suffix scan: the combination over threads AFTER this
+// one, nearest first: op(near, far).  (Used with "first event" operators.)
+template <int NT, typename T, typename Op>
+__device__ T block_exclusive_suffix(T v, Op op, T identity, T *smem, T *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T inc = v;   // op over [me .. end of warp]
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    T y = shfl_down_t(inc, d);
+    if (lane + d < 32) inc = op(inc, y);
+  }
+  if (lane == 0) smem[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int NW = NT / 32;
+    T w = lane < NW ? smem[lane] : identity;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      T y = shfl_down_t(w, d);
+      if (lane + d < NW) w = op(w, y);
+    }
+    if (lane < NW) smem[lane] = w;            // suffix over warps, inclusive
+  }
+  __syncthreads();
+  constexpr int NW = NT / 32;
+  T warp_suffix = warp == NW - 1 ? identity : smem[warp + 1];
+  T excl_in_warp = shfl_down_t(inc, 1);
+  if (lane == 31) excl_in_warp = identity;
+  T r = op(excl_in_warp, warp_suffix);
+  if (total) *total = smem[0];
+  __syncthreads();
+  return r;
+}
+
+// Decoupled look-back (one thread).  Publishes `local` as tile `tile`'s
+// aggregate, walks back over predecessors (combining aggregates until an
+// inclusive prefix is found), publishes the inclusive prefix and returns the
+// exclusive one.  Tiles must be claimed in increasing order by running CTAs.
+// Every wait is bounded: after `spin_limit` polls the status records
+// ST_TIMEOUT and the walk stops with what it has, so no CTA can hang.
+template <typename T, typename Op>
+__device__ T lookback(int tile, T local, Op op, T identity, T *agg, T *inc, int *flag, DevStatus *st,
+                      int spin_limit) {
+  if (tile == 0) {
+    inc[0] = local;
+    __threadfence();
+    st_release(&flag[0], 2);
+    return identity;
+  }
+  agg[tile] = local;
+  __threadfence();
+  st_release(&flag[tile], 1);
+  T excl = identity;
+  int t = tile - 1;
+  for (;;) {
+    int f = ld_acquire(&flag[t]);
+    int spins = 0;
+    while (f == 0) {
+      if (++spins > spin_limit) {
+        set_status(st, ST_TIMEOUT);
+        goto done;
+      }
+      __nanosleep(64);
+      f = ld_acquire(&flag[t]);
+    }
+    if (f == 2) {
+      excl = op(ld_cg(&inc[t]), excl);
+      break;
+    }
+    excl = op(ld_cg(&agg[t]), excl);
+    if (--t < 0) break;
+  }
+done:
+  inc[tile] = op(excl, local);
+  __threadfence();
+  st_release(&flag[tile], 2);
+  return excl;
+}
+#endif  // __CUDACC__
+
+// Per-call arguments, read by every kernel from device memory (so that a
+// captured graph can be replayed with new buffers).
+struct CallArgs {
+  const uint8_t *utf8;             // batch bytes (absolute)
+  const int64_t *offs;             // [n + 1]
+  int64_t n;                       // requests
+  int32_t *out_ids;
+  int64_t *out_id_offsets;         // [n + 1]
+  int64_t *hook_starts;            // test hook outputs (NULL unless the hook runs)
+  int64_t *hook_offsets;
+};
+
+// Per-stream workspace (device pointers; sizes fixed per capacity bucket).
+struct Work {
+  int64_t cap_bytes;               // largest batch this workspace holds
+  int64_t cap_reqs;
+  int32_t cap_tiles;
+  int32_t spin_limit;
+  // pre-pass summaries and carries
+  int2 *s1_sum, *s1_carry;         // mark resolution: (last stretch start, last trigger)
+  uint8_t *rq_sum, *rq_carry;      // [tiles][2]: first rq_ws / rq_up event
+  // look-back state
+  S2 *s2_agg, *s2_inc;
+  int *s2_flag;
+  int *cnt_agg, *cnt_inc, *cnt_flag;
+  int *ids_agg, *ids_inc, *ids_flag;
+  int *counters;                   // [0] pretok tile ticket, [1] ids tile ticket, [2] long list size,
+                                   // [3] pieces, [4] tokens, [5] bad requests seen
+  // pieces and tokens
+  int32_t *piece_start;            // [cap_bytes + 2], bit 31 = rejected-request placeholder
+  int32_t *n_ids;                  // [cap_bytes + 1]
+  int32_t *id_off;                 // [cap_bytes + 2]
+  int32_t *scratch;                // [cap_bytes] ids by byte position
+  int32_t *tmp_a, *tmp_b;          // [cap_bytes] long-piece work arrays
+  int32_t *long_list;              // [cap_bytes / (SMALL_MAX + 1) + 2]
+  uint8_t *bad;                    // [cap_reqs]
+  int32_t *bad_pre;                // [cap_reqs + 1] (test hook)
+  DevStatus *status;
+  CallArgs *args;
+};
+
+}  // namespace tt

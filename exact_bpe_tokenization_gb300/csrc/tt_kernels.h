@@ -1,0 +1,28 @@
+// tt_kernels.h - host-side launchers of the tokenizer's kernels.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "tt_common.cuh"
+
+namespace tt {
+
+size_t pretok_smem_bytes();
+cudaError_t pretok_configure();
+void launch_prepass(const Tables &T, const Work &W, int grid, cudaStream_t s);
+void launch_tilescan(const Tables &T, const Work &W, cudaStream_t s);
+void launch_pretok(const Tables &T, const Work &W, int grid, cudaStream_t s);
+
+void launch_bpe_small(const Tables &T, const Work &W, int grid, cudaStream_t s);
+void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s);
+void launch_ids(const Tables &T, const Work &W, int grid, cudaStream_t s);
+void launch_req(const Tables &T, const Work &W, int grid, cudaStream_t s);
+
+void launch_hook_pre(const Work &W, cudaStream_t s);
+void launch_hook_pieces(const Work &W, int grid, cudaStream_t s);
+void launch_hook_offsets(const Work &W, int grid, cudaStream_t s);
+
+constexpr int BPE_SMALL_THREADS = 256;
+constexpr int BPE_LONG_THREADS = 512;
+constexpr int IDS_THREADS = 256;
+
+}  // namespace tt

@@ -1,0 +1,525 @@
+// tt_pretok.cu - parallel pre-tokenizer: UTF-8 decode, character classes,
+// run aggregates by prefix scans, the piece-start predicate and piece
+// compaction (TokTier: Exact Stateful CPU+GPU Tokenization for Agentic LLM
+// Serving, §4.1 run decomposition, §4.3 multi-document batching: runs are cut
+// at document boundaries and counts stay in device memory).
+//
+// Three kernels per batch:
+//   k_prepass   one CTA per 4016-byte tile, independent: validates UTF-8
+//               (per request), and summarises each tile for the two scans
+//               whose carries are computed ahead of time: o200k mark
+//               resolution (max-scan of stretch starts and triggers, on a
+//               tiling shifted 32 bytes left) and the reverse "first event
+//               after" queries.
+//   k_tilescan  one CTA: exclusive scans of those tile summaries (forward for
+//               marks, backward for the reverse queries); resets look-back
+//               flags.
+//   k_pretok    one CTA per tile, tiles claimed in order: effective classes,
+//               the forward scan (number-run count, blank-run start, o200k
+//               contraction chain and case state) with decoupled look-back on
+//               a tiling shifted 16 bytes left, the reverse queries, the
+//               predicate, and compaction of piece starts with a second
+//               decoupled look-back.
+#include "tt_common.cuh"
+#include "tt_kernels.h"
+
+namespace tt {
+
+struct WinSmem {
+  uint8_t bytes[WIN + 8];
+  uint8_t rsb[WIN + 8];      // byte starts a request
+  uint8_t cp8[WIN];          // char's code point if ASCII, else 0x80
+  uint8_t raw[WIN];          // raw kind
+  uint8_t eff[WIN];          // effective kind
+  uint8_t rs[WIN];           // char starts a request
+  uint16_t lead[WIN];        // window index of the char's lead byte
+  int cbase[PT_THREADS + 1]; // chars of thread t: [cbase[t], cbase[t+1])
+  uint8_t ascii[128];
+  int r0, r1;
+  int nch;
+};
+
+__device__ __forceinline__ int64_t lower_bound64(const int64_t *a, int64_t n, int64_t v) {
+  int64_t lo = 0, hi = n;
+  while (lo < hi) {
+    int64_t mid = (lo + hi) >> 1;
+    if (__ldg(&a[mid]) < v) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ uint8_t kind_of(const Tables &T, const WinSmem &S, uint32_t cp) {
+  if (cp < 128) return S.ascii[cp];
+  return __ldg(&T.cls2[(uint32_t)__ldg(&T.cls1[cp >> 8]) * 256u + (cp & 255u)]);
+}
+
+// Load the window [ws, ws + WIN) of the batch, mark request starts, find
+// char starts, decode and classify.  All threads participate.
+__device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, int64_t total, int64_t ws,
+                            WinSmem &S, int *scan_tmp) {
+  const int tid = threadIdx.x;
+  const uint8_t *g = A.utf8 + base;
+  const int64_t x0 = ws + 16 * tid;
+  uint8_t *dst = &S.bytes[16 * tid];
+  if (x0 >= 0 && x0 + 16 <= total && ((reinterpret_cast<uintptr_t>(g + x0) & 15) == 0)) {
+    *reinterpret_cast<uint4 *>(dst) = __ldg(reinterpret_cast<const uint4 *>(g + x0));
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int64_t x = x0 + k;
+      dst[k] = (x >= 0 && x < total) ? __ldg(g + x) : 0;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) S.rsb[16 * tid + k] = 0;
+  if (tid < 8) { S.bytes[WIN + tid] = 0; S.rsb[WIN + tid] = 0; }
+  if (tid < 128) S.ascii[tid] = __ldg(&T.cls2[(uint32_t)__ldg(&T.cls1[0]) * 256u + tid]);
+  if (tid == 0) {
+    const int64_t lo = ws < 0 ? 0 : ws;
+    const int64_t hi = ws + WIN < total ? ws + WIN : total;
+    S.r0 = (int)lower_bound64(A.offs, A.n, base + lo);
+    S.r1 = (int)lower_bound64(A.offs, A.n, base + hi);
+  }
+  __syncthreads();
+  for (int r = S.r0 + tid; r < S.r1; r += PT_THREADS) {
+    const int64_t x = __ldg(&A.offs[r]) - base - ws;
+    if (x >= 0 && x < WIN && __ldg(&A.offs[r]) - base < total) S.rsb[x] = 1;
+  }
+  __syncthreads();
+  // char starts among my 16 bytes
+  uint32_t smask = 0;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int i = 16 * tid + k;
+    const int64_t x = ws + i;
+    if (x < 0 || x >= total) continue;
+    const uint8_t b = S.bytes[i];
+    if ((b & 0xC0) != 0x80 || S.rsb[i]) smask |= 1u << k;
+  }
+  const int cnt = __popc(smask);
+  int tot;
+  const int cb = block_exclusive_scan<PT_THREADS>(cnt, [](int a, int b) { return a + b; }, 0, scan_tmp, &tot);
+  S.cbase[tid] = cb;
+  if (tid == PT_THREADS - 1) { S.cbase[PT_THREADS] = tot; S.nch = tot; }
+  int j = cb;
+  for (uint32_t m = smask; m; m &= m - 1) {
+    const int k = __ffs(m) - 1;
+    const int i = 16 * tid + k;
+    const uint8_t b0 = S.bytes[i];
+    int len;
+    uint32_t cp;
+    if (b0 < 0x80) { len = 1; cp = b0; }
+    else if (b0 >= 0xC0 && b0 < 0xE0) { len = 2; cp = b0 & 0x1F; }
+    else if (b0 >= 0xE0 && b0 < 0xF0) { len = 3; cp = b0 & 0x0F; }
+    else if (b0 >= 0xF0 && b0 < 0xF8) { len = 4; cp = b0 & 0x07; }
+    else { len = 1; cp = 0xFFFD; }
+    bool ok = true;
+    for (int q = 1; q < len; ++q) {
+      if (i + q >= WIN || ws + i + q >= total || S.rsb[i + q] || (S.bytes[i + q] & 0xC0) != 0x80) { ok = false; break; }
+      cp = (cp << 6) | (S.bytes[i + q] & 0x3F);
+    }
+    if (!ok || cp >= 0x110000u) cp = 0xFFFD;
+    S.lead[j] = (uint16_t)i;
+    S.cp8[j] = cp < 128 ? (uint8_t)cp : (uint8_t)0x80;
+    S.raw[j] = kind_of(T, S, cp);
+    S.rs[j] = S.rsb[i];
+    ++j;
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- k_prepass
+__global__ void __launch_bounds__(PT_THREADS) k_prepass(Tables T, Work W) {
+  __shared__ WinSmem S;
+  __shared__ int scan_tmp[PT_THREADS / 32];
+  __shared__ int2 red2[PT_THREADS / 32];
+  __shared__ int red_rq[PT_THREADS / 32];
+  const CallArgs A = *W.args;
+  const int tid = threadIdx.x;
+  if (A.n <= 0) return;
+  const int64_t base = __ldg(&A.offs[0]);
+  const int64_t total = __ldg(&A.offs[A.n]) - base;
+  if (total > W.cap_bytes || total < 0 || base < 0) {
+    if (blockIdx.x == 0 && tid == 0) set_status(W.status, total > W.cap_bytes ? ST_CAPACITY : ST_INVALID_ARG);
+    return;
+  }
+  // offsets must be non-decreasing
+  for (int64_t r = (int64_t)blockIdx.x * PT_THREADS + tid; r < A.n; r += (int64_t)gridDim.x * PT_THREADS)
+    if (__ldg(&A.offs[r]) > __ldg(&A.offs[r + 1])) set_status(W.status, ST_INVALID_ARG);
+  const int ntiles = (int)((total + TILE - 1) / TILE);
+  const int t = blockIdx.x;
+  if (t >= ntiles) return;
+  const int64_t ts = (int64_t)t * TILE, te = ts + TILE < total ? ts + TILE : total;
+  const int64_t ws = ts - HALO_L;
+  load_window(T, A, base, total, ws, S, scan_tmp);
+
+  // --- UTF-8 validation of the tile's bytes (RFC 3629, per request)
+  for (int k = 0; k < 16; ++k) {
+    const int i = 16 * tid + k;
+    const int64_t x = ws + i;
+    if (x < ts || x >= te) continue;
+    const uint8_t b = S.bytes[i];
+    bool bad = false;
+    if (b < 0x80) {
+    } else if (b < 0xC0) {                    // continuation: claimed by a lead <= 3 bytes back?
+      bad = true;
+      if (!S.rsb[i]) {
+        for (int d = 1; d <= 3; ++d) {
+          const int q = i - d;
+          if (ws + q < 0) break;
+          const uint8_t bq = S.bytes[q];
+          if ((bq & 0xC0) == 0x80) { if (S.rsb[q]) break; continue; }
+          const int L = (bq >= 0xC2 && bq <= 0xDF) ? 2 : (bq >= 0xE0 && bq <= 0xEF) ? 3 : (bq >= 0xF0 && bq <= 0xF4) ? 4 : 1;
+          bad = L <= d;
+          break;
+        }
+      }
+    } else if (b >= 0xC2 && b <= 0xF4) {
+      const int L = b <= 0xDF ? 2 : b <= 0xEF ? 3 : 4;
+      for (int q = 1; q < L && !bad; ++q)
+        bad = x + q >= total || S.rsb[i + q] || (S.bytes[i + q] & 0xC0) != 0x80;
+      if (!bad) {
+        const uint8_t b1 = S.bytes[i + 1];
+        if ((b == 0xE0 && b1 < 0xA0) || (b == 0xED && b1 > 0x9F) || (b == 0xF0 && b1 < 0x90) || (b == 0xF4 && b1 > 0x8F))
+          bad = true;
+      }
+    } else {
+      bad = true;
+    }
+    if (bad) {
+      // request containing x: last r with offs[r] <= base + x
+      const int64_t r = lower_bound64(A.offs, A.n + 1, base + x + 1) - 1;
+      if (r >= 0 && r < A.n) {
+        W.bad[r] = 1;
+        atomicMin(&W.status->bad_request, (unsigned long long)r);
+        set_status(W.status, ST_INVALID_UTF8);
+        atomicExch(&W.counters[5], 1);
+      }
+    }
+  }
+
+  const int c0 = S.cbase[tid], c1 = S.cbase[tid + 1];
+  // --- mark-resolution summary over chars with pos in [ts - 32, te - 32)
+  if (T.family == FAM_O200K) {
+    int2 v = make_int2(-1, -1);
+    for (int j = c0; j < c1; ++j) {
+      const int64_t pos = ws + S.lead[j];
+      if (pos < ts - S1_SHIFT || pos >= te - S1_SHIFT) continue;
+      const bool in_prev = !S.rs[j] && j > 0;
+      const uint8_t rp = in_prev ? S.raw[j - 1] : K_NONE;
+      const uint32_t cpp = in_prev ? S.cp8[j - 1] : 0;
+      const uint8_t rn = (j + 1 < S.nch && !S.rs[j + 1]) ? S.raw[j + 1] : K_NONE;
+      if (region_start(S.raw[j], rp)) v.x = (int)pos;
+      if (trigger(S.raw[j], rp, cpp, rn)) v.y = (int)pos;
+    }
+    int2 tot;
+    block_exclusive_scan<PT_THREADS>(v, [](int2 a, int2 b) { return make_int2(max(a.x, b.x), max(a.y, b.y)); },
+                                     make_int2(-1, -1), red2, &tot);
+    if (tid == 0) W.s1_sum[t] = tot;
+  }
+  // --- reverse-query summary: first events among the tile's chars
+  {
+    int v = 0xFFFF;   // byte 0: rq_ws event, byte 1: rq_up event (0xFF = none)
+    for (int j = c0; j < c1; ++j) {
+      const int64_t pos = ws + S.lead[j];
+      if (pos < ts || pos >= te) continue;
+      const uint8_t ew = rq_ws_event(S.rs[j], S.raw[j], S.cp8[j]);
+      const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
+      if ((v & 0xFF) == 0xFF && ew != 0xFF) v = (v & 0xFF00) | ew;
+      if ((v >> 8) == 0xFF && eu != 0xFF) v = (v & 0x00FF) | (eu << 8);
+    }
+    auto first = [](int a, int b) {   // a before b: keep a's events where present
+      const int lo = (a & 0xFF) != 0xFF ? (a & 0xFF) : (b & 0xFF);
+      const int hi = (a >> 8) != 0xFF ? (a >> 8) : (b >> 8);
+      return lo | (hi << 8);
+    };
+    int tot;
+    block_exclusive_scan<PT_THREADS>(v, first, 0xFFFF, red_rq, &tot);
+    if (tid == 0) { W.rq_sum[2 * t] = (uint8_t)(tot & 0xFF); W.rq_sum[2 * t + 1] = (uint8_t)(tot >> 8); }
+  }
+}
+
+// ---------------------------------------------------------------- k_tilescan
+__global__ void __launch_bounds__(1024) k_tilescan(Tables T, Work W) {
+  __shared__ int2 red2[32];
+  __shared__ int red_rq[32];
+  __shared__ int2 carry2;
+  __shared__ int carry_rq;
+  const CallArgs A = *W.args;
+  const int tid = threadIdx.x;
+  // reset look-back flags of every tile / chunk this workspace can hold
+  for (int i = tid; i < W.cap_tiles; i += 1024) { W.s2_flag[i] = 0; W.cnt_flag[i] = 0; }
+  const int nchunks_max = (int)((W.cap_bytes + 1 + IDS_CHUNK - 1) / IDS_CHUNK) + 1;
+  for (int i = tid; i < nchunks_max; i += 1024) W.ids_flag[i] = 0;
+  if (A.n <= 0) return;
+  const int64_t base = __ldg(&A.offs[0]);
+  const int64_t total = __ldg(&A.offs[A.n]) - base;
+  if (total > W.cap_bytes || total < 0 || base < 0) return;
+  const int ntiles = (int)((total + TILE - 1) / TILE);
+  if (tid == 0) { carry2 = make_int2(-1, -1); carry_rq = R_END | (R_END << 8); }
+  __syncthreads();
+  auto mx = [](int2 a, int2 b) { return make_int2(max(a.x, b.x), max(a.y, b.y)); };
+  if (T.family == FAM_O200K) {
+    for (int c = 0; c < ntiles; c += 1024) {
+      const int t = c + tid;
+      const int2 v = t < ntiles ? W.s1_sum[t] : make_int2(-1, -1);
+      int2 tot;
+      const int2 ex = block_exclusive_scan<1024>(v, mx, make_int2(-1, -1), red2, &tot);
+      if (t < ntiles) W.s1_carry[t] = mx(carry2, ex);
+      __syncthreads();
+      if (tid == 0) carry2 = mx(carry2, tot);
+      __syncthreads();
+    }
+  }
+  auto first = [](int a, int b) {
+    const int lo = (a & 0xFF) != 0xFF ? (a & 0xFF) : (b & 0xFF);
+    const int hi = (a >> 8) != 0xFF ? (a >> 8) : (b >> 8);
+    return lo | (hi << 8);
+  };
+  // backward: carry of tile t = first event in tiles > t (R_END past the batch)
+  for (int c = ((ntiles - 1) / 1024) * 1024; c >= 0; c -= 1024) {
+    const int t = c + tid;
+    const int v = t < ntiles ? (W.rq_sum[2 * t] | (W.rq_sum[2 * t + 1] << 8)) : 0xFFFF;
+    int tot;
+    const int ex = block_exclusive_suffix<1024>(v, first, 0xFFFF, red_rq, &tot);
+    if (t < ntiles) {
+      const int r = first(ex, carry_rq);
+      W.rq_carry[2 * t] = (uint8_t)(r & 0xFF);
+      W.rq_carry[2 * t + 1] = (uint8_t)(r >> 8);
+    }
+    __syncthreads();
+    if (tid == 0) carry_rq = first(tot, carry_rq);
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- k_pretok
+struct PretokSmem {
+  WinSmem w;
+  uint8_t chain[WIN];
+  uint16_t aggs[WIN];
+  S2 s2_tmp[PT_THREADS / 32];
+  int2 i2_tmp[PT_THREADS / 32];
+  int i_tmp[PT_THREADS / 32];
+  S2 s2_prefix;
+  int tile;
+  int piece_base;
+};
+
+__device__ __forceinline__ Nbr make_nbr(const WinSmem &S, const uint8_t *chain, int j) {
+  Nbr b;
+  uint8_t e[5];
+  uint32_t c[5];
+  bool inside = true;
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const int x = j - k;
+    if (k > 0 && (x < 0 || S.rs[x + 1])) inside = false;
+    e[k] = inside ? S.eff[x] : K_NONE;
+    c[k] = inside ? S.cp8[x] : 0;
+  }
+  b.e0 = e[0]; b.e1 = e[1]; b.e2 = e[2]; b.e3 = e[3]; b.e4 = e[4];
+  b.c0 = c[0]; b.c1 = c[1]; b.c2 = c[2]; b.c3 = c[3]; b.c4 = c[4];
+  const bool in1 = j + 1 < S.nch && !S.rs[j + 1];
+  const bool in2 = in1 && j + 2 < S.nch && !S.rs[j + 2];
+  b.en1 = in1 ? S.eff[j + 1] : K_NONE;
+  b.en2 = in2 ? S.eff[j + 2] : K_NONE;
+  b.cn1 = in1 ? S.cp8[j + 1] : 0;
+  b.cn2 = in2 ? S.cp8[j + 2] : 0;
+  b.rs = S.rs[j] != 0;
+  if (chain) {
+    b.l1 = j >= 1 ? chain[j - 1] != 0 : true;
+    b.l2 = j >= 2 ? chain[j - 2] != 0 : true;
+    b.l3 = j >= 3 ? chain[j - 3] != 0 : true;
+  } else {
+    b.l1 = b.l2 = b.l3 = true;
+  }
+  return b;
+}
+
+__global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  PretokSmem &P = *reinterpret_cast<PretokSmem *>(smem_raw);
+  WinSmem &S = P.w;
+  const CallArgs A = *W.args;
+  const int tid = threadIdx.x;
+  if (A.n <= 0) return;
+  const int64_t base = __ldg(&A.offs[0]);
+  const int64_t total = __ldg(&A.offs[A.n]) - base;
+  if (total > W.cap_bytes || total < 0 || base < 0) return;
+  const int ntiles = (int)((total + TILE - 1) / TILE);
+  if (tid == 0) P.tile = atomicAdd(&W.counters[0], 1);
+  __syncthreads();
+  const int t = P.tile;
+  if (t >= ntiles) return;
+  const int fam = T.family;
+  const int64_t ts = (int64_t)t * TILE, te = ts + TILE < total ? ts + TILE : total;
+  const int64_t ws = ts - HALO_L;
+  load_window(T, A, base, total, ws, S, P.i_tmp);
+  const int c0 = S.cbase[tid], c1 = S.cbase[tid + 1];
+
+  // --- effective kinds (o200k: resolve marks with a max-scan entering at ts - 32)
+  if (fam == FAM_O200K) {
+    int2 v = make_int2(-1, -1);
+    for (int j = c0; j < c1; ++j) {
+      const int64_t pos = ws + S.lead[j];
+      if (pos < ts - S1_SHIFT) continue;
+      const bool in_prev = !S.rs[j] && j > 0;
+      const uint8_t rp = in_prev ? S.raw[j - 1] : K_NONE;
+      const uint32_t cpp = in_prev ? S.cp8[j - 1] : 0;
+      const uint8_t rn = (j + 1 < S.nch && !S.rs[j + 1]) ? S.raw[j + 1] : K_NONE;
+      if (region_start(S.raw[j], rp)) v.x = (int)pos;
+      if (trigger(S.raw[j], rp, cpp, rn)) v.y = (int)pos;
+    }
+    auto mx = [](int2 a, int2 b) { return make_int2(max(a.x, b.x), max(a.y, b.y)); };
+    int2 ex = block_exclusive_scan<PT_THREADS>(v, mx, make_int2(-1, -1), P.i2_tmp, (int2 *)nullptr);
+    int2 run = mx(W.s1_carry[t], ex);
+    for (int j = c0; j < c1; ++j) {
+      const int64_t pos = ws + S.lead[j];
+      if (pos < ts - S1_SHIFT) { S.eff[j] = effective(fam, S.raw[j], false); continue; }
+      const bool in_prev = !S.rs[j] && j > 0;
+      const uint8_t rp = in_prev ? S.raw[j - 1] : K_NONE;
+      const uint32_t cpp = in_prev ? S.cp8[j - 1] : 0;
+      const uint8_t rn = (j + 1 < S.nch && !S.rs[j + 1]) ? S.raw[j + 1] : K_NONE;
+      if (region_start(S.raw[j], rp)) run.x = (int)pos;
+      if (trigger(S.raw[j], rp, cpp, rn)) run.y = (int)pos;
+      const bool mark_other = S.raw[j] == K_MARK && run.x >= 0 && run.y >= run.x;
+      S.eff[j] = effective(fam, S.raw[j], mark_other);
+    }
+  } else {
+    for (int j = c0; j < c1; ++j) S.eff[j] = effective(fam, S.raw[j], false);
+  }
+  __syncthreads();
+
+  // --- forward scan (scan 2) over chars with pos in [ts - 16, te); the
+  // published aggregate covers the shifted tile [ts - 16, te - 16)
+  const int64_t s2_lo = ts - S2_SHIFT, s2_pub_hi = te - S2_SHIFT;
+  S2 agg_all = s2_identity(), agg_pub = s2_identity();
+  for (int j = c0; j < c1; ++j) {
+    const int64_t pos = ws + S.lead[j];
+    if (pos < s2_lo || pos >= te) continue;
+    const Nbr nb = make_nbr(S, nullptr, j);
+    const int64_t p1 = j + 1 < S.nch ? ws + S.lead[j + 1] : pos + 1;
+    const int64_t p2 = j + 2 < S.nch ? ws + S.lead[j + 2] : pos + 2;
+    const S2 el = s2_element(fam, nb, pos, p1, p2);
+    agg_all = s2_combine(agg_all, el);
+    if (t == ntiles - 1 || pos < s2_pub_hi) agg_pub = s2_combine(agg_pub, el);
+  }
+  auto comb = [](const S2 &a, const S2 &b) { return s2_combine(a, b); };
+  S2 tile_pub;
+  block_exclusive_scan<PT_THREADS>(agg_pub, comb, s2_identity(), P.s2_tmp, &tile_pub);
+  if (tid == 0)
+    P.s2_prefix = lookback(t, tile_pub, comb, s2_identity(), W.s2_agg, W.s2_inc, W.s2_flag, W.status, W.spin_limit);
+  const S2 my_ex = block_exclusive_scan<PT_THREADS>(agg_all, comb, s2_identity(), P.s2_tmp, (S2 *)nullptr);
+  S2 before = s2_combine(P.s2_prefix, my_ex);   // (P.s2_prefix visible after the scan's barriers)
+
+  // --- reverse queries over the tile's chars: first event strictly after j
+  int rq_first = 0xFFFF;
+  for (int j = c0; j < c1; ++j) {
+    const int64_t pos = ws + S.lead[j];
+    if (pos < ts || pos >= te) continue;
+    const uint8_t ew = rq_ws_event(S.rs[j], S.raw[j], S.cp8[j]);
+    const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
+    if ((rq_first & 0xFF) == 0xFF && ew != 0xFF) rq_first = (rq_first & 0xFF00) | ew;
+    if ((rq_first >> 8) == 0xFF && eu != 0xFF) rq_first = (rq_first & 0x00FF) | (eu << 8);
+  }
+  auto first = [](int a, int b) {
+    const int lo = (a & 0xFF) != 0xFF ? (a & 0xFF) : (b & 0xFF);
+    const int hi = (a >> 8) != 0xFF ? (a >> 8) : (b >> 8);
+    return lo | (hi << 8);
+  };
+  const int rq_after_me = first(block_exclusive_suffix<PT_THREADS>(rq_first, first, 0xFFFF, P.i_tmp, (int *)nullptr),
+                                W.rq_carry[2 * t] | (W.rq_carry[2 * t + 1] << 8));
+
+  // --- walk 1: per-char scan values (forward), chain states
+  for (int j = c0; j < c1; ++j) {
+    const int64_t pos = ws + S.lead[j];
+    if (pos < s2_lo || pos >= te) { P.chain[j] = 1; continue; }
+    const Nbr nb = make_nbr(S, nullptr, j);
+    const int64_t p1 = j + 1 < S.nch ? ws + S.lead[j + 1] : pos + 1;
+    const int64_t p2 = j + 2 < S.nch ? ws + S.lead[j + 2] : pos + 2;
+    const S2 el = s2_element(fam, nb, pos, p1, p2);
+    Aggs a;
+    bool ch;
+    s2_values(before, el, pos, a, ch);
+    before = s2_combine(before, el);
+    P.chain[j] = ch ? 1 : 0;
+    P.aggs[j] = (uint16_t)(a.nidx3 | (a.w_start << 2) | (a.w_prev_other << 3) | (a.w_ncw_before << 4) | (a.case_prev << 5));
+  }
+  // backward over my chars: reverse-query values
+  {
+    int after = rq_after_me;
+    for (int j = c1 - 1; j >= c0; --j) {
+      const int64_t pos = ws + S.lead[j];
+      if (pos < ts || pos >= te) continue;
+      P.aggs[j] |= (uint16_t)(((after & 0xFF) << 7) | (((after >> 8) & 0x3) << 9));
+      const uint8_t ew = rq_ws_event(S.rs[j], S.raw[j], S.cp8[j]);
+      const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
+      if (ew != 0xFF) after = (after & 0xFF00) | ew;
+      if (eu != 0xFF) after = (after & 0x00FF) | (eu << 8);
+    }
+  }
+  __syncthreads();
+
+  // --- walk 2: the predicate, then compaction of piece starts
+  uint32_t starts = 0, placeholder = 0;   // bit (j - c0) for my chars (<= 16)
+  const bool filter = __ldcg(&W.counters[5]) != 0;
+  for (int j = c0; j < c1; ++j) {
+    const int64_t pos = ws + S.lead[j];
+    if (pos < ts || pos >= te) continue;
+    const Nbr nb = make_nbr(S, P.chain, j);
+    const uint16_t g = P.aggs[j];
+    Aggs a;
+    a.nidx3 = g & 3;
+    a.w_start = (g >> 2) & 1;
+    a.w_prev_other = (g >> 3) & 1;
+    a.w_ncw_before = (g >> 4) & 1;
+    a.case_prev = (g >> 5) & 3;
+    a.rq_ws = (g >> 7) & 3;
+    a.rq_up = (g >> 9) & 3;
+    bool st = piece_start(fam, nb, a);
+    if (st && filter) {
+      const int64_t r = lower_bound64(A.offs, A.n + 1, base + pos + 1) - 1;
+      if (r >= 0 && r < A.n && W.bad[r]) {
+        if (nb.rs) placeholder |= 1u << (j - c0);
+        else st = false;
+      }
+    }
+    if (st) starts |= 1u << (j - c0);
+  }
+  int tile_count;
+  const int my_off = block_exclusive_scan<PT_THREADS>(__popc(starts), [](int a, int b) { return a + b; }, 0, P.i_tmp,
+                                                      &tile_count);
+  if (tid == 0) {
+    P.piece_base = lookback(t, tile_count, [](int a, int b) { return a + b; }, 0, W.cnt_agg, W.cnt_inc, W.cnt_flag,
+                            W.status, W.spin_limit);
+    if (t == ntiles - 1) {
+      const int np = P.piece_base + tile_count;
+      W.counters[3] = np;
+      W.piece_start[np] = (int32_t)total;
+    }
+  }
+  __syncthreads();
+  int k = P.piece_base + my_off;
+  for (uint32_t m = starts; m; m &= m - 1) {
+    const int b = __ffs(m) - 1;
+    const int j = c0 + b;
+    const int32_t pos = (int32_t)(ws + S.lead[j]);
+    W.piece_start[k++] = (placeholder >> b) & 1 ? (int32_t)(pos | 0x80000000u) : pos;
+  }
+}
+
+size_t pretok_smem_bytes() { return sizeof(PretokSmem); }
+
+void launch_prepass(const Tables &T, const Work &W, int grid, cudaStream_t s) {
+  k_prepass<<<grid, PT_THREADS, 0, s>>>(T, W);
+}
+void launch_tilescan(const Tables &T, const Work &W, cudaStream_t s) { k_tilescan<<<1, 1024, 0, s>>>(T, W); }
+void launch_pretok(const Tables &T, const Work &W, int grid, cudaStream_t s) {
+  k_pretok<<<grid, PT_THREADS, sizeof(PretokSmem), s>>>(T, W);
+}
+cudaError_t pretok_configure() {
+  return cudaFuncSetAttribute(k_pretok, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(PretokSmem));
+}
+
+}  // namespace tt

@@ -27,9 +27,25 @@ _cls = None
 _lock = threading.Lock()
 
 
+def elf_matches_host(path):
+    """True if `path` is an ELF object built for this machine's architecture."""
+    import platform
+    import struct
+    want = {"x86_64": 0x3E, "amd64": 0x3E, "aarch64": 0xB7, "arm64": 0xB7}.get(platform.machine().lower())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    if len(head) < 20 or head[:4] != b"\x7fELF":
+        return False
+    return want is None or struct.unpack("<H", head[18:20])[0] == want
+
+
 def build_lib(force=False):
     src = os.path.join(HERE, "oracle.c")
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= os.path.getmtime(src):
+    if (not force and os.path.exists(LIB_PATH) and elf_matches_host(LIB_PATH)
+            and os.path.getmtime(LIB_PATH) >= os.path.getmtime(src)):
         return LIB_PATH
     tmp = LIB_PATH + ".%d.tmp" % os.getpid()
     subprocess.check_call(["gcc", "-O2", "-std=gnu11", "-shared", "-fPIC", "-pthread", "-o", tmp, src])

@@ -1,0 +1,291 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle,
+bit-exact per piece boundary and per token ID (TokTier §4.1: both levels,
+because the ID level can hide a boundary fault), on the same seeded inputs.
+
+Covers the five workloads at full size, brute-force batches of tiny
+requests (document-boundary cuts, §4.3), runs straddling tiles at every
+alignment, long-piece lengths around the execution-unit thresholds, empty
+and invalid requests, graph replay, the host-buffer entry point, several
+streams and the status contract."""
+import os
+import random
+
+import numpy as np
+import pytest
+
+import brute
+import oracle
+from compare import compare_segmented
+from exact_bpe_tokenization_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+NCPU = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    from exact_bpe_tokenization_gb300 import binding
+    return binding
+
+
+@pytest.fixture(scope="module")
+def vocabs():
+    return {
+        "tiny": synth.make_vocab(synth.PROFILE_ASCII, 1 << 20, 4096),
+        "small1": synth.make_vocab(synth.PROFILE_MIXED, 1 << 20, 8000),
+        "small2": synth.make_vocab(synth.PROFILE_CAMEL_MARKS, 1 << 20, 8000),
+        "c1": synth.make_vocab(synth.PROFILE_MIXED, 8 << 20, 100000),
+    }
+
+
+def run_gpu(binding, tok, data, offs, stream=None, graph_repeats=1):
+    d = torch.from_numpy(np.ascontiguousarray(data)).cuda()
+    o = torch.from_numpy(np.ascontiguousarray(offs)).cuda()
+    for _ in range(graph_repeats):
+        ids, io = tok.encode(d, o, stream=stream)
+    starts, po = tok.pretokenize(d, o, stream=stream)
+    torch.cuda.synchronize()
+    status, bad = tok.status(stream)
+    io = io.cpu().numpy()
+    po = po.cpu().numpy()
+    return {"ids": ids[:int(io[-1])].cpu().numpy(), "id_offsets": io,
+            "piece_starts": starts[:int(po[-1])].cpu().numpy(), "piece_offsets": po,
+            "status": status, "bad": bad}
+
+
+def check(binding, vocab, family, reqs, threads=NCPU, expect_status=0):
+    merges, vb, vo = vocab
+    data, offs = synth.batch([r.encode() if isinstance(r, str) else r for r in reqs])
+    tok = binding.Tokenizer(merges, vb, vo, family)
+    got = run_gpu(binding, tok, data, offs)
+    ref = oracle.Oracle(merges, vb, vo, family).run(data, offs, threads=threads)
+    errs = compare_segmented(ref["piece_starts"], ref["piece_offsets"], got["piece_starts"], got["piece_offsets"],
+                             "pieces")
+    errs += compare_segmented(ref["ids"], ref["id_offsets"], got["ids"], got["id_offsets"], "ids")
+    assert not errs, "\n".join(errs)
+    bad_ref = np.nonzero(ref["status"])[0]
+    if len(bad_ref):
+        assert got["status"] == binding.TT_ERR_INVALID_UTF8 and got["bad"] == int(bad_ref[0])
+    else:
+        assert got["status"] == expect_status
+    tok.close()
+    return got
+
+
+# ------------------------------------------------------------ brute force
+ALPHABETS = {
+    1: ["a", "s", "1", " ", "\t", "\n", "\r", "'", ".", "é"],
+    2: ["a", "B", "1", " ", "\n", "'", ".", "か", "́", "\U0001F642"],
+    3: ["s", "T", "'", "a", "か", "́", " ", ".", "E", "r"],
+}
+
+
+@pytest.mark.parametrize("family,alphabet", [(1, 1), (2, 2), (2, 3), (1, 3)])
+def test_all_short_strings_as_tiny_requests(cuda, vocabs, family, alphabet):
+    """Every string of length <= 5 (111,110 requests in one batch)."""
+    reqs = list(brute.all_strings(ALPHABETS[alphabet], 5))
+    check(cuda, vocabs["small%d" % family], family, reqs)
+
+
+@pytest.mark.parametrize("family", [1, 2])
+def test_random_mixed_strings(cuda, vocabs, family):
+    alpha = ALPHABETS[family] + ["A", "t", "e", "r", "l", "m", "d", "v", "́", " ", "　", "٣", "ʰ", "ǅ", "Ü", "\t",
+                                 "\r", "0", "_", "(", "一"]
+    rng = random.Random(31 + family)
+    reqs = ["".join(rng.choice(alpha) for _ in range(rng.randint(1, 40))) for _ in range(60000)]
+    check(cuda, vocabs["small%d" % family], family, reqs)
+
+
+# ------------------------------------------------------------ workloads
+def test_tiny_ascii_64k(cuda, vocabs):
+    check(cuda, vocabs["tiny"], 1, synth.workload("tiny_ascii_64k"))
+
+
+@pytest.mark.parametrize("seed", [1, 2, 17])
+def test_single_1m_mixed(cuda, vocabs, seed):
+    check(cuda, vocabs["c1"], 1, synth.workload("single_1m_mixed", seed=seed))
+
+
+def test_burst_64_loguniform_full(cuda, vocabs):
+    check(cuda, vocabs["c1"], 1, synth.workload("burst_64_loguniform"))
+
+
+def test_adversarial_4_4m_full(cuda, vocabs):
+    check(cuda, vocabs["c1"], 1, synth.workload("adversarial_4_4m"))
+
+
+def test_o200k_256_lognormal_full(cuda):
+    vocab = synth.make_vocab(synth.PROFILE_CAMEL_MARKS, 16 << 20, 200000)
+    check(cuda, vocab, 2, synth.workload("o200k_256_lognormal"))
+
+
+# ------------------------------------------------------------ tiles and lengths
+PATHOLOGICAL = [
+    "7" * 10000, " " * 20000 + "x", "\r\n\r\n \n" * 900, ".,;:!" * 1200, "a " * 5000, "一" * 3000,
+    "x'd" + "'d" * 3000, "a" + "か" * 4000 + "B", "a" + "か" * 4000 + "Bc", "..́" + ".́" * 3000 + "a",
+    "\t" * 9000 + "\n" * 9000 + "y", "aB" * 3000, "ǅ" * 5000, "1 " * 4000,
+]
+
+
+@pytest.mark.parametrize("family", [1, 2])
+def test_runs_straddling_tiles_at_every_alignment(cuda, vocabs, family):
+    """Each pathological run is preceded by 0..47 filler bytes, so its start,
+    end and internal events fall at every offset mod 16 relative to the
+    4016-byte tiles and the 16-byte lanes."""
+    reqs = []
+    for k, run in enumerate(PATHOLOGICAL):
+        for pad in range(0, 48, 3 if k % 2 else 1):
+            reqs.append("q" * pad + " " + run + " tail")
+    check(cuda, vocabs["small%d" % family], family, reqs)
+    # and as one single request (runs cut only by content, not by documents)
+    check(cuda, vocabs["small%d" % family], family, ["z".join(reqs[::7])])
+
+
+@pytest.mark.parametrize("n", [1, 2, 31, 32, 33, 34, 64, 127, 128, 129, 1000, 4095, 4096, 4097, 50000])
+def test_piece_lengths_around_unit_thresholds(cuda, vocabs, n):
+    reqs = [" " * n + "x", "(" * n + "a", "a" * n, "é" * (n // 2 + 1), "一" * (n // 3 + 1), "b" * n + " ",
+            "\U0001F642" * (n // 4 + 1)]
+    check(cuda, vocabs["c1"], 1, reqs)
+
+
+# ------------------------------------------------------------ edge cases
+def test_empty_and_degenerate_batches(cuda, vocabs):
+    merges, vb, vo = vocabs["small1"]
+    tok = cuda.Tokenizer(merges, vb, vo, 1)
+    # n = 0
+    o = torch.zeros(1, dtype=torch.int64, device="cuda")
+    out = torch.full((1,), 7, dtype=torch.int64, device="cuda")
+    cuda.tt_encode_batch(tok.h, torch.zeros(1, dtype=torch.uint8, device="cuda"), o, 0,
+                         torch.zeros(1, dtype=torch.int32, device="cuda"), out)
+    torch.cuda.synchronize()
+    assert out.item() == 0
+    tok.close()
+    check(cuda, vocabs["small1"], 1, [""])
+    check(cuda, vocabs["small1"], 1, ["", "", ""])
+    check(cuda, vocabs["small1"], 1, ["", "a", "", " ", "", "1", ""])
+
+
+def test_invalid_utf8_requests_yield_no_ids(cuda, vocabs):
+    bad = [b"\xff", b"a\xc3", b"\x80abc", b"\xed\xa0\x80", b"\xe0\x80\x80", b"\xf4\x90\x80\x80", b"\xc0\xaf",
+           b"ok \xe2\x82", b"\xf0\x9f\x98"]
+    good = [s.encode() for s in ["hello world", "don't 123456", "  \n\t x", "camelCase"]]
+    reqs = []
+    for i in range(len(bad)):
+        reqs += [good[i % 4], bad[i]]
+    reqs.append(good[0])
+    got = check(cuda, vocabs["small1"], 1, reqs)
+    io = got["id_offsets"]
+    for r in range(1, len(reqs) - 1, 2):
+        assert io[r + 1] == io[r]
+    # a multi-byte char split across two requests is invalid on both sides
+    check(cuda, vocabs["small1"], 1, ["ab\xc3".encode("latin-1"), b"\xa9cd", b"fine"])
+
+
+def test_offsets_with_nonzero_base(cuda, vocabs):
+    merges, vb, vo = vocabs["small1"]
+    reqs = [synth.transcript(3 + i, 5000, 1) for i in range(5)]
+    data, offs = synth.batch(reqs)
+    pad = 37
+    data2 = np.concatenate([np.full(pad, 0x41, dtype=np.uint8), data])
+    offs2 = offs + pad
+    tok = cuda.Tokenizer(merges, vb, vo, 1)
+    d = torch.from_numpy(data2).cuda()
+    o = torch.from_numpy(offs2).cuda()
+    ids = torch.empty(len(data2), dtype=torch.int32, device="cuda")
+    io = torch.empty(len(offs2), dtype=torch.int64, device="cuda")
+    cuda.tt_encode_batch(tok.h, d, o, len(reqs), ids, io)
+    io = io.cpu().numpy()
+    ref = oracle.Oracle(merges, vb, vo, 1).run(data, offs)
+    assert np.array_equal(io, ref["id_offsets"])
+    assert np.array_equal(ids[:int(io[-1])].cpu().numpy(), ref["ids"])
+    tok.close()
+
+
+def test_graph_replay_eager_and_host_paths_agree(cuda, vocabs):
+    merges, vb, vo = vocabs["c1"]
+    reqs = synth.workload("burst_64_loguniform", scale=0.05)
+    data, offs = synth.batch(reqs)
+    ref = oracle.Oracle(merges, vb, vo, 1).run(data, offs, threads=NCPU)
+    tok = cuda.Tokenizer(merges, vb, vo, 1)
+    d = torch.from_numpy(data).cuda()
+    o = torch.from_numpy(offs).cuda()
+    outs = []
+    for rep in range(3):                         # first call captures, later ones replay
+        ids, io = tok.encode(d, o)
+        torch.cuda.synchronize()
+        outs.append((ids[:int(io[-1].item())].cpu().numpy(), io.cpu().numpy()))
+    cuda.tt_profile(tok.h, 1)                    # eager launches with events
+    ids, io = tok.encode(d, o)
+    prof = cuda.tt_profile_read(tok.h)
+    cuda.tt_profile(tok.h, 0)
+    outs.append((ids[:int(io[-1].item())].cpu().numpy(), io.cpu().numpy()))
+    hids, hio, st = tok.encode_host(data, offs)
+    outs.append((hids, hio))
+    for i, (a, b) in enumerate(outs):
+        assert np.array_equal(b, ref["id_offsets"]), i
+        assert np.array_equal(a, ref["ids"]), i
+    assert st == 0
+    assert set(prof) >= {"k_prepass", "k_pretok", "k_bpe_small", "k_ids"} and all(v[1] == 1 for v in prof.values())
+    tok.close()
+
+
+def test_two_streams_and_growing_batches(cuda, vocabs):
+    merges, vb, vo = vocabs["c1"]
+    tok = cuda.Tokenizer(merges, vb, vo, 1)
+    o1 = oracle.Oracle(merges, vb, vo, 1)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for size in (1000, 70000, 300000, 20000):
+        jobs = []
+        for si, s in enumerate(streams):
+            reqs = [synth.transcript(100 * size + si * 7 + i, size // 4 + 1, 1) for i in range(4)]
+            data, offs = synth.batch(reqs)
+            with torch.cuda.stream(s):
+                d = torch.from_numpy(data).cuda()
+                o = torch.from_numpy(offs).cuda()
+                ids, io = tok.encode(d, o, stream=s)
+            jobs.append((data, offs, ids, io, s))
+        for data, offs, ids, io, s in jobs:
+            s.synchronize()
+            io = io.cpu().numpy()
+            ref = o1.run(data, offs)
+            assert np.array_equal(io, ref["id_offsets"])
+            assert np.array_equal(ids[:int(io[-1])].cpu().numpy(), ref["ids"])
+    tok.close()
+
+
+def test_capacity_bound_is_reported(cuda, vocabs):
+    merges, vb, vo = vocabs["small1"]
+    tok = cuda.Tokenizer(merges, vb, vo, 1)
+    data, offs = synth.batch([synth.transcript(9, 300000, 1)])
+    d = torch.from_numpy(data).cuda()
+    o = torch.from_numpy(offs).cuda()
+    ids = torch.empty(len(data), dtype=torch.int32, device="cuda")
+    io = torch.full((2,), 5, dtype=torch.int64, device="cuda")
+    cuda.tt_encode_batch_bounded(tok.h, d, o, 1, 1000, ids, io)   # bound far below the batch
+    status, _ = tok.status()
+    assert status == cuda.TT_ERR_CAPACITY
+    assert io.cpu().tolist() == [0, 0]
+    ids, io = tok.encode(d, o)                                   # the handle keeps working
+    torch.cuda.synchronize()
+    assert tok.status()[0] == 0
+    ref = oracle.Oracle(merges, vb, vo, 1).run(data, offs)
+    assert np.array_equal(io.cpu().numpy(), ref["id_offsets"])
+    tok.close()
+
+
+def test_decreasing_offsets_are_rejected_by_status(cuda, vocabs):
+    merges, vb, vo = vocabs["small1"]
+    tok = cuda.Tokenizer(merges, vb, vo, 1)
+    data = np.frombuffer(b"hello world, this is fine", dtype=np.uint8).copy()
+    offs = np.array([0, 12, 5, 25], dtype=np.int64)
+    d = torch.from_numpy(data).cuda()
+    o = torch.from_numpy(offs).cuda()
+    tok.encode(d, o)
+    status, _ = tok.status()
+    assert status == cuda.TT_ERR_INVALID_ARG
+    tok.close()
