@@ -31,9 +31,9 @@ using namespace tt;
 
 namespace {
 
-constexpr int N_KERNELS = 7;
+constexpr int N_KERNELS = 8;
 const char *KERNEL_NAMES[N_KERNELS] = {"k_prepass", "k_tilescan", "k_pretok", "k_bpe_small",
-                                       "k_bpe_long", "k_ids", "k_req"};
+                                       "k_bpe_mid", "k_bpe_long", "k_ids", "k_req"};
 
 struct Workspace {
   Work W{};
@@ -41,6 +41,7 @@ struct Workspace {
   size_t mem_bytes = 0;
   int64_t cap_bytes = 0, cap_reqs = 0;
   cudaGraphExec_t graph = nullptr;
+  cudaStream_t cap_stream = nullptr;   // private stream the graph is captured on
   // device staging for tt_encode_host (bytes, offsets, ids, id offsets)
   void *stage = nullptr;
   size_t stage_bytes = 0;
@@ -248,6 +249,7 @@ extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, con
 static void free_workspace(Workspace *w) {
   if (!w) return;
   if (w->graph) cudaGraphExecDestroy(w->graph);
+  if (w->cap_stream) cudaStreamDestroy(w->cap_stream);
   if (w->mem) cudaFree(w->mem);
   if (w->stage) cudaFree(w->stage);
   delete w;
@@ -283,7 +285,9 @@ static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_
       {(void **)&W.piece_start, 4 * (size_t)(cap_bytes + 2)}, {(void **)&W.n_ids, 4 * (size_t)(cap_bytes + 1)},
       {(void **)&W.id_off, 4 * (size_t)(cap_bytes + 2)},      {(void **)&W.scratch, 4 * (size_t)(cap_bytes + 1)},
       {(void **)&W.tmp_a, 4 * (size_t)(cap_bytes + 1)},       {(void **)&W.tmp_b, 4 * (size_t)(cap_bytes + 1)},
+      {(void **)&W.tmp_c, 4 * (size_t)(cap_bytes + 1)},
       {(void **)&W.long_list, 4 * (size_t)(cap_bytes / (SMALL_MAX + 1) + 2)},
+      {(void **)&W.huge_list, 4 * (size_t)(cap_bytes / (MID_MAX + 1) + 2)},
       {(void **)&W.bad, (size_t)cap_reqs + 1},          {(void **)&W.bad_pre, 4 * (size_t)(cap_reqs + 2)},
       {(void **)&W.args, sizeof(CallArgs)},
   };
@@ -352,7 +356,13 @@ static int grid_small(const Workspace *w) {
   const int64_t g = (w->cap_bytes / 4 + BPE_SMALL_THREADS - 1) / BPE_SMALL_THREADS;
   return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 8);
 }
-static int grid_long(const Workspace *w) { return 152 * 2; }
+static int grid_mid(const Workspace *w) {   // one warp per listed piece
+  const int64_t g = (w->cap_bytes / (SMALL_MAX + 1) + (BPE_MID_THREADS / 32) - 1) / (BPE_MID_THREADS / 32);
+  return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 8);
+}
+static int grid_long(const Workspace *w) {
+  return (int)std::min<int64_t>(std::max<int64_t>(w->cap_bytes / (MID_MAX + 1), 1), 152 * 2);
+}
 
 // Enqueue the kernels of one encode on `stream` (eager; optionally timed).
 static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stream, bool timed) {
@@ -368,9 +378,10 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
       case 1: launch_tilescan(T, W, stream); break;
       case 2: launch_pretok(T, W, grid_tiles(w), stream); break;
       case 3: launch_bpe_small(T, W, grid_small(w), stream); break;
-      case 4: launch_bpe_long(T, W, grid_long(w), stream); break;
-      case 5: launch_ids(T, W, grid_chunks(w), stream); break;
-      case 6: launch_req(T, W, grid_reqs(w), stream); break;
+      case 4: launch_bpe_mid(T, W, grid_mid(w), stream); break;
+      case 5: launch_bpe_long(T, W, grid_long(w), stream); break;
+      case 6: launch_ids(T, W, grid_chunks(w), stream); break;
+      case 7: launch_req(T, W, grid_reqs(w), stream); break;
     }
     if (timed) { cudaEventRecord(b, stream); h->pending.push_back({kidx, a, b}); }
   }
@@ -379,17 +390,19 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
   return TT_OK;
 }
 
+// max_bytes: a host-known bound on the batch's bytes (-1 = unknown); buffers
+// for bytes and IDs may be NULL only when the batch has no bytes
 static tt_status check_batch_args(tt_tokenizer *h, const void *d_utf8, const int64_t *offs, int64_t n,
-                                  const void *out_ids, const int64_t *out_offs) {
+                                  const void *out_ids, const int64_t *out_offs, int64_t max_bytes) {
   if (!h || n < 0 || !offs || !out_offs) return TT_ERR_INVALID_ARG;
-  if (n > 0 && (!d_utf8 || !out_ids)) return TT_ERR_INVALID_ARG;
+  if (n > 0 && max_bytes != 0 && (!d_utf8 || !out_ids)) return TT_ERR_INVALID_ARG;
   return TT_OK;
 }
 
 extern "C" tt_status tt_encode_batch_bounded(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
                                              int64_t n_requests, int64_t max_total_bytes, int32_t *d_out_ids,
                                              int64_t *d_out_id_offsets, tt_stream_t stream_) {
-  tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets);
+  tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, max_total_bytes);
   if (s != TT_OK) return s;
   if (max_total_bytes < 0 || max_total_bytes >= INT32_MAX - 64) return TT_ERR_CAPACITY;
   cudaStream_t stream = (cudaStream_t)stream_;
@@ -404,10 +417,13 @@ extern "C" tt_status tt_encode_batch_bounded(tt_tokenizer *h, const uint8_t *d_u
   TT_CUDA(cudaMemcpyAsync(w->W.args, &args, sizeof(args), cudaMemcpyHostToDevice, stream));
   if (h->profiling || !h->graphs_enabled) return enqueue_encode(h, w, stream, h->profiling);
   if (!w->graph) {
+    // capture on a private stream (the caller's may be the legacy default
+    // stream, which cannot be captured); the graph is launched on the caller's
+    if (!w->cap_stream) TT_CUDA(cudaStreamCreateWithFlags(&w->cap_stream, cudaStreamNonBlocking));
     cudaGraph_t g;
-    TT_CUDA(cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal));
-    tt_status es = enqueue_encode(h, w, stream, false);
-    cudaError_t ce = cudaStreamEndCapture(stream, &g);
+    TT_CUDA(cudaStreamBeginCapture(w->cap_stream, cudaStreamCaptureModeThreadLocal));
+    tt_status es = enqueue_encode(h, w, w->cap_stream, false);
+    cudaError_t ce = cudaStreamEndCapture(w->cap_stream, &g);
     h->launches -= N_KERNELS;   // captured, not launched
     if (es != TT_OK) return es;
     TT_CUDA(ce);
@@ -423,7 +439,7 @@ extern "C" tt_status tt_encode_batch_bounded(tt_tokenizer *h, const uint8_t *d_u
 extern "C" tt_status tt_encode_batch(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
                                      int64_t n_requests, int32_t *d_out_ids, int64_t *d_out_id_offsets,
                                      tt_stream_t stream_) {
-  tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets);
+  tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, 0);
   if (s != TT_OK) return s;
   cudaStream_t stream = (cudaStream_t)stream_;
   if (n_requests == 0) {
@@ -435,6 +451,7 @@ extern "C" tt_status tt_encode_batch(tt_tokenizer *h, const uint8_t *d_utf8, con
   TT_CUDA(cudaMemcpyAsync(&ends[1], d_byte_offsets + n_requests, 8, cudaMemcpyDeviceToHost, stream));
   TT_CUDA(cudaStreamSynchronize(stream));
   if (ends[0] < 0 || ends[1] < ends[0]) return TT_ERR_INVALID_ARG;
+  if (ends[1] > ends[0] && (!d_utf8 || !d_out_ids)) return TT_ERR_INVALID_ARG;
   return tt_encode_batch_bounded(h, d_utf8, d_byte_offsets, n_requests, ends[1] - ends[0], d_out_ids,
                                  d_out_id_offsets, stream_);
 }
@@ -503,7 +520,7 @@ extern "C" tt_status tt_encode_host(tt_tokenizer *h, const uint8_t *utf8, const 
 extern "C" tt_status tt_pretokenize_batch(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
                                           int64_t n_requests, int64_t *d_piece_starts, int64_t *d_piece_offsets,
                                           tt_stream_t stream_) {
-  tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_piece_starts, d_piece_offsets);
+  tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_piece_starts, d_piece_offsets, 0);
   if (s != TT_OK) return s;
   cudaStream_t stream = (cudaStream_t)stream_;
   if (n_requests == 0) {
@@ -515,6 +532,7 @@ extern "C" tt_status tt_pretokenize_batch(tt_tokenizer *h, const uint8_t *d_utf8
   TT_CUDA(cudaMemcpyAsync(&ends[1], d_byte_offsets + n_requests, 8, cudaMemcpyDeviceToHost, stream));
   TT_CUDA(cudaStreamSynchronize(stream));
   if (ends[0] < 0 || ends[1] < ends[0]) return TT_ERR_INVALID_ARG;
+  if (ends[1] > ends[0] && (!d_utf8 || !d_piece_starts)) return TT_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(h->mu);
   Workspace *w;
   if ((s = get_workspace(h, stream, ends[1] - ends[0], n_requests, &w)) != TT_OK) return s;

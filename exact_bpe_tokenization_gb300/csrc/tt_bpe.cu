@@ -41,7 +41,43 @@ __device__ __forceinline__ int vocab_probe(const Tables &T, const uint8_t *b, in
   }
 }
 
+// Round merging of one piece by one thread.  ids/rk live in thread-local
+// arrays of MAXLEN entries; `bytes` points to the piece (any memory space).
+// Returns the number of IDs written to out.
+template <int MAXLEN>
+__device__ __forceinline__ int bpe_thread(const Tables &T, const uint8_t *bytes, int len, int32_t *out) {
+  int ids[MAXLEN], rk[MAXLEN];
+  int n = len;
+  for (int i = 0; i < n; ++i) ids[i] = __ldg(&T.byte_id[bytes[i]]);
+  for (int i = 0; i + 1 < n; ++i) rk[i] = pair_rank(T, ids[i], ids[i + 1]);
+  for (;;) {
+    int r = INT_MAX;
+    for (int i = 0; i + 1 < n; ++i)
+      if (rk[i] >= 0 && rk[i] < r) r = rk[i];
+    if (r == INT_MAX) break;
+    const int res = __ldg(&T.merge_result[r]);
+    // one sweep: merge every leftmost non-overlapping occurrence of rank r;
+    // ranks of untouched pairs are kept, pairs next to a merge are looked up
+    int w = 0, i = 0;
+    bool prev_merged = false;
+    while (i < n) {
+      const bool m = (i + 1 < n) && rk[i] == r;
+      const int tok = m ? res : ids[i];
+      if (w > 0) rk[w - 1] = (m || prev_merged) ? pair_rank(T, ids[w - 1], tok) : rk[i - 1];
+      ids[w] = tok;
+      prev_merged = m;
+      ++w;
+      i += m ? 2 : 1;
+    }
+    n = w;
+  }
+  for (int i = 0; i < n; ++i) out[i] = ids[i];
+  return n;
+}
+
 // ---------------------------------------------------------------- small
+// Thread per piece over all pieces; pieces longer than SMALL_MAX bytes are
+// listed for k_bpe_mid.
 __global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work W) {
   const CallArgs A = *W.args;
   if (A.n <= 0) return;
@@ -67,41 +103,165 @@ __global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work 
       const int id = vocab_probe(T, buf, len);
       if (id >= 0) { out[0] = id; W.n_ids[k] = 1; continue; }
     }
-    int ids[SMALL_MAX], rk[SMALL_MAX];
+    W.n_ids[k] = bpe_thread<SMALL_MAX>(T, buf, len, out);
+  }
+}
+
+// ---------------------------------------------------------------- mid
+// Warp per piece over the pieces longer than SMALL_MAX (up to MID_MAX bytes;
+// longer ones are listed for k_bpe_long).  The token and rank arrays live in
+// shared memory; lane l owns a contiguous segment.  A round: warp min of the
+// ranks, an exclusive max-scan carrying where the current run of hits started
+// (leftmost non-overlapping selection of (a, a) runs), an exclusive sum-scan
+// of kept tokens, the write into the other buffer, then lookups for the
+// pairs next to a merge -- shuffles only, no block barrier.
+__device__ __forceinline__ int warp_min(int v) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, d));
+  return v;
+}
+__device__ __forceinline__ int warp_excl_max(int v, int lane) {
+  int inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, d);
+    if (lane >= d) inc = max(inc, y);
+  }
+  const int ex = __shfl_up_sync(0xffffffffu, inc, 1);
+  return lane == 0 ? -1 : ex;
+}
+__device__ __forceinline__ int warp_excl_sum(int v, int lane, int *total) {
+  int inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, d);
+    if (lane >= d) inc += y;
+  }
+  *total = __shfl_sync(0xffffffffu, inc, 31);
+  return inc - v;
+}
+
+constexpr int MID_WARPS = BPE_MID_THREADS / 32;
+
+__global__ void __launch_bounds__(BPE_MID_THREADS) k_bpe_mid(Tables T, Work W) {
+  constexpr int32_t MERGED = (int32_t)0x80000000;
+  __shared__ int32_t sm[MID_WARPS][4][MID_MAX];
+  const CallArgs A = *W.args;
+  if (A.n <= 0) return;
+  const int64_t base = __ldg(&A.offs[0]);
+  const int64_t total = __ldg(&A.offs[A.n]) - base;
+  if (total > W.cap_bytes || total < 0 || base < 0) return;
+  const int nl = __ldcg(&W.counters[2]);
+  const uint8_t *g = A.utf8 + base;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = gridDim.x * MID_WARPS;
+  for (int li = blockIdx.x * MID_WARPS + warp; li < nl; li += nwarps) {
+    const int k = __ldcg(&W.long_list[li]);
+    const int32_t s = __ldcg(&W.piece_start[k]);
+    const int32_t e = __ldcg(&W.piece_start[k + 1]) & 0x7FFFFFFF;
+    const int len = e - s;
+    if (len > MID_MAX) {
+      if (lane == 0) W.huge_list[atomicAdd(&W.counters[6], 1)] = k;
+      continue;
+    }
+    const uint8_t *b = g + s;
+    if (len <= T.max_tok_len) {
+      int id = 0;
+      if (lane == 0) id = vocab_probe(T, b, len);
+      id = __shfl_sync(0xffffffffu, id, 0);
+      if (id >= 0) {
+        if (lane == 0) { W.scratch[s] = id; W.n_ids[k] = 1; }
+        continue;
+      }
+    }
+    int32_t *cur = sm[warp][0], *nxt = sm[warp][1], *rcur = sm[warp][2], *rnxt = sm[warp][3];
     int n = len;
-    for (int i = 0; i < n; ++i) ids[i] = __ldg(&T.byte_id[buf[i]]);
-    for (int i = 0; i + 1 < n; ++i) rk[i] = pair_rank(T, ids[i], ids[i + 1]);
+    for (int i = lane; i < n; i += 32) cur[i] = __ldg(&T.byte_id[__ldg(b + i)]);
+    __syncwarp();
+    for (int i = lane; i + 1 < n; i += 32) rcur[i] = pair_rank(T, cur[i], cur[i + 1]);
+    __syncwarp();
     for (;;) {
-      int r = INT_MAX;
-      for (int i = 0; i + 1 < n; ++i)
-        if (rk[i] >= 0 && rk[i] < r) r = rk[i];
+      const int seg = (n + 31) >> 5;
+      const int lo = min(lane * seg, n), hi = min(lo + seg, n);
+      int lm = INT_MAX;
+      for (int i = lo; i < hi && i + 1 < n; ++i)
+        if (rcur[i] >= 0 && rcur[i] < lm) lm = rcur[i];
+      const int r = warp_min(lm);
       if (r == INT_MAX) break;
       const int res = __ldg(&T.merge_result[r]);
-      // one sweep: merge every leftmost non-overlapping occurrence of rank r;
-      // ranks of untouched pairs are kept, pairs next to a merge are looked up
-      int w = 0, i = 0;
-      bool prev_merged = false;
-      while (i < n) {
-        const bool m = (i + 1 < n) && rk[i] == r;
-        const int tok = m ? res : ids[i];
-        if (w > 0) rk[w - 1] = (m || prev_merged) ? pair_rank(T, ids[w - 1], tok) : rk[i - 1];
-        ids[w] = tok;
-        prev_merged = m;
-        ++w;
-        i += m ? 2 : 1;
+      int after_nh = -1;
+      for (int i = lo; i < hi; ++i)
+        if (!(i + 1 < n && rcur[i] == r)) after_nh = i + 1;
+      int run_in = warp_excl_max(after_nh, lane);
+      if (run_in < 0) run_in = 0;
+      bool prev_sel = false;
+      if (lo > 0 && lo < n) prev_sel = rcur[lo - 1] == r && ((lo - 1 - run_in) % 2 == 0);
+      int keep = 0;
+      {
+        int run = run_in;
+        bool ps = prev_sel;
+        for (int i = lo; i < hi; ++i) {
+          const bool h = i + 1 < n && rcur[i] == r;
+          if (!h) run = i + 1;
+          if (!ps) ++keep;
+          ps = h && ((i - run) % 2 == 0);
+        }
       }
-      n = w;
+      int n_new;
+      const int wbase = warp_excl_sum(keep, lane, &n_new);
+      {
+        int run = run_in, w = wbase;
+        bool ps = prev_sel;
+        for (int i = lo; i < hi; ++i) {
+          const bool h = i + 1 < n && rcur[i] == r;
+          if (!h) run = i + 1;
+          const bool sel = h && ((i - run) % 2 == 0);
+          if (!ps) {
+            nxt[w] = sel ? (res | MERGED) : cur[i];
+            rnxt[w] = (i + 1 < n) ? rcur[i] : -1;
+            ++w;
+          }
+          ps = sel;
+        }
+      }
+      __syncwarp();
+      for (int j = wbase; j < wbase + keep; ++j) {
+        if (j + 1 >= n_new) { rnxt[j] = -1; continue; }
+        const int a = nxt[j], c = nxt[j + 1];
+        if ((a | c) & MERGED) rnxt[j] = pair_rank(T, a & 0x7FFFFFFF, c & 0x7FFFFFFF);
+      }
+      __syncwarp();
+      for (int j = wbase; j < wbase + keep; ++j) nxt[j] &= 0x7FFFFFFF;
+      __syncwarp();
+      int32_t *t1 = cur; cur = nxt; nxt = t1;
+      int32_t *t2 = rcur; rcur = rnxt; rnxt = t2;
+      n = n_new;
     }
-    for (int i = 0; i < n; ++i) out[i] = ids[i];
-    W.n_ids[k] = n;
+    for (int i = lane; i < n; i += 32) W.scratch[s + i] = cur[i];
+    if (lane == 0) W.n_ids[k] = n;
+    __syncwarp();
   }
 }
 
 // ---------------------------------------------------------------- long
+// Block per piece.  Thread t owns a contiguous segment of the current token
+// array; a round is: block min of the ranks, a block max-scan that carries
+// "where the current run of hits started" across segments (a run of equal
+// pairs (a, a) is merged at even offsets: the leftmost non-overlapping
+// selection), a block sum-scan of kept tokens, and a write of the new tokens
+// (merge flag in bit 31) and of the old rank of every untouched pair into the
+// other buffer; after a barrier the pairs next to a merge are looked up.
+// A one-entry cache per thread absorbs the repeated lookups of long runs.
+__device__ __forceinline__ int cached_rank(const Tables &T, int l, int r, int &cl, int &cr, int &cv) {
+  if (l == cl && r == cr) return cv;
+  cl = l; cr = r; cv = pair_rank(T, l, r);
+  return cv;
+}
+
 __global__ void __launch_bounds__(BPE_LONG_THREADS) k_bpe_long(Tables T, Work W) {
   constexpr int NT = BPE_LONG_THREADS;
+  constexpr int32_t MERGED = (int32_t)0x80000000;
   __shared__ int red[NT / 32];
-  __shared__ uint8_t sel_s[NT];
   __shared__ int s_whole;
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
@@ -109,76 +269,108 @@ __global__ void __launch_bounds__(BPE_LONG_THREADS) k_bpe_long(Tables T, Work W)
   const int64_t base = __ldg(&A.offs[0]);
   const int64_t total = __ldg(&A.offs[A.n]) - base;
   if (total > W.cap_bytes || total < 0 || base < 0) return;
-  const int nl = __ldcg(&W.counters[2]);
+  const int nh = __ldcg(&W.counters[6]);
   const uint8_t *g = A.utf8 + base;
   auto plus = [](int a, int b) { return a + b; };
   auto mx = [](int a, int b) { return a > b ? a : b; };
   auto mn = [](int a, int b) { return a < b ? a : b; };
-  for (int li = blockIdx.x; li < nl; li += gridDim.x) {
-    const int k = __ldcg(&W.long_list[li]);
+  int cl = -1, cr = -1, cv = -1;
+  for (int li = blockIdx.x; li < nh; li += gridDim.x) {
+    const int k = __ldcg(&W.huge_list[li]);
     const int32_t s = __ldcg(&W.piece_start[k]);
     const int32_t e = __ldcg(&W.piece_start[k + 1]) & 0x7FFFFFFF;
     const int len = e - s;
-    if (len <= 0 || e > total) {
-      if (tid == 0) W.n_ids[k] = 0;
-      continue;
-    }
     const uint8_t *b = g + s;
-    int32_t *tok = W.scratch + s;
-    int32_t *rk = W.tmp_a + s;
     if (len <= T.max_tok_len) {
       if (tid == 0) s_whole = vocab_probe(T, b, len);
       __syncthreads();
       const int whole = s_whole;
       __syncthreads();
       if (whole >= 0) {
-        if (tid == 0) { tok[0] = whole; W.n_ids[k] = 1; }
+        if (tid == 0) { W.scratch[s] = whole; W.n_ids[k] = 1; }
         continue;
       }
     }
+    int32_t *cur = W.scratch + s, *nxt = W.tmp_b + s;
+    int32_t *rcur = W.tmp_a + s, *rnxt = W.tmp_c + s;
     int n = len;
-    for (int i = tid; i < n; i += NT) tok[i] = __ldg(&T.byte_id[__ldg(b + i)]);
+    for (int i = tid; i < n; i += NT) cur[i] = __ldg(&T.byte_id[__ldg(b + i)]);
     __syncthreads();
-    for (int i = tid; i + 1 < n; i += NT) rk[i] = pair_rank(T, tok[i], tok[i + 1]);
+    for (int i = tid; i + 1 < n; i += NT) rcur[i] = cached_rank(T, cur[i], cur[i + 1], cl, cr, cv);
     __syncthreads();
     for (;;) {
+      const int seg = (n + NT - 1) / NT;
+      const int lo = min(tid * seg, n), hi = min(lo + seg, n);
       int lm = INT_MAX;
-      for (int i = tid; i + 1 < n; i += NT)
-        if (rk[i] >= 0 && rk[i] < lm) lm = rk[i];
+      for (int i = lo; i < hi && i + 1 < n; ++i)
+        if (rcur[i] >= 0 && rcur[i] < lm) lm = rcur[i];
       int r;
       block_exclusive_scan<NT>(lm, mn, INT_MAX, red, &r);
       if (r == INT_MAX) break;
       const int res = __ldg(&T.merge_result[r]);
-      // in-place compaction, chunk by chunk; carries: run start (position
-      // after the last non-hit), kept count, selected flag of the previous
-      // element
-      int carry_run = 0, carry_keep = 0;
+      // position after the last non-hit of my segment (-1 if all hits)
+      int after_nh = -1;
+      for (int i = lo; i < hi; ++i)
+        if (!(i + 1 < n && rcur[i] == r)) after_nh = i + 1;
+      int run_in = block_exclusive_scan<NT>(after_nh, mx, -1, red, (int *)nullptr);
+      if (run_in < 0) run_in = 0;
+      // was the element before my segment selected?
       bool prev_sel = false;
-      for (int c = 0; c < n; c += NT) {
-        const int i = c + tid;
-        const bool hit = i + 1 < n && rk[i] == r;
-        const int tv = i < n ? tok[i] : 0;
-        const int v = (i < n && !hit) ? i + 1 : -1;
-        int chunk_max;
-        const int ex_run = block_exclusive_scan<NT>(v, mx, -1, red, &chunk_max);
-        const int run = mx(carry_run, mx(ex_run, v));      // inclusive; v = -1 for hits
-        const bool sel = hit && ((i - run) % 2 == 0);
-        sel_s[tid] = sel;
-        __syncthreads();
-        const bool removed = tid == 0 ? prev_sel : sel_s[tid - 1] != 0;
-        const bool keep = i < n && !removed;
-        int chunk_keep;
-        const int ex_keep = block_exclusive_scan<NT>(keep ? 1 : 0, plus, 0, red, &chunk_keep);
-        if (keep) tok[carry_keep + ex_keep] = sel ? res : tv;   // reads of this chunk are done
-        const bool last_sel = sel_s[NT - 1] != 0;
-        carry_run = mx(carry_run, chunk_max);
-        carry_keep += chunk_keep;
-        prev_sel = last_sel;
-        __syncthreads();
+      if (lo > 0 && lo < n) {
+        const bool h = rcur[lo - 1] == r;          // lo - 1 + 1 < n holds
+        prev_sel = h && ((lo - 1 - run_in) % 2 == 0);
       }
-      n = carry_keep;
-      for (int i = tid; i + 1 < n; i += NT) rk[i] = pair_rank(T, tok[i], tok[i + 1]);
+      // count kept tokens
+      int keep = 0;
+      {
+        int run = run_in;
+        bool ps = prev_sel;
+        for (int i = lo; i < hi; ++i) {
+          const bool h = i + 1 < n && rcur[i] == r;
+          if (!h) run = i + 1;
+          const bool sel = h && ((i - run) % 2 == 0);
+          if (!ps) ++keep;
+          ps = sel;
+        }
+      }
+      int n_new;
+      const int wbase = block_exclusive_scan<NT>(keep, plus, 0, red, &n_new);
+      // write new tokens (merge flag in bit 31) and candidate ranks
+      {
+        int run = run_in, w = wbase;
+        bool ps = prev_sel;
+        for (int i = lo; i < hi; ++i) {
+          const bool h = i + 1 < n && rcur[i] == r;
+          if (!h) run = i + 1;
+          const bool sel = h && ((i - run) % 2 == 0);
+          if (!ps) {
+            nxt[w] = sel ? (res | MERGED) : cur[i];
+            // the old pair (i, i+1) survives unless i or i+1 merges
+            rnxt[w] = (i + 1 < n) ? rcur[i] : -1;
+            ++w;
+          }
+          ps = sel;
+        }
+      }
       __syncthreads();
+      // ranks of the new pairs next to a merge
+      {
+        const int nlo = wbase, nhi = wbase + keep;
+        for (int j = nlo; j < nhi; ++j) {
+          if (j + 1 >= n_new) { rnxt[j] = -1; continue; }
+          const int a = nxt[j], bb = nxt[j + 1];
+          if ((a | bb) & MERGED) rnxt[j] = cached_rank(T, a & 0x7FFFFFFF, bb & 0x7FFFFFFF, cl, cr, cv);
+        }
+      }
+      __syncthreads();
+      for (int j = wbase; j < wbase + keep; ++j) nxt[j] &= 0x7FFFFFFF;
+      __syncthreads();
+      int32_t *t1 = cur; cur = nxt; nxt = t1;
+      int32_t *t2 = rcur; rcur = rnxt; rnxt = t2;
+      n = n_new;
+    }
+    if (cur != W.scratch + s) {
+      for (int i = tid; i < n; i += NT) W.scratch[s + i] = cur[i];
     }
     if (tid == 0) W.n_ids[k] = n;
     __syncthreads();
@@ -214,12 +406,15 @@ __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
   }
   int chunk_total;
   const int ex = block_exclusive_scan<IDS_THREADS>(sum, [](int a, int b) { return a + b; }, 0, red, &chunk_total);
-  if (tid == 0) {
-    s_base = lookback(t, chunk_total, [](int a, int b) { return a + b; }, 0, W.ids_agg, W.ids_inc, W.ids_flag,
-                      W.status, W.spin_limit);
-    if (t == nchunks - 1) {
-      W.id_off[np] = s_base + chunk_total;
-      W.counters[4] = s_base + chunk_total;
+  if (tid < 32) {
+    const int b = warp_lookback(t, chunk_total, [](int a, int b) { return a + b; }, 0, W.ids_agg, W.ids_inc,
+                                W.ids_flag, W.status, W.spin_limit);
+    if (tid == 0) {
+      s_base = b;
+      if (t == nchunks - 1) {
+        W.id_off[np] = b + chunk_total;
+        W.counters[4] = b + chunk_total;
+      }
     }
   }
   __syncthreads();
@@ -322,6 +517,9 @@ __global__ void k_hook_offsets(Work W) {
 
 void launch_bpe_small(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   k_bpe_small<<<grid, BPE_SMALL_THREADS, 0, s>>>(T, W);
+}
+void launch_bpe_mid(const Tables &T, const Work &W, int grid, cudaStream_t s) {
+  k_bpe_mid<<<grid, BPE_MID_THREADS, 0, s>>>(T, W);
 }
 void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   k_bpe_long<<<grid, BPE_LONG_THREADS, 0, s>>>(T, W);

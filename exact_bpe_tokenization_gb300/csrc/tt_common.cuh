@@ -24,7 +24,9 @@ constexpr int S2_SHIFT = 16;                 // forward scan enters at tile star
 static_assert(TILE % 16 == 0, "tile must keep 16-byte alignment");
 
 // BPE execution units by piece length (bytes)
-constexpr int SMALL_MAX = 32;                // thread per piece, state in registers / local
+constexpr int SMALL_MAX = 32;                // thread per piece, dense over all pieces
+constexpr int MID_MAX = 256;                 // thread per piece, dense over the longer ones
+                                             // (> MID_MAX: a block per piece)
 constexpr int IDS_CHUNK = 2048;              // pieces per CTA in the ID scatter
 
 // status codes (mirror include/toktier.h)
@@ -262,6 +264,69 @@ done:
   st_release(&flag[tile], 2);
   return excl;
 }
+// Decoupled look-back by one full warp (the warp that calls it; all 32 lanes
+// must call).  Each step inspects the 32 nearest unread predecessors at once:
+// a ballot finds the nearest one with an inclusive prefix, and the aggregates
+// in between are combined by a warp reduction in tile order.  Returns the
+// exclusive prefix on every lane; lane 0 publishes.  Every wait is bounded.
+template <typename T, typename Op>
+__device__ T warp_lookback(int tile, T local, Op op, T identity, T *agg, T *inc, int *flag, DevStatus *st,
+                           int spin_limit) {
+  const int lane = threadIdx.x & 31;
+  if (tile == 0) {
+    if (lane == 0) {
+      inc[0] = local;
+      __threadfence();
+      st_release(&flag[0], 2);
+    }
+    __syncwarp();
+    return identity;
+  }
+  if (lane == 0) {
+    agg[tile] = local;
+    __threadfence();
+    st_release(&flag[tile], 1);
+  }
+  T excl = identity;
+  int top = tile - 1;                 // nearest predecessor not yet combined
+  bool timed_out = false;
+  for (;;) {
+    const int t = top - lane;
+    int f = t >= 0 ? ld_acquire(&flag[t]) : 2;
+    int spins = 0;
+    while (__any_sync(0xffffffffu, f == 0)) {
+      if (++spins > spin_limit) { timed_out = true; break; }
+      __nanosleep(64);
+      if (f == 0) f = ld_acquire(&flag[t]);
+    }
+    if (timed_out) {
+      if (lane == 0) set_status(st, ST_TIMEOUT);
+      break;
+    }
+    const unsigned incl = __ballot_sync(0xffffffffu, f == 2);
+    const int first = incl ? __ffs(incl) - 1 : 32;   // nearest inclusive predecessor in this window
+    T v = identity;
+    if (t >= 0 && lane < first) v = ld_cg(&agg[t]);
+    else if (t >= 0 && lane == first) v = ld_cg(&inc[t]);
+    // combine in tile order: higher lanes are earlier tiles
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const T y = shfl_down_t(v, d);
+      if (lane + d < 32) v = op(y, v);
+    }
+    v = shfl_idx_t(v, 0);
+    excl = op(v, excl);
+    if (first < 32) break;
+    top -= 32;
+  }
+  if (lane == 0) {
+    inc[tile] = op(excl, local);
+    __threadfence();
+    st_release(&flag[tile], 2);
+  }
+  __syncwarp();
+  return excl;
+}
 #endif  // __CUDACC__
 
 // Per-call arguments, read by every kernel from device memory (so that a
@@ -291,14 +356,15 @@ struct Work {
   int *cnt_agg, *cnt_inc, *cnt_flag;
   int *ids_agg, *ids_inc, *ids_flag;
   int *counters;                   // [0] pretok tile ticket, [1] ids tile ticket, [2] long list size,
-                                   // [3] pieces, [4] tokens, [5] bad requests seen
+                                   // [3] pieces, [4] tokens, [5] bad requests seen, [6] huge list size
   // pieces and tokens
   int32_t *piece_start;            // [cap_bytes + 2], bit 31 = rejected-request placeholder
   int32_t *n_ids;                  // [cap_bytes + 1]
   int32_t *id_off;                 // [cap_bytes + 2]
   int32_t *scratch;                // [cap_bytes] ids by byte position
-  int32_t *tmp_a, *tmp_b;          // [cap_bytes] long-piece work arrays
-  int32_t *long_list;              // [cap_bytes / (SMALL_MAX + 1) + 2]
+  int32_t *tmp_a, *tmp_b, *tmp_c;  // [cap_bytes] long-piece work arrays
+  int32_t *long_list;              // [cap_bytes / (SMALL_MAX + 1) + 2] pieces > SMALL_MAX bytes
+  int32_t *huge_list;              // [cap_bytes / (MID_MAX + 1) + 2] pieces > MID_MAX bytes
   uint8_t *bad;                    // [cap_reqs]
   int32_t *bad_pre;                // [cap_reqs + 1] (test hook)
   DevStatus *status;

@@ -408,8 +408,11 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
   auto comb = [](const S2 &a, const S2 &b) { return s2_combine(a, b); };
   S2 tile_pub;
   block_exclusive_scan<PT_THREADS>(agg_pub, comb, s2_identity(), P.s2_tmp, &tile_pub);
-  if (tid == 0)
-    P.s2_prefix = lookback(t, tile_pub, comb, s2_identity(), W.s2_agg, W.s2_inc, W.s2_flag, W.status, W.spin_limit);
+  if (tid < 32) {
+    const S2 pre = warp_lookback(t, tile_pub, comb, s2_identity(), W.s2_agg, W.s2_inc, W.s2_flag, W.status,
+                                 W.spin_limit);
+    if (tid == 0) P.s2_prefix = pre;
+  }
   const S2 my_ex = block_exclusive_scan<PT_THREADS>(agg_all, comb, s2_identity(), P.s2_tmp, (S2 *)nullptr);
   S2 before = s2_combine(P.s2_prefix, my_ex);   // (P.s2_prefix visible after the scan's barriers)
 
@@ -490,13 +493,15 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
   int tile_count;
   const int my_off = block_exclusive_scan<PT_THREADS>(__popc(starts), [](int a, int b) { return a + b; }, 0, P.i_tmp,
                                                       &tile_count);
-  if (tid == 0) {
-    P.piece_base = lookback(t, tile_count, [](int a, int b) { return a + b; }, 0, W.cnt_agg, W.cnt_inc, W.cnt_flag,
-                            W.status, W.spin_limit);
-    if (t == ntiles - 1) {
-      const int np = P.piece_base + tile_count;
-      W.counters[3] = np;
-      W.piece_start[np] = (int32_t)total;
+  if (tid < 32) {
+    const int pb = warp_lookback(t, tile_count, [](int a, int b) { return a + b; }, 0, W.cnt_agg, W.cnt_inc,
+                                 W.cnt_flag, W.status, W.spin_limit);
+    if (tid == 0) {
+      P.piece_base = pb;
+      if (t == ntiles - 1) {
+        W.counters[3] = pb + tile_count;
+        W.piece_start[pb + tile_count] = (int32_t)total;
+      }
     }
   }
   __syncthreads();

@@ -139,9 +139,9 @@ tt_status tt_encode_batch(tt_tokenizer *h,
  *                    device memory.  If the batch is larger, nothing is
  *                    written except a zeroed d_out_id_offsets and the device
  *                    status TT_ERR_CAPACITY.
- * Work is launched as one captured CUDA graph per (stream, size bucket) once
- * a bucket has been seen; the first call of a bucket on a stream launches the
- * kernels directly and captures them.
+ * Work is launched as one CUDA graph per (stream, size bucket): the first
+ * call of a bucket captures it (on a private stream), later calls replay it.
+ * d_utf8 and d_out_ids may be NULL only if max_total_bytes is 0.
  */
 tt_status tt_encode_batch_bounded(tt_tokenizer *h,
                                   const uint8_t *d_utf8, const int64_t *d_byte_offsets, int64_t n_requests,
