@@ -404,7 +404,7 @@ extern "C" tt_status tt_encode_batch_bounded(tt_tokenizer *h, const uint8_t *d_u
                                              int64_t *d_out_id_offsets, tt_stream_t stream_) {
   tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, max_total_bytes);
   if (s != TT_OK) return s;
-  if (max_total_bytes < 0 || max_total_bytes >= INT32_MAX - 64) return TT_ERR_CAPACITY;
+  if (max_total_bytes < 0 || max_total_bytes >= S2_MAX_POS - 64) return TT_ERR_CAPACITY;
   cudaStream_t stream = (cudaStream_t)stream_;
   if (n_requests == 0) {
     TT_CUDA(cudaMemsetAsync(d_out_id_offsets, 0, sizeof(int64_t), stream));
@@ -477,7 +477,7 @@ extern "C" tt_status tt_encode_host(tt_tokenizer *h, const uint8_t *utf8, const 
   for (int64_t r = 0; r < n_requests; ++r)
     if (byte_offsets[r] > byte_offsets[r + 1]) return TT_ERR_INVALID_ARG;
   const int64_t total = b1 - b0;
-  if (total >= INT32_MAX - 64) return TT_ERR_CAPACITY;
+  if (total >= S2_MAX_POS - 64) return TT_ERR_CAPACITY;
   cudaStream_t stream = (cudaStream_t)stream_;
   const size_t in_b = ((size_t)total + 16 + 255) & ~(size_t)255;
   const size_t off_b = ((size_t)(n_requests + 1) * 8 + 255) & ~(size_t)255;

@@ -22,9 +22,10 @@
 
 namespace tt {
 
-// whole-piece vocabulary probe; b points to len bytes (any memory space)
+// whole-piece vocabulary probe of len bytes at b (global memory): hash and
+// compare 8 bytes at a time
 __device__ __forceinline__ int vocab_probe(const Tables &T, const uint8_t *b, int len) {
-  const uint64_t h = hash_bytes(b, len);
+  const uint64_t h = hash_global(b, len);
   const uint32_t fp = vocab_fp(h);
   uint32_t s = (uint32_t)h & T.vocab_mask;
   for (;;) {
@@ -34,7 +35,7 @@ __device__ __forceinline__ int vocab_probe(const Tables &T, const uint8_t *b, in
       const int id = (int)(e & 0xFFFFF);
       const uint8_t *v = T.vbytes + __ldg(&T.voff[id]);
       bool same = true;
-      for (int i = 0; i < len && same; ++i) same = __ldg(&v[i]) == b[i];
+      for (int i = 0; i < len && same; i += 8) same = load8(v + i, len - i) == load8(b + i, len - i);
       if (same) return id;
     }
     s = (s + 1) & T.vocab_mask;
@@ -48,7 +49,7 @@ template <int MAXLEN>
 __device__ __forceinline__ int bpe_thread(const Tables &T, const uint8_t *bytes, int len, int32_t *out) {
   int ids[MAXLEN], rk[MAXLEN];
   int n = len;
-  for (int i = 0; i < n; ++i) ids[i] = __ldg(&T.byte_id[bytes[i]]);
+  for (int i = 0; i < n; ++i) ids[i] = __ldg(&T.byte_id[__ldg(bytes + i)]);
   for (int i = 0; i + 1 < n; ++i) rk[i] = pair_rank(T, ids[i], ids[i + 1]);
   for (;;) {
     int r = INT_MAX;
@@ -96,14 +97,12 @@ __global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work 
       W.long_list[atomicAdd(&W.counters[2], 1)] = k;
       continue;
     }
-    uint8_t buf[SMALL_MAX];
-    for (int i = 0; i < len; ++i) buf[i] = __ldg(g + s + i);
     int32_t *out = W.scratch + s;
     if (len <= T.max_tok_len) {
-      const int id = vocab_probe(T, buf, len);
+      const int id = vocab_probe(T, g + s, len);
       if (id >= 0) { out[0] = id; W.n_ids[k] = 1; continue; }
     }
-    W.n_ids[k] = bpe_thread<SMALL_MAX>(T, buf, len, out);
+    W.n_ids[k] = bpe_thread<SMALL_MAX>(T, g + s, len, out);
   }
 }
 

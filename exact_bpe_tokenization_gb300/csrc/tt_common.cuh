@@ -102,6 +102,28 @@ __device__ __forceinline__ int pair_rank(const Tables &T, int l, int r) {
   }
 }
 
+// 8 bytes starting at p, little-endian, bytes at or past `avail` zeroed
+// (avail >= 1).  Reads only the 8-byte-aligned words that hold a byte of
+// [p, p + min(avail, 8)); such a word never crosses a page, so no read can
+// fault even at the very end of a buffer.
+__device__ __forceinline__ uint64_t load8(const uint8_t *p, int avail) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uint64_t *q = reinterpret_cast<const uint64_t *>(a & ~(uintptr_t)7);
+  const int off = (int)(a & 7);
+  uint64_t v = __ldg(q) >> (8 * off);
+  if (off && avail > 8 - off) v |= __ldg(q + 1) << (64 - 8 * off);
+  if (avail < 8) v &= (1ull << (8 * avail)) - 1;
+  return v;
+}
+
+// hash_bytes() of len bytes at p (global memory), from 8-byte loads
+__device__ __forceinline__ uint64_t hash_global(const uint8_t *p, int len) {
+  ByteHash bh;
+  bh.init(len);
+  for (int i = 0; i < len; i += 8) bh.word(load8(p + i, len - i));
+  return bh.fin();
+}
+
 // ------------------------------------------------------------ memory order
 __device__ __forceinline__ int ld_acquire(const int *p) {
   int v;

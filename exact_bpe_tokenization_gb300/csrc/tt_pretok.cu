@@ -297,7 +297,8 @@ __global__ void __launch_bounds__(1024) k_tilescan(Tables T, Work W) {
 struct PretokSmem {
   WinSmem w;
   uint8_t chain[WIN];
-  uint16_t aggs[WIN];
+  uint8_t rq8[WIN];          // reverse-query results per tile char: rq_ws | rq_up << 2
+  uint16_t dagg[PT_THREADS][3];  // scan values of chars whose predicate waits for the barrier
   S2 s2_tmp[PT_THREADS / 32];
   int2 i2_tmp[PT_THREADS / 32];
   int i_tmp[PT_THREADS / 32];
@@ -391,6 +392,35 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
   }
   __syncthreads();
 
+  // --- reverse queries over the tile's chars: first event strictly after j
+  auto first = [](int a, int b) {
+    const int lo = (a & 0xFF) != 0xFF ? (a & 0xFF) : (b & 0xFF);
+    const int hi = (a >> 8) != 0xFF ? (a >> 8) : (b >> 8);
+    return lo | (hi << 8);
+  };
+  {
+    int rq_first = 0xFFFF;
+    for (int j = c0; j < c1; ++j) {
+      const int64_t pos = ws + S.lead[j];
+      if (pos < ts || pos >= te) continue;
+      const uint8_t ew = rq_ws_event(S.rs[j], S.raw[j], S.cp8[j]);
+      const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
+      if ((rq_first & 0xFF) == 0xFF && ew != 0xFF) rq_first = (rq_first & 0xFF00) | ew;
+      if ((rq_first >> 8) == 0xFF && eu != 0xFF) rq_first = (rq_first & 0x00FF) | (eu << 8);
+    }
+    int after = first(block_exclusive_suffix<PT_THREADS>(rq_first, first, 0xFFFF, P.i_tmp, (int *)nullptr),
+                      W.rq_carry[2 * t] | (W.rq_carry[2 * t + 1] << 8));
+    for (int j = c1 - 1; j >= c0; --j) {
+      const int64_t pos = ws + S.lead[j];
+      if (pos < ts || pos >= te) continue;
+      P.rq8[j] = (uint8_t)((after & 0x3) | (((after >> 8) & 0x3) << 2));
+      const uint8_t ew = rq_ws_event(S.rs[j], S.raw[j], S.cp8[j]);
+      const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
+      if (ew != 0xFF) after = (after & 0xFF00) | ew;
+      if (eu != 0xFF) after = (after & 0x00FF) | (eu << 8);
+    }
+  }
+
   // --- forward scan (scan 2) over chars with pos in [ts - 16, te); the
   // published aggregate covers the shifted tile [ts - 16, te - 16)
   const int64_t s2_lo = ts - S2_SHIFT, s2_pub_hi = te - S2_SHIFT;
@@ -399,9 +429,9 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
     const int64_t pos = ws + S.lead[j];
     if (pos < s2_lo || pos >= te) continue;
     const Nbr nb = make_nbr(S, nullptr, j);
-    const int64_t p1 = j + 1 < S.nch ? ws + S.lead[j + 1] : pos + 1;
-    const int64_t p2 = j + 2 < S.nch ? ws + S.lead[j + 2] : pos + 2;
-    const S2 el = s2_element(fam, nb, pos, p1, p2);
+    const int32_t p1 = (int32_t)(j + 1 < S.nch ? ws + S.lead[j + 1] : pos + 1);
+    const int32_t p2 = (int32_t)(j + 2 < S.nch ? ws + S.lead[j + 2] : pos + 2);
+    const S2 el = s2_element(fam, nb, (int32_t)pos, p1, p2);
     agg_all = s2_combine(agg_all, el);
     if (t == ntiles - 1 || pos < s2_pub_hi) agg_pub = s2_combine(agg_pub, el);
   }
@@ -416,70 +446,12 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
   const S2 my_ex = block_exclusive_scan<PT_THREADS>(agg_all, comb, s2_identity(), P.s2_tmp, (S2 *)nullptr);
   S2 before = s2_combine(P.s2_prefix, my_ex);   // (P.s2_prefix visible after the scan's barriers)
 
-  // --- reverse queries over the tile's chars: first event strictly after j
-  int rq_first = 0xFFFF;
-  for (int j = c0; j < c1; ++j) {
-    const int64_t pos = ws + S.lead[j];
-    if (pos < ts || pos >= te) continue;
-    const uint8_t ew = rq_ws_event(S.rs[j], S.raw[j], S.cp8[j]);
-    const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
-    if ((rq_first & 0xFF) == 0xFF && ew != 0xFF) rq_first = (rq_first & 0xFF00) | ew;
-    if ((rq_first >> 8) == 0xFF && eu != 0xFF) rq_first = (rq_first & 0x00FF) | (eu << 8);
-  }
-  auto first = [](int a, int b) {
-    const int lo = (a & 0xFF) != 0xFF ? (a & 0xFF) : (b & 0xFF);
-    const int hi = (a >> 8) != 0xFF ? (a >> 8) : (b >> 8);
-    return lo | (hi << 8);
-  };
-  const int rq_after_me = first(block_exclusive_suffix<PT_THREADS>(rq_first, first, 0xFFFF, P.i_tmp, (int *)nullptr),
-                                W.rq_carry[2 * t] | (W.rq_carry[2 * t + 1] << 8));
-
-  // --- walk 1: per-char scan values (forward), chain states
-  for (int j = c0; j < c1; ++j) {
-    const int64_t pos = ws + S.lead[j];
-    if (pos < s2_lo || pos >= te) { P.chain[j] = 1; continue; }
-    const Nbr nb = make_nbr(S, nullptr, j);
-    const int64_t p1 = j + 1 < S.nch ? ws + S.lead[j + 1] : pos + 1;
-    const int64_t p2 = j + 2 < S.nch ? ws + S.lead[j + 2] : pos + 2;
-    const S2 el = s2_element(fam, nb, pos, p1, p2);
-    Aggs a;
-    bool ch;
-    s2_values(before, el, pos, a, ch);
-    before = s2_combine(before, el);
-    P.chain[j] = ch ? 1 : 0;
-    P.aggs[j] = (uint16_t)(a.nidx3 | (a.w_start << 2) | (a.w_prev_other << 3) | (a.w_ncw_before << 4) | (a.case_prev << 5));
-  }
-  // backward over my chars: reverse-query values
-  {
-    int after = rq_after_me;
-    for (int j = c1 - 1; j >= c0; --j) {
-      const int64_t pos = ws + S.lead[j];
-      if (pos < ts || pos >= te) continue;
-      P.aggs[j] |= (uint16_t)(((after & 0xFF) << 7) | (((after >> 8) & 0x3) << 9));
-      const uint8_t ew = rq_ws_event(S.rs[j], S.raw[j], S.cp8[j]);
-      const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
-      if (ew != 0xFF) after = (after & 0xFF00) | ew;
-      if (eu != 0xFF) after = (after & 0x00FF) | (eu << 8);
-    }
-  }
-  __syncthreads();
-
-  // --- walk 2: the predicate, then compaction of piece starts
-  uint32_t starts = 0, placeholder = 0;   // bit (j - c0) for my chars (<= 16)
+  // --- walk: per-char scan values and the predicate.  o200k chars whose
+  // contraction lookback reaches the previous thread's chars wait for the
+  // barrier (their chain states are written by that thread in this walk).
+  uint32_t starts = 0, placeholder = 0, deferred = 0;   // bit (j - c0) for my chars (<= 16)
   const bool filter = __ldcg(&W.counters[5]) != 0;
-  for (int j = c0; j < c1; ++j) {
-    const int64_t pos = ws + S.lead[j];
-    if (pos < ts || pos >= te) continue;
-    const Nbr nb = make_nbr(S, P.chain, j);
-    const uint16_t g = P.aggs[j];
-    Aggs a;
-    a.nidx3 = g & 3;
-    a.w_start = (g >> 2) & 1;
-    a.w_prev_other = (g >> 3) & 1;
-    a.w_ncw_before = (g >> 4) & 1;
-    a.case_prev = (g >> 5) & 3;
-    a.rq_ws = (g >> 7) & 3;
-    a.rq_up = (g >> 9) & 3;
+  auto decide = [&](int j, const Nbr &nb, const Aggs &a, int64_t pos) {
     bool st = piece_start(fam, nb, a);
     if (st && filter) {
       const int64_t r = lower_bound64(A.offs, A.n + 1, base + pos + 1) - 1;
@@ -489,6 +461,48 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
       }
     }
     if (st) starts |= 1u << (j - c0);
+  };
+  for (int j = c0; j < c1; ++j) {
+    const int64_t pos = ws + S.lead[j];
+    if (pos < s2_lo || pos >= te) { P.chain[j] = 1; continue; }
+    Nbr nb = make_nbr(S, P.chain, j);
+    const int32_t p1 = (int32_t)(j + 1 < S.nch ? ws + S.lead[j + 1] : pos + 1);
+    const int32_t p2 = (int32_t)(j + 2 < S.nch ? ws + S.lead[j + 2] : pos + 2);
+    const S2 el = s2_element(fam, nb, (int32_t)pos, p1, p2);
+    Aggs a;
+    bool ch;
+    s2_values(before, el, (int32_t)pos, a, ch);
+    before = s2_combine(before, el);
+    P.chain[j] = ch ? 1 : 0;
+    if (pos < ts) continue;
+    const uint8_t q = P.rq8[j];
+    a.rq_ws = q & 3;
+    a.rq_up = (q >> 2) & 3;
+    // (chain states are read only next to an apostrophe: c0 with l1, c2 with l2, c3 with l3)
+    if (fam == FAM_O200K && j < c0 + 3 &&
+        (nb.c0 == '\'' || nb.c1 == '\'' || nb.c2 == '\'' || nb.c3 == '\'')) {
+      deferred |= 1u << (j - c0);
+      P.dagg[tid][j - c0] = (uint16_t)(a.nidx3 | (a.w_start << 2) | (a.w_prev_other << 3) | (a.w_ncw_before << 4) |
+                             (a.case_prev << 5) | (a.rq_ws << 7) | (a.rq_up << 9));
+      continue;
+    }
+    decide(j, nb, a, pos);
+  }
+  __syncthreads();
+  for (uint32_t m = deferred; m; m &= m - 1) {
+    const int j = c0 + __ffs(m) - 1;
+    const int64_t pos = ws + S.lead[j];
+    const Nbr nb = make_nbr(S, P.chain, j);
+    const uint16_t g = P.dagg[tid][j - c0];
+    Aggs a;
+    a.nidx3 = g & 3;
+    a.w_start = (g >> 2) & 1;
+    a.w_prev_other = (g >> 3) & 1;
+    a.w_ncw_before = (g >> 4) & 1;
+    a.case_prev = (g >> 5) & 3;
+    a.rq_ws = (g >> 7) & 3;
+    a.rq_up = (g >> 9) & 3;
+    decide(j, nb, a, pos);
   }
   int tile_count;
   const int my_off = block_exclusive_scan<PT_THREADS>(__popc(starts), [](int a, int b) { return a + b; }, 0, P.i_tmp,

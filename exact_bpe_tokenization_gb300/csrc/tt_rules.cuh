@@ -218,38 +218,39 @@ TT_HD uint8_t chain_event(int fam, const Nbr &n) {
 // A char's element depends only on the state just before it, so prefixes
 // compose: combine(a, b) = "a, then b".
 struct S2 {
-  int64_t wst, ncw;        // max-scans, -1 = none
-  int64_t case0, case1;    // case max given chain bit false / true on entry
+  int32_t wst, ncw;        // max-scans, -1 = none
+  int32_t case0, case1;    // case max given chain bit false / true on entry
   uint8_t nflag, ncount;   // number runs: a reset happened; count since it (mod 3)
   uint8_t chain, pad;      // chain function (CH_*)
-  uint32_t pad2;
 };
+// Positions are byte offsets below 2^29, so pos * 4 + type fits an int32.
+constexpr int64_t S2_MAX_POS = (int64_t)1 << 29;
 
 TT_HD S2 s2_identity() {
   S2 r;
   r.wst = r.ncw = r.case0 = r.case1 = -1;
   r.nflag = r.ncount = 0;
   r.chain = CH_ID;
-  r.pad = 0; r.pad2 = 0;
+  r.pad = 0;
   return r;
 }
-TT_HD int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+TT_HD int32_t max32(int32_t a, int32_t b) { return a > b ? a : b; }
 TT_HD S2 s2_combine(const S2 &a, const S2 &b) {
   S2 r;
   r.nflag = a.nflag | b.nflag;
   r.ncount = b.nflag ? b.ncount : (uint8_t)((a.ncount + b.ncount) % 3);
-  r.wst = max64(a.wst, b.wst);
-  r.ncw = max64(a.ncw, b.ncw);
+  r.wst = max32(a.wst, b.wst);
+  r.ncw = max32(a.ncw, b.ncw);
   r.chain = chain_then(a.chain, b.chain);
-  r.case0 = max64(a.case0, chain_apply(a.chain, false) ? b.case1 : b.case0);
-  r.case1 = max64(a.case1, chain_apply(a.chain, true) ? b.case1 : b.case0);
-  r.pad = 0; r.pad2 = 0;
+  r.case0 = max32(a.case0, chain_apply(a.chain, false) ? b.case1 : b.case0);
+  r.case1 = max32(a.case1, chain_apply(a.chain, true) ? b.case1 : b.case0);
+  r.pad = 0;
   return r;
 }
 
 // The element of char i.  pos: byte position of i; pos1 / pos2: byte
 // positions of chars i+1 / i+2 (used only when they exist).
-TT_HD S2 s2_element(int fam, const Nbr &n, int64_t pos, int64_t pos1, int64_t pos2) {
+TT_HD S2 s2_element(int fam, const Nbr &n, int32_t pos, int32_t pos1, int32_t pos2) {
   S2 r = s2_identity();
   if (n.e0 == K_NUM) {
     r.nflag = n.e1 != K_NUM;
@@ -262,7 +263,7 @@ TT_HD S2 s2_element(int fam, const Nbr &n, int64_t pos, int64_t pos1, int64_t po
   if (fam == FAM_O200K && is_letter(n.e0)) {
     const bool run_start = !is_letter(n.e1);
     const int t = n.e0 == K_LU ? 1 : n.e0 == K_LL ? 2 : 0;
-    const int64_t ev = (run_start || t) ? pos * 4 + t : -1;
+    const int32_t ev = (run_start || t) ? pos * 4 + t : -1;
     r.case0 = r.case1 = ev;
     if (run_start) {
       r.chain = CH_TRUE;
@@ -275,7 +276,7 @@ TT_HD S2 s2_element(int fam, const Nbr &n, int64_t pos, int64_t pos1, int64_t po
           // if the apostrophe is swallowed (chain bit true), a new segment
           // starts after the contraction letters
           const int tk = ek == K_LU ? 1 : ek == K_LL ? 2 : 0;
-          r.case1 = max64(ev, (k == 1 ? pos1 : pos2) * 4 + tk);
+          r.case1 = max32(ev, (k == 1 ? pos1 : pos2) * 4 + tk);
         }
       }
     }
@@ -285,14 +286,14 @@ TT_HD S2 s2_element(int fam, const Nbr &n, int64_t pos, int64_t pos1, int64_t po
 
 // Per-char aggregates from the state before char i and i's element.  The
 // chain bit is true before the first char of the batch.
-TT_HD void s2_values(const S2 &before, const S2 &elem, int64_t pos, Aggs &a, bool &chain_after) {
+TT_HD void s2_values(const S2 &before, const S2 &elem, int32_t pos, Aggs &a, bool &chain_after) {
   const S2 after = s2_combine(before, elem);
   a.nidx3 = (after.ncount + 2) % 3;
-  const int64_t s = after.wst >> 1;
+  const int32_t s = after.wst >> 1;
   a.w_start = s == pos;
   a.w_prev_other = (after.wst & 1) != 0;
   a.w_ncw_before = before.ncw >= s;
-  const int64_t ce = before.case1;                 // exclusive, chain bit true on entry
+  const int32_t ce = before.case1;                 // exclusive, chain bit true on entry
   a.case_prev = ce >= 0 ? (int)(ce & 3) : 0;
   chain_after = chain_apply(after.chain, true) != 0;
 }

@@ -24,8 +24,9 @@
  *   - A batch is `n_requests` UTF-8 byte strings stored back to back:
  *     request r is bytes [byte_offsets[r], byte_offsets[r+1]) of the byte
  *     buffer.  byte_offsets has n_requests + 1 non-decreasing entries, the
- *     first >= 0.  Empty requests are allowed.  byte_offsets[n] -
- *     byte_offsets[0] must be < 2^31.
+ *     first >= 0.  Empty requests are allowed.  A batch holds fewer than
+ *     2^29 - 64 bytes (byte_offsets[n] - byte_offsets[0]); larger batches are
+ *     rejected with TT_ERR_CAPACITY.
  *   - Output IDs are int32, concatenated per request: request r owns
  *     out_ids[out_id_offsets[r] - out_id_offsets[0] ...).  out_id_offsets is
  *     int64 with n_requests + 1 entries and out_id_offsets[0] = 0.  A request

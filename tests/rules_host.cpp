@@ -64,10 +64,10 @@ extern "C" void rules_host_starts(int fam, const uint32_t *cp, const uint8_t *ra
   S2 before = s2_identity();
   for (int64_t j = 0; j < n; ++j) {
     Nbr b = nbr(j);
-    S2 el = s2_element(fam, b, j, j + 1, j + 2);
+    S2 el = s2_element(fam, b, (int32_t)j, (int32_t)(j + 1), (int32_t)(j + 2));
     Aggs a;
     bool ch;
-    s2_values(before, el, j, a, ch);
+    s2_values(before, el, (int32_t)j, a, ch);
     chain[j] = ch;
     before = s2_combine(before, el);
     a.rq_ws = rq_ws[j];
