@@ -19,6 +19,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "toktier.h")
 TT_OK, TT_ERR_INVALID_ARG, TT_ERR_BAD_VOCAB, TT_ERR_BAD_FAMILY, TT_ERR_INVALID_UTF8, \
     TT_ERR_CAPACITY, TT_ERR_OOM, TT_ERR_CUDA, TT_ERR_TIMEOUT = range(9)
 TT_FAMILY_CL100K_STYLE, TT_FAMILY_O200K_STYLE = 1, 2
+TT_NOALLOC_MAX_BYTES, TT_NOALLOC_MAX_REQUESTS = 256 * 1024, 1024
 
 _lib = None
 _lock = threading.Lock()
@@ -44,6 +45,7 @@ def lib():
             L.tt_destroy.argtypes = [p]
             L.tt_encode_batch.argtypes = [p, p, p, i64, p, p, p]
             L.tt_encode_batch_bounded.argtypes = [p, p, p, i64, i64, p, p, p]
+            L.tt_encode_batch_noalloc.argtypes = [p, p, p, i64, i64, p, p, p]
             L.tt_encode_host.argtypes = [p, p, p, i64, p, i64, p, p]
             L.tt_get_status.argtypes = [p, p, ctypes.POINTER(i64)]
             L.tt_pretokenize_batch.argtypes = [p, p, p, i64, p, p, p]
@@ -55,7 +57,8 @@ def lib():
             L.tt_launch_count.argtypes = [p]
             L.tt_launch_count.restype = i64
             L.tt_table_digest.restype = ctypes.c_char_p
-            for name in ("tt_create", "tt_encode_batch", "tt_encode_batch_bounded", "tt_encode_host",
+            for name in ("tt_create", "tt_encode_batch", "tt_encode_batch_bounded", "tt_encode_batch_noalloc",
+                         "tt_encode_host",
                          "tt_get_status", "tt_pretokenize_batch", "tt_profile_read"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -125,6 +128,15 @@ def tt_encode_batch_bounded(h, d_utf8, d_byte_offsets, n_requests, max_total_byt
     _check(lib().tt_encode_batch_bounded(h, _ptr(d_utf8), _ptr(d_byte_offsets), int(n_requests),
                                          int(max_total_bytes), _ptr(d_out_ids), _ptr(d_out_id_offsets),
                                          _stream(stream)), "tt_encode_batch_bounded")
+
+
+def tt_encode_batch_noalloc(h, d_utf8, d_byte_offsets, n_requests, max_total_bytes, d_out_ids, d_out_id_offsets,
+                            stream=None):
+    """As tt_encode_batch_bounded, with the library's fixed scratch: no device
+    allocation, batches up to TT_NOALLOC_MAX_BYTES / TT_NOALLOC_MAX_REQUESTS."""
+    _check(lib().tt_encode_batch_noalloc(h, _ptr(d_utf8), _ptr(d_byte_offsets), int(n_requests),
+                                         int(max_total_bytes), _ptr(d_out_ids), _ptr(d_out_id_offsets),
+                                         _stream(stream)), "tt_encode_batch_noalloc")
 
 
 def tt_encode_host(h, utf8, byte_offsets, out_ids, out_id_offsets, stream=None):

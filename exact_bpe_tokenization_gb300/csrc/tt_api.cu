@@ -600,3 +600,135 @@ extern "C" int tt_profile_read(tt_tokenizer *h, const char **names, double *ms, 
 extern "C" int64_t tt_launch_count(tt_tokenizer *h) { return h ? h->launches.load() : 0; }
 
 extern "C" const char *tt_table_digest(void) { return TT_CLASS_DIGEST; }
+
+// ===================================================================
+// tt_encode_batch_noalloc: the same kernels as tt_encode_batch_bounded,
+// with their scratch carved from one array compiled into the library
+// instead of a workspace allocated on demand.  For callers that cannot
+// allocate device memory once they are running.
+namespace {
+
+constexpr int64_t NA_BYTES = TT_NOALLOC_MAX_BYTES;
+constexpr int64_t NA_REQS = TT_NOALLOC_MAX_REQUESTS;
+constexpr int64_t NA_TILES = (NA_BYTES + TILE - 1) / TILE + 1;
+constexpr int64_t NA_CHUNKS = (NA_BYTES + 1 + IDS_CHUNK - 1) / IDS_CHUNK + 2;
+constexpr size_t na_round(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// sizes of the scratch arrays, in the order they are carved
+constexpr size_t NA_SIZES[] = {
+    sizeof(int2) * NA_TILES, sizeof(int2) * NA_TILES,                 // s1_sum, s1_carry
+    2 * (size_t)NA_TILES, 2 * (size_t)NA_TILES,                        // rq_sum, rq_carry
+    sizeof(S2) * NA_TILES, sizeof(S2) * NA_TILES, 4 * (size_t)NA_TILES, // s2_agg, s2_inc, s2_flag
+    4 * (size_t)NA_TILES, 4 * (size_t)NA_TILES, 4 * (size_t)NA_TILES,  // cnt_agg, cnt_inc, cnt_flag
+    4 * (size_t)NA_CHUNKS, 4 * (size_t)NA_CHUNKS, 4 * (size_t)NA_CHUNKS, // ids_agg, ids_inc, ids_flag
+    4 * 16,                                                            // counters
+    4 * (size_t)(NA_BYTES + 2), 4 * (size_t)(NA_BYTES + 1),            // piece_start, n_ids
+    4 * (size_t)(NA_BYTES + 2), 4 * (size_t)(NA_BYTES + 1),            // id_off, scratch
+    4 * (size_t)(NA_BYTES + 1), 4 * (size_t)(NA_BYTES + 1), 4 * (size_t)(NA_BYTES + 1),  // tmp_a, tmp_b, tmp_c
+    4 * (size_t)(NA_BYTES / (SMALL_MAX + 1) + 2), 4 * (size_t)(NA_BYTES / (MID_MAX + 1) + 2),  // lists
+    (size_t)NA_REQS + 1, 4 * (size_t)(NA_REQS + 2),                    // bad, bad_pre
+    sizeof(CallArgs),                                                  // args
+};
+constexpr size_t na_total() {
+  size_t t = 0;
+  for (size_t s : NA_SIZES) t += na_round(s);
+  return t;
+}
+
+}  // namespace
+
+// The fixed scratch.  In host code this name is only a stand-in for the
+// device array: its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char tt_noalloc_scratch[na_total()];
+
+// writes the per-call arguments into the scratch (no host staging buffer)
+static __global__ void k_noalloc_args(CallArgs a, CallArgs *dst) { *dst = a; }
+
+// Device address of the scratch on the current device, looked up once per
+// device (the first call on a device should precede any stream capture).
+static tt_status noalloc_scratch_address(int dev, unsigned char **out) {
+  static std::mutex mu;
+  static std::map<int, unsigned char *> addr;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = addr.find(dev);
+  if (it == addr.end()) {
+    unsigned char *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress((void **)&p, tt_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      fprintf(stderr, "toktier: cudaGetSymbolAddress failed: %s\n", cudaGetErrorString(e));
+      return TT_ERR_CUDA;
+    }
+    it = addr.emplace(dev, p).first;
+  }
+  *out = it->second;
+  return TT_OK;
+}
+
+extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
+                                             int64_t n_requests, int64_t max_total_bytes, int32_t *d_out_ids,
+                                             int64_t *d_out_id_offsets, tt_stream_t stream_) {
+  if (!h || n_requests < 0 || !d_byte_offsets || !d_out_id_offsets || max_total_bytes < 0) return TT_ERR_INVALID_ARG;
+  if (max_total_bytes > NA_BYTES || n_requests > NA_REQS) {
+    fprintf(stderr, "toktier: tt_encode_batch_noalloc: batch of up to %lld bytes / %lld requests exceeds the fixed "
+            "scratch (%d bytes, %d requests)\n", (long long)max_total_bytes, (long long)n_requests,
+            TT_NOALLOC_MAX_BYTES, TT_NOALLOC_MAX_REQUESTS);
+    return TT_ERR_CAPACITY;
+  }
+  if (n_requests > 0 && max_total_bytes > 0 && (!d_utf8 || !d_out_ids)) return TT_ERR_INVALID_ARG;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  int dev = -1;
+  TT_CUDA(cudaGetDevice(&dev));
+  if (dev != h->device) return TT_ERR_INVALID_ARG;
+  if (n_requests == 0) {
+    TT_CUDA(cudaMemsetAsync(d_out_id_offsets, 0, sizeof(int64_t), stream));
+    return TT_OK;
+  }
+  unsigned char *base = nullptr;
+  tt_status s = noalloc_scratch_address(dev, &base);
+  if (s != TT_OK) return s;
+  Work W{};
+  void **dst[] = {(void **)&W.s1_sum,  (void **)&W.s1_carry, (void **)&W.rq_sum,   (void **)&W.rq_carry,
+                  (void **)&W.s2_agg,  (void **)&W.s2_inc,   (void **)&W.s2_flag,  (void **)&W.cnt_agg,
+                  (void **)&W.cnt_inc, (void **)&W.cnt_flag, (void **)&W.ids_agg,  (void **)&W.ids_inc,
+                  (void **)&W.ids_flag, (void **)&W.counters, (void **)&W.piece_start, (void **)&W.n_ids,
+                  (void **)&W.id_off,  (void **)&W.scratch,  (void **)&W.tmp_a,    (void **)&W.tmp_b,
+                  (void **)&W.tmp_c,   (void **)&W.long_list, (void **)&W.huge_list, (void **)&W.bad,
+                  (void **)&W.bad_pre, (void **)&W.args};
+  static_assert(sizeof(dst) / sizeof(dst[0]) == sizeof(NA_SIZES) / sizeof(NA_SIZES[0]), "layout");
+  size_t off = 0;
+  for (size_t i = 0; i < sizeof(NA_SIZES) / sizeof(NA_SIZES[0]); ++i) {
+    *dst[i] = base + off;
+    off += na_round(NA_SIZES[i]);
+  }
+  W.cap_bytes = NA_BYTES;
+  W.cap_reqs = NA_REQS;
+  W.cap_tiles = (int32_t)NA_TILES;
+  W.spin_limit = 1 << 22;
+  W.status = h->d_status;
+  const CallArgs args = {d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, nullptr, nullptr};
+  k_noalloc_args<<<1, 1, 0, stream>>>(args, W.args);
+  // what must start at zero: the counters and the rejected-request flags
+  // (look-back flags are reset by k_tilescan)
+  TT_CUDA(cudaMemsetAsync(W.counters, 0, 4 * 16, stream));
+  TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)NA_REQS + 1, stream));
+  const Tables &T = h->T;
+  const int g_tiles = (int)((NA_BYTES + TILE - 1) / TILE);
+  const int g_small = (int)std::min<int64_t>(std::max<int64_t>((NA_BYTES / 4 + BPE_SMALL_THREADS - 1) / BPE_SMALL_THREADS, 1),
+                                             152 * 8);
+  const int g_mid = (int)std::min<int64_t>(
+      std::max<int64_t>((NA_BYTES / (SMALL_MAX + 1) + (BPE_MID_THREADS / 32) - 1) / (BPE_MID_THREADS / 32), 1), 152 * 8);
+  const int g_long = (int)std::min<int64_t>(std::max<int64_t>(NA_BYTES / (MID_MAX + 1), 1), 152 * 2);
+  const int g_chunks = (int)((NA_BYTES + 1 + IDS_CHUNK - 1) / IDS_CHUNK);
+  const int g_reqs = (int)((NA_REQS + 1 + 255) / 256);
+  launch_prepass(T, W, g_tiles, stream);
+  launch_tilescan(T, W, stream);
+  launch_pretok(T, W, g_tiles, stream);
+  launch_bpe_small(T, W, g_small, stream);
+  launch_bpe_mid(T, W, g_mid, stream);
+  launch_bpe_long(T, W, g_long, stream);
+  launch_ids(T, W, g_chunks, stream);
+  launch_req(T, W, g_reqs, stream);
+  TT_CUDA(cudaGetLastError());
+  h->launches += N_KERNELS;
+  return TT_OK;
+}

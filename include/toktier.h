@@ -150,6 +150,40 @@ tt_status tt_encode_batch_bounded(tt_tokenizer *h,
                                   int32_t *d_out_ids, int64_t *d_out_id_offsets, tt_stream_t stream);
 
 /*
+ * tt_encode_batch_noalloc - tokenize a small device batch without allocating.
+ *
+ * The paper has no counterpart: this exists for callers that must not
+ * allocate device memory while they run, e.g. code inside a fixed memory
+ * budget or a custom allocator that forbids cudaMalloc/cudaFree after
+ * start-up, or latency-critical paths where an allocation would
+ * synchronise the device.  tt_encode_batch_bounded may allocate a
+ * per-stream workspace on first use or when a batch outgrows it; this entry
+ * point never does: its scratch is one fixed array compiled into the
+ * library (about 7.4 MB, held on every device that loads the library until
+ * the process exits).
+ *
+ *   Arguments and outputs as tt_encode_batch_bounded; the limits are
+ *   max_total_bytes <= TT_NOALLOC_MAX_BYTES and
+ *   n_requests <= TT_NOALLOC_MAX_REQUESTS.  Larger values are rejected with
+ *   TT_ERR_CAPACITY before anything is enqueued (a batch whose true size
+ *   exceeds the stated bound is caught on the device as in the bounded
+ *   call).  The current device must be the handle's.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call on a device shares the one array and leaves its contents
+ * behind (each call clears what must start at zero), so calls that overlap
+ * on the GPU race: serialise them, e.g. issue them on one stream.  The
+ * handle's status word is shared with the other entry points.
+ */
+#define TT_NOALLOC_MAX_BYTES (256 * 1024)
+#define TT_NOALLOC_MAX_REQUESTS 1024
+tt_status tt_encode_batch_noalloc(tt_tokenizer *h,
+                                  const uint8_t *d_utf8, const int64_t *d_byte_offsets, int64_t n_requests,
+                                  int64_t max_total_bytes,
+                                  int32_t *d_out_ids, int64_t *d_out_id_offsets, tt_stream_t stream);
+
+/*
  * tt_encode_host - tokenize a batch held in HOST memory (synchronous).
  *
  *   utf8, byte_offsets  host; the batch (byte_offsets[0] may be > 0).
