@@ -42,6 +42,8 @@ struct Workspace {
   int64_t cap_bytes = 0, cap_reqs = 0;
   cudaGraphExec_t graph = nullptr;
   cudaStream_t cap_stream = nullptr;   // private stream the graph is captured on
+  cudaStream_t side = nullptr;         // second branch: long-piece BPE beside the short pieces
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // device staging for tt_encode_host (bytes, offsets, ids, id offsets)
   void *stage = nullptr;
   size_t stage_bytes = 0;
@@ -250,6 +252,9 @@ static void free_workspace(Workspace *w) {
   if (!w) return;
   if (w->graph) cudaGraphExecDestroy(w->graph);
   if (w->cap_stream) cudaStreamDestroy(w->cap_stream);
+  if (w->side) cudaStreamDestroy(w->side);
+  if (w->ev_fork) cudaEventDestroy(w->ev_fork);
+  if (w->ev_join) cudaEventDestroy(w->ev_join);
   if (w->mem) cudaFree(w->mem);
   if (w->stage) cudaFree(w->stage);
   delete w;
@@ -278,8 +283,8 @@ static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_
       {(void **)&W.s1_sum, sizeof(int2) * tiles},       {(void **)&W.s1_carry, sizeof(int2) * tiles},
       {(void **)&W.rq_sum, 2 * (size_t)tiles},          {(void **)&W.rq_carry, 2 * (size_t)tiles},
       {(void **)&W.s2_agg, sizeof(S2) * tiles},         {(void **)&W.s2_inc, sizeof(S2) * tiles},
-      {(void **)&W.s2_flag, 4 * (size_t)tiles},         {(void **)&W.cnt_agg, 4 * (size_t)tiles},
-      {(void **)&W.cnt_inc, 4 * (size_t)tiles},         {(void **)&W.cnt_flag, 4 * (size_t)tiles},
+      {(void **)&W.s2_flag, 4 * (size_t)tiles},         {(void **)&W.cnt_agg, sizeof(int2) * tiles},
+      {(void **)&W.cnt_inc, sizeof(int2) * tiles},      {(void **)&W.cnt_flag, 4 * (size_t)tiles},
       {(void **)&W.ids_agg, 4 * (size_t)chunks},        {(void **)&W.ids_inc, 4 * (size_t)chunks},
       {(void **)&W.ids_flag, 4 * (size_t)chunks},       {(void **)&W.counters, 4 * 16},
       {(void **)&W.piece_start, 4 * (size_t)(cap_bytes + 2)}, {(void **)&W.n_ids, 4 * (size_t)(cap_bytes + 1)},
@@ -364,15 +369,39 @@ static int grid_long(const Workspace *w) {
   return (int)std::min<int64_t>(std::max<int64_t>(w->cap_bytes / (MID_MAX + 1), 1), 152 * 2);
 }
 
-// Enqueue the kernels of one encode on `stream` (eager; optionally timed).
+// Enqueue the kernels of one encode on `stream`.  Untimed, the BPE of the
+// listed long pieces (k_bpe_mid, k_bpe_long) runs on a second stream beside
+// the short pieces (k_bpe_small), forked after k_pretok and joined before
+// k_ids; under capture this becomes two parallel graph branches.  Timed
+// (profiling), every kernel runs in turn on `stream` between events.
 static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stream, bool timed) {
   const Tables &T = h->T;
   const Work &W = w->W;
   TT_CUDA(cudaMemsetAsync(W.counters, 0, 4 * 16, stream));
   TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)w->cap_reqs + 1, stream));
+  if (!timed) {
+    if (!w->side) TT_CUDA(cudaStreamCreateWithFlags(&w->side, cudaStreamNonBlocking));
+    if (!w->ev_fork) TT_CUDA(cudaEventCreateWithFlags(&w->ev_fork, cudaEventDisableTiming));
+    if (!w->ev_join) TT_CUDA(cudaEventCreateWithFlags(&w->ev_join, cudaEventDisableTiming));
+    launch_prepass(T, W, grid_tiles(w), stream);
+    launch_tilescan(T, W, stream);
+    launch_pretok(T, W, grid_tiles(w), stream);
+    TT_CUDA(cudaEventRecord(w->ev_fork, stream));
+    TT_CUDA(cudaStreamWaitEvent(w->side, w->ev_fork, 0));
+    launch_bpe_mid(T, W, grid_mid(w), w->side);
+    launch_bpe_long(T, W, grid_long(w), w->side);
+    TT_CUDA(cudaEventRecord(w->ev_join, w->side));
+    launch_bpe_small(T, W, grid_small(w), stream);
+    TT_CUDA(cudaStreamWaitEvent(stream, w->ev_join, 0));
+    launch_ids(T, W, grid_chunks(w), stream);
+    launch_req(T, W, grid_reqs(w), stream);
+    TT_CUDA(cudaGetLastError());
+    h->launches += N_KERNELS;
+    return TT_OK;
+  }
   for (int kidx = 0; kidx < N_KERNELS; ++kidx) {
-    cudaEvent_t a = nullptr, b = nullptr;
-    if (timed) { a = pool_event(h); b = pool_event(h); cudaEventRecord(a, stream); }
+    cudaEvent_t a = pool_event(h), b = pool_event(h);
+    cudaEventRecord(a, stream);
     switch (kidx) {
       case 0: launch_prepass(T, W, grid_tiles(w), stream); break;
       case 1: launch_tilescan(T, W, stream); break;
@@ -383,15 +412,14 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
       case 6: launch_ids(T, W, grid_chunks(w), stream); break;
       case 7: launch_req(T, W, grid_reqs(w), stream); break;
     }
-    if (timed) { cudaEventRecord(b, stream); h->pending.push_back({kidx, a, b}); }
+    cudaEventRecord(b, stream);
+    h->pending.push_back({kidx, a, b});
   }
   TT_CUDA(cudaGetLastError());
   h->launches += N_KERNELS;
   return TT_OK;
 }
 
-// max_bytes: a host-known bound on the batch's bytes (-1 = unknown); buffers
-// for bytes and IDs may be NULL only when the batch has no bytes
 static tt_status check_batch_args(tt_tokenizer *h, const void *d_utf8, const int64_t *offs, int64_t n,
                                   const void *out_ids, const int64_t *out_offs, int64_t max_bytes) {
   if (!h || n < 0 || !offs || !out_offs) return TT_ERR_INVALID_ARG;
@@ -619,7 +647,7 @@ constexpr size_t NA_SIZES[] = {
     sizeof(int2) * NA_TILES, sizeof(int2) * NA_TILES,                 // s1_sum, s1_carry
     2 * (size_t)NA_TILES, 2 * (size_t)NA_TILES,                        // rq_sum, rq_carry
     sizeof(S2) * NA_TILES, sizeof(S2) * NA_TILES, 4 * (size_t)NA_TILES, // s2_agg, s2_inc, s2_flag
-    4 * (size_t)NA_TILES, 4 * (size_t)NA_TILES, 4 * (size_t)NA_TILES,  // cnt_agg, cnt_inc, cnt_flag
+    sizeof(int2) * NA_TILES, sizeof(int2) * NA_TILES, 4 * (size_t)NA_TILES,  // cnt_agg, cnt_inc, cnt_flag
     4 * (size_t)NA_CHUNKS, 4 * (size_t)NA_CHUNKS, 4 * (size_t)NA_CHUNKS, // ids_agg, ids_inc, ids_flag
     4 * 16,                                                            // counters
     4 * (size_t)(NA_BYTES + 2), 4 * (size_t)(NA_BYTES + 1),            // piece_start, n_ids

@@ -10,9 +10,10 @@
 // looked up again.  With a well-ordered merge list (checked when the handle
 // is created) a round equals that many single leftmost merges.
 //
-// Execution units by piece length: a thread per piece up to 32 bytes
-// (state in thread-local arrays); a 512-thread block per longer piece
-// (state in global memory, compacted in place each round).  IDs land in a
+// Execution units by piece length: a thread per piece up to 16 bytes
+// (state in thread-local arrays), a warp per piece up to 256 bytes (state in
+// shared memory), a 512-thread block per longer piece (state in global
+// memory, ping-pong buffers).  IDs land in a
 // byte-indexed scratch array; k_ids scans the per-piece counts with
 // decoupled look-back and writes the final contiguous IDs.
 #include <limits.h>
@@ -77,8 +78,9 @@ __device__ __forceinline__ int bpe_thread(const Tables &T, const uint8_t *bytes,
 }
 
 // ---------------------------------------------------------------- small
-// Thread per piece over all pieces; pieces longer than SMALL_MAX bytes are
-// listed for k_bpe_mid.
+// Thread per piece over the pieces of at most SMALL_MAX bytes (the longer ones
+// were listed by k_pretok and are encoded by k_bpe_mid / k_bpe_long, which
+// may run at the same time on another stream).
 __global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work W) {
   const CallArgs A = *W.args;
   if (A.n <= 0) return;
@@ -93,10 +95,7 @@ __global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work 
     const int32_t e = __ldcg(&W.piece_start[k + 1]) & 0x7FFFFFFF;
     const int len = e - s;
     if (len <= 0 || e > total) { W.n_ids[k] = 0; set_status(W.status, ST_INVALID_ARG); continue; }
-    if (len > SMALL_MAX) {
-      W.long_list[atomicAdd(&W.counters[2], 1)] = k;
-      continue;
-    }
+    if (len > SMALL_MAX) continue;              // listed by k_pretok for k_bpe_mid / k_bpe_long
     int32_t *out = W.scratch + s;
     if (len <= T.max_tok_len) {
       const int id = vocab_probe(T, g + s, len);

@@ -24,7 +24,7 @@ constexpr int S2_SHIFT = 16;                 // forward scan enters at tile star
 static_assert(TILE % 16 == 0, "tile must keep 16-byte alignment");
 
 // BPE execution units by piece length (bytes)
-constexpr int SMALL_MAX = 32;                // thread per piece, dense over all pieces
+constexpr int SMALL_MAX = 16;                // thread per piece, dense over all pieces
 constexpr int MID_MAX = 256;                 // thread per piece, dense over the longer ones
                                              // (> MID_MAX: a block per piece)
 constexpr int IDS_CHUNK = 2048;              // pieces per CTA in the ID scatter
@@ -375,7 +375,8 @@ struct Work {
   // look-back state
   S2 *s2_agg, *s2_inc;
   int *s2_flag;
-  int *cnt_agg, *cnt_inc, *cnt_flag;
+  int2 *cnt_agg, *cnt_inc;         // (pieces, last piece start * 2 + placeholder bit)
+  int *cnt_flag;
   int *ids_agg, *ids_inc, *ids_flag;
   int *counters;                   // [0] pretok tile ticket, [1] ids tile ticket, [2] long list size,
                                    // [3] pieces, [4] tokens, [5] bad requests seen, [6] huge list size

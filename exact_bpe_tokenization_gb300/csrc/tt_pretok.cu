@@ -20,6 +20,8 @@
 //               a tiling shifted 16 bytes left, the reverse queries, the
 //               predicate, and compaction of piece starts with a second
 //               decoupled look-back.
+#include <limits.h>
+
 #include "tt_common.cuh"
 #include "tt_kernels.h"
 
@@ -305,6 +307,7 @@ struct PretokSmem {
   S2 s2_prefix;
   int tile;
   int piece_base;
+  int prev_last;
 };
 
 __device__ __forceinline__ Nbr make_nbr(const WinSmem &S, const uint8_t *chain, int j) {
@@ -504,27 +507,61 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
     a.rq_up = (g >> 9) & 3;
     decide(j, nb, a, pos);
   }
-  int tile_count;
-  const int my_off = block_exclusive_scan<PT_THREADS>(__popc(starts), [](int a, int b) { return a + b; }, 0, P.i_tmp,
-                                                      &tile_count);
+  // --- compaction of piece starts.  The count scan also carries the latest
+  // piece start (pos * 2 + placeholder bit), so each tile learns the start of
+  // the piece running into it and can classify every piece by length as soon
+  // as its successor's start is known: pieces longer than SMALL_MAX bytes are
+  // listed for the warp / block BPE kernels.
+  int my_first = INT_MAX, my_last = -1;
+  for (uint32_t m = starts; m; m &= m - 1) {
+    const int b = __ffs(m) - 1;
+    const int code = (int)(ws + S.lead[c0 + b]) * 2 + (int)((placeholder >> b) & 1);
+    if (my_first == INT_MAX) my_first = code;
+    my_last = code;
+  }
+  auto cnt_op = [](int2 a, int2 b) { return make_int2(a.x + b.x, max(a.y, b.y)); };
+  int2 tile_agg;
+  const int2 my_cnt = block_exclusive_scan<PT_THREADS>(make_int2(__popc(starts), my_last), cnt_op, make_int2(0, -1),
+                                                      P.i2_tmp, &tile_agg);
+  int tile_first;
+  const int next_after_me = block_exclusive_suffix<PT_THREADS>(my_first, [](int a, int b) { return min(a, b); },
+                                                               INT_MAX, P.i_tmp, &tile_first);
   if (tid < 32) {
-    const int pb = warp_lookback(t, tile_count, [](int a, int b) { return a + b; }, 0, W.cnt_agg, W.cnt_inc,
-                                 W.cnt_flag, W.status, W.spin_limit);
+    const int2 pb = warp_lookback(t, tile_agg, cnt_op, make_int2(0, -1), W.cnt_agg, W.cnt_inc, W.cnt_flag, W.status,
+                                  W.spin_limit);
     if (tid == 0) {
-      P.piece_base = pb;
+      P.piece_base = pb.x;
+      P.prev_last = pb.y;
       if (t == ntiles - 1) {
-        W.counters[3] = pb + tile_count;
-        W.piece_start[pb + tile_count] = (int32_t)total;
+        W.counters[3] = pb.x + tile_agg.x;
+        W.piece_start[pb.x + tile_agg.x] = (int32_t)total;
       }
     }
   }
   __syncthreads();
-  int k = P.piece_base + my_off;
+  const bool last_tile = t == ntiles - 1;
+  auto classify = [&](int index, int code, int64_t end) {
+    if (!(code & 1) && end - (code >> 1) > SMALL_MAX) W.long_list[atomicAdd(&W.counters[2], 1)] = index;
+  };
+  int k = P.piece_base + my_cnt.x;
+  int prev_code = -1;
   for (uint32_t m = starts; m; m &= m - 1) {
     const int b = __ffs(m) - 1;
     const int j = c0 + b;
     const int32_t pos = (int32_t)(ws + S.lead[j]);
-    W.piece_start[k++] = (placeholder >> b) & 1 ? (int32_t)(pos | 0x80000000u) : pos;
+    const bool ph = (placeholder >> b) & 1;
+    W.piece_start[k] = ph ? (int32_t)(pos | 0x80000000u) : pos;
+    if (prev_code >= 0) classify(k - 1, prev_code, pos);
+    prev_code = pos * 2 + (ph ? 1 : 0);
+    ++k;
+  }
+  if (prev_code >= 0) {                       // my last piece ends at the next start of the tile
+    if (next_after_me != INT_MAX) classify(k - 1, prev_code, next_after_me >> 1);
+    else if (last_tile) classify(k - 1, prev_code, total);
+  }
+  if (tid == 0 && P.prev_last >= 0) {         // the piece running into this tile
+    if (tile_agg.x > 0) classify(P.piece_base - 1, P.prev_last, tile_first >> 1);
+    else if (last_tile) classify(P.piece_base - 1, P.prev_last, total);
   }
 }
 
