@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", metavar="WORKLOAD", default=None,
+                    help="encode one batch of WORKLOAD once and exit (a small case for an ncu capture)")
     return ap.parse_args()
 
 
@@ -126,6 +128,68 @@ def measured_peak_gbs():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return 6800.0, "fallback"
+
+
+def piece_classes(binding, tok, d_in, d_off, ids, vocab_offsets, cap, dev):
+    """Pieces of one request (from the pre-tokenizer test hook) split by the
+    execution unit that encodes them, with their bytes and token counts (IDs
+    are mapped back to pieces through the byte lengths of their tokens)."""
+    import torch
+    starts, po = tok.pretokenize(d_in, d_off)
+    torch.cuda.synchronize(dev)
+    n = int(po[-1].item())
+    st = starts[:n].cpu().numpy() - int(d_off[0].item())
+    total = int(d_off[-1].item() - d_off[0].item())
+    lens = np.diff(np.append(st, total))
+    tok_len = np.diff(np.asarray(vocab_offsets))[ids]
+    ends = np.cumsum(tok_len)                     # byte end of every token
+    piece_of_token = np.searchsorted(np.cumsum(lens), ends, side="left")
+    tokens = np.bincount(piece_of_token, minlength=n)
+    out = {}
+    for name, lo, hi in (("small", 1, 16), ("mid", 17, 256), ("long", 257, 1 << 40)):
+        sel = (lens >= lo) & (lens <= hi)
+        out[name] = {"pieces": int(sel.sum()), "bytes": int(lens[sel].sum()), "tokens": int(tokens[sel].sum())}
+    out["all"] = {"pieces": n, "bytes": total, "tokens": int(len(ids))}
+    return out
+
+
+def alg_bytes(kernel, c):
+    """Algorithmic bytes of one launch ("Kernels and their
+    rooflines"): bytes a kernel must read and write at minimum."""
+    a = c["all"]
+    if kernel in ("k_prepass", "k_tilescan"):
+        return a["bytes"]                                     # the batch bytes, read once
+    if kernel == "k_pretok":
+        return a["bytes"] + 4 * a["pieces"]                   # bytes in, int32 piece starts out
+    cls = {"k_bpe_small": ["small"], "k_bpe_mid": ["mid"], "k_bpe_long": ["long"]}.get(kernel)
+    if cls:
+        p = sum(c[k]["pieces"] for k in cls)
+        return sum(c[k]["bytes"] + 4 * c[k]["tokens"] for k in cls) + 12 * p   # bytes + starts in, IDs + count out
+    if kernel == "k_ids":
+        return 12 * a["pieces"] + 8 * a["tokens"]             # counts + starts in, IDs in and out
+    return a["bytes"] + 4 * a["tokens"]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel's file (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for r in rec.get("kernels", []):
+        if r.get("kernel") != kernel or r.get("workload") != workload:
+            continue
+        src = os.path.join(ROOT, "exact_bpe_tokenization_gb300", "csrc", r.get("source", ""))
+        try:
+            sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        except OSError:
+            return None
+        return r.get("dram_bytes_per_launch") if sha == r.get("source_sha256") else None
+    return None
 
 
 def cpu_baseline(merges_vocab, family, seeds):
@@ -291,17 +355,18 @@ def run_ours(args):
     peak, peak_kind = measured_peak_gbs()
     per_kernel = {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]} for k, v in prof.items() if v[1]}
     dominant = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_launch"])
+    # algorithmic bytes of the dominant kernel for the last step's request
+    last_ids = ids                                 # host IDs of the last e2e request (same input as step K)
+    classes = piece_classes(binding, tok, dev_in[-1], offs[-1], last_ids, vo, cap, dev)
+    flush.fill_(0)
+    binding.tt_profile(tok.h, 1)
+    encode(dev_in[-1], offs[-1])
+    last_prof = binding.tt_profile_read(tok.h)
+    binding.tt_profile(tok.h, 0)
+    dom_ms = last_prof[dominant][0] / max(last_prof[dominant][1], 1)
+    alg = alg_bytes(dominant, classes)
+    achieved = alg / (dom_ms / 1e3) / 1e9
     mean_req_bytes = nbytes / args.steps
-    # algorithmic bytes per launch of the dominant kernel:
-    #   k_pretok: request bytes read + int32 piece starts written
-    #   k_bpe_small: piece starts + piece bytes read, int32 IDs + counts written
-    #   otherwise: request bytes in + int32 IDs out
-    pieces_per_byte = 0.15
-    alg = {"k_pretok": mean_req_bytes * (1 + 4 * pieces_per_byte),
-           "k_bpe_small": mean_req_bytes * (1 + 8 * pieces_per_byte) + 4 * tokens}.get(
-        dominant, mean_req_bytes + 4 * tokens)
-    dom_s = per_kernel[dominant]["ms_per_launch"] / 1e3
-    achieved = alg / dom_s / 1e9
     p_ms = np.array(step_ms)
     line = {
         "metric": METRIC, "value": nbytes_all / device_s / 1e9, "unit": UNIT, "n_gpus": world,
@@ -321,8 +386,11 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h / args.steps, "p50_ms": float(np.percentile(np.array(e2e_t) * 1e3, 50)),
                 "api": "tt_encode_host (pageable host buffers)"},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
-                     "alg_bytes_per_launch": alg},
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": recorded_traffic(dominant, WORKLOAD),
+                     "alg_bytes_per_launch": alg, "launch_ms": dom_ms,
+                     "timing": "CUDA events around the kernel on its stream, L2 flushed before the launch",
+                     "pieces": classes},
         "kernels_ms_per_launch": {k: round(v["ms_per_launch"], 5) for k, v in per_kernel.items()},
     }
     # the batched burst (~20 MB, 64 requests) as one call, for the batched part of the metric
@@ -358,8 +426,30 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_ncu_case(name):
+    """One encode of a named workload, for a bounded ncu capture."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from exact_bpe_tokenization_gb300 import binding, synth
+    W = synth.WORKLOADS[name]
+    merges, vb, vo = synth.make_vocab(*W["vocab"])
+    data, offs = synth.batch(synth.workload(name))
+    tok = binding.Tokenizer(merges, vb, vo, W["family"])
+    d = torch.from_numpy(data).cuda()
+    o = torch.from_numpy(offs).cuda()
+    ids, io = tok.encode(d, o)
+    torch.cuda.synchronize()
+    status, _ = tok.status()
+    print(json.dumps({"ncu_case": name, "bytes": len(data), "tokens": int(io[-1].item()), "status": status}))
+    tok.close()
+
+
 def main():
     args = parse()
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
