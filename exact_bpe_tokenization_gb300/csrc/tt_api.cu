@@ -42,8 +42,9 @@ struct Workspace {
   int64_t cap_bytes = 0, cap_reqs = 0;
   cudaGraphExec_t graph = nullptr;
   cudaStream_t cap_stream = nullptr;   // private stream the graph is captured on
-  cudaStream_t side = nullptr;         // second branch: long-piece BPE beside the short pieces
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaStream_t side = nullptr;         // second branch: warp BPE of the listed mid-length pieces
+  cudaStream_t side2 = nullptr;        // third branch: block BPE of the listed huge pieces
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_join2 = nullptr;
   // device staging for tt_encode_host (bytes, offsets, ids, id offsets)
   void *stage = nullptr;
   size_t stage_bytes = 0;
@@ -202,12 +203,12 @@ extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, con
   if (pretok_configure() != cudaSuccess) return fail(TT_ERR_CUDA);
   // ---- pair table
   const uint64_t pcap = next_pow2((uint64_t)std::max<int64_t>(2 * n_merges, 1024));
-  std::vector<uint64_t> ptab(pcap, PAIR_EMPTY);
+  std::vector<uint4> ptab(pcap, make_uint4(PAIR_EMPTY, PAIR_EMPTY, 0xFFFFFFFFu, 0xFFFFFFFFu));
   for (int64_t k = 0; k < n_merges; ++k) {
     const uint32_t l = (uint32_t)merge_pairs[2 * k], r = (uint32_t)merge_pairs[2 * k + 1];
     uint64_t sl = pair_hash(l, r) & (pcap - 1);
-    while (ptab[sl] != PAIR_EMPTY) sl = (sl + 1) & (pcap - 1);
-    ptab[sl] = (pair_key(l, r) << MAX_RANK_BITS) | (uint64_t)k;
+    while (ptab[sl].x != PAIR_EMPTY) sl = (sl + 1) & (pcap - 1);
+    ptab[sl] = make_uint4(l, r, (uint32_t)k, (uint32_t)result[k]);
   }
   // ---- vocab table
   const uint64_t vcap = next_pow2((uint64_t)std::max<int64_t>(2 * n_vocab, 1024));
@@ -222,8 +223,8 @@ extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, con
   std::vector<int32_t> voff32((size_t)n_vocab + 1);
   for (int64_t i = 0; i <= n_vocab; ++i) voff32[i] = (int32_t)(vocab_offsets[i] - vbase);
   void *p;
-  if ((s = upload(h, ptab.data(), ptab.size() * 8, &p)) != TT_OK) return fail(s);
-  h->T.pair_tab = (const uint64_t *)p;
+  if ((s = upload(h, ptab.data(), ptab.size() * sizeof(uint4), &p)) != TT_OK) return fail(s);
+  h->T.pair_tab = (const uint4 *)p;
   h->T.pair_mask = (uint32_t)(pcap - 1);
   if ((s = upload(h, result.data(), result.size() * 4, &p)) != TT_OK) return fail(s);
   h->T.merge_result = (const int32_t *)p;
@@ -253,6 +254,8 @@ static void free_workspace(Workspace *w) {
   if (w->graph) cudaGraphExecDestroy(w->graph);
   if (w->cap_stream) cudaStreamDestroy(w->cap_stream);
   if (w->side) cudaStreamDestroy(w->side);
+  if (w->side2) cudaStreamDestroy(w->side2);
+  if (w->ev_join2) cudaEventDestroy(w->ev_join2);
   if (w->ev_fork) cudaEventDestroy(w->ev_fork);
   if (w->ev_join) cudaEventDestroy(w->ev_join);
   if (w->mem) cudaFree(w->mem);
@@ -291,7 +294,7 @@ static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_
       {(void **)&W.id_off, 4 * (size_t)(cap_bytes + 2)},      {(void **)&W.scratch, 4 * (size_t)(cap_bytes + 1)},
       {(void **)&W.tmp_a, 4 * (size_t)(cap_bytes + 1)},       {(void **)&W.tmp_b, 4 * (size_t)(cap_bytes + 1)},
       {(void **)&W.tmp_c, 4 * (size_t)(cap_bytes + 1)},
-      {(void **)&W.long_list, 4 * (size_t)(cap_bytes / (SMALL_MAX + 1) + 2)},
+      {(void **)&W.long_list, 4 * 3 * (size_t)list_cap(cap_bytes)},
       {(void **)&W.huge_list, 4 * (size_t)(cap_bytes / (MID_MAX + 1) + 2)},
       {(void **)&W.bad, (size_t)cap_reqs + 1},          {(void **)&W.bad_pre, 4 * (size_t)(cap_reqs + 2)},
       {(void **)&W.args, sizeof(CallArgs)},
@@ -361,18 +364,19 @@ static int grid_small(const Workspace *w) {
   const int64_t g = (w->cap_bytes / 4 + BPE_SMALL_THREADS - 1) / BPE_SMALL_THREADS;
   return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 8);
 }
-static int grid_mid(const Workspace *w) {   // one warp per listed piece
+static int grid_mid(const Workspace *w) {   // persistent warps taking tickets
   const int64_t g = (w->cap_bytes / (SMALL_MAX + 1) + (BPE_MID_THREADS / 32) - 1) / (BPE_MID_THREADS / 32);
-  return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 8);
+  return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 4);
 }
 static int grid_long(const Workspace *w) {
   return (int)std::min<int64_t>(std::max<int64_t>(w->cap_bytes / (MID_MAX + 1), 1), 152 * 2);
 }
 
 // Enqueue the kernels of one encode on `stream`.  Untimed, the BPE of the
-// listed long pieces (k_bpe_mid, k_bpe_long) runs on a second stream beside
-// the short pieces (k_bpe_small), forked after k_pretok and joined before
-// k_ids; under capture this becomes two parallel graph branches.  Timed
+// listed mid-length pieces (k_bpe_mid) and of the huge pieces (k_bpe_long)
+// run on two more streams beside the short pieces (k_bpe_small), forked
+// after k_pretok and joined before k_ids; under capture these become three
+// parallel graph branches.  Timed
 // (profiling), every kernel runs in turn on `stream` between events.
 static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stream, bool timed) {
   const Tables &T = h->T;
@@ -381,18 +385,23 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
   TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)w->cap_reqs + 1, stream));
   if (!timed) {
     if (!w->side) TT_CUDA(cudaStreamCreateWithFlags(&w->side, cudaStreamNonBlocking));
+    if (!w->side2) TT_CUDA(cudaStreamCreateWithFlags(&w->side2, cudaStreamNonBlocking));
     if (!w->ev_fork) TT_CUDA(cudaEventCreateWithFlags(&w->ev_fork, cudaEventDisableTiming));
     if (!w->ev_join) TT_CUDA(cudaEventCreateWithFlags(&w->ev_join, cudaEventDisableTiming));
+    if (!w->ev_join2) TT_CUDA(cudaEventCreateWithFlags(&w->ev_join2, cudaEventDisableTiming));
     launch_prepass(T, W, grid_tiles(w), stream);
     launch_tilescan(T, W, stream);
     launch_pretok(T, W, grid_tiles(w), stream);
     TT_CUDA(cudaEventRecord(w->ev_fork, stream));
     TT_CUDA(cudaStreamWaitEvent(w->side, w->ev_fork, 0));
+    TT_CUDA(cudaStreamWaitEvent(w->side2, w->ev_fork, 0));
     launch_bpe_mid(T, W, grid_mid(w), w->side);
-    launch_bpe_long(T, W, grid_long(w), w->side);
     TT_CUDA(cudaEventRecord(w->ev_join, w->side));
+    launch_bpe_long(T, W, grid_long(w), w->side2);
+    TT_CUDA(cudaEventRecord(w->ev_join2, w->side2));
     launch_bpe_small(T, W, grid_small(w), stream);
     TT_CUDA(cudaStreamWaitEvent(stream, w->ev_join, 0));
+    TT_CUDA(cudaStreamWaitEvent(stream, w->ev_join2, 0));
     launch_ids(T, W, grid_chunks(w), stream);
     launch_req(T, W, grid_reqs(w), stream);
     TT_CUDA(cudaGetLastError());
@@ -653,7 +662,7 @@ constexpr size_t NA_SIZES[] = {
     4 * (size_t)(NA_BYTES + 2), 4 * (size_t)(NA_BYTES + 1),            // piece_start, n_ids
     4 * (size_t)(NA_BYTES + 2), 4 * (size_t)(NA_BYTES + 1),            // id_off, scratch
     4 * (size_t)(NA_BYTES + 1), 4 * (size_t)(NA_BYTES + 1), 4 * (size_t)(NA_BYTES + 1),  // tmp_a, tmp_b, tmp_c
-    4 * (size_t)(NA_BYTES / (SMALL_MAX + 1) + 2), 4 * (size_t)(NA_BYTES / (MID_MAX + 1) + 2),  // lists
+    4 * 3 * (size_t)list_cap(NA_BYTES), 4 * (size_t)(NA_BYTES / (MID_MAX + 1) + 2),  // lists
     (size_t)NA_REQS + 1, 4 * (size_t)(NA_REQS + 2),                    // bad, bad_pre
     sizeof(CallArgs),                                                  // args
 };
@@ -744,7 +753,7 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   const int g_small = (int)std::min<int64_t>(std::max<int64_t>((NA_BYTES / 4 + BPE_SMALL_THREADS - 1) / BPE_SMALL_THREADS, 1),
                                              152 * 8);
   const int g_mid = (int)std::min<int64_t>(
-      std::max<int64_t>((NA_BYTES / (SMALL_MAX + 1) + (BPE_MID_THREADS / 32) - 1) / (BPE_MID_THREADS / 32), 1), 152 * 8);
+      std::max<int64_t>((NA_BYTES / (SMALL_MAX + 1) + (BPE_MID_THREADS / 32) - 1) / (BPE_MID_THREADS / 32), 1), 152 * 4);
   const int g_long = (int)std::min<int64_t>(std::max<int64_t>(NA_BYTES / (MID_MAX + 1), 1), 152 * 2);
   const int g_chunks = (int)((NA_BYTES + 1 + IDS_CHUNK - 1) / IDS_CHUNK);
   const int g_reqs = (int)((NA_REQS + 1 + 255) / 256);

@@ -106,8 +106,9 @@ __global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work 
 }
 
 // ---------------------------------------------------------------- mid
-// Warp per piece over the pieces longer than SMALL_MAX (up to MID_MAX bytes;
-// longer ones are listed for k_bpe_long).  The token and rank arrays live in
+// Warp per piece over the pieces of SMALL_MAX+1 .. MID_MAX bytes, listed by
+// k_pretok in three length buckets; warps take pieces one at a time through
+// an atomic ticket, longest bucket first.  The token and rank arrays live in
 // shared memory; lane l owns a contiguous segment.  A round: warp min of the
 // ranks, an exclusive max-scan carrying where the current run of hits started
 // (leftmost non-overlapping selection of (a, a) runs), an exclusive sum-scan
@@ -143,25 +144,31 @@ constexpr int MID_WARPS = BPE_MID_THREADS / 32;
 
 __global__ void __launch_bounds__(BPE_MID_THREADS) k_bpe_mid(Tables T, Work W) {
   constexpr int32_t MERGED = (int32_t)0x80000000;
-  __shared__ int32_t sm[MID_WARPS][4][MID_MAX];
+  // per warp: tokens, ranks and merge results of the pair starting at each
+  // position, current and next
+  __shared__ int32_t sm[MID_WARPS][6][MID_MAX];
   const CallArgs A = *W.args;
   if (A.n <= 0) return;
   const int64_t base = __ldg(&A.offs[0]);
   const int64_t total = __ldg(&A.offs[A.n]) - base;
   if (total > W.cap_bytes || total < 0 || base < 0) return;
-  const int nl = __ldcg(&W.counters[2]);
+  const int c0 = __ldcg(&W.counters[mid_bucket_counter(0)]), c1 = __ldcg(&W.counters[mid_bucket_counter(1)]);
+  const int c2 = __ldcg(&W.counters[mid_bucket_counter(2)]);
+  const int64_t lcap = list_cap(W.cap_bytes);
   const uint8_t *g = A.utf8 + base;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = gridDim.x * MID_WARPS;
-  for (int li = blockIdx.x * MID_WARPS + warp; li < nl; li += nwarps) {
-    const int k = __ldcg(&W.long_list[li]);
+  (void)warp;
+  for (;;) {
+    // dynamic assignment, longest bucket first
+    int gi = 0;
+    if (lane == 0) gi = atomicAdd(&W.counters[9], 1);
+    gi = __shfl_sync(0xffffffffu, gi, 0);
+    if (gi >= c0 + c1 + c2) break;
+    const int64_t slot = gi < c0 ? gi : gi < c0 + c1 ? lcap + (gi - c0) : 2 * lcap + (gi - c0 - c1);
+    const int k = __ldcg(&W.long_list[slot]);
     const int32_t s = __ldcg(&W.piece_start[k]);
     const int32_t e = __ldcg(&W.piece_start[k + 1]) & 0x7FFFFFFF;
     const int len = e - s;
-    if (len > MID_MAX) {
-      if (lane == 0) W.huge_list[atomicAdd(&W.counters[6], 1)] = k;
-      continue;
-    }
     const uint8_t *b = g + s;
     if (len <= T.max_tok_len) {
       int id = 0;
@@ -173,10 +180,15 @@ __global__ void __launch_bounds__(BPE_MID_THREADS) k_bpe_mid(Tables T, Work W) {
       }
     }
     int32_t *cur = sm[warp][0], *nxt = sm[warp][1], *rcur = sm[warp][2], *rnxt = sm[warp][3];
+    int32_t *qcur = sm[warp][4], *qnxt = sm[warp][5];
     int n = len;
     for (int i = lane; i < n; i += 32) cur[i] = __ldg(&T.byte_id[__ldg(b + i)]);
     __syncwarp();
-    for (int i = lane; i + 1 < n; i += 32) rcur[i] = pair_rank(T, cur[i], cur[i + 1]);
+    for (int i = lane; i + 1 < n; i += 32) {
+      const int2 pr = pair_lookup(T, cur[i], cur[i + 1]);
+      rcur[i] = pr.x;
+      qcur[i] = pr.y;
+    }
     __syncwarp();
     for (;;) {
       const int seg = (n + 31) >> 5;
@@ -186,14 +198,28 @@ __global__ void __launch_bounds__(BPE_MID_THREADS) k_bpe_mid(Tables T, Work W) {
         if (rcur[i] >= 0 && rcur[i] < lm) lm = rcur[i];
       const int r = warp_min(lm);
       if (r == INT_MAX) break;
-      const int res = __ldg(&T.merge_result[r]);
-      int after_nh = -1;
-      for (int i = lo; i < hi; ++i)
-        if (!(i + 1 < n && rcur[i] == r)) after_nh = i + 1;
-      int run_in = warp_excl_max(after_nh, lane);
-      if (run_in < 0) run_in = 0;
+      // the result of the pair and whether it joins two equal tokens, from a
+      // lane that holds an occurrence
+      int at = -1;
+      if (lm == r)
+        for (int i = lo; i < hi && i + 1 < n; ++i)
+          if (rcur[i] == r) { at = i; break; }
+      const unsigned holders = __ballot_sync(0xffffffffu, at >= 0);
+      const int src = __ffs(holders) - 1;
+      const int res = __shfl_sync(0xffffffffu, at >= 0 ? qcur[at] : 0, src);
+      const bool dbl = __shfl_sync(0xffffffffu, at >= 0 ? (int)(cur[at] == cur[at + 1]) : 0, src) != 0;
+      // runs of hits occur only for a pair (a, a): there the leftmost
+      // non-overlapping selection takes every other hit of a run
+      int run_in = 0;
+      if (dbl) {
+        int after_nh = -1;
+        for (int i = lo; i < hi; ++i)
+          if (!(i + 1 < n && rcur[i] == r)) after_nh = i + 1;
+        run_in = warp_excl_max(after_nh, lane);
+        if (run_in < 0) run_in = 0;
+      }
       bool prev_sel = false;
-      if (lo > 0 && lo < n) prev_sel = rcur[lo - 1] == r && ((lo - 1 - run_in) % 2 == 0);
+      if (lo > 0 && lo < n) prev_sel = rcur[lo - 1] == r && (!dbl || ((lo - 1 - run_in) % 2 == 0));
       int keep = 0;
       {
         int run = run_in;
@@ -202,7 +228,7 @@ __global__ void __launch_bounds__(BPE_MID_THREADS) k_bpe_mid(Tables T, Work W) {
           const bool h = i + 1 < n && rcur[i] == r;
           if (!h) run = i + 1;
           if (!ps) ++keep;
-          ps = h && ((i - run) % 2 == 0);
+          ps = h && (!dbl || ((i - run) % 2 == 0));
         }
       }
       int n_new;
@@ -213,10 +239,11 @@ __global__ void __launch_bounds__(BPE_MID_THREADS) k_bpe_mid(Tables T, Work W) {
         for (int i = lo; i < hi; ++i) {
           const bool h = i + 1 < n && rcur[i] == r;
           if (!h) run = i + 1;
-          const bool sel = h && ((i - run) % 2 == 0);
+          const bool sel = h && (!dbl || ((i - run) % 2 == 0));
           if (!ps) {
             nxt[w] = sel ? (res | MERGED) : cur[i];
             rnxt[w] = (i + 1 < n) ? rcur[i] : -1;
+            qnxt[w] = (i + 1 < n) ? qcur[i] : -1;
             ++w;
           }
           ps = sel;
@@ -226,13 +253,18 @@ __global__ void __launch_bounds__(BPE_MID_THREADS) k_bpe_mid(Tables T, Work W) {
       for (int j = wbase; j < wbase + keep; ++j) {
         if (j + 1 >= n_new) { rnxt[j] = -1; continue; }
         const int a = nxt[j], c = nxt[j + 1];
-        if ((a | c) & MERGED) rnxt[j] = pair_rank(T, a & 0x7FFFFFFF, c & 0x7FFFFFFF);
+        if ((a | c) & MERGED) {
+          const int2 pr = pair_lookup(T, a & 0x7FFFFFFF, c & 0x7FFFFFFF);
+          rnxt[j] = pr.x;
+          qnxt[j] = pr.y;
+        }
       }
       __syncwarp();
       for (int j = wbase; j < wbase + keep; ++j) nxt[j] &= 0x7FFFFFFF;
       __syncwarp();
       int32_t *t1 = cur; cur = nxt; nxt = t1;
       int32_t *t2 = rcur; rcur = rnxt; rnxt = t2;
+      int32_t *t3 = qcur; qcur = qnxt; qnxt = t3;
       n = n_new;
     }
     for (int i = lane; i < n; i += 32) W.scratch[s + i] = cur[i];

@@ -28,6 +28,10 @@ constexpr int SMALL_MAX = 16;                // thread per piece, dense over all
 constexpr int MID_MAX = 256;                 // thread per piece, dense over the longer ones
                                              // (> MID_MAX: a block per piece)
 constexpr int IDS_CHUNK = 2048;              // pieces per CTA in the ID scatter
+// capacity of one mid-length bucket, and the bucket of a piece length
+constexpr int64_t list_cap(int64_t cap_bytes) { return cap_bytes / (SMALL_MAX + 1) + 2; }
+TT_HD int mid_bucket(int64_t len) { return len > 128 ? 0 : len > 48 ? 1 : 2; }
+TT_HD int mid_bucket_counter(int b) { return b == 0 ? 2 : b == 1 ? 7 : 8; }   // counters[] slot
 
 // status codes (mirror include/toktier.h)
 enum : int { ST_OK = 0, ST_INVALID_ARG = 1, ST_INVALID_UTF8 = 4, ST_CAPACITY = 5, ST_TIMEOUT = 8 };
@@ -41,16 +45,16 @@ struct DevStatus {
 __device__ __forceinline__ void set_status(DevStatus *st, int code) { atomicCAS(&st->code, 0, code); }
 
 // ------------------------------------------------------------ tables
-// pair table entry: left << 44 | right << 24 | rank ; empty = ~0
+// pair table entry (16 bytes): {left, right, rank, result}; empty: left = ~0
 // vocab table entry: fp << 32 | len << 20 | id ; empty = 0
-constexpr uint64_t PAIR_EMPTY = ~0ull;
+constexpr uint32_t PAIR_EMPTY = 0xFFFFFFFFu;
 constexpr int MAX_VOCAB_BITS = 20;
 constexpr int MAX_RANK_BITS = 24;
 
 struct Tables {
   const uint16_t *cls1;       // code point >> 8 -> block index
   const uint8_t *cls2;        // block * 256 + (cp & 255) -> raw kind (K_*)
-  const uint64_t *pair_tab;
+  const uint4 *pair_tab;       // {left, right, rank, result}
   uint32_t pair_mask;
   const int32_t *merge_result;
   const uint64_t *vocab_tab;
@@ -90,17 +94,17 @@ TT_HD uint64_t hash_bytes(const uint8_t *b, int len) {
 TT_HD uint32_t vocab_fp(uint64_t h) { uint32_t f = (uint32_t)(h >> 32); return f ? f : 1u; }
 
 #if defined(__CUDACC__)
-// rank of the pair (l, r), or -1
-__device__ __forceinline__ int pair_rank(const Tables &T, int l, int r) {
-  const uint64_t key = pair_key((uint32_t)l, (uint32_t)r);
+// (rank, result) of the pair (l, r); rank -1 if (l, r) is not a merge
+__device__ __forceinline__ int2 pair_lookup(const Tables &T, int l, int r) {
   uint32_t s = (uint32_t)pair_hash((uint32_t)l, (uint32_t)r) & T.pair_mask;
   for (;;) {
-    const uint64_t e = __ldg(&T.pair_tab[s]);
-    if (e == PAIR_EMPTY) return -1;
-    if ((e >> MAX_RANK_BITS) == key) return (int)(e & ((1u << MAX_RANK_BITS) - 1));
+    const uint4 e = __ldg(&T.pair_tab[s]);
+    if (e.x == PAIR_EMPTY) return make_int2(-1, -1);
+    if (e.x == (uint32_t)l && e.y == (uint32_t)r) return make_int2((int)e.z, (int)e.w);
     s = (s + 1) & T.pair_mask;
   }
 }
+__device__ __forceinline__ int pair_rank(const Tables &T, int l, int r) { return pair_lookup(T, l, r).x; }
 
 // 8 bytes starting at p, little-endian, bytes at or past `avail` zeroed
 // (avail >= 1).  Reads only the 8-byte-aligned words that hold a byte of
@@ -378,15 +382,17 @@ struct Work {
   int2 *cnt_agg, *cnt_inc;         // (pieces, last piece start * 2 + placeholder bit)
   int *cnt_flag;
   int *ids_agg, *ids_inc, *ids_flag;
-  int *counters;                   // [0] pretok tile ticket, [1] ids tile ticket, [2] long list size,
-                                   // [3] pieces, [4] tokens, [5] bad requests seen, [6] huge list size
+  int *counters;                   // [0] pretok tile ticket, [1] ids tile ticket, [2] [7] [8] sizes of
+                                   // the mid-length buckets 0..2, [3] pieces, [4] tokens, [5] bad
+                                   // requests seen, [6] huge list size, [9] mid work ticket
   // pieces and tokens
   int32_t *piece_start;            // [cap_bytes + 2], bit 31 = rejected-request placeholder
   int32_t *n_ids;                  // [cap_bytes + 1]
   int32_t *id_off;                 // [cap_bytes + 2]
   int32_t *scratch;                // [cap_bytes] ids by byte position
   int32_t *tmp_a, *tmp_b, *tmp_c;  // [cap_bytes] long-piece work arrays
-  int32_t *long_list;              // [cap_bytes / (SMALL_MAX + 1) + 2] pieces > SMALL_MAX bytes
+  int32_t *long_list;              // 3 buckets of LIST_CAP(cap_bytes) entries: pieces of
+                                   // 129..256, 49..128 and 17..48 bytes
   int32_t *huge_list;              // [cap_bytes / (MID_MAX + 1) + 2] pieces > MID_MAX bytes
   uint8_t *bad;                    // [cap_reqs]
   int32_t *bad_pre;                // [cap_reqs + 1] (test hook)

@@ -511,7 +511,8 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
   // piece start (pos * 2 + placeholder bit), so each tile learns the start of
   // the piece running into it and can classify every piece by length as soon
   // as its successor's start is known: pieces longer than SMALL_MAX bytes are
-  // listed for the warp / block BPE kernels.
+  // listed for the warp BPE kernel (three buckets by length, so that the
+  // longest are taken first) or, beyond MID_MAX bytes, the block kernel.
   int my_first = INT_MAX, my_last = -1;
   for (uint32_t m = starts; m; m &= m - 1) {
     const int b = __ffs(m) - 1;
@@ -540,8 +541,16 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
   }
   __syncthreads();
   const bool last_tile = t == ntiles - 1;
+  const int64_t lcap = list_cap(W.cap_bytes);
   auto classify = [&](int index, int code, int64_t end) {
-    if (!(code & 1) && end - (code >> 1) > SMALL_MAX) W.long_list[atomicAdd(&W.counters[2], 1)] = index;
+    const int64_t len = end - (code >> 1);
+    if ((code & 1) || len <= SMALL_MAX) return;
+    if (len > MID_MAX) {
+      W.huge_list[atomicAdd(&W.counters[6], 1)] = index;
+    } else {
+      const int b = mid_bucket(len);
+      W.long_list[b * lcap + atomicAdd(&W.counters[mid_bucket_counter(b)], 1)] = index;
+    }
   };
   int k = P.piece_base + my_cnt.x;
   int prev_code = -1;
