@@ -341,6 +341,42 @@ __device__ __forceinline__ Nbr make_nbr(const WinSmem &S, const uint8_t *chain, 
   return b;
 }
 
+// A char's neighbourhood slid along a thread's contiguous chars: each step
+// shifts the lookback registers and loads only what enters the window.
+struct Slider {
+  Nbr b;
+  int32_t pos, p1, p2;   // byte positions of j, j+1, j+2
+  __device__ __forceinline__ void start(const WinSmem &S, int64_t ws, int j) {
+    b = make_nbr(S, nullptr, j);
+    pos = (int32_t)(ws + S.lead[j]);
+    p1 = j + 1 < S.nch ? (int32_t)(ws + S.lead[j + 1]) : pos + 1;
+    p2 = j + 2 < S.nch ? (int32_t)(ws + S.lead[j + 2]) : pos + 2;
+  }
+  __device__ __forceinline__ void step(const WinSmem &S, int64_t ws, int j) {   // from j - 1 to j
+    const bool rsj = S.rs[j] != 0;
+    if (rsj) {
+      b.e1 = b.e2 = b.e3 = b.e4 = K_NONE;
+      b.c1 = b.c2 = b.c3 = b.c4 = 0;
+      b.e0 = S.eff[j];
+      b.c0 = S.cp8[j];
+    } else {
+      b.e4 = b.e3; b.e3 = b.e2; b.e2 = b.e1; b.e1 = b.e0; b.e0 = b.en1;
+      b.c4 = b.c3; b.c3 = b.c2; b.c2 = b.c1; b.c1 = b.c0; b.c0 = b.cn1;
+    }
+    b.rs = rsj;
+    const bool in1 = j + 1 < S.nch && !S.rs[j + 1];
+    const bool in2 = in1 && j + 2 < S.nch && !S.rs[j + 2];
+    if (!rsj) { b.en1 = in1 ? b.en2 : K_NONE; b.cn1 = in1 ? b.cn2 : 0; }   // old j+2 is new j+1
+    else { b.en1 = in1 ? S.eff[j + 1] : K_NONE; b.cn1 = in1 ? S.cp8[j + 1] : 0; }
+    b.en2 = in2 ? S.eff[j + 2] : K_NONE;
+    b.cn2 = in2 ? S.cp8[j + 2] : 0;
+    pos = p1;
+    p1 = p2;
+    p2 = j + 2 < S.nch ? (int32_t)(ws + S.lead[j + 2]) : pos + 2;
+  }
+};
+
+template <int FAM>
 __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   PretokSmem &P = *reinterpret_cast<PretokSmem *>(smem_raw);
@@ -356,7 +392,7 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
   __syncthreads();
   const int t = P.tile;
   if (t >= ntiles) return;
-  const int fam = T.family;
+  constexpr int fam = FAM;
   const int64_t ts = (int64_t)t * TILE, te = ts + TILE < total ? ts + TILE : total;
   const int64_t ws = ts - HALO_L;
   load_window(T, A, base, total, ws, S, P.i_tmp);
@@ -426,18 +462,23 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
 
   // --- forward scan (scan 2) over chars with pos in [ts - 16, te); the
   // published aggregate covers the shifted tile [ts - 16, te - 16)
-  const int64_t s2_lo = ts - S2_SHIFT, s2_pub_hi = te - S2_SHIFT;
+  const int64_t s2_lo = ts - S2_SHIFT, s2_pub_hi = t == ntiles - 1 ? INT64_MAX : te - S2_SHIFT;
+  int jlo = c0, jhi = c1;                       // my chars with pos in [s2_lo, te)
+  while (jlo < jhi && ws + S.lead[jlo] < s2_lo) ++jlo;
+  while (jhi > jlo && ws + S.lead[jhi - 1] >= te) --jhi;
   S2 agg_all = s2_identity(), agg_pub = s2_identity();
-  for (int j = c0; j < c1; ++j) {
-    const int64_t pos = ws + S.lead[j];
-    if (pos < s2_lo || pos >= te) continue;
-    const Nbr nb = make_nbr(S, nullptr, j);
-    const int32_t p1 = (int32_t)(j + 1 < S.nch ? ws + S.lead[j + 1] : pos + 1);
-    const int32_t p2 = (int32_t)(j + 2 < S.nch ? ws + S.lead[j + 2] : pos + 2);
-    const S2 el = s2_element(fam, nb, (int32_t)pos, p1, p2);
-    agg_all = s2_combine(agg_all, el);
-    if (t == ntiles - 1 || pos < s2_pub_hi) agg_pub = s2_combine(agg_pub, el);
+  bool pub_done = false;
+  if (jlo < jhi) {
+    Slider w;
+    w.start(S, ws, jlo);
+    for (int j = jlo;;) {
+      if (!pub_done && w.pos >= s2_pub_hi) { agg_pub = agg_all; pub_done = true; }
+      if (!s2_trivial(fam, w.b)) agg_all = s2_combine(agg_all, s2_element(fam, w.b, w.pos, w.p1, w.p2));
+      if (++j >= jhi) break;
+      w.step(S, ws, j);
+    }
   }
+  if (!pub_done) agg_pub = agg_all;
   auto comb = [](const S2 &a, const S2 &b) { return s2_combine(a, b); };
   S2 tile_pub;
   block_exclusive_scan<PT_THREADS>(agg_pub, comb, s2_identity(), P.s2_tmp, &tile_pub);
@@ -465,31 +506,44 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
     }
     if (st) starts |= 1u << (j - c0);
   };
-  for (int j = c0; j < c1; ++j) {
-    const int64_t pos = ws + S.lead[j];
-    if (pos < s2_lo || pos >= te) { P.chain[j] = 1; continue; }
-    Nbr nb = make_nbr(S, P.chain, j);
-    const int32_t p1 = (int32_t)(j + 1 < S.nch ? ws + S.lead[j + 1] : pos + 1);
-    const int32_t p2 = (int32_t)(j + 2 < S.nch ? ws + S.lead[j + 2] : pos + 2);
-    const S2 el = s2_element(fam, nb, (int32_t)pos, p1, p2);
-    Aggs a;
-    bool ch;
-    s2_values(before, el, (int32_t)pos, a, ch);
-    before = s2_combine(before, el);
-    P.chain[j] = ch ? 1 : 0;
-    if (pos < ts) continue;
-    const uint8_t q = P.rq8[j];
-    a.rq_ws = q & 3;
-    a.rq_up = (q >> 2) & 3;
-    // (chain states are read only next to an apostrophe: c0 with l1, c2 with l2, c3 with l3)
-    if (fam == FAM_O200K && j < c0 + 3 &&
-        (nb.c0 == '\'' || nb.c1 == '\'' || nb.c2 == '\'' || nb.c3 == '\'')) {
-      deferred |= 1u << (j - c0);
-      P.dagg[tid][j - c0] = (uint16_t)(a.nidx3 | (a.w_start << 2) | (a.w_prev_other << 3) | (a.w_ncw_before << 4) |
-                             (a.case_prev << 5) | (a.rq_ws << 7) | (a.rq_up << 9));
-      continue;
+  for (int j = c0; j < jlo; ++j) P.chain[j] = 1;
+  for (int j = jhi; j < c1; ++j) P.chain[j] = 1;
+  if (jlo < jhi) {
+    Slider w;
+    w.start(S, ws, jlo);
+    // chain states of the three chars before jlo (valid for o200k only where
+    // they belong to this thread; other cases are deferred below)
+    bool l1 = jlo >= 1 ? P.chain[jlo - 1] != 0 : true, l2 = jlo >= 2 ? P.chain[jlo - 2] != 0 : true;
+    bool l3 = jlo >= 3 ? P.chain[jlo - 3] != 0 : true;
+    for (int j = jlo;;) {
+      const S2 after = s2_trivial(fam, w.b) ? before : s2_combine(before, s2_element(fam, w.b, w.pos, w.p1, w.p2));
+      Aggs a;
+      bool ch;
+      s2_values(before, after, w.pos, a, ch);
+      before = after;
+      if (fam == FAM_O200K) P.chain[j] = ch ? 1 : 0;
+      if (w.pos >= ts) {
+        const uint8_t q = P.rq8[j];
+        a.rq_ws = q & 3;
+        a.rq_up = (q >> 2) & 3;
+        const Nbr &nb = w.b;
+        // (chain states are read only next to an apostrophe: c0 with l1, c2 with l2, c3 with l3)
+        if (fam == FAM_O200K && j < c0 + 3 &&
+            (nb.c0 == '\'' || nb.c1 == '\'' || nb.c2 == '\'' || nb.c3 == '\'')) {
+          deferred |= 1u << (j - c0);
+          P.dagg[tid][j - c0] = (uint16_t)(a.nidx3 | (a.w_start << 2) | (a.w_prev_other << 3) |
+                                           (a.w_ncw_before << 4) | (a.case_prev << 5) | (a.rq_ws << 7) |
+                                           (a.rq_up << 9));
+        } else {
+          Nbr nbl = nb;
+          nbl.l1 = l1; nbl.l2 = l2; nbl.l3 = l3;
+          decide(j, nbl, a, w.pos);
+        }
+      }
+      l3 = l2; l2 = l1; l1 = ch;
+      if (++j >= jhi) break;
+      w.step(S, ws, j);
     }
-    decide(j, nb, a, pos);
   }
   __syncthreads();
   for (uint32_t m = deferred; m; m &= m - 1) {
@@ -581,10 +635,15 @@ void launch_prepass(const Tables &T, const Work &W, int grid, cudaStream_t s) {
 }
 void launch_tilescan(const Tables &T, const Work &W, cudaStream_t s) { k_tilescan<<<1, 1024, 0, s>>>(T, W); }
 void launch_pretok(const Tables &T, const Work &W, int grid, cudaStream_t s) {
-  k_pretok<<<grid, PT_THREADS, sizeof(PretokSmem), s>>>(T, W);
+  if (T.family == FAM_O200K) k_pretok<FAM_O200K><<<grid, PT_THREADS, sizeof(PretokSmem), s>>>(T, W);
+  else k_pretok<FAM_CL100K><<<grid, PT_THREADS, sizeof(PretokSmem), s>>>(T, W);
 }
 cudaError_t pretok_configure() {
-  return cudaFuncSetAttribute(k_pretok, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(PretokSmem));
+  cudaError_t e = cudaFuncSetAttribute(k_pretok<FAM_CL100K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(PretokSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_pretok<FAM_O200K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(PretokSmem));
 }
 
 }  // namespace tt

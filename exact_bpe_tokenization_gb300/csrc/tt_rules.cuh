@@ -284,10 +284,15 @@ TT_HD S2 s2_element(int fam, const Nbr &n, int32_t pos, int32_t pos1, int32_t po
   return r;
 }
 
-// Per-char aggregates from the state before char i and i's element.  The
-// chain bit is true before the first char of the batch.
-TT_HD void s2_values(const S2 &before, const S2 &elem, int32_t pos, Aggs &a, bool &chain_after) {
-  const S2 after = s2_combine(before, elem);
+// True when char i's element is the identity (most chars): nothing to combine.
+TT_HD bool s2_trivial(int fam, const Nbr &n) {
+  return n.e0 != K_NUM && n.e0 != K_WS && !(fam == FAM_O200K && is_letter(n.e0));
+}
+
+// Per-char aggregates from the state before char i and the state after it
+// (before combined with i's element).  The chain bit is true before the
+// first char of the batch.
+TT_HD void s2_values(const S2 &before, const S2 &after, int32_t pos, Aggs &a, bool &chain_after) {
   a.nidx3 = (after.ncount + 2) % 3;
   const int32_t s = after.wst >> 1;
   a.w_start = s == pos;

@@ -64,12 +64,13 @@ extern "C" void rules_host_starts(int fam, const uint32_t *cp, const uint8_t *ra
   S2 before = s2_identity();
   for (int64_t j = 0; j < n; ++j) {
     Nbr b = nbr(j);
-    S2 el = s2_element(fam, b, (int32_t)j, (int32_t)(j + 1), (int32_t)(j + 2));
+    const S2 after = s2_trivial(fam, b) ? before
+                     : s2_combine(before, s2_element(fam, b, (int32_t)j, (int32_t)(j + 1), (int32_t)(j + 2)));
     Aggs a;
     bool ch;
-    s2_values(before, el, (int32_t)j, a, ch);
+    s2_values(before, after, (int32_t)j, a, ch);
     chain[j] = ch;
-    before = s2_combine(before, el);
+    before = after;
     a.rq_ws = rq_ws[j];
     a.rq_up = rq_up[j];
     start[j] = piece_start(fam, b, a) ? 1 : 0;
