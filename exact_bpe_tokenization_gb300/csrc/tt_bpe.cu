@@ -108,45 +108,40 @@ __global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work 
 // ---------------------------------------------------------------- mid
 // Warp per piece over the pieces of SMALL_MAX+1 .. MID_MAX bytes, listed by
 // k_pretok in three length buckets; warps take pieces one at a time through
-// an atomic ticket, longest bucket first.  The token and rank arrays live in
-// shared memory; lane l owns a contiguous segment.  A round: warp min of the
-// ranks, an exclusive max-scan carrying where the current run of hits started
-// (leftmost non-overlapping selection of (a, a) runs), an exclusive sum-scan
-// of kept tokens, the write into the other buffer, then lookups for the
-// pairs next to a merge -- shuffles only, no block barrier.
-__device__ __forceinline__ int warp_min(int v) {
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, d));
-  return v;
-}
-__device__ __forceinline__ int warp_excl_max(int v, int lane) {
-  int inc = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, inc, d);
-    if (lane >= d) inc = max(inc, y);
-  }
-  const int ex = __shfl_up_sync(0xffffffffu, inc, 1);
-  return lane == 0 ? -1 : ex;
-}
-__device__ __forceinline__ int warp_excl_sum(int v, int lane, int *total) {
-  int inc = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, inc, d);
-    if (lane >= d) inc += y;
-  }
-  *total = __shfl_sync(0xffffffffu, inc, 31);
-  return inc - v;
-}
-
+// an atomic ticket, longest bucket first.  Symbols never move: the piece is
+// a doubly linked list over fixed positions in shared memory (lane l owns
+// positions l, l + 32, ...), each alive position holding its token and the
+// rank and result of the pair it starts.  A round: warp min of the ranks
+// (r); every occurrence of r whose predecessor is not itself an occurrence
+// merges in place (its right neighbour is unlinked) and looks up the two
+// pairs it touches.  Occurrences left over -- only inside runs of a pair
+// (a, a) -- repeat that step with the same r, which takes every other member
+// of a run from its left end: the leftmost non-overlapping set.  Pairs made
+// by a merge rank above r (well-ordered list), so they never join a run.
 constexpr int MID_WARPS = BPE_MID_THREADS / 32;
+constexpr int MID_SLOTS = MID_MAX / 32;
 
-__global__ void __launch_bounds__(BPE_MID_THREADS) k_bpe_mid(Tables T, Work W) {
-  constexpr int32_t MERGED = (int32_t)0x80000000;
-  // per warp: tokens, ranks and merge results of the pair starting at each
-  // position, current and next
-  __shared__ int32_t sm[MID_WARPS][6][MID_MAX];
+__device__ __forceinline__ int rank_or_max(int r) { return r < 0 ? INT_MAX : r; }
+
+// the rest of a pair lookup whose first probe e (slot s) is already loaded
+__device__ __forceinline__ int2 pair_finish(const Tables &T, uint4 e, uint32_t s, int l, int r) {
+  for (;;) {
+    if (e.x == PAIR_EMPTY) return make_int2(-1, -1);
+    if (e.x == (uint32_t)l && e.y == (uint32_t)r) return make_int2((int)e.z, (int)e.w);
+    s = (s + 1) & T.pair_mask;
+    e = __ldg(&T.pair_tab[s]);
+  }
+}
+__device__ __forceinline__ uint32_t pair_slot(const Tables &T, int l, int r) {
+  return (uint32_t)pair_hash((uint32_t)l, (uint32_t)r) & T.pair_mask;
+}
+
+__global__ void __launch_bounds__(BPE_MID_THREADS, 4) k_bpe_mid(Tables T, Work W) {
+  __shared__ int32_t s_tok[MID_WARPS][MID_MAX];   // token, -1 once unlinked
+  __shared__ int32_t s_rank[MID_WARPS][MID_MAX];  // rank of (p, next), INT_MAX if none
+  __shared__ int32_t s_res[MID_WARPS][MID_MAX];   // its merge result
+  __shared__ int16_t s_nx[MID_WARPS][MID_MAX];
+  __shared__ int16_t s_pv[MID_WARPS][MID_MAX];
   const CallArgs A = *W.args;
   if (A.n <= 0) return;
   const int64_t base = __ldg(&A.offs[0]);
@@ -157,7 +152,9 @@ __global__ void __launch_bounds__(BPE_MID_THREADS) k_bpe_mid(Tables T, Work W) {
   const int64_t lcap = list_cap(W.cap_bytes);
   const uint8_t *g = A.utf8 + base;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  (void)warp;
+  const unsigned lt_mask = (1u << lane) - 1;
+  int32_t *tok = s_tok[warp], *rank = s_rank[warp], *res = s_res[warp];
+  int16_t *nx = s_nx[warp], *pv = s_pv[warp];
   for (;;) {
     // dynamic assignment, longest bucket first
     int gi = 0;
@@ -165,110 +162,124 @@ __global__ void __launch_bounds__(BPE_MID_THREADS) k_bpe_mid(Tables T, Work W) {
     gi = __shfl_sync(0xffffffffu, gi, 0);
     if (gi >= c0 + c1 + c2) break;
     const int64_t slot = gi < c0 ? gi : gi < c0 + c1 ? lcap + (gi - c0) : 2 * lcap + (gi - c0 - c1);
-    const int k = __ldcg(&W.long_list[slot]);
-    const int32_t s = __ldcg(&W.piece_start[k]);
-    const int32_t e = __ldcg(&W.piece_start[k + 1]) & 0x7FFFFFFF;
-    const int len = e - s;
+    const int pc = __ldcg(&W.long_list[slot]);
+    const int32_t s = __ldcg(&W.piece_start[pc]);
+    const int32_t e = __ldcg(&W.piece_start[pc + 1]) & 0x7FFFFFFF;
+    const int n = e - s;
     const uint8_t *b = g + s;
-    if (len <= T.max_tok_len) {
+    if (n <= T.max_tok_len) {
       int id = 0;
-      if (lane == 0) id = vocab_probe(T, b, len);
+      if (lane == 0) id = vocab_probe(T, b, n);
       id = __shfl_sync(0xffffffffu, id, 0);
       if (id >= 0) {
-        if (lane == 0) { W.scratch[s] = id; W.n_ids[k] = 1; }
+        if (lane == 0) { W.scratch[s] = id; W.n_ids[pc] = 1; }
         continue;
       }
     }
-    int32_t *cur = sm[warp][0], *nxt = sm[warp][1], *rcur = sm[warp][2], *rnxt = sm[warp][3];
-    int32_t *qcur = sm[warp][4], *qnxt = sm[warp][5];
-    int n = len;
-    for (int i = lane; i < n; i += 32) cur[i] = __ldg(&T.byte_id[__ldg(b + i)]);
+    const int nslot = (n + 31) >> 5;
+#pragma unroll
+    for (int k = 0; k < MID_SLOTS; ++k) {
+      const int p = lane + 32 * k;
+      if (k < nslot) {
+        tok[p] = p < n ? __ldg(&T.byte_id[__ldg(b + p)]) : -1;
+        rank[p] = INT_MAX;
+        nx[p] = (int16_t)(p + 1);
+        pv[p] = (int16_t)(p - 1);
+      }
+    }
     __syncwarp();
-    for (int i = lane; i + 1 < n; i += 32) {
-      const int2 pr = pair_lookup(T, cur[i], cur[i + 1]);
-      rcur[i] = pr.x;
-      qcur[i] = pr.y;
+    // initial pair lookups, first probes of four slots in flight together
+    for (int k0 = 0; k0 < nslot; k0 += 4) {
+      uint4 ent[4];
+      uint32_t sl[4];
+      int lt[4], rt[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int p = lane + 32 * (k0 + j);
+        const bool v = k0 + j < nslot && p + 1 < n;
+        lt[j] = v ? tok[p] : 0;
+        rt[j] = v ? tok[p + 1] : 0;
+        sl[j] = pair_slot(T, lt[j], rt[j]);
+        ent[j] = v ? __ldg(&T.pair_tab[sl[j]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int p = lane + 32 * (k0 + j);
+        if (k0 + j < nslot && p + 1 < n) {
+          const int2 pr = pair_finish(T, ent[j], sl[j], lt[j], rt[j]);
+          rank[p] = rank_or_max(pr.x);
+          res[p] = pr.y;
+        }
+      }
     }
     __syncwarp();
     for (;;) {
-      const int seg = (n + 31) >> 5;
-      const int lo = min(lane * seg, n), hi = min(lo + seg, n);
       int lm = INT_MAX;
-      for (int i = lo; i < hi && i + 1 < n; ++i)
-        if (rcur[i] >= 0 && rcur[i] < lm) lm = rcur[i];
-      const int r = warp_min(lm);
+#pragma unroll
+      for (int k = 0; k < MID_SLOTS; ++k)
+        if (k < nslot) lm = min(lm, rank[lane + 32 * k]);
+      const int r = __reduce_min_sync(0xffffffffu, lm);
       if (r == INT_MAX) break;
-      // the result of the pair and whether it joins two equal tokens, from a
-      // lane that holds an occurrence
-      int at = -1;
-      if (lm == r)
-        for (int i = lo; i < hi && i + 1 < n; ++i)
-          if (rcur[i] == r) { at = i; break; }
-      const unsigned holders = __ballot_sync(0xffffffffu, at >= 0);
-      const int src = __ffs(holders) - 1;
-      const int res = __shfl_sync(0xffffffffu, at >= 0 ? qcur[at] : 0, src);
-      const bool dbl = __shfl_sync(0xffffffffu, at >= 0 ? (int)(cur[at] == cur[at + 1]) : 0, src) != 0;
-      // runs of hits occur only for a pair (a, a): there the leftmost
-      // non-overlapping selection takes every other hit of a run
-      int run_in = 0;
-      if (dbl) {
-        int after_nh = -1;
-        for (int i = lo; i < hi; ++i)
-          if (!(i + 1 < n && rcur[i] == r)) after_nh = i + 1;
-        run_in = warp_excl_max(after_nh, lane);
-        if (run_in < 0) run_in = 0;
-      }
-      bool prev_sel = false;
-      if (lo > 0 && lo < n) prev_sel = rcur[lo - 1] == r && (!dbl || ((lo - 1 - run_in) % 2 == 0));
-      int keep = 0;
-      {
-        int run = run_in;
-        bool ps = prev_sel;
-        for (int i = lo; i < hi; ++i) {
-          const bool h = i + 1 < n && rcur[i] == r;
-          if (!h) run = i + 1;
-          if (!ps) ++keep;
-          ps = h && (!dbl || ((i - run) % 2 == 0));
-        }
-      }
-      int n_new;
-      const int wbase = warp_excl_sum(keep, lane, &n_new);
-      {
-        int run = run_in, w = wbase;
-        bool ps = prev_sel;
-        for (int i = lo; i < hi; ++i) {
-          const bool h = i + 1 < n && rcur[i] == r;
-          if (!h) run = i + 1;
-          const bool sel = h && (!dbl || ((i - run) % 2 == 0));
-          if (!ps) {
-            nxt[w] = sel ? (res | MERGED) : cur[i];
-            rnxt[w] = (i + 1 < n) ? rcur[i] : -1;
-            qnxt[w] = (i + 1 < n) ? qcur[i] : -1;
-            ++w;
+      for (int step = 0; step < n; ++step) {
+        uint32_t sel = 0;
+        bool left = false;
+#pragma unroll
+        for (int k = 0; k < MID_SLOTS; ++k) {
+          const int p = lane + 32 * k;
+          if (k < nslot && rank[p] == r) {
+            const int q = pv[p];
+            if (q < 0 || rank[q] != r) sel |= 1u << k;
+            else left = true;
           }
-          ps = sel;
         }
-      }
-      __syncwarp();
-      for (int j = wbase; j < wbase + keep; ++j) {
-        if (j + 1 >= n_new) { rnxt[j] = -1; continue; }
-        const int a = nxt[j], c = nxt[j + 1];
-        if ((a | c) & MERGED) {
-          const int2 pr = pair_lookup(T, a & 0x7FFFFFFF, c & 0x7FFFFFFF);
-          rnxt[j] = pr.x;
-          qnxt[j] = pr.y;
+        __syncwarp();
+        for (uint32_t m = sel; m; m &= m - 1) {
+          const int p = lane + 32 * (__ffs(m) - 1);
+          const int q = nx[p], nq = nx[q];
+          tok[p] = res[p];
+          tok[q] = -1;
+          rank[q] = INT_MAX;
+          rank[p] = INT_MAX;
+          nx[p] = (int16_t)nq;
+          if (nq < n) pv[nq] = (int16_t)p;
         }
+        __syncwarp();
+        for (uint32_t m = sel; m; m &= m - 1) {
+          const int p = lane + 32 * (__ffs(m) - 1);
+          const int a = pv[p], c = nx[p];
+          const int tp = tok[p];
+          const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
+          const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
+          const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+          const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+          if (a >= 0) {
+            const int2 pr = pair_finish(T, ea, sa, ta, tp);
+            rank[a] = rank_or_max(pr.x);
+            res[a] = pr.y;
+          }
+          if (c < n) {
+            const int2 pr = pair_finish(T, ec, sc, tp, tc);
+            rank[p] = rank_or_max(pr.x);
+            res[p] = pr.y;
+          }
+        }
+        __syncwarp();
+        if (!__any_sync(0xffffffffu, left)) break;
       }
-      __syncwarp();
-      for (int j = wbase; j < wbase + keep; ++j) nxt[j] &= 0x7FFFFFFF;
-      __syncwarp();
-      int32_t *t1 = cur; cur = nxt; nxt = t1;
-      int32_t *t2 = rcur; rcur = rnxt; rnxt = t2;
-      int32_t *t3 = qcur; qcur = qnxt; qnxt = t3;
-      n = n_new;
     }
-    for (int i = lane; i < n; i += 32) W.scratch[s + i] = cur[i];
-    if (lane == 0) W.n_ids[k] = n;
+    // surviving tokens in position order
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < MID_SLOTS; ++k) {
+      if (k < nslot) {
+        const int p = lane + 32 * k;
+        const int t = tok[p];
+        const unsigned bal = __ballot_sync(0xffffffffu, t >= 0);
+        if (t >= 0) W.scratch[s + cnt + __popc(bal & lt_mask)] = t;
+        cnt += __popc(bal);
+      }
+    }
+    if (lane == 0) W.n_ids[pc] = cnt;
     __syncwarp();
   }
 }
