@@ -297,6 +297,7 @@ static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_
       {(void **)&W.long_list, 4 * 3 * (size_t)list_cap(cap_bytes)},
       {(void **)&W.huge_list, 4 * (size_t)(cap_bytes / (MID_MAX + 1) + 2)},
       {(void **)&W.bad, (size_t)cap_reqs + 1},          {(void **)&W.bad_pre, 4 * (size_t)(cap_reqs + 2)},
+      {(void **)&W.req_piece, 4 * (size_t)(cap_reqs + 1)},
       {(void **)&W.args, sizeof(CallArgs)},
   };
   size_t total = 0;
@@ -358,7 +359,10 @@ static cudaEvent_t pool_event(tt_tokenizer *h) {
 
 // grid sizes, all from capacity
 static int grid_tiles(const Workspace *w) { return (int)((w->cap_bytes + TILE - 1) / TILE); }
-static int grid_chunks(const Workspace *w) { return (int)((w->cap_bytes + 1 + IDS_CHUNK - 1) / IDS_CHUNK); }
+static int grid_chunks(const Workspace *w) {   // persistent CTAs taking chunk tickets
+  const int64_t g = (w->cap_bytes + 1 + IDS_CHUNK - 1) / IDS_CHUNK;
+  return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 4);
+}
 static int grid_reqs(const Workspace *w) { return (int)((w->cap_reqs + 1 + 255) / 256); }
 static int grid_small(const Workspace *w) {
   const int64_t g = (w->cap_bytes / 4 + BPE_SMALL_THREADS - 1) / BPE_SMALL_THREADS;
@@ -664,6 +668,7 @@ constexpr size_t NA_SIZES[] = {
     4 * (size_t)(NA_BYTES + 1), 4 * (size_t)(NA_BYTES + 1), 4 * (size_t)(NA_BYTES + 1),  // tmp_a, tmp_b, tmp_c
     4 * 3 * (size_t)list_cap(NA_BYTES), 4 * (size_t)(NA_BYTES / (MID_MAX + 1) + 2),  // lists
     (size_t)NA_REQS + 1, 4 * (size_t)(NA_REQS + 2),                    // bad, bad_pre
+    4 * (size_t)(NA_REQS + 1),                                         // req_piece
     sizeof(CallArgs),                                                  // args
 };
 constexpr size_t na_total() {
@@ -730,7 +735,7 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
                   (void **)&W.ids_flag, (void **)&W.counters, (void **)&W.piece_start, (void **)&W.n_ids,
                   (void **)&W.id_off,  (void **)&W.scratch,  (void **)&W.tmp_a,    (void **)&W.tmp_b,
                   (void **)&W.tmp_c,   (void **)&W.long_list, (void **)&W.huge_list, (void **)&W.bad,
-                  (void **)&W.bad_pre, (void **)&W.args};
+                  (void **)&W.bad_pre, (void **)&W.req_piece, (void **)&W.args};
   static_assert(sizeof(dst) / sizeof(dst[0]) == sizeof(NA_SIZES) / sizeof(NA_SIZES[0]), "layout");
   size_t off = 0;
   for (size_t i = 0; i < sizeof(NA_SIZES) / sizeof(NA_SIZES[0]); ++i) {

@@ -421,7 +421,8 @@ __global__ void __launch_bounds__(BPE_LONG_THREADS) k_bpe_long(Tables T, Work W)
 // ---------------------------------------------------------------- ids
 __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
   constexpr int PER = IDS_CHUNK / IDS_THREADS;
-  __shared__ int s_off[IDS_CHUNK];
+  __shared__ int s_off[IDS_CHUNK + 1];   // chunk-local output offset of each piece
+  __shared__ int s_st[IDS_CHUNK];        // its start byte (its IDs sit at scratch[start ...])
   __shared__ int red[IDS_THREADS / 32];
   __shared__ int s_tile, s_base;
   const CallArgs A = *W.args;
@@ -432,53 +433,72 @@ __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
   if (total > W.cap_bytes || total < 0 || base < 0) return;
   const int np = __ldcg(&W.counters[3]);
   const int nchunks = (np + IDS_CHUNK - 1) / IDS_CHUNK;
-  if (tid == 0) s_tile = atomicAdd(&W.counters[1], 1);
-  __syncthreads();
-  const int t = s_tile;
-  if (t >= nchunks) return;
-  const int k0 = t * IDS_CHUNK;
-  int cnt[PER];
-  int sum = 0;
+  for (;;) {
+    if (tid == 0) s_tile = atomicAdd(&W.counters[1], 1);
+    __syncthreads();
+    const int t = s_tile;
+    if (t >= nchunks) return;
+    const int k0 = t * IDS_CHUNK;
+    const int nloc = min(IDS_CHUNK, np - k0);
+    int cnt[PER], st[PER];
+    int sum = 0;
 #pragma unroll
-  for (int m = 0; m < PER; ++m) {
-    const int k = k0 + tid * PER + m;
-    cnt[m] = k < np ? __ldcg(&W.n_ids[k]) : 0;
-    sum += cnt[m];
-  }
-  int chunk_total;
-  const int ex = block_exclusive_scan<IDS_THREADS>(sum, [](int a, int b) { return a + b; }, 0, red, &chunk_total);
-  if (tid < 32) {
-    const int b = warp_lookback(t, chunk_total, [](int a, int b) { return a + b; }, 0, W.ids_agg, W.ids_inc,
-                                W.ids_flag, W.status, W.spin_limit);
-    if (tid == 0) {
-      s_base = b;
-      if (t == nchunks - 1) {
-        W.id_off[np] = b + chunk_total;
-        W.counters[4] = b + chunk_total;
+    for (int m = 0; m < PER; ++m) {
+      const int q = tid * PER + m;
+      cnt[m] = 0;
+      st[m] = 0;
+      if (q < nloc) {
+        cnt[m] = __ldcg(&W.n_ids[k0 + q]);
+        st[m] = __ldcg(&W.piece_start[k0 + q]) & 0x7FFFFFFF;
+        if (cnt[m] < 0 || (int64_t)st[m] + cnt[m] > total) {   // never for a sound piece table
+          set_status(W.status, ST_INVALID_ARG);
+          cnt[m] = 0;
+        }
+      }
+      sum += cnt[m];
+    }
+    int chunk_total;
+    const int ex = block_exclusive_scan<IDS_THREADS>(sum, [](int a, int b) { return a + b; }, 0, red, &chunk_total);
+    if (tid < 32) {
+      const int b = warp_lookback(t, chunk_total, [](int a, int b) { return a + b; }, 0, W.ids_agg, W.ids_inc,
+                                  W.ids_flag, W.status, W.spin_limit);
+      if (tid == 0) {
+        s_base = b;
+        if (t == nchunks - 1) {
+          W.id_off[np] = b + chunk_total;
+          W.counters[4] = b + chunk_total;
+        }
       }
     }
-  }
-  __syncthreads();
-  int off = s_base + ex;
+    __syncthreads();
+    const int cb = s_base;
+    int off = ex;
 #pragma unroll
-  for (int m = 0; m < PER; ++m) {
-    const int k = k0 + tid * PER + m;
-    s_off[tid * PER + m] = off;
-    if (k < np) W.id_off[k] = off;
-    off += cnt[m];
-  }
-  __syncthreads();
-  for (int q = tid; q < IDS_CHUNK; q += IDS_THREADS) {
-    const int k = k0 + q;
-    if (k >= np) break;
-    const int c = __ldcg(&W.n_ids[k]);
-    const int32_t st = __ldcg(&W.piece_start[k]) & 0x7FFFFFFF;
-    const int o = s_off[q];
-    if (c < 0 || o < 0 || (int64_t)o + c > total || (int64_t)st + c > total) {   // never for a sound piece table
-      set_status(W.status, ST_INVALID_ARG);
-      continue;
+    for (int m = 0; m < PER; ++m) {
+      const int q = tid * PER + m;
+      s_off[q] = off;
+      s_st[q] = st[m];
+      if (q < nloc) W.id_off[k0 + q] = cb + off;
+      off += cnt[m];
     }
-    for (int j = 0; j < c; ++j) A.out_ids[o + j] = __ldcg(&W.scratch[st + j]);
+    if (tid == 0) s_off[IDS_CHUNK] = chunk_total;
+    __syncthreads();
+    // output-parallel copy: output o of the chunk belongs to the last piece
+    // whose offset is <= o (pieces with no IDs share their successor's offset)
+    if ((int64_t)cb + chunk_total > total) {
+      if (tid == 0) set_status(W.status, ST_INVALID_ARG);
+    } else {
+      for (int o = tid; o < chunk_total; o += IDS_THREADS) {
+        int lo = 0, hi = nloc - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_off[mid] <= o) lo = mid;
+          else hi = mid - 1;
+        }
+        A.out_ids[cb + o] = __ldcg(&W.scratch[s_st[lo] + (o - s_off[lo])]);
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -492,6 +512,9 @@ __device__ __forceinline__ int lower_bound_piece(const int32_t *ps, int np, int6
   return lo;
 }
 
+// out_id_offsets[r]: the ID offset of request r's first piece (recorded by
+// the pre-tokenizer); empty requests at the end of the batch get the token
+// count.
 __global__ void k_req(Tables T, Work W) {
   const CallArgs A = *W.args;
   const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -501,7 +524,12 @@ __global__ void k_req(Tables T, Work W) {
   if (total > W.cap_bytes || total < 0 || base < 0) { A.out_id_offsets[r] = 0; return; }
   const int np = __ldcg(&W.counters[3]);
   const int tokens = __ldcg(&W.counters[4]);
-  const int k = lower_bound_piece(W.piece_start, np, __ldg(&A.offs[r]) - base);
+  const int64_t pos = __ldg(&A.offs[r]) - base;
+  int k = np;
+  if (r < A.n && pos < total) {
+    k = __ldcg(&W.req_piece[r]);
+    if (k < 0 || k >= np) { set_status(W.status, ST_INVALID_ARG); k = np; }
+  }
   A.out_id_offsets[r] = k < np ? __ldcg(&W.id_off[k]) : tokens;
 }
 

@@ -27,7 +27,7 @@ static_assert(TILE % 16 == 0, "tile must keep 16-byte alignment");
 constexpr int SMALL_MAX = 16;                // thread per piece, dense over all pieces
 constexpr int MID_MAX = 256;                 // thread per piece, dense over the longer ones
                                              // (> MID_MAX: a block per piece)
-constexpr int IDS_CHUNK = 2048;              // pieces per CTA in the ID scatter
+constexpr int IDS_CHUNK = 512;               // pieces per ticket in the ID scatter
 // capacity of one mid-length bucket, and the bucket of a piece length
 constexpr int64_t list_cap(int64_t cap_bytes) { return cap_bytes / (SMALL_MAX + 1) + 2; }
 TT_HD int mid_bucket(int64_t len) { return len > 128 ? 0 : len > 48 ? 1 : 2; }
@@ -396,6 +396,7 @@ struct Work {
   int32_t *huge_list;              // [cap_bytes / (MID_MAX + 1) + 2] pieces > MID_MAX bytes
   uint8_t *bad;                    // [cap_reqs]
   int32_t *bad_pre;                // [cap_reqs + 1] (test hook)
+  int32_t *req_piece;              // [cap_reqs + 1] first piece of each non-empty request
   DevStatus *status;
   CallArgs *args;
 };

@@ -614,6 +614,10 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
     const int32_t pos = (int32_t)(ws + S.lead[j]);
     const bool ph = (placeholder >> b) & 1;
     W.piece_start[k] = ph ? (int32_t)(pos | 0x80000000u) : pos;
+    if (S.rs[j]) {                            // first piece of the requests starting here
+      int r = S.r0 + (int)lower_bound64(A.offs + S.r0, S.r1 - S.r0, base + pos);
+      for (; r < S.r1 && __ldg(&A.offs[r]) == base + pos; ++r) W.req_piece[r] = k;
+    }
     if (prev_code >= 0) classify(k - 1, prev_code, pos);
     prev_code = pos * 2 + (ph ? 1 : 0);
     ++k;
