@@ -10,10 +10,11 @@
 // looked up again.  With a well-ordered merge list (checked when the handle
 // is created) a round equals that many single leftmost merges.
 //
-// Execution units by piece length: a thread per piece up to 16 bytes
-// (state in thread-local arrays), a warp per piece up to 256 bytes (state in
-// shared memory), a 512-thread block per longer piece (state in global
-// memory, ping-pong buffers).  IDs land in a
+// Execution units by piece length: up to 16 bytes a thread per piece for
+// the whole-piece probe and 16 lanes per piece for merging (state in
+// registers), a warp per piece up to 256 bytes (registers up to 32 bytes,
+// else a linked list in shared memory), a 512-thread block per longer piece
+// (state in global memory, ping-pong buffers).  IDs land in a
 // byte-indexed scratch array; k_ids scans the per-piece counts with
 // decoupled look-back and writes the final contiguous IDs.
 #include <limits.h>
@@ -43,44 +44,89 @@ __device__ __forceinline__ int vocab_probe(const Tables &T, const uint8_t *b, in
   }
 }
 
-// Round merging of one piece by one thread.  ids/rk live in thread-local
-// arrays of MAXLEN entries; `bytes` points to the piece (any memory space).
-// Returns the number of IDs written to out.
-template <int MAXLEN>
-__device__ __forceinline__ int bpe_thread(const Tables &T, const uint8_t *bytes, int len, int32_t *out) {
-  int ids[MAXLEN], rk[MAXLEN];
-  int n = len;
-  for (int i = 0; i < n; ++i) ids[i] = __ldg(&T.byte_id[__ldg(bytes + i)]);
-  for (int i = 0; i + 1 < n; ++i) rk[i] = pair_rank(T, ids[i], ids[i + 1]);
+__device__ __forceinline__ int rank_or_max(int r) { return r < 0 ? INT_MAX : r; }
+
+// the rest of a pair lookup whose first probe e (slot s) is already loaded
+__device__ __forceinline__ int2 pair_finish(const Tables &T, uint4 e, uint32_t s, int l, int r) {
   for (;;) {
-    int r = INT_MAX;
-    for (int i = 0; i + 1 < n; ++i)
-      if (rk[i] >= 0 && rk[i] < r) r = rk[i];
-    if (r == INT_MAX) break;
-    const int res = __ldg(&T.merge_result[r]);
-    // one sweep: merge every leftmost non-overlapping occurrence of rank r;
-    // ranks of untouched pairs are kept, pairs next to a merge are looked up
-    int w = 0, i = 0;
-    bool prev_merged = false;
-    while (i < n) {
-      const bool m = (i + 1 < n) && rk[i] == r;
-      const int tok = m ? res : ids[i];
-      if (w > 0) rk[w - 1] = (m || prev_merged) ? pair_rank(T, ids[w - 1], tok) : rk[i - 1];
-      ids[w] = tok;
-      prev_merged = m;
-      ++w;
-      i += m ? 2 : 1;
-    }
-    n = w;
+    if (e.x == PAIR_EMPTY) return make_int2(-1, -1);
+    if (e.x == (uint32_t)l && e.y == (uint32_t)r) return make_int2((int)e.z, (int)e.w);
+    s = (s + 1) & T.pair_mask;
+    e = __ldg(&T.pair_tab[s]);
   }
-  for (int i = 0; i < n; ++i) out[i] = ids[i];
-  return n;
+}
+__device__ __forceinline__ uint32_t pair_slot(const Tables &T, int l, int r) {
+  return (uint32_t)pair_hash((uint32_t)l, (uint32_t)r) & T.pair_mask;
+}
+
+// Round merging of up to 32 / G pieces of at most G bytes at once, G lanes
+// per piece and one symbol per lane: lane p of a group holds the symbol that
+// starts at byte p (while alive), the rank and result of the pair it starts
+// with the next alive lane.  Neighbours come from a ballot of alive lanes.
+// A round: group min of the ranks (r); occurrences of r whose previous alive
+// lane is not itself an occurrence take their merge result and unlink their
+// right neighbour; leftover occurrences (inside runs of (a, a)) repeat with
+// the same r; lanes whose pair changed look it up again.  All 32 lanes take
+// part; a group with len 0 idles.  Writes the group's IDs to out[0..] and
+// returns their count (on every lane of the group).
+template <int G>
+__device__ __forceinline__ int bpe_lanes(const Tables &T, const uint8_t *bytes, int len, int32_t *out) {
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr unsigned GM = G == 32 ? FULL : ((1u << G) - 1);
+  const int lane = threadIdx.x & 31;
+  const int p = lane % G, sh = lane - p;
+  const unsigned below = (1u << p) - 1, above_me = ~((2u << p) - 1);
+  bool alive = p < len;
+  int tok = alive ? __ldg(&T.byte_id[__ldg(bytes + p)]) : -1;
+  const int tn0 = __shfl_down_sync(FULL, tok, 1);
+  int rank = INT_MAX, res = 0;
+  if (p + 1 < len) {
+    const int2 pr = pair_lookup(T, tok, tn0);
+    rank = rank_or_max(pr.x);
+    res = pr.y;
+  }
+  for (int round = 0; round < G; ++round) {   // each round unlinks at least one symbol
+    int r = rank;
+#pragma unroll
+    for (int d = G / 2; d >= 1; d >>= 1) r = min(r, __shfl_xor_sync(FULL, r, d));
+    if (__all_sync(FULL, r == INT_MAX)) break;
+    for (int step = 0; step < G; ++step) {
+      const unsigned am = (__ballot_sync(FULL, alive) >> sh) & GM;
+      const unsigned lo = am & below;
+      const int pvl = lo ? 31 - __clz(lo) : -1;
+      const bool hit = alive && rank == r && r != INT_MAX;
+      const unsigned hm = (__ballot_sync(FULL, hit) >> sh) & GM;
+      const bool sel = hit && !(pvl >= 0 && ((hm >> pvl) & 1u));
+      const unsigned sm = (__ballot_sync(FULL, sel) >> sh) & GM;
+      const bool pending = hit && !sel;
+      if (sel) tok = res;
+      if (alive && pvl >= 0 && ((sm >> pvl) & 1u)) { alive = false; rank = INT_MAX; }
+      const unsigned am2 = (__ballot_sync(FULL, alive) >> sh) & GM;
+      const unsigned hi = am2 & above_me;
+      const int nxl = hi ? __ffs(hi) - 1 : -1;
+      const int tn = __shfl_sync(FULL, tok, sh + (nxl < 0 ? p : nxl));
+      if (alive && (sel || (nxl >= 0 && ((sm >> nxl) & 1u)))) {
+        if (nxl < 0) {
+          rank = INT_MAX;
+        } else {
+          const int2 pr = pair_lookup(T, tok, tn);
+          rank = rank_or_max(pr.x);
+          res = pr.y;
+        }
+      }
+      if (!__any_sync(FULL, pending)) break;
+    }
+  }
+  const unsigned fm = (__ballot_sync(FULL, alive) >> sh) & GM;
+  if (alive) out[__popc(fm & below)] = tok;
+  return __popc(fm);
 }
 
 // ---------------------------------------------------------------- small
-// Thread per piece over the pieces of at most SMALL_MAX bytes (the longer ones
-// were listed by k_pretok and are encoded by k_bpe_mid / k_bpe_long, which
-// may run at the same time on another stream).
+// Pieces of at most SMALL_MAX bytes (the longer ones were listed by k_pretok
+// and are encoded by k_bpe_mid / k_bpe_long, which may run at the same time
+// on another stream).  A thread per piece tries the whole-piece shortcut;
+// the warp then encodes its misses two at a time, 16 lanes per piece.
 __global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work W) {
   const CallArgs A = *W.args;
   if (A.n <= 0) return;
@@ -89,19 +135,46 @@ __global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work 
   if (total > W.cap_bytes || total < 0 || base < 0) return;
   const int np = __ldcg(&W.counters[3]);
   const uint8_t *g = A.utf8 + base;
-  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < np; k += gridDim.x * blockDim.x) {
-    const int32_t s = __ldcg(&W.piece_start[k]);
-    if (s < 0) { W.n_ids[k] = 0; continue; }                         // rejected request
-    const int32_t e = __ldcg(&W.piece_start[k + 1]) & 0x7FFFFFFF;
-    const int len = e - s;
-    if (len <= 0 || e > total) { W.n_ids[k] = 0; set_status(W.status, ST_INVALID_ARG); continue; }
-    if (len > SMALL_MAX) continue;              // listed by k_pretok for k_bpe_mid / k_bpe_long
-    int32_t *out = W.scratch + s;
-    if (len <= T.max_tok_len) {
-      const int id = vocab_probe(T, g + s, len);
-      if (id >= 0) { out[0] = id; W.n_ids[k] = 1; continue; }
+  const int lane = threadIdx.x & 31;
+  const int stride = gridDim.x * blockDim.x;
+  for (int kb = blockIdx.x * blockDim.x + (threadIdx.x & ~31); kb < np; kb += stride) {
+    const int k = kb + lane;
+    int32_t s = 0;
+    int len = 0;
+    bool miss = false;
+    if (k < np) {
+      s = __ldcg(&W.piece_start[k]);
+      if (s < 0) {
+        W.n_ids[k] = 0;                                                  // rejected request
+      } else {
+        const int32_t e = __ldcg(&W.piece_start[k + 1]) & 0x7FFFFFFF;
+        len = e - s;
+        if (len <= 0 || e > total) {
+          W.n_ids[k] = 0;
+          set_status(W.status, ST_INVALID_ARG);
+        } else if (len <= SMALL_MAX) {            // longer: listed by k_pretok for k_bpe_mid / k_bpe_long
+          const int id = len <= T.max_tok_len ? vocab_probe(T, g + s, len) : -1;
+          if (id >= 0) {
+            W.scratch[s] = id;
+            W.n_ids[k] = 1;
+          } else {
+            miss = true;
+          }
+        }
+      }
     }
-    W.n_ids[k] = bpe_thread<SMALL_MAX>(T, g + s, len, out);
+    for (unsigned mm = __ballot_sync(0xffffffffu, miss); mm;) {
+      const int la = __ffs(mm) - 1;
+      mm &= mm - 1;
+      const int lb = mm ? __ffs(mm) - 1 : -1;
+      if (mm) mm &= mm - 1;
+      const int src = lane < 16 ? la : lb;
+      const int ps = __shfl_sync(0xffffffffu, s, src < 0 ? la : src);
+      int pl = __shfl_sync(0xffffffffu, len, src < 0 ? la : src);
+      if (src < 0) pl = 0;
+      const int cnt = bpe_lanes<16>(T, g + ps, pl, W.scratch + ps);
+      if ((lane & 15) == 0 && src >= 0) W.n_ids[kb + src] = cnt;
+    }
   }
 }
 
@@ -120,21 +193,6 @@ __global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work 
 // by a merge rank above r (well-ordered list), so they never join a run.
 constexpr int MID_WARPS = BPE_MID_THREADS / 32;
 constexpr int MID_SLOTS = MID_MAX / 32;
-
-__device__ __forceinline__ int rank_or_max(int r) { return r < 0 ? INT_MAX : r; }
-
-// the rest of a pair lookup whose first probe e (slot s) is already loaded
-__device__ __forceinline__ int2 pair_finish(const Tables &T, uint4 e, uint32_t s, int l, int r) {
-  for (;;) {
-    if (e.x == PAIR_EMPTY) return make_int2(-1, -1);
-    if (e.x == (uint32_t)l && e.y == (uint32_t)r) return make_int2((int)e.z, (int)e.w);
-    s = (s + 1) & T.pair_mask;
-    e = __ldg(&T.pair_tab[s]);
-  }
-}
-__device__ __forceinline__ uint32_t pair_slot(const Tables &T, int l, int r) {
-  return (uint32_t)pair_hash((uint32_t)l, (uint32_t)r) & T.pair_mask;
-}
 
 __global__ void __launch_bounds__(BPE_MID_THREADS, 4) k_bpe_mid(Tables T, Work W) {
   __shared__ int32_t s_tok[MID_WARPS][MID_MAX];   // token, -1 once unlinked
@@ -176,6 +234,11 @@ __global__ void __launch_bounds__(BPE_MID_THREADS, 4) k_bpe_mid(Tables T, Work W
         continue;
       }
     }
+    if (n <= 32) {                              // one symbol per lane, state in registers
+      const int cnt = bpe_lanes<32>(T, b, n, W.scratch + s);
+      if (lane == 0) W.n_ids[pc] = cnt;
+      continue;
+    }
     const int nslot = (n + 31) >> 5;
 #pragma unroll
     for (int k = 0; k < MID_SLOTS; ++k) {
@@ -213,7 +276,7 @@ __global__ void __launch_bounds__(BPE_MID_THREADS, 4) k_bpe_mid(Tables T, Work W
       }
     }
     __syncwarp();
-    for (;;) {
+    for (int round = 0; round < n; ++round) {   // each round unlinks at least one symbol
       int lm = INT_MAX;
 #pragma unroll
       for (int k = 0; k < MID_SLOTS; ++k)
