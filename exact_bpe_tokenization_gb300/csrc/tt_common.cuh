@@ -11,17 +11,16 @@
 namespace tt {
 
 // ------------------------------------------------------------ geometry
-// Pre-tokenizer tiles: one CTA of 256 threads reads a 4096-byte window, one
-// 16-byte vector per thread: 48 bytes before the tile (lookback and the
+// Pre-tokenizer tiles: one CTA reads a 4096-byte window, 8 or 16 bytes (one
+// vector load) per thread: 48 bytes before the tile (lookback and the
 // shifted scan entry points), the 4016-byte tile, 32 bytes after it.
-constexpr int PT_THREADS = 256;
 constexpr int WIN = 4096;
 constexpr int HALO_L = 48;
 constexpr int HALO_R = 32;
 constexpr int TILE = WIN - HALO_L - HALO_R;  // 4016 = 16 * 251
 constexpr int S1_SHIFT = 32;                 // mark-resolution scan enters at tile start - 32
 constexpr int S2_SHIFT = 16;                 // forward scan enters at tile start - 16
-static_assert(TILE % 16 == 0, "tile must keep 16-byte alignment");
+static_assert(TILE % 16 == 0 && HALO_L % 16 == 0, "windows keep 16-byte alignment");
 
 // BPE execution units by piece length (bytes)
 constexpr int SMALL_MAX = 16;                // thread per piece, dense over all pieces

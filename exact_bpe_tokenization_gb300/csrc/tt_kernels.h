@@ -6,7 +6,6 @@
 
 namespace tt {
 
-size_t pretok_smem_bytes();
 cudaError_t pretok_configure();
 void launch_prepass(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_tilescan(const Tables &T, const Work &W, cudaStream_t s);

@@ -27,6 +27,7 @@
 
 namespace tt {
 
+template <int NT>   // threads per window
 struct WinSmem {
   uint8_t bytes[WIN + 8];
   uint8_t rsb[WIN + 8];      // byte starts a request
@@ -35,7 +36,7 @@ struct WinSmem {
   uint8_t eff[WIN];          // effective kind
   uint8_t rs[WIN];           // char starts a request
   uint16_t lead[WIN];        // window index of the char's lead byte
-  int cbase[PT_THREADS + 1]; // chars of thread t: [cbase[t], cbase[t+1])
+  int cbase[NT + 1];         // chars of thread t: [cbase[t], cbase[t+1])
   uint8_t ascii[128];
   int r0, r1;
   int nch;
@@ -50,30 +51,34 @@ __device__ __forceinline__ int64_t lower_bound64(const int64_t *a, int64_t n, in
   return lo;
 }
 
-__device__ __forceinline__ uint8_t kind_of(const Tables &T, const WinSmem &S, uint32_t cp) {
+template <class WS>
+__device__ __forceinline__ uint8_t kind_of(const Tables &T, const WS &S, uint32_t cp) {
   if (cp < 128) return S.ascii[cp];
   return __ldg(&T.cls2[(uint32_t)__ldg(&T.cls1[cp >> 8]) * 256u + (cp & 255u)]);
 }
 
 // Load the window [ws, ws + WIN) of the batch, mark request starts, find
 // char starts, decode and classify.  All threads participate.
+template <int NT>
 __device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, int64_t total, int64_t ws,
-                            WinSmem &S, int *scan_tmp) {
+                            WinSmem<NT> &S, int *scan_tmp) {
+  constexpr int PT_BYTES = WIN / NT;
   const int tid = threadIdx.x;
   const uint8_t *g = A.utf8 + base;
-  const int64_t x0 = ws + 16 * tid;
-  uint8_t *dst = &S.bytes[16 * tid];
-  if (x0 >= 0 && x0 + 16 <= total && ((reinterpret_cast<uintptr_t>(g + x0) & 15) == 0)) {
-    *reinterpret_cast<uint4 *>(dst) = __ldg(reinterpret_cast<const uint4 *>(g + x0));
+  const int64_t x0 = ws + PT_BYTES * tid;
+  uint8_t *dst = &S.bytes[PT_BYTES * tid];
+  if (x0 >= 0 && x0 + PT_BYTES <= total && ((reinterpret_cast<uintptr_t>(g + x0) & (PT_BYTES - 1)) == 0)) {
+    if constexpr (PT_BYTES == 16) *reinterpret_cast<uint4 *>(dst) = __ldg(reinterpret_cast<const uint4 *>(g + x0));
+    else *reinterpret_cast<uint2 *>(dst) = __ldg(reinterpret_cast<const uint2 *>(g + x0));
   } else {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < PT_BYTES; ++k) {
       const int64_t x = x0 + k;
       dst[k] = (x >= 0 && x < total) ? __ldg(g + x) : 0;
     }
   }
 #pragma unroll
-  for (int k = 0; k < 16; ++k) S.rsb[16 * tid + k] = 0;
+  for (int k = 0; k < PT_BYTES; ++k) S.rsb[PT_BYTES * tid + k] = 0;
   if (tid < 8) { S.bytes[WIN + tid] = 0; S.rsb[WIN + tid] = 0; }
   if (tid < 128) S.ascii[tid] = __ldg(&T.cls2[(uint32_t)__ldg(&T.cls1[0]) * 256u + tid]);
   if (tid == 0) {
@@ -83,16 +88,16 @@ __device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, in
     S.r1 = (int)lower_bound64(A.offs, A.n, base + hi);
   }
   __syncthreads();
-  for (int r = S.r0 + tid; r < S.r1; r += PT_THREADS) {
+  for (int r = S.r0 + tid; r < S.r1; r += NT) {
     const int64_t x = __ldg(&A.offs[r]) - base - ws;
     if (x >= 0 && x < WIN && __ldg(&A.offs[r]) - base < total) S.rsb[x] = 1;
   }
   __syncthreads();
-  // char starts among my 16 bytes
+  // char starts among my PT_BYTES bytes
   uint32_t smask = 0;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const int i = 16 * tid + k;
+  for (int k = 0; k < PT_BYTES; ++k) {
+    const int i = PT_BYTES * tid + k;
     const int64_t x = ws + i;
     if (x < 0 || x >= total) continue;
     const uint8_t b = S.bytes[i];
@@ -100,13 +105,13 @@ __device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, in
   }
   const int cnt = __popc(smask);
   int tot;
-  const int cb = block_exclusive_scan<PT_THREADS>(cnt, [](int a, int b) { return a + b; }, 0, scan_tmp, &tot);
+  const int cb = block_exclusive_scan<NT>(cnt, [](int a, int b) { return a + b; }, 0, scan_tmp, &tot);
   S.cbase[tid] = cb;
-  if (tid == PT_THREADS - 1) { S.cbase[PT_THREADS] = tot; S.nch = tot; }
+  if (tid == NT - 1) { S.cbase[NT] = tot; S.nch = tot; }
   int j = cb;
   for (uint32_t m = smask; m; m &= m - 1) {
     const int k = __ffs(m) - 1;
-    const int i = 16 * tid + k;
+    const int i = PT_BYTES * tid + k;
     const uint8_t b0 = S.bytes[i];
     int len;
     uint32_t cp;
@@ -131,11 +136,13 @@ __device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, in
 }
 
 // ---------------------------------------------------------------- k_prepass
-__global__ void __launch_bounds__(PT_THREADS) k_prepass(Tables T, Work W) {
-  __shared__ WinSmem S;
-  __shared__ int scan_tmp[PT_THREADS / 32];
-  __shared__ int2 red2[PT_THREADS / 32];
-  __shared__ int red_rq[PT_THREADS / 32];
+template <int NT>
+__global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
+  constexpr int PT_BYTES = WIN / NT;
+  __shared__ WinSmem<NT> S;
+  __shared__ int scan_tmp[NT / 32];
+  __shared__ int2 red2[NT / 32];
+  __shared__ int red_rq[NT / 32];
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
   if (A.n <= 0) return;
@@ -146,7 +153,7 @@ __global__ void __launch_bounds__(PT_THREADS) k_prepass(Tables T, Work W) {
     return;
   }
   // offsets must be non-decreasing
-  for (int64_t r = (int64_t)blockIdx.x * PT_THREADS + tid; r < A.n; r += (int64_t)gridDim.x * PT_THREADS)
+  for (int64_t r = (int64_t)blockIdx.x * NT + tid; r < A.n; r += (int64_t)gridDim.x * NT)
     if (__ldg(&A.offs[r]) > __ldg(&A.offs[r + 1])) set_status(W.status, ST_INVALID_ARG);
   const int ntiles = (int)((total + TILE - 1) / TILE);
   const int t = blockIdx.x;
@@ -156,8 +163,8 @@ __global__ void __launch_bounds__(PT_THREADS) k_prepass(Tables T, Work W) {
   load_window(T, A, base, total, ws, S, scan_tmp);
 
   // --- UTF-8 validation of the tile's bytes (RFC 3629, per request)
-  for (int k = 0; k < 16; ++k) {
-    const int i = 16 * tid + k;
+  for (int k = 0; k < PT_BYTES; ++k) {
+    const int i = PT_BYTES * tid + k;
     const int64_t x = ws + i;
     if (x < ts || x >= te) continue;
     const uint8_t b = S.bytes[i];
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(PT_THREADS) k_prepass(Tables T, Work W) {
       if (trigger(S.raw[j], rp, cpp, rn)) v.y = (int)pos;
     }
     int2 tot;
-    block_exclusive_scan<PT_THREADS>(v, [](int2 a, int2 b) { return make_int2(max(a.x, b.x), max(a.y, b.y)); },
+    block_exclusive_scan<NT>(v, [](int2 a, int2 b) { return make_int2(max(a.x, b.x), max(a.y, b.y)); },
                                      make_int2(-1, -1), red2, &tot);
     if (tid == 0) W.s1_sum[t] = tot;
   }
@@ -236,7 +243,7 @@ __global__ void __launch_bounds__(PT_THREADS) k_prepass(Tables T, Work W) {
       return lo | (hi << 8);
     };
     int tot;
-    block_exclusive_scan<PT_THREADS>(v, first, 0xFFFF, red_rq, &tot);
+    block_exclusive_scan<NT>(v, first, 0xFFFF, red_rq, &tot);
     if (tid == 0) { W.rq_sum[2 * t] = (uint8_t)(tot & 0xFF); W.rq_sum[2 * t + 1] = (uint8_t)(tot >> 8); }
   }
 }
@@ -296,21 +303,23 @@ __global__ void __launch_bounds__(1024) k_tilescan(Tables T, Work W) {
 }
 
 // ---------------------------------------------------------------- k_pretok
+template <int NT>
 struct PretokSmem {
-  WinSmem w;
+  WinSmem<NT> w;
   uint8_t chain[WIN];
   uint8_t rq8[WIN];          // reverse-query results per tile char: rq_ws | rq_up << 2
-  uint16_t dagg[PT_THREADS][3];  // scan values of chars whose predicate waits for the barrier
-  S2 s2_tmp[PT_THREADS / 32];
-  int2 i2_tmp[PT_THREADS / 32];
-  int i_tmp[PT_THREADS / 32];
+  uint16_t dagg[NT][3];  // scan values of chars whose predicate waits for the barrier
+  S2 s2_tmp[NT / 32];
+  int2 i2_tmp[NT / 32];
+  int i_tmp[NT / 32];
   S2 s2_prefix;
   int tile;
   int piece_base;
   int prev_last;
 };
 
-__device__ __forceinline__ Nbr make_nbr(const WinSmem &S, const uint8_t *chain, int j) {
+template <class WS>
+__device__ __forceinline__ Nbr make_nbr(const WS &S, const uint8_t *chain, int j) {
   Nbr b;
   uint8_t e[5];
   uint32_t c[5];
@@ -346,13 +355,15 @@ __device__ __forceinline__ Nbr make_nbr(const WinSmem &S, const uint8_t *chain, 
 struct Slider {
   Nbr b;
   int32_t pos, p1, p2;   // byte positions of j, j+1, j+2
-  __device__ __forceinline__ void start(const WinSmem &S, int64_t ws, int j) {
+  template <class WS>
+  __device__ __forceinline__ void start(const WS &S, int64_t ws, int j) {
     b = make_nbr(S, nullptr, j);
     pos = (int32_t)(ws + S.lead[j]);
     p1 = j + 1 < S.nch ? (int32_t)(ws + S.lead[j + 1]) : pos + 1;
     p2 = j + 2 < S.nch ? (int32_t)(ws + S.lead[j + 2]) : pos + 2;
   }
-  __device__ __forceinline__ void step(const WinSmem &S, int64_t ws, int j) {   // from j - 1 to j
+  template <class WS>
+  __device__ __forceinline__ void step(const WS &S, int64_t ws, int j) {   // from j - 1 to j
     const bool rsj = S.rs[j] != 0;
     if (rsj) {
       b.e1 = b.e2 = b.e3 = b.e4 = K_NONE;
@@ -376,11 +387,11 @@ struct Slider {
   }
 };
 
-template <int FAM>
-__global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
+template <int FAM, int NT>
+__global__ void __launch_bounds__(NT) k_pretok(Tables T, Work W) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  PretokSmem &P = *reinterpret_cast<PretokSmem *>(smem_raw);
-  WinSmem &S = P.w;
+  PretokSmem<NT> &P = *reinterpret_cast<PretokSmem<NT> *>(smem_raw);
+  WinSmem<NT> &S = P.w;
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
   if (A.n <= 0) return;
@@ -412,7 +423,7 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
       if (trigger(S.raw[j], rp, cpp, rn)) v.y = (int)pos;
     }
     auto mx = [](int2 a, int2 b) { return make_int2(max(a.x, b.x), max(a.y, b.y)); };
-    int2 ex = block_exclusive_scan<PT_THREADS>(v, mx, make_int2(-1, -1), P.i2_tmp, (int2 *)nullptr);
+    int2 ex = block_exclusive_scan<NT>(v, mx, make_int2(-1, -1), P.i2_tmp, (int2 *)nullptr);
     int2 run = mx(W.s1_carry[t], ex);
     for (int j = c0; j < c1; ++j) {
       const int64_t pos = ws + S.lead[j];
@@ -447,7 +458,7 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
       if ((rq_first & 0xFF) == 0xFF && ew != 0xFF) rq_first = (rq_first & 0xFF00) | ew;
       if ((rq_first >> 8) == 0xFF && eu != 0xFF) rq_first = (rq_first & 0x00FF) | (eu << 8);
     }
-    int after = first(block_exclusive_suffix<PT_THREADS>(rq_first, first, 0xFFFF, P.i_tmp, (int *)nullptr),
+    int after = first(block_exclusive_suffix<NT>(rq_first, first, 0xFFFF, P.i_tmp, (int *)nullptr),
                       W.rq_carry[2 * t] | (W.rq_carry[2 * t + 1] << 8));
     for (int j = c1 - 1; j >= c0; --j) {
       const int64_t pos = ws + S.lead[j];
@@ -481,19 +492,19 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
   if (!pub_done) agg_pub = agg_all;
   auto comb = [](const S2 &a, const S2 &b) { return s2_combine(a, b); };
   S2 tile_pub;
-  block_exclusive_scan<PT_THREADS>(agg_pub, comb, s2_identity(), P.s2_tmp, &tile_pub);
+  block_exclusive_scan<NT>(agg_pub, comb, s2_identity(), P.s2_tmp, &tile_pub);
   if (tid < 32) {
     const S2 pre = warp_lookback(t, tile_pub, comb, s2_identity(), W.s2_agg, W.s2_inc, W.s2_flag, W.status,
                                  W.spin_limit);
     if (tid == 0) P.s2_prefix = pre;
   }
-  const S2 my_ex = block_exclusive_scan<PT_THREADS>(agg_all, comb, s2_identity(), P.s2_tmp, (S2 *)nullptr);
+  const S2 my_ex = block_exclusive_scan<NT>(agg_all, comb, s2_identity(), P.s2_tmp, (S2 *)nullptr);
   S2 before = s2_combine(P.s2_prefix, my_ex);   // (P.s2_prefix visible after the scan's barriers)
 
   // --- walk: per-char scan values and the predicate.  o200k chars whose
   // contraction lookback reaches the previous thread's chars wait for the
   // barrier (their chain states are written by that thread in this walk).
-  uint32_t starts = 0, placeholder = 0, deferred = 0;   // bit (j - c0) for my chars (<= 16)
+  uint32_t starts = 0, placeholder = 0, deferred = 0;   // bit (j - c0) for my chars (<= PT_BYTES)
   const bool filter = __ldcg(&W.counters[5]) != 0;
   auto decide = [&](int j, const Nbr &nb, const Aggs &a, int64_t pos) {
     bool st = piece_start(fam, nb, a);
@@ -576,10 +587,10 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
   }
   auto cnt_op = [](int2 a, int2 b) { return make_int2(a.x + b.x, max(a.y, b.y)); };
   int2 tile_agg;
-  const int2 my_cnt = block_exclusive_scan<PT_THREADS>(make_int2(__popc(starts), my_last), cnt_op, make_int2(0, -1),
+  const int2 my_cnt = block_exclusive_scan<NT>(make_int2(__popc(starts), my_last), cnt_op, make_int2(0, -1),
                                                       P.i2_tmp, &tile_agg);
   int tile_first;
-  const int next_after_me = block_exclusive_suffix<PT_THREADS>(my_first, [](int a, int b) { return min(a, b); },
+  const int next_after_me = block_exclusive_suffix<NT>(my_first, [](int a, int b) { return min(a, b); },
                                                                INT_MAX, P.i_tmp, &tile_first);
   if (tid < 32) {
     const int2 pb = warp_lookback(t, tile_agg, cnt_op, make_int2(0, -1), W.cnt_agg, W.cnt_inc, W.cnt_flag, W.status,
@@ -632,22 +643,39 @@ __global__ void __launch_bounds__(PT_THREADS) k_pretok(Tables T, Work W) {
   }
 }
 
-size_t pretok_smem_bytes() { return sizeof(PretokSmem); }
+// Threads per window: 512 (8 bytes each) for workspaces up to
+// PT_NARROW_MAX_BYTES, whose batches leave most SMs idle at 16 bytes a
+// thread; 256 (16 bytes each) above, where the GPU is full either way and
+// fewer threads mean fewer instructions.
+constexpr int64_t PT_NARROW_MAX_BYTES = 4ll << 20;
+static bool pt_narrow(const Work &W) { return W.cap_bytes <= PT_NARROW_MAX_BYTES; }
+
 
 void launch_prepass(const Tables &T, const Work &W, int grid, cudaStream_t s) {
-  k_prepass<<<grid, PT_THREADS, 0, s>>>(T, W);
+  if (pt_narrow(W)) k_prepass<WIN / 8><<<grid, WIN / 8, 0, s>>>(T, W);
+  else k_prepass<WIN / 16><<<grid, WIN / 16, 0, s>>>(T, W);
 }
 void launch_tilescan(const Tables &T, const Work &W, cudaStream_t s) { k_tilescan<<<1, 1024, 0, s>>>(T, W); }
+template <int NT>
+static void launch_pretok_nt(const Tables &T, const Work &W, int grid, cudaStream_t s) {
+  if (T.family == FAM_O200K) k_pretok<FAM_O200K, NT><<<grid, NT, sizeof(PretokSmem<NT>), s>>>(T, W);
+  else k_pretok<FAM_CL100K, NT><<<grid, NT, sizeof(PretokSmem<NT>), s>>>(T, W);
+}
 void launch_pretok(const Tables &T, const Work &W, int grid, cudaStream_t s) {
-  if (T.family == FAM_O200K) k_pretok<FAM_O200K><<<grid, PT_THREADS, sizeof(PretokSmem), s>>>(T, W);
-  else k_pretok<FAM_CL100K><<<grid, PT_THREADS, sizeof(PretokSmem), s>>>(T, W);
+  if (pt_narrow(W)) launch_pretok_nt<WIN / 8>(T, W, grid, s);
+  else launch_pretok_nt<WIN / 16>(T, W, grid, s);
+}
+template <int FAM, int NT>
+static cudaError_t configure_one() {
+  return cudaFuncSetAttribute(k_pretok<FAM, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(PretokSmem<NT>));
 }
 cudaError_t pretok_configure() {
-  cudaError_t e = cudaFuncSetAttribute(k_pretok<FAM_CL100K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)sizeof(PretokSmem));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_pretok<FAM_O200K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sizeof(PretokSmem));
+  cudaError_t e;
+  if ((e = configure_one<FAM_CL100K, WIN / 8>()) != cudaSuccess) return e;
+  if ((e = configure_one<FAM_O200K, WIN / 8>()) != cudaSuccess) return e;
+  if ((e = configure_one<FAM_CL100K, WIN / 16>()) != cudaSuccess) return e;
+  return configure_one<FAM_O200K, WIN / 16>();
 }
 
 }  // namespace tt
