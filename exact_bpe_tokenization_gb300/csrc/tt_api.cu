@@ -201,6 +201,7 @@ extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, con
   tt_status s;
   auto fail = [&](tt_status st) { tt_destroy(h); return st; };
   if (pretok_configure() != cudaSuccess) return fail(TT_ERR_CUDA);
+  if (bpe_configure() != cudaSuccess) return fail(TT_ERR_CUDA);
   // ---- pair table
   const uint64_t pcap = next_pow2((uint64_t)std::max<int64_t>(2 * n_merges, 1024));
   std::vector<uint4> ptab(pcap, make_uint4(PAIR_EMPTY, PAIR_EMPTY, 0xFFFFFFFFu, 0xFFFFFFFFu));

@@ -362,9 +362,127 @@ __device__ __forceinline__ int cached_rank(const Tables &T, int l, int r, int &c
   return cv;
 }
 
+// Pieces of up to LONG_SMEM_MAX bytes run the warp kernel's linked-list
+// rounds with the whole block: the list lives in dynamic shared memory
+// (thread t owns positions t, t + NT, ...), the round minimum is a block
+// reduction, and each merge step costs three barriers and one lookup.
+constexpr int LONG_SMEM_MAX = 8192;
+constexpr size_t LONG_SMEM_BYTES = (size_t)LONG_SMEM_MAX * (4 + 4 + 4 + 2 + 2);
+static_assert(LONG_SMEM_MAX / BPE_LONG_THREADS <= 32, "slot mask is 32 bits");
+
+__device__ void bpe_block_list(const Tables &T, const uint8_t *b, int n, int32_t *out, int *n_out,
+                               unsigned char *dsm, int *red) {
+  constexpr int NT = BPE_LONG_THREADS;
+  const int tid = threadIdx.x, lane = tid & 31;
+  int32_t *tok = reinterpret_cast<int32_t *>(dsm);
+  int32_t *rank = tok + LONG_SMEM_MAX;
+  int32_t *res = rank + LONG_SMEM_MAX;
+  int16_t *nx = reinterpret_cast<int16_t *>(res + LONG_SMEM_MAX);
+  int16_t *pv = nx + LONG_SMEM_MAX;
+  const int nslot = (n + NT - 1) / NT;
+  for (int k = 0; k < nslot; ++k) {
+    const int p = tid + NT * k;
+    tok[p] = p < n ? __ldg(&T.byte_id[__ldg(b + p)]) : -1;
+    rank[p] = INT_MAX;
+    nx[p] = (int16_t)(p + 1);
+    pv[p] = (int16_t)(p - 1);
+  }
+  __syncthreads();
+  for (int k0 = 0; k0 < nslot; k0 += 4) {
+    uint4 ent[4];
+    uint32_t sl[4];
+    int lt[4], rt[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int p = tid + NT * (k0 + j);
+      const bool v = k0 + j < nslot && p + 1 < n;
+      lt[j] = v ? tok[p] : 0;
+      rt[j] = v ? tok[p + 1] : 0;
+      sl[j] = pair_slot(T, lt[j], rt[j]);
+      ent[j] = v ? __ldg(&T.pair_tab[sl[j]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int p = tid + NT * (k0 + j);
+      if (k0 + j < nslot && p + 1 < n) {
+        const int2 pr = pair_finish(T, ent[j], sl[j], lt[j], rt[j]);
+        rank[p] = rank_or_max(pr.x);
+        res[p] = pr.y;
+      }
+    }
+  }
+  __syncthreads();
+  for (int round = 0; round < n; ++round) {       // each round unlinks at least one symbol
+    int lm = INT_MAX;
+    for (int k = 0; k < nslot; ++k) lm = min(lm, rank[tid + NT * k]);
+    lm = __reduce_min_sync(0xffffffffu, lm);
+    if (lane == 0) red[tid >> 5] = lm;
+    __syncthreads();
+    const int r = __reduce_min_sync(0xffffffffu, lane < NT / 32 ? red[lane] : INT_MAX);
+    if (r == INT_MAX) break;
+    for (int step = 0; step < n; ++step) {
+      uint32_t sel = 0;
+      bool pending = false;
+      for (int k = 0; k < nslot; ++k) {
+        const int p = tid + NT * k;
+        if (rank[p] == r) {
+          const int q = pv[p];
+          if (q < 0 || rank[q] != r) sel |= 1u << k;
+          else pending = true;
+        }
+      }
+      __syncthreads();
+      for (uint32_t m = sel; m; m &= m - 1) {
+        const int p = tid + NT * (__ffs(m) - 1);
+        const int q = nx[p], nq = nx[q];
+        tok[p] = res[p];
+        tok[q] = -1;
+        rank[q] = INT_MAX;
+        rank[p] = INT_MAX;
+        nx[p] = (int16_t)nq;
+        if (nq < n) pv[nq] = (int16_t)p;
+      }
+      __syncthreads();
+      for (uint32_t m = sel; m; m &= m - 1) {
+        const int p = tid + NT * (__ffs(m) - 1);
+        const int a = pv[p], c = nx[p];
+        const int tp = tok[p];
+        const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
+        const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
+        const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+        const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+        if (a >= 0) {
+          const int2 pr = pair_finish(T, ea, sa, ta, tp);
+          rank[a] = rank_or_max(pr.x);
+          res[a] = pr.y;
+        }
+        if (c < n) {
+          const int2 pr = pair_finish(T, ec, sc, tp, tc);
+          rank[p] = rank_or_max(pr.x);
+          res[p] = pr.y;
+        }
+      }
+      if (!__syncthreads_or(pending)) break;
+    }
+  }
+  __syncthreads();   // every thread has read red[] before it is reused below
+  // surviving tokens in position order: thread t compacts positions [t*seg, (t+1)*seg)
+  const int seg = (n + NT - 1) / NT;
+  const int lo = min(tid * seg, n), hi = min(lo + seg, n);
+  int cnt = 0;
+  for (int p = lo; p < hi; ++p) cnt += tok[p] >= 0;
+  int tot;
+  int w = block_exclusive_scan<NT>(cnt, [](int x, int y) { return x + y; }, 0, red, &tot);
+  for (int p = lo; p < hi; ++p)
+    if (tok[p] >= 0) out[w++] = tok[p];
+  if (tid == 0) *n_out = tot;
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(BPE_LONG_THREADS) k_bpe_long(Tables T, Work W) {
   constexpr int NT = BPE_LONG_THREADS;
   constexpr int32_t MERGED = (int32_t)0x80000000;
+  extern __shared__ __align__(16) unsigned char dsm[];
   __shared__ int red[NT / 32];
   __shared__ int s_whole;
   const CallArgs A = *W.args;
@@ -394,6 +512,10 @@ __global__ void __launch_bounds__(BPE_LONG_THREADS) k_bpe_long(Tables T, Work W)
         if (tid == 0) { W.scratch[s] = whole; W.n_ids[k] = 1; }
         continue;
       }
+    }
+    if (len <= LONG_SMEM_MAX) {
+      bpe_block_list(T, b, len, W.scratch + s, &W.n_ids[k], dsm, red);
+      continue;
     }
     int32_t *cur = W.scratch + s, *nxt = W.tmp_b + s;
     int32_t *rcur = W.tmp_a + s, *rnxt = W.tmp_c + s;
@@ -654,12 +776,16 @@ void launch_bpe_mid(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   k_bpe_mid<<<grid, BPE_MID_THREADS, 0, s>>>(T, W);
 }
 void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s) {
-  k_bpe_long<<<grid, BPE_LONG_THREADS, 0, s>>>(T, W);
+  k_bpe_long<<<grid, BPE_LONG_THREADS, LONG_SMEM_BYTES, s>>>(T, W);
 }
 void launch_ids(const Tables &T, const Work &W, int grid, cudaStream_t s) { k_ids<<<grid, IDS_THREADS, 0, s>>>(T, W); }
 void launch_req(const Tables &T, const Work &W, int grid, cudaStream_t s) { k_req<<<grid, 256, 0, s>>>(T, W); }
 void launch_hook_pre(const Work &W, cudaStream_t s) { k_hook_pre<<<1, 1024, 0, s>>>(W); }
 void launch_hook_pieces(const Work &W, int grid, cudaStream_t s) { k_hook_pieces<<<grid, 256, 0, s>>>(W); }
 void launch_hook_offsets(const Work &W, int grid, cudaStream_t s) { k_hook_offsets<<<grid, 256, 0, s>>>(W); }
+
+cudaError_t bpe_configure() {
+  return cudaFuncSetAttribute(k_bpe_long, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LONG_SMEM_BYTES);
+}
 
 }  // namespace tt
