@@ -161,7 +161,7 @@ def alg_bytes(kernel, c):
         return a["bytes"]                                     # the batch bytes, read once
     if kernel == "k_pretok":
         return a["bytes"] + 4 * a["pieces"]                   # bytes in, int32 piece starts out
-    cls = {"k_bpe_small": ["small"], "k_bpe_mid": ["mid"], "k_bpe_long": ["long"]}.get(kernel)
+    cls = {"k_bpe_warp": ["small", "mid"], "k_bpe_long": ["long"]}.get(kernel)
     if cls:
         p = sum(c[k]["pieces"] for k in cls)
         return sum(c[k]["bytes"] + 4 * c[k]["tokens"] for k in cls) + 12 * p   # bytes + starts in, IDs + count out

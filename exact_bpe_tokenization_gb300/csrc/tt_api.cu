@@ -31,9 +31,9 @@ using namespace tt;
 
 namespace {
 
-constexpr int N_KERNELS = 8;
-const char *KERNEL_NAMES[N_KERNELS] = {"k_prepass", "k_tilescan", "k_pretok", "k_bpe_small",
-                                       "k_bpe_mid", "k_bpe_long", "k_ids", "k_req"};
+constexpr int N_KERNELS = 7;
+const char *KERNEL_NAMES[N_KERNELS] = {"k_prepass", "k_tilescan", "k_pretok", "k_bpe_warp",
+                                       "k_bpe_long", "k_ids", "k_req"};
 
 struct Workspace {
   Work W{};
@@ -42,9 +42,8 @@ struct Workspace {
   int64_t cap_bytes = 0, cap_reqs = 0;
   cudaGraphExec_t graph = nullptr;
   cudaStream_t cap_stream = nullptr;   // private stream the graph is captured on
-  cudaStream_t side = nullptr;         // second branch: warp BPE of the listed mid-length pieces
-  cudaStream_t side2 = nullptr;        // third branch: block BPE of the listed huge pieces
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_join2 = nullptr;
+  cudaStream_t side = nullptr;         // second branch: block BPE of the listed huge pieces
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // device staging for tt_encode_host (bytes, offsets, ids, id offsets)
   void *stage = nullptr;
   size_t stage_bytes = 0;
@@ -202,8 +201,9 @@ extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, con
   auto fail = [&](tt_status st) { tt_destroy(h); return st; };
   if (pretok_configure() != cudaSuccess) return fail(TT_ERR_CUDA);
   if (bpe_configure() != cudaSuccess) return fail(TT_ERR_CUDA);
-  // ---- pair table
-  const uint64_t pcap = next_pow2((uint64_t)std::max<int64_t>(2 * n_merges, 1024));
+  // ---- pair table: load factor <= 1/8, so that the lookups of pairs that
+  // are not merges (most of them) end after about one probe
+  const uint64_t pcap = next_pow2((uint64_t)std::max<int64_t>(8 * n_merges, 1024));
   std::vector<uint4> ptab(pcap, make_uint4(PAIR_EMPTY, PAIR_EMPTY, 0xFFFFFFFFu, 0xFFFFFFFFu));
   for (int64_t k = 0; k < n_merges; ++k) {
     const uint32_t l = (uint32_t)merge_pairs[2 * k], r = (uint32_t)merge_pairs[2 * k + 1];
@@ -255,8 +255,6 @@ static void free_workspace(Workspace *w) {
   if (w->graph) cudaGraphExecDestroy(w->graph);
   if (w->cap_stream) cudaStreamDestroy(w->cap_stream);
   if (w->side) cudaStreamDestroy(w->side);
-  if (w->side2) cudaStreamDestroy(w->side2);
-  if (w->ev_join2) cudaEventDestroy(w->ev_join2);
   if (w->ev_fork) cudaEventDestroy(w->ev_fork);
   if (w->ev_join) cudaEventDestroy(w->ev_join);
   if (w->mem) cudaFree(w->mem);
@@ -365,23 +363,26 @@ static int grid_chunks(const Workspace *w) {   // persistent CTAs taking chunk t
   return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 4);
 }
 static int grid_reqs(const Workspace *w) { return (int)((w->cap_reqs + 1 + 255) / 256); }
-static int grid_small(const Workspace *w) {
-  const int64_t g = (w->cap_bytes / 4 + BPE_SMALL_THREADS - 1) / BPE_SMALL_THREADS;
+static int grid_pieces(const Workspace *w) {   // a thread per piece (test hook)
+  const int64_t g = (w->cap_bytes / 4 + 255) / 256;
   return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 8);
 }
-static int grid_mid(const Workspace *w) {   // persistent warps taking tickets
-  const int64_t g = (w->cap_bytes / (SMALL_MAX + 1) + (BPE_MID_THREADS / 32) - 1) / (BPE_MID_THREADS / 32);
-  return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 4);
+// persistent warps taking tickets: all resident at once, fewer for small
+// workspaces
+static int64_t warp_grid(int64_t cap_bytes) {
+  const int64_t warps = cap_bytes / 128 + 1;   // about one ticket per 128 bytes
+  const int64_t g = (warps + BPE_WARP_THREADS / 32 - 1) / (BPE_WARP_THREADS / 32);
+  return std::min<int64_t>(std::max<int64_t>(g, 1), 152 * BPE_WARP_CTAS_PER_SM);
 }
+static int grid_warp(const Workspace *w) { return (int)warp_grid(w->cap_bytes); }
 static int grid_long(const Workspace *w) {
   return (int)std::min<int64_t>(std::max<int64_t>(w->cap_bytes / (MID_MAX + 1), 1), 152 * 2);
 }
 
 // Enqueue the kernels of one encode on `stream`.  Untimed, the BPE of the
-// listed mid-length pieces (k_bpe_mid) and of the huge pieces (k_bpe_long)
-// run on two more streams beside the short pieces (k_bpe_small), forked
-// after k_pretok and joined before k_ids; under capture these become three
-// parallel graph branches.  Timed
+// huge pieces (k_bpe_long) runs on a second stream beside the warp kernel
+// (k_bpe_warp, every other piece), forked after k_pretok and joined before
+// k_ids; under capture these become two parallel graph branches.  Timed
 // (profiling), every kernel runs in turn on `stream` between events.
 static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stream, bool timed) {
   const Tables &T = h->T;
@@ -390,23 +391,17 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
   TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)w->cap_reqs + 1, stream));
   if (!timed) {
     if (!w->side) TT_CUDA(cudaStreamCreateWithFlags(&w->side, cudaStreamNonBlocking));
-    if (!w->side2) TT_CUDA(cudaStreamCreateWithFlags(&w->side2, cudaStreamNonBlocking));
     if (!w->ev_fork) TT_CUDA(cudaEventCreateWithFlags(&w->ev_fork, cudaEventDisableTiming));
     if (!w->ev_join) TT_CUDA(cudaEventCreateWithFlags(&w->ev_join, cudaEventDisableTiming));
-    if (!w->ev_join2) TT_CUDA(cudaEventCreateWithFlags(&w->ev_join2, cudaEventDisableTiming));
     launch_prepass(T, W, grid_tiles(w), stream);
     launch_tilescan(T, W, stream);
     launch_pretok(T, W, grid_tiles(w), stream);
     TT_CUDA(cudaEventRecord(w->ev_fork, stream));
     TT_CUDA(cudaStreamWaitEvent(w->side, w->ev_fork, 0));
-    TT_CUDA(cudaStreamWaitEvent(w->side2, w->ev_fork, 0));
-    launch_bpe_mid(T, W, grid_mid(w), w->side);
+    launch_bpe_long(T, W, grid_long(w), w->side);
     TT_CUDA(cudaEventRecord(w->ev_join, w->side));
-    launch_bpe_long(T, W, grid_long(w), w->side2);
-    TT_CUDA(cudaEventRecord(w->ev_join2, w->side2));
-    launch_bpe_small(T, W, grid_small(w), stream);
+    launch_bpe_warp(T, W, grid_warp(w), stream);
     TT_CUDA(cudaStreamWaitEvent(stream, w->ev_join, 0));
-    TT_CUDA(cudaStreamWaitEvent(stream, w->ev_join2, 0));
     launch_ids(T, W, grid_chunks(w), stream);
     launch_req(T, W, grid_reqs(w), stream);
     TT_CUDA(cudaGetLastError());
@@ -420,11 +415,10 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
       case 0: launch_prepass(T, W, grid_tiles(w), stream); break;
       case 1: launch_tilescan(T, W, stream); break;
       case 2: launch_pretok(T, W, grid_tiles(w), stream); break;
-      case 3: launch_bpe_small(T, W, grid_small(w), stream); break;
-      case 4: launch_bpe_mid(T, W, grid_mid(w), stream); break;
-      case 5: launch_bpe_long(T, W, grid_long(w), stream); break;
-      case 6: launch_ids(T, W, grid_chunks(w), stream); break;
-      case 7: launch_req(T, W, grid_reqs(w), stream); break;
+      case 3: launch_bpe_warp(T, W, grid_warp(w), stream); break;
+      case 4: launch_bpe_long(T, W, grid_long(w), stream); break;
+      case 5: launch_ids(T, W, grid_chunks(w), stream); break;
+      case 6: launch_req(T, W, grid_reqs(w), stream); break;
     }
     cudaEventRecord(b, stream);
     h->pending.push_back({kidx, a, b});
@@ -587,7 +581,7 @@ extern "C" tt_status tt_pretokenize_batch(tt_tokenizer *h, const uint8_t *d_utf8
   launch_tilescan(h->T, W, stream);
   launch_pretok(h->T, W, grid_tiles(w), stream);
   launch_hook_pre(W, stream);
-  launch_hook_pieces(W, grid_small(w), stream);
+  launch_hook_pieces(W, grid_pieces(w), stream);
   launch_hook_offsets(W, grid_reqs(w), stream);
   TT_CUDA(cudaGetLastError());
   h->launches += 6;
@@ -756,18 +750,14 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)NA_REQS + 1, stream));
   const Tables &T = h->T;
   const int g_tiles = (int)((NA_BYTES + TILE - 1) / TILE);
-  const int g_small = (int)std::min<int64_t>(std::max<int64_t>((NA_BYTES / 4 + BPE_SMALL_THREADS - 1) / BPE_SMALL_THREADS, 1),
-                                             152 * 8);
-  const int g_mid = (int)std::min<int64_t>(
-      std::max<int64_t>((NA_BYTES / (SMALL_MAX + 1) + (BPE_MID_THREADS / 32) - 1) / (BPE_MID_THREADS / 32), 1), 152 * 4);
+  const int g_warp = (int)warp_grid(NA_BYTES);
   const int g_long = (int)std::min<int64_t>(std::max<int64_t>(NA_BYTES / (MID_MAX + 1), 1), 152 * 2);
   const int g_chunks = (int)((NA_BYTES + 1 + IDS_CHUNK - 1) / IDS_CHUNK);
   const int g_reqs = (int)((NA_REQS + 1 + 255) / 256);
   launch_prepass(T, W, g_tiles, stream);
   launch_tilescan(T, W, stream);
   launch_pretok(T, W, g_tiles, stream);
-  launch_bpe_small(T, W, g_small, stream);
-  launch_bpe_mid(T, W, g_mid, stream);
+  launch_bpe_warp(T, W, g_warp, stream);
   launch_bpe_long(T, W, g_long, stream);
   launch_ids(T, W, g_chunks, stream);
   launch_req(T, W, g_reqs, stream);

@@ -122,67 +122,17 @@ __device__ __forceinline__ int bpe_lanes(const Tables &T, const uint8_t *bytes, 
   return __popc(fm);
 }
 
-// ---------------------------------------------------------------- small
-// Pieces of at most SMALL_MAX bytes (the longer ones were listed by k_pretok
-// and are encoded by k_bpe_mid / k_bpe_long, which may run at the same time
-// on another stream).  A thread per piece tries the whole-piece shortcut;
-// the warp then encodes its misses two at a time, 16 lanes per piece.
-__global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work W) {
-  const CallArgs A = *W.args;
-  if (A.n <= 0) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) return;
-  const int np = __ldcg(&W.counters[3]);
-  const uint8_t *g = A.utf8 + base;
-  const int lane = threadIdx.x & 31;
-  const int stride = gridDim.x * blockDim.x;
-  for (int kb = blockIdx.x * blockDim.x + (threadIdx.x & ~31); kb < np; kb += stride) {
-    const int k = kb + lane;
-    int32_t s = 0;
-    int len = 0;
-    bool miss = false;
-    if (k < np) {
-      s = __ldcg(&W.piece_start[k]);
-      if (s < 0) {
-        W.n_ids[k] = 0;                                                  // rejected request
-      } else {
-        const int32_t e = __ldcg(&W.piece_start[k + 1]) & 0x7FFFFFFF;
-        len = e - s;
-        if (len <= 0 || e > total) {
-          W.n_ids[k] = 0;
-          set_status(W.status, ST_INVALID_ARG);
-        } else if (len <= SMALL_MAX) {            // longer: listed by k_pretok for k_bpe_mid / k_bpe_long
-          const int id = len <= T.max_tok_len ? vocab_probe(T, g + s, len) : -1;
-          if (id >= 0) {
-            W.scratch[s] = id;
-            W.n_ids[k] = 1;
-          } else {
-            miss = true;
-          }
-        }
-      }
-    }
-    for (unsigned mm = __ballot_sync(0xffffffffu, miss); mm;) {
-      const int la = __ffs(mm) - 1;
-      mm &= mm - 1;
-      const int lb = mm ? __ffs(mm) - 1 : -1;
-      if (mm) mm &= mm - 1;
-      const int src = lane < 16 ? la : lb;
-      const int ps = __shfl_sync(0xffffffffu, s, src < 0 ? la : src);
-      int pl = __shfl_sync(0xffffffffu, len, src < 0 ? la : src);
-      if (src < 0) pl = 0;
-      const int cnt = bpe_lanes<16>(T, g + ps, pl, W.scratch + ps);
-      if ((lane & 15) == 0 && src >= 0) W.n_ids[kb + src] = cnt;
-    }
-  }
-}
-
-// ---------------------------------------------------------------- mid
-// Warp per piece over the pieces of SMALL_MAX+1 .. MID_MAX bytes, listed by
-// k_pretok in three length buckets; warps take pieces one at a time through
-// an atomic ticket, longest bucket first.  Symbols never move: the piece is
-// a doubly linked list over fixed positions in shared memory (lane l owns
+// ---------------------------------------------------------------- warp kernel
+// Every piece of at most MID_MAX bytes, in one persistent kernel whose warps
+// take tickets from one counter, the longest work first: the pieces of
+// SMALL_MAX+1 .. MID_MAX bytes that k_pretok listed in three length buckets
+// (a warp per piece), then chunks of 32 consecutive pieces, where each lane
+// tries the whole-piece shortcut for its piece of at most SMALL_MAX bytes and
+// the warp merges the misses two at a time, 16 lanes per piece.  Longer
+// pieces are left to k_bpe_long, which runs beside this kernel.
+//
+// A listed piece of at most 32 bytes runs bpe_lanes<32>; a longer one is a
+// doubly linked list over fixed positions in shared memory (lane l owns
 // positions l, l + 32, ...), each alive position holding its token and the
 // rank and result of the pair it starts.  A round: warp min of the ranks
 // (r); every occurrence of r whose predecessor is not itself an occurrence
@@ -191,159 +141,212 @@ __global__ void __launch_bounds__(BPE_SMALL_THREADS) k_bpe_small(Tables T, Work 
 // (a, a) -- repeat that step with the same r, which takes every other member
 // of a run from its left end: the leftmost non-overlapping set.  Pairs made
 // by a merge rank above r (well-ordered list), so they never join a run.
-constexpr int MID_WARPS = BPE_MID_THREADS / 32;
+constexpr int WARP_KERNEL_WARPS = BPE_WARP_THREADS / 32;
 constexpr int MID_SLOTS = MID_MAX / 32;
+constexpr int SMALL_CHUNK = 32;   // pieces per small-piece ticket
 
-__global__ void __launch_bounds__(BPE_MID_THREADS, 4) k_bpe_mid(Tables T, Work W) {
-  __shared__ int32_t s_tok[MID_WARPS][MID_MAX];   // token, -1 once unlinked
-  __shared__ int32_t s_rank[MID_WARPS][MID_MAX];  // rank of (p, next), INT_MAX if none
-  __shared__ int32_t s_res[MID_WARPS][MID_MAX];   // its merge result
-  __shared__ int16_t s_nx[MID_WARPS][MID_MAX];
-  __shared__ int16_t s_pv[MID_WARPS][MID_MAX];
+__device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, const uint8_t *g, int64_t total,
+                                            int np, int kb) {
+  const int lane = threadIdx.x & 31;
+  const int k = kb + lane;
+  int32_t s = 0;
+  int len = 0;
+  bool miss = false;
+  if (k < np) {
+    s = __ldcg(&W.piece_start[k]);
+    if (s < 0) {
+      W.n_ids[k] = 0;                                                  // rejected request
+    } else {
+      const int32_t e = __ldcg(&W.piece_start[k + 1]) & 0x7FFFFFFF;
+      len = e - s;
+      if (len <= 0 || e > total) {
+        W.n_ids[k] = 0;
+        set_status(W.status, ST_INVALID_ARG);
+      } else if (len <= SMALL_MAX) {            // longer: listed by k_pretok
+        const int id = len <= T.max_tok_len ? vocab_probe(T, g + s, len) : -1;
+        if (id >= 0) {
+          W.scratch[s] = id;
+          W.n_ids[k] = 1;
+        } else {
+          miss = true;
+        }
+      }
+    }
+  }
+  for (unsigned mm = __ballot_sync(0xffffffffu, miss); mm;) {
+    const int la = __ffs(mm) - 1;
+    mm &= mm - 1;
+    const int lb = mm ? __ffs(mm) - 1 : -1;
+    if (mm) mm &= mm - 1;
+    const int src = lane < 16 ? la : lb;
+    const int ps = __shfl_sync(0xffffffffu, s, src < 0 ? la : src);
+    int pl = __shfl_sync(0xffffffffu, len, src < 0 ? la : src);
+    if (src < 0) pl = 0;
+    const int cnt = bpe_lanes<16>(T, g + ps, pl, W.scratch + ps);
+    if ((lane & 15) == 0 && src >= 0) W.n_ids[kb + src] = cnt;
+  }
+}
+
+__device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const uint8_t *g, int pc, int32_t *tok,
+                                          int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1;
+  const int32_t s = __ldcg(&W.piece_start[pc]);
+  const int32_t e = __ldcg(&W.piece_start[pc + 1]) & 0x7FFFFFFF;
+  const int n = e - s;
+  const uint8_t *b = g + s;
+  if (n <= T.max_tok_len) {
+    int id = 0;
+    if (lane == 0) id = vocab_probe(T, b, n);
+    id = __shfl_sync(0xffffffffu, id, 0);
+    if (id >= 0) {
+      if (lane == 0) { W.scratch[s] = id; W.n_ids[pc] = 1; }
+      return;
+    }
+  }
+  if (n <= 32) {                              // one symbol per lane, state in registers
+    const int cnt = bpe_lanes<32>(T, b, n, W.scratch + s);
+    if (lane == 0) W.n_ids[pc] = cnt;
+    return;
+  }
+  const int nslot = (n + 31) >> 5;
+#pragma unroll
+  for (int k = 0; k < MID_SLOTS; ++k) {
+    const int p = lane + 32 * k;
+    if (k < nslot) {
+      tok[p] = p < n ? __ldg(&T.byte_id[__ldg(b + p)]) : -1;
+      rank[p] = INT_MAX;
+      nx[p] = (int16_t)(p + 1);
+      pv[p] = (int16_t)(p - 1);
+    }
+  }
+  __syncwarp();
+  // initial pair lookups, first probes of four slots in flight together
+  for (int k0 = 0; k0 < nslot; k0 += 4) {
+    uint4 ent[4];
+    uint32_t sl[4];
+    int lt[4], rt[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int p = lane + 32 * (k0 + j);
+      const bool v = k0 + j < nslot && p + 1 < n;
+      lt[j] = v ? tok[p] : 0;
+      rt[j] = v ? tok[p + 1] : 0;
+      sl[j] = pair_slot(T, lt[j], rt[j]);
+      ent[j] = v ? __ldg(&T.pair_tab[sl[j]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int p = lane + 32 * (k0 + j);
+      if (k0 + j < nslot && p + 1 < n) {
+        const int2 pr = pair_finish(T, ent[j], sl[j], lt[j], rt[j]);
+        rank[p] = rank_or_max(pr.x);
+        res[p] = pr.y;
+      }
+    }
+  }
+  __syncwarp();
+  for (int round = 0; round < n; ++round) {   // each round unlinks at least one symbol
+    int lm = INT_MAX;
+#pragma unroll
+    for (int k = 0; k < MID_SLOTS; ++k)
+      if (k < nslot) lm = min(lm, rank[lane + 32 * k]);
+    const int r = __reduce_min_sync(0xffffffffu, lm);
+    if (r == INT_MAX) break;
+    for (int step = 0; step < n; ++step) {
+      uint32_t sel = 0;
+      bool left = false;
+#pragma unroll
+      for (int k = 0; k < MID_SLOTS; ++k) {
+        const int p = lane + 32 * k;
+        if (k < nslot && rank[p] == r) {
+          const int q = pv[p];
+          if (q < 0 || rank[q] != r) sel |= 1u << k;
+          else left = true;
+        }
+      }
+      __syncwarp();
+      for (uint32_t m = sel; m; m &= m - 1) {
+        const int p = lane + 32 * (__ffs(m) - 1);
+        const int q = nx[p], nq = nx[q];
+        tok[p] = res[p];
+        tok[q] = -1;
+        rank[q] = INT_MAX;
+        rank[p] = INT_MAX;
+        nx[p] = (int16_t)nq;
+        if (nq < n) pv[nq] = (int16_t)p;
+      }
+      __syncwarp();
+      for (uint32_t m = sel; m; m &= m - 1) {
+        const int p = lane + 32 * (__ffs(m) - 1);
+        const int a = pv[p], c = nx[p];
+        const int tp = tok[p];
+        const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
+        const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
+        const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+        const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+        if (a >= 0) {
+          const int2 pr = pair_finish(T, ea, sa, ta, tp);
+          rank[a] = rank_or_max(pr.x);
+          res[a] = pr.y;
+        }
+        if (c < n) {
+          const int2 pr = pair_finish(T, ec, sc, tp, tc);
+          rank[p] = rank_or_max(pr.x);
+          res[p] = pr.y;
+        }
+      }
+      __syncwarp();
+      if (!__any_sync(0xffffffffu, left)) break;
+    }
+  }
+  // surviving tokens in position order
+  int cnt = 0;
+#pragma unroll
+  for (int k = 0; k < MID_SLOTS; ++k) {
+    if (k < nslot) {
+      const int p = lane + 32 * k;
+      const int t = tok[p];
+      const unsigned bal = __ballot_sync(0xffffffffu, t >= 0);
+      if (t >= 0) W.scratch[s + cnt + __popc(bal & lt_mask)] = t;
+      cnt += __popc(bal);
+    }
+  }
+  if (lane == 0) W.n_ids[pc] = cnt;
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_warp(Tables T, Work W) {
+  __shared__ int32_t s_tok[WARP_KERNEL_WARPS][MID_MAX];   // token, -1 once unlinked
+  __shared__ int32_t s_rank[WARP_KERNEL_WARPS][MID_MAX];  // rank of (p, next), INT_MAX if none
+  __shared__ int32_t s_res[WARP_KERNEL_WARPS][MID_MAX];   // its merge result
+  __shared__ int16_t s_nx[WARP_KERNEL_WARPS][MID_MAX];
+  __shared__ int16_t s_pv[WARP_KERNEL_WARPS][MID_MAX];
   const CallArgs A = *W.args;
   if (A.n <= 0) return;
   const int64_t base = __ldg(&A.offs[0]);
   const int64_t total = __ldg(&A.offs[A.n]) - base;
   if (total > W.cap_bytes || total < 0 || base < 0) return;
+  const int np = __ldcg(&W.counters[3]);
   const int c0 = __ldcg(&W.counters[mid_bucket_counter(0)]), c1 = __ldcg(&W.counters[mid_bucket_counter(1)]);
   const int c2 = __ldcg(&W.counters[mid_bucket_counter(2)]);
+  const int nmid = c0 + c1 + c2;
+  const int nwork = nmid + (np + SMALL_CHUNK - 1) / SMALL_CHUNK;
   const int64_t lcap = list_cap(W.cap_bytes);
   const uint8_t *g = A.utf8 + base;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned lt_mask = (1u << lane) - 1;
-  int32_t *tok = s_tok[warp], *rank = s_rank[warp], *res = s_res[warp];
-  int16_t *nx = s_nx[warp], *pv = s_pv[warp];
   for (;;) {
-    // dynamic assignment, longest bucket first
     int gi = 0;
     if (lane == 0) gi = atomicAdd(&W.counters[9], 1);
     gi = __shfl_sync(0xffffffffu, gi, 0);
-    if (gi >= c0 + c1 + c2) break;
-    const int64_t slot = gi < c0 ? gi : gi < c0 + c1 ? lcap + (gi - c0) : 2 * lcap + (gi - c0 - c1);
-    const int pc = __ldcg(&W.long_list[slot]);
-    const int32_t s = __ldcg(&W.piece_start[pc]);
-    const int32_t e = __ldcg(&W.piece_start[pc + 1]) & 0x7FFFFFFF;
-    const int n = e - s;
-    const uint8_t *b = g + s;
-    if (n <= T.max_tok_len) {
-      int id = 0;
-      if (lane == 0) id = vocab_probe(T, b, n);
-      id = __shfl_sync(0xffffffffu, id, 0);
-      if (id >= 0) {
-        if (lane == 0) { W.scratch[s] = id; W.n_ids[pc] = 1; }
-        continue;
-      }
+    if (gi >= nwork) break;
+    if (gi < nmid) {
+      const int64_t slot = gi < c0 ? gi : gi < c0 + c1 ? lcap + (gi - c0) : 2 * lcap + (gi - c0 - c1);
+      mid_piece(T, W, g, __ldcg(&W.long_list[slot]), s_tok[warp], s_rank[warp], s_res[warp], s_nx[warp],
+                s_pv[warp]);
+    } else {
+      small_chunk(T, W, g, total, np, (gi - nmid) * SMALL_CHUNK);
     }
-    if (n <= 32) {                              // one symbol per lane, state in registers
-      const int cnt = bpe_lanes<32>(T, b, n, W.scratch + s);
-      if (lane == 0) W.n_ids[pc] = cnt;
-      continue;
-    }
-    const int nslot = (n + 31) >> 5;
-#pragma unroll
-    for (int k = 0; k < MID_SLOTS; ++k) {
-      const int p = lane + 32 * k;
-      if (k < nslot) {
-        tok[p] = p < n ? __ldg(&T.byte_id[__ldg(b + p)]) : -1;
-        rank[p] = INT_MAX;
-        nx[p] = (int16_t)(p + 1);
-        pv[p] = (int16_t)(p - 1);
-      }
-    }
-    __syncwarp();
-    // initial pair lookups, first probes of four slots in flight together
-    for (int k0 = 0; k0 < nslot; k0 += 4) {
-      uint4 ent[4];
-      uint32_t sl[4];
-      int lt[4], rt[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int p = lane + 32 * (k0 + j);
-        const bool v = k0 + j < nslot && p + 1 < n;
-        lt[j] = v ? tok[p] : 0;
-        rt[j] = v ? tok[p + 1] : 0;
-        sl[j] = pair_slot(T, lt[j], rt[j]);
-        ent[j] = v ? __ldg(&T.pair_tab[sl[j]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int p = lane + 32 * (k0 + j);
-        if (k0 + j < nslot && p + 1 < n) {
-          const int2 pr = pair_finish(T, ent[j], sl[j], lt[j], rt[j]);
-          rank[p] = rank_or_max(pr.x);
-          res[p] = pr.y;
-        }
-      }
-    }
-    __syncwarp();
-    for (int round = 0; round < n; ++round) {   // each round unlinks at least one symbol
-      int lm = INT_MAX;
-#pragma unroll
-      for (int k = 0; k < MID_SLOTS; ++k)
-        if (k < nslot) lm = min(lm, rank[lane + 32 * k]);
-      const int r = __reduce_min_sync(0xffffffffu, lm);
-      if (r == INT_MAX) break;
-      for (int step = 0; step < n; ++step) {
-        uint32_t sel = 0;
-        bool left = false;
-#pragma unroll
-        for (int k = 0; k < MID_SLOTS; ++k) {
-          const int p = lane + 32 * k;
-          if (k < nslot && rank[p] == r) {
-            const int q = pv[p];
-            if (q < 0 || rank[q] != r) sel |= 1u << k;
-            else left = true;
-          }
-        }
-        __syncwarp();
-        for (uint32_t m = sel; m; m &= m - 1) {
-          const int p = lane + 32 * (__ffs(m) - 1);
-          const int q = nx[p], nq = nx[q];
-          tok[p] = res[p];
-          tok[q] = -1;
-          rank[q] = INT_MAX;
-          rank[p] = INT_MAX;
-          nx[p] = (int16_t)nq;
-          if (nq < n) pv[nq] = (int16_t)p;
-        }
-        __syncwarp();
-        for (uint32_t m = sel; m; m &= m - 1) {
-          const int p = lane + 32 * (__ffs(m) - 1);
-          const int a = pv[p], c = nx[p];
-          const int tp = tok[p];
-          const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
-          const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
-          const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-          const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-          if (a >= 0) {
-            const int2 pr = pair_finish(T, ea, sa, ta, tp);
-            rank[a] = rank_or_max(pr.x);
-            res[a] = pr.y;
-          }
-          if (c < n) {
-            const int2 pr = pair_finish(T, ec, sc, tp, tc);
-            rank[p] = rank_or_max(pr.x);
-            res[p] = pr.y;
-          }
-        }
-        __syncwarp();
-        if (!__any_sync(0xffffffffu, left)) break;
-      }
-    }
-    // surviving tokens in position order
-    int cnt = 0;
-#pragma unroll
-    for (int k = 0; k < MID_SLOTS; ++k) {
-      if (k < nslot) {
-        const int p = lane + 32 * k;
-        const int t = tok[p];
-        const unsigned bal = __ballot_sync(0xffffffffu, t >= 0);
-        if (t >= 0) W.scratch[s + cnt + __popc(bal & lt_mask)] = t;
-        cnt += __popc(bal);
-      }
-    }
-    if (lane == 0) W.n_ids[pc] = cnt;
-    __syncwarp();
   }
 }
 
@@ -479,7 +482,7 @@ __device__ void bpe_block_list(const Tables &T, const uint8_t *b, int n, int32_t
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(BPE_LONG_THREADS) k_bpe_long(Tables T, Work W) {
+__global__ void __launch_bounds__(BPE_LONG_THREADS, 1) k_bpe_long(Tables T, Work W) {
   constexpr int NT = BPE_LONG_THREADS;
   constexpr int32_t MERGED = (int32_t)0x80000000;
   extern __shared__ __align__(16) unsigned char dsm[];
@@ -769,11 +772,8 @@ __global__ void k_hook_offsets(Work W) {
   A.hook_offsets[r] = k - W.bad_pre[r];
 }
 
-void launch_bpe_small(const Tables &T, const Work &W, int grid, cudaStream_t s) {
-  k_bpe_small<<<grid, BPE_SMALL_THREADS, 0, s>>>(T, W);
-}
-void launch_bpe_mid(const Tables &T, const Work &W, int grid, cudaStream_t s) {
-  k_bpe_mid<<<grid, BPE_MID_THREADS, 0, s>>>(T, W);
+void launch_bpe_warp(const Tables &T, const Work &W, int grid, cudaStream_t s) {
+  k_bpe_warp<<<grid, BPE_WARP_THREADS, 0, s>>>(T, W);
 }
 void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   k_bpe_long<<<grid, BPE_LONG_THREADS, LONG_SMEM_BYTES, s>>>(T, W);

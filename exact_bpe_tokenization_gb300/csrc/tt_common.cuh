@@ -71,7 +71,16 @@ TT_HD uint64_t mix64(uint64_t x) {
   x ^= x >> 33;
   return x;
 }
-TT_HD uint64_t pair_hash(uint32_t l, uint32_t r) { return mix64(((uint64_t)l << 32) | r); }
+// slot hash of a token pair: ids are below 2^20 and table masks below 2^32,
+// so 32-bit multiply-xorshift mixing suffices (and costs a third of a 64-bit
+// mix on the GPU)
+TT_HD uint32_t pair_hash(uint32_t l, uint32_t r) {
+  uint32_t h = l * 0x9E3779B1u ^ (r + 0x7F4A7C15u) * 0x85EBCA77u;
+  h ^= h >> 16;
+  h *= 0x7FEB352Du;
+  h ^= h >> 15;
+  return h;
+}
 TT_HD uint64_t pair_key(uint32_t l, uint32_t r) { return ((uint64_t)l << MAX_VOCAB_BITS) | r; }
 
 // hash of a byte string, 8 bytes at a time (little-endian words, zero padded)

@@ -12,8 +12,7 @@ void launch_prepass(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_tilescan(const Tables &T, const Work &W, cudaStream_t s);
 void launch_pretok(const Tables &T, const Work &W, int grid, cudaStream_t s);
 
-void launch_bpe_small(const Tables &T, const Work &W, int grid, cudaStream_t s);
-void launch_bpe_mid(const Tables &T, const Work &W, int grid, cudaStream_t s);
+void launch_bpe_warp(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_ids(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_req(const Tables &T, const Work &W, int grid, cudaStream_t s);
@@ -22,8 +21,8 @@ void launch_hook_pre(const Work &W, cudaStream_t s);
 void launch_hook_pieces(const Work &W, int grid, cudaStream_t s);
 void launch_hook_offsets(const Work &W, int grid, cudaStream_t s);
 
-constexpr int BPE_SMALL_THREADS = 256;
-constexpr int BPE_MID_THREADS = 256;
+constexpr int BPE_WARP_THREADS = 256;
+constexpr int BPE_WARP_CTAS_PER_SM = 4;   // all resident: 64 registers, 32 KB shared memory each
 constexpr int BPE_LONG_THREADS = 512;
 constexpr int IDS_THREADS = 256;
 

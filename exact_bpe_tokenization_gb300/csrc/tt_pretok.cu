@@ -388,7 +388,7 @@ struct Slider {
 };
 
 template <int FAM, int NT>
-__global__ void __launch_bounds__(NT) k_pretok(Tables T, Work W) {
+__global__ void __launch_bounds__(NT, NT == 512 ? 3 : 0) k_pretok(Tables T, Work W) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   PretokSmem<NT> &P = *reinterpret_cast<PretokSmem<NT> *>(smem_raw);
   WinSmem<NT> &S = P.w;

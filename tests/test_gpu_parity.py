@@ -230,7 +230,7 @@ def test_graph_replay_eager_and_host_paths_agree(cuda, vocabs):
         assert np.array_equal(b, ref["id_offsets"]), i
         assert np.array_equal(a, ref["ids"]), i
     assert st == 0
-    assert set(prof) >= {"k_prepass", "k_pretok", "k_bpe_small", "k_ids"} and all(v[1] == 1 for v in prof.values())
+    assert set(prof) >= {"k_prepass", "k_pretok", "k_bpe_warp", "k_ids"} and all(v[1] == 1 for v in prof.values())
     tok.close()
 
 
