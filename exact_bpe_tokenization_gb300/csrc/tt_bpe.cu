@@ -124,12 +124,13 @@ __device__ __forceinline__ int bpe_lanes(const Tables &T, const uint8_t *bytes, 
 
 // ---------------------------------------------------------------- warp kernel
 // Every piece of at most MID_MAX bytes, in one persistent kernel whose warps
-// take tickets from one counter, the longest work first: the pieces of
-// SMALL_MAX+1 .. MID_MAX bytes that k_pretok listed in three length buckets
-// (a warp per piece), then chunks of 32 consecutive pieces, where each lane
-// tries the whole-piece shortcut for its piece of at most SMALL_MAX bytes and
-// the warp merges the misses two at a time, 16 lanes per piece.  Longer
-// pieces are left to k_bpe_long, which runs beside this kernel.
+// take tickets from one counter, the longest expected work first: the pieces
+// of 49 .. MID_MAX bytes that k_pretok listed (a warp per piece), then chunks
+// of 32 consecutive pieces, where each lane tries the whole-piece shortcut
+// for its piece of at most SMALL_MAX bytes and the warp merges the misses two
+// at a time, 16 lanes per piece, then the listed pieces of SMALL_MAX+1 .. 48
+// bytes.  Longer pieces are left to k_bpe_long, which runs beside this
+// kernel.
 //
 // A listed piece of at most 32 bytes runs bpe_lanes<32>; a longer one is a
 // doubly linked list over fixed positions in shared memory (lane l owns
@@ -173,7 +174,18 @@ __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, cons
       }
     }
   }
-  for (unsigned mm = __ballot_sync(0xffffffffu, miss); mm;) {
+  // misses in order of length, longest first, so that the two pieces of a
+  // pair need similar numbers of rounds
+  const unsigned all_miss = __ballot_sync(0xffffffffu, miss);
+  unsigned mm = 0;
+  int len_at = SMALL_MAX + 1;
+  for (unsigned rest = all_miss; rest || mm;) {
+    while (__popc(mm) < 2 && rest) {            // refill from the next shorter length
+      --len_at;
+      const unsigned b = __ballot_sync(0xffffffffu, miss && len == len_at);
+      mm |= b;
+      rest &= ~b;
+    }
     const int la = __ffs(mm) - 1;
     mm &= mm - 1;
     const int lb = mm ? __ffs(mm) - 1 : -1;
@@ -330,8 +342,9 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
   const int np = __ldcg(&W.counters[3]);
   const int c0 = __ldcg(&W.counters[mid_bucket_counter(0)]), c1 = __ldcg(&W.counters[mid_bucket_counter(1)]);
   const int c2 = __ldcg(&W.counters[mid_bucket_counter(2)]);
-  const int nmid = c0 + c1 + c2;
-  const int nwork = nmid + (np + SMALL_CHUNK - 1) / SMALL_CHUNK;
+  // ticket order, longest expected work first: listed pieces of 49..256
+  // bytes, chunks of short pieces, listed pieces of 17..48 bytes
+  const int t1 = c0 + c1, t2 = t1 + (np + SMALL_CHUNK - 1) / SMALL_CHUNK, nwork = t2 + c2;
   const int64_t lcap = list_cap(W.cap_bytes);
   const uint8_t *g = A.utf8 + base;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -340,12 +353,12 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
     if (lane == 0) gi = atomicAdd(&W.counters[9], 1);
     gi = __shfl_sync(0xffffffffu, gi, 0);
     if (gi >= nwork) break;
-    if (gi < nmid) {
-      const int64_t slot = gi < c0 ? gi : gi < c0 + c1 ? lcap + (gi - c0) : 2 * lcap + (gi - c0 - c1);
+    if (gi < t1 || gi >= t2) {
+      const int64_t slot = gi < c0 ? gi : gi < t1 ? lcap + (gi - c0) : 2 * lcap + (gi - t2);
       mid_piece(T, W, g, __ldcg(&W.long_list[slot]), s_tok[warp], s_rank[warp], s_res[warp], s_nx[warp],
                 s_pv[warp]);
     } else {
-      small_chunk(T, W, g, total, np, (gi - nmid) * SMALL_CHUNK);
+      small_chunk(T, W, g, total, np, (gi - t1) * SMALL_CHUNK);
     }
   }
 }
