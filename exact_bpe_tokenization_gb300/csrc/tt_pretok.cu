@@ -57,11 +57,31 @@ __device__ __forceinline__ uint8_t kind_of(const Tables &T, const WS &S, uint32_
   return __ldg(&T.cls2[(uint32_t)__ldg(&T.cls1[cp >> 8]) * 256u + (cp & 255u)]);
 }
 
-// Load the window [ws, ws + WIN) of the batch, mark request starts, find
-// char starts, decode and classify.  All threads participate.
+// Code point of the char whose lead byte is window byte i (a char start):
+// U+FFFD for a malformed or truncated sequence, or one that runs into the
+// next request.
+template <class WS>
+__device__ __forceinline__ uint32_t decode_at(const WS &S, int64_t ws, int64_t total, int i) {
+  const uint8_t b0 = S.bytes[i];
+  int len;
+  uint32_t cp;
+  if (b0 < 0x80) return b0;
+  if (b0 >= 0xC0 && b0 < 0xE0) { len = 2; cp = b0 & 0x1F; }
+  else if (b0 >= 0xE0 && b0 < 0xF0) { len = 3; cp = b0 & 0x0F; }
+  else if (b0 >= 0xF0 && b0 < 0xF8) { len = 4; cp = b0 & 0x07; }
+  else return 0xFFFD;
+  for (int q = 1; q < len; ++q) {
+    if (i + q >= WIN || ws + i + q >= total || S.rsb[i + q] || (S.bytes[i + q] & 0xC0) != 0x80) return 0xFFFD;
+    cp = (cp << 6) | (S.bytes[i + q] & 0x3F);
+  }
+  return cp < 0x110000u ? cp : 0xFFFD;
+}
+
+// Load the bytes of the window [ws, ws + WIN) and mark request starts.  All
+// threads participate.
 template <int NT>
-__device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, int64_t total, int64_t ws,
-                            WinSmem<NT> &S, int *scan_tmp) {
+__device__ void load_bytes(const Tables &T, const CallArgs &A, int64_t base, int64_t total, int64_t ws,
+                           WinSmem<NT> &S) {
   constexpr int PT_BYTES = WIN / NT;
   const int tid = threadIdx.x;
   const uint8_t *g = A.utf8 + base;
@@ -93,6 +113,16 @@ __device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, in
     if (x >= 0 && x < WIN && __ldg(&A.offs[r]) - base < total) S.rsb[x] = 1;
   }
   __syncthreads();
+}
+
+// Load the window [ws, ws + WIN) of the batch, mark request starts, find
+// char starts, decode and classify.  All threads participate.
+template <int NT>
+__device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, int64_t total, int64_t ws,
+                            WinSmem<NT> &S, int *scan_tmp) {
+  constexpr int PT_BYTES = WIN / NT;
+  const int tid = threadIdx.x;
+  load_bytes<NT>(T, A, base, total, ws, S);
   // char starts among my PT_BYTES bytes
   uint32_t smask = 0;
 #pragma unroll
@@ -112,20 +142,7 @@ __device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, in
   for (uint32_t m = smask; m; m &= m - 1) {
     const int k = __ffs(m) - 1;
     const int i = PT_BYTES * tid + k;
-    const uint8_t b0 = S.bytes[i];
-    int len;
-    uint32_t cp;
-    if (b0 < 0x80) { len = 1; cp = b0; }
-    else if (b0 >= 0xC0 && b0 < 0xE0) { len = 2; cp = b0 & 0x1F; }
-    else if (b0 >= 0xE0 && b0 < 0xF0) { len = 3; cp = b0 & 0x0F; }
-    else if (b0 >= 0xF0 && b0 < 0xF8) { len = 4; cp = b0 & 0x07; }
-    else { len = 1; cp = 0xFFFD; }
-    bool ok = true;
-    for (int q = 1; q < len; ++q) {
-      if (i + q >= WIN || ws + i + q >= total || S.rsb[i + q] || (S.bytes[i + q] & 0xC0) != 0x80) { ok = false; break; }
-      cp = (cp << 6) | (S.bytes[i + q] & 0x3F);
-    }
-    if (!ok || cp >= 0x110000u) cp = 0xFFFD;
+    const uint32_t cp = decode_at(S, ws, total, i);
     S.lead[j] = (uint16_t)i;
     S.cp8[j] = cp < 128 ? (uint8_t)cp : (uint8_t)0x80;
     S.raw[j] = kind_of(T, S, cp);
@@ -160,7 +177,12 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
   if (t >= ntiles) return;
   const int64_t ts = (int64_t)t * TILE, te = ts + TILE < total ? ts + TILE : total;
   const int64_t ws = ts - HALO_L;
-  load_window(T, A, base, total, ws, S, scan_tmp);
+  // cl100k needs no mark resolution and no upper-case queries: bytes and
+  // request starts suffice, and the few chars its summary looks at are
+  // decoded where they are met
+  const bool bytes_only = T.family != FAM_O200K;
+  if (bytes_only) load_bytes<NT>(T, A, base, total, ws, S);
+  else load_window(T, A, base, total, ws, S, scan_tmp);
 
   // --- UTF-8 validation of the tile's bytes (RFC 3629, per request)
   for (int k = 0; k < PT_BYTES; ++k) {
@@ -207,6 +229,27 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
     }
   }
 
+  if (bytes_only) {
+    // --- reverse-query summary: the first rq_ws event among the tile's chars,
+    // 32 bytes at a time by one warp (usually within the first step)
+    if (tid < 32) {
+      const int lane = tid;
+      int ev = 0xFF;
+      for (int64_t x0 = ts; x0 < te && ev == 0xFF; x0 += 32) {
+        const int64_t x = x0 + lane;
+        const int i = (int)(x - ws);
+        int e = 0xFF;
+        if (x < te && ((S.bytes[i] & 0xC0) != 0x80 || S.rsb[i])) {
+          const uint32_t cp = decode_at(S, ws, total, i);
+          e = rq_ws_event(S.rsb[i] != 0, kind_of(T, S, cp), cp < 128 ? cp : 0x80u);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, e != 0xFF);
+        if (m) ev = __shfl_sync(0xffffffffu, e, __ffs(m) - 1);
+      }
+      if (lane == 0) { W.rq_sum[2 * t] = (uint8_t)ev; W.rq_sum[2 * t + 1] = 0xFF; }
+    }
+    return;
+  }
   const int c0 = S.cbase[tid], c1 = S.cbase[tid + 1];
   // --- mark-resolution summary over chars with pos in [ts - 32, te - 32)
   if (T.family == FAM_O200K) {
