@@ -121,6 +121,83 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, ctypes, read-only queries) every millisecond from a thread:
+    the timed loop is far shorter than nvidia-smi's sampling period.  The NVML
+    device is the one whose UUID matches the CUDA device's."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, torch_device):
+        self.dev = torch_device
+        self.sm, self.reasons, self.max_mhz = [], set(), None
+        self.ok = False
+        self.stop = threading.Event()
+
+    def _open(self):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        count = ctypes.c_uint()
+        lib.nvmlDeviceGetCount_v2(ctypes.byref(count))
+        want = str(getattr(torch.cuda.get_device_properties(self.dev), "uuid", "")).lower()
+        chosen = None
+        for i in range(count.value):
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(i, ctypes.byref(h)) != 0:
+                continue
+            buf = ctypes.create_string_buffer(96)
+            lib.nvmlDeviceGetUUID(h, buf, 96)
+            if want and buf.value.decode().lower().replace("gpu-", "") == want:
+                chosen = h
+        if chosen is None and count.value == 1:
+            chosen = ctypes.c_void_p()
+            lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(chosen))
+        return (lib, chosen) if chosen is not None else None
+
+    def _run(self, lib, h):
+        import ctypes
+        mhz, reasons = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:   # 1: SM clock
+                self.sm.append(float(mhz.value))
+            if lib.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(reasons)) == 0:
+                for bit, name in self.REASONS.items():
+                    if reasons.value & bit:
+                        self.reasons.add(name)
+            time.sleep(0.001)
+
+    def __enter__(self):
+        try:
+            opened = self._open()
+        except (OSError, AttributeError):
+            opened = None
+        if opened:
+            import ctypes
+            lib, h = opened
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.ok = True
+            self.t = threading.Thread(target=self._run, args=(lib, h), daemon=True)
+            self.t.start()
+            while not self.sm and self.t.is_alive():        # first sample before the timed region
+                time.sleep(0.0005)
+        return self
+
+    def __exit__(self, *exc):
+        self.stop.set()
+        if self.ok:
+            self.t.join(timeout=2)
+
+    def summary(self):
+        return {"sm_mhz": statistics.median(self.sm) if self.sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.sm), "source": "nvml, 1 ms"}
+
+
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -300,7 +377,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk, NvmlClockSampler(dev) as nclk:
         t0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(i)                       # evict the previous step's data from L2
@@ -381,7 +458,7 @@ def run_ours(args):
                    "l2": "flushed between steps by a 256 MiB write", "parallelism": "replicas" if world > 1 else "1 GPU"},
         "gpu_launches": launches,
         "wall_s_timed_loop": wall,
-        "clocks": clk.summary(),
+        "clocks": nclk.summary() if nclk.sm else clk.summary(),
         "e2e": {"value": nbytes / sum(e2e_t) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d / args.steps,
                 "d2h_bytes_per_step": d2h / args.steps, "p50_ms": float(np.percentile(np.array(e2e_t) * 1e3, 50)),
                 "api": "tt_encode_host (pageable host buffers)"},
