@@ -45,6 +45,7 @@ def lib():
             L.tt_destroy.argtypes = [p]
             L.tt_encode_batch.argtypes = [p, p, p, i64, p, p, p]
             L.tt_encode_batch_bounded.argtypes = [p, p, p, i64, i64, p, p, p]
+            L.tt_encode_batch_spans.argtypes = [p, p, p, i64, i64, p, p, p, p]
             L.tt_encode_batch_noalloc.argtypes = [p, p, p, i64, i64, p, p, p]
             L.tt_encode_host.argtypes = [p, p, p, i64, p, i64, p, p]
             L.tt_get_status.argtypes = [p, p, ctypes.POINTER(i64)]
@@ -57,7 +58,8 @@ def lib():
             L.tt_launch_count.argtypes = [p]
             L.tt_launch_count.restype = i64
             L.tt_table_digest.restype = ctypes.c_char_p
-            for name in ("tt_create", "tt_encode_batch", "tt_encode_batch_bounded", "tt_encode_batch_noalloc",
+            for name in ("tt_create", "tt_encode_batch", "tt_encode_batch_bounded", "tt_encode_batch_spans",
+                         "tt_encode_batch_noalloc",
                          "tt_encode_host",
                          "tt_get_status", "tt_pretokenize_batch", "tt_profile_read"):
                 getattr(L, name).restype = ctypes.c_int
@@ -128,6 +130,13 @@ def tt_encode_batch_bounded(h, d_utf8, d_byte_offsets, n_requests, max_total_byt
     _check(lib().tt_encode_batch_bounded(h, _ptr(d_utf8), _ptr(d_byte_offsets), int(n_requests),
                                          int(max_total_bytes), _ptr(d_out_ids), _ptr(d_out_id_offsets),
                                          _stream(stream)), "tt_encode_batch_bounded")
+
+
+def tt_encode_batch_spans(h, d_utf8, d_byte_offsets, n_requests, max_total_bytes, d_out_ids, d_out_id_offsets,
+                          d_out_spans, stream=None):
+    _check(lib().tt_encode_batch_spans(h, _ptr(d_utf8), _ptr(d_byte_offsets), int(n_requests), int(max_total_bytes),
+                                       _ptr(d_out_ids), _ptr(d_out_id_offsets), _ptr(d_out_spans),
+                                       _stream(stream)), "tt_encode_batch_spans")
 
 
 def tt_encode_batch_noalloc(h, d_utf8, d_byte_offsets, n_requests, max_total_bytes, d_out_ids, d_out_id_offsets,
@@ -205,6 +214,21 @@ class Tokenizer:
             out_offsets = torch.empty(n + 1, dtype=torch.int64, device=d_utf8.device)
         tt_encode_batch_bounded(self.h, d_utf8, d_offsets, n, max_total_bytes, out_ids, out_offsets, stream)
         return out_ids, out_offsets
+
+    def encode_spans(self, d_utf8, d_offsets, max_total_bytes=None, stream=None):
+        """Encode a device batch with byte spans; returns (ids, id_offsets,
+        spans) device tensors, spans int32 [capacity, 2] (start, end) from the
+        batch start."""
+        import torch
+        n = d_offsets.numel() - 1
+        if max_total_bytes is None:
+            max_total_bytes = d_utf8.numel()
+        cap = max(int(max_total_bytes), 1)
+        out_ids = torch.empty(cap, dtype=torch.int32, device=d_utf8.device)
+        out_offsets = torch.empty(n + 1, dtype=torch.int64, device=d_utf8.device)
+        spans = torch.empty((cap, 2), dtype=torch.int32, device=d_utf8.device)
+        tt_encode_batch_spans(self.h, d_utf8, d_offsets, n, max_total_bytes, out_ids, out_offsets, spans, stream)
+        return out_ids, out_offsets, spans
 
     def pretokenize(self, d_utf8, d_offsets, stream=None):
         import torch

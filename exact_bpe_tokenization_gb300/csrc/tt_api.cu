@@ -435,9 +435,9 @@ static tt_status check_batch_args(tt_tokenizer *h, const void *d_utf8, const int
   return TT_OK;
 }
 
-extern "C" tt_status tt_encode_batch_bounded(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
-                                             int64_t n_requests, int64_t max_total_bytes, int32_t *d_out_ids,
-                                             int64_t *d_out_id_offsets, tt_stream_t stream_) {
+static tt_status encode_bounded(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
+                                int64_t n_requests, int64_t max_total_bytes, int32_t *d_out_ids,
+                                int64_t *d_out_id_offsets, int32_t *d_out_spans, tt_stream_t stream_) {
   tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, max_total_bytes);
   if (s != TT_OK) return s;
   if (max_total_bytes < 0 || max_total_bytes >= S2_MAX_POS - 64) return TT_ERR_CAPACITY;
@@ -449,7 +449,7 @@ extern "C" tt_status tt_encode_batch_bounded(tt_tokenizer *h, const uint8_t *d_u
   std::lock_guard<std::mutex> lock(h->mu);
   Workspace *w;
   if ((s = get_workspace(h, stream, max_total_bytes, n_requests, &w)) != TT_OK) return s;
-  CallArgs args = {d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, nullptr, nullptr};
+  CallArgs args = {d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, nullptr, nullptr, d_out_spans};
   TT_CUDA(cudaMemcpyAsync(w->W.args, &args, sizeof(args), cudaMemcpyHostToDevice, stream));
   if (h->profiling || !h->graphs_enabled) return enqueue_encode(h, w, stream, h->profiling);
   if (!w->graph) {
@@ -470,6 +470,21 @@ extern "C" tt_status tt_encode_batch_bounded(tt_tokenizer *h, const uint8_t *d_u
   TT_CUDA(cudaGraphLaunch(w->graph, stream));
   h->launches += N_KERNELS;
   return TT_OK;
+}
+
+extern "C" tt_status tt_encode_batch_bounded(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
+                                             int64_t n_requests, int64_t max_total_bytes, int32_t *d_out_ids,
+                                             int64_t *d_out_id_offsets, tt_stream_t stream) {
+  return encode_bounded(h, d_utf8, d_byte_offsets, n_requests, max_total_bytes, d_out_ids, d_out_id_offsets, nullptr,
+                        stream);
+}
+
+extern "C" tt_status tt_encode_batch_spans(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
+                                           int64_t n_requests, int64_t max_total_bytes, int32_t *d_out_ids,
+                                           int64_t *d_out_id_offsets, int32_t *d_out_spans, tt_stream_t stream) {
+  if (!d_out_spans && n_requests > 0 && max_total_bytes > 0) return TT_ERR_INVALID_ARG;
+  return encode_bounded(h, d_utf8, d_byte_offsets, n_requests, max_total_bytes, d_out_ids, d_out_id_offsets,
+                        d_out_spans, stream);
 }
 
 extern "C" tt_status tt_encode_batch(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,

@@ -625,6 +625,7 @@ __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
   __shared__ int s_off[IDS_CHUNK + 1];   // chunk-local output offset of each piece
   __shared__ int s_st[IDS_CHUNK];        // its start byte (its IDs sit at scratch[start ...])
   __shared__ int red[IDS_THREADS / 32];
+  __shared__ int2 s_red2[IDS_THREADS / 32];
   __shared__ int s_tile, s_base;
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
@@ -686,17 +687,50 @@ __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
     __syncthreads();
     // output-parallel copy: output o of the chunk belongs to the last piece
     // whose offset is <= o (pieces with no IDs share their successor's offset)
+    auto piece_of = [&](int o) {
+      int lo = 0, hi = nloc - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] <= o) lo = mid;
+        else hi = mid - 1;
+      }
+      return lo;
+    };
     if ((int64_t)cb + chunk_total > total) {
       if (tid == 0) set_status(W.status, ST_INVALID_ARG);
-    } else {
+    } else if (!A.out_spans) {
       for (int o = tid; o < chunk_total; o += IDS_THREADS) {
-        int lo = 0, hi = nloc - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (s_off[mid] <= o) lo = mid;
-          else hi = mid - 1;
+        const int q = piece_of(o);
+        A.out_ids[cb + o] = __ldcg(&W.scratch[s_st[q] + (o - s_off[q])]);
+      }
+    } else {
+      // with byte spans: the IDs of a piece cover its bytes in order, so an
+      // ID starts where the lengths of the piece's earlier IDs end -- a scan
+      // of token lengths segmented by piece, IDS_THREADS outputs at a time,
+      // the open piece's byte count carried from one step to the next
+      auto seg = [](int2 a, int2 b) { return make_int2(a.x | b.x, b.x ? b.y : a.y + b.y); };
+      int carry = 0;
+      for (int ob = 0; ob < chunk_total; ob += IDS_THREADS) {
+        const int o = ob + tid;
+        int q = 0, len = 0;
+        bool head = false;
+        if (o < chunk_total) {
+          q = piece_of(o);
+          const int id = __ldcg(&W.scratch[s_st[q] + (o - s_off[q])]);
+          A.out_ids[cb + o] = id;
+          len = __ldg(&T.voff[id + 1]) - __ldg(&T.voff[id]);
+          head = o == s_off[q];
         }
-        A.out_ids[cb + o] = __ldcg(&W.scratch[s_st[lo] + (o - s_off[lo])]);
+        int2 step;
+        const int2 ex = block_exclusive_scan<IDS_THREADS>(make_int2(head, len), seg, make_int2(0, 0), s_red2,
+                                                          &step);
+        if (o < chunk_total) {
+          const int before = head ? 0 : ex.y + (ex.x ? 0 : carry);   // bytes of my piece before me
+          const int start = s_st[q] + before;
+          A.out_spans[2 * ((int64_t)cb + o)] = start;
+          A.out_spans[2 * ((int64_t)cb + o) + 1] = start + len;
+        }
+        carry = step.x ? step.y : carry + step.y;
       }
     }
     __syncthreads();

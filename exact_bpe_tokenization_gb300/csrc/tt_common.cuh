@@ -373,6 +373,7 @@ struct CallArgs {
   int64_t *out_id_offsets;         // [n + 1]
   int64_t *hook_starts;            // test hook outputs (NULL unless the hook runs)
   int64_t *hook_offsets;
+  int32_t *out_spans;              // [2 * tokens]: (start, end) byte offsets from offs[0] per ID; NULL: none
 };
 
 // Per-stream workspace (device pointers; sizes fixed per capacity bucket).

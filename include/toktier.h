@@ -150,6 +150,33 @@ tt_status tt_encode_batch_bounded(tt_tokenizer *h,
                                   int32_t *d_out_ids, int64_t *d_out_id_offsets, tt_stream_t stream);
 
 /*
+ * tt_encode_batch_spans - as tt_encode_batch_bounded, and for every ID the
+ * source bytes it covers.
+ *
+ * The paper's session state holds, beside each token ID, the byte span of the
+ * text it encodes (TokTier §3 "session store"; §5.7, Figure 14a: 4 bytes of
+ * ID and 8 bytes of span per token), and its GPU full path returns IDs
+ * without spans, so a state miss that must build that state falls back to the
+ * CPU (§4.4).  This call returns both.
+ *
+ *   d_out_spans  device, int32 [2 * capacity], capacity as d_out_ids (>= the
+ *                batch bytes).  ID i gets (start, end) = d_out_spans[2i],
+ *                d_out_spans[2i + 1]: the half-open range of batch bytes it
+ *                encodes, as offsets from d_byte_offsets[0] (the batch
+ *                start; subtract d_byte_offsets[r] - d_byte_offsets[0] for
+ *                offsets within request r).  A request's spans tile its bytes
+ *                in order; a rejected request has no IDs and no spans.
+ *   other arguments, the graph and the errors as tt_encode_batch_bounded;
+ *   d_out_spans may be NULL only if max_total_bytes is 0 (else
+ *   TT_ERR_INVALID_ARG).  The caller owns every buffer.
+ */
+tt_status tt_encode_batch_spans(tt_tokenizer *h,
+                                const uint8_t *d_utf8, const int64_t *d_byte_offsets, int64_t n_requests,
+                                int64_t max_total_bytes,
+                                int32_t *d_out_ids, int64_t *d_out_id_offsets, int32_t *d_out_spans,
+                                tt_stream_t stream);
+
+/*
  * tt_encode_batch_noalloc - tokenize a small device batch without allocating.
  *
  * The paper has no counterpart: this exists for callers that must not

@@ -348,12 +348,24 @@ void oracle_destroy(void *h) {
 
 /* E: encode one piece's bytes.  ids must hold len entries; returns the count.
  * rank[] caches the rank of each adjacent pair; after a merge only the two
- * pairs next to it change, so only they are looked up again. */
-static int64_t encode_piece(const oracle_t *o, const uint8_t *b, int64_t len, int32_t *ids, int64_t *rank) {
+ * pairs next to it change, so only they are looked up again.
+ * If sstart is not NULL it must hold len entries and receives, for every
+ * emitted ID, the offset in the piece of the first byte that ID covers: each
+ * symbol starts as one byte at its own offset, and a merge keeps the left
+ * symbol's start (the byte range of a merged symbol is the union of the two
+ * adjacent ranges it joins).  This provenance is tracked through the merges,
+ * not derived from token lengths. */
+static int64_t encode_piece_spans(const oracle_t *o, const uint8_t *b, int64_t len, int32_t *ids, int64_t *rank,
+                                  int64_t *sstart) {
   int64_t whole = vocab_find(o, b, len);
-  if (whole >= 0) { ids[0] = (int32_t)whole; return 1; }
+  if (whole >= 0) {
+    ids[0] = (int32_t)whole;
+    if (sstart) sstart[0] = 0;
+    return 1;
+  }
   int64_t n = len;
   for (int64_t i = 0; i < n; ++i) ids[i] = (int32_t)vocab_find(o, b + i, 1);
+  if (sstart) for (int64_t i = 0; i < n; ++i) sstart[i] = i;
   for (int64_t i = 0; i + 1 < n; ++i) rank[i] = merge_rank(o, ids[i], ids[i + 1]);
   for (;;) {
     int64_t best = -1, at = -1;
@@ -362,12 +374,17 @@ static int64_t encode_piece(const oracle_t *o, const uint8_t *b, int64_t len, in
     if (best < 0) break;
     ids[at] = o->mresult[best];
     memmove(ids + at + 1, ids + at + 2, sizeof(int32_t) * (size_t)(n - at - 2));
+    if (sstart) memmove(sstart + at + 1, sstart + at + 2, sizeof(int64_t) * (size_t)(n - at - 2));
     memmove(rank + at + 1, rank + at + 2, sizeof(int64_t) * (size_t)(n > at + 3 ? n - at - 3 : 0));
     --n;
     if (at > 0) rank[at - 1] = merge_rank(o, ids[at - 1], ids[at]);
     if (at + 1 < n) rank[at] = merge_rank(o, ids[at], ids[at + 1]);
   }
   return n;
+}
+
+static int64_t encode_piece(const oracle_t *o, const uint8_t *b, int64_t len, int32_t *ids, int64_t *rank) {
+  return encode_piece_spans(o, b, len, ids, rank, NULL);
 }
 
 /* ---------------------------------------------------------- batch API */
@@ -380,9 +397,10 @@ typedef struct {
   pthread_mutex_t lock;
   /* per request results, owned by the job */
   int32_t **ids; int64_t *nids;
+  int64_t **spans;               /* per request: (start, end) per ID, relative to the request */
   int64_t **pieces; int64_t *npieces;
   int *status;
-  int want_ids;
+  int want_ids, want_spans;
 } job_t;
 
 static void run_request(job_t *j, int64_t r) {
@@ -402,10 +420,21 @@ static void run_request(job_t *j, int64_t r) {
   if (j->want_ids) {
     int32_t *ids = malloc(sizeof(int32_t) * (size_t)(nb + 1));
     int64_t *rank = malloc(sizeof(int64_t) * (size_t)(nb + 1));
+    int64_t *ss = j->want_spans ? malloc(sizeof(int64_t) * (size_t)(nb + 1)) : NULL;
+    int64_t *sp = j->want_spans ? malloc(sizeof(int64_t) * 2 * (size_t)(nb + 1)) : NULL;
     int64_t t = 0;
-    for (int64_t k = 0; k < np; ++k) t += encode_piece(o, b + st[k], st[k + 1] - st[k], ids + t, rank);
-    free(rank);
+    for (int64_t k = 0; k < np; ++k) {
+      const int64_t plen = st[k + 1] - st[k];
+      const int64_t m = encode_piece_spans(o, b + st[k], plen, ids + t, rank, ss);
+      for (int64_t i = 0; ss && i < m; ++i) {     /* an ID ends where the next one in its piece starts */
+        sp[2 * (t + i)] = st[k] + ss[i];
+        sp[2 * (t + i) + 1] = st[k] + (i + 1 < m ? ss[i + 1] : plen);
+      }
+      t += m;
+    }
+    free(rank); free(ss);
     j->ids[r] = ids; j->nids[r] = t;
+    j->spans[r] = sp;
   }
   free(cp); free(pos);
 }
@@ -430,16 +459,18 @@ static void *worker(void *arg) {
  *   out_status[n_req]   per-request status (ERR_UTF8 for invalid requests,
  *                       which contribute no pieces and no IDs)
  * threads: worker threads (>= 1).  Returns OK or ERR_CAPACITY. */
-int oracle_run_batch(void *h, const uint8_t *bytes, const int64_t *offs, int64_t n_req, int threads,
-                     int32_t *out_ids, int64_t cap_ids, int64_t *out_id_offsets,
+static int run_batch(void *h, const uint8_t *bytes, const int64_t *offs, int64_t n_req, int threads,
+                     int32_t *out_ids, int64_t cap_ids, int64_t *out_id_offsets, int64_t *out_spans,
                      int64_t *out_piece_starts, int64_t cap_pieces, int64_t *out_piece_offsets,
                      int32_t *out_status) {
   job_t j;
   memset(&j, 0, sizeof(j));
   j.o = h; j.bytes = bytes; j.offs = offs; j.n_req = n_req;
-  j.want_ids = out_ids != NULL || out_id_offsets != NULL;
+  j.want_spans = out_spans != NULL;
+  j.want_ids = out_ids != NULL || out_id_offsets != NULL || j.want_spans;
   pthread_mutex_init(&j.lock, NULL);
   j.ids = calloc((size_t)(n_req + 1), sizeof(int32_t *)); j.nids = calloc((size_t)(n_req + 1), sizeof(int64_t));
+  j.spans = calloc((size_t)(n_req + 1), sizeof(int64_t *));
   j.pieces = calloc((size_t)(n_req + 1), sizeof(int64_t *)); j.npieces = calloc((size_t)(n_req + 1), sizeof(int64_t));
   j.status = calloc((size_t)(n_req + 1), sizeof(int));
   if (threads < 1) threads = 1;
@@ -462,6 +493,10 @@ int oracle_run_batch(void *h, const uint8_t *bytes, const int64_t *offs, int64_t
         if (ti + j.nids[r] > cap_ids) rc = ERR_CAPACITY;
         else memcpy(out_ids + ti, j.ids[r], sizeof(int32_t) * (size_t)j.nids[r]);
       }
+      if (out_spans) {                            /* byte offsets from the batch start offs[0] */
+        if (ti + j.nids[r] > cap_ids) rc = ERR_CAPACITY;
+        else for (int64_t i = 0; i < 2 * j.nids[r]; ++i) out_spans[2 * ti + i] = offs[r] - offs[0] + j.spans[r][i];
+      }
       ti += j.nids[r];
       if (out_id_offsets) out_id_offsets[r + 1] = ti;
     }
@@ -471,11 +506,31 @@ int oracle_run_batch(void *h, const uint8_t *bytes, const int64_t *offs, int64_t
     }
     tp += j.npieces[r];
     if (out_piece_offsets) out_piece_offsets[r + 1] = tp;
-    free(j.ids[r]); free(j.pieces[r]);
+    free(j.ids[r]); free(j.spans[r]); free(j.pieces[r]);
   }
-  free(j.ids); free(j.nids); free(j.pieces); free(j.npieces); free(j.status);
+  free(j.ids); free(j.nids); free(j.spans); free(j.pieces); free(j.npieces); free(j.status);
   pthread_mutex_destroy(&j.lock);
   return rc;
+}
+
+int oracle_run_batch(void *h, const uint8_t *bytes, const int64_t *offs, int64_t n_req, int threads,
+                     int32_t *out_ids, int64_t cap_ids, int64_t *out_id_offsets,
+                     int64_t *out_piece_starts, int64_t cap_pieces, int64_t *out_piece_offsets,
+                     int32_t *out_status) {
+  return run_batch(h, bytes, offs, n_req, threads, out_ids, cap_ids, out_id_offsets, NULL, out_piece_starts,
+                   cap_pieces, out_piece_offsets, out_status);
+}
+
+/* As oracle_run_batch with IDs and, for every ID, the source byte range it
+ * covers: out_spans[2 * cap_ids] receives (start, end) per ID, byte offsets
+ * from the batch start offs[0] (TokTier §3: the session state a repair step
+ * edits holds IDs and byte spans; §4.4: the paper's GPU path does not return
+ * them).  Tracked through the merges as described at encode_piece_spans. */
+int oracle_run_batch_spans(void *h, const uint8_t *bytes, const int64_t *offs, int64_t n_req, int threads,
+                           int32_t *out_ids, int64_t cap_ids, int64_t *out_id_offsets, int64_t *out_spans,
+                           int32_t *out_status) {
+  return run_batch(h, bytes, offs, n_req, threads, out_ids, cap_ids, out_id_offsets, out_spans, NULL, 0, NULL,
+                   out_status);
 }
 
 /* E alone on one byte string (for the BPE pins): ids must hold len entries */

@@ -62,6 +62,8 @@ def load_lib(path):
     lib.oracle_destroy.argtypes = [p]
     lib.oracle_run_batch.argtypes = [p, p, p, i64, ctypes.c_int, p, i64, p, p, i64, p, p]
     lib.oracle_run_batch.restype = ctypes.c_int
+    lib.oracle_run_batch_spans.argtypes = [p, p, p, i64, ctypes.c_int, p, i64, p, p, p]
+    lib.oracle_run_batch_spans.restype = ctypes.c_int
     lib.oracle_encode_bytes.argtypes = [p, p, i64, p]
     lib.oracle_encode_bytes.restype = i64
     lib.oracle_encode_bytes_plain.argtypes = [p, p, i64, p]
@@ -166,6 +168,28 @@ class Oracle:
             out["piece_starts"] = ops[:int(opo[-1])]
             out["piece_offsets"] = opo
         return out
+
+    def run_spans(self, data, offsets, threads=1):
+        """IDs with the source byte span of each: a dict with ids (int32),
+        id_offsets (int64), spans (int64 [tokens, 2]: start, end as byte
+        offsets from offsets[0]) and status."""
+        data = np.ascontiguousarray(np.frombuffer(data, dtype=np.uint8) if isinstance(data, (bytes, bytearray)) else data,
+                                    dtype=np.uint8)
+        offs = np.ascontiguousarray(offsets, dtype=np.int64)
+        n = len(offs) - 1
+        total = int(offs[-1] - offs[0]) if n > 0 else 0
+        cap = max(total, 1)
+        status = np.zeros(max(n, 1), dtype=np.int32)
+        ids = np.zeros(cap, dtype=np.int32)
+        io = np.zeros(n + 1, dtype=np.int64)
+        spans = np.zeros((cap, 2), dtype=np.int64)
+        rc = self._lib.oracle_run_batch_spans(self._h, data.ctypes.data if len(data) else None, offs.ctypes.data, n,
+                                              int(threads), ids.ctypes.data, cap, io.ctypes.data, spans.ctypes.data,
+                                              status.ctypes.data)
+        if rc != 0:
+            raise RuntimeError("oracle_run_batch_spans failed: status %d" % rc)
+        t = int(io[-1])
+        return {"ids": ids[:t], "id_offsets": io, "spans": spans[:t], "status": status[:n]}
 
     def encode_bytes(self, b, plain=False):
         """E on one byte string (whole-piece shortcut unless plain=True)."""

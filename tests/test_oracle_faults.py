@@ -27,12 +27,14 @@ MUTANTS = {
     "prefix_allows_newline": ("return !isCRLF(c) && !isL(o, c) && !isN(o, c); }",
                               "return !isL(o, c) && !isN(o, c); }", "pretok"),
     "o200k_lower_set_without_marks": ("(B_LL | B_LM | B_LO | B_M); }", "(B_LL | B_LM | B_LO); }", "pretok2"),
-    "bpe_rightmost_on_ties": ("if (rank[i] >= 0 && (best < 0 || rank[i] < best)) { best = rank[i]; at = i; }\n    if (best < 0) break;\n    ids[at] = o->mresult[best];\n    memmove(ids + at + 1, ids + at + 2, sizeof(int32_t) * (size_t)(n - at - 2));\n    memmove(rank + at + 1, rank + at + 2, sizeof(int64_t) * (size_t)(n > at + 3 ? n - at - 3 : 0));\n    --n;\n    if (at > 0) rank[at - 1] = merge_rank(o, ids[at - 1], ids[at]);\n    if (at + 1 < n) rank[at] = merge_rank(o, ids[at], ids[at + 1]);\n  }\n  return n;\n}\n\n/* ----",
-                              "if (rank[i] >= 0 && (best < 0 || rank[i] <= best)) { best = rank[i]; at = i; }\n    if (best < 0) break;\n    ids[at] = o->mresult[best];\n    memmove(ids + at + 1, ids + at + 2, sizeof(int32_t) * (size_t)(n - at - 2));\n    memmove(rank + at + 1, rank + at + 2, sizeof(int64_t) * (size_t)(n > at + 3 ? n - at - 3 : 0));\n    --n;\n    if (at > 0) rank[at - 1] = merge_rank(o, ids[at - 1], ids[at]);\n    if (at + 1 < n) rank[at] = merge_rank(o, ids[at], ids[at + 1]);\n  }\n  return n;\n}\n\n/* ----", "bpe"),
-    "no_whole_piece_shortcut": ("if (whole >= 0) { ids[0] = (int32_t)whole; return 1; }",
-                                "if (0 && whole >= 0) { ids[0] = (int32_t)whole; return 1; }", "bpe"),
-    "stale_left_rank": ("    if (at > 0) rank[at - 1] = merge_rank(o, ids[at - 1], ids[at]);\n    if (at + 1 < n) rank[at] = merge_rank(o, ids[at], ids[at + 1]);\n  }\n  return n;\n}\n\n/* ----",
-                        "    if (at + 1 < n) rank[at] = merge_rank(o, ids[at], ids[at + 1]);\n  }\n  return n;\n}\n\n/* ----", "bpe"),
+    "bpe_rightmost_on_ties": ("if (rank[i] >= 0 && (best < 0 || rank[i] < best)) { best = rank[i]; at = i; }\n    if (best < 0) break;\n    ids[at] = o->mresult[best];\n    memmove(ids + at + 1, ids + at + 2, sizeof(int32_t) * (size_t)(n - at - 2));\n    if (sstart)",
+                              "if (rank[i] >= 0 && (best < 0 || rank[i] <= best)) { best = rank[i]; at = i; }\n    if (best < 0) break;\n    ids[at] = o->mresult[best];\n    memmove(ids + at + 1, ids + at + 2, sizeof(int32_t) * (size_t)(n - at - 2));\n    if (sstart)", "bpe"),
+    "no_whole_piece_shortcut": ("  if (whole >= 0) {\n    ids[0] = (int32_t)whole;",
+                                "  if (0 && whole >= 0) {\n    ids[0] = (int32_t)whole;", "bpe"),
+    "stale_left_rank": ("    if (at > 0) rank[at - 1] = merge_rank(o, ids[at - 1], ids[at]);\n    if (at + 1 < n) rank[at] = merge_rank(o, ids[at], ids[at + 1]);\n  }\n  return n;\n}\n\nstatic int64_t encode_piece(",
+                        "    if (at + 1 < n) rank[at] = merge_rank(o, ids[at], ids[at + 1]);\n  }\n  return n;\n}\n\nstatic int64_t encode_piece(", "bpe"),
+    "span_keeps_right_start": ("if (sstart) memmove(sstart + at + 1, sstart + at + 2,", "if (sstart) memmove(sstart + at, sstart + at + 1,",
+                               "spans"),
     "surrogates_accepted": ("(c >= 0xD800 && c <= 0xDFFF)", "(0)", "utf8"),
 }
 
@@ -59,6 +61,19 @@ def pretok_pin_fails(lib, family, masks):
     return False
 
 
+def spans_pin_fails(lib):
+    from test_oracle_spans import textbook_spans
+    m, vb, vo, toks = hand_vocab()
+    o = oracle.Oracle(m, vb, vo, 1, lib=lib)
+    ranks, results, index = tables(m, toks)
+    for s in brute.all_strings("abcd", 6):
+        b = s.encode()
+        got = o.run_spans(b, np.array([0, len(b)], dtype=np.int64))
+        if [tuple(x) for x in got["spans"].tolist()] != textbook_spans(b, ranks, results, index, toks)[1]:
+            return True
+    return False
+
+
 def bpe_pin_fails(lib):
     m, vb, vo, toks = hand_vocab()
     o = oracle.Oracle(m, vb, vo, 1, lib=lib)
@@ -79,6 +94,8 @@ def test_planted_oracle_fault_is_caught(name, tmp_path, masks):
         assert pretok_pin_fails(lib, 2, masks)
     elif kind == "bpe":
         assert bpe_pin_fails(lib)
+    elif kind == "spans":
+        assert spans_pin_fails(lib)
     else:
         pt = oracle.pretokenizer(1, lib=lib)
         bad = b"\xed\xa0\x80"
@@ -92,6 +109,7 @@ def test_unmutated_oracle_passes_the_same_pins(masks):
     assert not pretok_pin_fails(lib, 1, masks)
     assert not pretok_pin_fails(lib, 2, masks)
     assert not bpe_pin_fails(lib)
+    assert not spans_pin_fails(lib)
 
 
 @pytest.mark.parametrize("fault", ["substitute", "delete", "duplicate", "swap", "tail_resplit"])
