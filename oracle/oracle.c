@@ -63,6 +63,10 @@ typedef struct {
   int32_t *mleft, *mright;       /* by rank */
   int32_t *mresult;              /* result id by rank */
   int64_t *msorted;              /* ranks sorted by (left, right) */
+  int64_t n_lit;                 /* added-token literals (copies) */
+  uint8_t *lbytes;
+  int64_t *loff;
+  int32_t *lid;
 } oracle_t;
 
 /* ------------------------------------------------------------ classes */
@@ -338,9 +342,36 @@ int oracle_create(const uint16_t *cls, int family,
   return st;
 }
 
+/* Added tokens (TokTier §4.4: literal strings the model reserves as single
+ * IDs, extracted leftmost-longest before the family tokenizes the rest):
+ * n literals, bytes[offs[k] .. offs[k+1]) with ID ids[k].  Replaces any
+ * earlier set; n = 0 clears it.  Literals must be non-empty and distinct. */
+int oracle_set_added_tokens(void *h, const uint8_t *bytes, const int64_t *offs, const int32_t *ids, int64_t n) {
+  oracle_t *o = h;
+  if (!o || n < 0 || (n > 0 && (!bytes || !offs || !ids))) return ERR_ARG;
+  for (int64_t k = 0; k < n; ++k) {
+    if (offs[k + 1] - offs[k] < 1) return ERR_ARG;
+    for (int64_t q = 0; q < k; ++q)
+      if (offs[q + 1] - offs[q] == offs[k + 1] - offs[k] &&
+          memcmp(bytes + offs[q], bytes + offs[k], (size_t)(offs[k + 1] - offs[k])) == 0)
+        return ERR_ARG;
+  }
+  free(o->lbytes); free(o->loff); free(o->lid);
+  o->n_lit = n;
+  const int64_t total = n > 0 ? offs[n] - offs[0] : 0;
+  o->lbytes = malloc((size_t)(total ? total : 1));
+  o->loff = malloc(sizeof(int64_t) * (size_t)(n + 1));
+  o->lid = malloc(sizeof(int32_t) * (size_t)(n ? n : 1));
+  if (total) memcpy(o->lbytes, bytes + offs[0], (size_t)total);
+  o->loff[0] = 0;
+  for (int64_t k = 0; k < n; ++k) { o->loff[k + 1] = offs[k + 1] - offs[0]; o->lid[k] = ids[k]; }
+  return OK;
+}
+
 void oracle_destroy(void *h) {
   oracle_t *o = h;
   if (!o) return;
+  free(o->lbytes); free(o->loff); free(o->lid);
   free((void *)o->vbytes); free(o->voff); free(o->vsorted);
   free(o->mleft); free(o->mright); free(o->mresult); free(o->msorted);
   free(o);
@@ -403,6 +434,35 @@ typedef struct {
   int want_ids, want_spans;
 } job_t;
 
+/* The longest added-token literal that occurs at byte x of b[0..nb), as an
+ * index, or -1. */
+static int64_t literal_at(const oracle_t *o, const uint8_t *b, int64_t nb, int64_t x) {
+  int64_t best = -1, best_len = 0;
+  for (int64_t k = 0; k < o->n_lit; ++k) {
+    const int64_t len = o->loff[k + 1] - o->loff[k];
+    if (len > best_len && x + len <= nb && memcmp(b + x, o->lbytes + o->loff[k], (size_t)len) == 0) {
+      best = k;
+      best_len = len;
+    }
+  }
+  return best;
+}
+
+/* G on the chars of bytes [from, to) of a valid request: appends the piece
+ * starts (byte offsets relative to the request) to st, marks them unforced. */
+static int64_t pretokenize_segment(const oracle_t *o, const uint8_t *b, int64_t from, int64_t to, int64_t *st,
+                                   int64_t *forced, int64_t np) {
+  if (to <= from) return np;
+  uint32_t *cp = malloc(sizeof(uint32_t) * (size_t)(to - from + 1));
+  int64_t *pos = malloc(sizeof(int64_t) * (size_t)(to - from + 2));
+  int64_t *s = malloc(sizeof(int64_t) * (size_t)(to - from + 1));
+  const int64_t nc = utf8_decode(b + from, to - from, cp, pos);     /* valid: the request passed */
+  const int64_t k = pretokenize_chars(o, cp, nc, s);
+  for (int64_t i = 0; i < k; ++i) { st[np] = from + pos[s[i]]; forced[np] = -1; ++np; }
+  free(cp); free(pos); free(s);
+  return np;
+}
+
 static void run_request(job_t *j, int64_t r) {
   const oracle_t *o = j->o;
   const uint8_t *b = j->bytes + j->offs[r];
@@ -410,23 +470,43 @@ static void run_request(job_t *j, int64_t r) {
   uint32_t *cp = malloc(sizeof(uint32_t) * (size_t)(nb + 1));
   int64_t *pos = malloc(sizeof(int64_t) * (size_t)(nb + 2));
   int64_t nc = utf8_decode(b, nb, cp, pos);
-  if (nc < 0) { j->status[r] = ERR_UTF8; free(cp); free(pos); return; }
-  int64_t *st = malloc(sizeof(int64_t) * (size_t)(nc + 1));
-  int64_t np = pretokenize_chars(o, cp, nc, st);
-  /* piece starts as byte offsets relative to the request */
-  for (int64_t k = 0; k < np; ++k) st[k] = pos[st[k]];
+  free(cp); free(pos);
+  if (nc < 0) { j->status[r] = ERR_UTF8; return; }
+  /* Added tokens first (TokTier §4.4): scanning left to right, the longest
+   * literal at the leftmost position where one occurs is cut out as one piece
+   * with its reserved ID; the segments between literals are pre-tokenized
+   * separately, as documents of their own. */
+  int64_t *st = malloc(sizeof(int64_t) * (size_t)(nb + 1));
+  int64_t *forced = malloc(sizeof(int64_t) * (size_t)(nb + 1));   /* literal ID of a piece, or -1 */
+  int64_t np = 0, seg = 0;
+  for (int64_t x = 0; o->n_lit > 0 && x < nb;) {
+    const int64_t k = literal_at(o, b, nb, x);
+    if (k < 0) { ++x; continue; }
+    np = pretokenize_segment(o, b, seg, x, st, forced, np);
+    st[np] = x; forced[np] = o->lid[k]; ++np;
+    x += o->loff[k + 1] - o->loff[k];
+    seg = x;
+  }
+  np = pretokenize_segment(o, b, seg, nb, st, forced, np);
   st[np] = nb;
   j->pieces[r] = st; j->npieces[r] = np;
   if (j->want_ids) {
     int32_t *ids = malloc(sizeof(int32_t) * (size_t)(nb + 1));
     int64_t *rank = malloc(sizeof(int64_t) * (size_t)(nb + 1));
-    int64_t *ss = j->want_spans ? malloc(sizeof(int64_t) * (size_t)(nb + 1)) : NULL;
+    int64_t *ss = malloc(sizeof(int64_t) * (size_t)(nb + 1));
     int64_t *sp = j->want_spans ? malloc(sizeof(int64_t) * 2 * (size_t)(nb + 1)) : NULL;
     int64_t t = 0;
     for (int64_t k = 0; k < np; ++k) {
       const int64_t plen = st[k + 1] - st[k];
-      const int64_t m = encode_piece_spans(o, b + st[k], plen, ids + t, rank, ss);
-      for (int64_t i = 0; ss && i < m; ++i) {     /* an ID ends where the next one in its piece starts */
+      int64_t m;
+      if (forced[k] >= 0) {                       /* a literal: its one reserved ID */
+        ids[t] = (int32_t)forced[k];
+        ss[0] = 0;
+        m = 1;
+      } else {
+        m = encode_piece_spans(o, b + st[k], plen, ids + t, rank, ss);
+      }
+      for (int64_t i = 0; sp && i < m; ++i) {     /* an ID ends where the next one in its piece starts */
         sp[2 * (t + i)] = st[k] + ss[i];
         sp[2 * (t + i) + 1] = st[k] + (i + 1 < m ? ss[i + 1] : plen);
       }
@@ -436,7 +516,7 @@ static void run_request(job_t *j, int64_t r) {
     j->ids[r] = ids; j->nids[r] = t;
     j->spans[r] = sp;
   }
-  free(cp); free(pos);
+  free(forced);
 }
 
 static void *worker(void *arg) {

@@ -64,6 +64,8 @@ def load_lib(path):
     lib.oracle_run_batch.restype = ctypes.c_int
     lib.oracle_run_batch_spans.argtypes = [p, p, p, i64, ctypes.c_int, p, i64, p, p, p]
     lib.oracle_run_batch_spans.restype = ctypes.c_int
+    lib.oracle_set_added_tokens.argtypes = [p, p, p, p, i64]
+    lib.oracle_set_added_tokens.restype = ctypes.c_int
     lib.oracle_encode_bytes.argtypes = [p, p, i64, p]
     lib.oracle_encode_bytes.restype = i64
     lib.oracle_encode_bytes_plain.argtypes = [p, p, i64, p]
@@ -127,6 +129,19 @@ class Oracle:
             raise ValueError("oracle_create failed: status %d" % rc)
         self._h = h
         self.family = family
+
+    def set_added_tokens(self, literals):
+        """literals: {bytes: id}; extracted leftmost-longest before the
+        family tokenizes the rest (an empty dict clears them)."""
+        items = list(literals.items())
+        data = np.frombuffer(b"".join(k for k, _ in items), dtype=np.uint8).copy()
+        offs = np.zeros(len(items) + 1, dtype=np.int64)
+        np.cumsum([len(k) for k, _ in items], out=offs[1:])
+        ids = np.array([v for _, v in items], dtype=np.int32)
+        rc = self._lib.oracle_set_added_tokens(self._h, data.ctypes.data if len(data) else None, offs.ctypes.data,
+                                               ids.ctypes.data if len(ids) else None, len(items))
+        if rc != 0:
+            raise ValueError("oracle_set_added_tokens failed: status %d" % rc)
 
     def close(self):
         if self._h:

@@ -35,6 +35,7 @@ MUTANTS = {
                         "    if (at + 1 < n) rank[at] = merge_rank(o, ids[at], ids[at + 1]);\n  }\n  return n;\n}\n\nstatic int64_t encode_piece(", "bpe"),
     "span_keeps_right_start": ("if (sstart) memmove(sstart + at + 1, sstart + at + 2,", "if (sstart) memmove(sstart + at, sstart + at + 1,",
                                "spans"),
+    "literal_shortest": ("    if (len > best_len && x + len <= nb", "    if ((best < 0 || len < best_len) && x + len <= nb", "literals"),
     "surrogates_accepted": ("(c >= 0xD800 && c <= 0xDFFF)", "(0)", "utf8"),
 }
 
@@ -74,6 +75,16 @@ def spans_pin_fails(lib):
     return False
 
 
+def literals_pin_fails(lib):
+    from exact_bpe_tokenization_gb300 import synth
+    m, vb, vo = synth.make_vocab(synth.PROFILE_ASCII, 1 << 20, 4096)
+    o = oracle.Oracle(m, vb, vo, 1, lib=lib)
+    n = len(vo) - 1
+    o.set_added_tokens({b"ab": n + 1, b"abc": n + 2})
+    r = o.run(b"abcd", np.array([0, 4], dtype=np.int64))
+    return r["ids"].tolist()[:1] != [n + 2]
+
+
 def bpe_pin_fails(lib):
     m, vb, vo, toks = hand_vocab()
     o = oracle.Oracle(m, vb, vo, 1, lib=lib)
@@ -96,6 +107,8 @@ def test_planted_oracle_fault_is_caught(name, tmp_path, masks):
         assert bpe_pin_fails(lib)
     elif kind == "spans":
         assert spans_pin_fails(lib)
+    elif kind == "literals":
+        assert literals_pin_fails(lib)
     else:
         pt = oracle.pretokenizer(1, lib=lib)
         bad = b"\xed\xa0\x80"
@@ -110,6 +123,7 @@ def test_unmutated_oracle_passes_the_same_pins(masks):
     assert not pretok_pin_fails(lib, 2, masks)
     assert not bpe_pin_fails(lib)
     assert not spans_pin_fails(lib)
+    assert not literals_pin_fails(lib)
 
 
 @pytest.mark.parametrize("fault", ["substitute", "delete", "duplicate", "swap", "tail_resplit"])
