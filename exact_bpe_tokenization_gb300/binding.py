@@ -46,6 +46,7 @@ def lib():
             L.tt_encode_batch.argtypes = [p, p, p, i64, p, p, p]
             L.tt_encode_batch_bounded.argtypes = [p, p, p, i64, i64, p, p, p]
             L.tt_encode_batch_spans.argtypes = [p, p, p, i64, i64, p, p, p, p]
+            L.tt_set_added_tokens.argtypes = [p, p, p, p, i64]
             L.tt_encode_batch_noalloc.argtypes = [p, p, p, i64, i64, p, p, p]
             L.tt_encode_host.argtypes = [p, p, p, i64, p, i64, p, p]
             L.tt_get_status.argtypes = [p, p, ctypes.POINTER(i64)]
@@ -59,6 +60,7 @@ def lib():
             L.tt_launch_count.restype = i64
             L.tt_table_digest.restype = ctypes.c_char_p
             for name in ("tt_create", "tt_encode_batch", "tt_encode_batch_bounded", "tt_encode_batch_spans",
+                         "tt_set_added_tokens",
                          "tt_encode_batch_noalloc",
                          "tt_encode_host",
                          "tt_get_status", "tt_pretokenize_batch", "tt_profile_read"):
@@ -130,6 +132,17 @@ def tt_encode_batch_bounded(h, d_utf8, d_byte_offsets, n_requests, max_total_byt
     _check(lib().tt_encode_batch_bounded(h, _ptr(d_utf8), _ptr(d_byte_offsets), int(n_requests),
                                          int(max_total_bytes), _ptr(d_out_ids), _ptr(d_out_id_offsets),
                                          _stream(stream)), "tt_encode_batch_bounded")
+
+
+def tt_set_added_tokens(h, literals):
+    """literals: {bytes: id} (host); an empty dict removes the set."""
+    items = list(literals.items())
+    data = np.frombuffer(b"".join(k for k, _ in items), dtype=np.uint8).copy()
+    offs = np.zeros(len(items) + 1, dtype=np.int64)
+    np.cumsum([len(k) for k, _ in items], out=offs[1:])
+    ids = np.array([v for _, v in items], dtype=np.int32)
+    _check(lib().tt_set_added_tokens(h, _ptr(data) if len(data) else None, _ptr(offs),
+                                     _ptr(ids) if len(ids) else None, len(items)), "tt_set_added_tokens")
 
 
 def tt_encode_batch_spans(h, d_utf8, d_byte_offsets, n_requests, max_total_bytes, d_out_ids, d_out_id_offsets,
@@ -214,6 +227,10 @@ class Tokenizer:
             out_offsets = torch.empty(n + 1, dtype=torch.int64, device=d_utf8.device)
         tt_encode_batch_bounded(self.h, d_utf8, d_offsets, n, max_total_bytes, out_ids, out_offsets, stream)
         return out_ids, out_offsets
+
+    def set_added_tokens(self, literals):
+        """Reserve literal byte strings as single IDs ({bytes: id})."""
+        tt_set_added_tokens(self.h, literals)
 
     def encode_spans(self, d_utf8, d_offsets, max_total_bytes=None, stream=None):
         """Encode a device batch with byte spans; returns (ids, id_offsets,

@@ -16,7 +16,7 @@ REPO = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(REPO, "_build", "toktier-" + platform.machine())
 LIB = os.path.join(HERE, "libtoktier.so")
-SOURCES = ["tt_api.cu", "tt_pretok.cu", "tt_bpe.cu"]
+SOURCES = ["tt_api.cu", "tt_pretok.cu", "tt_bpe.cu", "tt_literals.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall"]

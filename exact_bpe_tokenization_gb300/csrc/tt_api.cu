@@ -31,9 +31,9 @@ using namespace tt;
 
 namespace {
 
-constexpr int N_KERNELS = 7;
-const char *KERNEL_NAMES[N_KERNELS] = {"k_prepass", "k_tilescan", "k_pretok", "k_bpe_warp",
-                                       "k_bpe_long", "k_ids", "k_req"};
+constexpr int N_KERNELS = 9;
+const char *KERNEL_NAMES[N_KERNELS] = {"k_lit_find", "k_lit_pick", "k_prepass", "k_tilescan", "k_pretok",
+                                       "k_bpe_warp", "k_bpe_long", "k_ids",      "k_req"};
 
 struct Workspace {
   Work W{};
@@ -75,7 +75,16 @@ struct tt_tokenizer {
   double prof_ms[N_KERNELS] = {0};
   int64_t prof_n[N_KERNELS] = {0};
   bool graphs_enabled = true;
+  // host copies of the vocabulary (rebuilt with added-token literals)
+  std::vector<uint8_t> hv_bytes;
+  std::vector<int64_t> hv_off;         // [n_vocab + 1], from 0
+  int64_t n_vocab = 0;
+  int vocab_max_len = 0;
 };
+
+// kernels of one encode: seven, and the two literal kernels when the handle
+// has added-token literals
+static int launches_per_encode(const tt_tokenizer *h) { return 7 + (h->T.n_lit ? 2 : 0); }
 
 #define TT_CUDA(call)                                                   \
   do {                                                                  \
@@ -133,6 +142,54 @@ static tt_status build_class_tables(tt_tokenizer *h) {
   if ((s = upload(h, stage2.data(), stage2.size(), &p2)) != TT_OK) return s;
   h->T.cls1 = (const uint16_t *)p1;
   h->T.cls2 = (const uint8_t *)p2;
+  return TT_OK;
+}
+
+// Whole-piece table, token bytes and offsets for the handle's vocabulary plus
+// n added-token literals (bytes lb[lo[k] .. lo[k+1]) reserved as ID ids[k],
+// every ID >= n_vocab): literal IDs get their bytes at their offsets (IDs
+// between them, none), and the literals enter the hash table first, so that a
+// piece whose bytes are a literal -- only a literal cut out before the
+// family, since any other occurrence of those bytes would have been cut out
+// too -- probes to the literal's ID.
+static tt_status upload_vocab(tt_tokenizer *h, const uint8_t *lb, const int64_t *lo, const int32_t *ids, int64_t n) {
+  int64_t n_ids = h->n_vocab;
+  for (int64_t k = 0; k < n; ++k) n_ids = std::max<int64_t>(n_ids, (int64_t)ids[k] + 1);
+  std::vector<int32_t> owner((size_t)(n_ids - h->n_vocab), -1);
+  for (int64_t k = 0; k < n; ++k) owner[(size_t)(ids[k] - h->n_vocab)] = (int32_t)k;
+  std::vector<uint8_t> bytes = h->hv_bytes;
+  std::vector<int32_t> voff((size_t)n_ids + 1);
+  for (int64_t i = 0; i <= h->n_vocab; ++i) voff[(size_t)i] = (int32_t)h->hv_off[(size_t)i];
+  int max_len = h->vocab_max_len;
+  for (int64_t i = h->n_vocab; i < n_ids; ++i) {
+    const int32_t k = owner[(size_t)(i - h->n_vocab)];
+    if (k >= 0) {
+      bytes.insert(bytes.end(), lb + lo[k], lb + lo[k + 1]);
+      max_len = std::max<int>(max_len, (int)(lo[k + 1] - lo[k]));
+    }
+    voff[(size_t)i + 1] = (int32_t)bytes.size();
+  }
+  const uint64_t vcap = next_pow2((uint64_t)std::max<int64_t>(2 * (h->n_vocab + n), 1024));
+  std::vector<uint64_t> vtab(vcap, 0);
+  auto insert = [&](int64_t id) {
+    const int len = voff[(size_t)id + 1] - voff[(size_t)id];
+    const uint64_t hh = hash_bytes(bytes.data() + voff[(size_t)id], len);
+    uint64_t sl = hh & (vcap - 1);
+    while (vtab[sl] != 0) sl = (sl + 1) & (vcap - 1);
+    vtab[sl] = ((uint64_t)vocab_fp(hh) << 32) | ((uint64_t)len << 20) | (uint64_t)id;
+  };
+  for (int64_t k = 0; k < n; ++k) insert(ids[k]);
+  for (int64_t i = 0; i < h->n_vocab; ++i) insert(i);
+  void *p;
+  tt_status s;
+  if ((s = upload(h, vtab.data(), vtab.size() * 8, &p)) != TT_OK) return s;
+  h->T.vocab_tab = (const uint64_t *)p;
+  h->T.vocab_mask = (uint32_t)(vcap - 1);
+  if ((s = upload(h, bytes.data(), bytes.size(), &p)) != TT_OK) return s;
+  h->T.vbytes = (const uint8_t *)p;
+  if ((s = upload(h, voff.data(), voff.size() * 4, &p)) != TT_OK) return s;
+  h->T.voff = (const int32_t *)p;
+  h->T.max_tok_len = max_len;
   return TT_OK;
 }
 
@@ -211,34 +268,20 @@ extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, con
     while (ptab[sl].x != PAIR_EMPTY) sl = (sl + 1) & (pcap - 1);
     ptab[sl] = make_uint4(l, r, (uint32_t)k, (uint32_t)result[k]);
   }
-  // ---- vocab table
-  const uint64_t vcap = next_pow2((uint64_t)std::max<int64_t>(2 * n_vocab, 1024));
-  std::vector<uint64_t> vtab(vcap, 0);
-  for (int64_t i = 0; i < n_vocab; ++i) {
-    const int len = (int)(vocab_offsets[i + 1] - vocab_offsets[i]);
-    const uint64_t hh = hash_bytes(vocab_bytes + vocab_offsets[i], len);
-    uint64_t sl = hh & (vcap - 1);
-    while (vtab[sl] != 0) sl = (sl + 1) & (vcap - 1);
-    vtab[sl] = ((uint64_t)vocab_fp(hh) << 32) | ((uint64_t)len << 20) | (uint64_t)i;
-  }
-  std::vector<int32_t> voff32((size_t)n_vocab + 1);
-  for (int64_t i = 0; i <= n_vocab; ++i) voff32[i] = (int32_t)(vocab_offsets[i] - vbase);
+  h->n_vocab = n_vocab;
+  h->vocab_max_len = max_len;
+  h->hv_bytes.assign(vocab_bytes + vbase, vocab_bytes + vbase + vtotal);
+  h->hv_off.resize((size_t)n_vocab + 1);
+  for (int64_t i = 0; i <= n_vocab; ++i) h->hv_off[i] = vocab_offsets[i] - vbase;
   void *p;
   if ((s = upload(h, ptab.data(), ptab.size() * sizeof(uint4), &p)) != TT_OK) return fail(s);
   h->T.pair_tab = (const uint4 *)p;
   h->T.pair_mask = (uint32_t)(pcap - 1);
   if ((s = upload(h, result.data(), result.size() * 4, &p)) != TT_OK) return fail(s);
   h->T.merge_result = (const int32_t *)p;
-  if ((s = upload(h, vtab.data(), vtab.size() * 8, &p)) != TT_OK) return fail(s);
-  h->T.vocab_tab = (const uint64_t *)p;
-  h->T.vocab_mask = (uint32_t)(vcap - 1);
-  if ((s = upload(h, vocab_bytes + vbase, (size_t)vtotal, &p)) != TT_OK) return fail(s);
-  h->T.vbytes = (const uint8_t *)p;
-  if ((s = upload(h, voff32.data(), voff32.size() * 4, &p)) != TT_OK) return fail(s);
-  h->T.voff = (const int32_t *)p;
+  if ((s = upload_vocab(h, nullptr, nullptr, nullptr, 0)) != TT_OK) return fail(s);
   if ((s = upload(h, byte_id.data(), 256 * 4, &p)) != TT_OK) return fail(s);
   h->T.byte_id = (const int32_t *)p;
-  h->T.max_tok_len = max_len;
   h->T.family = pattern_family;
   if ((s = build_class_tables(h)) != TT_OK) return fail(s);
   DevStatus init = {0, 0, ~0ull};
@@ -247,6 +290,88 @@ extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, con
   const char *env = getenv("TOKTIER_NO_GRAPHS");
   if (env && env[0] == '1') h->graphs_enabled = false;
   *out = h;
+  return TT_OK;
+}
+
+// strict UTF-8 (RFC 3629): no overlongs, surrogates or code points past U+10FFFF
+static bool valid_utf8(const uint8_t *b, int64_t n) {
+  for (int64_t i = 0; i < n;) {
+    const uint8_t c = b[i];
+    int len;
+    uint32_t cp;
+    if (c < 0x80) { ++i; continue; }
+    if (c >= 0xC2 && c <= 0xDF) { len = 2; cp = c & 0x1F; }
+    else if (c >= 0xE0 && c <= 0xEF) { len = 3; cp = c & 0x0F; }
+    else if (c >= 0xF0 && c <= 0xF4) { len = 4; cp = c & 0x07; }
+    else return false;
+    if (i + len > n) return false;
+    for (int q = 1; q < len; ++q) {
+      if ((b[i + q] & 0xC0) != 0x80) return false;
+      cp = (cp << 6) | (b[i + q] & 0x3F);
+    }
+    if ((len == 3 && cp < 0x800) || (len == 4 && (cp < 0x10000 || cp > 0x10FFFF)) || (cp >= 0xD800 && cp <= 0xDFFF))
+      return false;
+    i += len;
+  }
+  return true;
+}
+
+static void free_workspace(Workspace *w);
+
+extern "C" tt_status tt_set_added_tokens(tt_tokenizer *h, const uint8_t *literal_bytes, const int64_t *literal_offsets,
+                                         const int32_t *literal_ids, int64_t n_literals) {
+  if (!h || n_literals < 0) return TT_ERR_INVALID_ARG;
+  if (n_literals > LIT_MAX_COUNT) return TT_ERR_BAD_VOCAB;
+  if (n_literals > 0 && (!literal_bytes || !literal_offsets || !literal_ids)) return TT_ERR_INVALID_ARG;
+  std::vector<int64_t> lo((size_t)n_literals + 1, 0);
+  std::unordered_map<std::string, int64_t> strings;
+  std::unordered_map<int32_t, int64_t> used;
+  for (int64_t k = 0; k < n_literals; ++k) {
+    const int64_t len = literal_offsets[k + 1] - literal_offsets[k];
+    if (len < 1 || len > LIT_MAX_LEN || literal_offsets[k] < literal_offsets[0]) return TT_ERR_BAD_VOCAB;
+    const uint8_t *b = literal_bytes + literal_offsets[k];
+    if (!valid_utf8(b, len)) return TT_ERR_BAD_VOCAB;
+    const int32_t id = literal_ids[k];
+    if (id < h->n_vocab || id >= (1 << MAX_VOCAB_BITS)) return TT_ERR_BAD_VOCAB;
+    if (!strings.emplace(std::string(reinterpret_cast<const char *>(b), (size_t)len), k).second) return TT_ERR_BAD_VOCAB;
+    if (!used.emplace(id, k).second) return TT_ERR_BAD_VOCAB;
+    lo[(size_t)k + 1] = lo[(size_t)k] + len;
+  }
+  std::lock_guard<std::mutex> lock(h->mu);
+  // literal tables: bytes, offsets, and an order by (first byte, length
+  // descending) with the range of each first byte
+  std::vector<uint8_t> lb((size_t)std::max<int64_t>(lo[(size_t)n_literals], 1));
+  std::vector<int32_t> loff32((size_t)n_literals + 1), order((size_t)std::max<int64_t>(n_literals, 1)), first(257, 0);
+  for (int64_t k = 0; k < n_literals; ++k) {
+    memcpy(lb.data() + lo[(size_t)k], literal_bytes + literal_offsets[k], (size_t)(lo[(size_t)k + 1] - lo[(size_t)k]));
+    loff32[(size_t)k + 1] = (int32_t)lo[(size_t)k + 1];
+    order[(size_t)k] = (int32_t)k;
+  }
+  std::sort(order.begin(), order.begin() + n_literals, [&](int32_t a, int32_t b) {
+    const uint8_t fa = lb[(size_t)lo[(size_t)a]], fb = lb[(size_t)lo[(size_t)b]];
+    if (fa != fb) return fa < fb;
+    return lo[(size_t)a + 1] - lo[(size_t)a] > lo[(size_t)b + 1] - lo[(size_t)b];
+  });
+  for (int64_t k = 0; k < n_literals; ++k) first[lb[(size_t)lo[(size_t)order[(size_t)k]]] + 1] += 1;
+  for (int c = 0; c < 256; ++c) first[(size_t)c + 1] += first[(size_t)c];
+  tt_status s;
+  void *p;
+  if ((s = upload(h, lb.data(), lb.size(), &p)) != TT_OK) return s;
+  h->T.lit_bytes = (const uint8_t *)p;
+  if ((s = upload(h, loff32.data(), loff32.size() * 4, &p)) != TT_OK) return s;
+  h->T.lit_off = (const int32_t *)p;
+  if ((s = upload(h, order.data(), order.size() * 4, &p)) != TT_OK) return s;
+  h->T.lit_order = (const int32_t *)p;
+  if ((s = upload(h, first.data(), first.size() * 4, &p)) != TT_OK) return s;
+  h->T.lit_first = (const int32_t *)p;
+  if ((s = upload_vocab(h, lb.data(), lo.data(), literal_ids, n_literals)) != TT_OK) return s;
+  h->T.n_lit = (int32_t)n_literals;
+  // captured graphs hold the old tables and kernel sequence
+  for (auto &kv : h->ws)
+    if (kv.second->graph) {
+      cudaGraphExecDestroy(kv.second->graph);
+      kv.second->graph = nullptr;
+    }
   return TT_OK;
 }
 
@@ -297,6 +422,8 @@ static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_
       {(void **)&W.huge_list, 4 * (size_t)(cap_bytes / (MID_MAX + 1) + 2)},
       {(void **)&W.bad, (size_t)cap_reqs + 1},          {(void **)&W.bad_pre, 4 * (size_t)(cap_reqs + 2)},
       {(void **)&W.req_piece, 4 * (size_t)(cap_reqs + 1)},
+      {(void **)&W.lit_cand, 4 * (size_t)tiles * TILE}, {(void **)&W.lit_cnt, 4 * (size_t)tiles},
+      {(void **)&W.lit_flag, (size_t)cap_bytes + 8},
       {(void **)&W.args, sizeof(CallArgs)},
   };
   size_t total = 0;
@@ -375,6 +502,9 @@ static int64_t warp_grid(int64_t cap_bytes) {
   return std::min<int64_t>(std::max<int64_t>(g, 1), 152 * BPE_WARP_CTAS_PER_SM);
 }
 static int grid_warp(const Workspace *w) { return (int)warp_grid(w->cap_bytes); }
+static int grid_lit_pick(const Workspace *w) {   // a warp per request
+  return (int)std::min<int64_t>((w->cap_reqs + 7) / 8, 152 * 8);
+}
 static int grid_long(const Workspace *w) {
   return (int)std::min<int64_t>(std::max<int64_t>(w->cap_bytes / (MID_MAX + 1), 1), 152 * 2);
 }
@@ -389,10 +519,15 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
   const Work &W = w->W;
   TT_CUDA(cudaMemsetAsync(W.counters, 0, 4 * 16, stream));
   TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)w->cap_reqs + 1, stream));
+  if (T.n_lit) TT_CUDA(cudaMemsetAsync(W.lit_flag, 0, (size_t)w->cap_bytes + 8, stream));
   if (!timed) {
     if (!w->side) TT_CUDA(cudaStreamCreateWithFlags(&w->side, cudaStreamNonBlocking));
     if (!w->ev_fork) TT_CUDA(cudaEventCreateWithFlags(&w->ev_fork, cudaEventDisableTiming));
     if (!w->ev_join) TT_CUDA(cudaEventCreateWithFlags(&w->ev_join, cudaEventDisableTiming));
+    if (T.n_lit) {
+      launch_lit_find(T, W, grid_tiles(w), stream);
+      launch_lit_pick(T, W, grid_lit_pick(w), stream);
+    }
     launch_prepass(T, W, grid_tiles(w), stream);
     launch_tilescan(T, W, stream);
     launch_pretok(T, W, grid_tiles(w), stream);
@@ -405,26 +540,28 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
     launch_ids(T, W, grid_chunks(w), stream);
     launch_req(T, W, grid_reqs(w), stream);
     TT_CUDA(cudaGetLastError());
-    h->launches += N_KERNELS;
+    h->launches += launches_per_encode(h);
     return TT_OK;
   }
-  for (int kidx = 0; kidx < N_KERNELS; ++kidx) {
+  for (int kidx = T.n_lit ? 0 : 2; kidx < N_KERNELS; ++kidx) {
     cudaEvent_t a = pool_event(h), b = pool_event(h);
     cudaEventRecord(a, stream);
     switch (kidx) {
-      case 0: launch_prepass(T, W, grid_tiles(w), stream); break;
-      case 1: launch_tilescan(T, W, stream); break;
-      case 2: launch_pretok(T, W, grid_tiles(w), stream); break;
-      case 3: launch_bpe_warp(T, W, grid_warp(w), stream); break;
-      case 4: launch_bpe_long(T, W, grid_long(w), stream); break;
-      case 5: launch_ids(T, W, grid_chunks(w), stream); break;
-      case 6: launch_req(T, W, grid_reqs(w), stream); break;
+      case 0: launch_lit_find(T, W, grid_tiles(w), stream); break;
+      case 1: launch_lit_pick(T, W, grid_lit_pick(w), stream); break;
+      case 2: launch_prepass(T, W, grid_tiles(w), stream); break;
+      case 3: launch_tilescan(T, W, stream); break;
+      case 4: launch_pretok(T, W, grid_tiles(w), stream); break;
+      case 5: launch_bpe_warp(T, W, grid_warp(w), stream); break;
+      case 6: launch_bpe_long(T, W, grid_long(w), stream); break;
+      case 7: launch_ids(T, W, grid_chunks(w), stream); break;
+      case 8: launch_req(T, W, grid_reqs(w), stream); break;
     }
     cudaEventRecord(b, stream);
     h->pending.push_back({kidx, a, b});
   }
   TT_CUDA(cudaGetLastError());
-  h->launches += N_KERNELS;
+  h->launches += launches_per_encode(h);
   return TT_OK;
 }
 
@@ -460,7 +597,7 @@ static tt_status encode_bounded(tt_tokenizer *h, const uint8_t *d_utf8, const in
     TT_CUDA(cudaStreamBeginCapture(w->cap_stream, cudaStreamCaptureModeThreadLocal));
     tt_status es = enqueue_encode(h, w, w->cap_stream, false);
     cudaError_t ce = cudaStreamEndCapture(w->cap_stream, &g);
-    h->launches -= N_KERNELS;   // captured, not launched
+    h->launches -= launches_per_encode(h);   // captured, not launched
     if (es != TT_OK) return es;
     TT_CUDA(ce);
     cudaError_t ie = cudaGraphInstantiate(&w->graph, g, 0);
@@ -468,7 +605,7 @@ static tt_status encode_bounded(tt_tokenizer *h, const uint8_t *d_utf8, const in
     TT_CUDA(ie);
   }
   TT_CUDA(cudaGraphLaunch(w->graph, stream));
-  h->launches += N_KERNELS;
+  h->launches += launches_per_encode(h);
   return TT_OK;
 }
 
@@ -592,6 +729,13 @@ extern "C" tt_status tt_pretokenize_batch(tt_tokenizer *h, const uint8_t *d_utf8
   const Work &W = w->W;
   TT_CUDA(cudaMemsetAsync(W.counters, 0, 4 * 16, stream));
   TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)w->cap_reqs + 1, stream));
+  int launched = 6;
+  if (h->T.n_lit) {
+    TT_CUDA(cudaMemsetAsync(W.lit_flag, 0, (size_t)w->cap_bytes + 8, stream));
+    launch_lit_find(h->T, W, grid_tiles(w), stream);
+    launch_lit_pick(h->T, W, grid_lit_pick(w), stream);
+    launched += 2;
+  }
   launch_prepass(h->T, W, grid_tiles(w), stream);
   launch_tilescan(h->T, W, stream);
   launch_pretok(h->T, W, grid_tiles(w), stream);
@@ -599,7 +743,7 @@ extern "C" tt_status tt_pretokenize_batch(tt_tokenizer *h, const uint8_t *d_utf8
   launch_hook_pieces(W, grid_pieces(w), stream);
   launch_hook_offsets(W, grid_reqs(w), stream);
   TT_CUDA(cudaGetLastError());
-  h->launches += 6;
+  h->launches += launched;
   return TT_OK;
 }
 
@@ -638,12 +782,14 @@ extern "C" int tt_profile_read(tt_tokenizer *h, const char **names, double *ms, 
   }
   h->pending.clear();
   int n = 0;
-  for (int k = 0; k < N_KERNELS && n < cap; ++k, ++n) {
+  for (int k = 0; k < N_KERNELS && n < cap; ++k) {
+    if (h->prof_n[k] == 0) continue;          // not launched (the literal kernels without literals)
     if (names) names[n] = KERNEL_NAMES[k];
     if (ms) ms[n] = h->prof_ms[k];
     if (launches) launches[n] = h->prof_n[k];
     h->prof_ms[k] = 0;
     h->prof_n[k] = 0;
+    ++n;
   }
   return n;
 }
@@ -679,6 +825,7 @@ constexpr size_t NA_SIZES[] = {
     4 * 3 * (size_t)list_cap(NA_BYTES), 4 * (size_t)(NA_BYTES / (MID_MAX + 1) + 2),  // lists
     (size_t)NA_REQS + 1, 4 * (size_t)(NA_REQS + 2),                    // bad, bad_pre
     4 * (size_t)(NA_REQS + 1),                                         // req_piece
+    4 * (size_t)NA_TILES * TILE, 4 * (size_t)NA_TILES, (size_t)NA_BYTES + 8,  // lit_cand, lit_cnt, lit_flag
     sizeof(CallArgs),                                                  // args
 };
 constexpr size_t na_total() {
@@ -745,7 +892,8 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
                   (void **)&W.ids_flag, (void **)&W.counters, (void **)&W.piece_start, (void **)&W.n_ids,
                   (void **)&W.id_off,  (void **)&W.scratch,  (void **)&W.tmp_a,    (void **)&W.tmp_b,
                   (void **)&W.tmp_c,   (void **)&W.long_list, (void **)&W.huge_list, (void **)&W.bad,
-                  (void **)&W.bad_pre, (void **)&W.req_piece, (void **)&W.args};
+                  (void **)&W.bad_pre, (void **)&W.req_piece, (void **)&W.lit_cand, (void **)&W.lit_cnt,
+                  (void **)&W.lit_flag, (void **)&W.args};
   static_assert(sizeof(dst) / sizeof(dst[0]) == sizeof(NA_SIZES) / sizeof(NA_SIZES[0]), "layout");
   size_t off = 0;
   for (size_t i = 0; i < sizeof(NA_SIZES) / sizeof(NA_SIZES[0]); ++i) {
@@ -769,6 +917,11 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   const int g_long = (int)std::min<int64_t>(std::max<int64_t>(NA_BYTES / (MID_MAX + 1), 1), 152 * 2);
   const int g_chunks = (int)((NA_BYTES + 1 + IDS_CHUNK - 1) / IDS_CHUNK);
   const int g_reqs = (int)((NA_REQS + 1 + 255) / 256);
+  if (T.n_lit) {
+    TT_CUDA(cudaMemsetAsync(W.lit_flag, 0, (size_t)NA_BYTES + 8, stream));
+    launch_lit_find(T, W, g_tiles, stream);
+    launch_lit_pick(T, W, (int)((NA_REQS + 7) / 8), stream);
+  }
   launch_prepass(T, W, g_tiles, stream);
   launch_tilescan(T, W, stream);
   launch_pretok(T, W, g_tiles, stream);
@@ -777,6 +930,6 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   launch_ids(T, W, g_chunks, stream);
   launch_req(T, W, g_reqs, stream);
   TT_CUDA(cudaGetLastError());
-  h->launches += N_KERNELS;
+  h->launches += launches_per_encode(h);
   return TT_OK;
 }

@@ -63,7 +63,16 @@ struct Tables {
   const int32_t *byte_id;     // [256]
   int32_t max_tok_len;
   int32_t family;
+  // added-token literals (n_lit == 0: none)
+  const uint8_t *lit_bytes;
+  const int32_t *lit_off;     // [n_lit + 1] into lit_bytes
+  const int32_t *lit_order;   // literal indices by (first byte, length descending)
+  const int32_t *lit_first;   // [257]: the lit_order range of each first byte
+  int32_t n_lit;
 };
+constexpr int LIT_MAX_LEN = 255;       // bytes of one literal
+constexpr int LIT_MAX_COUNT = 4095;    // literals (12-bit index)
+enum : uint8_t { LIT_SEG = 1, LIT_INNER = 2 };   // per-byte marks of taken literals
 
 TT_HD uint64_t mix64(uint64_t x) {
   x ^= x >> 33; x *= 0xff51afd7ed558ccdull;
@@ -406,6 +415,10 @@ struct Work {
   uint8_t *bad;                    // [cap_reqs]
   int32_t *bad_pre;                // [cap_reqs + 1] (test hook)
   int32_t *req_piece;              // [cap_reqs + 1] first piece of each non-empty request
+  int32_t *lit_cand;               // [cap_tiles * TILE] literal candidates per tile, position order:
+                                   // position in tile | literal index << 12
+  int32_t *lit_cnt;                // [cap_tiles]
+  uint8_t *lit_flag;               // [cap_bytes + 8] LIT_SEG / LIT_INNER marks of taken literals
   DevStatus *status;
   CallArgs *args;
 };

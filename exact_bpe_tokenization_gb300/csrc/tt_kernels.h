@@ -12,6 +12,8 @@ void launch_prepass(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_tilescan(const Tables &T, const Work &W, cudaStream_t s);
 void launch_pretok(const Tables &T, const Work &W, int grid, cudaStream_t s);
 
+void launch_lit_find(const Tables &T, const Work &W, int grid, cudaStream_t s);
+void launch_lit_pick(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_bpe_warp(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_ids(const Tables &T, const Work &W, int grid, cudaStream_t s);

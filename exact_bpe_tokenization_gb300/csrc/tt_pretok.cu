@@ -34,7 +34,8 @@ struct WinSmem {
   uint8_t cp8[WIN];          // char's code point if ASCII, else 0x80
   uint8_t raw[WIN];          // raw kind
   uint8_t eff[WIN];          // effective kind
-  uint8_t rs[WIN];           // char starts a request
+  uint8_t rs[WIN];           // char starts a request or a segment beside an added-token literal
+  uint8_t lin[WIN];          // char lies inside an added-token literal after its first char
   uint16_t lead[WIN];        // window index of the char's lead byte
   int cbase[NT + 1];         // chars of thread t: [cbase[t], cbase[t+1])
   uint8_t ascii[128];
@@ -117,9 +118,11 @@ __device__ void load_bytes(const Tables &T, const CallArgs &A, int64_t base, int
 
 // Load the window [ws, ws + WIN) of the batch, mark request starts, find
 // char starts, decode and classify.  All threads participate.
+// lit: the batch's added-token marks (LIT_SEG / LIT_INNER per byte), or
+// NULL when the handle has no literals.
 template <int NT>
 __device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, int64_t total, int64_t ws,
-                            WinSmem<NT> &S, int *scan_tmp) {
+                            WinSmem<NT> &S, int *scan_tmp, const uint8_t *lit) {
   constexpr int PT_BYTES = WIN / NT;
   const int tid = threadIdx.x;
   load_bytes<NT>(T, A, base, total, ws, S);
@@ -143,10 +146,12 @@ __device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, in
     const int k = __ffs(m) - 1;
     const int i = PT_BYTES * tid + k;
     const uint32_t cp = decode_at(S, ws, total, i);
+    const uint8_t mark = lit ? __ldg(lit + ws + i) : 0;
     S.lead[j] = (uint16_t)i;
     S.cp8[j] = cp < 128 ? (uint8_t)cp : (uint8_t)0x80;
     S.raw[j] = kind_of(T, S, cp);
-    S.rs[j] = S.rsb[i];
+    S.rs[j] = S.rsb[i] | (mark == LIT_SEG);
+    S.lin[j] = mark == LIT_INNER;
     ++j;
   }
   __syncthreads();
@@ -182,7 +187,7 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
   // decoded where they are met
   const bool bytes_only = T.family != FAM_O200K;
   if (bytes_only) load_bytes<NT>(T, A, base, total, ws, S);
-  else load_window(T, A, base, total, ws, S, scan_tmp);
+  else load_window(T, A, base, total, ws, S, scan_tmp, T.n_lit ? W.lit_flag : nullptr);
 
   // --- UTF-8 validation of the tile's bytes (RFC 3629, per request)
   for (int k = 0; k < PT_BYTES; ++k) {
@@ -241,7 +246,8 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
         int e = 0xFF;
         if (x < te && ((S.bytes[i] & 0xC0) != 0x80 || S.rsb[i])) {
           const uint32_t cp = decode_at(S, ws, total, i);
-          e = rq_ws_event(S.rsb[i] != 0, kind_of(T, S, cp), cp < 128 ? cp : 0x80u);
+          const bool seg = S.rsb[i] != 0 || (T.n_lit && W.lit_flag[x] == LIT_SEG);
+          e = rq_ws_event(seg, kind_of(T, S, cp), cp < 128 ? cp : 0x80u);
         }
         const unsigned m = __ballot_sync(0xffffffffu, e != 0xFF);
         if (m) ev = __shfl_sync(0xffffffffu, e, __ffs(m) - 1);
@@ -449,7 +455,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 0) k_pretok(Tables T, Work
   constexpr int fam = FAM;
   const int64_t ts = (int64_t)t * TILE, te = ts + TILE < total ? ts + TILE : total;
   const int64_t ws = ts - HALO_L;
-  load_window(T, A, base, total, ws, S, P.i_tmp);
+  load_window(T, A, base, total, ws, S, P.i_tmp, T.n_lit ? W.lit_flag : nullptr);
   const int c0 = S.cbase[tid], c1 = S.cbase[tid + 1];
 
   // --- effective kinds (o200k: resolve marks with a max-scan entering at ts - 32)
@@ -550,11 +556,11 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 0) k_pretok(Tables T, Work
   uint32_t starts = 0, placeholder = 0, deferred = 0;   // bit (j - c0) for my chars (<= PT_BYTES)
   const bool filter = __ldcg(&W.counters[5]) != 0;
   auto decide = [&](int j, const Nbr &nb, const Aggs &a, int64_t pos) {
-    bool st = piece_start(fam, nb, a);
+    bool st = piece_start(fam, nb, a) && !S.lin[j];   // an added-token literal is one piece
     if (st && filter) {
       const int64_t r = lower_bound64(A.offs, A.n + 1, base + pos + 1) - 1;
       if (r >= 0 && r < A.n && W.bad[r]) {
-        if (nb.rs) placeholder |= 1u << (j - c0);
+        if (S.rsb[S.lead[j]]) placeholder |= 1u << (j - c0);   // the request's start, not a literal's
         else st = false;
       }
     }

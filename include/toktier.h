@@ -109,6 +109,32 @@ tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges,
                     const uint8_t *vocab_bytes, const int64_t *vocab_offsets, int64_t n_vocab,
                     int32_t pattern_family, tt_tokenizer **out);
 
+/*
+ * tt_set_added_tokens - reserve literal strings as single IDs (added and
+ * special tokens such as "<|endoftext|>").
+ *
+ * TokTier §4.4: a leftmost-longest literal pass extracts them before the
+ * pattern family handles the remaining segments.  Every later encode of the
+ * handle does the same: scanning each request left to right, at the leftmost
+ * position where a literal occurs, the longest literal occurring there is cut
+ * out as one piece with its ID; the text between literals is pre-tokenized as
+ * separate documents (runs are cut at literal boundaries, as at request
+ * boundaries) and encoded as usual.  A literal never spans two requests.
+ *
+ *   literal_bytes    host, the literals concatenated;
+ *   literal_offsets  host, int64 [n_literals + 1]: literal k is
+ *                    literal_bytes[offsets[k] .. offsets[k+1]);
+ *   literal_ids      host, int32 [n_literals]: its reserved ID, distinct,
+ *                    >= the handle's n_vocab and < 2^20;
+ *   n_literals       0 .. 4095; 0 removes the set.
+ * Each literal is 1 .. 255 bytes of valid UTF-8 and no two are equal; else
+ * TT_ERR_BAD_VOCAB and the previous set stays.  The arrays are copied.  Call
+ * it while no encode of the handle is in flight; the next encode on each
+ * stream captures its graph again.  Spans of a literal ID cover its bytes.
+ */
+tt_status tt_set_added_tokens(tt_tokenizer *h, const uint8_t *literal_bytes, const int64_t *literal_offsets,
+                              const int32_t *literal_ids, int64_t n_literals);
+
 /* tt_destroy - release the handle and every device buffer it owns (waits for
  * the handle's outstanding work).  NULL is ignored. */
 void tt_destroy(tt_tokenizer *h);

@@ -84,3 +84,30 @@ def test_no_alloc_rejects_batches_beyond_its_limits(env):
         binding.tt_encode_batch_noalloc(tok.h, d, o, binding.TT_NOALLOC_MAX_REQUESTS + 1, 16, ids, io)
     assert e.value.status == binding.TT_ERR_CAPACITY
     tok.close()
+
+
+def test_no_alloc_with_added_tokens(env):
+    """Literal extraction runs on the fixed scratch too, equal to the
+    regular entry point's output."""
+    merges, vb, vo = synth.make_vocab(synth.PROFILE_MIXED, 8 << 20, 100000)
+    n = len(vo) - 1
+    lits = {b"<|endoftext|>": n + 1, b"<|im_start|>": n + 2, b"<|im": n + 3}
+    text = synth.workload("single_1m_mixed", seed=11, scale=0.05)[0]
+    keys = list(lits)
+    reqs, at = [], 0
+    for i in range(40):                        # 40 requests with literals at varied places
+        c = text[at:at + 700]
+        k = keys[i % 3]
+        reqs.append(c[:i * 13 % 300] + k + c[i * 13 % 300:] if i % 4 else k + c)
+        at += 700
+    data, offs = synth.batch(reqs)
+    assert len(data) <= env.TT_NOALLOC_MAX_BYTES
+    tok = env.Tokenizer(merges, vb, vo, 1)
+    tok.set_added_tokens(lits)
+    d, o = torch.from_numpy(data).cuda(), torch.from_numpy(offs).cuda()
+    want = regular(env, tok, d, o, len(reqs))
+    for _ in range(2):
+        got = no_alloc(env, tok, d, o, len(reqs))
+        assert np.array_equal(got[1], want[1]) and np.array_equal(got[0], want[0])
+    assert np.any(np.isin(want[0], [n + 1, n + 2, n + 3]))
+    tok.close()
