@@ -423,7 +423,7 @@ static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_
       {(void **)&W.bad, (size_t)cap_reqs + 1},          {(void **)&W.bad_pre, 4 * (size_t)(cap_reqs + 2)},
       {(void **)&W.req_piece, 4 * (size_t)(cap_reqs + 1)},
       {(void **)&W.lit_cand, 4 * (size_t)tiles * TILE}, {(void **)&W.lit_cnt, 4 * (size_t)tiles},
-      {(void **)&W.lit_flag, (size_t)cap_bytes + 8},
+      {(void **)&W.lit_flag, (size_t)cap_bytes + 8},   {(void **)&W.lit_len, (size_t)cap_bytes + 8},
       {(void **)&W.args, sizeof(CallArgs)},
   };
   size_t total = 0;
@@ -502,8 +502,8 @@ static int64_t warp_grid(int64_t cap_bytes) {
   return std::min<int64_t>(std::max<int64_t>(g, 1), 152 * BPE_WARP_CTAS_PER_SM);
 }
 static int grid_warp(const Workspace *w) { return (int)warp_grid(w->cap_bytes); }
-static int grid_lit_pick(const Workspace *w) {   // a warp per request
-  return (int)std::min<int64_t>((w->cap_reqs + 7) / 8, 152 * 8);
+static int grid_lit_pick(const Workspace *w) {   // a warp per tile
+  return (int)std::min<int64_t>((grid_tiles(w) + 7) / 8, 152 * 8);
 }
 static int grid_long(const Workspace *w) {
   return (int)std::min<int64_t>(std::max<int64_t>(w->cap_bytes / (MID_MAX + 1), 1), 152 * 2);
@@ -826,6 +826,7 @@ constexpr size_t NA_SIZES[] = {
     (size_t)NA_REQS + 1, 4 * (size_t)(NA_REQS + 2),                    // bad, bad_pre
     4 * (size_t)(NA_REQS + 1),                                         // req_piece
     4 * (size_t)NA_TILES * TILE, 4 * (size_t)NA_TILES, (size_t)NA_BYTES + 8,  // lit_cand, lit_cnt, lit_flag
+    (size_t)NA_BYTES + 8,                                              // lit_len
     sizeof(CallArgs),                                                  // args
 };
 constexpr size_t na_total() {
@@ -893,7 +894,7 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
                   (void **)&W.id_off,  (void **)&W.scratch,  (void **)&W.tmp_a,    (void **)&W.tmp_b,
                   (void **)&W.tmp_c,   (void **)&W.long_list, (void **)&W.huge_list, (void **)&W.bad,
                   (void **)&W.bad_pre, (void **)&W.req_piece, (void **)&W.lit_cand, (void **)&W.lit_cnt,
-                  (void **)&W.lit_flag, (void **)&W.args};
+                  (void **)&W.lit_flag, (void **)&W.lit_len, (void **)&W.args};
   static_assert(sizeof(dst) / sizeof(dst[0]) == sizeof(NA_SIZES) / sizeof(NA_SIZES[0]), "layout");
   size_t off = 0;
   for (size_t i = 0; i < sizeof(NA_SIZES) / sizeof(NA_SIZES[0]); ++i) {
@@ -920,7 +921,7 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   if (T.n_lit) {
     TT_CUDA(cudaMemsetAsync(W.lit_flag, 0, (size_t)NA_BYTES + 8, stream));
     launch_lit_find(T, W, g_tiles, stream);
-    launch_lit_pick(T, W, (int)((NA_REQS + 7) / 8), stream);
+    launch_lit_pick(T, W, (g_tiles + 7) / 8, stream);
   }
   launch_prepass(T, W, g_tiles, stream);
   launch_tilescan(T, W, stream);

@@ -415,9 +415,10 @@ struct Work {
   uint8_t *bad;                    // [cap_reqs]
   int32_t *bad_pre;                // [cap_reqs + 1] (test hook)
   int32_t *req_piece;              // [cap_reqs + 1] first piece of each non-empty request
-  int32_t *lit_cand;               // [cap_tiles * TILE] literal candidates per tile, position order:
-                                   // position in tile | literal index << 12
+  int32_t *lit_cand;               // [cap_tiles * TILE] per tile, the positions (in the tile) of
+                                   // literal candidates no earlier candidate reaches over
   int32_t *lit_cnt;                // [cap_tiles]
+  uint8_t *lit_len;                // [cap_bytes + 8] longest literal starting at each byte (0: none)
   uint8_t *lit_flag;               // [cap_bytes + 8] LIT_SEG / LIT_INNER marks of taken literals
   DevStatus *status;
   CallArgs *args;
