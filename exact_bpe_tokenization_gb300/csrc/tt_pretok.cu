@@ -35,7 +35,6 @@ struct WinSmem {
   uint8_t raw[WIN];          // raw kind
   uint8_t eff[WIN];          // effective kind
   uint8_t rs[WIN];           // char starts a request or a segment beside an added-token literal
-  uint8_t lin[WIN];          // char lies inside an added-token literal after its first char
   uint16_t lead[WIN];        // window index of the char's lead byte
   int cbase[NT + 1];         // chars of thread t: [cbase[t], cbase[t+1])
   uint8_t ascii[128];
@@ -149,9 +148,8 @@ __device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, in
     const uint8_t mark = lit ? __ldg(lit + ws + i) : 0;
     S.lead[j] = (uint16_t)i;
     S.cp8[j] = cp < 128 ? (uint8_t)cp : (uint8_t)0x80;
-    S.raw[j] = kind_of(T, S, cp);
+    S.raw[j] = mark == LIT_INNER ? (uint8_t)K_LIT : kind_of(T, S, cp);
     S.rs[j] = S.rsb[i] | (mark == LIT_SEG);
-    S.lin[j] = mark == LIT_INNER;
     ++j;
   }
   __syncthreads();
@@ -246,8 +244,9 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
         int e = 0xFF;
         if (x < te && ((S.bytes[i] & 0xC0) != 0x80 || S.rsb[i])) {
           const uint32_t cp = decode_at(S, ws, total, i);
-          const bool seg = S.rsb[i] != 0 || (T.n_lit && W.lit_flag[x] == LIT_SEG);
-          e = rq_ws_event(seg, kind_of(T, S, cp), cp < 128 ? cp : 0x80u);
+          const uint8_t mark = T.n_lit ? W.lit_flag[x] : 0;
+          e = rq_ws_event(S.rsb[i] != 0 || mark == LIT_SEG, mark == LIT_INNER ? (uint8_t)K_LIT : kind_of(T, S, cp),
+                          cp < 128 ? cp : 0x80u);
         }
         const unsigned m = __ballot_sync(0xffffffffu, e != 0xFF);
         if (m) ev = __shfl_sync(0xffffffffu, e, __ffs(m) - 1);
@@ -437,7 +436,7 @@ struct Slider {
 };
 
 template <int FAM, int NT>
-__global__ void __launch_bounds__(NT, NT == 512 ? 3 : 0) k_pretok(Tables T, Work W) {
+__global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work W) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   PretokSmem<NT> &P = *reinterpret_cast<PretokSmem<NT> *>(smem_raw);
   WinSmem<NT> &S = P.w;
@@ -556,7 +555,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 0) k_pretok(Tables T, Work
   uint32_t starts = 0, placeholder = 0, deferred = 0;   // bit (j - c0) for my chars (<= PT_BYTES)
   const bool filter = __ldcg(&W.counters[5]) != 0;
   auto decide = [&](int j, const Nbr &nb, const Aggs &a, int64_t pos) {
-    bool st = piece_start(fam, nb, a) && !S.lin[j];   // an added-token literal is one piece
+    bool st = piece_start(fam, nb, a);
     if (st && filter) {
       const int64_t r = lower_bound64(A.offs, A.n + 1, base + pos + 1) - 1;
       if (r >= 0 && r < A.n && W.bad[r]) {

@@ -68,7 +68,8 @@
 namespace tt {
 
 // raw / effective character kinds
-enum : uint8_t { K_OTHER = 0, K_LU = 1, K_LL = 2, K_LB = 3, K_MARK = 4, K_NUM = 5, K_WS = 6, K_NONE = 7 };
+enum : uint8_t { K_OTHER = 0, K_LU = 1, K_LL = 2, K_LB = 3, K_MARK = 4, K_NUM = 5, K_WS = 6, K_NONE = 7,
+                 K_LIT = 8 };   // K_LIT: a char of an added-token literal after its first (never starts a piece)
 enum : int { FAM_CL100K = 1, FAM_O200K = 2 };
 // results of the "first char after i" queries
 enum : uint8_t { R_END = 0, R_CRLF = 1, R_OTHER = 2, R_LETTER = 3 };
@@ -137,6 +138,7 @@ TT_HD bool contraction_end(int fam, const Nbr &n) {
 TT_HD bool piece_start(int fam, const Nbr &n, const Aggs &a) {
   if (n.rs) return true;
   const uint8_t e = n.e0;
+  if (e == K_LIT) return false;
   if (e == K_NUM) return a.nidx3 == 0;
   if (e == K_WS) {
     const bool crlf0 = is_crlf(n.c0);
