@@ -143,7 +143,6 @@ __device__ __forceinline__ int bpe_lanes(const Tables &T, const uint8_t *bytes, 
 // of a run from its left end: the leftmost non-overlapping set.  Pairs made
 // by a merge rank above r (well-ordered list), so they never join a run.
 constexpr int WARP_KERNEL_WARPS = BPE_WARP_THREADS / 32;
-constexpr int MID_SLOTS = MID_MAX / 32;
 constexpr int SMALL_CHUNK = 32;   // pieces per small-piece ticket
 
 __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, const uint8_t *g, int64_t total,
@@ -199,59 +198,43 @@ __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, cons
   }
 }
 
-__device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const uint8_t *g, int pc, int32_t *tok,
-                                          int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
+// The linked-list rounds of one piece of n bytes (32 < n <= 32 * NS) in the
+// warp's shared arrays, NS positions per lane (lane l owns l, l + 32, ...);
+// writes the IDs to out and returns their count.  The ranks of a lane's own
+// positions are read once per step into registers.
+template <int NS>
+__device__ __forceinline__ int list_rounds(const Tables &T, const uint8_t *b, int n, int32_t *out, int32_t *tok,
+                                           int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
   const int lane = threadIdx.x & 31;
   const unsigned lt_mask = (1u << lane) - 1;
-  const int32_t s = __ldcg(&W.piece_start[pc]);
-  const int32_t e = __ldcg(&W.piece_start[pc + 1]) & 0x7FFFFFFF;
-  const int n = e - s;
-  const uint8_t *b = g + s;
-  if (n <= T.max_tok_len) {
-    int id = 0;
-    if (lane == 0) id = vocab_probe(T, b, n);
-    id = __shfl_sync(0xffffffffu, id, 0);
-    if (id >= 0) {
-      if (lane == 0) { W.scratch[s] = id; W.n_ids[pc] = 1; }
-      return;
-    }
-  }
-  if (n <= 32) {                              // one symbol per lane, state in registers
-    const int cnt = bpe_lanes<32>(T, b, n, W.scratch + s);
-    if (lane == 0) W.n_ids[pc] = cnt;
-    return;
-  }
-  const int nslot = (n + 31) >> 5;
 #pragma unroll
-  for (int k = 0; k < MID_SLOTS; ++k) {
+  for (int k = 0; k < NS; ++k) {
     const int p = lane + 32 * k;
-    if (k < nslot) {
-      tok[p] = p < n ? __ldg(&T.byte_id[__ldg(b + p)]) : -1;
-      rank[p] = INT_MAX;
-      nx[p] = (int16_t)(p + 1);
-      pv[p] = (int16_t)(p - 1);
-    }
+    tok[p] = p < n ? __ldg(&T.byte_id[__ldg(b + p)]) : -1;
+    rank[p] = INT_MAX;
+    nx[p] = (int16_t)(p + 1);
+    pv[p] = (int16_t)(p - 1);
   }
   __syncwarp();
-  // initial pair lookups, first probes of four slots in flight together
-  for (int k0 = 0; k0 < nslot; k0 += 4) {
-    uint4 ent[4];
-    uint32_t sl[4];
-    int lt[4], rt[4];
+  // initial pair lookups, first probes of all slots in flight together
+  {
+    uint4 ent[NS];
+    uint32_t sl[NS];
+    int lt[NS], rt[NS];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int p = lane + 32 * (k0 + j);
-      const bool v = k0 + j < nslot && p + 1 < n;
-      lt[j] = v ? tok[p] : 0;
-      rt[j] = v ? tok[p + 1] : 0;
-      sl[j] = pair_slot(T, lt[j], rt[j]);
-      ent[j] = v ? __ldg(&T.pair_tab[sl[j]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+    for (int k = 0; k < NS; ++k) {
+      const int p = lane + 32 * k;
+      const bool v = p + 1 < n;
+      lt[k] = v ? tok[p] : 0;
+      rt[k] = v ? tok[p + 1] : 0;
+      sl[k] = pair_slot(T, lt[k], rt[k]);
+      ent[k] = v ? __ldg(&T.pair_tab[sl[k]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int p = lane + 32 * (k0 + j);
-      if (k0 + j < nslot && p + 1 < n) {
-        const int2 pr = pair_finish(T, ent[j], sl[j], lt[j], rt[j]);
+    for (int k = 0; k < NS; ++k) {
+      const int p = lane + 32 * k;
+      if (p + 1 < n) {
+        const int2 pr = pair_finish(T, ent[k], sl[k], lt[k], rt[k]);
         rank[p] = rank_or_max(pr.x);
         res[p] = pr.y;
       }
@@ -259,20 +242,26 @@ __device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const 
   }
   __syncwarp();
   for (int round = 0; round < n; ++round) {   // each round unlinks at least one symbol
+    int rr[NS];
     int lm = INT_MAX;
 #pragma unroll
-    for (int k = 0; k < MID_SLOTS; ++k)
-      if (k < nslot) lm = min(lm, rank[lane + 32 * k]);
+    for (int k = 0; k < NS; ++k) {
+      rr[k] = rank[lane + 32 * k];
+      lm = min(lm, rr[k]);
+    }
     const int r = __reduce_min_sync(0xffffffffu, lm);
     if (r == INT_MAX) break;
     for (int step = 0; step < n; ++step) {
+      if (step > 0) {                         // ranks changed in the previous step
+#pragma unroll
+        for (int k = 0; k < NS; ++k) rr[k] = rank[lane + 32 * k];
+      }
       uint32_t sel = 0;
       bool left = false;
 #pragma unroll
-      for (int k = 0; k < MID_SLOTS; ++k) {
-        const int p = lane + 32 * k;
-        if (k < nslot && rank[p] == r) {
-          const int q = pv[p];
+      for (int k = 0; k < NS; ++k) {
+        if (rr[k] == r) {
+          const int q = pv[lane + 32 * k];
           if (q < 0 || rank[q] != r) sel |= 1u << k;
           else left = true;
         }
@@ -315,14 +304,46 @@ __device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const 
   // surviving tokens in position order
   int cnt = 0;
 #pragma unroll
-  for (int k = 0; k < MID_SLOTS; ++k) {
-    if (k < nslot) {
-      const int p = lane + 32 * k;
-      const int t = tok[p];
-      const unsigned bal = __ballot_sync(0xffffffffu, t >= 0);
-      if (t >= 0) W.scratch[s + cnt + __popc(bal & lt_mask)] = t;
-      cnt += __popc(bal);
+  for (int k = 0; k < NS; ++k) {
+    const int t = tok[lane + 32 * k];
+    const unsigned bal = __ballot_sync(0xffffffffu, t >= 0);
+    if (t >= 0) out[cnt + __popc(bal & lt_mask)] = t;
+    cnt += __popc(bal);
+  }
+  __syncwarp();
+  return cnt;
+}
+
+__device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const uint8_t *g, int pc, int32_t *tok,
+                                          int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
+  const int lane = threadIdx.x & 31;
+  const int32_t s = __ldcg(&W.piece_start[pc]);
+  const int32_t e = __ldcg(&W.piece_start[pc + 1]) & 0x7FFFFFFF;
+  const int n = e - s;
+  const uint8_t *b = g + s;
+  if (n <= T.max_tok_len) {
+    int id = 0;
+    if (lane == 0) id = vocab_probe(T, b, n);
+    id = __shfl_sync(0xffffffffu, id, 0);
+    if (id >= 0) {
+      if (lane == 0) { W.scratch[s] = id; W.n_ids[pc] = 1; }
+      return;
     }
+  }
+  if (n <= 32) {                              // one symbol per lane, state in registers
+    const int cnt = bpe_lanes<32>(T, b, n, W.scratch + s);
+    if (lane == 0) W.n_ids[pc] = cnt;
+    return;
+  }
+  int cnt;
+  switch ((n + 31) >> 5) {                    // 2 .. MID_MAX / 32 positions per lane
+    case 2: cnt = list_rounds<2>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    case 3: cnt = list_rounds<3>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    case 4: cnt = list_rounds<4>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    case 5: cnt = list_rounds<5>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    case 6: cnt = list_rounds<6>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    case 7: cnt = list_rounds<7>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    default: cnt = list_rounds<8>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
   }
   if (lane == 0) W.n_ids[pc] = cnt;
   __syncwarp();
