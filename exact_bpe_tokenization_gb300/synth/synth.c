@@ -134,15 +134,19 @@ typedef struct {
   int lexicon;              /* words in the lexicon */
   double p_digits, p_punct, p_cjk, p_emoji, p_marks;
   double p_title, p_upper, p_camel, p_contraction, p_latin1, p_blank_run, p_attach;
+  double p_glue;            /* a token follows the previous one with no separator */
+  double p_kana;            /* a CJK token is kana rather than ideographs */
 } profile_t;
 
-static const profile_t PROFILES[3] = {
+static const profile_t PROFILES[4] = {
   /* 0: ASCII code-like text */
   {5000, 0.07, 0.10, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.14},
   /* 1: mixed UTF-8 */
   {50000, 0.065, 0.09, 0.034, 0.085, 0.0, 0.12, 0.04, 0.05, 0.03, 0.035, 0.02, 0.13},
   /* 2: as 1, with camelCase/PascalCase identifiers and combining marks */
   {50000, 0.055, 0.08, 0.036, 0.09, 0.14, 0.08, 0.03, 0.30, 0.03, 0.035, 0.02, 0.13},
+  /* 3: as 1, with kana and ideograph runs often glued to words, digits and punctuation */
+  {50000, 0.08, 0.10, 0.30, 0.01, 0.0, 0.08, 0.03, 0.0, 0.03, 0.02, 0.02, 0.10, 0.35, 0.4},
 };
 
 static const char PUNCT[] = "()[]{};:,.=+-*/<>!&|\"#%@$^~?_'`\\";
@@ -187,6 +191,16 @@ static void put_token(gen_t *g, sink_t *s) {
   }
   if ((u -= pf->p_cjk) < 0) {
     int n = 2 + (int)rnd_below(r, 39);
+    if (pf->p_kana > 0.0 && rnd_chance(r, pf->p_kana)) {
+      /* hiragana / katakana, with a few of the blocks' marks, long-vowel sign and middle dot */
+      static const uint32_t extra[] = {0x30FC, 0x30FB, 0x3099, 0x309B, 0x30FC, 0x309D};
+      for (int i = 0; i < n; ++i) {
+        uint64_t k = rnd_below(r, 100);
+        put_cp(s, k < 50 ? 0x3041u + (uint32_t)rnd_below(r, 86)
+                  : k < 94 ? 0x30A1u + (uint32_t)rnd_below(r, 90) : extra[rnd_below(r, 6)]);
+      }
+      return;
+    }
     for (int i = 0; i < n; ++i) put_cp(s, 0x4E00u + (uint32_t)zipf_draw(r, g->cjk_cdf, 3000));
     return;
   }
@@ -246,7 +260,7 @@ static void gen_lines(gen_t *g, sink_t *s) {
       /* measure the next separator + token into a scratch sink, then copy if it fits */
       uint8_t tmp[512];
       sink_t t = {tmp, 0, sizeof(tmp), 0, 1 << 30, 0};
-      if (!first) {
+      if (!first && !(g->pf->p_glue > 0.0 && rnd_chance(r, g->pf->p_glue))) {
         if (rnd_chance(r, g->pf->p_blank_run)) {
           int n = 1 + (int)rnd_below(r, 64);
           for (int i = 0; i < n; ++i) put_cp(&t, rnd_below(r, 4) ? ' ' : '\t');
@@ -277,7 +291,7 @@ static void gen_lines(gen_t *g, sink_t *s) {
 /* Transcript text of exactly n_chars code points.  Returns the byte length;
  * bytes are written only if they fit in cap (call with out=NULL to size). */
 int64_t synth_transcript(uint64_t seed, int64_t n_chars, int profile, uint8_t *out, int64_t cap) {
-  if (profile < 0 || profile > 2 || n_chars < 0) return -1;
+  if (profile < 0 || profile > 3 || n_chars < 0) return -1;
   gen_t g; gen_init(&g, seed, profile);
   sink_t s = {out, 0, out ? cap : 0, 0, n_chars, n_chars == 0};
   gen_lines(&g, &s);
@@ -392,6 +406,12 @@ static int ck_class(uint32_t cp) {
   if (cp >= 0x1F000 && cp < 0x20000) return CK_OTH;     /* pictographs */
   return CK_LET;                                          /* other non-ASCII: treated as letters */
 }
+/* with han_split, kana / CJK ideograph runs are chunks of their own */
+enum { CK_HAN = 5 };
+static int ck_class2(uint32_t cp, int han_split) {
+  if (han_split && ((cp >= 0x3040 && cp <= 0x30FF) || (cp >= 0x4E00 && cp <= 0x9FFF))) return CK_HAN;
+  return ck_class(cp);
+}
 static int ck_upper(uint32_t cp) { return (cp >= 'A' && cp <= 'Z') || (cp >= 0xC0 && cp <= 0xDE); }
 
 typedef struct { int64_t start, len; } span_t;
@@ -413,7 +433,8 @@ static int64_t utf8_decode_all(const uint8_t *t, int64_t n, uint32_t *cps, int64
 
 /* split into chunks (byte spans); case_split also cuts lower->Upper inside letter runs
  * and keeps a following 's/'t/... on the word */
-static int64_t crude_chunks(const uint8_t *t, int64_t n, int case_split, span_t **out) {
+static int64_t crude_chunks(const uint8_t *t, int64_t n, int flags, span_t **out) {
+  const int case_split = flags & 1, han = (flags >> 1) & 1;
   uint32_t *cp = malloc(sizeof(uint32_t) * (size_t)(n + 1));
   int64_t *pos = malloc(sizeof(int64_t) * (size_t)(n + 2));
   int64_t m = utf8_decode_all(t, n, cp, pos);
@@ -422,33 +443,34 @@ static int64_t crude_chunks(const uint8_t *t, int64_t n, int case_split, span_t 
 #define EMIT(a, b) do { sp[k].start = pos[a]; sp[k].len = pos[b] - pos[a]; ++k; } while (0)
   int64_t i = 0;
   while (i < m) {
-    int c = ck_class(cp[i]);
+    int c = ck_class2(cp[i], han);
     int64_t j = i;
     if (c == CK_BLANK) {
-      while (j < m && ck_class(cp[j]) == CK_BLANK) ++j;
-      int nx = j < m ? ck_class(cp[j]) : CK_NL;
+      while (j < m && ck_class2(cp[j], han) == CK_BLANK) ++j;
+      int nx = j < m ? ck_class2(cp[j], han) : CK_NL;
       if ((nx == CK_LET || nx == CK_OTH) && j - i >= 2) { EMIT(i, j - 1); i = j - 1; continue; }
       if (nx == CK_LET || nx == CK_OTH) { /* single blank joins the next chunk */
         int64_t s = i; i = j; c = nx; j = i;
         if (c == CK_LET) {
-          while (j < m && ck_class(cp[j]) == CK_LET && !(case_split && j > i && ck_upper(cp[j]) && !ck_upper(cp[j - 1]))) ++j;
+          while (j < m && ck_class2(cp[j], han) == CK_LET && !(case_split && j > i && ck_upper(cp[j]) && !ck_upper(cp[j - 1]))) ++j;
         } else {
-          while (j < m && ck_class(cp[j]) == CK_OTH) ++j;
+          while (j < m && ck_class2(cp[j], han) == CK_OTH) ++j;
         }
         EMIT(s, j); i = j; continue;
       }
       EMIT(i, j); i = j; continue;
     }
-    if (c == CK_NL) { while (j < m && ck_class(cp[j]) == CK_NL) ++j; EMIT(i, j); i = j; continue; }
-    if (c == CK_DIG) { while (j < m && j - i < 3 && ck_class(cp[j]) == CK_DIG) ++j; EMIT(i, j); i = j; continue; }
+    if (c == CK_HAN) { while (j < m && ck_class2(cp[j], han) == CK_HAN) ++j; EMIT(i, j); i = j; continue; }
+    if (c == CK_NL) { while (j < m && ck_class2(cp[j], han) == CK_NL) ++j; EMIT(i, j); i = j; continue; }
+    if (c == CK_DIG) { while (j < m && j - i < 3 && ck_class2(cp[j], han) == CK_DIG) ++j; EMIT(i, j); i = j; continue; }
     if (c == CK_LET) {
       ++j;
-      while (j < m && ck_class(cp[j]) == CK_LET && !(case_split && ck_upper(cp[j]) && !ck_upper(cp[j - 1]))) ++j;
-      if (case_split && j + 1 < m && cp[j] == '\'' && ck_class(cp[j + 1]) == CK_LET) j += 2;
+      while (j < m && ck_class2(cp[j], han) == CK_LET && !(case_split && ck_upper(cp[j]) && !ck_upper(cp[j - 1]))) ++j;
+      if (case_split && j + 1 < m && cp[j] == '\'' && ck_class2(cp[j + 1], han) == CK_LET) j += 2;
       EMIT(i, j); i = j; continue;
     }
     /* other */
-    while (j < m && ck_class(cp[j]) == CK_OTH) ++j;
+    while (j < m && ck_class2(cp[j], han) == CK_OTH) ++j;
     EMIT(i, j); i = j;
   }
 #undef EMIT
@@ -517,9 +539,9 @@ static void wlist_add(wlist_t *l, int32_t w) {
 }
 #define PAIR(a, b) (((uint64_t)(uint32_t)(a) << 32) | (uint32_t)(b))
 
-int64_t synth_train_bpe(const uint8_t *text, int64_t len, int64_t n_merges, int case_split, int32_t *out_pairs) {
+int64_t synth_train_bpe(const uint8_t *text, int64_t len, int64_t n_merges, int flags, int32_t *out_pairs) {
   span_t *sp;
-  int64_t nch = crude_chunks(text, len, case_split, &sp);
+  int64_t nch = crude_chunks(text, len, flags, &sp);
   /* unique chunks with counts: hash of bytes -> word index (collisions resolved by compare) */
   map_t wmap; map_init(&wmap, 1 << 20);
   word_t *words = NULL; int64_t nw = 0, capw = 0;

@@ -1,9 +1,10 @@
 """Python side of the seeded input generators (ctypes over synth.c).
 
 Everything here produces inputs: UTF-8 request batches and merge lists.  The
-workload table mirrors the five configurations the benchmark and the parity
-tests use (tiny ASCII request; 1M-char mixed request; 64-request rebuild
-burst; 4.4M-char adversarial request; 256-request o200k-style batch).
+workload table mirrors the configurations the benchmark and the parity tests
+use (tiny ASCII request; 1M-char mixed request; 64-request rebuild burst;
+4.4M-char adversarial request; 256-request o200k-style batch; 64-request
+deepseek-style batch of kana/CJK-mixed text).
 """
 import ctypes
 import hashlib
@@ -18,12 +19,12 @@ REPO = os.path.dirname(os.path.dirname(HERE))
 LIB_PATH = os.path.join(HERE, "libttsynth.so")
 CACHE_DIR = os.path.join(REPO, "_build", "cache")
 
-PROFILE_ASCII, PROFILE_MIXED, PROFILE_CAMEL_MARKS = 0, 1, 2
+PROFILE_ASCII, PROFILE_MIXED, PROFILE_CAMEL_MARKS, PROFILE_KANA_HAN = 0, 1, 2, 3
 # bumped whenever synth.c changes what it writes (part of every cache key)
 GENERATOR_VERSION = 1
 
 # pattern-family ids, as data (the same numbers the C ABI uses)
-FAMILY_CL100K_STYLE, FAMILY_O200K_STYLE = 1, 2
+FAMILY_CL100K_STYLE, FAMILY_O200K_STYLE, FAMILY_DEEPSEEK_STYLE = 1, 2, 3
 
 _lib = None
 _lock = threading.Lock()
@@ -108,11 +109,14 @@ def lengths_lognormal(seed, n, median, sigma, cap):
     return out
 
 
-def train_merges(text, n_merges, case_split=False):
-    """Greedy BPE merges (rank = row) trained on `text`; int32 [k, 2]."""
+def train_merges(text, n_merges, case_split=False, han_split=False):
+    """Greedy BPE merges (rank = row) trained on `text`; int32 [k, 2].
+    case_split cuts training chunks at lower-to-upper changes; han_split
+    makes kana / CJK ideograph runs chunks of their own."""
     buf = np.frombuffer(text, dtype=np.uint8)
     out = np.empty((n_merges, 2), dtype=np.int32)
-    k = _get().synth_train_bpe(buf.ctypes.data, len(buf), n_merges, int(bool(case_split)), out.ctypes.data)
+    flags = int(bool(case_split)) | (int(bool(han_split)) << 1)
+    k = _get().synth_train_bpe(buf.ctypes.data, len(buf), n_merges, flags, out.ctypes.data)
     return out[:k].copy()
 
 
@@ -150,7 +154,8 @@ def make_vocab(profile, corpus_bytes, n_merges, seed=0):
     if merges is None:
         # ~1.0-1.3 bytes per char for these profiles: ask for enough chars, then cut
         text = _cut_bytes(transcript(seed, corpus_bytes, profile), corpus_bytes)
-        merges = train_merges(text, n_merges, case_split=(profile == PROFILE_CAMEL_MARKS))
+        merges = train_merges(text, n_merges, case_split=(profile == PROFILE_CAMEL_MARKS),
+                              han_split=(profile == PROFILE_KANA_HAN))
         os.makedirs(CACHE_DIR, exist_ok=True)
         tmp = path + ".%d.tmp.npy" % os.getpid()
         np.save(tmp, merges)
@@ -186,6 +191,10 @@ WORKLOADS = {
         desc="256 requests, lognormal chars (median 120K, sigma 1.0, cap 1M; seeds 1000+i); camelCase + marks; "
              "200,000 merges on 16 MiB; o200k-style",
         vocab=(PROFILE_CAMEL_MARKS, 16 * MIB, 200000), family=FAMILY_O200K_STYLE),
+    "deepseek_64_loguniform": dict(
+        desc="64 requests, log-uniform 10K..1M chars of kana/CJK-mixed text (seeds 2000+i); 100,000 merges on "
+             "8 MiB; deepseek-style",
+        vocab=(PROFILE_KANA_HAN, 8 * MIB, 100000), family=FAMILY_DEEPSEEK_STYLE),
 }
 
 
@@ -207,6 +216,9 @@ def workload(name, seed=None, scale=1.0):
     if name == "o200k_256_lognormal":
         lens = lengths_lognormal(4, 256, 120_000, 1.0, 1_000_000)
         return [transcript(1000 + i, n(int(l)), PROFILE_CAMEL_MARKS) for i, l in enumerate(lens)]
+    if name == "deepseek_64_loguniform":
+        lens = lengths_loguniform(5, 64, 10_000, 1_000_000)
+        return [transcript(2000 + i, n(int(l)), PROFILE_KANA_HAN) for i, l in enumerate(lens)]
     raise KeyError(name)
 
 

@@ -42,6 +42,17 @@
  *     O1  [^\r\n\p{L}\p{N}]?U*W+K?
  *     O2  [^\r\n\p{L}\p{N}]?U+W*K?
  *     O3..O7 as C3..C7
+ *   deepseek-style (the paper, §4.1: DeepSeek-family tokenizers run three
+ *   splitters one after another; each one re-splits every piece the one
+ *   before it produced, and the text between two of its matches stays a
+ *   piece of its own).  The three splitters:
+ *     D1  \p{N}{1,3}
+ *     D2  [\x{3040}-\x{30FF}\x{4E00}-\x{9FFF}]+   (Hiragana, Katakana and CJK
+ *         Unified Ideographs blocks)
+ *     D3  C1 | C2 | C4 | C5 | C6 | C7   (no digit alternative: a digit group
+ *         left by D1 matches nothing and survives whole)
+ *   A splitter applied to a piece sees that piece as its whole subject: the
+ *   piece's end is the end of the text for C6's lookahead.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -49,7 +60,7 @@
 #include <pthread.h>
 
 enum { B_L = 1, B_LU = 2, B_LL = 4, B_LT = 8, B_LM = 16, B_LO = 32, B_M = 64, B_N = 128, B_S = 256 };
-enum { FAM_CL100K = 1, FAM_O200K = 2 };
+enum { FAM_CL100K = 1, FAM_O200K = 2, FAM_DEEPSEEK = 3 };
 enum { OK = 0, ERR_ARG = 1, ERR_VOCAB = 2, ERR_FAMILY = 3, ERR_UTF8 = 4, ERR_CAPACITY = 5, ERR_OOM = 6 };
 
 typedef struct {
@@ -82,6 +93,8 @@ static int isOther(const oracle_t *o, uint32_t c) { return !isS(o, c) && !isL(o,
 /* o200k U = [\p{Lu}\p{Lt}\p{Lm}\p{Lo}\p{M}], W = [\p{Ll}\p{Lm}\p{Lo}\p{M}] */
 static int isUpperSet(const oracle_t *o, uint32_t c) { return mask(o, c) & (B_LU | B_LT | B_LM | B_LO | B_M); }
 static int isLowerSet(const oracle_t *o, uint32_t c) { return mask(o, c) & (B_LL | B_LM | B_LO | B_M); }
+/* deepseek-style D2: the Hiragana, Katakana and CJK Unified Ideographs blocks */
+static int isKanaHan(uint32_t c) { return (c >= 0x3040 && c <= 0x30FF) || (c >= 0x4E00 && c <= 0x9FFF); }
 
 /* ------------------------------------------------------- strict UTF-8 */
 /* RFC 3629: no overlongs, no surrogates, nothing above U+10FFFF, no stray or
@@ -234,8 +247,54 @@ static int64_t match_at(const oracle_t *o, const uint32_t *c, int64_t n, int64_t
   return -1;   /* unreachable: every code point is L, N, \s or other */
 }
 
+/* deepseek-style: the end of a match of splitter `stage` (1 = D1, 2 = D2,
+ * 3 = D3) at p inside the subject c[0..n), or -1 */
+static int64_t ds_match(const oracle_t *o, int stage, const uint32_t *c, int64_t n, int64_t p) {
+  int64_t e;
+  if (stage == 1) return alt_digits(o, c, n, p);
+  if (stage == 2) {
+    e = p;
+    while (e < n && isKanaHan(c[e])) ++e;
+    return e > p ? e : -1;
+  }
+  int k = contraction_len(c, n, p);
+  if (k) return p + k;
+  if ((e = alt_letters(o, c, n, p)) > 0) return e;
+  if ((e = alt_other(o, c, n, p)) > 0) return e;
+  if ((e = alt_newlines(o, c, n, p)) > 0) return e;
+  if ((e = alt_trailing_ws(o, c, n, p)) > 0) return e;
+  return alt_ws(o, c, n, p);
+}
+
+static int64_t ds_split(const oracle_t *o, int stage, const uint32_t *c, int64_t a, int64_t b, int64_t *starts,
+                        int64_t k);
+/* a piece [a, b) that splitter `stage` produced: the last splitter's pieces
+ * are final, the others go to the next splitter */
+static int64_t ds_emit(const oracle_t *o, int stage, const uint32_t *c, int64_t a, int64_t b, int64_t *starts,
+                       int64_t k) {
+  if (stage == 3) { starts[k] = a; return k + 1; }
+  return ds_split(o, stage + 1, c, a, b, starts, k);
+}
+/* Splitter `stage` over the piece c[a..b), which is its whole subject: scan
+ * for the leftmost match from the end of the previous one; the stretch
+ * skipped before a match (and the rest after the last match) is a piece too. */
+static int64_t ds_split(const oracle_t *o, int stage, const uint32_t *c, int64_t a, int64_t b, int64_t *starts,
+                        int64_t k) {
+  int64_t p = a, q = a;   /* p: start of the unmatched stretch; q: where a match is tried */
+  while (q < b) {
+    const int64_t e = ds_match(o, stage, c + a, b - a, q - a);
+    if (e < 0) { ++q; continue; }
+    if (q > p) k = ds_emit(o, stage, c, p, q, starts, k);
+    k = ds_emit(o, stage, c, q, a + e, starts, k);
+    p = q = a + e;
+  }
+  if (b > p) k = ds_emit(o, stage, c, p, b, starts, k);
+  return k;
+}
+
 /* pre-tokenize c[0..n): writes piece start indices (char indices); returns count */
 static int64_t pretokenize_chars(const oracle_t *o, const uint32_t *c, int64_t n, int64_t *starts) {
+  if (o->family == FAM_DEEPSEEK) return ds_split(o, 1, c, 0, n, starts, 0);
   int64_t p = 0, k = 0;
   while (p < n) {
     int64_t e = match_at(o, c, n, p);
@@ -300,7 +359,7 @@ int oracle_create(const uint16_t *cls, int family,
                   const int32_t *merges, int64_t n_merges,
                   const uint8_t *vbytes, const int64_t *voff, int64_t n_vocab, void **out) {
   if (!cls || !out || n_vocab < 256 || n_merges < 0 || (n_merges && !merges)) return ERR_ARG;
-  if (family != FAM_CL100K && family != FAM_O200K) return ERR_FAMILY;
+  if (family != FAM_CL100K && family != FAM_O200K && family != FAM_DEEPSEEK) return ERR_FAMILY;
   oracle_t *o = calloc(1, sizeof(oracle_t));
   o->cls = cls; o->family = family; o->n_vocab = n_vocab; o->n_merges = n_merges;
   int64_t nb = voff[n_vocab] - voff[0];

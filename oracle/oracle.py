@@ -19,7 +19,7 @@ REPO = os.path.dirname(HERE)
 LIB_PATH = os.path.join(HERE, "liboracle.so")
 CLASS_TABLE = os.path.join(REPO, "exact_bpe_tokenization_gb300", "data", "char_classes.txt")
 
-FAMILY_CL100K_STYLE, FAMILY_O200K_STYLE = 1, 2
+FAMILY_CL100K_STYLE, FAMILY_O200K_STYLE, FAMILY_DEEPSEEK_STYLE = 1, 2, 3
 ERR_UTF8 = 4
 
 _lib = None

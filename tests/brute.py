@@ -8,8 +8,10 @@
    backtracking").  It shares nothing with oracle.c but the frozen class table.
 2. The textbook BPE definition: every step rescans all adjacent pairs, takes
    the lowest rank and merges its leftmost occurrence (TokTier, §4.2).
-3. The same two pattern families as pattern strings for the installed `regex`
+3. The same pattern families as pattern strings for the installed `regex`
    module (a library run, used as a second cross-check where installed).
+4. The deepseek-style family's three splitters, run one after another by a
+   plain split driver over either matcher.
 """
 import sys
 
@@ -129,6 +131,60 @@ def family_ast(family, masks):
                *tail)
 
 
+def is_kana_han(c):
+    """deepseek-style D2 set: the Hiragana, Katakana and CJK Unified
+    Ideographs blocks."""
+    return 0x3040 <= c <= 0x30FF or 0x4E00 <= c <= 0x9FFF
+
+
+def deepseek_asts(masks):
+    """The three splitters of the deepseek-style family, in order, as ASTs:
+    digit groups, kana/CJK runs, then the cl100k-style alternatives without
+    the digit alternative."""
+    def m(c):
+        return int(masks[c]) if c < len(masks) else 0
+    isL = lambda c: m(c) & B_L
+    isN = lambda c: m(c) & B_N
+    isS = lambda c: m(c) & B_S
+    crlf = lambda c: c in (10, 13)
+    pre = Cls(lambda c: not crlf(c) and not isL(c) and not isN(c))
+    other = Cls(lambda c: not isS(c) and not isL(c) and not isN(c))
+    contraction = Seq(Lit("'"), Alt(*(Lit(x, ci=True) for x in ("s", "t", "re", "ve", "m", "ll", "d"))))
+    third = Alt(contraction, Seq(Opt(pre), Plus(Cls(isL))),
+                Seq(Opt(Lit(" ")), Plus(other), Star(Cls(crlf))),
+                Seq(Star(Cls(isS)), Plus(Cls(crlf))),
+                Seq(Plus(Cls(isS)), NegLook(Cls(lambda c: not isS(c)))),
+                Plus(Cls(isS)))
+    return [Rep(Cls(isN), 1, 3), Plus(Cls(is_kana_han)), third]
+
+
+def split_pieces(ast, s):
+    """One splitter over the subject s: the leftmost match from the end of
+    the previous one is a piece, and so is each stretch between matches."""
+    out, p, q = [], 0, 0
+    while q < len(s):
+        e = _m(ast, s, q, lambda j: j)
+        if e is None:
+            q += 1
+            continue
+        assert e > q
+        if q > p:
+            out.append(s[p:q])
+        out.append(s[q:e])
+        p = q = e
+    if p < len(s):
+        out.append(s[p:])
+    return out
+
+
+def split_sequence(splitters, s, split=split_pieces):
+    """Splitters in sequence: each re-splits every piece of the one before."""
+    pieces = [s] if s else []
+    for sp in splitters:
+        pieces = [x for piece in pieces for x in split(sp, piece)]
+    return pieces
+
+
 def brute_pieces(ast, s):
     """Leftmost-first scan: the first alternative matching at p is the piece."""
     out, p = [], 0
@@ -168,6 +224,27 @@ REGEX_PATTERNS = {
     2: (r"[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}\p{Lm}\p{Lo}\p{M}]*[\p{Ll}\p{Lm}\p{Lo}\p{M}]+" + _K + "?|"
         r"[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}\p{Lm}\p{Lo}\p{M}]+[\p{Ll}\p{Lm}\p{Lo}\p{M}]*" + _K + "?|" + TAIL),
 }
+
+
+DEEPSEEK_REGEX_SPLITTERS = [
+    r"\p{N}{1,3}",
+    r"[\u3040-\u30FF\u4E00-\u9FFF]+",
+    _K + r"|[^\r\n\p{L}\p{N}]?\p{L}+| ?[^\s\p{L}\p{N}]+[\r\n]*|\s*[\r\n]+|\s+(?!\S)|\s+",
+]
+
+
+def regex_split(pat, s):
+    """One splitter run by the regex engine: its matches over s, with the
+    stretches between them kept as pieces."""
+    out, p = [], 0
+    for mt in pat.finditer(s):
+        if mt.start() > p:
+            out.append(s[p:mt.start()])
+        out.append(mt.group())
+        p = mt.end()
+    if p < len(s):
+        out.append(s[p:])
+    return out
 
 
 def all_strings(alphabet, max_len):

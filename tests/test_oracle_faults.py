@@ -37,6 +37,11 @@ MUTANTS = {
                                "spans"),
     "literal_shortest": ("    if (len > best_len && x + len <= nb", "    if ((best < 0 || len < best_len) && x + len <= nb", "literals"),
     "surrogates_accepted": ("(c >= 0xD800 && c <= 0xDFFF)", "(0)", "utf8"),
+    "deepseek_katakana_missing": ("(c >= 0x3040 && c <= 0x30FF) || (c >= 0x4E00", "(c >= 0x3040 && c <= 0x309F) || (c >= 0x4E00",
+                                  "pretok3"),
+    "deepseek_gap_dropped": ("    if (q > p) k = ds_emit(o, stage, c, p, q, starts, k);\n", "", "pretok3"),
+    "deepseek_no_rescan_of_pieces": ("  if (stage == 3) { starts[k] = a; return k + 1; }",
+                                     "  if (stage >= 2) { starts[k] = a; return k + 1; }", "pretok3"),
 }
 
 
@@ -58,6 +63,15 @@ def pretok_pin_fails(lib, family, masks):
     pt = oracle.pretokenizer(family, lib=lib)
     for s in brute.all_strings(alpha, 4):
         if pt.pieces(s) != brute.brute_pieces(ast, s):
+            return True
+    return False
+
+
+def deepseek_pin_fails(lib, masks):
+    asts = brute.deepseek_asts(masks)
+    pt = oracle.pretokenizer(3, lib=lib)
+    for s in brute.all_strings(["a", "1", " ", "\n", "'", ".", "日", "・", "s"], 4):
+        if pt.pieces(s) != brute.split_sequence(asts, s):
             return True
     return False
 
@@ -103,6 +117,8 @@ def test_planted_oracle_fault_is_caught(name, tmp_path, masks):
         assert pretok_pin_fails(lib, 1, masks)
     elif kind == "pretok2":
         assert pretok_pin_fails(lib, 2, masks)
+    elif kind == "pretok3":
+        assert deepseek_pin_fails(lib, masks)
     elif kind == "bpe":
         assert bpe_pin_fails(lib)
     elif kind == "spans":
@@ -121,6 +137,7 @@ def test_unmutated_oracle_passes_the_same_pins(masks):
     lib = oracle.oracle._get()
     assert not pretok_pin_fails(lib, 1, masks)
     assert not pretok_pin_fails(lib, 2, masks)
+    assert not deepseek_pin_fails(lib, masks)
     assert not bpe_pin_fails(lib)
     assert not spans_pin_fails(lib)
     assert not literals_pin_fails(lib)
