@@ -13,6 +13,8 @@ One JSON line on stdout (rank 0).  Keys beyond the base contract:
                     against the measured HBM copy bandwidth
   cpu_baseline      the CPU oracle on the host cores (a bounded sample)
   batched_gbs       the 64-request rebuild burst (~20 MB) as one call
+  deepseek_batched_gbs  the same batch shape of kana/CJK-mixed text in the
+                    deepseek-style family, as one call
 
 --impl reference times the CPU oracle on the same workload and metric.
 Under torchrun (N > 1) every rank encodes its own requests (replicas; the
@@ -45,6 +47,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-families", action="store_true", help="skip the deepseek-style batch line")
     ap.add_argument("--ncu-case", metavar="WORKLOAD", default=None,
                     help="encode one batch of WORKLOAD once and exit (a small case for an ncu capture)")
     return ap.parse_args()
@@ -470,30 +473,44 @@ def run_ours(args):
                      "pieces": classes},
         "kernels_ms_per_launch": {k: round(v["ms_per_launch"], 5) for k, v in per_kernel.items()},
     }
-    # the batched burst (~20 MB, 64 requests) as one call, for the batched part of the metric
-    try:
-        reqs = synth.workload("burst_64_loguniform")
+    def batched(name, h):
+        """One named multi-request workload as one call: median of 10 calls,
+        L2 flushed before each."""
+        reqs = synth.workload(name)
         data, bo = synth.batch(reqs)
         d = torch.from_numpy(data).to(dev)
         o = torch.from_numpy(bo).to(dev)
         bi = torch.empty(len(data), dtype=torch.int32, device=dev)
         bio = torch.empty(len(bo), dtype=torch.int64, device=dev)
         for _ in range(3):
-            binding.tt_encode_batch_bounded(tok.h, d, o, len(reqs), len(data), bi, bio, stream)
+            binding.tt_encode_batch_bounded(h, d, o, len(reqs), len(data), bi, bio, stream)
         ts = []
         for i in range(10):
             flush.fill_(i)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
-            binding.tt_encode_batch_bounded(tok.h, d, o, len(reqs), len(data), bi, bio, stream)
+            binding.tt_encode_batch_bounded(h, d, o, len(reqs), len(data), bi, bio, stream)
             e.record(stream)
             e.synchronize()
             ts.append(s.elapsed_time(e))
-        line["batched_gbs"] = {"workload": "burst_64_loguniform", "bytes": len(data),
-                               "value": len(data) / (statistics.median(ts) / 1e3) / 1e9, "unit": UNIT,
-                               "ms_median": statistics.median(ts)}
+        st, _ = binding.tt_get_status(h, stream)
+        return {"workload": name, "bytes": len(data), "value": len(data) / (statistics.median(ts) / 1e3) / 1e9,
+                "unit": UNIT, "ms_median": statistics.median(ts), "status": st}
+
+    # the batched burst (~20 MB, 64 requests) as one call, for the batched part of the metric
+    try:
+        line["batched_gbs"] = batched("burst_64_loguniform", tok.h)
     except Exception as exc:  # reported, never fatal to the main line
         line["batched_gbs"] = {"error": str(exc)}
+    # the same shape of batch in the deepseek-style family (kana/CJK-mixed text)
+    if not args.no_families:
+        try:
+            Wd = synth.WORKLOADS["deepseek_64_loguniform"]
+            dtok = binding.Tokenizer(*synth.make_vocab(*Wd["vocab"]), Wd["family"])
+            line["deepseek_batched_gbs"] = batched("deepseek_64_loguniform", dtok.h)
+            dtok.close()
+        except Exception as exc:  # reported, never fatal to the main line
+            line["deepseek_batched_gbs"] = {"error": str(exc)}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline((merges, vb, vo), family, list(range(1, 25)))
     print(json.dumps(line), flush=True)

@@ -18,7 +18,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "toktier.h")
 
 TT_OK, TT_ERR_INVALID_ARG, TT_ERR_BAD_VOCAB, TT_ERR_BAD_FAMILY, TT_ERR_INVALID_UTF8, \
     TT_ERR_CAPACITY, TT_ERR_OOM, TT_ERR_CUDA, TT_ERR_TIMEOUT = range(9)
-TT_FAMILY_CL100K_STYLE, TT_FAMILY_O200K_STYLE = 1, 2
+TT_FAMILY_CL100K_STYLE, TT_FAMILY_O200K_STYLE, TT_FAMILY_DEEPSEEK_STYLE = 1, 2, 3
 TT_NOALLOC_MAX_BYTES, TT_NOALLOC_MAX_REQUESTS = 256 * 1024, 1024
 
 _lib = None

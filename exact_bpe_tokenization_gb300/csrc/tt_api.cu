@@ -120,6 +120,11 @@ static tt_status build_class_tables(tt_tokenizer *h) {
   std::vector<uint8_t> kind(0x110000, K_OTHER);
   for (int i = 0; i < TT_CLASS_RANGE_COUNT; ++i)
     for (uint32_t c = TT_CLASS_RANGES[i][0]; c <= TT_CLASS_RANGES[i][1]; ++c) kind[c] = kind_from_mask(TT_CLASS_RANGES[i][2]);
+  if (h->T.family == FAM_DEEPSEEK) {
+    // the second splitter's set: Hiragana, Katakana, CJK Unified Ideographs
+    for (uint32_t c = 0x3040; c <= 0x30FF; ++c) kind[c] |= K_HAN_FLAG;
+    for (uint32_t c = 0x4E00; c <= 0x9FFF; ++c) kind[c] |= K_HAN_FLAG;
+  }
   std::vector<uint16_t> stage1(0x110000 / 256);
   std::vector<uint8_t> stage2;
   std::map<std::string, int> seen;
@@ -198,7 +203,9 @@ extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, con
                                tt_tokenizer **out) {
   if (!out) return TT_ERR_INVALID_ARG;
   *out = nullptr;
-  if (pattern_family != TT_FAMILY_CL100K_STYLE && pattern_family != TT_FAMILY_O200K_STYLE) return TT_ERR_BAD_FAMILY;
+  if (pattern_family != TT_FAMILY_CL100K_STYLE && pattern_family != TT_FAMILY_O200K_STYLE &&
+      pattern_family != TT_FAMILY_DEEPSEEK_STYLE)
+    return TT_ERR_BAD_FAMILY;
   if (!vocab_offsets || n_vocab < 256 || n_vocab > (1 << MAX_VOCAB_BITS) || n_merges < 0 ||
       n_merges > (1 << MAX_RANK_BITS) - 1 || (n_merges > 0 && !merge_pairs))
     return n_vocab > (1 << MAX_VOCAB_BITS) || n_merges > (1 << MAX_RANK_BITS) - 1 ? TT_ERR_BAD_VOCAB : TT_ERR_INVALID_ARG;

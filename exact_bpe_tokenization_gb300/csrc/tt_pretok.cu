@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
         if (x < te && ((S.bytes[i] & 0xC0) != 0x80 || S.rsb[i])) {
           const uint32_t cp = decode_at(S, ws, total, i);
           const uint8_t mark = T.n_lit ? W.lit_flag[x] : 0;
-          e = rq_ws_event(S.rsb[i] != 0 || mark == LIT_SEG, mark == LIT_INNER ? (uint8_t)K_LIT : kind_of(T, S, cp),
+          e = rq_ws_event(T.family, S.rsb[i] != 0 || mark == LIT_SEG, mark == LIT_INNER ? (uint8_t)K_LIT : kind_of(T, S, cp),
                           cp < 128 ? cp : 0x80u);
         }
         const unsigned m = __ballot_sync(0xffffffffu, e != 0xFF);
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
     for (int j = c0; j < c1; ++j) {
       const int64_t pos = ws + S.lead[j];
       if (pos < ts || pos >= te) continue;
-      const uint8_t ew = rq_ws_event(S.rs[j], S.raw[j], S.cp8[j]);
+      const uint8_t ew = rq_ws_event(T.family, S.rs[j], S.raw[j], S.cp8[j]);
       const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
       if ((v & 0xFF) == 0xFF && ew != 0xFF) v = (v & 0xFF00) | ew;
       if ((v >> 8) == 0xFF && eu != 0xFF) v = (v & 0x00FF) | (eu << 8);
@@ -486,7 +486,13 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
       S.eff[j] = effective(fam, S.raw[j], mark_other);
     }
   } else {
-    for (int j = c0; j < c1; ++j) S.eff[j] = effective(fam, S.raw[j], false);
+    for (int j = c0; j < c1; ++j) {
+      S.eff[j] = effective(fam, S.raw[j], false);
+      // deepseek-style: segment starts of the first two splitters act as
+      // request starts (j = 0 has no predecessor in the window; it lies in
+      // the left halo, further back than any rule or scan looks)
+      if (fam == FAM_DEEPSEEK && j > 0 && ds_segment_start(S.raw[j - 1], S.raw[j])) S.rs[j] = 1;
+    }
   }
   __syncthreads();
 
@@ -501,7 +507,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
     for (int j = c0; j < c1; ++j) {
       const int64_t pos = ws + S.lead[j];
       if (pos < ts || pos >= te) continue;
-      const uint8_t ew = rq_ws_event(S.rs[j], S.raw[j], S.cp8[j]);
+      const uint8_t ew = rq_ws_event(fam, S.rs[j], S.raw[j], S.cp8[j]);
       const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
       if ((rq_first & 0xFF) == 0xFF && ew != 0xFF) rq_first = (rq_first & 0xFF00) | ew;
       if ((rq_first >> 8) == 0xFF && eu != 0xFF) rq_first = (rq_first & 0x00FF) | (eu << 8);
@@ -512,7 +518,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
       const int64_t pos = ws + S.lead[j];
       if (pos < ts || pos >= te) continue;
       P.rq8[j] = (uint8_t)((after & 0x3) | (((after >> 8) & 0x3) << 2));
-      const uint8_t ew = rq_ws_event(S.rs[j], S.raw[j], S.cp8[j]);
+      const uint8_t ew = rq_ws_event(fam, S.rs[j], S.raw[j], S.cp8[j]);
       const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
       if (ew != 0xFF) after = (after & 0xFF00) | ew;
       if (eu != 0xFF) after = (after & 0x00FF) | (eu << 8);
@@ -673,7 +679,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
     const int32_t pos = (int32_t)(ws + S.lead[j]);
     const bool ph = (placeholder >> b) & 1;
     W.piece_start[k] = ph ? (int32_t)(pos | 0x80000000u) : pos;
-    if (S.rs[j]) {                            // first piece of the requests starting here
+    if (S.rsb[S.lead[j]]) {                   // first piece of the requests starting here
       int r = S.r0 + (int)lower_bound64(A.offs + S.r0, S.r1 - S.r0, base + pos);
       for (; r < S.r1 && __ldg(&A.offs[r]) == base + pos; ++r) W.req_piece[r] = k;
     }
@@ -707,6 +713,7 @@ void launch_tilescan(const Tables &T, const Work &W, cudaStream_t s) { k_tilesca
 template <int NT>
 static void launch_pretok_nt(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   if (T.family == FAM_O200K) k_pretok<FAM_O200K, NT><<<grid, NT, sizeof(PretokSmem<NT>), s>>>(T, W);
+  else if (T.family == FAM_DEEPSEEK) k_pretok<FAM_DEEPSEEK, NT><<<grid, NT, sizeof(PretokSmem<NT>), s>>>(T, W);
   else k_pretok<FAM_CL100K, NT><<<grid, NT, sizeof(PretokSmem<NT>), s>>>(T, W);
 }
 void launch_pretok(const Tables &T, const Work &W, int grid, cudaStream_t s) {
@@ -722,7 +729,9 @@ cudaError_t pretok_configure() {
   cudaError_t e;
   if ((e = configure_one<FAM_CL100K, WIN / 8>()) != cudaSuccess) return e;
   if ((e = configure_one<FAM_O200K, WIN / 8>()) != cudaSuccess) return e;
+  if ((e = configure_one<FAM_DEEPSEEK, WIN / 8>()) != cudaSuccess) return e;
   if ((e = configure_one<FAM_CL100K, WIN / 16>()) != cudaSuccess) return e;
+  if ((e = configure_one<FAM_DEEPSEEK, WIN / 16>()) != cudaSuccess) return e;
   return configure_one<FAM_O200K, WIN / 16>();
 }
 

@@ -1,4 +1,4 @@
-// tt_rules.cuh - run-local piece-start rules of the two pattern families.
+// tt_rules.cuh - run-local piece-start rules of the pattern families.
 //
 // TokTier: Exact Stateful CPU+GPU Tokenization for Agentic LLM Serving, §4.1
 // ("run decomposition"): each character gets one of four classes (letter,
@@ -20,6 +20,11 @@
 //                   ?[^\s L N]+[\r\n]* | \s*[\r\n]+ | \s+(?!\S) | \s+
 //   o200k-style:   [^\r\n L N]?U*W+K? | [^\r\n L N]?U+W*K? | (the rest as above)
 //                  U = Lu Lt Lm Lo M,  W = Ll Lm Lo M,  K = optional contraction
+//   deepseek-style: three splitters in sequence, each re-splitting every
+//                   piece of the one before, the stretches between matches
+//                   kept as pieces: N{1,3}, then runs of kana / CJK
+//                   ideographs (U+3040-30FF, U+4E00-9FFF), then the
+//                   cl100k-style alternatives without N{1,3}
 //
 // Derived rules (a "run" is a maximal stretch of one effective class inside
 // one request; s = run start, e = run end):
@@ -54,6 +59,17 @@
 //                 alternate between swallowed and piece-starting.  The state
 //                 "the last letter run ended with its letter part" is carried
 //                 by a scan over the functions {identity, not, true, false}.
+//   deepseek-style: the first two splitters cut a request into segments at
+//                 every change between digits, kana/CJK chars and the rest,
+//                 and into digit groups of three (the number-run rule).  A
+//                 segment is the third splitter's whole subject, so its start
+//                 acts exactly like a request start: the cl100k-style rules
+//                 apply unchanged once segment starts are flagged like
+//                 request starts (lookback and lookahead stop there, a blank
+//                 run's lookahead sees the segment end as the text end).
+//                 The paper (§4.1) names this composition property; the
+//                 digit groups need no flag since digits only ever meet
+//                 digits inside a segment.
 #pragma once
 #include <stdint.h>
 
@@ -70,7 +86,9 @@ namespace tt {
 // raw / effective character kinds
 enum : uint8_t { K_OTHER = 0, K_LU = 1, K_LL = 2, K_LB = 3, K_MARK = 4, K_NUM = 5, K_WS = 6, K_NONE = 7,
                  K_LIT = 8 };   // K_LIT: a char of an added-token literal after its first (never starts a piece)
-enum : int { FAM_CL100K = 1, FAM_O200K = 2 };
+// deepseek-style tables flag kana / CJK ideograph chars in the raw kind
+enum : uint8_t { K_HAN_FLAG = 0x10, K_KIND_MASK = 0x0F };
+enum : int { FAM_CL100K = 1, FAM_O200K = 2, FAM_DEEPSEEK = 3 };
 // results of the "first char after i" queries
 enum : uint8_t { R_END = 0, R_CRLF = 1, R_OTHER = 2, R_LETTER = 3 };
 
@@ -121,7 +139,7 @@ struct Aggs {
 // was a lone "other" char at a piece start (cl100k) / followed letters (o200k)
 TT_HD bool contraction_end(int fam, const Nbr &n) {
   if (!is_letter(n.e1)) return false;
-  if (fam == FAM_CL100K) {
+  if (fam != FAM_O200K) {   // cl100k-style and deepseek-style
     if (n.c2 == '\'' && n.e2 == K_OTHER && contraction1(n.c1) && n.e3 != K_OTHER && n.c3 != ' ') return true;
     if (n.c3 == '\'' && n.e3 == K_OTHER && is_letter(n.e2) && contraction2(n.c2, n.c1) && n.e4 != K_OTHER &&
         n.c4 != ' ')
@@ -184,6 +202,7 @@ TT_HD bool trigger(uint8_t raw0, uint8_t raw_prev, uint32_t cp_prev, uint8_t raw
 }
 // effective kind of a char from its raw kind and (for marks) the resolution
 TT_HD uint8_t effective(int fam, uint8_t raw, bool mark_is_other) {
+  raw &= K_KIND_MASK;
   if (raw != K_MARK) return raw;
   return (fam == FAM_O200K && !mark_is_other) ? K_LB : K_OTHER;
 }
@@ -305,9 +324,23 @@ TT_HD void s2_values(const S2 &before, const S2 &after, int32_t pos, Aggs &a, bo
   chain_after = chain_apply(after.chain, true) != 0;
 }
 
-// reverse-query events: what a char at j means to queries from before j
-TT_HD uint8_t rq_ws_event(bool rs_j, uint8_t raw_j, uint32_t cp_j) {  // 0xFF = not an event
+// deepseek-style segments: 0 the rest, 1 digits, 2 kana / CJK ideographs
+// (raw kinds; an added-token literal's inner chars are never cut)
+TT_HD int ds_segment_class(uint8_t raw) {
+  return (raw & K_HAN_FLAG) ? 2 : (raw == K_NUM ? 1 : 0);
+}
+// char j (raw kind raw_j, not the first of its request) starts a segment
+TT_HD bool ds_segment_start(uint8_t raw_prev, uint8_t raw_j) {
+  return raw_j != K_LIT && ds_segment_class(raw_prev) != ds_segment_class(raw_j);
+}
+
+// reverse-query events: what a char at j means to queries from before j.
+// deepseek-style: a digit or kana/CJK char met by a blank run's lookahead
+// starts a segment (the blank run's piece ends with its segment), so it reads
+// as the end; elsewhere those chars are never the first event a blank sees.
+TT_HD uint8_t rq_ws_event(int fam, bool rs_j, uint8_t raw_j, uint32_t cp_j) {  // 0xFF = not an event
   if (rs_j) return R_END;
+  if (fam == FAM_DEEPSEEK && ds_segment_class(raw_j) != 0) return R_END;
   if (raw_j != K_WS) return R_OTHER;
   return is_crlf(cp_j) ? R_CRLF : 0xFF;
 }

@@ -76,7 +76,15 @@ typedef enum {
   TT_FAMILY_CL100K_STYLE = 1,
   /* letter pieces split on case (upper* lower+ | upper+ lower*), marks count
    * as letters, contractions attach to the preceding letters */
-  TT_FAMILY_O200K_STYLE = 2
+  TT_FAMILY_O200K_STYLE = 2,
+  /* three splitters in sequence, each re-splitting every piece of the one
+   * before and keeping the text between its matches as pieces (TokTier §4.1
+   * on DeepSeek-family tokenizers): digit groups of 1..3, then runs of
+   * Hiragana / Katakana / CJK Unified Ideographs (U+3040-U+30FF,
+   * U+4E00-U+9FFF), then the cl100k-style alternatives without the digit one,
+   * with each piece as the whole text (a blank run's lookahead ends at the
+   * piece end) */
+  TT_FAMILY_DEEPSEEK_STYLE = 3
 } tt_pattern_family;
 
 /*

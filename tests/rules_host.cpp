@@ -9,10 +9,17 @@
 
 using namespace tt;
 
-// cp/raw/rs: per char of the whole batch (rs = first char of a request).
-// Writes 1/0 into start[] per char.
-extern "C" void rules_host_starts(int fam, const uint32_t *cp, const uint8_t *raw, const uint8_t *rs, int64_t n,
+// cp/raw/rs: per char of the whole batch (rs = first char of a request;
+// deepseek-style raw kinds carry K_HAN_FLAG).  Writes 1/0 into start[] per
+// char.
+extern "C" void rules_host_starts(int fam, const uint32_t *cp, const uint8_t *raw, const uint8_t *rs_in, int64_t n,
                                   uint8_t *start) {
+  // deepseek-style: the first two splitters' segment starts act as request starts
+  std::vector<uint8_t> rsx(rs_in, rs_in + n);
+  if (fam == FAM_DEEPSEEK)
+    for (int64_t j = 1; j < n; ++j)
+      if (ds_segment_start(raw[j - 1], raw[j])) rsx[j] = 1;
+  const uint8_t *rs = rsx.data();
   std::vector<uint8_t> eff(n);
   // scan 1: mark resolution
   int64_t last_region = -1, last_trig = -1;
@@ -55,7 +62,7 @@ extern "C" void rules_host_starts(int fam, const uint32_t *cp, const uint8_t *ra
   for (int64_t j = n - 1; j >= 0; --j) {
     rq_ws[j] = cw;
     rq_up[j] = cu;
-    uint8_t ew = rq_ws_event(rs[j], raw[j], cp[j]);
+    uint8_t ew = rq_ws_event(fam, rs[j], raw[j], cp[j]);
     uint8_t eu = rq_up_event(rs[j], raw[j]);
     if (ew != 0xFF) cw = ew;
     if (eu != 0xFF) cu = eu;

@@ -30,7 +30,12 @@ def rules_lib(tmp_path_factory):
     return lib
 
 
-def raw_kinds(masks):
+K_HAN_FLAG = 0x10
+
+
+def raw_kinds(masks, family=1):
+    """Raw kinds per code point as the CUDA path's class table holds them
+    (deepseek-style: kana / CJK ideographs flagged)."""
     m = masks.astype(np.int64)
     k = np.full(len(m), K_OTHER, dtype=np.uint8)
     k[(m & 64) != 0] = K_MARK
@@ -39,6 +44,9 @@ def raw_kinds(masks):
     k[(m & (2 | 8)) != 0] = K_LU
     k[(m & 128) != 0] = K_NUM
     k[(m & 256) != 0] = K_WS
+    if family == 3:
+        k[0x3040:0x3100] |= K_HAN_FLAG
+        k[0x4E00:0xA000] |= K_HAN_FLAG
     return k
 
 
@@ -80,16 +88,21 @@ ALPHABETS = {
     2: ["a", "B", "1", " ", "\n", "'", ".", "か", "́", "\U0001F642"],
     # o200k contractions, case and marks together
     3: ["s", "T", "'", "a", "か", "́", " ", ".", "E", "r"],
+    # deepseek-style segments: digits, kana / ideographs (one of them "other")
+    4: ["a", "s", "1", " ", "\n", "'", ".", "日", "か", "・"],
+    5: ["B", "2", "\t", "\r", "ー", "゙", "'", "t", " ", "\U0001F642"],
 }
 EXTRA = {
     1: ["A", "t", "e", "r", "l", "m", "d", "v", "́", " ", "　", "٣"],
     2: ["s", "t", "r", "e", "l", "d", "\t", "\r", "ʰ", "ǅ", "é", "Ü"],
+    3: ["A", "t", "e", "r", "\t", "\r", "́", "　", "٣", "カ", "ー", "゛", "\U0001F642"],
 }
+FAMILY_ALPHABET = {1: 1, 2: 2, 3: 4}
 
 
-@pytest.mark.parametrize("family,alphabet", [(1, 1), (2, 2), (2, 3), (1, 3)])
+@pytest.mark.parametrize("family,alphabet", [(1, 1), (2, 2), (2, 3), (1, 3), (3, 4), (3, 5)])
 def test_rules_all_short_strings(rules_lib, masks, family, alphabet):
-    kinds = raw_kinds(masks)
+    kinds = raw_kinds(masks, family)
     strings = list(brute.all_strings(ALPHABETS[alphabet], 6))
     got = rule_starts(rules_lib, family, kinds, strings)
     exp = oracle_starts(family, strings)
@@ -97,10 +110,10 @@ def test_rules_all_short_strings(rules_lib, masks, family, alphabet):
     assert not bad, bad[:5]
 
 
-@pytest.mark.parametrize("family", [1, 2])
+@pytest.mark.parametrize("family", [1, 2, 3])
 def test_rules_mixed_alphabet_random(rules_lib, masks, family):
-    kinds = raw_kinds(masks)
-    alpha = ALPHABETS[family] + EXTRA[family]
+    kinds = raw_kinds(masks, family)
+    alpha = ALPHABETS[FAMILY_ALPHABET[family]] + EXTRA[family]
     rng = random.Random(17 + family)
     strings = ["".join(rng.choice(alpha) for _ in range(rng.randint(1, 14))) for _ in range(200000)]
     got = rule_starts(rules_lib, family, kinds, strings)
@@ -109,9 +122,9 @@ def test_rules_mixed_alphabet_random(rules_lib, masks, family):
     assert not bad, bad[:5]
 
 
-@pytest.mark.parametrize("family,profile", [(1, 0), (1, 1), (1, 2), (2, 1), (2, 2)])
+@pytest.mark.parametrize("family,profile", [(1, 0), (1, 1), (1, 2), (2, 1), (2, 2), (3, 3), (3, 1)])
 def test_rules_generated_text(rules_lib, masks, family, profile):
-    kinds = raw_kinds(masks)
+    kinds = raw_kinds(masks, family)
     strings = [synth.transcript(100 + i, 20000, profile).decode() for i in range(8)]
     strings.append(synth.adversarial(7, 300000).decode())
     assert rule_starts(rules_lib, family, kinds, strings) == oracle_starts(family, strings)
