@@ -47,7 +47,8 @@ struct Workspace {
   // device staging for tt_encode_host (bytes, offsets, ids, id offsets)
   void *stage = nullptr;
   size_t stage_bytes = 0;
-  std::vector<int64_t> h_offs;     // rebased host offsets
+  int64_t *h_offs = nullptr;       // rebased host offsets (pinned, so the copy is a plain DMA)
+  size_t h_offs_cap = 0;
 };
 
 struct Pending { int kernel; cudaEvent_t a, b; };
@@ -391,6 +392,7 @@ static void free_workspace(Workspace *w) {
   if (w->ev_join) cudaEventDestroy(w->ev_join);
   if (w->mem) cudaFree(w->mem);
   if (w->stage) cudaFree(w->stage);
+  if (w->h_offs) cudaFreeHost(w->h_offs);
   delete w;
 }
 
@@ -697,13 +699,23 @@ extern "C" tt_status tt_encode_host(tt_tokenizer *h, const uint8_t *utf8, const 
     d_offs = (int64_t *)(cur + in_b);
     d_out_offs = (int64_t *)(cur + in_b + off_b);
     d_out = (int32_t *)(cur + in_b + 2 * off_b);
-    w->h_offs.resize((size_t)n_requests + 1);
+    // (the previous call on this stream has waited for its copies, so the
+    // staging buffer is free to overwrite)
+    if (w->h_offs_cap < (size_t)n_requests + 1) {
+      if (w->h_offs) { cudaFreeHost(w->h_offs); w->h_offs = nullptr; w->h_offs_cap = 0; }
+      const size_t cap = next_pow2((uint64_t)n_requests + 1);
+      if (cudaMallocHost(&w->h_offs, cap * sizeof(int64_t)) != cudaSuccess) { w->h_offs = nullptr; return TT_ERR_OOM; }
+      w->h_offs_cap = cap;
+    }
     for (int64_t r = 0; r <= n_requests; ++r) w->h_offs[r] = byte_offsets[r] - b0;
     if (total) TT_CUDA(cudaMemcpyAsync(d_in, utf8 + b0, (size_t)total, cudaMemcpyHostToDevice, stream));
-    TT_CUDA(cudaMemcpyAsync(d_offs, w->h_offs.data(), (size_t)(n_requests + 1) * 8, cudaMemcpyHostToDevice, stream));
+    TT_CUDA(cudaMemcpyAsync(d_offs, w->h_offs, (size_t)(n_requests + 1) * 8, cudaMemcpyHostToDevice, stream));
   }
   tt_status s = tt_encode_batch_bounded(h, d_in, d_offs, n_requests, total, d_out, d_out_offs, stream_);
-  if (s != TT_OK) return s;
+  if (s != TT_OK) {
+    cudaStreamSynchronize(stream);   // the staged copies are done before the buffers are reused
+    return s;
+  }
   TT_CUDA(cudaMemcpyAsync(out_id_offsets, d_out_offs, (size_t)(n_requests + 1) * 8, cudaMemcpyDeviceToHost, stream));
   TT_CUDA(cudaStreamSynchronize(stream));
   const int64_t ntok = out_id_offsets[n_requests];

@@ -253,7 +253,9 @@ tt_status tt_encode_batch_noalloc(tt_tokenizer *h,
  * Copies the batch to device buffers owned by the handle, encodes it on
  * `stream`, copies the IDs back and waits.  Returns the device status of the
  * batch (TT_OK, TT_ERR_INVALID_UTF8, ...), or TT_ERR_CAPACITY if the IDs do
- * not fit in out_capacity (out_id_offsets is then still filled).
+ * not fit in out_capacity (out_id_offsets is then still filled).  Any host
+ * memory works; page-locked (pinned) buffers make both copies direct DMA.
+ * Two host waits per call: one for the ID count, one for the IDs and status.
  */
 tt_status tt_encode_host(tt_tokenizer *h,
                          const uint8_t *utf8, const int64_t *byte_offsets, int64_t n_requests,
