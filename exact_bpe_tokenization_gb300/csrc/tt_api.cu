@@ -49,6 +49,7 @@ struct Workspace {
   size_t stage_bytes = 0;
   int64_t *h_offs = nullptr;       // rebased host offsets (pinned, so the copy is a plain DMA)
   size_t h_offs_cap = 0;
+  DevStatus *h_status = nullptr;   // pinned: [0] the status read back, [1] the value that resets it
 };
 
 struct Pending { int kernel; cudaEvent_t a, b; };
@@ -393,6 +394,7 @@ static void free_workspace(Workspace *w) {
   if (w->mem) cudaFree(w->mem);
   if (w->stage) cudaFree(w->stage);
   if (w->h_offs) cudaFreeHost(w->h_offs);
+  if (w->h_status) cudaFreeHost(w->h_status);
   delete w;
 }
 
@@ -664,6 +666,32 @@ extern "C" tt_status tt_get_status(tt_tokenizer *h, tt_stream_t stream, int64_t 
   return (tt_status)st.code;
 }
 
+// Device address of a page-locked or managed host buffer, or null for
+// ordinary pageable memory.
+static void *device_view(const void *p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if ((a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeManaged) && a.devicePointer) return a.devicePointer;
+  return nullptr;
+}
+
+// Enqueue the read-back and reset of the handle's status word into the
+// workspace's pinned pair (the caller waits for the stream, then calls
+// status_result).
+static tt_status enqueue_status_read(tt_tokenizer *h, Workspace *w, cudaStream_t stream) {
+  if (!w->h_status) {
+    if (cudaMallocHost(&w->h_status, 2 * sizeof(DevStatus)) != cudaSuccess) { w->h_status = nullptr; return TT_ERR_OOM; }
+    w->h_status[1] = DevStatus{0, 0, ~0ull};
+  }
+  TT_CUDA(cudaMemcpyAsync(&w->h_status[0], h->d_status, sizeof(DevStatus), cudaMemcpyDeviceToHost, stream));
+  TT_CUDA(cudaMemcpyAsync(h->d_status, &w->h_status[1], sizeof(DevStatus), cudaMemcpyHostToDevice, stream));
+  return TT_OK;
+}
+static tt_status status_result(const Workspace *w) { return (tt_status)w->h_status[0].code; }
+
 extern "C" tt_status tt_encode_host(tt_tokenizer *h, const uint8_t *utf8, const int64_t *byte_offsets,
                                     int64_t n_requests, int32_t *out_ids, int64_t out_capacity,
                                     int64_t *out_id_offsets, tt_stream_t stream_) {
@@ -676,15 +704,24 @@ extern "C" tt_status tt_encode_host(tt_tokenizer *h, const uint8_t *utf8, const 
   const int64_t total = b1 - b0;
   if (total >= S2_MAX_POS - 64) return TT_ERR_CAPACITY;
   cudaStream_t stream = (cudaStream_t)stream_;
+  // Page-locked output buffers with room for the worst case are written by
+  // the kernels directly (no copy back, one wait); anything else is staged.
+  int32_t *dv_ids = nullptr;
+  int64_t *dv_offs = nullptr;
+  if (total > 0 && out_capacity >= total) {
+    dv_ids = (int32_t *)device_view(out_ids);
+    dv_offs = dv_ids ? (int64_t *)device_view(out_id_offsets) : nullptr;
+  }
+  const bool direct = dv_ids && dv_offs;
   const size_t in_b = ((size_t)total + 16 + 255) & ~(size_t)255;
   const size_t off_b = ((size_t)(n_requests + 1) * 8 + 255) & ~(size_t)255;
-  const size_t out_b = ((size_t)total + 1) * 4;
+  const size_t out_b = direct ? 0 : ((size_t)total + 1) * 4;
   uint8_t *d_in;
   int64_t *d_offs, *d_out_offs;
   int32_t *d_out;
+  Workspace *w;
   {
     std::lock_guard<std::mutex> lock(h->mu);
-    Workspace *w;
     tt_status s = get_workspace(h, stream, total, n_requests, &w);
     if (s != TT_OK) return s;
     const size_t need = in_b + 2 * off_b + out_b;
@@ -697,8 +734,8 @@ extern "C" tt_status tt_encode_host(tt_tokenizer *h, const uint8_t *utf8, const 
     char *cur = (char *)w->stage;
     d_in = (uint8_t *)cur;
     d_offs = (int64_t *)(cur + in_b);
-    d_out_offs = (int64_t *)(cur + in_b + off_b);
-    d_out = (int32_t *)(cur + in_b + 2 * off_b);
+    d_out_offs = direct ? dv_offs : (int64_t *)(cur + in_b + off_b);
+    d_out = direct ? dv_ids : (int32_t *)(cur + in_b + 2 * off_b);
     // (the previous call on this stream has waited for its copies, so the
     // staging buffer is free to overwrite)
     if (w->h_offs_cap < (size_t)n_requests + 1) {
@@ -712,16 +749,22 @@ extern "C" tt_status tt_encode_host(tt_tokenizer *h, const uint8_t *utf8, const 
     TT_CUDA(cudaMemcpyAsync(d_offs, w->h_offs, (size_t)(n_requests + 1) * 8, cudaMemcpyHostToDevice, stream));
   }
   tt_status s = tt_encode_batch_bounded(h, d_in, d_offs, n_requests, total, d_out, d_out_offs, stream_);
+  if (s == TT_OK) s = enqueue_status_read(h, w, stream);
   if (s != TT_OK) {
     cudaStreamSynchronize(stream);   // the staged copies are done before the buffers are reused
     return s;
   }
-  TT_CUDA(cudaMemcpyAsync(out_id_offsets, d_out_offs, (size_t)(n_requests + 1) * 8, cudaMemcpyDeviceToHost, stream));
+  if (!direct) TT_CUDA(cudaMemcpyAsync(out_id_offsets, d_out_offs, (size_t)(n_requests + 1) * 8, cudaMemcpyDeviceToHost,
+                                       stream));
   TT_CUDA(cudaStreamSynchronize(stream));
+  if (direct) return status_result(w);
   const int64_t ntok = out_id_offsets[n_requests];
   if (ntok > out_capacity) return TT_ERR_CAPACITY;
-  if (ntok) TT_CUDA(cudaMemcpyAsync(out_ids, d_out, (size_t)ntok * 4, cudaMemcpyDeviceToHost, stream));
-  return tt_get_status(h, stream_, nullptr);
+  if (ntok) {
+    TT_CUDA(cudaMemcpyAsync(out_ids, d_out, (size_t)ntok * 4, cudaMemcpyDeviceToHost, stream));
+    TT_CUDA(cudaStreamSynchronize(stream));
+  }
+  return status_result(w);
 }
 
 extern "C" tt_status tt_pretokenize_batch(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,

@@ -254,8 +254,12 @@ tt_status tt_encode_batch_noalloc(tt_tokenizer *h,
  * `stream`, copies the IDs back and waits.  Returns the device status of the
  * batch (TT_OK, TT_ERR_INVALID_UTF8, ...), or TT_ERR_CAPACITY if the IDs do
  * not fit in out_capacity (out_id_offsets is then still filled).  Any host
- * memory works; page-locked (pinned) buffers make both copies direct DMA.
- * Two host waits per call: one for the ID count, one for the IDs and status.
+ * memory works.  When out_ids and out_id_offsets are both page-locked (or
+ * managed) memory and out_capacity >= the batch bytes, the kernels write the
+ * IDs and offsets into them directly and the call waits once; otherwise the
+ * IDs are staged on the device and copied back after the count is read (two
+ * waits).  The input is always copied to the device first (page-locked input
+ * makes that a plain DMA).
  */
 tt_status tt_encode_host(tt_tokenizer *h,
                          const uint8_t *utf8, const int64_t *byte_offsets, int64_t n_requests,

@@ -234,6 +234,34 @@ def test_graph_replay_eager_and_host_paths_agree(cuda, vocabs):
     tok.close()
 
 
+def test_host_entry_point_pinned_direct_and_staged(cuda, vocabs):
+    """tt_encode_host with page-locked output buffers (written by the kernels
+    directly) and with pageable, mixed or too-small ones (staged and copied
+    back): the same IDs and offsets, the same status for a rejected request,
+    and repeated calls reusing the buffers."""
+    merges, vb, vo = vocabs["c1"]
+    reqs = synth.workload("burst_64_loguniform", scale=0.02) + [b"\xc3(", b"", "第3章 ok".encode()]
+    data, offs = synth.batch(reqs)
+    ref = oracle.Oracle(merges, vb, vo, 1).run(data, offs, threads=NCPU)
+    ntok = int(ref["id_offsets"][-1])
+    tok = cuda.Tokenizer(merges, vb, vo, 1)
+    pin_in = torch.from_numpy(data).pin_memory()
+    pin_ids = torch.full((len(data) + 5,), -7, dtype=torch.int32).pin_memory()
+    pin_io = torch.zeros(len(offs), dtype=torch.int64).pin_memory()
+    cases = [("pinned", pin_ids.numpy(), pin_io.numpy()),
+             ("pageable", np.full(len(data), -7, dtype=np.int32), np.zeros(len(offs), dtype=np.int64)),
+             ("mixed", pin_ids.numpy(), np.zeros(len(offs), dtype=np.int64)),
+             ("pinned, capacity below the bytes", pin_ids.numpy()[:ntok], pin_io.numpy())]
+    for rep in range(2):
+        for name, ids, io in cases:
+            ids[:] = -7
+            st = cuda.tt_encode_host(tok.h, pin_in.numpy(), offs, ids, io)
+            assert st == cuda.TT_ERR_INVALID_UTF8, (name, st)
+            assert np.array_equal(io, ref["id_offsets"]), name
+            assert np.array_equal(ids[:ntok], ref["ids"]), name
+    tok.close()
+
+
 def test_two_streams_and_growing_batches(cuda, vocabs):
     merges, vb, vo = vocabs["c1"]
     tok = cuda.Tokenizer(merges, vb, vo, 1)
