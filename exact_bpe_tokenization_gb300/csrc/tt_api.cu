@@ -31,9 +31,9 @@ using namespace tt;
 
 namespace {
 
-constexpr int N_KERNELS = 9;
+constexpr int N_KERNELS = 8;
 const char *KERNEL_NAMES[N_KERNELS] = {"k_lit_find", "k_lit_pick", "k_prepass", "k_tilescan", "k_pretok",
-                                       "k_bpe_warp", "k_bpe_long", "k_ids",      "k_req"};
+                                       "k_bpe_warp", "k_bpe_long", "k_ids"};
 
 struct Workspace {
   Work W{};
@@ -84,9 +84,9 @@ struct tt_tokenizer {
   int vocab_max_len = 0;
 };
 
-// kernels of one encode: seven, and the two literal kernels when the handle
+// kernels of one encode: six, and the two literal kernels when the handle
 // has added-token literals
-static int launches_per_encode(const tt_tokenizer *h) { return 7 + (h->T.n_lit ? 2 : 0); }
+static int launches_per_encode(const tt_tokenizer *h) { return 6 + (h->T.n_lit ? 2 : 0); }
 
 #define TT_CUDA(call)                                                   \
   do {                                                                  \
@@ -426,7 +426,7 @@ static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_
       {(void **)&W.ids_agg, 4 * (size_t)chunks},        {(void **)&W.ids_inc, 4 * (size_t)chunks},
       {(void **)&W.ids_flag, 4 * (size_t)chunks},       {(void **)&W.counters, 4 * 16},
       {(void **)&W.piece_start, 4 * (size_t)(cap_bytes + 2)}, {(void **)&W.n_ids, 4 * (size_t)(cap_bytes + 1)},
-      {(void **)&W.id_off, 4 * (size_t)(cap_bytes + 2)},      {(void **)&W.scratch, 4 * (size_t)(cap_bytes + 1)},
+      {(void **)&W.scratch, 4 * (size_t)(cap_bytes + 1)},
       {(void **)&W.tmp_a, 4 * (size_t)(cap_bytes + 1)},       {(void **)&W.tmp_b, 4 * (size_t)(cap_bytes + 1)},
       {(void **)&W.tmp_c, 4 * (size_t)(cap_bytes + 1)},
       {(void **)&W.long_list, 4 * 3 * (size_t)list_cap(cap_bytes)},
@@ -496,11 +496,11 @@ static cudaEvent_t pool_event(tt_tokenizer *h) {
 
 // grid sizes, all from capacity
 static int grid_tiles(const Workspace *w) { return (int)((w->cap_bytes + TILE - 1) / TILE); }
+static int grid_reqs(const Workspace *w) { return (int)((w->cap_reqs + 1 + 255) / 256); }
 static int grid_chunks(const Workspace *w) {   // persistent CTAs taking chunk tickets
   const int64_t g = (w->cap_bytes + 1 + IDS_CHUNK - 1) / IDS_CHUNK;
   return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 4);
 }
-static int grid_reqs(const Workspace *w) { return (int)((w->cap_reqs + 1 + 255) / 256); }
 static int grid_pieces(const Workspace *w) {   // a thread per piece (test hook)
   const int64_t g = (w->cap_bytes / 4 + 255) / 256;
   return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 8);
@@ -549,7 +549,6 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
     launch_bpe_warp(T, W, grid_warp(w), stream);
     TT_CUDA(cudaStreamWaitEvent(stream, w->ev_join, 0));
     launch_ids(T, W, grid_chunks(w), stream);
-    launch_req(T, W, grid_reqs(w), stream);
     TT_CUDA(cudaGetLastError());
     h->launches += launches_per_encode(h);
     return TT_OK;
@@ -566,7 +565,6 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
       case 5: launch_bpe_warp(T, W, grid_warp(w), stream); break;
       case 6: launch_bpe_long(T, W, grid_long(w), stream); break;
       case 7: launch_ids(T, W, grid_chunks(w), stream); break;
-      case 8: launch_req(T, W, grid_reqs(w), stream); break;
     }
     cudaEventRecord(b, stream);
     h->pending.push_back({kidx, a, b});
@@ -882,7 +880,7 @@ constexpr size_t NA_SIZES[] = {
     4 * (size_t)NA_CHUNKS, 4 * (size_t)NA_CHUNKS, 4 * (size_t)NA_CHUNKS, // ids_agg, ids_inc, ids_flag
     4 * 16,                                                            // counters
     4 * (size_t)(NA_BYTES + 2), 4 * (size_t)(NA_BYTES + 1),            // piece_start, n_ids
-    4 * (size_t)(NA_BYTES + 2), 4 * (size_t)(NA_BYTES + 1),            // id_off, scratch
+    4 * (size_t)(NA_BYTES + 1),                                        // scratch
     4 * (size_t)(NA_BYTES + 1), 4 * (size_t)(NA_BYTES + 1), 4 * (size_t)(NA_BYTES + 1),  // tmp_a, tmp_b, tmp_c
     4 * 3 * (size_t)list_cap(NA_BYTES), 4 * (size_t)(NA_BYTES / (MID_MAX + 1) + 2),  // lists
     (size_t)NA_REQS + 1, 4 * (size_t)(NA_REQS + 2),                    // bad, bad_pre
@@ -953,7 +951,7 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
                   (void **)&W.s2_agg,  (void **)&W.s2_inc,   (void **)&W.s2_flag,  (void **)&W.cnt_agg,
                   (void **)&W.cnt_inc, (void **)&W.cnt_flag, (void **)&W.ids_agg,  (void **)&W.ids_inc,
                   (void **)&W.ids_flag, (void **)&W.counters, (void **)&W.piece_start, (void **)&W.n_ids,
-                  (void **)&W.id_off,  (void **)&W.scratch,  (void **)&W.tmp_a,    (void **)&W.tmp_b,
+                  (void **)&W.scratch,  (void **)&W.tmp_a,    (void **)&W.tmp_b,
                   (void **)&W.tmp_c,   (void **)&W.long_list, (void **)&W.huge_list, (void **)&W.bad,
                   (void **)&W.bad_pre, (void **)&W.req_piece, (void **)&W.lit_cand, (void **)&W.lit_cnt,
                   (void **)&W.lit_flag, (void **)&W.lit_len, (void **)&W.args};
@@ -979,7 +977,6 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   const int g_warp = (int)warp_grid(NA_BYTES);
   const int g_long = (int)std::min<int64_t>(std::max<int64_t>(NA_BYTES / (MID_MAX + 1), 1), 152 * 2);
   const int g_chunks = (int)((NA_BYTES + 1 + IDS_CHUNK - 1) / IDS_CHUNK);
-  const int g_reqs = (int)((NA_REQS + 1 + 255) / 256);
   if (T.n_lit) {
     TT_CUDA(cudaMemsetAsync(W.lit_flag, 0, (size_t)NA_BYTES + 8, stream));
     launch_lit_find(T, W, g_tiles, stream);
@@ -991,7 +988,6 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   launch_bpe_warp(T, W, g_warp, stream);
   launch_bpe_long(T, W, g_long, stream);
   launch_ids(T, W, g_chunks, stream);
-  launch_req(T, W, g_reqs, stream);
   TT_CUDA(cudaGetLastError());
   h->launches += launches_per_encode(h);
   return TT_OK;

@@ -641,6 +641,38 @@ __global__ void __launch_bounds__(BPE_LONG_THREADS, 1) k_bpe_long(Tables T, Work
 }
 
 // ---------------------------------------------------------------- ids
+// The first piece of request r (recorded by the pre-tokenizer), or np for a
+// request with no piece (empty at the batch end) and for r = n.  It never
+// decreases with r; `bad` reports an entry outside the piece table.
+__device__ __forceinline__ int request_piece(const CallArgs &A, const Work &W, int64_t base, int64_t total, int np,
+                                             int64_t r, bool *bad) {
+  if (r >= A.n || __ldg(&A.offs[r]) - base >= total) return np;
+  const int k = __ldcg(&W.req_piece[r]);
+  if (k < 0 || k >= np) { *bad = true; return np; }
+  return k;
+}
+// The first request r in [0, n] whose first piece is >= p (p <= np), by one
+// warp: 32 probes per step, so a handful of steps for any batch.
+__device__ int64_t first_request_from(const CallArgs &A, const Work &W, int64_t base, int64_t total, int np, int p) {
+  const int lane = threadIdx.x & 31;
+  int64_t lo = 0, hi = A.n;   // the answer lies in [lo, hi]; request_piece(n) = np >= p
+  bool bad = false;
+  while (lo < hi) {
+    const int64_t step = (hi - lo + 31) / 32;
+    const int64_t r = lo + (int64_t)lane * step;
+    const bool ge = r < hi && request_piece(A, W, base, total, np, r, &bad) >= p;
+    const unsigned m = __ballot_sync(0xffffffffu, ge);
+    if (m) {
+      const int f = __ffs(m) - 1;
+      hi = lo + (int64_t)f * step;
+      if (f) lo += (int64_t)(f - 1) * step + 1;
+    } else {
+      lo += ((hi - 1 - lo) / step) * step + 1;   // past the last probe below hi
+    }
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
   constexpr int PER = IDS_CHUNK / IDS_THREADS;
   __shared__ int s_off[IDS_CHUNK + 1];   // chunk-local output offset of each piece
@@ -648,14 +680,20 @@ __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
   __shared__ int red[IDS_THREADS / 32];
   __shared__ int2 s_red2[IDS_THREADS / 32];
   __shared__ int s_tile, s_base;
+  __shared__ int64_t s_rlo, s_rhi;       // requests whose first piece is in the chunk
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
   if (A.n <= 0) return;
   const int64_t base = __ldg(&A.offs[0]);
   const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) return;
-  const int np = __ldcg(&W.counters[3]);
+  const bool sound = !(total > W.cap_bytes || total < 0 || base < 0);
+  const int np = sound ? __ldcg(&W.counters[3]) : 0;
   const int nchunks = (np + IDS_CHUNK - 1) / IDS_CHUNK;
+  if (nchunks == 0) {   // no pieces (an empty or unsound batch): every request has no IDs
+    for (int64_t r = (int64_t)blockIdx.x * IDS_THREADS + tid; r <= A.n; r += (int64_t)gridDim.x * IDS_THREADS)
+      A.out_id_offsets[r] = 0;
+    return;
+  }
   for (;;) {
     if (tid == 0) s_tile = atomicAdd(&W.counters[1], 1);
     __syncthreads();
@@ -682,15 +720,20 @@ __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
     }
     int chunk_total;
     const int ex = block_exclusive_scan<IDS_THREADS>(sum, [](int a, int b) { return a + b; }, 0, red, &chunk_total);
+    // (warps 1 and 2 find the chunk's requests while warp 0 waits on its predecessors)
+    if (tid >= 32 && tid < 64) {
+      const int64_t r = first_request_from(A, W, base, total, np, k0);
+      if (tid == 32) s_rlo = r;
+    } else if (tid >= 64 && tid < 96) {
+      const int64_t r = t == nchunks - 1 ? A.n + 1 : first_request_from(A, W, base, total, np, k0 + nloc);
+      if (tid == 64) s_rhi = r;
+    }
     if (tid < 32) {
       const int b = warp_lookback(t, chunk_total, [](int a, int b) { return a + b; }, 0, W.ids_agg, W.ids_inc,
                                   W.ids_flag, W.status, W.spin_limit);
       if (tid == 0) {
         s_base = b;
-        if (t == nchunks - 1) {
-          W.id_off[np] = b + chunk_total;
-          W.counters[4] = b + chunk_total;
-        }
+        if (t == nchunks - 1) W.counters[4] = b + chunk_total;
       }
     }
     __syncthreads();
@@ -701,11 +744,19 @@ __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
       const int q = tid * PER + m;
       s_off[q] = off;
       s_st[q] = st[m];
-      if (q < nloc) W.id_off[k0 + q] = cb + off;
       off += cnt[m];
     }
     if (tid == 0) s_off[IDS_CHUNK] = chunk_total;
     __syncthreads();
+    // per-request ID offsets: a request starts at its first piece's offset
+    // (the last chunk also writes those past its last piece: the batch's token
+    // count for empty requests at the end and for the end offset n)
+    for (int64_t r = s_rlo + tid; r < s_rhi; r += IDS_THREADS) {
+      bool bad = false;
+      const int k = request_piece(A, W, base, total, np, r, &bad);
+      if (bad) set_status(W.status, ST_INVALID_ARG);
+      A.out_id_offsets[r] = cb + ((k >= k0 && k < k0 + nloc) ? s_off[k - k0] : chunk_total);
+    }
     // output-parallel copy: output o of the chunk belongs to the last piece
     // whose offset is <= o (pieces with no IDs share their successor's offset)
     auto piece_of = [&](int o) {
@@ -768,27 +819,6 @@ __device__ __forceinline__ int lower_bound_piece(const int32_t *ps, int np, int6
   return lo;
 }
 
-// out_id_offsets[r]: the ID offset of request r's first piece (recorded by
-// the pre-tokenizer); empty requests at the end of the batch get the token
-// count.
-__global__ void k_req(Tables T, Work W) {
-  const CallArgs A = *W.args;
-  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (A.n <= 0 || r > A.n) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) { A.out_id_offsets[r] = 0; return; }
-  const int np = __ldcg(&W.counters[3]);
-  const int tokens = __ldcg(&W.counters[4]);
-  const int64_t pos = __ldg(&A.offs[r]) - base;
-  int k = np;
-  if (r < A.n && pos < total) {
-    k = __ldcg(&W.req_piece[r]);
-    if (k < 0 || k >= np) { set_status(W.status, ST_INVALID_ARG); k = np; }
-  }
-  A.out_id_offsets[r] = k < np ? __ldcg(&W.id_off[k]) : tokens;
-}
-
 // ---------------------------------------------------------------- test hook
 __global__ void __launch_bounds__(1024) k_hook_pre(Work W) {
   __shared__ int red[32];
@@ -847,7 +877,6 @@ void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   k_bpe_long<<<grid, BPE_LONG_THREADS, LONG_SMEM_BYTES, s>>>(T, W);
 }
 void launch_ids(const Tables &T, const Work &W, int grid, cudaStream_t s) { k_ids<<<grid, IDS_THREADS, 0, s>>>(T, W); }
-void launch_req(const Tables &T, const Work &W, int grid, cudaStream_t s) { k_req<<<grid, 256, 0, s>>>(T, W); }
 void launch_hook_pre(const Work &W, cudaStream_t s) { k_hook_pre<<<1, 1024, 0, s>>>(W); }
 void launch_hook_pieces(const Work &W, int grid, cudaStream_t s) { k_hook_pieces<<<grid, 256, 0, s>>>(W); }
 void launch_hook_offsets(const Work &W, int grid, cudaStream_t s) { k_hook_offsets<<<grid, 256, 0, s>>>(W); }

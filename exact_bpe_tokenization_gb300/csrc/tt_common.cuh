@@ -406,7 +406,6 @@ struct Work {
   // pieces and tokens
   int32_t *piece_start;            // [cap_bytes + 2], bit 31 = rejected-request placeholder
   int32_t *n_ids;                  // [cap_bytes + 1]
-  int32_t *id_off;                 // [cap_bytes + 2]
   int32_t *scratch;                // [cap_bytes] ids by byte position
   int32_t *tmp_a, *tmp_b, *tmp_c;  // [cap_bytes] long-piece work arrays
   int32_t *long_list;              // 3 buckets of LIST_CAP(cap_bytes) entries: pieces of

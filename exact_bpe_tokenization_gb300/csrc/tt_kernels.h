@@ -17,7 +17,6 @@ void launch_lit_pick(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_bpe_warp(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_ids(const Tables &T, const Work &W, int grid, cudaStream_t s);
-void launch_req(const Tables &T, const Work &W, int grid, cudaStream_t s);
 
 void launch_hook_pre(const Work &W, cudaStream_t s);
 void launch_hook_pieces(const Work &W, int grid, cudaStream_t s);

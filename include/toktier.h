@@ -220,7 +220,7 @@ tt_status tt_encode_batch_spans(tt_tokenizer *h,
  * synchronise the device.  tt_encode_batch_bounded may allocate a
  * per-stream workspace on first use or when a batch outgrows it; this entry
  * point never does: its scratch is one fixed array compiled into the
- * library (about 7.4 MB, held on every device that loads the library until
+ * library (about 6.4 MB, held on every device that loads the library until
  * the process exits).
  *
  *   Arguments and outputs as tt_encode_batch_bounded; the limits are
