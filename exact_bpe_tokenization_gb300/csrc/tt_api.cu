@@ -499,7 +499,7 @@ static int grid_tiles(const Workspace *w) { return (int)((w->cap_bytes + TILE - 
 static int grid_reqs(const Workspace *w) { return (int)((w->cap_reqs + 1 + 255) / 256); }
 static int grid_chunks(const Workspace *w) {   // persistent CTAs taking chunk tickets
   const int64_t g = (w->cap_bytes + 1 + IDS_CHUNK - 1) / IDS_CHUNK;
-  return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 4);
+  return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 5);   // 5 resident per SM at 47 registers
 }
 static int grid_pieces(const Workspace *w) {   // a thread per piece (test hook)
   const int64_t g = (w->cap_bytes / 4 + 255) / 256;

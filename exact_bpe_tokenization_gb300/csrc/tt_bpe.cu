@@ -771,9 +771,25 @@ __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
     if ((int64_t)cb + chunk_total > total) {
       if (tid == 0) set_status(W.status, ST_INVALID_ARG);
     } else if (!A.out_spans) {
-      for (int o = tid; o < chunk_total; o += IDS_THREADS) {
-        const int q = piece_of(o);
-        A.out_ids[cb + o] = __ldcg(&W.scratch[s_st[q] + (o - s_off[q])]);
+      // four outputs a thread at a time: their searches and loads overlap
+      constexpr int U = 4;
+      for (int ob = 0; ob < chunk_total; ob += U * IDS_THREADS) {
+        int src[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int o = ob + u * IDS_THREADS + tid;
+          src[u] = -1;
+          if (o < chunk_total) {
+            const int q = piece_of(o);
+            src[u] = s_st[q] + (o - s_off[q]);
+          }
+        }
+        int id[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) id[u] = src[u] >= 0 ? __ldcg(&W.scratch[src[u]]) : 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (src[u] >= 0) A.out_ids[cb + ob + u * IDS_THREADS + tid] = id[u];
       }
     } else {
       // with byte spans: the IDs of a piece cover its bytes in order, so an

@@ -307,17 +307,34 @@ done:
   st_release(&flag[tile], 2);
   return excl;
 }
+// Make a tile's aggregate (tile 0: its inclusive prefix) visible to its
+// successors' look-back (one thread).
+template <typename T>
+__device__ __forceinline__ void lookback_publish(int tile, T local, T *agg, T *inc, int *flag) {
+  if (tile == 0) {
+    inc[0] = local;
+    __threadfence();
+    st_release(&flag[0], 2);
+  } else {
+    agg[tile] = local;
+    __threadfence();
+    st_release(&flag[tile], 1);
+  }
+}
 // Decoupled look-back by one full warp (the warp that calls it; all 32 lanes
 // must call).  Each step inspects the 32 nearest unread predecessors at once:
 // a ballot finds the nearest one with an inclusive prefix, and the aggregates
 // in between are combined by a warp reduction in tile order.  Returns the
 // exclusive prefix on every lane; lane 0 publishes.  Every wait is bounded.
+// With `published`, the tile's aggregate was already made visible by
+// lookback_publish (so that the successors' look-back can start while this
+// tile does other work).
 template <typename T, typename Op>
 __device__ T warp_lookback(int tile, T local, Op op, T identity, T *agg, T *inc, int *flag, DevStatus *st,
-                           int spin_limit) {
+                           int spin_limit, bool published = false) {
   const int lane = threadIdx.x & 31;
   if (tile == 0) {
-    if (lane == 0) {
+    if (lane == 0 && !published) {
       inc[0] = local;
       __threadfence();
       st_release(&flag[0], 2);
@@ -325,7 +342,7 @@ __device__ T warp_lookback(int tile, T local, Op op, T identity, T *agg, T *inc,
     __syncwarp();
     return identity;
   }
-  if (lane == 0) {
+  if (lane == 0 && !published) {
     agg[tile] = local;
     __threadfence();
     st_release(&flag[tile], 1);

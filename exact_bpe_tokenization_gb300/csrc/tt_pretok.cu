@@ -42,6 +42,14 @@ struct WinSmem {
   int nch;
 };
 
+// The prepass's view of a window: bytes, request starts and the ASCII classes.
+struct ByteWin {
+  uint8_t bytes[WIN + 8];
+  uint8_t rsb[WIN + 8];
+  uint8_t ascii[128];
+  int r0, r1;
+};
+
 __device__ __forceinline__ int64_t lower_bound64(const int64_t *a, int64_t n, int64_t v) {
   int64_t lo = 0, hi = n;
   while (lo < hi) {
@@ -79,9 +87,8 @@ __device__ __forceinline__ uint32_t decode_at(const WS &S, int64_t ws, int64_t t
 
 // Load the bytes of the window [ws, ws + WIN) and mark request starts.  All
 // threads participate.
-template <int NT>
-__device__ void load_bytes(const Tables &T, const CallArgs &A, int64_t base, int64_t total, int64_t ws,
-                           WinSmem<NT> &S) {
+template <int NT, class WS>
+__device__ void load_bytes(const Tables &T, const CallArgs &A, int64_t base, int64_t total, int64_t ws, WS &S) {
   constexpr int PT_BYTES = WIN / NT;
   const int tid = threadIdx.x;
   const uint8_t *g = A.utf8 + base;
@@ -159,10 +166,7 @@ __device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, in
 template <int NT>
 __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
   constexpr int PT_BYTES = WIN / NT;
-  __shared__ WinSmem<NT> S;
-  __shared__ int scan_tmp[NT / 32];
-  __shared__ int2 red2[NT / 32];
-  __shared__ int red_rq[NT / 32];
+  __shared__ ByteWin S;
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
   if (A.n <= 0) return;
@@ -180,12 +184,9 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
   if (t >= ntiles) return;
   const int64_t ts = (int64_t)t * TILE, te = ts + TILE < total ? ts + TILE : total;
   const int64_t ws = ts - HALO_L;
-  // cl100k needs no mark resolution and no upper-case queries: bytes and
-  // request starts suffice, and the few chars its summary looks at are
-  // decoded where they are met
-  const bool bytes_only = T.family != FAM_O200K;
-  if (bytes_only) load_bytes<NT>(T, A, base, total, ws, S);
-  else load_window(T, A, base, total, ws, S, scan_tmp, T.n_lit ? W.lit_flag : nullptr);
+  // bytes and request starts suffice: the few chars the summaries look at
+  // are decoded where they are met
+  load_bytes<NT>(T, A, base, total, ws, S);
 
   // --- UTF-8 validation of the tile's bytes (RFC 3629, per request)
   for (int k = 0; k < PT_BYTES; ++k) {
@@ -232,67 +233,87 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
     }
   }
 
-  if (bytes_only) {
-    // --- reverse-query summary: the first rq_ws event among the tile's chars,
-    // 32 bytes at a time by one warp (usually within the first step)
-    if (tid < 32) {
-      const int lane = tid;
-      int ev = 0xFF;
-      for (int64_t x0 = ts; x0 < te && ev == 0xFF; x0 += 32) {
-        const int64_t x = x0 + lane;
-        const int i = (int)(x - ws);
-        int e = 0xFF;
-        if (x < te && ((S.bytes[i] & 0xC0) != 0x80 || S.rsb[i])) {
-          const uint32_t cp = decode_at(S, ws, total, i);
-          const uint8_t mark = T.n_lit ? W.lit_flag[x] : 0;
-          e = rq_ws_event(T.family, S.rsb[i] != 0 || mark == LIT_SEG, mark == LIT_INNER ? (uint8_t)K_LIT : kind_of(T, S, cp),
-                          cp < 128 ? cp : 0x80u);
-        }
-        const unsigned m = __ballot_sync(0xffffffffu, e != 0xFF);
-        if (m) ev = __shfl_sync(0xffffffffu, e, __ffs(m) - 1);
+  const uint8_t *lit = T.n_lit ? W.lit_flag : nullptr;
+  // the char starting at window byte i: request-or-segment start, raw kind, code point
+  auto char_at = [&](int i, bool &rs, uint8_t &raw, uint32_t &cp) {
+    cp = decode_at(S, ws, total, i);
+    const uint8_t mark = lit ? __ldg(lit + ws + i) : 0;
+    rs = S.rsb[i] != 0 || mark == LIT_SEG;
+    raw = mark == LIT_INNER ? (uint8_t)K_LIT : kind_of(T, S, cp);
+  };
+  auto is_start = [&](int64_t x) { return x >= 0 && x < total && ((S.bytes[x - ws] & 0xC0) != 0x80 || S.rsb[x - ws]); };
+  const int lane = tid & 31;
+  if (tid < 32) {
+    // --- reverse-query summary: the first rq_ws (and, o200k, rq_up) event
+    // among the tile's chars, 32 bytes a step (usually one step)
+    const bool want_up = T.family == FAM_O200K;
+    int evw = 0xFF, evu = want_up ? 0xFF : 0x00;
+    for (int64_t x0 = ts; x0 < te && (evw == 0xFF || evu == 0xFF); x0 += 32) {
+      const int64_t x = x0 + lane;
+      int ew = 0xFF, eu = 0xFF;
+      if (x < te && is_start(x)) {
+        bool rs;
+        uint8_t raw;
+        uint32_t cp;
+        char_at((int)(x - ws), rs, raw, cp);
+        ew = rq_ws_event(T.family, rs, raw, cp < 128 ? cp : 0x80u);
+        eu = rq_up_event(rs, raw);
       }
-      if (lane == 0) { W.rq_sum[2 * t] = (uint8_t)ev; W.rq_sum[2 * t + 1] = 0xFF; }
+      const unsigned mw = __ballot_sync(0xffffffffu, ew != 0xFF);
+      const unsigned mu = __ballot_sync(0xffffffffu, eu != 0xFF);
+      if (evw == 0xFF && mw) evw = __shfl_sync(0xffffffffu, ew, __ffs(mw) - 1);
+      if (evu == 0xFF && mu) evu = __shfl_sync(0xffffffffu, eu, __ffs(mu) - 1);
     }
-    return;
-  }
-  const int c0 = S.cbase[tid], c1 = S.cbase[tid + 1];
-  // --- mark-resolution summary over chars with pos in [ts - 32, te - 32)
-  if (T.family == FAM_O200K) {
-    int2 v = make_int2(-1, -1);
-    for (int j = c0; j < c1; ++j) {
-      const int64_t pos = ws + S.lead[j];
-      if (pos < ts - S1_SHIFT || pos >= te - S1_SHIFT) continue;
-      const bool in_prev = !S.rs[j] && j > 0;
-      const uint8_t rp = in_prev ? S.raw[j - 1] : K_NONE;
-      const uint32_t cpp = in_prev ? S.cp8[j - 1] : 0;
-      const uint8_t rn = (j + 1 < S.nch && !S.rs[j + 1]) ? S.raw[j + 1] : K_NONE;
-      if (region_start(S.raw[j], rp)) v.x = (int)pos;
-      if (trigger(S.raw[j], rp, cpp, rn)) v.y = (int)pos;
+    if (lane == 0) { W.rq_sum[2 * t] = (uint8_t)evw; W.rq_sum[2 * t + 1] = want_up ? (uint8_t)evu : (uint8_t)0xFF; }
+  } else if (tid < 64 && T.family == FAM_O200K) {
+    // --- mark-resolution summary over the chars in [ts - 32, te - 32): the
+    // last stretch start x and the last trigger y, scanning back from the end
+    // 32 bytes a step until a stretch start is met.  A trigger before x is
+    // reported as none: every use compares the latest trigger with the latest
+    // stretch start, and x is at least as late as any earlier one.
+    const int64_t lo = ts - S1_SHIFT > 0 ? ts - S1_SHIFT : 0, hi = te - S1_SHIFT;
+    int xs = -1, ys = -1;
+    for (int64_t x1 = hi; x1 > lo && xs < 0; x1 -= 32) {
+      const int64_t x = x1 - 32 + lane;
+      bool rstart = false, trig = false;
+      if (x >= lo && x < hi && is_start(x)) {
+        bool rs0;
+        uint8_t raw0;
+        uint32_t cp0;
+        char_at((int)(x - ws), rs0, raw0, cp0);
+        uint8_t rp = K_NONE, rn = K_NONE;
+        uint32_t cpp = 0;
+        if (!rs0) {                               // the previous char: at most 3 bytes back
+          int64_t px = x - 1;
+          while (px > x - 4 && px > 0 && !is_start(px)) --px;
+          bool rsp;
+          uint32_t cpv;
+          char_at((int)(px - ws), rsp, rp, cpv);
+          cpp = cpv < 128 ? cpv : 0x80u;
+        }
+        int64_t nx = x + 1;                       // the next char: at most 4 bytes on
+        while (nx < x + 4 && nx < total && !is_start(nx)) ++nx;
+        if (nx < total && is_start(nx)) {
+          bool rsn;
+          uint32_t cpn;
+          uint8_t rawn;
+          char_at((int)(nx - ws), rsn, rawn, cpn);
+          if (!rsn) rn = rawn;
+        }
+        rstart = region_start(raw0, rp);
+        trig = trigger(raw0, rp, cpp, rn);
+      }
+      const unsigned mr = __ballot_sync(0xffffffffu, rstart), mt = __ballot_sync(0xffffffffu, trig);
+      if (mr) {
+        const int fl = 31 - __clz(mr);
+        xs = (int)(x1 - 32 + fl);
+        const unsigned at_or_after = mt & ~((1u << fl) - 1);
+        if (ys < 0 && at_or_after) ys = (int)(x1 - 32 + 31 - __clz(at_or_after));
+      } else if (ys < 0 && mt) {
+        ys = (int)(x1 - 32 + 31 - __clz(mt));
+      }
     }
-    int2 tot;
-    block_exclusive_scan<NT>(v, [](int2 a, int2 b) { return make_int2(max(a.x, b.x), max(a.y, b.y)); },
-                                     make_int2(-1, -1), red2, &tot);
-    if (tid == 0) W.s1_sum[t] = tot;
-  }
-  // --- reverse-query summary: first events among the tile's chars
-  {
-    int v = 0xFFFF;   // byte 0: rq_ws event, byte 1: rq_up event (0xFF = none)
-    for (int j = c0; j < c1; ++j) {
-      const int64_t pos = ws + S.lead[j];
-      if (pos < ts || pos >= te) continue;
-      const uint8_t ew = rq_ws_event(T.family, S.rs[j], S.raw[j], S.cp8[j]);
-      const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
-      if ((v & 0xFF) == 0xFF && ew != 0xFF) v = (v & 0xFF00) | ew;
-      if ((v >> 8) == 0xFF && eu != 0xFF) v = (v & 0x00FF) | (eu << 8);
-    }
-    auto first = [](int a, int b) {   // a before b: keep a's events where present
-      const int lo = (a & 0xFF) != 0xFF ? (a & 0xFF) : (b & 0xFF);
-      const int hi = (a >> 8) != 0xFF ? (a >> 8) : (b >> 8);
-      return lo | (hi << 8);
-    };
-    int tot;
-    block_exclusive_scan<NT>(v, first, 0xFFFF, red_rq, &tot);
-    if (tid == 0) { W.rq_sum[2 * t] = (uint8_t)(tot & 0xFF); W.rq_sum[2 * t + 1] = (uint8_t)(tot >> 8); }
+    if (lane == 0) W.s1_sum[t] = make_int2(xs, ys);
   }
 }
 
@@ -496,6 +517,33 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
   }
   __syncthreads();
 
+  // --- forward scan (scan 2) over chars with pos in [ts - 16, te); the
+  // published aggregate covers the shifted tile [ts - 16, te - 16)
+  const int64_t s2_lo = ts - S2_SHIFT, s2_pub_hi = t == ntiles - 1 ? INT64_MAX : te - S2_SHIFT;
+  int jlo = c0, jhi = c1;                       // my chars with pos in [s2_lo, te)
+  while (jlo < jhi && ws + S.lead[jlo] < s2_lo) ++jlo;
+  while (jhi > jlo && ws + S.lead[jhi - 1] >= te) --jhi;
+  S2 agg_all = s2_identity(), agg_pub = s2_identity();
+  bool pub_done = false;
+  if (jlo < jhi) {
+    Slider w;
+    w.start(S, ws, jlo);
+    for (int j = jlo;;) {
+      if (!pub_done && w.pos >= s2_pub_hi) { agg_pub = agg_all; pub_done = true; }
+      if (!s2_trivial(fam, w.b)) agg_all = s2_combine(agg_all, s2_element(fam, w.b, w.pos, w.p1, w.p2));
+      if (++j >= jhi) break;
+      w.step(S, ws, j);
+    }
+  }
+  if (!pub_done) agg_pub = agg_all;
+  auto comb = [](const S2 &a, const S2 &b) { return s2_combine(a, b); };
+  S2 tile_pub;
+  block_exclusive_scan<NT>(agg_pub, comb, s2_identity(), P.s2_tmp, &tile_pub);
+  // publish now: the successors' look-back runs while this tile answers its
+  // reverse queries
+  if (tid == 0) lookback_publish(t, tile_pub, W.s2_agg, W.s2_inc, W.s2_flag);
+  const S2 my_ex = block_exclusive_scan<NT>(agg_all, comb, s2_identity(), P.s2_tmp, (S2 *)nullptr);
+
   // --- reverse queries over the tile's chars: first event strictly after j
   auto first = [](int a, int b) {
     const int lo = (a & 0xFF) != 0xFF ? (a & 0xFF) : (b & 0xFF);
@@ -525,35 +573,13 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
     }
   }
 
-  // --- forward scan (scan 2) over chars with pos in [ts - 16, te); the
-  // published aggregate covers the shifted tile [ts - 16, te - 16)
-  const int64_t s2_lo = ts - S2_SHIFT, s2_pub_hi = t == ntiles - 1 ? INT64_MAX : te - S2_SHIFT;
-  int jlo = c0, jhi = c1;                       // my chars with pos in [s2_lo, te)
-  while (jlo < jhi && ws + S.lead[jlo] < s2_lo) ++jlo;
-  while (jhi > jlo && ws + S.lead[jhi - 1] >= te) --jhi;
-  S2 agg_all = s2_identity(), agg_pub = s2_identity();
-  bool pub_done = false;
-  if (jlo < jhi) {
-    Slider w;
-    w.start(S, ws, jlo);
-    for (int j = jlo;;) {
-      if (!pub_done && w.pos >= s2_pub_hi) { agg_pub = agg_all; pub_done = true; }
-      if (!s2_trivial(fam, w.b)) agg_all = s2_combine(agg_all, s2_element(fam, w.b, w.pos, w.p1, w.p2));
-      if (++j >= jhi) break;
-      w.step(S, ws, j);
-    }
-  }
-  if (!pub_done) agg_pub = agg_all;
-  auto comb = [](const S2 &a, const S2 &b) { return s2_combine(a, b); };
-  S2 tile_pub;
-  block_exclusive_scan<NT>(agg_pub, comb, s2_identity(), P.s2_tmp, &tile_pub);
   if (tid < 32) {
     const S2 pre = warp_lookback(t, tile_pub, comb, s2_identity(), W.s2_agg, W.s2_inc, W.s2_flag, W.status,
-                                 W.spin_limit);
+                                 W.spin_limit, true);
     if (tid == 0) P.s2_prefix = pre;
   }
-  const S2 my_ex = block_exclusive_scan<NT>(agg_all, comb, s2_identity(), P.s2_tmp, (S2 *)nullptr);
-  S2 before = s2_combine(P.s2_prefix, my_ex);   // (P.s2_prefix visible after the scan's barriers)
+  __syncthreads();
+  S2 before = s2_combine(P.s2_prefix, my_ex);
 
   // --- walk: per-char scan values and the predicate.  o200k chars whose
   // contraction lookback reaches the previous thread's chars wait for the
