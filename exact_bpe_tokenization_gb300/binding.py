@@ -34,6 +34,8 @@ class TokTierError(RuntimeError):
 def lib():
     """The loaded library with declared signatures (raises if not built)."""
     global _lib
+    if _lib is not None:          # loaded once; no lock on the hot path
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -82,8 +84,17 @@ def _ptr(x):
     if hasattr(x, "data_ptr"):
         return x.data_ptr()
     if isinstance(x, np.ndarray):
-        return x.ctypes.data
+        return _np_addr(x)
     return int(x)
+
+
+def _np_addr(a):
+    """Address of a numpy array's data (a writable buffer through ctypes,
+    a third of the cost of ndarray.ctypes; read-only or empty ones the slow way)."""
+    try:
+        return ctypes.addressof(ctypes.c_char.from_buffer(a))
+    except (TypeError, ValueError):
+        return a.ctypes.data
 
 
 def _stream(stream):
@@ -165,8 +176,8 @@ def tt_encode_host(h, utf8, byte_offsets, out_ids, out_id_offsets, stream=None):
     """Host buffers in and out (numpy).  Returns the batch's status code."""
     u = np.ascontiguousarray(utf8, dtype=np.uint8)
     o = np.ascontiguousarray(byte_offsets, dtype=np.int64)
-    return lib().tt_encode_host(h, u.ctypes.data if len(u) else None, o.ctypes.data, len(o) - 1,
-                                out_ids.ctypes.data, len(out_ids), out_id_offsets.ctypes.data, _stream(stream))
+    return lib().tt_encode_host(h, _np_addr(u) if len(u) else None, _np_addr(o), len(o) - 1,
+                                _np_addr(out_ids), len(out_ids), _np_addr(out_id_offsets), _stream(stream))
 
 
 def tt_get_status(h, stream=None):

@@ -583,7 +583,8 @@ static tt_status check_batch_args(tt_tokenizer *h, const void *d_utf8, const int
 
 static tt_status encode_bounded(tt_tokenizer *h, const uint8_t *d_utf8, const int64_t *d_byte_offsets,
                                 int64_t n_requests, int64_t max_total_bytes, int32_t *d_out_ids,
-                                int64_t *d_out_id_offsets, int32_t *d_out_spans, tt_stream_t stream_) {
+                                int64_t *d_out_id_offsets, int32_t *d_out_spans, tt_stream_t stream_,
+                                const uint8_t *src = nullptr) {
   tt_status s = check_batch_args(h, d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, max_total_bytes);
   if (s != TT_OK) return s;
   if (max_total_bytes < 0 || max_total_bytes >= S2_MAX_POS - 64) return TT_ERR_CAPACITY;
@@ -595,7 +596,7 @@ static tt_status encode_bounded(tt_tokenizer *h, const uint8_t *d_utf8, const in
   std::lock_guard<std::mutex> lock(h->mu);
   Workspace *w;
   if ((s = get_workspace(h, stream, max_total_bytes, n_requests, &w)) != TT_OK) return s;
-  CallArgs args = {d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, nullptr, nullptr, d_out_spans};
+  CallArgs args = {d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, nullptr, nullptr, d_out_spans, src};
   TT_CUDA(cudaMemcpyAsync(w->W.args, &args, sizeof(args), cudaMemcpyHostToDevice, stream));
   if (h->profiling || !h->graphs_enabled) return enqueue_encode(h, w, stream, h->profiling);
   if (!w->graph) {
@@ -711,6 +712,10 @@ extern "C" tt_status tt_encode_host(tt_tokenizer *h, const uint8_t *utf8, const 
     dv_offs = dv_ids ? (int64_t *)device_view(out_id_offsets) : nullptr;
   }
   const bool direct = dv_ids && dv_offs;
+  // page-locked input is read in place by the pre-pass, which copies it to
+  // the device tile by tile (not with added-token literals: their search runs
+  // before the pre-pass)
+  const uint8_t *dv_in = total > 0 && !h->T.n_lit ? (const uint8_t *)device_view(utf8 + b0) : nullptr;
   const size_t in_b = ((size_t)total + 16 + 255) & ~(size_t)255;
   const size_t off_b = ((size_t)(n_requests + 1) * 8 + 255) & ~(size_t)255;
   const size_t out_b = direct ? 0 : ((size_t)total + 1) * 4;
@@ -743,10 +748,10 @@ extern "C" tt_status tt_encode_host(tt_tokenizer *h, const uint8_t *utf8, const 
       w->h_offs_cap = cap;
     }
     for (int64_t r = 0; r <= n_requests; ++r) w->h_offs[r] = byte_offsets[r] - b0;
-    if (total) TT_CUDA(cudaMemcpyAsync(d_in, utf8 + b0, (size_t)total, cudaMemcpyHostToDevice, stream));
+    if (total && !dv_in) TT_CUDA(cudaMemcpyAsync(d_in, utf8 + b0, (size_t)total, cudaMemcpyHostToDevice, stream));
     TT_CUDA(cudaMemcpyAsync(d_offs, w->h_offs, (size_t)(n_requests + 1) * 8, cudaMemcpyHostToDevice, stream));
   }
-  tt_status s = tt_encode_batch_bounded(h, d_in, d_offs, n_requests, total, d_out, d_out_offs, stream_);
+  tt_status s = encode_bounded(h, d_in, d_offs, n_requests, total, d_out, d_out_offs, nullptr, stream_, dv_in);
   if (s == TT_OK) s = enqueue_status_read(h, w, stream);
   if (s != TT_OK) {
     cudaStreamSynchronize(stream);   // the staged copies are done before the buffers are reused

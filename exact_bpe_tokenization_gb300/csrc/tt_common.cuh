@@ -400,6 +400,8 @@ struct CallArgs {
   int64_t *hook_starts;            // test hook outputs (NULL unless the hook runs)
   int64_t *hook_offsets;
   int32_t *out_spans;              // [2 * tokens]: (start, end) byte offsets from offs[0] per ID; NULL: none
+  const uint8_t *utf8_src;         // the same bytes in page-locked host memory: the pre-pass reads them there
+                                   // and copies each tile into utf8 (a buffer of the handle); NULL: none
 };
 
 // Per-stream workspace (device pointers; sizes fixed per capacity bucket).

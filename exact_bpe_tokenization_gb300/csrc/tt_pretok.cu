@@ -86,12 +86,13 @@ __device__ __forceinline__ uint32_t decode_at(const WS &S, int64_t ws, int64_t t
 }
 
 // Load the bytes of the window [ws, ws + WIN) and mark request starts.  All
-// threads participate.
+// threads participate.  src: where to read the batch (NULL: A.utf8).
 template <int NT, class WS>
-__device__ void load_bytes(const Tables &T, const CallArgs &A, int64_t base, int64_t total, int64_t ws, WS &S) {
+__device__ void load_bytes(const Tables &T, const CallArgs &A, int64_t base, int64_t total, int64_t ws, WS &S,
+                           const uint8_t *src = nullptr) {
   constexpr int PT_BYTES = WIN / NT;
   const int tid = threadIdx.x;
-  const uint8_t *g = A.utf8 + base;
+  const uint8_t *g = (src ? src : A.utf8) + base;
   const int64_t x0 = ws + PT_BYTES * tid;
   uint8_t *dst = &S.bytes[PT_BYTES * tid];
   if (x0 >= 0 && x0 + PT_BYTES <= total && ((reinterpret_cast<uintptr_t>(g + x0) & (PT_BYTES - 1)) == 0)) {
@@ -186,7 +187,14 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
   const int64_t ws = ts - HALO_L;
   // bytes and request starts suffice: the few chars the summaries look at
   // are decoded where they are met
-  load_bytes<NT>(T, A, base, total, ws, S);
+  load_bytes<NT>(T, A, base, total, ws, S, A.utf8_src);
+  if (A.utf8_src) {                           // the later kernels read the device copy of the tile
+    uint8_t *dst = const_cast<uint8_t *>(A.utf8) + base;
+    for (int k = 0; k < PT_BYTES; ++k) {
+      const int64_t x = ws + PT_BYTES * tid + k;
+      if (x >= ts && x < te) dst[x] = S.bytes[PT_BYTES * tid + k];
+    }
+  }
 
   // --- UTF-8 validation of the tile's bytes (RFC 3629, per request)
   for (int k = 0; k < PT_BYTES; ++k) {

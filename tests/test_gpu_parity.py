@@ -235,8 +235,9 @@ def test_graph_replay_eager_and_host_paths_agree(cuda, vocabs):
 
 
 def test_host_entry_point_pinned_direct_and_staged(cuda, vocabs):
-    """tt_encode_host with page-locked output buffers (written by the kernels
-    directly) and with pageable, mixed or too-small ones (staged and copied
+    """tt_encode_host with page-locked input (read in place by the pre-pass)
+    or pageable input (copied), and page-locked output buffers (written by the
+    kernels directly) or pageable, mixed or too-small ones (staged and copied
     back): the same IDs and offsets, the same status for a rejected request,
     and repeated calls reusing the buffers."""
     merges, vb, vo = vocabs["c1"]
@@ -253,12 +254,13 @@ def test_host_entry_point_pinned_direct_and_staged(cuda, vocabs):
              ("mixed", pin_ids.numpy(), np.zeros(len(offs), dtype=np.int64)),
              ("pinned, capacity below the bytes", pin_ids.numpy()[:ntok], pin_io.numpy())]
     for rep in range(2):
-        for name, ids, io in cases:
-            ids[:] = -7
-            st = cuda.tt_encode_host(tok.h, pin_in.numpy(), offs, ids, io)
-            assert st == cuda.TT_ERR_INVALID_UTF8, (name, st)
-            assert np.array_equal(io, ref["id_offsets"]), name
-            assert np.array_equal(ids[:ntok], ref["ids"]), name
+        for src_name, src in (("pinned input", pin_in.numpy()), ("pageable input", data)):
+            for name, ids, io in cases:
+                ids[:] = -7
+                st = cuda.tt_encode_host(tok.h, src, offs, ids, io)
+                assert st == cuda.TT_ERR_INVALID_UTF8, (src_name, name, st)
+                assert np.array_equal(io, ref["id_offsets"]), (src_name, name)
+                assert np.array_equal(ids[:ntok], ref["ids"]), (src_name, name)
     tok.close()
 
 
