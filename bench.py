@@ -250,9 +250,10 @@ def alg_bytes(kernel, c):
     return a["bytes"] + 4 * a["tokens"]
 
 
-def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of the kernel's file (else None)."""
+def recorded_traffic(kernel, workload, key="dram_bytes_per_launch"):
+    """A per-launch counter (DRAM bytes; warp instructions) from the committed
+    ncu summary, if it was taken on the current source of the kernel's file
+    (else None)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
     try:
@@ -268,8 +269,24 @@ def recorded_traffic(kernel, workload):
             sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
         except OSError:
             return None
-        return r.get("dram_bytes_per_launch") if sha == r.get("source_sha256") else None
+        return r.get(key) if sha == r.get("source_sha256") else None
     return None
+
+
+SMS, SCHEDULERS_PER_SM = 152, 4
+
+
+def issue_roofline(kernel, workload, launch_ms, sm_mhz):
+    """The kernel's instruction issue against the GPU's issue peak: one warp
+    instruction per cycle per scheduler, 4 schedulers per SM, at the SM clock
+    sampled during the run."""
+    inst = recorded_traffic(kernel, workload, "warp_inst_per_launch")
+    if inst is None or not sm_mhz or not launch_ms:
+        return None
+    achieved = inst / (launch_ms / 1e3)
+    peak = SMS * SCHEDULERS_PER_SM * sm_mhz * 1e6
+    return {"achieved": achieved, "peak": peak, "unit": "warp-inst/s", "frac": achieved / peak,
+            "warp_inst_per_launch": inst, "peak_from": "152 SMs x 4 schedulers x 1 warp-inst/cycle x SM clock"}
 
 
 def cpu_baseline(merges_vocab, family, seeds):
@@ -479,6 +496,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": recorded_traffic(dominant, WORKLOAD),
+                     "issue": issue_roofline(dominant, WORKLOAD, dom_ms,
+                                             (nclk.summary() if nclk.sm else clk.summary()).get("sm_mhz")),
                      "alg_bytes_per_launch": alg, "launch_ms": dom_ms,
                      "timing": "CUDA events around the kernel on its stream, L2 flushed before the launch",
                      "pieces": classes},
