@@ -69,7 +69,9 @@ struct tt_tokenizer {
   std::vector<void *> dev_allocs;
   DevStatus *d_status = nullptr;
   std::mutex mu;
-  std::map<cudaStream_t, Workspace *> ws;
+  // workspaces by (stream, capacity bucket): each batch size runs on the
+  // geometry of its own bucket, whatever ran on the stream before
+  std::map<std::pair<cudaStream_t, int64_t>, Workspace *> ws;
   std::atomic<int64_t> launches{0};
   bool profiling = false;
   std::vector<Pending> pending;
@@ -460,17 +462,17 @@ static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_
 // Capacities are powers of two (>= 64 KiB, >= 64 requests) so that a stream
 // sees few distinct buckets; growing drops the old bucket and its graph.
 static tt_status get_workspace(tt_tokenizer *h, cudaStream_t stream, int64_t bytes, int64_t reqs, Workspace **out) {
-  int64_t cb = (int64_t)next_pow2((uint64_t)std::max<int64_t>(bytes, 1 << 16));
+  const int64_t cb = (int64_t)next_pow2((uint64_t)std::max<int64_t>(bytes, 1 << 16));
   int64_t cr = (int64_t)next_pow2((uint64_t)std::max<int64_t>(reqs, 64));
-  auto it = h->ws.find(stream);
+  const auto key = std::make_pair(stream, cb);
+  auto it = h->ws.find(key);
   if (it != h->ws.end()) {
     Workspace *old = it->second;
-    if (old->cap_bytes >= cb && old->cap_reqs >= cr) {
+    if (old->cap_reqs >= cr) {
       *out = old;
       return TT_OK;
     }
-    cb = std::max(cb, old->cap_bytes);
-    cr = std::max(cr, old->cap_reqs);
+    cr = std::max(cr, old->cap_reqs);          // more requests than before: rebuild this bucket
     cudaStreamSynchronize(stream);
     free_workspace(old);
     h->ws.erase(it);
@@ -478,7 +480,7 @@ static tt_status get_workspace(tt_tokenizer *h, cudaStream_t stream, int64_t byt
   Workspace *w;
   tt_status s = make_workspace(h, cb, cr, &w);
   if (s != TT_OK) return s;
-  h->ws[stream] = w;
+  h->ws[key] = w;
   *out = w;
   return TT_OK;
 }

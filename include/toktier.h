@@ -176,6 +176,9 @@ tt_status tt_encode_batch(tt_tokenizer *h,
  *                    status TT_ERR_CAPACITY.
  * Work is launched as one CUDA graph per (stream, size bucket): the first
  * call of a bucket captures it (on a private stream), later calls replay it.
+ * Buckets are powers of two of max_total_bytes (at least 64 KiB); each
+ * (stream, bucket) keeps its own device workspace, about 31 bytes per byte of
+ * bucket capacity, until tt_destroy.
  * d_utf8 and d_out_ids may be NULL only if max_total_bytes is 0.
  */
 tt_status tt_encode_batch_bounded(tt_tokenizer *h,
