@@ -269,7 +269,9 @@ def test_two_streams_and_growing_batches(cuda, vocabs):
     tok = cuda.Tokenizer(merges, vb, vo, 1)
     o1 = oracle.Oracle(merges, vb, vo, 1)
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
-    for size in (1000, 70000, 300000, 20000):
+    # growing, then back to smaller buckets the streams already hold (each
+    # (stream, bucket) keeps its workspace and replays its own graph)
+    for size in (1000, 70000, 300000, 20000, 1000, 300000, 70000):
         jobs = []
         for si, s in enumerate(streams):
             reqs = [synth.transcript(100 * size + si * 7 + i, size // 4 + 1, 1) for i in range(4)]
