@@ -60,6 +60,27 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seeds(rank, steps, warmup):
+    """The request seeds a rank times and warms up on: every rank its own,
+    none shared between ranks or between warm-up and timed steps."""
+    return ([1 + rank * 10_000 + i for i in range(steps)],
+            [100_001 + rank * 10_000 + i for i in range(warmup)])
+
+
+def combine_ranks(device_s, nbytes, world, device):
+    """Whole-job figures: the slowest rank's device time and all ranks' bytes."""
+    if world <= 1:
+        return device_s, float(nbytes)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([device_s, float(nbytes)], dtype=torch.float64, device=device)
+    mx = t[:1].clone()
+    sm = t[1:].clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(sm[0])
+
+
 def requests_for(seeds):
     from exact_bpe_tokenization_gb300 import synth
     return [synth.workload(WORKLOAD, seed=s)[0] for s in seeds]
@@ -367,8 +388,7 @@ def run_ours(args):
     (merges, vb, vo), family = vocab()
     tok = binding.Tokenizer(merges, vb, vo, family)
     # each rank gets its own seeds (replicas of the same protocol)
-    seeds = [1 + rank * 10_000 + i for i in range(args.steps)]
-    warm_seeds = [100_001 + rank * 10_000 + i for i in range(args.warmup)]
+    seeds, warm_seeds = rank_seeds(rank, args.steps, args.warmup)
     host = [np.frombuffer(r, dtype=np.uint8) for r in requests_for(seeds)]
     warm = [np.frombuffer(r, dtype=np.uint8) for r in requests_for(warm_seeds)]
     cap = max(len(h) for h in host + warm)
@@ -410,14 +430,7 @@ def run_ours(args):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     nbytes = sum(len(h) for h in host)
     device_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([device_s, float(nbytes)], dtype=torch.float64, device=dev)
-        mx = t.clone()
-        dist.all_reduce(mx[:1], op=dist.ReduceOp.MAX)
-        dist.all_reduce(t[1:], op=dist.ReduceOp.SUM)
-        device_s, nbytes_all = float(mx[0]), float(t[1])
-    else:
-        nbytes_all = float(nbytes)
+    device_s, nbytes_all = combine_ranks(device_s, nbytes, world, dev)
     status, _ = tok.status()
     assert status == 0, binding.status_string(status)
     # tokens of the last step (for the e2e byte counts)
