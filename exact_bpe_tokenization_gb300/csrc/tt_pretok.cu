@@ -27,19 +27,37 @@
 
 namespace tt {
 
+// A window char's attributes in one word: the window index of its lead byte
+// (12 bits), its code point if ASCII else 0x80 (8), raw kind (5), effective
+// kind (4), and whether it starts a request or a segment (1).
+__device__ __forceinline__ uint32_t ci_pack(int lead, uint32_t cp8, uint32_t raw, bool rs) {
+  return (uint32_t)lead | (cp8 << 12) | (raw << 20) | ((uint32_t)rs << 29);
+}
+__device__ __forceinline__ int ci_lead(uint32_t c) { return (int)(c & 0xFFFu); }
+__device__ __forceinline__ uint32_t ci_cp8(uint32_t c) { return (c >> 12) & 0xFFu; }
+__device__ __forceinline__ uint8_t ci_raw(uint32_t c) { return (uint8_t)((c >> 20) & 0x1Fu); }
+__device__ __forceinline__ uint8_t ci_eff(uint32_t c) { return (uint8_t)((c >> 25) & 0xFu); }
+__device__ __forceinline__ bool ci_rs(uint32_t c) { return (c >> 29) & 1u; }
+static_assert(WIN <= 4096, "lead index is 12 bits");
+
 template <int NT>   // threads per window
 struct WinSmem {
   uint8_t bytes[WIN + 8];
   uint8_t rsb[WIN + 8];      // byte starts a request
-  uint8_t cp8[WIN];          // char's code point if ASCII, else 0x80
-  uint8_t raw[WIN];          // raw kind
-  uint8_t eff[WIN];          // effective kind
-  uint8_t rs[WIN];           // char starts a request or a segment beside an added-token literal
-  uint16_t lead[WIN];        // window index of the char's lead byte
+  uint32_t ci[WIN];          // per char: ci_pack
   int cbase[NT + 1];         // chars of thread t: [cbase[t], cbase[t+1])
   uint8_t ascii[128];
   int r0, r1;
   int nch;
+  __device__ __forceinline__ int lead(int j) const { return ci_lead(ci[j]); }
+  __device__ __forceinline__ uint32_t cp8(int j) const { return ci_cp8(ci[j]); }
+  __device__ __forceinline__ uint8_t raw(int j) const { return ci_raw(ci[j]); }
+  __device__ __forceinline__ uint8_t eff(int j) const { return ci_eff(ci[j]); }
+  __device__ __forceinline__ bool rs(int j) const { return ci_rs(ci[j]); }
+  // (only the char's own thread writes these; neighbours may read the word
+  // meanwhile, and the bits they read do not change)
+  __device__ __forceinline__ void set_eff(int j, uint8_t e) { ci[j] = (ci[j] & ~(0xFu << 25)) | ((uint32_t)e << 25); }
+  __device__ __forceinline__ void set_rs(int j) { ci[j] |= 1u << 29; }
 };
 
 // The prepass's view of a window: bytes, request starts and the ASCII classes.
@@ -154,10 +172,8 @@ __device__ void load_window(const Tables &T, const CallArgs &A, int64_t base, in
     const int i = PT_BYTES * tid + k;
     const uint32_t cp = decode_at(S, ws, total, i);
     const uint8_t mark = lit ? __ldg(lit + ws + i) : 0;
-    S.lead[j] = (uint16_t)i;
-    S.cp8[j] = cp < 128 ? (uint8_t)cp : (uint8_t)0x80;
-    S.raw[j] = mark == LIT_INNER ? (uint8_t)K_LIT : kind_of(T, S, cp);
-    S.rs[j] = S.rsb[i] | (mark == LIT_SEG);
+    S.ci[j] = ci_pack(i, cp < 128 ? cp : 0x80u, mark == LIT_INNER ? (uint32_t)K_LIT : kind_of(T, S, cp),
+                      S.rsb[i] || mark == LIT_SEG);
     ++j;
   }
   __syncthreads();
@@ -404,19 +420,19 @@ __device__ __forceinline__ Nbr make_nbr(const WS &S, const uint8_t *chain, int j
 #pragma unroll
   for (int k = 0; k < 5; ++k) {
     const int x = j - k;
-    if (k > 0 && (x < 0 || S.rs[x + 1])) inside = false;
-    e[k] = inside ? S.eff[x] : K_NONE;
-    c[k] = inside ? S.cp8[x] : 0;
+    if (k > 0 && (x < 0 || S.rs(x + 1))) inside = false;
+    e[k] = inside ? S.eff(x) : K_NONE;
+    c[k] = inside ? S.cp8(x) : 0;
   }
   b.e0 = e[0]; b.e1 = e[1]; b.e2 = e[2]; b.e3 = e[3]; b.e4 = e[4];
   b.c0 = c[0]; b.c1 = c[1]; b.c2 = c[2]; b.c3 = c[3]; b.c4 = c[4];
-  const bool in1 = j + 1 < S.nch && !S.rs[j + 1];
-  const bool in2 = in1 && j + 2 < S.nch && !S.rs[j + 2];
-  b.en1 = in1 ? S.eff[j + 1] : K_NONE;
-  b.en2 = in2 ? S.eff[j + 2] : K_NONE;
-  b.cn1 = in1 ? S.cp8[j + 1] : 0;
-  b.cn2 = in2 ? S.cp8[j + 2] : 0;
-  b.rs = S.rs[j] != 0;
+  const bool in1 = j + 1 < S.nch && !S.rs(j + 1);
+  const bool in2 = in1 && j + 2 < S.nch && !S.rs(j + 2);
+  b.en1 = in1 ? S.eff(j + 1) : K_NONE;
+  b.en2 = in2 ? S.eff(j + 2) : K_NONE;
+  b.cn1 = in1 ? S.cp8(j + 1) : 0;
+  b.cn2 = in2 ? S.cp8(j + 2) : 0;
+  b.rs = S.rs(j) != 0;
   if (chain) {
     b.l1 = j >= 1 ? chain[j - 1] != 0 : true;
     b.l2 = j >= 2 ? chain[j - 2] != 0 : true;
@@ -430,37 +446,44 @@ __device__ __forceinline__ Nbr make_nbr(const WS &S, const uint8_t *chain, int j
 // A char's neighbourhood slid along a thread's contiguous chars: each step
 // shifts the lookback registers and loads only what enters the window.
 struct Slider {
+  static constexpr uint32_t NO_CHAR = 1u << 29;   // past the window's chars: reads as a request start
   Nbr b;
   int32_t pos, p1, p2;   // byte positions of j, j+1, j+2
+  uint32_t w1, w2;       // char words of j+1, j+2 (one shared-memory load a step)
   template <class WS>
   __device__ __forceinline__ void start(const WS &S, int64_t ws, int j) {
     b = make_nbr(S, nullptr, j);
-    pos = (int32_t)(ws + S.lead[j]);
-    p1 = j + 1 < S.nch ? (int32_t)(ws + S.lead[j + 1]) : pos + 1;
-    p2 = j + 2 < S.nch ? (int32_t)(ws + S.lead[j + 2]) : pos + 2;
+    w1 = j + 1 < S.nch ? S.ci[j + 1] : NO_CHAR;
+    w2 = j + 2 < S.nch ? S.ci[j + 2] : NO_CHAR;
+    pos = (int32_t)(ws + S.lead(j));
+    p1 = j + 1 < S.nch ? (int32_t)(ws + ci_lead(w1)) : pos + 1;
+    p2 = j + 2 < S.nch ? (int32_t)(ws + ci_lead(w2)) : pos + 2;
   }
   template <class WS>
   __device__ __forceinline__ void step(const WS &S, int64_t ws, int j) {   // from j - 1 to j
-    const bool rsj = S.rs[j] != 0;
+    const uint32_t w0 = w1;
+    w1 = w2;
+    w2 = j + 2 < S.nch ? S.ci[j + 2] : NO_CHAR;
+    const bool rsj = ci_rs(w0);
     if (rsj) {
       b.e1 = b.e2 = b.e3 = b.e4 = K_NONE;
       b.c1 = b.c2 = b.c3 = b.c4 = 0;
-      b.e0 = S.eff[j];
-      b.c0 = S.cp8[j];
+      b.e0 = ci_eff(w0);
+      b.c0 = ci_cp8(w0);
     } else {
       b.e4 = b.e3; b.e3 = b.e2; b.e2 = b.e1; b.e1 = b.e0; b.e0 = b.en1;
       b.c4 = b.c3; b.c3 = b.c2; b.c2 = b.c1; b.c1 = b.c0; b.c0 = b.cn1;
     }
     b.rs = rsj;
-    const bool in1 = j + 1 < S.nch && !S.rs[j + 1];
-    const bool in2 = in1 && j + 2 < S.nch && !S.rs[j + 2];
+    const bool in1 = !ci_rs(w1);
+    const bool in2 = in1 && !ci_rs(w2);
     if (!rsj) { b.en1 = in1 ? b.en2 : K_NONE; b.cn1 = in1 ? b.cn2 : 0; }   // old j+2 is new j+1
-    else { b.en1 = in1 ? S.eff[j + 1] : K_NONE; b.cn1 = in1 ? S.cp8[j + 1] : 0; }
-    b.en2 = in2 ? S.eff[j + 2] : K_NONE;
-    b.cn2 = in2 ? S.cp8[j + 2] : 0;
+    else { b.en1 = in1 ? ci_eff(w1) : K_NONE; b.cn1 = in1 ? ci_cp8(w1) : 0; }
+    b.en2 = in2 ? ci_eff(w2) : K_NONE;
+    b.cn2 = in2 ? ci_cp8(w2) : 0;
     pos = p1;
     p1 = p2;
-    p2 = j + 2 < S.nch ? (int32_t)(ws + S.lead[j + 2]) : pos + 2;
+    p2 = j + 2 < S.nch ? (int32_t)(ws + ci_lead(w2)) : pos + 2;
   }
 };
 
@@ -490,37 +513,37 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
   if (fam == FAM_O200K) {
     int2 v = make_int2(-1, -1);
     for (int j = c0; j < c1; ++j) {
-      const int64_t pos = ws + S.lead[j];
+      const int64_t pos = ws + S.lead(j);
       if (pos < ts - S1_SHIFT) continue;
-      const bool in_prev = !S.rs[j] && j > 0;
-      const uint8_t rp = in_prev ? S.raw[j - 1] : K_NONE;
-      const uint32_t cpp = in_prev ? S.cp8[j - 1] : 0;
-      const uint8_t rn = (j + 1 < S.nch && !S.rs[j + 1]) ? S.raw[j + 1] : K_NONE;
-      if (region_start(S.raw[j], rp)) v.x = (int)pos;
-      if (trigger(S.raw[j], rp, cpp, rn)) v.y = (int)pos;
+      const bool in_prev = !S.rs(j) && j > 0;
+      const uint8_t rp = in_prev ? S.raw(j - 1) : K_NONE;
+      const uint32_t cpp = in_prev ? S.cp8(j - 1) : 0;
+      const uint8_t rn = (j + 1 < S.nch && !S.rs(j + 1)) ? S.raw(j + 1) : K_NONE;
+      if (region_start(S.raw(j), rp)) v.x = (int)pos;
+      if (trigger(S.raw(j), rp, cpp, rn)) v.y = (int)pos;
     }
     auto mx = [](int2 a, int2 b) { return make_int2(max(a.x, b.x), max(a.y, b.y)); };
     int2 ex = block_exclusive_scan<NT>(v, mx, make_int2(-1, -1), P.i2_tmp, (int2 *)nullptr);
     int2 run = mx(W.s1_carry[t], ex);
     for (int j = c0; j < c1; ++j) {
-      const int64_t pos = ws + S.lead[j];
-      if (pos < ts - S1_SHIFT) { S.eff[j] = effective(fam, S.raw[j], false); continue; }
-      const bool in_prev = !S.rs[j] && j > 0;
-      const uint8_t rp = in_prev ? S.raw[j - 1] : K_NONE;
-      const uint32_t cpp = in_prev ? S.cp8[j - 1] : 0;
-      const uint8_t rn = (j + 1 < S.nch && !S.rs[j + 1]) ? S.raw[j + 1] : K_NONE;
-      if (region_start(S.raw[j], rp)) run.x = (int)pos;
-      if (trigger(S.raw[j], rp, cpp, rn)) run.y = (int)pos;
-      const bool mark_other = S.raw[j] == K_MARK && run.x >= 0 && run.y >= run.x;
-      S.eff[j] = effective(fam, S.raw[j], mark_other);
+      const int64_t pos = ws + S.lead(j);
+      if (pos < ts - S1_SHIFT) { S.set_eff(j, effective(fam, S.raw(j), false)); continue; }
+      const bool in_prev = !S.rs(j) && j > 0;
+      const uint8_t rp = in_prev ? S.raw(j - 1) : K_NONE;
+      const uint32_t cpp = in_prev ? S.cp8(j - 1) : 0;
+      const uint8_t rn = (j + 1 < S.nch && !S.rs(j + 1)) ? S.raw(j + 1) : K_NONE;
+      if (region_start(S.raw(j), rp)) run.x = (int)pos;
+      if (trigger(S.raw(j), rp, cpp, rn)) run.y = (int)pos;
+      const bool mark_other = S.raw(j) == K_MARK && run.x >= 0 && run.y >= run.x;
+      S.set_eff(j, effective(fam, S.raw(j), mark_other));
     }
   } else {
     for (int j = c0; j < c1; ++j) {
-      S.eff[j] = effective(fam, S.raw[j], false);
+      S.set_eff(j, effective(fam, S.raw(j), false));
       // deepseek-style: segment starts of the first two splitters act as
       // request starts (j = 0 has no predecessor in the window; it lies in
       // the left halo, further back than any rule or scan looks)
-      if (fam == FAM_DEEPSEEK && j > 0 && ds_segment_start(S.raw[j - 1], S.raw[j])) S.rs[j] = 1;
+      if (fam == FAM_DEEPSEEK && j > 0 && ds_segment_start(S.raw(j - 1), S.raw(j))) S.set_rs(j);
     }
   }
   __syncthreads();
@@ -529,8 +552,8 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
   // published aggregate covers the shifted tile [ts - 16, te - 16)
   const int64_t s2_lo = ts - S2_SHIFT, s2_pub_hi = t == ntiles - 1 ? INT64_MAX : te - S2_SHIFT;
   int jlo = c0, jhi = c1;                       // my chars with pos in [s2_lo, te)
-  while (jlo < jhi && ws + S.lead[jlo] < s2_lo) ++jlo;
-  while (jhi > jlo && ws + S.lead[jhi - 1] >= te) --jhi;
+  while (jlo < jhi && ws + S.lead(jlo) < s2_lo) ++jlo;
+  while (jhi > jlo && ws + S.lead(jhi - 1) >= te) --jhi;
   S2 agg_all = s2_identity(), agg_pub = s2_identity();
   bool pub_done = false;
   if (jlo < jhi) {
@@ -561,21 +584,21 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
   {
     int rq_first = 0xFFFF;
     for (int j = c0; j < c1; ++j) {
-      const int64_t pos = ws + S.lead[j];
+      const int64_t pos = ws + S.lead(j);
       if (pos < ts || pos >= te) continue;
-      const uint8_t ew = rq_ws_event(fam, S.rs[j], S.raw[j], S.cp8[j]);
-      const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
+      const uint8_t ew = rq_ws_event(fam, S.rs(j), S.raw(j), S.cp8(j));
+      const uint8_t eu = rq_up_event(S.rs(j), S.raw(j));
       if ((rq_first & 0xFF) == 0xFF && ew != 0xFF) rq_first = (rq_first & 0xFF00) | ew;
       if ((rq_first >> 8) == 0xFF && eu != 0xFF) rq_first = (rq_first & 0x00FF) | (eu << 8);
     }
     int after = first(block_exclusive_suffix<NT>(rq_first, first, 0xFFFF, P.i_tmp, (int *)nullptr),
                       W.rq_carry[2 * t] | (W.rq_carry[2 * t + 1] << 8));
     for (int j = c1 - 1; j >= c0; --j) {
-      const int64_t pos = ws + S.lead[j];
+      const int64_t pos = ws + S.lead(j);
       if (pos < ts || pos >= te) continue;
       P.rq8[j] = (uint8_t)((after & 0x3) | (((after >> 8) & 0x3) << 2));
-      const uint8_t ew = rq_ws_event(fam, S.rs[j], S.raw[j], S.cp8[j]);
-      const uint8_t eu = rq_up_event(S.rs[j], S.raw[j]);
+      const uint8_t ew = rq_ws_event(fam, S.rs(j), S.raw(j), S.cp8(j));
+      const uint8_t eu = rq_up_event(S.rs(j), S.raw(j));
       if (ew != 0xFF) after = (after & 0xFF00) | ew;
       if (eu != 0xFF) after = (after & 0x00FF) | (eu << 8);
     }
@@ -599,7 +622,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
     if (st && filter) {
       const int64_t r = lower_bound64(A.offs, A.n + 1, base + pos + 1) - 1;
       if (r >= 0 && r < A.n && W.bad[r]) {
-        if (S.rsb[S.lead[j]]) placeholder |= 1u << (j - c0);   // the request's start, not a literal's
+        if (S.rsb[S.lead(j)]) placeholder |= 1u << (j - c0);   // the request's start, not a literal's
         else st = false;
       }
     }
@@ -647,7 +670,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
   __syncthreads();
   for (uint32_t m = deferred; m; m &= m - 1) {
     const int j = c0 + __ffs(m) - 1;
-    const int64_t pos = ws + S.lead[j];
+    const int64_t pos = ws + S.lead(j);
     const Nbr nb = make_nbr(S, P.chain, j);
     const uint16_t g = P.dagg[tid][j - c0];
     Aggs a;
@@ -669,7 +692,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
   int my_first = INT_MAX, my_last = -1;
   for (uint32_t m = starts; m; m &= m - 1) {
     const int b = __ffs(m) - 1;
-    const int code = (int)(ws + S.lead[c0 + b]) * 2 + (int)((placeholder >> b) & 1);
+    const int code = (int)(ws + S.lead(c0 + b)) * 2 + (int)((placeholder >> b) & 1);
     if (my_first == INT_MAX) my_first = code;
     my_last = code;
   }
@@ -710,10 +733,10 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
   for (uint32_t m = starts; m; m &= m - 1) {
     const int b = __ffs(m) - 1;
     const int j = c0 + b;
-    const int32_t pos = (int32_t)(ws + S.lead[j]);
+    const int32_t pos = (int32_t)(ws + S.lead(j));
     const bool ph = (placeholder >> b) & 1;
     W.piece_start[k] = ph ? (int32_t)(pos | 0x80000000u) : pos;
-    if (S.rsb[S.lead[j]]) {                   // first piece of the requests starting here
+    if (S.rsb[S.lead(j)]) {                   // first piece of the requests starting here
       int r = S.r0 + (int)lower_bound64(A.offs + S.r0, S.r1 - S.r0, base + pos);
       for (; r < S.r1 && __ldg(&A.offs[r]) == base + pos; ++r) W.req_piece[r] = k;
     }
