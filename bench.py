@@ -457,6 +457,27 @@ def run_ours(args):
         if i >= 3:
             ss.append(s0.elapsed_time(s1))
 
+    # small requests (the paper's Figure 10 quotes 1K chars): device time of a
+    # 1,000-char request and of the 64 KB tiny configuration, 50 calls each
+    # after one untimed call, L2 flushed before each
+    small = {}
+    for label, text in (("1k_chars", synth.transcript(5, 1000, synth.PROFILE_MIXED)),
+                        ("tiny_ascii_64k", synth.workload("tiny_ascii_64k")[0])):
+        dsm = torch.from_numpy(np.frombuffer(text, dtype=np.uint8).copy()).to(dev)
+        osm = torch.tensor([0, len(text)], dtype=torch.int64, device=dev)
+        tsm = []
+        for k in range(51):
+            flush.fill_(k)
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            binding.tt_encode_batch_bounded(tok.h, dsm, osm, 1, len(text), out_ids, out_off, stream)
+            s1.record(stream)
+            s1.synchronize()
+            if k:
+                tsm.append(s0.elapsed_time(s1))
+        small[label] = {"bytes": len(text), "p50_ms": float(np.percentile(tsm, 50)),
+                        "p99_ms": float(np.percentile(tsm, 99)), "vocab": "the main line's 100,000 merges"}
+
     # end to end through host buffers (copies and the wait inside): each
     # step's request sits in pinned host memory before the timed call, and
     # its IDs come back into pinned host memory
@@ -533,6 +554,7 @@ def run_ours(args):
                      "timing": "CUDA events around the kernel on its stream, L2 flushed before the launch",
                      "pieces": classes},
         "kernels_ms_per_launch": {k: round(v["ms_per_launch"], 5) for k, v in per_kernel.items()},
+        "small_requests": small,
         "steady_state": {"p50_ms": float(np.percentile(ss, 50)), "p99_ms": float(np.percentile(ss, 99)),
                          "protocol": "one 1M-char request, 200 graph replays back to back, no L2 flush"},
     }
