@@ -7,17 +7,20 @@
 // Three kernels per batch:
 //   k_prepass   one CTA per 4016-byte tile, independent: validates UTF-8
 //               (per request), and summarises each tile for the two scans
-//               whose carries are computed ahead of time: o200k mark
-//               resolution (max-scan of stretch starts and triggers, on a
-//               tiling shifted 32 bytes left) and the reverse "first event
-//               after" queries.
+//               whose carries are computed ahead of time, from the bytes
+//               alone: the reverse "first event after" queries (one warp
+//               from the tile start) and o200k mark resolution (the last
+//               stretch start and trigger, on a tiling shifted 32 bytes left:
+//               one warp back from the tile end); it also copies page-locked
+//               host input into the device batch when asked to.
 //   k_tilescan  one CTA: exclusive scans of those tile summaries (forward for
 //               marks, backward for the reverse queries); resets look-back
 //               flags.
-//   k_pretok    one CTA per tile, tiles claimed in order: effective classes,
-//               the forward scan (number-run count, blank-run start, o200k
-//               contraction chain and case state) with decoupled look-back on
-//               a tiling shifted 16 bytes left, the reverse queries, the
+//   k_pretok    one CTA per tile, tiles claimed in order: effective classes
+//               (deepseek-style: segment starts), the forward scan (number-run
+//               count, blank-run start, o200k contraction chain and case
+//               state) with decoupled look-back on a tiling shifted 16 bytes
+//               left, its aggregate published before the reverse queries, the
 //               predicate, and compaction of piece starts with a second
 //               decoupled look-back.
 #include <limits.h>
