@@ -14,9 +14,10 @@
 // the whole-piece probe and 16 lanes per piece for merging (state in
 // registers), a warp per piece up to 256 bytes (registers up to 32 bytes,
 // else a linked list in shared memory), a 512-thread block per longer piece
-// (state in global memory, ping-pong buffers).  IDs land in a
-// byte-indexed scratch array; k_ids scans the per-piece counts with
-// decoupled look-back and writes the final contiguous IDs.
+// (a linked list in shared memory up to 8 KiB, else global ping-pong
+// buffers).  IDs land in a byte-indexed scratch array; k_ids scans the
+// per-piece counts with decoupled look-back, writes the final contiguous IDs
+// and each request's ID offset.
 #include <limits.h>
 
 #include "tt_common.cuh"
