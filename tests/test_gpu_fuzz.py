@@ -52,9 +52,10 @@ def random_request(rng):
     return b"".join(parts)
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
 @pytest.mark.parametrize("family", [1, 2, 3])
-def test_fuzz_batch_against_the_oracle(cuda, family):
-    rng = random.Random(1000 + family)
+def test_fuzz_batch_against_the_oracle(cuda, family, seed):
+    rng = random.Random(1000 * seed + family)
     reqs = [random_request(rng) for _ in range(6000)] + [b"", b"", b" "]
     profile = {1: synth.PROFILE_MIXED, 2: synth.PROFILE_CAMEL_MARKS, 3: synth.PROFILE_KANA_HAN}[family]
     vocab = synth.make_vocab(profile, 1 << 20, 8000)
