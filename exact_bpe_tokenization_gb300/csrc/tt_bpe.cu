@@ -1,6 +1,6 @@
 // tt_bpe.cu - segmented byte-level BPE over the piece table and output
 // compaction (TokTier: Exact Stateful CPU+GPU Tokenization for Agentic LLM
-// Serving, §4.2 "segmented BPE" and §4.3 "output compaction").
+// Serving, §4.2 on BPE per piece and §4.3 on compacting the output).
 //
 // Every piece is encoded independently.  A piece whose bytes are a
 // vocabulary entry is emitted as that one ID (the whole-piece shortcut).

@@ -1,7 +1,7 @@
 // tt_rules.cuh - run-local piece-start rules of the pattern families.
 //
 // TokTier: Exact Stateful CPU+GPU Tokenization for Agentic LLM Serving, §4.1
-// ("run decomposition"): each character gets one of four classes (letter,
+// (the run decomposition): each character gets one of four classes (letter,
 // number, whitespace, other); whether it begins a piece depends only on its
 // offset in its maximal same-class run, at most four characters of lookback
 // across the run boundary, and per-run aggregates (run start, first non-CRLF,

@@ -191,7 +191,7 @@ tt_status tt_encode_batch_bounded(tt_tokenizer *h,
  * source bytes it covers.
  *
  * The paper's session state holds, beside each token ID, the byte span of the
- * text it encodes (TokTier §3 "session store"; §5.7, Figure 14a: 4 bytes of
+ * text it encodes (TokTier §3, the per-session store; §5.7, Figure 14a: 4 bytes of
  * ID and 8 bytes of span per token), and its GPU full path returns IDs
  * without spans, so a state miss that must build that state falls back to the
  * CPU (§4.4).  This call returns both.

@@ -4,16 +4,17 @@
  * load this library.  It shares no code with the CUDA path.
  *
  * What it computes (TokTier: Exact Stateful CPU+GPU Tokenization for Agentic
- * LLM Serving, §3.1 "two stages", and the pipeline definition F = E* o G of
- * the summary page's §2.2): for every request independently,
+ * LLM Serving, §3.1: pre-tokenization, then BPE per piece; and the pipeline
+ * definition F = E* o G of the summary page's §2.2): for every request
+ * independently,
  *   1. decode the request as strict UTF-8 (a request that is not valid
  *      UTF-8 is rejected and yields no IDs);
  *   2. pre-tokenize it G: starting at position 0, try the pattern family's
  *      alternatives in order, take the first that matches (each alternative
  *      with the regex's own greedy-with-backtracking semantics), emit that
- *      match as one piece and continue at its end (leftmost-first alternation,
- *      §4.1 "GPT-family tokenizers specify pre-tokenization as a leftmost-first
- *      alternation regex with backtracking");
+ *      match as one piece and continue at its end (§4.1: the GPT-family
+ *      patterns are ordered alternatives tried leftmost-first, each with the
+ *      usual backtracking);
  *   3. encode every piece E independently (§4.2): if the piece's bytes are a
  *      vocabulary entry emit that one ID (the ignore_merges shortcut), else
  *      start from single-byte IDs and repeatedly merge the LEFTMOST occurrence

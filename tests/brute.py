@@ -4,8 +4,9 @@
    the textbook semantics of ordered alternation, greedy quantifiers with
    backtracking and negative lookahead.  The two pattern families are written
    as ASTs; pieces are found the way a leftmost-first regex scanner finds
-   them (TokTier, §4.1: "a leftmost-first alternation regex with
-   backtracking").  It shares nothing with oracle.c but the frozen class table.
+   them (TokTier, §4.1: the patterns are ordered alternatives tried
+   leftmost-first, with backtracking).  It shares nothing with oracle.c but
+   the frozen class table.
 2. The textbook BPE definition: every step rescans all adjacent pairs, takes
    the lowest rank and merges its leftmost occurrence (TokTier, §4.2).
 3. The same pattern families as pattern strings for the installed `regex`
