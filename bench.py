@@ -255,8 +255,9 @@ def piece_classes(binding, tok, d_in, d_off, ids, vocab_offsets, cap, dev):
 
 
 def alg_bytes(kernel, c):
-    """Algorithmic bytes of one launch ("Kernels and their
-    rooflines"): bytes a kernel must read and write at minimum."""
+    """Algorithmic bytes of one launch: what a kernel must read and write at
+    minimum for the pieces and tokens it handles (intermediate traffic such
+    as hash-table gathers is not credited)."""
     a = c["all"]
     if kernel in ("k_prepass", "k_tilescan"):
         return a["bytes"]                                     # the batch bytes, read once
