@@ -144,6 +144,9 @@ __device__ __forceinline__ int bpe_lanes(const Tables &T, const uint8_t *bytes, 
 // of a run from its left end: the leftmost non-overlapping set.  Pairs made
 // by a merge rank above r (well-ordered list), so they never join a run.
 constexpr int WARP_KERNEL_WARPS = BPE_WARP_THREADS / 32;
+// workspaces above this size (batches; the single request stays below) pair
+// the pieces of 49..128 bytes
+constexpr int64_t PAIR_MIN_CAP_BYTES = 4ll << 20;
 constexpr int SMALL_CHUNK = 32;   // pieces per small-piece ticket
 
 __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, const uint8_t *g, int64_t total,
@@ -315,6 +318,156 @@ __device__ __forceinline__ int list_rounds(const Tables &T, const uint8_t *b, in
   return cnt;
 }
 
+// Two pieces of at most PAIR_MAX bytes side by side, 16 lanes each (half h
+// of the warp takes piece h; lane l of a half owns positions l, l + 16, ...),
+// each half on its own 128-entry share of the warp's arrays.  Rounds run in
+// lockstep: each half takes its own lowest rank (an xor butterfly over its 16
+// lanes) and merges as list_rounds does; a half with nothing left idles until
+// the other is done.  Each half passes its own piece (n = 0: none) and gets
+// its IDs' count.  For batches, where warps are the scarce resource: a round's
+// instructions serve two pieces.
+constexpr int PAIR_MAX = MID_MAX / 2;
+__device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, int n, int32_t *out, int32_t *tok,
+                                           int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
+  constexpr int NS = PAIR_MAX / 16;
+  constexpr unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31, hl = lane & 15;
+  const unsigned lt_mask = (1u << hl) - 1;
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    const int p = hl + 16 * k;
+    tok[p] = p < n ? __ldg(&T.byte_id[__ldg(b + p)]) : -1;
+    rank[p] = INT_MAX;
+    nx[p] = (int16_t)(p + 1);
+    pv[p] = (int16_t)(p - 1);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k0 = 0; k0 < NS; k0 += 4) {        // initial lookups, four first probes in flight at a time
+    uint4 ent[4];
+    uint32_t sl[4];
+    int lt[4], rt[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int p = hl + 16 * (k0 + k);
+      const bool v = p + 1 < n;
+      lt[k] = v ? tok[p] : 0;
+      rt[k] = v ? tok[p + 1] : 0;
+      sl[k] = pair_slot(T, lt[k], rt[k]);
+      ent[k] = v ? __ldg(&T.pair_tab[sl[k]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int p = hl + 16 * (k0 + k);
+      if (p + 1 < n) {
+        const int2 pr = pair_finish(T, ent[k], sl[k], lt[k], rt[k]);
+        rank[p] = rank_or_max(pr.x);
+        res[p] = pr.y;
+      }
+    }
+  }
+  __syncwarp();
+  for (int round = 0; round < PAIR_MAX; ++round) {   // a half with pairs unlinks at least one symbol a round
+    int rr[NS];
+    int r = INT_MAX;
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      rr[k] = rank[hl + 16 * k];
+      r = min(r, rr[k]);
+    }
+#pragma unroll
+    for (int d = 8; d >= 1; d >>= 1) r = min(r, __shfl_xor_sync(FULL, r, d));   // my half's lowest rank
+    if (__all_sync(FULL, r == INT_MAX)) break;
+    for (int step = 0; step < PAIR_MAX; ++step) {   // (a bound the same on every lane: the loop holds warp votes)
+      if (step > 0) {
+#pragma unroll
+        for (int k = 0; k < NS; ++k) rr[k] = rank[hl + 16 * k];
+      }
+      uint32_t sel = 0;
+      bool left = false;
+#pragma unroll
+      for (int k = 0; k < NS; ++k) {
+        if (r != INT_MAX && rr[k] == r) {
+          const int q = pv[hl + 16 * k];
+          if (q < 0 || rank[q] != r) sel |= 1u << k;
+          else left = true;
+        }
+      }
+      __syncwarp();
+      for (uint32_t m = sel; m; m &= m - 1) {
+        const int p = hl + 16 * (__ffs(m) - 1);
+        const int q = nx[p], nq = nx[q];
+        tok[p] = res[p];
+        tok[q] = -1;
+        rank[q] = INT_MAX;
+        rank[p] = INT_MAX;
+        nx[p] = (int16_t)nq;
+        if (nq < n) pv[nq] = (int16_t)p;
+      }
+      __syncwarp();
+      for (uint32_t m = sel; m; m &= m - 1) {
+        const int p = hl + 16 * (__ffs(m) - 1);
+        const int a = pv[p], c = nx[p];
+        const int tp = tok[p];
+        const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
+        const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
+        const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+        const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+        if (a >= 0) {
+          const int2 pr = pair_finish(T, ea, sa, ta, tp);
+          rank[a] = rank_or_max(pr.x);
+          res[a] = pr.y;
+        }
+        if (c < n) {
+          const int2 pr = pair_finish(T, ec, sc, tp, tc);
+          rank[p] = rank_or_max(pr.x);
+          res[p] = pr.y;
+        }
+      }
+      __syncwarp();
+      if (!__any_sync(FULL, left)) break;
+    }
+  }
+  // surviving tokens of my half in position order
+  int cnt = 0;
+  const int sh = lane & 16;
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    const int t = tok[hl + 16 * k];
+    const unsigned bal = (__ballot_sync(FULL, t >= 0) >> sh) & 0xFFFFu;
+    if (t >= 0) out[cnt + __popc(bal & lt_mask)] = t;
+    cnt += __popc(bal);
+  }
+  __syncwarp();
+  return cnt;
+}
+
+// Two listed pieces of 49 .. PAIR_MAX bytes (pc1 < 0: only one) on one warp:
+// each half probes its piece whole, then the misses merge side by side.
+__device__ __forceinline__ void mid_pair(const Tables &T, const Work &W, const uint8_t *g, int pc0, int pc1,
+                                         int32_t *tok, int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
+  const int lane = threadIdx.x & 31, half = lane >> 4;
+  const int pc = half ? pc1 : pc0;
+  int32_t s = 0;
+  int n = 0;
+  if (pc >= 0) {
+    s = __ldcg(&W.piece_start[pc]);
+    n = (__ldcg(&W.piece_start[pc + 1]) & 0x7FFFFFFF) - s;
+  }
+  const uint8_t *b = g + s;
+  int id = -1;
+  if ((lane & 15) == 0 && n > 0 && n <= T.max_tok_len) id = vocab_probe(T, b, n);
+  id = __shfl_sync(0xffffffffu, id, lane & 16);
+  if (id >= 0) {
+    if ((lane & 15) == 0) { W.scratch[s] = id; W.n_ids[pc] = 1; }
+    n = 0;                                    // this half idles
+  }
+  const int off = half * PAIR_MAX;
+  const int cnt = pair_rounds(T, b, n, W.scratch + s, tok + off, rank + off, res + off, nx + off, pv + off);
+  if ((lane & 15) == 0 && n > 0) W.n_ids[pc] = cnt;
+  __syncwarp();
+}
+
 __device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const uint8_t *g, int pc, int32_t *tok,
                                           int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
   const int lane = threadIdx.x & 31;
@@ -365,8 +518,12 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
   const int c0 = __ldcg(&W.counters[mid_bucket_counter(0)]), c1 = __ldcg(&W.counters[mid_bucket_counter(1)]);
   const int c2 = __ldcg(&W.counters[mid_bucket_counter(2)]);
   // ticket order, longest expected work first: listed pieces of 49..256
-  // bytes, chunks of short pieces, listed pieces of 17..48 bytes
-  const int t1 = c0 + c1, t2 = t1 + (np + SMALL_CHUNK - 1) / SMALL_CHUNK, nwork = t2 + c2;
+  // bytes, chunks of short pieces, listed pieces of 17..48 bytes.  In
+  // workspaces beyond the single-request size the pieces of 49..128 bytes go
+  // two to a ticket (pair_rounds)
+  const bool pairs = W.cap_bytes > PAIR_MIN_CAP_BYTES;
+  const int tb1 = pairs ? (c1 + 1) / 2 : c1;
+  const int t1 = c0 + tb1, t2 = t1 + (np + SMALL_CHUNK - 1) / SMALL_CHUNK, nwork = t2 + c2;
   const int64_t lcap = list_cap(W.cap_bytes);
   const uint8_t *g = A.utf8 + base;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -375,7 +532,12 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
     if (lane == 0) gi = atomicAdd(&W.counters[9], 1);
     gi = __shfl_sync(0xffffffffu, gi, 0);
     if (gi >= nwork) break;
-    if (gi < t1 || gi >= t2) {
+    if (pairs && gi >= c0 && gi < t1) {
+      const int i = 2 * (gi - c0);
+      const int pc1 = i + 1 < c1 ? __ldcg(&W.long_list[lcap + i + 1]) : -1;
+      mid_pair(T, W, g, __ldcg(&W.long_list[lcap + i]), pc1, s_tok[warp], s_rank[warp], s_res[warp],
+               s_nx[warp], s_pv[warp]);
+    } else if (gi < t1 || gi >= t2) {
       const int64_t slot = gi < c0 ? gi : gi < t1 ? lcap + (gi - c0) : 2 * lcap + (gi - t2);
       mid_piece(T, W, g, __ldcg(&W.long_list[slot]), s_tok[warp], s_rank[warp], s_res[warp], s_nx[warp],
                 s_pv[warp]);
