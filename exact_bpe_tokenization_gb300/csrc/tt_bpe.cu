@@ -503,6 +503,9 @@ __device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const 
   __syncwarp();
 }
 
+// PAIRS: the batch instantiation (pieces of 49..128 bytes two to a warp); the
+// single-request one is compiled without that path.
+template <bool PAIRS>
 __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_warp(Tables T, Work W) {
   __shared__ int32_t s_tok[WARP_KERNEL_WARPS][MID_MAX];   // token, -1 once unlinked
   __shared__ int32_t s_rank[WARP_KERNEL_WARPS][MID_MAX];  // rank of (p, next), INT_MAX if none
@@ -521,7 +524,7 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
   // bytes, chunks of short pieces, listed pieces of 17..48 bytes.  In
   // workspaces beyond the single-request size the pieces of 49..128 bytes go
   // two to a ticket (pair_rounds)
-  const bool pairs = W.cap_bytes > PAIR_MIN_CAP_BYTES;
+  constexpr bool pairs = PAIRS;
   const int tb1 = pairs ? (c1 + 1) / 2 : c1;
   const int t1 = c0 + tb1, t2 = t1 + (np + SMALL_CHUNK - 1) / SMALL_CHUNK, nwork = t2 + c2;
   const int64_t lcap = list_cap(W.cap_bytes);
@@ -532,7 +535,7 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
     if (lane == 0) gi = atomicAdd(&W.counters[9], 1);
     gi = __shfl_sync(0xffffffffu, gi, 0);
     if (gi >= nwork) break;
-    if (pairs && gi >= c0 && gi < t1) {
+    if (PAIRS && gi >= c0 && gi < t1) {
       const int i = 2 * (gi - c0);
       const int pc1 = i + 1 < c1 ? __ldcg(&W.long_list[lcap + i + 1]) : -1;
       mid_pair(T, W, g, __ldcg(&W.long_list[lcap + i]), pc1, s_tok[warp], s_rank[warp], s_res[warp],
@@ -1050,7 +1053,8 @@ __global__ void k_hook_offsets(Work W) {
 }
 
 void launch_bpe_warp(const Tables &T, const Work &W, int grid, cudaStream_t s) {
-  k_bpe_warp<<<grid, BPE_WARP_THREADS, 0, s>>>(T, W);
+  if (W.cap_bytes > PAIR_MIN_CAP_BYTES) k_bpe_warp<true><<<grid, BPE_WARP_THREADS, 0, s>>>(T, W);
+  else k_bpe_warp<false><<<grid, BPE_WARP_THREADS, 0, s>>>(T, W);
 }
 void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   k_bpe_long<<<grid, BPE_LONG_THREADS, LONG_SMEM_BYTES, s>>>(T, W);
