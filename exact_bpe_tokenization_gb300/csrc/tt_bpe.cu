@@ -326,10 +326,12 @@ __device__ __forceinline__ int list_rounds(const Tables &T, const uint8_t *b, in
 // the other is done.  Each half passes its own piece (n = 0: none) and gets
 // its IDs' count.  For batches, where warps are the scarce resource: a round's
 // instructions serve two pieces.
+// NS: positions per lane (pieces of at most 16 * NS bytes).
 constexpr int PAIR_MAX = MID_MAX / 2;
+template <int NS>
 __device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, int n, int32_t *out, int32_t *tok,
                                            int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
-  constexpr int NS = PAIR_MAX / 16;
+  static_assert(16 * NS <= PAIR_MAX, "a half's share of the arrays");
   constexpr unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31, hl = lane & 15;
   const unsigned lt_mask = (1u << hl) - 1;
@@ -350,7 +352,7 @@ __device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, in
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int p = hl + 16 * (k0 + k);
-      const bool v = p + 1 < n;
+      const bool v = k0 + k < NS && p + 1 < n;
       lt[k] = v ? tok[p] : 0;
       rt[k] = v ? tok[p + 1] : 0;
       sl[k] = pair_slot(T, lt[k], rt[k]);
@@ -359,7 +361,7 @@ __device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, in
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int p = hl + 16 * (k0 + k);
-      if (p + 1 < n) {
+      if (k0 + k < NS && p + 1 < n) {
         const int2 pr = pair_finish(T, ent[k], sl[k], lt[k], rt[k]);
         rank[p] = rank_or_max(pr.x);
         res[p] = pr.y;
@@ -442,8 +444,9 @@ __device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, in
   return cnt;
 }
 
-// Two listed pieces of 49 .. PAIR_MAX bytes (pc1 < 0: only one) on one warp:
-// each half probes its piece whole, then the misses merge side by side.
+// Two listed pieces of at most 16 * NS bytes (pc1 < 0: only one) on one
+// warp: each half probes its piece whole, then the misses merge side by side.
+template <int NS>
 __device__ __forceinline__ void mid_pair(const Tables &T, const Work &W, const uint8_t *g, int pc0, int pc1,
                                          int32_t *tok, int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
   const int lane = threadIdx.x & 31, half = lane >> 4;
@@ -463,7 +466,7 @@ __device__ __forceinline__ void mid_pair(const Tables &T, const Work &W, const u
     n = 0;                                    // this half idles
   }
   const int off = half * PAIR_MAX;
-  const int cnt = pair_rounds(T, b, n, W.scratch + s, tok + off, rank + off, res + off, nx + off, pv + off);
+  const int cnt = pair_rounds<NS>(T, b, n, W.scratch + s, tok + off, rank + off, res + off, nx + off, pv + off);
   if ((lane & 15) == 0 && n > 0) W.n_ids[pc] = cnt;
   __syncwarp();
 }
@@ -525,8 +528,8 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
   // workspaces beyond the single-request size the pieces of 49..128 bytes go
   // two to a ticket (pair_rounds)
   constexpr bool pairs = PAIRS;
-  const int tb1 = pairs ? (c1 + 1) / 2 : c1;
-  const int t1 = c0 + tb1, t2 = t1 + (np + SMALL_CHUNK - 1) / SMALL_CHUNK, nwork = t2 + c2;
+  const int tb1 = pairs ? (c1 + 1) / 2 : c1, tb2 = pairs ? (c2 + 1) / 2 : c2;
+  const int t1 = c0 + tb1, t2 = t1 + (np + SMALL_CHUNK - 1) / SMALL_CHUNK, nwork = t2 + tb2;
   const int64_t lcap = list_cap(W.cap_bytes);
   const uint8_t *g = A.utf8 + base;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -535,11 +538,16 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
     if (lane == 0) gi = atomicAdd(&W.counters[9], 1);
     gi = __shfl_sync(0xffffffffu, gi, 0);
     if (gi >= nwork) break;
-    if (PAIRS && gi >= c0 && gi < t1) {
+    if (PAIRS && gi >= c0 && gi < t1) {          // pieces of 49..128 bytes, two a ticket
       const int i = 2 * (gi - c0);
       const int pc1 = i + 1 < c1 ? __ldcg(&W.long_list[lcap + i + 1]) : -1;
-      mid_pair(T, W, g, __ldcg(&W.long_list[lcap + i]), pc1, s_tok[warp], s_rank[warp], s_res[warp],
-               s_nx[warp], s_pv[warp]);
+      mid_pair<PAIR_MAX / 16>(T, W, g, __ldcg(&W.long_list[lcap + i]), pc1, s_tok[warp], s_rank[warp],
+                              s_res[warp], s_nx[warp], s_pv[warp]);
+    } else if (PAIRS && gi >= t2) {              // pieces of 17..48 bytes, two a ticket
+      const int i = 2 * (gi - t2);
+      const int pc1 = i + 1 < c2 ? __ldcg(&W.long_list[2 * lcap + i + 1]) : -1;
+      mid_pair<3>(T, W, g, __ldcg(&W.long_list[2 * lcap + i]), pc1, s_tok[warp], s_rank[warp], s_res[warp],
+                  s_nx[warp], s_pv[warp]);
     } else if (gi < t1 || gi >= t2) {
       const int64_t slot = gi < c0 ? gi : gi < t1 ? lcap + (gi - c0) : 2 * lcap + (gi - t2);
       mid_piece(T, W, g, __ldcg(&W.long_list[slot]), s_tok[warp], s_rank[warp], s_res[warp], s_nx[warp],

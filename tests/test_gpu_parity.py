@@ -154,12 +154,12 @@ def test_piece_lengths_around_unit_thresholds(cuda, vocabs, n):
 
 
 def test_pieces_merged_two_to_a_warp_in_large_batches(cuda, vocabs):
-    """Batches beyond 4 MiB merge the pieces of 49..128 bytes two to a warp:
-    pieces of every length around that range (letters, CJK, punctuation,
-    whole tokens and misses side by side, an odd count) inside 4.3 MB of
-    text."""
+    """Batches beyond 4 MiB merge the pieces of 17..48 and 49..128 bytes two
+    to a warp: pieces of every length around those ranges (letters, CJK,
+    punctuation, whole tokens and misses side by side, an odd count) inside
+    4.3 MB of text."""
     reqs = []
-    for n in range(45, 133):
+    for n in range(15, 133):
         reqs += [" " + "a" * n, "日" * (n // 3 + 1), "(" * n, "ab" * (n // 2) + " x", "é" * (n // 2)]
     reqs.append("q" * 77)
     filler = synth.transcript(77, 3_500_000, synth.PROFILE_MIXED)
