@@ -506,9 +506,11 @@ __device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const 
   __syncwarp();
 }
 
-// PAIRS: the batch instantiation (pieces of 49..128 bytes two to a warp); the
-// single-request one is compiled without that path.
-template <bool PAIRS>
+// PAIRS: which listed pieces go two to a warp: 0 none (a single request,
+// whose longest merge chains set its latency: pairing even the short pieces
+// measured slower there), 1 those of 17..48 bytes, 2 those of 17..48 and of
+// 49..128 bytes (batches).
+template <int PAIRS>
 __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_warp(Tables T, Work W) {
   __shared__ int32_t s_tok[WARP_KERNEL_WARPS][MID_MAX];   // token, -1 once unlinked
   __shared__ int32_t s_rank[WARP_KERNEL_WARPS][MID_MAX];  // rank of (p, next), INT_MAX if none
@@ -527,8 +529,7 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
   // bytes, chunks of short pieces, listed pieces of 17..48 bytes.  In
   // workspaces beyond the single-request size the pieces of 49..128 bytes go
   // two to a ticket (pair_rounds)
-  constexpr bool pairs = PAIRS;
-  const int tb1 = pairs ? (c1 + 1) / 2 : c1, tb2 = pairs ? (c2 + 1) / 2 : c2;
+  const int tb1 = PAIRS >= 2 ? (c1 + 1) / 2 : c1, tb2 = PAIRS >= 1 ? (c2 + 1) / 2 : c2;
   const int t1 = c0 + tb1, t2 = t1 + (np + SMALL_CHUNK - 1) / SMALL_CHUNK, nwork = t2 + tb2;
   const int64_t lcap = list_cap(W.cap_bytes);
   const uint8_t *g = A.utf8 + base;
@@ -538,12 +539,12 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
     if (lane == 0) gi = atomicAdd(&W.counters[9], 1);
     gi = __shfl_sync(0xffffffffu, gi, 0);
     if (gi >= nwork) break;
-    if (PAIRS && gi >= c0 && gi < t1) {          // pieces of 49..128 bytes, two a ticket
+    if (PAIRS >= 2 && gi >= c0 && gi < t1) {     // pieces of 49..128 bytes, two a ticket
       const int i = 2 * (gi - c0);
       const int pc1 = i + 1 < c1 ? __ldcg(&W.long_list[lcap + i + 1]) : -1;
       mid_pair<PAIR_MAX / 16>(T, W, g, __ldcg(&W.long_list[lcap + i]), pc1, s_tok[warp], s_rank[warp],
                               s_res[warp], s_nx[warp], s_pv[warp]);
-    } else if (PAIRS && gi >= t2) {              // pieces of 17..48 bytes, two a ticket
+    } else if (PAIRS >= 1 && gi >= t2) {         // pieces of 17..48 bytes, two a ticket
       const int i = 2 * (gi - t2);
       const int pc1 = i + 1 < c2 ? __ldcg(&W.long_list[2 * lcap + i + 1]) : -1;
       mid_pair<3>(T, W, g, __ldcg(&W.long_list[2 * lcap + i]), pc1, s_tok[warp], s_rank[warp], s_res[warp],
@@ -1061,8 +1062,8 @@ __global__ void k_hook_offsets(Work W) {
 }
 
 void launch_bpe_warp(const Tables &T, const Work &W, int grid, cudaStream_t s) {
-  if (W.cap_bytes > PAIR_MIN_CAP_BYTES) k_bpe_warp<true><<<grid, BPE_WARP_THREADS, 0, s>>>(T, W);
-  else k_bpe_warp<false><<<grid, BPE_WARP_THREADS, 0, s>>>(T, W);
+  if (W.cap_bytes > PAIR_MIN_CAP_BYTES) k_bpe_warp<2><<<grid, BPE_WARP_THREADS, 0, s>>>(T, W);
+  else k_bpe_warp<0><<<grid, BPE_WARP_THREADS, 0, s>>>(T, W);
 }
 void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   k_bpe_long<<<grid, BPE_LONG_THREADS, LONG_SMEM_BYTES, s>>>(T, W);
