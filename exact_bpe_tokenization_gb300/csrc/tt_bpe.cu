@@ -147,6 +147,7 @@ constexpr int WARP_KERNEL_WARPS = BPE_WARP_THREADS / 32;
 // workspaces above this size (batches; the single request stays below) pair
 // the pieces of 49..128 bytes
 constexpr int64_t PAIR_MIN_CAP_BYTES = 4ll << 20;
+constexpr int GROUP2 = 4;   // pieces of 17..48 bytes a warp when grouped (8 lanes x 6 positions each)
 constexpr int SMALL_CHUNK = 32;   // pieces per small-piece ticket
 
 __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, const uint8_t *g, int64_t total,
@@ -318,26 +319,27 @@ __device__ __forceinline__ int list_rounds(const Tables &T, const uint8_t *b, in
   return cnt;
 }
 
-// Two pieces of at most PAIR_MAX bytes side by side, 16 lanes each (half h
-// of the warp takes piece h; lane l of a half owns positions l, l + 16, ...),
-// each half on its own 128-entry share of the warp's arrays.  Rounds run in
-// lockstep: each half takes its own lowest rank (an xor butterfly over its 16
-// lanes) and merges as list_rounds does; a half with nothing left idles until
-// the other is done.  Each half passes its own piece (n = 0: none) and gets
-// its IDs' count.  For batches, where warps are the scarce resource: a round's
-// instructions serve two pieces.
-// NS: positions per lane (pieces of at most 16 * NS bytes).
+// 32 / G pieces side by side, G lanes each (group q of the warp takes piece
+// q; lane l of a group owns positions l, l + G, ...), each group on its own
+// share of the warp's arrays.  Rounds run in lockstep: each group takes its
+// own lowest rank (an xor butterfly over its lanes) and merges as list_rounds
+// does; a group with nothing left idles until the others are done.  Each
+// group passes its own piece (n = 0: none) and gets its IDs' count.  For
+// batches, where warps are the scarce resource: a round's instructions serve
+// several pieces.
+// NS: positions per lane (pieces of at most G * NS bytes).
 constexpr int PAIR_MAX = MID_MAX / 2;
-template <int NS>
-__device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, int n, int32_t *out, int32_t *tok,
-                                           int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
-  static_assert(16 * NS <= PAIR_MAX, "a half's share of the arrays");
+template <int G, int NS>
+__device__ __forceinline__ int group_rounds(const Tables &T, const uint8_t *b, int n, int32_t *out, int32_t *tok,
+                                            int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
+  static_assert(G * NS <= MID_MAX * G / 32, "a group's share of the arrays");
   constexpr unsigned FULL = 0xffffffffu;
-  const int lane = threadIdx.x & 31, hl = lane & 15;
+  constexpr int SHARE = MID_MAX * G / 32;
+  const int lane = threadIdx.x & 31, hl = lane % G;
   const unsigned lt_mask = (1u << hl) - 1;
 #pragma unroll
   for (int k = 0; k < NS; ++k) {
-    const int p = hl + 16 * k;
+    const int p = hl + G * k;
     tok[p] = p < n ? __ldg(&T.byte_id[__ldg(b + p)]) : -1;
     rank[p] = INT_MAX;
     nx[p] = (int16_t)(p + 1);
@@ -351,7 +353,7 @@ __device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, in
     int lt[4], rt[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int p = hl + 16 * (k0 + k);
+      const int p = hl + G * (k0 + k);
       const bool v = k0 + k < NS && p + 1 < n;
       lt[k] = v ? tok[p] : 0;
       rt[k] = v ? tok[p + 1] : 0;
@@ -360,7 +362,7 @@ __device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, in
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int p = hl + 16 * (k0 + k);
+      const int p = hl + G * (k0 + k);
       if (k0 + k < NS && p + 1 < n) {
         const int2 pr = pair_finish(T, ent[k], sl[k], lt[k], rt[k]);
         rank[p] = rank_or_max(pr.x);
@@ -369,35 +371,35 @@ __device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, in
     }
   }
   __syncwarp();
-  for (int round = 0; round < PAIR_MAX; ++round) {   // a half with pairs unlinks at least one symbol a round
+  for (int round = 0; round < SHARE; ++round) {      // a group with pairs unlinks at least one symbol a round
     int rr[NS];
     int r = INT_MAX;
 #pragma unroll
     for (int k = 0; k < NS; ++k) {
-      rr[k] = rank[hl + 16 * k];
+      rr[k] = rank[hl + G * k];
       r = min(r, rr[k]);
     }
 #pragma unroll
-    for (int d = 8; d >= 1; d >>= 1) r = min(r, __shfl_xor_sync(FULL, r, d));   // my half's lowest rank
+    for (int d = G / 2; d >= 1; d >>= 1) r = min(r, __shfl_xor_sync(FULL, r, d));   // my group's lowest rank
     if (__all_sync(FULL, r == INT_MAX)) break;
-    for (int step = 0; step < PAIR_MAX; ++step) {   // (a bound the same on every lane: the loop holds warp votes)
+    for (int step = 0; step < SHARE; ++step) {      // (a bound the same on every lane: the loop holds warp votes)
       if (step > 0) {
 #pragma unroll
-        for (int k = 0; k < NS; ++k) rr[k] = rank[hl + 16 * k];
+        for (int k = 0; k < NS; ++k) rr[k] = rank[hl + G * k];
       }
       uint32_t sel = 0;
       bool left = false;
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
         if (r != INT_MAX && rr[k] == r) {
-          const int q = pv[hl + 16 * k];
+          const int q = pv[hl + G * k];
           if (q < 0 || rank[q] != r) sel |= 1u << k;
           else left = true;
         }
       }
       __syncwarp();
       for (uint32_t m = sel; m; m &= m - 1) {
-        const int p = hl + 16 * (__ffs(m) - 1);
+        const int p = hl + G * (__ffs(m) - 1);
         const int q = nx[p], nq = nx[q];
         tok[p] = res[p];
         tok[q] = -1;
@@ -408,7 +410,7 @@ __device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, in
       }
       __syncwarp();
       for (uint32_t m = sel; m; m &= m - 1) {
-        const int p = hl + 16 * (__ffs(m) - 1);
+        const int p = hl + G * (__ffs(m) - 1);
         const int a = pv[p], c = nx[p];
         const int tp = tok[p];
         const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
@@ -430,13 +432,13 @@ __device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, in
       if (!__any_sync(FULL, left)) break;
     }
   }
-  // surviving tokens of my half in position order
+  // surviving tokens of my group in position order
   int cnt = 0;
-  const int sh = lane & 16;
+  const int sh = lane - hl;
 #pragma unroll
   for (int k = 0; k < NS; ++k) {
-    const int t = tok[hl + 16 * k];
-    const unsigned bal = (__ballot_sync(FULL, t >= 0) >> sh) & 0xFFFFu;
+    const int t = tok[hl + G * k];
+    const unsigned bal = (__ballot_sync(FULL, t >= 0) >> sh) & (G == 32 ? FULL : (1u << G) - 1);
     if (t >= 0) out[cnt + __popc(bal & lt_mask)] = t;
     cnt += __popc(bal);
   }
@@ -444,13 +446,15 @@ __device__ __forceinline__ int pair_rounds(const Tables &T, const uint8_t *b, in
   return cnt;
 }
 
-// Two listed pieces of at most 16 * NS bytes (pc1 < 0: only one) on one
-// warp: each half probes its piece whole, then the misses merge side by side.
-template <int NS>
-__device__ __forceinline__ void mid_pair(const Tables &T, const Work &W, const uint8_t *g, int pc0, int pc1,
-                                         int32_t *tok, int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
-  const int lane = threadIdx.x & 31, half = lane >> 4;
-  const int pc = half ? pc1 : pc0;
+// 32 / G listed pieces of at most G * NS bytes on one warp -- entries
+// first .. first + 32 / G - 1 of a list of n_list pieces (past n_list: none): each
+// group probes its piece whole, then the misses merge side by side.
+template <int G, int NS>
+__device__ __forceinline__ void mid_group(const Tables &T, const Work &W, const uint8_t *g, const int32_t *list,
+                                          int first, int n_list, int32_t *tok, int32_t *rank, int32_t *res,
+                                          int16_t *nx, int16_t *pv) {
+  const int lane = threadIdx.x & 31, grp = lane / G, gl = lane % G;
+  const int pc = first + grp < n_list ? __ldcg(&list[first + grp]) : -1;
   int32_t s = 0;
   int n = 0;
   if (pc >= 0) {
@@ -459,15 +463,15 @@ __device__ __forceinline__ void mid_pair(const Tables &T, const Work &W, const u
   }
   const uint8_t *b = g + s;
   int id = -1;
-  if ((lane & 15) == 0 && n > 0 && n <= T.max_tok_len) id = vocab_probe(T, b, n);
-  id = __shfl_sync(0xffffffffu, id, lane & 16);
+  if (gl == 0 && n > 0 && n <= T.max_tok_len) id = vocab_probe(T, b, n);
+  id = __shfl_sync(0xffffffffu, id, lane - gl);
   if (id >= 0) {
-    if ((lane & 15) == 0) { W.scratch[s] = id; W.n_ids[pc] = 1; }
-    n = 0;                                    // this half idles
+    if (gl == 0) { W.scratch[s] = id; W.n_ids[pc] = 1; }
+    n = 0;                                    // this group idles
   }
-  const int off = half * PAIR_MAX;
-  const int cnt = pair_rounds<NS>(T, b, n, W.scratch + s, tok + off, rank + off, res + off, nx + off, pv + off);
-  if ((lane & 15) == 0 && n > 0) W.n_ids[pc] = cnt;
+  const int off = grp * (MID_MAX * G / 32);
+  const int cnt = group_rounds<G, NS>(T, b, n, W.scratch + s, tok + off, rank + off, res + off, nx + off, pv + off);
+  if (gl == 0 && n > 0) W.n_ids[pc] = cnt;
   __syncwarp();
 }
 
@@ -529,7 +533,8 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
   // bytes, chunks of short pieces, listed pieces of 17..48 bytes.  In
   // workspaces beyond the single-request size the pieces of 49..128 bytes go
   // two to a ticket (pair_rounds)
-  const int tb1 = PAIRS >= 2 ? (c1 + 1) / 2 : c1, tb2 = PAIRS >= 1 ? (c2 + 1) / 2 : c2;
+  // (GROUP2 pieces of 17..48 bytes a ticket when paired)
+  const int tb1 = PAIRS >= 2 ? (c1 + 1) / 2 : c1, tb2 = PAIRS >= 1 ? (c2 + GROUP2 - 1) / GROUP2 : c2;
   const int t1 = c0 + tb1, t2 = t1 + (np + SMALL_CHUNK - 1) / SMALL_CHUNK, nwork = t2 + tb2;
   const int64_t lcap = list_cap(W.cap_bytes);
   const uint8_t *g = A.utf8 + base;
@@ -540,15 +545,12 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
     gi = __shfl_sync(0xffffffffu, gi, 0);
     if (gi >= nwork) break;
     if (PAIRS >= 2 && gi >= c0 && gi < t1) {     // pieces of 49..128 bytes, two a ticket
-      const int i = 2 * (gi - c0);
-      const int pc1 = i + 1 < c1 ? __ldcg(&W.long_list[lcap + i + 1]) : -1;
-      mid_pair<PAIR_MAX / 16>(T, W, g, __ldcg(&W.long_list[lcap + i]), pc1, s_tok[warp], s_rank[warp],
-                              s_res[warp], s_nx[warp], s_pv[warp]);
-    } else if (PAIRS >= 1 && gi >= t2) {         // pieces of 17..48 bytes, two a ticket
-      const int i = 2 * (gi - t2);
-      const int pc1 = i + 1 < c2 ? __ldcg(&W.long_list[2 * lcap + i + 1]) : -1;
-      mid_pair<3>(T, W, g, __ldcg(&W.long_list[2 * lcap + i]), pc1, s_tok[warp], s_rank[warp], s_res[warp],
-                  s_nx[warp], s_pv[warp]);
+      mid_group<16, PAIR_MAX / 16>(T, W, g, W.long_list + lcap, 2 * (gi - c0), c1, s_tok[warp], s_rank[warp],
+                                   s_res[warp], s_nx[warp], s_pv[warp]);
+    } else if (PAIRS >= 1 && gi >= t2) {         // pieces of 17..48 bytes, GROUP2 a ticket
+      mid_group<32 / GROUP2, (48 * GROUP2 + 31) / 32>(T, W, g, W.long_list + 2 * lcap, GROUP2 * (gi - t2), c2,
+                                                      s_tok[warp], s_rank[warp], s_res[warp], s_nx[warp],
+                                                      s_pv[warp]);
     } else if (gi < t1 || gi >= t2) {
       const int64_t slot = gi < c0 ? gi : gi < t1 ? lcap + (gi - c0) : 2 * lcap + (gi - t2);
       mid_piece(T, W, g, __ldcg(&W.long_list[slot]), s_tok[warp], s_rank[warp], s_res[warp], s_nx[warp],
