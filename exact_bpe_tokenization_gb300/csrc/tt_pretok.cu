@@ -65,7 +65,7 @@ struct WinSmem {
 
 // The prepass's view of a window: bytes, request starts and the ASCII classes.
 struct ByteWin {
-  uint8_t bytes[WIN + 8];
+  alignas(16) uint8_t bytes[WIN + 8];
   uint8_t rsb[WIN + 8];
   uint8_t ascii[128];
   int r0, r1;
@@ -207,23 +207,37 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
   // bytes and request starts suffice: the few chars the summaries look at
   // are decoded where they are met
   load_bytes<NT>(T, A, base, total, ws, S, A.utf8_src);
+  // this thread's bytes as words, and which of them lie in the tile
+  uint32_t wd[PT_BYTES / 4];
+#pragma unroll
+  for (int q = 0; q < PT_BYTES / 4; ++q) wd[q] = reinterpret_cast<const uint32_t *>(&S.bytes[PT_BYTES * tid])[q];
+  const int64_t x0 = ws + PT_BYTES * tid;
+  const bool whole = x0 >= ts && x0 + PT_BYTES <= te;
+  uint32_t in_tile = whole ? (1u << PT_BYTES) - 1 : 0;
+  if (!whole)
+    for (int k = 0; k < PT_BYTES; ++k) in_tile |= (uint32_t)(x0 + k >= ts && x0 + k < te) << k;
   if (A.utf8_src) {                           // the later kernels read the device copy of the tile
-    uint8_t *dst = const_cast<uint8_t *>(A.utf8) + base;
-    for (int k = 0; k < PT_BYTES; ++k) {
-      const int64_t x = ws + PT_BYTES * tid + k;
-      if (x >= ts && x < te) dst[x] = S.bytes[PT_BYTES * tid + k];
+    uint8_t *dst = const_cast<uint8_t *>(A.utf8) + base + x0;
+    if (whole && (reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
+#pragma unroll
+      for (int q = 0; q < PT_BYTES / 4; ++q) reinterpret_cast<uint32_t *>(dst)[q] = wd[q];
+    } else {
+      for (int k = 0; k < PT_BYTES; ++k)
+        if ((in_tile >> k) & 1) dst[k] = S.bytes[PT_BYTES * tid + k];
     }
   }
 
-  // --- UTF-8 validation of the tile's bytes (RFC 3629, per request)
-  for (int k = 0; k < PT_BYTES; ++k) {
-    const int i = PT_BYTES * tid + k;
+  // --- UTF-8 validation of the tile's bytes (RFC 3629, per request).  ASCII
+  // bytes are always valid, so only the others are visited.
+  uint32_t hi = 0;
+#pragma unroll
+  for (int q = 0; q < PT_BYTES / 4; ++q) hi |= top_bits4(wd[q]) << (4 * q);
+  for (uint32_t m = hi & in_tile; m; m &= m - 1) {
+    const int i = PT_BYTES * tid + __ffs(m) - 1;
     const int64_t x = ws + i;
-    if (x < ts || x >= te) continue;
     const uint8_t b = S.bytes[i];
     bool bad = false;
-    if (b < 0x80) {
-    } else if (b < 0xC0) {                    // continuation: claimed by a lead <= 3 bytes back?
+    if (b < 0xC0) {                    // continuation: claimed by a lead <= 3 bytes back?
       bad = true;
       if (!S.rsb[i]) {
         for (int d = 1; d <= 3; ++d) {

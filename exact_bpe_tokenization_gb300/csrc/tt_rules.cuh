@@ -338,6 +338,11 @@ TT_HD bool ds_segment_start(uint8_t raw_prev, uint8_t raw_j) {
 // deepseek-style: a digit or kana/CJK char met by a blank run's lookahead
 // starts a segment (the blank run's piece ends with its segment), so it reads
 // as the end; elsewhere those chars are never the first event a blank sees.
+// Bit k (k < 4) = the top bit of byte k of w (little-endian): the four top
+// bits, shifted down to bits 0, 8, 16, 24, are gathered by one multiply whose
+// partial products (at 0/7/14/21 + 8k) never overlap, so nothing carries.
+TT_HD uint32_t top_bits4(uint32_t w) { return (((w & 0x80808080u) >> 7) * 0x204081u) >> 21 & 0xFu; }
+
 TT_HD uint8_t rq_ws_event(int fam, bool rs_j, uint8_t raw_j, uint32_t cp_j) {  // 0xFF = not an event
   if (rs_j) return R_END;
   if (fam == FAM_DEEPSEEK && ds_segment_class(raw_j) != 0) return R_END;

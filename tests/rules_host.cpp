@@ -83,3 +83,6 @@ extern "C" void rules_host_starts(int fam, const uint32_t *cp, const uint8_t *ra
     start[j] = piece_start(fam, b, a) ? 1 : 0;
   }
 }
+
+// The kernels' gather of the top bit of each byte of a word.
+extern "C" uint32_t rules_host_top_bits4(uint32_t w) { return top_bits4(w); }

@@ -154,10 +154,10 @@ def test_piece_lengths_around_unit_thresholds(cuda, vocabs, n):
 
 
 def test_pieces_merged_two_to_a_warp_in_large_batches(cuda, vocabs):
-    """Batches beyond 4 MiB merge the pieces of 17..48 and 49..128 bytes two
-    to a warp: pieces of every length around those ranges (letters, CJK,
-    punctuation, whole tokens and misses side by side, an odd count) inside
-    4.3 MB of text."""
+    """Batches beyond 4 MiB merge the pieces of 49..128 bytes two to a warp
+    and those of 17..48 bytes four to a warp: pieces of every length around
+    those ranges (letters, CJK, punctuation, whole tokens and misses side by
+    side, counts that leave a group part-filled) inside 4.3 MB of text."""
     reqs = []
     for n in range(15, 133):
         reqs += [" " + "a" * n, "日" * (n // 3 + 1), "(" * n, "ab" * (n // 2) + " x", "é" * (n // 2)]
@@ -197,6 +197,29 @@ def test_invalid_utf8_requests_yield_no_ids(cuda, vocabs):
         assert io[r + 1] == io[r]
     # a multi-byte char split across two requests is invalid on both sides
     check(cuda, vocabs["small1"], 1, ["ab\xc3".encode("latin-1"), b"\xa9cd", b"fine"])
+
+
+@pytest.mark.parametrize("large", [False, True])
+def test_utf8_sequences_straddling_tile_edges(cuda, vocabs, large):
+    """Valid and invalid multi-byte sequences at every position across a
+    4016-byte tile edge: each request is two tiles long and starts on a tile
+    edge, so its sequence sits at the edge in its middle.  large: behind a
+    filler that takes the batch past 4 MiB (the 16-bytes-a-thread kernels)."""
+    tile = 4016
+    seqs = ["é".encode(), "日".encode(), "\U0001F642".encode(), b"\xff", b"\xc3(", b"\x80", b"\xe4\xb8",
+            b"\xe0\x80\x80", b"\xed\xa0\x80", b"\xf4\x90\x80\x80", b"\xf0\x9f\x98"]
+    reqs = []
+    if large:                                  # its length is a whole number of tiles too
+        text, n = synth.transcript(78, 3_600_000, synth.PROFILE_MIXED), 1080 * tile
+        cut = n
+        while text[cut] & 0xC0 == 0x80:        # end on a char boundary
+            cut -= 1
+        reqs.append(text[:cut].ljust(n, b" "))
+    for seq in seqs:
+        for d in range(-5, 6):
+            head = b"ab " * ((tile + d) // 3) + b"x" * ((tile + d) % 3)
+            reqs.append((head + seq).ljust(2 * tile, b"z"))
+    check(cuda, vocabs["c1"], 1, reqs)
 
 
 def test_offsets_with_nonzero_base(cuda, vocabs):

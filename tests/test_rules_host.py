@@ -27,7 +27,22 @@ def rules_lib(tmp_path_factory):
                            os.path.join(HERE, "rules_host.cpp")])
     lib = ctypes.CDLL(so)
     lib.rules_host_starts.argtypes = [ctypes.c_int] + [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_void_p]
+    lib.rules_host_top_bits4.argtypes = [ctypes.c_uint32]
+    lib.rules_host_top_bits4.restype = ctypes.c_uint32
     return lib
+
+
+def test_top_bit_gather_matches_the_bytes(rules_lib):
+    # the UTF-8 check visits only bytes with the top bit set; the gather that
+    # finds them must give bit k = top bit of byte k for every pattern of top
+    # bits under any low bits
+    rng = random.Random(5)
+    words = [rng.getrandbits(32) for _ in range(20000)]
+    words += [sum(((p >> k & 1) << (8 * k + 7)) | (low << (8 * k)) for k in range(4))
+              for p in range(16) for low in (0x00, 0x7F, 0x55)]
+    for w in words:
+        want = sum(((w >> (8 * k + 7)) & 1) << k for k in range(4))
+        assert rules_lib.rules_host_top_bits4(w) == want, hex(w)
 
 
 K_HAN_FLAG = 0x10
