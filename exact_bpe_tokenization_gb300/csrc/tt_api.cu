@@ -31,9 +31,9 @@ using namespace tt;
 
 namespace {
 
-constexpr int N_KERNELS = 8;
+constexpr int N_KERNELS = 9;
 const char *KERNEL_NAMES[N_KERNELS] = {"k_lit_find", "k_lit_pick", "k_prepass", "k_tilescan", "k_pretok",
-                                       "k_bpe_warp", "k_bpe_long", "k_ids"};
+                                       "k_bpe_warp", "k_bpe_long", "k_idscan", "k_ids"};
 
 struct Workspace {
   Work W{};
@@ -88,7 +88,7 @@ struct tt_tokenizer {
 
 // kernels of one encode: six, and the two literal kernels when the handle
 // has added-token literals
-static int launches_per_encode(const tt_tokenizer *h) { return 6 + (h->T.n_lit ? 2 : 0); }
+static int launches_per_encode(const tt_tokenizer *h) { return 7 + (h->T.n_lit ? 2 : 0); }
 
 #define TT_CUDA(call)                                                   \
   do {                                                                  \
@@ -426,7 +426,7 @@ static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_
       {(void **)&W.s2_flag, 4 * (size_t)tiles},         {(void **)&W.cnt_agg, sizeof(int2) * tiles},
       {(void **)&W.cnt_inc, sizeof(int2) * tiles},      {(void **)&W.cnt_flag, 4 * (size_t)tiles},
       {(void **)&W.ids_agg, 4 * (size_t)chunks},        {(void **)&W.ids_inc, 4 * (size_t)chunks},
-      {(void **)&W.ids_flag, 4 * (size_t)chunks},       {(void **)&W.counters, 4 * 16},
+      {(void **)&W.counters, 4 * 16},
       {(void **)&W.piece_start, 4 * (size_t)(cap_bytes + 2)}, {(void **)&W.n_ids, 4 * (size_t)(cap_bytes + 1)},
       {(void **)&W.scratch, 4 * (size_t)(cap_bytes + 1)},
       {(void **)&W.tmp_a, 4 * (size_t)(cap_bytes + 1)},       {(void **)&W.tmp_b, 4 * (size_t)(cap_bytes + 1)},
@@ -550,6 +550,7 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
     TT_CUDA(cudaEventRecord(w->ev_join, w->side));
     launch_bpe_warp(T, W, grid_warp(w), stream);
     TT_CUDA(cudaStreamWaitEvent(stream, w->ev_join, 0));
+    launch_idscan(W, stream);
     launch_ids(T, W, grid_chunks(w), stream);
     TT_CUDA(cudaGetLastError());
     h->launches += launches_per_encode(h);
@@ -566,7 +567,8 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
       case 4: launch_pretok(T, W, grid_tiles(w), stream); break;
       case 5: launch_bpe_warp(T, W, grid_warp(w), stream); break;
       case 6: launch_bpe_long(T, W, grid_long(w), stream); break;
-      case 7: launch_ids(T, W, grid_chunks(w), stream); break;
+      case 7: launch_idscan(W, stream); break;
+      case 8: launch_ids(T, W, grid_chunks(w), stream); break;
     }
     cudaEventRecord(b, stream);
     h->pending.push_back({kidx, a, b});
@@ -884,7 +886,7 @@ constexpr size_t NA_SIZES[] = {
     2 * (size_t)NA_TILES, 2 * (size_t)NA_TILES,                        // rq_sum, rq_carry
     sizeof(S2) * NA_TILES, sizeof(S2) * NA_TILES, 4 * (size_t)NA_TILES, // s2_agg, s2_inc, s2_flag
     sizeof(int2) * NA_TILES, sizeof(int2) * NA_TILES, 4 * (size_t)NA_TILES,  // cnt_agg, cnt_inc, cnt_flag
-    4 * (size_t)NA_CHUNKS, 4 * (size_t)NA_CHUNKS, 4 * (size_t)NA_CHUNKS, // ids_agg, ids_inc, ids_flag
+    4 * (size_t)NA_CHUNKS, 4 * (size_t)NA_CHUNKS,                      // ids_agg, ids_inc
     4 * 16,                                                            // counters
     4 * (size_t)(NA_BYTES + 2), 4 * (size_t)(NA_BYTES + 1),            // piece_start, n_ids
     4 * (size_t)(NA_BYTES + 1),                                        // scratch
@@ -957,7 +959,7 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   void **dst[] = {(void **)&W.s1_sum,  (void **)&W.s1_carry, (void **)&W.rq_sum,   (void **)&W.rq_carry,
                   (void **)&W.s2_agg,  (void **)&W.s2_inc,   (void **)&W.s2_flag,  (void **)&W.cnt_agg,
                   (void **)&W.cnt_inc, (void **)&W.cnt_flag, (void **)&W.ids_agg,  (void **)&W.ids_inc,
-                  (void **)&W.ids_flag, (void **)&W.counters, (void **)&W.piece_start, (void **)&W.n_ids,
+                  (void **)&W.counters, (void **)&W.piece_start, (void **)&W.n_ids,
                   (void **)&W.scratch,  (void **)&W.tmp_a,    (void **)&W.tmp_b,
                   (void **)&W.tmp_c,   (void **)&W.long_list, (void **)&W.huge_list, (void **)&W.bad,
                   (void **)&W.bad_pre, (void **)&W.req_piece, (void **)&W.lit_cand, (void **)&W.lit_cnt,
@@ -994,6 +996,7 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   launch_pretok(T, W, g_tiles, stream);
   launch_bpe_warp(T, W, g_warp, stream);
   launch_bpe_long(T, W, g_long, stream);
+  launch_idscan(W, stream);
   launch_ids(T, W, g_chunks, stream);
   TT_CUDA(cudaGetLastError());
   h->launches += launches_per_encode(h);

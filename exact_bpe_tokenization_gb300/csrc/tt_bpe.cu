@@ -15,9 +15,10 @@
 // registers), a warp per piece up to 256 bytes (registers up to 32 bytes,
 // else a linked list in shared memory), a 512-thread block per longer piece
 // (a linked list in shared memory up to 8 KiB, else global ping-pong
-// buffers).  IDs land in a byte-indexed scratch array; k_ids scans the
-// per-piece counts with decoupled look-back, writes the final contiguous IDs
-// and each request's ID offset.
+// buffers).  IDs land in a byte-indexed scratch array, and each piece's ID
+// count is also added into its 512-piece chunk's total; k_idscan (one CTA)
+// scans the chunk totals, and k_ids scans each chunk's counts on its own,
+// writes the final contiguous IDs and each request's ID offset.
 #include <limits.h>
 
 #include "tt_common.cuh"
@@ -148,7 +149,15 @@ constexpr int WARP_KERNEL_WARPS = BPE_WARP_THREADS / 32;
 // the pieces of 49..128 bytes
 constexpr int64_t PAIR_MIN_CAP_BYTES = 4ll << 20;
 constexpr int GROUP2 = 4;   // pieces of 17..48 bytes a warp when grouped (8 lanes x 6 positions each)
-constexpr int SMALL_CHUNK = 32;   // pieces per small-piece ticket
+constexpr int SMALL_CHUNK = 32;   // pieces per small-piece ticket (IDS_CHUNK is a multiple)
+static_assert(IDS_CHUNK % SMALL_CHUNK == 0, "a small-piece ticket lies in one ID chunk");
+
+// A piece's ID count, also added into the total of its ID chunk (IDS_CHUNK
+// pieces), which the ID scatter's chunk scan reads.
+__device__ __forceinline__ void put_count(const Work &W, int k, int c) {
+  W.n_ids[k] = c;
+  if (c) atomicAdd(&W.ids_agg[k / IDS_CHUNK], c);
+}
 
 __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, const uint8_t *g, int64_t total,
                                             int np, int kb) {
@@ -157,6 +166,7 @@ __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, cons
   int32_t s = 0;
   int len = 0;
   bool miss = false;
+  int mine = 0;                                 // IDs this lane wrote counts for
   if (k < np) {
     s = __ldcg(&W.piece_start[k]);
     if (s < 0) {
@@ -172,6 +182,7 @@ __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, cons
         if (id >= 0) {
           W.scratch[s] = id;
           W.n_ids[k] = 1;
+          mine = 1;
         } else {
           miss = true;
         }
@@ -199,8 +210,12 @@ __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, cons
     int pl = __shfl_sync(0xffffffffu, len, src < 0 ? la : src);
     if (src < 0) pl = 0;
     const int cnt = bpe_lanes<16>(T, g + ps, pl, W.scratch + ps);
-    if ((lane & 15) == 0 && src >= 0) W.n_ids[kb + src] = cnt;
+    if ((lane & 15) == 0 && src >= 0) { W.n_ids[kb + src] = cnt; mine += cnt; }
   }
+  // the chunk's pieces of at most SMALL_MAX bytes, all in one ID chunk
+#pragma unroll
+  for (int d = 16; d; d >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, d);
+  if (lane == 0 && mine) atomicAdd(&W.ids_agg[kb / IDS_CHUNK], mine);
 }
 
 // The linked-list rounds of one piece of n bytes (32 < n <= 32 * NS) in the
@@ -466,12 +481,12 @@ __device__ __forceinline__ void mid_group(const Tables &T, const Work &W, const 
   if (gl == 0 && n > 0 && n <= T.max_tok_len) id = vocab_probe(T, b, n);
   id = __shfl_sync(0xffffffffu, id, lane - gl);
   if (id >= 0) {
-    if (gl == 0) { W.scratch[s] = id; W.n_ids[pc] = 1; }
+    if (gl == 0) { W.scratch[s] = id; put_count(W, pc, 1); }
     n = 0;                                    // this group idles
   }
   const int off = grp * (MID_MAX * G / 32);
   const int cnt = group_rounds<G, NS>(T, b, n, W.scratch + s, tok + off, rank + off, res + off, nx + off, pv + off);
-  if (gl == 0 && n > 0) W.n_ids[pc] = cnt;
+  if (gl == 0 && n > 0) put_count(W, pc, cnt);
   __syncwarp();
 }
 
@@ -487,13 +502,13 @@ __device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const 
     if (lane == 0) id = vocab_probe(T, b, n);
     id = __shfl_sync(0xffffffffu, id, 0);
     if (id >= 0) {
-      if (lane == 0) { W.scratch[s] = id; W.n_ids[pc] = 1; }
+      if (lane == 0) { W.scratch[s] = id; put_count(W, pc, 1); }
       return;
     }
   }
   if (n <= 32) {                              // one symbol per lane, state in registers
     const int cnt = bpe_lanes<32>(T, b, n, W.scratch + s);
-    if (lane == 0) W.n_ids[pc] = cnt;
+    if (lane == 0) put_count(W, pc, cnt);
     return;
   }
   int cnt;
@@ -506,7 +521,7 @@ __device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const 
     case 7: cnt = list_rounds<7>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
     default: cnt = list_rounds<8>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
   }
-  if (lane == 0) W.n_ids[pc] = cnt;
+  if (lane == 0) put_count(W, pc, cnt);
   __syncwarp();
 }
 
@@ -584,7 +599,7 @@ constexpr int LONG_SMEM_MAX = 8192;
 constexpr size_t LONG_SMEM_BYTES = (size_t)LONG_SMEM_MAX * (4 + 4 + 4 + 2 + 2);
 static_assert(LONG_SMEM_MAX / BPE_LONG_THREADS <= 32, "slot mask is 32 bits");
 
-__device__ void bpe_block_list(const Tables &T, const uint8_t *b, int n, int32_t *out, int *n_out,
+__device__ void bpe_block_list(const Tables &T, const Work &W, const uint8_t *b, int n, int32_t *out, int piece,
                                unsigned char *dsm, int *red) {
   constexpr int NT = BPE_LONG_THREADS;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -689,7 +704,7 @@ __device__ void bpe_block_list(const Tables &T, const uint8_t *b, int n, int32_t
   int w = block_exclusive_scan<NT>(cnt, [](int x, int y) { return x + y; }, 0, red, &tot);
   for (int p = lo; p < hi; ++p)
     if (tok[p] >= 0) out[w++] = tok[p];
-  if (tid == 0) *n_out = tot;
+  if (tid == 0) put_count(W, piece, tot);
   __syncthreads();
 }
 
@@ -723,12 +738,12 @@ __global__ void __launch_bounds__(BPE_LONG_THREADS, 1) k_bpe_long(Tables T, Work
       const int whole = s_whole;
       __syncthreads();
       if (whole >= 0) {
-        if (tid == 0) { W.scratch[s] = whole; W.n_ids[k] = 1; }
+        if (tid == 0) { W.scratch[s] = whole; put_count(W, k, 1); }
         continue;
       }
     }
     if (len <= LONG_SMEM_MAX) {
-      bpe_block_list(T, b, len, W.scratch + s, &W.n_ids[k], dsm, red);
+      bpe_block_list(T, W, b, len, W.scratch + s, k, dsm, red);
       continue;
     }
     int32_t *cur = W.scratch + s, *nxt = W.tmp_b + s;
@@ -812,7 +827,7 @@ __global__ void __launch_bounds__(BPE_LONG_THREADS, 1) k_bpe_long(Tables T, Work
     if (cur != W.scratch + s) {
       for (int i = tid; i < n; i += NT) W.scratch[s + i] = cur[i];
     }
-    if (tid == 0) W.n_ids[k] = n;
+    if (tid == 0) put_count(W, k, n);
     __syncthreads();
   }
 }
@@ -850,13 +865,42 @@ __device__ int64_t first_request_from(const CallArgs &A, const Work &W, int64_t 
   return lo;
 }
 
+// Exclusive scan of the ID chunks' totals (summed by the BPE kernels as they
+// write each piece's count) into each chunk's first output, and the batch's
+// ID count.  One CTA: each thread sums a contiguous run of chunks (loads in
+// flight together), one block scan, then the run's prefixes.
+__global__ void __launch_bounds__(1024) k_idscan(Work W) {
+  __shared__ int red[32];
+  const CallArgs A = *W.args;
+  const int tid = threadIdx.x;
+  int np = 0;
+  if (A.n > 0) {
+    const int64_t base = __ldg(&A.offs[0]);
+    const int64_t total = __ldg(&A.offs[A.n]) - base;
+    if (!(total > W.cap_bytes || total < 0 || base < 0)) np = __ldcg(&W.counters[3]);
+  }
+  const int nchunks = (np + IDS_CHUNK - 1) / IDS_CHUNK;
+  const int per = (nchunks + 1023) / 1024;
+  const int lo = min(tid * per, nchunks), hi = min(lo + per, nchunks);
+  int sum = 0;
+#pragma unroll 8
+  for (int c = lo; c < hi; ++c) sum += __ldcg(&W.ids_agg[c]);
+  int tot;
+  int ex = block_exclusive_scan<1024>(sum, [](int a, int b) { return a + b; }, 0, red, &tot);
+  for (int c = lo; c < hi; ++c) {
+    const int v = __ldcg(&W.ids_agg[c]);
+    W.ids_inc[c] = ex;
+    ex += v;
+  }
+  if (tid == 0) W.counters[4] = tot;
+}
+
 __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
   constexpr int PER = IDS_CHUNK / IDS_THREADS;
   __shared__ int s_off[IDS_CHUNK + 1];   // chunk-local output offset of each piece
   __shared__ int s_st[IDS_CHUNK];        // its start byte (its IDs sit at scratch[start ...])
   __shared__ int red[IDS_THREADS / 32];
   __shared__ int2 s_red2[IDS_THREADS / 32];
-  __shared__ int s_tile, s_base;
   __shared__ int64_t s_rlo, s_rhi;       // requests whose first piece is in the chunk
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
@@ -871,11 +915,9 @@ __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
       A.out_id_offsets[r] = 0;
     return;
   }
-  for (;;) {
-    if (tid == 0) s_tile = atomicAdd(&W.counters[1], 1);
-    __syncthreads();
-    const int t = s_tile;
-    if (t >= nchunks) return;
+  // chunks are independent: each one's first output comes from the chunk scan
+  for (int t = blockIdx.x; t < nchunks; t += gridDim.x) {
+    const int cb = __ldcg(&W.ids_inc[t]);
     const int k0 = t * IDS_CHUNK;
     const int nloc = min(IDS_CHUNK, np - k0);
     int cnt[PER], st[PER];
@@ -897,24 +939,18 @@ __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
     }
     int chunk_total;
     const int ex = block_exclusive_scan<IDS_THREADS>(sum, [](int a, int b) { return a + b; }, 0, red, &chunk_total);
-    // (warps 1 and 2 find the chunk's requests while warp 0 waits on its predecessors)
-    if (tid >= 32 && tid < 64) {
-      const int64_t r = first_request_from(A, W, base, total, np, k0);
-      if (tid == 32) s_rlo = r;
-    } else if (tid >= 64 && tid < 96) {
-      const int64_t r = t == nchunks - 1 ? A.n + 1 : first_request_from(A, W, base, total, np, k0 + nloc);
-      if (tid == 64) s_rhi = r;
-    }
+    // (warps 0 and 1 find the chunk's requests; the counts the chunk scan
+    // summed must be the ones read here)
     if (tid < 32) {
-      const int b = warp_lookback(t, chunk_total, [](int a, int b) { return a + b; }, 0, W.ids_agg, W.ids_inc,
-                                  W.ids_flag, W.status, W.spin_limit);
-      if (tid == 0) {
-        s_base = b;
-        if (t == nchunks - 1) W.counters[4] = b + chunk_total;
-      }
+      const int64_t r = first_request_from(A, W, base, total, np, k0);
+      if (tid == 0) s_rlo = r;
+    } else if (tid < 64) {
+      const int64_t r = t == nchunks - 1 ? A.n + 1 : first_request_from(A, W, base, total, np, k0 + nloc);
+      if (tid == 32) s_rhi = r;
+    } else if (tid == 64 && __ldcg(&W.ids_agg[t]) != chunk_total) {
+      set_status(W.status, ST_INVALID_ARG);
     }
     __syncthreads();
-    const int cb = s_base;
     int off = ex;
 #pragma unroll
     for (int m = 0; m < PER; ++m) {
@@ -1070,6 +1106,7 @@ void launch_bpe_warp(const Tables &T, const Work &W, int grid, cudaStream_t s) {
 void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   k_bpe_long<<<grid, BPE_LONG_THREADS, LONG_SMEM_BYTES, s>>>(T, W);
 }
+void launch_idscan(const Work &W, cudaStream_t s) { k_idscan<<<1, 1024, 0, s>>>(W); }
 void launch_ids(const Tables &T, const Work &W, int grid, cudaStream_t s) { k_ids<<<grid, IDS_THREADS, 0, s>>>(T, W); }
 void launch_hook_pre(const Work &W, cudaStream_t s) { k_hook_pre<<<1, 1024, 0, s>>>(W); }
 void launch_hook_pieces(const Work &W, int grid, cudaStream_t s) { k_hook_pieces<<<grid, 256, 0, s>>>(W); }

@@ -418,8 +418,8 @@ struct Work {
   int *s2_flag;
   int2 *cnt_agg, *cnt_inc;         // (pieces, last piece start * 2 + placeholder bit)
   int *cnt_flag;
-  int *ids_agg, *ids_inc, *ids_flag;
-  int *counters;                   // [0] pretok tile ticket, [1] ids tile ticket, [2] [7] [8] sizes of
+  int *ids_agg, *ids_inc;          // per ID chunk: its ID count (summed by the BPE kernels), its first output
+  int *counters;                   // [0] pretok tile ticket, [1] unused, [2] [7] [8] sizes of
                                    // the mid-length buckets 0..2, [3] pieces, [4] tokens, [5] bad
                                    // requests seen, [6] huge list size, [9] mid work ticket
   // pieces and tokens

@@ -16,6 +16,7 @@ void launch_lit_find(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_lit_pick(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_bpe_warp(const Tables &T, const Work &W, int grid, cudaStream_t s);
 void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s);
+void launch_idscan(const Work &W, cudaStream_t s);
 void launch_ids(const Tables &T, const Work &W, int grid, cudaStream_t s);
 
 void launch_hook_pre(const Work &W, cudaStream_t s);

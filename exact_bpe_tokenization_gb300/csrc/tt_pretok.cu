@@ -366,10 +366,11 @@ __global__ void __launch_bounds__(1024) k_tilescan(Tables T, Work W) {
   __shared__ int carry_rq;
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
-  // reset look-back flags of every tile / chunk this workspace can hold
+  // reset the look-back flags of every tile and the ID totals of every
+  // chunk this workspace can hold
   for (int i = tid; i < W.cap_tiles; i += 1024) { W.s2_flag[i] = 0; W.cnt_flag[i] = 0; }
   const int nchunks_max = (int)((W.cap_bytes + 1 + IDS_CHUNK - 1) / IDS_CHUNK) + 1;
-  for (int i = tid; i < nchunks_max; i += 1024) W.ids_flag[i] = 0;
+  for (int i = tid; i < nchunks_max; i += 1024) W.ids_agg[i] = 0;
   if (A.n <= 0) return;
   const int64_t base = __ldg(&A.offs[0]);
   const int64_t total = __ldg(&A.offs[A.n]) - base;
