@@ -267,6 +267,8 @@ def alg_bytes(kernel, c):
     if cls:
         p = sum(c[k]["pieces"] for k in cls)
         return sum(c[k]["bytes"] + 4 * c[k]["tokens"] for k in cls) + 12 * p   # bytes + starts in, IDs + count out
+    if kernel == "k_idscan":
+        return 8 * ((a["pieces"] + 511) // 512) + 4          # chunk totals in, chunk offsets and the ID count out
     if kernel == "k_ids":
         return 8 * a["pieces"] + 8 * a["tokens"] + 16        # counts + starts in, IDs in and out, 2 offsets out
     return a["bytes"] + 4 * a["tokens"]
