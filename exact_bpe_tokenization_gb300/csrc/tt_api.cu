@@ -31,8 +31,8 @@ using namespace tt;
 
 namespace {
 
-constexpr int N_KERNELS = 9;
-const char *KERNEL_NAMES[N_KERNELS] = {"k_lit_find", "k_lit_pick", "k_prepass", "k_tilescan", "k_pretok",
+constexpr int N_KERNELS = 8;
+const char *KERNEL_NAMES[N_KERNELS] = {"k_lit_find", "k_lit_pick", "k_prepass", "k_pretok",
                                        "k_bpe_warp", "k_bpe_long", "k_idscan", "k_ids"};
 
 struct Workspace {
@@ -88,7 +88,7 @@ struct tt_tokenizer {
 
 // kernels of one encode: six, and the two literal kernels when the handle
 // has added-token literals
-static int launches_per_encode(const tt_tokenizer *h) { return 7 + (h->T.n_lit ? 2 : 0); }
+static int launches_per_encode(const tt_tokenizer *h) { return 6 + (h->T.n_lit ? 2 : 0); }
 
 #define TT_CUDA(call)                                                   \
   do {                                                                  \
@@ -420,8 +420,7 @@ static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_
   struct Item { void **dst; size_t bytes; };
   Work &W = w->W;
   std::vector<Item> items = {
-      {(void **)&W.s1_sum, sizeof(int2) * tiles},       {(void **)&W.s1_carry, sizeof(int2) * tiles},
-      {(void **)&W.rq_sum, 2 * (size_t)tiles},          {(void **)&W.rq_carry, 2 * (size_t)tiles},
+      {(void **)&W.s1_sum, sizeof(int2) * tiles},       {(void **)&W.rq_sum, 2 * (size_t)tiles},
       {(void **)&W.s2_agg, sizeof(S2) * tiles},         {(void **)&W.s2_inc, sizeof(S2) * tiles},
       {(void **)&W.s2_flag, 4 * (size_t)tiles},         {(void **)&W.cnt_agg, sizeof(int2) * tiles},
       {(void **)&W.cnt_inc, sizeof(int2) * tiles},      {(void **)&W.cnt_flag, 4 * (size_t)tiles},
@@ -542,7 +541,6 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
       launch_lit_pick(T, W, grid_lit_pick(w), stream);
     }
     launch_prepass(T, W, grid_tiles(w), stream);
-    launch_tilescan(T, W, stream);
     launch_pretok(T, W, grid_tiles(w), stream);
     TT_CUDA(cudaEventRecord(w->ev_fork, stream));
     TT_CUDA(cudaStreamWaitEvent(w->side, w->ev_fork, 0));
@@ -563,12 +561,11 @@ static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stre
       case 0: launch_lit_find(T, W, grid_tiles(w), stream); break;
       case 1: launch_lit_pick(T, W, grid_lit_pick(w), stream); break;
       case 2: launch_prepass(T, W, grid_tiles(w), stream); break;
-      case 3: launch_tilescan(T, W, stream); break;
-      case 4: launch_pretok(T, W, grid_tiles(w), stream); break;
-      case 5: launch_bpe_warp(T, W, grid_warp(w), stream); break;
-      case 6: launch_bpe_long(T, W, grid_long(w), stream); break;
-      case 7: launch_idscan(W, stream); break;
-      case 8: launch_ids(T, W, grid_chunks(w), stream); break;
+      case 3: launch_pretok(T, W, grid_tiles(w), stream); break;
+      case 4: launch_bpe_warp(T, W, grid_warp(w), stream); break;
+      case 5: launch_bpe_long(T, W, grid_long(w), stream); break;
+      case 6: launch_idscan(W, stream); break;
+      case 7: launch_ids(T, W, grid_chunks(w), stream); break;
     }
     cudaEventRecord(b, stream);
     h->pending.push_back({kidx, a, b});
@@ -798,7 +795,7 @@ extern "C" tt_status tt_pretokenize_batch(tt_tokenizer *h, const uint8_t *d_utf8
   const Work &W = w->W;
   TT_CUDA(cudaMemsetAsync(W.counters, 0, 4 * 16, stream));
   TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)w->cap_reqs + 1, stream));
-  int launched = 6;
+  int launched = 5;
   if (h->T.n_lit) {
     TT_CUDA(cudaMemsetAsync(W.lit_flag, 0, (size_t)w->cap_bytes + 8, stream));
     launch_lit_find(h->T, W, grid_tiles(w), stream);
@@ -806,7 +803,6 @@ extern "C" tt_status tt_pretokenize_batch(tt_tokenizer *h, const uint8_t *d_utf8
     launched += 2;
   }
   launch_prepass(h->T, W, grid_tiles(w), stream);
-  launch_tilescan(h->T, W, stream);
   launch_pretok(h->T, W, grid_tiles(w), stream);
   launch_hook_pre(W, stream);
   launch_hook_pieces(W, grid_pieces(w), stream);
@@ -882,8 +878,7 @@ constexpr size_t na_round(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // sizes of the scratch arrays, in the order they are carved
 constexpr size_t NA_SIZES[] = {
-    sizeof(int2) * NA_TILES, sizeof(int2) * NA_TILES,                 // s1_sum, s1_carry
-    2 * (size_t)NA_TILES, 2 * (size_t)NA_TILES,                        // rq_sum, rq_carry
+    sizeof(int2) * NA_TILES, 2 * (size_t)NA_TILES,                     // s1_sum, rq_sum
     sizeof(S2) * NA_TILES, sizeof(S2) * NA_TILES, 4 * (size_t)NA_TILES, // s2_agg, s2_inc, s2_flag
     sizeof(int2) * NA_TILES, sizeof(int2) * NA_TILES, 4 * (size_t)NA_TILES,  // cnt_agg, cnt_inc, cnt_flag
     4 * (size_t)NA_CHUNKS, 4 * (size_t)NA_CHUNKS,                      // ids_agg, ids_inc
@@ -956,7 +951,7 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   tt_status s = noalloc_scratch_address(dev, &base);
   if (s != TT_OK) return s;
   Work W{};
-  void **dst[] = {(void **)&W.s1_sum,  (void **)&W.s1_carry, (void **)&W.rq_sum,   (void **)&W.rq_carry,
+  void **dst[] = {(void **)&W.s1_sum,  (void **)&W.rq_sum,
                   (void **)&W.s2_agg,  (void **)&W.s2_inc,   (void **)&W.s2_flag,  (void **)&W.cnt_agg,
                   (void **)&W.cnt_inc, (void **)&W.cnt_flag, (void **)&W.ids_agg,  (void **)&W.ids_inc,
                   (void **)&W.counters, (void **)&W.piece_start, (void **)&W.n_ids,
@@ -978,7 +973,7 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   const CallArgs args = {d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, nullptr, nullptr};
   k_noalloc_args<<<1, 1, 0, stream>>>(args, W.args);
   // what must start at zero: the counters and the rejected-request flags
-  // (look-back flags are reset by k_tilescan)
+  // (look-back flags and ID chunk totals are reset by k_prepass)
   TT_CUDA(cudaMemsetAsync(W.counters, 0, 4 * 16, stream));
   TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)NA_REQS + 1, stream));
   const Tables &T = h->T;
@@ -992,7 +987,6 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
     launch_lit_pick(T, W, (g_tiles + 7) / 8, stream);
   }
   launch_prepass(T, W, g_tiles, stream);
-  launch_tilescan(T, W, stream);
   launch_pretok(T, W, g_tiles, stream);
   launch_bpe_warp(T, W, g_warp, stream);
   launch_bpe_long(T, W, g_long, stream);

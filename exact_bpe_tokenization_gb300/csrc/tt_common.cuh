@@ -411,8 +411,8 @@ struct Work {
   int32_t cap_tiles;
   int32_t spin_limit;
   // pre-pass summaries and carries
-  int2 *s1_sum, *s1_carry;         // mark resolution: (last stretch start, last trigger)
-  uint8_t *rq_sum, *rq_carry;      // [tiles][2]: first rq_ws / rq_up event
+  int2 *s1_sum;                    // mark resolution: (last stretch start, last trigger)
+  uint8_t *rq_sum;                 // [tiles][2]: first rq_ws / rq_up event
   // look-back state
   S2 *s2_agg, *s2_inc;
   int *s2_flag;

@@ -9,7 +9,6 @@ namespace tt {
 cudaError_t pretok_configure();
 cudaError_t bpe_configure();
 void launch_prepass(const Tables &T, const Work &W, int grid, cudaStream_t s);
-void launch_tilescan(const Tables &T, const Work &W, cudaStream_t s);
 void launch_pretok(const Tables &T, const Work &W, int grid, cudaStream_t s);
 
 void launch_lit_find(const Tables &T, const Work &W, int grid, cudaStream_t s);

@@ -4,25 +4,24 @@
 // Serving, §4.1 run decomposition, §4.3 multi-document batching: runs are cut
 // at document boundaries and counts stay in device memory).
 //
-// Three kernels per batch:
+// Two kernels per batch:
 //   k_prepass   one CTA per 4016-byte tile, independent: validates UTF-8
 //               (per request), and summarises each tile for the two scans
-//               whose carries are computed ahead of time, from the bytes
+//               whose carries are found ahead of their use, from the bytes
 //               alone: the reverse "first event after" queries (one warp
 //               from the tile start) and o200k mark resolution (the last
 //               stretch start and trigger, on a tiling shifted 32 bytes left:
-//               one warp back from the tile end); it also copies page-locked
+//               one warp back from the tile end); it resets the look-back
+//               flags and ID chunk totals of its tile, and copies page-locked
 //               host input into the device batch when asked to.
-//   k_tilescan  one CTA: exclusive scans of those tile summaries (forward for
-//               marks, backward for the reverse queries); resets look-back
-//               flags.
-//   k_pretok    one CTA per tile, tiles claimed in order: effective classes
-//               (deepseek-style: segment starts), the forward scan (number-run
-//               count, blank-run start, o200k contraction chain and case
-//               state) with decoupled look-back on a tiling shifted 16 bytes
-//               left, its aggregate published before the reverse queries, the
-//               predicate, and compaction of piece starts with a second
-//               decoupled look-back.
+//   k_pretok    one CTA per tile, tiles claimed in order: the two carries
+//               from the other tiles' summaries (one warp each, 32 summaries
+//               a step), effective classes (deepseek-style: segment starts),
+//               the forward scan (number-run count, blank-run start, o200k
+//               contraction chain and case state) with decoupled look-back
+//               on a tiling shifted 16 bytes left, its aggregate published
+//               before the reverse queries, the predicate, and compaction of
+//               piece starts with a second decoupled look-back.
 #include <limits.h>
 
 #include "tt_common.cuh"
@@ -204,6 +203,12 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
   if (t >= ntiles) return;
   const int64_t ts = (int64_t)t * TILE, te = ts + TILE < total ? ts + TILE : total;
   const int64_t ws = ts - HALO_L;
+  // reset what the later kernels accumulate into: this tile's look-back
+  // flags, and the ID totals of the 512-piece chunks whose index times 512
+  // falls in the tile (over all tiles: every chunk the batch's pieces can fill)
+  if (tid == 0) { W.s2_flag[t] = 0; W.cnt_flag[t] = 0; }
+  for (int64_t c = (ts + IDS_CHUNK - 1) / IDS_CHUNK + tid; c < (te + IDS_CHUNK - 1) / IDS_CHUNK; c += NT)
+    W.ids_agg[c] = 0;
   // bytes and request starts suffice: the few chars the summaries look at
   // are decoded where they are met
   load_bytes<NT>(T, A, base, total, ws, S, A.utf8_src);
@@ -358,59 +363,52 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
   }
 }
 
-// ---------------------------------------------------------------- k_tilescan
-__global__ void __launch_bounds__(1024) k_tilescan(Tables T, Work W) {
-  __shared__ int2 red2[32];
-  __shared__ int red_rq[32];
-  __shared__ int2 carry2;
-  __shared__ int carry_rq;
-  const CallArgs A = *W.args;
-  const int tid = threadIdx.x;
-  // reset the look-back flags of every tile and the ID totals of every
-  // chunk this workspace can hold
-  for (int i = tid; i < W.cap_tiles; i += 1024) { W.s2_flag[i] = 0; W.cnt_flag[i] = 0; }
-  const int nchunks_max = (int)((W.cap_bytes + 1 + IDS_CHUNK - 1) / IDS_CHUNK) + 1;
-  for (int i = tid; i < nchunks_max; i += 1024) W.ids_agg[i] = 0;
-  if (A.n <= 0) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) return;
-  const int ntiles = (int)((total + TILE - 1) / TILE);
-  if (tid == 0) { carry2 = make_int2(-1, -1); carry_rq = R_END | (R_END << 8); }
-  __syncthreads();
-  auto mx = [](int2 a, int2 b) { return make_int2(max(a.x, b.x), max(a.y, b.y)); };
-  if (T.family == FAM_O200K) {
-    for (int c = 0; c < ntiles; c += 1024) {
-      const int t = c + tid;
-      const int2 v = t < ntiles ? W.s1_sum[t] : make_int2(-1, -1);
-      int2 tot;
-      const int2 ex = block_exclusive_scan<1024>(v, mx, make_int2(-1, -1), red2, &tot);
-      if (t < ntiles) W.s1_carry[t] = mx(carry2, ex);
-      __syncthreads();
-      if (tid == 0) carry2 = mx(carry2, tot);
-      __syncthreads();
-    }
+// ---------------------------------------------------------------- tile carries
+// A tile's carries come from the pre-pass summaries of the other tiles, found
+// by one warp 32 summaries a step (usually one step: nearly every tile holds
+// both kinds of event).
+
+// Summary of tile u for the reverse queries (low byte rq_ws, high byte
+// rq_up; 0xFF: none in the tile), 0xFFFF past the batch.
+__device__ __forceinline__ int rq_summary(const Work &W, int u, int ntiles) {
+  return u < ntiles ? (int)__ldcg(reinterpret_cast<const uint16_t *>(W.rq_sum) + u) : 0xFFFF;
+}
+
+// The reverse-query carry of tile t: per byte, the first event in the tiles
+// after t, R_END past the batch (without rq_up events, as in cl100k- and
+// deepseek-style, always R_END).  v: this lane's rq_summary of tile
+// t + 1 + lane, loaded ahead.
+__device__ int rq_carry_of(const Work &W, int t, int ntiles, bool want_up, int v) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0xFF, hi = want_up ? 0xFF : (int)R_END;
+  for (int u0 = t + 1;; u0 += 32) {
+    const unsigned ml = __ballot_sync(0xffffffffu, (v & 0xFF) != 0xFF);
+    const unsigned mh = __ballot_sync(0xffffffffu, (v >> 8) != 0xFF);
+    if (lo == 0xFF && ml) lo = __shfl_sync(0xffffffffu, v & 0xFF, __ffs(ml) - 1);
+    if (hi == 0xFF && mh) hi = __shfl_sync(0xffffffffu, v >> 8, __ffs(mh) - 1);
+    if ((lo != 0xFF && hi != 0xFF) || u0 + 32 >= ntiles) break;
+    v = rq_summary(W, u0 + 32 + lane, ntiles);
   }
-  auto first = [](int a, int b) {
-    const int lo = (a & 0xFF) != 0xFF ? (a & 0xFF) : (b & 0xFF);
-    const int hi = (a >> 8) != 0xFF ? (a >> 8) : (b >> 8);
-    return lo | (hi << 8);
-  };
-  // backward: carry of tile t = first event in tiles > t (R_END past the batch)
-  for (int c = ((ntiles - 1) / 1024) * 1024; c >= 0; c -= 1024) {
-    const int t = c + tid;
-    const int v = t < ntiles ? (W.rq_sum[2 * t] | (W.rq_sum[2 * t + 1] << 8)) : 0xFFFF;
-    int tot;
-    const int ex = block_exclusive_suffix<1024>(v, first, 0xFFFF, red_rq, &tot);
-    if (t < ntiles) {
-      const int r = first(ex, carry_rq);
-      W.rq_carry[2 * t] = (uint8_t)(r & 0xFF);
-      W.rq_carry[2 * t + 1] = (uint8_t)(r >> 8);
-    }
-    __syncthreads();
-    if (tid == 0) carry_rq = first(tot, carry_rq);
-    __syncthreads();
+  return (lo == 0xFF ? (int)R_END : lo) | ((hi == 0xFF ? (int)R_END : hi) << 8);
+}
+
+// The mark-resolution carry of tile t (o200k): the latest stretch start and
+// the latest trigger in the tiles before t, -1 for none.  Summary positions
+// grow with the tile index, so the latest is the nearest tile's.  v: this
+// lane's summary of tile t - 1 - lane, loaded ahead.
+__device__ int2 s1_carry_of(const Work &W, int t, int2 v) {
+  const int lane = threadIdx.x & 31;
+  int x = -1, y = -1;
+  bool fx = false, fy = false;
+  for (int u0 = t - 1;; u0 -= 32) {
+    const unsigned mx = __ballot_sync(0xffffffffu, v.x >= 0), my = __ballot_sync(0xffffffffu, v.y >= 0);
+    if (!fx && mx) { x = __shfl_sync(0xffffffffu, v.x, __ffs(mx) - 1); fx = true; }
+    if (!fy && my) { y = __shfl_sync(0xffffffffu, v.y, __ffs(my) - 1); fy = true; }
+    if ((fx && fy) || u0 < 32) break;
+    const int u = u0 - 32 - lane;
+    v = u >= 0 ? __ldcg(&W.s1_sum[u]) : make_int2(-1, -1);
   }
+  return make_int2(x, y);
 }
 
 // ---------------------------------------------------------------- k_pretok
@@ -424,6 +422,8 @@ struct PretokSmem {
   int2 i2_tmp[NT / 32];
   int i_tmp[NT / 32];
   S2 s2_prefix;
+  int2 s1c;                  // mark-resolution carry (o200k)
+  int rqc;                   // reverse-query carry
   int tile;
   int piece_base;
   int prev_last;
@@ -524,8 +524,23 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
   constexpr int fam = FAM;
   const int64_t ts = (int64_t)t * TILE, te = ts + TILE < total ? ts + TILE : total;
   const int64_t ws = ts - HALO_L;
+  // the first steps of the carry searches load while the window does
+  const int wid = tid >> 5, lane = tid & 31;
+  int rq_v = 0;
+  int2 s1_v = make_int2(-1, -1);
+  if (wid == 0) rq_v = rq_summary(W, t + 1 + lane, ntiles);
+  if (fam == FAM_O200K && wid == 1 && t - 1 - lane >= 0) s1_v = __ldcg(&W.s1_sum[t - 1 - lane]);
   load_window(T, A, base, total, ws, S, P.i_tmp, T.n_lit ? W.lit_flag : nullptr);
   const int c0 = S.cbase[tid], c1 = S.cbase[tid + 1];
+  // (read after the barriers of the scans below)
+  if (wid == 0) {
+    const int c = rq_carry_of(W, t, ntiles, fam == FAM_O200K, rq_v);
+    if (lane == 0) P.rqc = c;
+  }
+  if (fam == FAM_O200K && wid == 1) {
+    const int2 c = s1_carry_of(W, t, s1_v);
+    if (lane == 0) P.s1c = c;
+  }
 
   // --- effective kinds (o200k: resolve marks with a max-scan entering at ts - 32)
   if (fam == FAM_O200K) {
@@ -542,7 +557,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
     }
     auto mx = [](int2 a, int2 b) { return make_int2(max(a.x, b.x), max(a.y, b.y)); };
     int2 ex = block_exclusive_scan<NT>(v, mx, make_int2(-1, -1), P.i2_tmp, (int2 *)nullptr);
-    int2 run = mx(W.s1_carry[t], ex);
+    int2 run = mx(P.s1c, ex);
     for (int j = c0; j < c1; ++j) {
       const int64_t pos = ws + S.lead(j);
       if (pos < ts - S1_SHIFT) { S.set_eff(j, effective(fam, S.raw(j), false)); continue; }
@@ -609,8 +624,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
       if ((rq_first & 0xFF) == 0xFF && ew != 0xFF) rq_first = (rq_first & 0xFF00) | ew;
       if ((rq_first >> 8) == 0xFF && eu != 0xFF) rq_first = (rq_first & 0x00FF) | (eu << 8);
     }
-    int after = first(block_exclusive_suffix<NT>(rq_first, first, 0xFFFF, P.i_tmp, (int *)nullptr),
-                      W.rq_carry[2 * t] | (W.rq_carry[2 * t + 1] << 8));
+    int after = first(block_exclusive_suffix<NT>(rq_first, first, 0xFFFF, P.i_tmp, (int *)nullptr), P.rqc);
     for (int j = c1 - 1; j >= c0; --j) {
       const int64_t pos = ws + S.lead(j);
       if (pos < ts || pos >= te) continue;
@@ -784,7 +798,6 @@ void launch_prepass(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   if (pt_narrow(W)) k_prepass<WIN / 8><<<grid, WIN / 8, 0, s>>>(T, W);
   else k_prepass<WIN / 16><<<grid, WIN / 16, 0, s>>>(T, W);
 }
-void launch_tilescan(const Tables &T, const Work &W, cudaStream_t s) { k_tilescan<<<1, 1024, 0, s>>>(T, W); }
 template <int NT>
 static void launch_pretok_nt(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   if (T.family == FAM_O200K) k_pretok<FAM_O200K, NT><<<grid, NT, sizeof(PretokSmem<NT>), s>>>(T, W);
