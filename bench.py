@@ -259,7 +259,7 @@ def alg_bytes(kernel, c):
     minimum for the pieces and tokens it handles (intermediate traffic such
     as hash-table gathers is not credited)."""
     a = c["all"]
-    if kernel in ("k_prepass", "k_tilescan"):
+    if kernel == "k_prepass":
         return a["bytes"]                                     # the batch bytes, read once
     if kernel == "k_pretok":
         return a["bytes"] + 4 * a["pieces"]                   # bytes in, int32 piece starts out
