@@ -222,6 +222,22 @@ def test_utf8_sequences_straddling_tile_edges(cuda, vocabs, large):
     check(cuda, vocabs["c1"], 1, reqs)
 
 
+@pytest.mark.parametrize("family", [1, 2, 3])
+def test_carries_from_tiles_far_away(cuda, vocabs, family):
+    """Runs of 35 tiles and more, so that a tile finds its carries several
+    windows of 32 tile summaries away: a tab run before a letter and before
+    CR/LF (the first later event of the reverse queries), an uppercase run
+    before lowercase letters (o200k's rest-of-run-uppercase query), and
+    combining marks far from the stretch start and trigger that decide
+    whether they count as letters (o200k mark resolution).  The
+    ASCII-trained vocabulary has no merges for these runs, which keeps the
+    oracle fast."""
+    n = 140_000
+    reqs = ["\t" * n + "x", "\t" * n + "\r\n" + "y", "A" * n + "bc d", "x!!" + "\u0301" * (n // 2) + "a",
+            "a" + "\u0301" * (n // 2) + " z", " " + "\u3042" * (n // 3) + "x", "tail"]
+    check(cuda, vocabs["tiny"], family, reqs)
+
+
 def test_offsets_with_nonzero_base(cuda, vocabs):
     merges, vb, vo = vocabs["small1"]
     reqs = [synth.transcript(3 + i, 5000, 1) for i in range(5)]
