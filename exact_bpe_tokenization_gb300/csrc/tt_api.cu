@@ -498,7 +498,7 @@ static cudaEvent_t pool_event(tt_tokenizer *h) {
 // grid sizes, all from capacity
 static int grid_tiles(const Workspace *w) { return (int)((w->cap_bytes + TILE - 1) / TILE); }
 static int grid_reqs(const Workspace *w) { return (int)((w->cap_reqs + 1 + 255) / 256); }
-static int grid_chunks(const Workspace *w) {   // persistent CTAs taking chunk tickets
+static int grid_chunks(const Workspace *w) {   // CTAs striding over the 512-piece ID chunks
   const int64_t g = (w->cap_bytes + 1 + IDS_CHUNK - 1) / IDS_CHUNK;
   return (int)std::min<int64_t>(std::max<int64_t>(g, 1), 152 * 5);   // 5 resident per SM at 47 registers
 }

@@ -26,7 +26,7 @@ static_assert(TILE % 16 == 0 && HALO_L % 16 == 0, "windows keep 16-byte alignmen
 constexpr int SMALL_MAX = 16;                // thread per piece, dense over all pieces
 constexpr int MID_MAX = 256;                 // thread per piece, dense over the longer ones
                                              // (> MID_MAX: a block per piece)
-constexpr int IDS_CHUNK = 512;               // pieces per ticket in the ID scatter
+constexpr int IDS_CHUNK = 512;               // pieces per chunk in the ID scatter
 // capacity of one mid-length bucket, and the bucket of a piece length
 constexpr int64_t list_cap(int64_t cap_bytes) { return cap_bytes / (SMALL_MAX + 1) + 2; }
 TT_HD int mid_bucket(int64_t len) { return len > 128 ? 0 : len > 48 ? 1 : 2; }
@@ -263,50 +263,6 @@ __device__ T block_exclusive_suffix(T v, Op op, T identity, T *smem, T *total) {
   return r;
 }
 
-// Decoupled look-back (one thread).  Publishes `local` as tile `tile`'s
-// aggregate, walks back over predecessors (combining aggregates until an
-// inclusive prefix is found), publishes the inclusive prefix and returns the
-// exclusive one.  Tiles must be claimed in increasing order by running CTAs.
-// Every wait is bounded: after `spin_limit` polls the status records
-// ST_TIMEOUT and the walk stops with what it has, so no CTA can hang.
-template <typename T, typename Op>
-__device__ T lookback(int tile, T local, Op op, T identity, T *agg, T *inc, int *flag, DevStatus *st,
-                      int spin_limit) {
-  if (tile == 0) {
-    inc[0] = local;
-    __threadfence();
-    st_release(&flag[0], 2);
-    return identity;
-  }
-  agg[tile] = local;
-  __threadfence();
-  st_release(&flag[tile], 1);
-  T excl = identity;
-  int t = tile - 1;
-  for (;;) {
-    int f = ld_acquire(&flag[t]);
-    int spins = 0;
-    while (f == 0) {
-      if (++spins > spin_limit) {
-        set_status(st, ST_TIMEOUT);
-        goto done;
-      }
-      __nanosleep(64);
-      f = ld_acquire(&flag[t]);
-    }
-    if (f == 2) {
-      excl = op(ld_cg(&inc[t]), excl);
-      break;
-    }
-    excl = op(ld_cg(&agg[t]), excl);
-    if (--t < 0) break;
-  }
-done:
-  inc[tile] = op(excl, local);
-  __threadfence();
-  st_release(&flag[tile], 2);
-  return excl;
-}
 // Make a tile's aggregate (tile 0: its inclusive prefix) visible to its
 // successors' look-back (one thread).
 template <typename T>
@@ -325,8 +281,10 @@ __device__ __forceinline__ void lookback_publish(int tile, T local, T *agg, T *i
 // must call).  Each step inspects the 32 nearest unread predecessors at once:
 // a ballot finds the nearest one with an inclusive prefix, and the aggregates
 // in between are combined by a warp reduction in tile order.  Returns the
-// exclusive prefix on every lane; lane 0 publishes.  Every wait is bounded.
-// With `published`, the tile's aggregate was already made visible by
+// exclusive prefix on every lane; lane 0 publishes.  Tiles must be claimed
+// in increasing order by running CTAs.  Every wait is bounded: after
+// `spin_limit` polls the status records ST_TIMEOUT and the walk stops with
+// what it has, so no CTA can hang.  With `published`, the tile's aggregate was already made visible by
 // lookback_publish (so that the successors' look-back can start while this
 // tile does other work).
 template <typename T, typename Op>
