@@ -140,11 +140,11 @@ typedef struct {
 
 static const profile_t PROFILES[4] = {
   /* 0: ASCII code-like text */
-  {5000, 0.07, 0.10, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.14},
+  {5000, 0.07, 0.10, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.14, 0.0, 0.0},
   /* 1: mixed UTF-8 */
-  {50000, 0.065, 0.09, 0.034, 0.085, 0.0, 0.12, 0.04, 0.05, 0.03, 0.035, 0.02, 0.13},
+  {50000, 0.065, 0.09, 0.034, 0.085, 0.0, 0.12, 0.04, 0.05, 0.03, 0.035, 0.02, 0.13, 0.0, 0.0},
   /* 2: as 1, with camelCase/PascalCase identifiers and combining marks */
-  {50000, 0.055, 0.08, 0.036, 0.09, 0.14, 0.08, 0.03, 0.30, 0.03, 0.035, 0.02, 0.13},
+  {50000, 0.055, 0.08, 0.036, 0.09, 0.14, 0.08, 0.03, 0.30, 0.03, 0.035, 0.02, 0.13, 0.0, 0.0},
   /* 3: as 1, with kana and ideograph runs often glued to words, digits and punctuation */
   {50000, 0.08, 0.10, 0.30, 0.01, 0.0, 0.08, 0.03, 0.0, 0.03, 0.02, 0.02, 0.10, 0.35, 0.4},
 };
