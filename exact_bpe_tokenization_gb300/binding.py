@@ -61,11 +61,12 @@ def lib():
             L.tt_launch_count.argtypes = [p]
             L.tt_launch_count.restype = i64
             L.tt_table_digest.restype = ctypes.c_char_p
+            L.tt_debug_lookback.argtypes = [p, i32, i32]
             for name in ("tt_create", "tt_encode_batch", "tt_encode_batch_bounded", "tt_encode_batch_spans",
                          "tt_set_added_tokens",
                          "tt_encode_batch_noalloc",
                          "tt_encode_host",
-                         "tt_get_status", "tt_pretokenize_batch", "tt_profile_read"):
+                         "tt_get_status", "tt_pretokenize_batch", "tt_profile_read", "tt_debug_lookback"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -206,6 +207,12 @@ def tt_profile_read(h, cap=16):
 
 def tt_launch_count(h):
     return lib().tt_launch_count(h)
+
+
+def tt_debug_lookback(h, spin_limit, withhold_tile=-1):
+    """Test setting: poll limit of the pre-tokenizer's look-back waits (0: the
+    default) and a tile that publishes nothing (-1: none)."""
+    _check(lib().tt_debug_lookback(h, int(spin_limit), int(withhold_tile)), "tt_debug_lookback")
 
 
 class Tokenizer:

@@ -79,6 +79,9 @@ struct tt_tokenizer {
   double prof_ms[N_KERNELS] = {0};
   int64_t prof_n[N_KERNELS] = {0};
   bool graphs_enabled = true;
+  // look-back wait settings given to every workspace (tt_debug_lookback)
+  int32_t spin_limit = 1 << 22;
+  int32_t withhold_tile = -1;
   // host copies of the vocabulary (rebuilt with added-token literals)
   std::vector<uint8_t> hv_bytes;
   std::vector<int64_t> hv_off;         // [n_vocab + 1], from 0
@@ -450,7 +453,8 @@ static tt_status make_workspace(tt_tokenizer *h, int64_t cap_bytes, int64_t cap_
   W.cap_bytes = cap_bytes;
   W.cap_reqs = cap_reqs;
   W.cap_tiles = (int32_t)tiles;
-  W.spin_limit = 1 << 22;
+  W.spin_limit = h->spin_limit;
+  W.withhold_tile = h->withhold_tile;
   W.status = h->d_status;
   if (cudaMemset(w->mem, 0, total) != cudaSuccess) { free_workspace(w); return TT_ERR_CUDA; }
   *out = w;
@@ -597,7 +601,8 @@ static tt_status encode_bounded(tt_tokenizer *h, const uint8_t *d_utf8, const in
   std::lock_guard<std::mutex> lock(h->mu);
   Workspace *w;
   if ((s = get_workspace(h, stream, max_total_bytes, n_requests, &w)) != TT_OK) return s;
-  CallArgs args = {d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, nullptr, nullptr, d_out_spans, src};
+  CallArgs args = {d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, nullptr, nullptr, d_out_spans, src,
+                   max_total_bytes};
   TT_CUDA(cudaMemcpyAsync(w->W.args, &args, sizeof(args), cudaMemcpyHostToDevice, stream));
   if (h->profiling || !h->graphs_enabled) return enqueue_encode(h, w, stream, h->profiling);
   if (!w->graph) {
@@ -790,7 +795,8 @@ extern "C" tt_status tt_pretokenize_batch(tt_tokenizer *h, const uint8_t *d_utf8
   std::lock_guard<std::mutex> lock(h->mu);
   Workspace *w;
   if ((s = get_workspace(h, stream, ends[1] - ends[0], n_requests, &w)) != TT_OK) return s;
-  CallArgs args = {d_utf8, d_byte_offsets, n_requests, nullptr, nullptr, d_piece_starts, d_piece_offsets};
+  CallArgs args = {d_utf8, d_byte_offsets, n_requests, nullptr, nullptr, d_piece_starts, d_piece_offsets, nullptr,
+                   nullptr, ends[1] - ends[0]};
   TT_CUDA(cudaMemcpyAsync(w->W.args, &args, sizeof(args), cudaMemcpyHostToDevice, stream));
   const Work &W = w->W;
   TT_CUDA(cudaMemsetAsync(W.counters, 0, 4 * 16, stream));
@@ -862,6 +868,23 @@ extern "C" int tt_profile_read(tt_tokenizer *h, const char **names, double *ms, 
 extern "C" int64_t tt_launch_count(tt_tokenizer *h) { return h ? h->launches.load() : 0; }
 
 extern "C" const char *tt_table_digest(void) { return TT_CLASS_DIGEST; }
+
+extern "C" tt_status tt_debug_lookback(tt_tokenizer *h, int32_t spin_limit, int32_t withhold_tile) {
+  if (!h || spin_limit < 0 || withhold_tile < -1) return TT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(h->mu);
+  cudaDeviceSynchronize();                   // no encode of the handle is in flight while the settings change
+  h->spin_limit = spin_limit == 0 ? (1 << 22) : spin_limit;
+  h->withhold_tile = withhold_tile;
+  for (auto &kv : h->ws) {
+    kv.second->W.spin_limit = h->spin_limit;
+    kv.second->W.withhold_tile = h->withhold_tile;
+    if (kv.second->graph) {                  // the captured kernels hold the old settings
+      cudaGraphExecDestroy(kv.second->graph);
+      kv.second->graph = nullptr;
+    }
+  }
+  return TT_OK;
+}
 
 // ===================================================================
 // tt_encode_batch_noalloc: the same kernels as tt_encode_batch_bounded,
@@ -968,15 +991,23 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   W.cap_bytes = NA_BYTES;
   W.cap_reqs = NA_REQS;
   W.cap_tiles = (int32_t)NA_TILES;
-  W.spin_limit = 1 << 22;
   W.status = h->d_status;
-  const CallArgs args = {d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, nullptr, nullptr};
+  Tables T;
+  {
+    // a consistent view of the tables and settings (tt_set_added_tokens and
+    // tt_debug_lookback change them under this lock); the launches need no lock
+    std::lock_guard<std::mutex> lock(h->mu);
+    T = h->T;
+    W.spin_limit = h->spin_limit;
+    W.withhold_tile = h->withhold_tile;
+  }
+  const CallArgs args = {d_utf8, d_byte_offsets, n_requests, d_out_ids, d_out_id_offsets, nullptr, nullptr, nullptr,
+                         nullptr, max_total_bytes};
   k_noalloc_args<<<1, 1, 0, stream>>>(args, W.args);
   // what must start at zero: the counters and the rejected-request flags
   // (look-back flags and ID chunk totals are reset by k_prepass)
   TT_CUDA(cudaMemsetAsync(W.counters, 0, 4 * 16, stream));
   TT_CUDA(cudaMemsetAsync(W.bad, 0, (size_t)NA_REQS + 1, stream));
-  const Tables &T = h->T;
   const int g_tiles = (int)((NA_BYTES + TILE - 1) / TILE);
   const int g_warp = (int)warp_grid(NA_BYTES);
   const int g_long = (int)std::min<int64_t>(std::max<int64_t>(NA_BYTES / (MID_MAX + 1), 1), 152 * 2);
@@ -993,6 +1024,6 @@ extern "C" tt_status tt_encode_batch_noalloc(tt_tokenizer *h, const uint8_t *d_u
   launch_idscan(W, stream);
   launch_ids(T, W, g_chunks, stream);
   TT_CUDA(cudaGetLastError());
-  h->launches += launches_per_encode(h);
+  h->launches += 7 + (T.n_lit ? 2 : 0);       // the encode's kernels and k_noalloc_args
   return TT_OK;
 }

@@ -538,9 +538,8 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
   __shared__ int16_t s_pv[WARP_KERNEL_WARPS][MID_MAX];
   const CallArgs A = *W.args;
   if (A.n <= 0) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) return;
+  int64_t base, total;
+  if (!batch_extent(A, base, total) || call_timed_out(W)) return;
   const int np = __ldcg(&W.counters[3]);
   const int c0 = __ldcg(&W.counters[mid_bucket_counter(0)]), c1 = __ldcg(&W.counters[mid_bucket_counter(1)]);
   const int c2 = __ldcg(&W.counters[mid_bucket_counter(2)]);
@@ -717,9 +716,8 @@ __global__ void __launch_bounds__(BPE_LONG_THREADS, 1) k_bpe_long(Tables T, Work
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
   if (A.n <= 0) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) return;
+  int64_t base, total;
+  if (!batch_extent(A, base, total) || call_timed_out(W)) return;
   const int nh = __ldcg(&W.counters[6]);
   const uint8_t *g = A.utf8 + base;
   auto plus = [](int a, int b) { return a + b; };
@@ -875,9 +873,8 @@ __global__ void __launch_bounds__(1024) k_idscan(Work W) {
   const int tid = threadIdx.x;
   int np = 0;
   if (A.n > 0) {
-    const int64_t base = __ldg(&A.offs[0]);
-    const int64_t total = __ldg(&A.offs[A.n]) - base;
-    if (!(total > W.cap_bytes || total < 0 || base < 0)) np = __ldcg(&W.counters[3]);
+    int64_t base, total;
+    if (batch_extent(A, base, total) && !call_timed_out(W)) np = __ldcg(&W.counters[3]);
   }
   const int nchunks = (np + IDS_CHUNK - 1) / IDS_CHUNK;
   const int per = (nchunks + 1023) / 1024;
@@ -905,12 +902,11 @@ __global__ void __launch_bounds__(IDS_THREADS) k_ids(Tables T, Work W) {
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
   if (A.n <= 0) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  const bool sound = !(total > W.cap_bytes || total < 0 || base < 0);
+  int64_t base, total;
+  const bool sound = batch_extent(A, base, total) && !call_timed_out(W);
   const int np = sound ? __ldcg(&W.counters[3]) : 0;
   const int nchunks = (np + IDS_CHUNK - 1) / IDS_CHUNK;
-  if (nchunks == 0) {   // no pieces (an empty or unsound batch): every request has no IDs
+  if (nchunks == 0) {   // no pieces (an empty, unsound or timed-out batch): every request has no IDs
     for (int64_t r = (int64_t)blockIdx.x * IDS_THREADS + tid; r <= A.n; r += (int64_t)gridDim.x * IDS_THREADS)
       A.out_id_offsets[r] = 0;
     return;
@@ -1070,9 +1066,8 @@ __global__ void __launch_bounds__(1024) k_hook_pre(Work W) {
 __global__ void k_hook_pieces(Work W) {
   const CallArgs A = *W.args;
   if (A.n <= 0) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) return;
+  int64_t base, total;
+  if (!batch_extent(A, base, total) || call_timed_out(W)) return;
   const int np = __ldcg(&W.counters[3]);
   for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < np; k += gridDim.x * blockDim.x) {
     const int32_t s = __ldcg(&W.piece_start[k]);
@@ -1091,9 +1086,8 @@ __global__ void k_hook_offsets(Work W) {
   const CallArgs A = *W.args;
   const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (A.n <= 0 || r > A.n) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) { A.hook_offsets[r] = 0; return; }
+  int64_t base, total;
+  if (!batch_extent(A, base, total) || call_timed_out(W)) { A.hook_offsets[r] = 0; return; }
   const int np = __ldcg(&W.counters[3]);
   const int k = lower_bound_piece(W.piece_start, np, __ldg(&A.offs[r]) - base);
   A.hook_offsets[r] = k - W.bad_pre[r];

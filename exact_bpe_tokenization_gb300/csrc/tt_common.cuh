@@ -283,16 +283,22 @@ __device__ __forceinline__ void lookback_publish(int tile, T local, T *agg, T *i
 // in between are combined by a warp reduction in tile order.  Returns the
 // exclusive prefix on every lane; lane 0 publishes.  Tiles must be claimed
 // in increasing order by running CTAs.  Every wait is bounded: after
-// `spin_limit` polls the status records ST_TIMEOUT and the walk stops with
-// what it has, so no CTA can hang.  With `published`, the tile's aggregate was already made visible by
-// lookback_publish (so that the successors' look-back can start while this
-// tile does other work).
+// `spin_limit` polls the status records ST_TIMEOUT, *call_timeout is set (the
+// later kernels of the call then withhold its outputs: a batch whose prefix
+// is incomplete yields zero IDs, never approximate ones) and the walk stops
+// with what it has, so no CTA can hang.  The prefix it then publishes is a
+// partial sum of the predecessors' counts, never more than the true one, so
+// indices derived from it stay inside the workspace.  With `published`, the
+// tile's aggregate was already made visible by lookback_publish (so that the
+// successors' look-back can start while this tile does other work).  With
+// `withhold` (a test setting), the tile publishes nothing, so that its
+// successors' waits run out.
 template <typename T, typename Op>
 __device__ T warp_lookback(int tile, T local, Op op, T identity, T *agg, T *inc, int *flag, DevStatus *st,
-                           int spin_limit, bool published = false) {
+                           int *call_timeout, int spin_limit, bool published = false, bool withhold = false) {
   const int lane = threadIdx.x & 31;
   if (tile == 0) {
-    if (lane == 0 && !published) {
+    if (lane == 0 && !published && !withhold) {
       inc[0] = local;
       __threadfence();
       st_release(&flag[0], 2);
@@ -300,7 +306,7 @@ __device__ T warp_lookback(int tile, T local, Op op, T identity, T *agg, T *inc,
     __syncwarp();
     return identity;
   }
-  if (lane == 0 && !published) {
+  if (lane == 0 && !published && !withhold) {
     agg[tile] = local;
     __threadfence();
     st_release(&flag[tile], 1);
@@ -318,7 +324,10 @@ __device__ T warp_lookback(int tile, T local, Op op, T identity, T *agg, T *inc,
       if (f == 0) f = ld_acquire(&flag[t]);
     }
     if (timed_out) {
-      if (lane == 0) set_status(st, ST_TIMEOUT);
+      if (lane == 0) {
+        set_status(st, ST_TIMEOUT);
+        atomicExch(call_timeout, 1);
+      }
       break;
     }
     const unsigned incl = __ballot_sync(0xffffffffu, f == 2);
@@ -337,7 +346,7 @@ __device__ T warp_lookback(int tile, T local, Op op, T identity, T *agg, T *inc,
     if (first < 32) break;
     top -= 32;
   }
-  if (lane == 0) {
+  if (lane == 0 && !withhold) {
     inc[tile] = op(excl, local);
     __threadfence();
     st_release(&flag[tile], 2);
@@ -360,14 +369,31 @@ struct CallArgs {
   int32_t *out_spans;              // [2 * tokens]: (start, end) byte offsets from offs[0] per ID; NULL: none
   const uint8_t *utf8_src;         // the same bytes in page-locked host memory: the pre-pass reads them there
                                    // and copies each tile into utf8 (a buffer of the handle); NULL: none
+  int64_t bound;                   // the caller's upper bound on the batch bytes (<= the workspace capacity):
+                                   // a larger batch is refused on the device with ST_CAPACITY
 };
+
+#if defined(__CUDACC__)
+// The batch's first byte offset and size, read from the per-call arguments.
+// False when the batch is unsound (a negative offset or size) or larger than
+// the bound the caller stated: every kernel then leaves the caller's buffers
+// alone, except k_ids, which zeroes the ID offsets.
+__device__ __forceinline__ bool batch_extent(const CallArgs &A, int64_t &base, int64_t &total) {
+  base = __ldg(&A.offs[0]);
+  total = __ldg(&A.offs[A.n]) - base;
+  return !(total > A.bound || total < 0 || base < 0);
+}
+#endif
+
+constexpr int CTR_TIMEOUT = 10;
 
 // Per-stream workspace (device pointers; sizes fixed per capacity bucket).
 struct Work {
   int64_t cap_bytes;               // largest batch this workspace holds
   int64_t cap_reqs;
   int32_t cap_tiles;
-  int32_t spin_limit;
+  int32_t spin_limit;              // polls before a look-back wait gives up (ST_TIMEOUT)
+  int32_t withhold_tile;           // test setting: this pre-tokenizer tile never publishes (-1: none)
   // pre-pass summaries and carries
   int2 *s1_sum;                    // mark resolution: (last stretch start, last trigger)
   uint8_t *rq_sum;                 // [tiles][2]: first rq_ws / rq_up event
@@ -379,7 +405,8 @@ struct Work {
   int *ids_agg, *ids_inc;          // per ID chunk: its ID count (summed by the BPE kernels), its first output
   int *counters;                   // [0] pretok tile ticket, [1] unused, [2] [7] [8] sizes of
                                    // the mid-length buckets 0..2, [3] pieces, [4] tokens, [5] bad
-                                   // requests seen, [6] huge list size, [9] mid work ticket
+                                   // requests seen, [6] huge list size, [9] mid work ticket,
+                                   // [CTR_TIMEOUT] a look-back wait of this call ran out
   // pieces and tokens
   int32_t *piece_start;            // [cap_bytes + 2], bit 31 = rejected-request placeholder
   int32_t *n_ids;                  // [cap_bytes + 1]
@@ -399,5 +426,11 @@ struct Work {
   DevStatus *status;
   CallArgs *args;
 };
+
+#if defined(__CUDACC__)
+// A look-back wait of this call ran out: the kernels after the pre-tokenizer
+// do no work and the call yields zero IDs for every request.
+__device__ __forceinline__ bool call_timed_out(const Work &W) { return __ldcg(&W.counters[CTR_TIMEOUT]) != 0; }
+#endif
 
 }  // namespace tt

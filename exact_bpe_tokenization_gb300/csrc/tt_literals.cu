@@ -82,9 +82,8 @@ __global__ void __launch_bounds__(LF_THREADS) k_lit_find(Tables T, Work W) {
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
   if (A.n <= 0) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) return;
+  int64_t base, total;
+  if (!batch_extent(A, base, total)) return;
   const int ntiles = (int)((total + TILE - 1) / TILE);
   const int t = blockIdx.x;
   if (t >= ntiles) return;
@@ -140,9 +139,8 @@ __global__ void __launch_bounds__(256) k_lit_pick(Tables T, Work W) {
   const CallArgs A = *W.args;
   const int lane = threadIdx.x & 31;
   if (A.n <= 0) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) return;
+  int64_t base, total;
+  if (!batch_extent(A, base, total)) return;
   const int ntiles = (int)((total + TILE - 1) / TILE);
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles; t += nwarps) {

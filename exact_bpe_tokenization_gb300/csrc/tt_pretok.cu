@@ -189,10 +189,9 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
   if (A.n <= 0) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) {
-    if (blockIdx.x == 0 && tid == 0) set_status(W.status, total > W.cap_bytes ? ST_CAPACITY : ST_INVALID_ARG);
+  int64_t base, total;
+  if (!batch_extent(A, base, total)) {
+    if (blockIdx.x == 0 && tid == 0) set_status(W.status, total > A.bound ? ST_CAPACITY : ST_INVALID_ARG);
     return;
   }
   // offsets must be non-decreasing
@@ -513,9 +512,8 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
   const CallArgs A = *W.args;
   const int tid = threadIdx.x;
   if (A.n <= 0) return;
-  const int64_t base = __ldg(&A.offs[0]);
-  const int64_t total = __ldg(&A.offs[A.n]) - base;
-  if (total > W.cap_bytes || total < 0 || base < 0) return;
+  int64_t base, total;
+  if (!batch_extent(A, base, total)) return;
   const int ntiles = (int)((total + TILE - 1) / TILE);
   if (tid == 0) P.tile = atomicAdd(&W.counters[0], 1);
   __syncthreads();
@@ -605,7 +603,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
   block_exclusive_scan<NT>(agg_pub, comb, s2_identity(), P.s2_tmp, &tile_pub);
   // publish now: the successors' look-back runs while this tile answers its
   // reverse queries
-  if (tid == 0) lookback_publish(t, tile_pub, W.s2_agg, W.s2_inc, W.s2_flag);
+  if (tid == 0 && t != W.withhold_tile) lookback_publish(t, tile_pub, W.s2_agg, W.s2_inc, W.s2_flag);
   const S2 my_ex = block_exclusive_scan<NT>(agg_all, comb, s2_identity(), P.s2_tmp, (S2 *)nullptr);
 
   // --- reverse queries over the tile's chars: first event strictly after j
@@ -638,7 +636,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
 
   if (tid < 32) {
     const S2 pre = warp_lookback(t, tile_pub, comb, s2_identity(), W.s2_agg, W.s2_inc, W.s2_flag, W.status,
-                                 W.spin_limit, true);
+                                 &W.counters[CTR_TIMEOUT], W.spin_limit, true, t == W.withhold_tile);
     if (tid == 0) P.s2_prefix = pre;
   }
   __syncthreads();
@@ -737,7 +735,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
                                                                INT_MAX, P.i_tmp, &tile_first);
   if (tid < 32) {
     const int2 pb = warp_lookback(t, tile_agg, cnt_op, make_int2(0, -1), W.cnt_agg, W.cnt_inc, W.cnt_flag, W.status,
-                                  W.spin_limit);
+                                  &W.counters[CTR_TIMEOUT], W.spin_limit, false, t == W.withhold_tile);
     if (tid == 0) {
       P.piece_base = pb.x;
       P.prev_last = pb.y;

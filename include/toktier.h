@@ -42,6 +42,11 @@
  *     immediately; errors found by the kernels (invalid UTF-8, a capacity
  *     bound exceeded, a bounded device wait that ran out) are recorded in a
  *     device status word owned by the handle and read with tt_get_status.
+ *     A batch larger than its stated bound, or one whose bounded device wait
+ *     ran out, yields zero IDs for every request (out_id_offsets all 0) and
+ *     writes nothing to out_ids: IDs are exact or absent, never approximate
+ *     (the paper's output contract, TokTier §4.1 and §4.4: a fallback may
+ *     change latency, never the returned IDs).
  *   - A handle may be used from several host threads on different streams;
  *     each stream gets its own device workspace.  Calls on the same stream
  *     are ordered by the stream.
@@ -144,11 +149,19 @@ tt_status tt_set_added_tokens(tt_tokenizer *h, const uint8_t *literal_bytes, con
                               const int32_t *literal_ids, int64_t n_literals);
 
 /* tt_destroy - release the handle and every device buffer it owns (waits for
- * the handle's outstanding work).  NULL is ignored. */
+ * the handle's outstanding work).  NULL is ignored.  The pages say only that
+ * tokenizer entries are immutable after registration (TokTier §4.4), so a
+ * handle keeps its tables unchanged from tt_create to this call. */
 void tt_destroy(tt_tokenizer *h);
 
 /*
  * tt_encode_batch - tokenize a batch held in device memory.
+ *
+ * The state-miss full path of TokTier §4.1-§4.3: per request, pre-tokenization
+ * by the run rules (§4.1), each piece encoded independently by BPE (§4.2),
+ * requests concatenated with runs cut at their boundaries and the IDs
+ * compacted in device memory (§4.3).  IDs are delivered as a device array,
+ * the delivery the paper's Figure 10(b) measures against Python lists.
  *
  *   d_utf8          device, the batch bytes (see the batch convention above).
  *   d_byte_offsets  device, int64 [n_requests + 1].
@@ -171,9 +184,11 @@ tt_status tt_encode_batch(tt_tokenizer *h,
  *   max_total_bytes  host-known upper bound on byte_offsets[n] -
  *                    byte_offsets[0]; the launch geometry and the workspace
  *                    are sized from it, the kernels read the true sizes from
- *                    device memory.  If the batch is larger, nothing is
- *                    written except a zeroed d_out_id_offsets and the device
- *                    status TT_ERR_CAPACITY.
+ *                    device memory.  If the batch is larger than this bound
+ *                    (even if it would fit the workspace's size bucket),
+ *                    nothing is written except a zeroed d_out_id_offsets and
+ *                    the device status TT_ERR_CAPACITY, so d_out_ids needs
+ *                    room for max_total_bytes IDs only.
  * Work is launched as one CUDA graph per (stream, size bucket): the first
  * call of a bucket captures it (on a private stream), later calls replay it.
  * Buckets are powers of two of max_total_bytes (at least 64 KiB); each
@@ -229,9 +244,10 @@ tt_status tt_encode_batch_spans(tt_tokenizer *h,
  *   Arguments and outputs as tt_encode_batch_bounded; the limits are
  *   max_total_bytes <= TT_NOALLOC_MAX_BYTES and
  *   n_requests <= TT_NOALLOC_MAX_REQUESTS.  Larger values are rejected with
- *   TT_ERR_CAPACITY before anything is enqueued (a batch whose true size
- *   exceeds the stated bound is caught on the device as in the bounded
- *   call).  The current device must be the handle's.
+ *   TT_ERR_CAPACITY before anything is enqueued.  A batch whose true size
+ *   exceeds max_total_bytes is caught on the device as in the bounded call:
+ *   zeroed d_out_id_offsets, nothing written to d_out_ids, device status
+ *   TT_ERR_CAPACITY.  The current device must be the handle's.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
@@ -273,12 +289,21 @@ tt_status tt_encode_host(tt_tokenizer *h,
  * tt_get_status - wait for `stream`, then return and clear the device status
  * recorded by the handle's kernels since the last call (TT_OK if none).
  * *bad_request (may be NULL) receives the lowest rejected request index for
- * TT_ERR_INVALID_UTF8, else -1.
+ * TT_ERR_INVALID_UTF8, else -1.  The pages define no status interface; this
+ * call carries the paper's output contract (TokTier §4.4: requests that fail
+ * a check change latency, never the IDs returned) to a device pipeline whose
+ * checks run in the kernels: a failed request has zero IDs and its cause is
+ * reported here.
  */
 tt_status tt_get_status(tt_tokenizer *h, tt_stream_t stream, int64_t *bad_request);
 
 /*
  * tt_pretokenize_batch - test hook: pre-tokenizer piece boundaries only.
+ *
+ * TokTier §4.1 checks an implementation at two levels, piece boundaries and
+ * final IDs, because a boundary fault can leave the IDs unchanged; this call
+ * exposes the first level (the kernels of tt_encode_batch up to the piece
+ * table, then a copy of the boundaries).
  *
  *   d_piece_starts   device, int64, capacity >= total bytes of the batch:
  *                    the absolute byte offset (in d_utf8) of every piece
@@ -309,12 +334,28 @@ void tt_profile(tt_tokenizer *h, int enable);
 int tt_profile_read(tt_tokenizer *h, const char **names, double *ms, int64_t *launches, int cap);
 
 /* tt_launch_count - total kernels launched (directly or inside replayed
- * graphs) by this handle since creation. */
+ * graphs) by this handle since creation, the argument-staging kernel of
+ * tt_encode_batch_noalloc included. */
 int64_t tt_launch_count(tt_tokenizer *h);
 
 /* tt_table_digest - SHA-256 (hex, 64 chars + NUL) of the frozen character
  * class table compiled into the library. */
 const char *tt_table_digest(void);
+
+/*
+ * tt_debug_lookback - test setting for the pre-tokenizer's bounded waits.
+ *
+ * The pages describe no such setting; it exists so that tests can make a
+ * device wait run out without faulting or hanging anything.  The two
+ * decoupled look-backs of the pre-tokenizer poll their predecessors' flags at
+ * most `spin_limit` times per window (0 restores the default, 2^22); with
+ * withhold_tile >= 0, that tile of every later batch publishes nothing, so
+ * its successors' waits run out: the batch then yields zero IDs and the
+ * device status TT_ERR_TIMEOUT.  withhold_tile = -1 turns this off.  Waits
+ * for the handle's outstanding work; later encodes capture their graphs
+ * again.  Returns TT_ERR_INVALID_ARG for spin_limit < 0 or withhold_tile < -1.
+ */
+tt_status tt_debug_lookback(tt_tokenizer *h, int32_t spin_limit, int32_t withhold_tile);
 
 #ifdef __cplusplus
 }

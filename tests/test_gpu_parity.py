@@ -362,6 +362,79 @@ def test_capacity_bound_is_reported(cuda, vocabs):
     tok.close()
 
 
+@pytest.mark.parametrize("bound", [16, 4000, 9000])
+def test_bound_below_the_batch_inside_its_bucket(cuda, vocabs, bound):
+    """A stated bound below the true batch size, with the batch still inside
+    the workspace's smallest size bucket (64 KiB): the kernels refuse it
+    (TT_ERR_CAPACITY), zero the ID offsets and write no ID at all, so an IDs
+    buffer sized to the bound is never overrun.  The spans entry point
+    behaves the same, and the handle keeps working."""
+    merges, vb, vo = vocabs["small1"]
+    tok = cuda.Tokenizer(merges, vb, vo, 1)
+    data, offs = synth.batch([synth.transcript(5, 6000, 1), synth.transcript(6, 3000, 1)])
+    assert bound < len(data) < 1 << 16
+    d = torch.from_numpy(data).cuda()
+    o = torch.from_numpy(offs).cuda()
+    ids = torch.full((len(data) + 64,), -7, dtype=torch.int32, device="cuda")
+    io = torch.full((3,), 5, dtype=torch.int64, device="cuda")
+    cuda.tt_encode_batch_bounded(tok.h, d, o, 2, bound, ids, io)
+    assert tok.status() == (cuda.TT_ERR_CAPACITY, -1)
+    assert io.cpu().tolist() == [0, 0, 0]
+    assert bool((ids == -7).all())
+    spans = torch.full((len(data) + 64, 2), -7, dtype=torch.int32, device="cuda")
+    cuda.tt_encode_batch_spans(tok.h, d, o, 2, bound, ids, io, spans)
+    assert tok.status() == (cuda.TT_ERR_CAPACITY, -1)
+    assert io.cpu().tolist() == [0, 0, 0]
+    assert bool((ids == -7).all()) and bool((spans == -7).all())
+    cuda.tt_encode_batch_bounded(tok.h, d, o, 2, len(data), ids, io)   # the true size: exact again
+    torch.cuda.synchronize()
+    assert tok.status() == (0, -1)
+    ref = oracle.Oracle(merges, vb, vo, 1).run(data, offs)
+    io = io.cpu().numpy()
+    assert np.array_equal(io, ref["id_offsets"])
+    assert np.array_equal(ids[:int(io[-1])].cpu().numpy(), ref["ids"])
+    tok.close()
+
+
+def test_lookback_wait_that_runs_out_yields_no_ids(cuda, vocabs):
+    """A bounded device wait made to run out (one pre-tokenizer tile publishes
+    nothing and the poll limit is small, a test setting): the batch reports
+    TT_ERR_TIMEOUT, every request gets zero IDs and no ID is written -- never
+    approximate IDs -- and the same handle is exact again once the setting is
+    cleared.  Nothing faults or hangs: every wait gives up after its polls."""
+    merges, vb, vo = vocabs["small1"]
+    tok = cuda.Tokenizer(merges, vb, vo, 1)
+    reqs = [synth.transcript(40 + i, 20000, 1) for i in range(5)] + [b""]
+    data, offs = synth.batch(reqs)
+    assert len(data) > 20 * 4016                              # tiles after the withheld one
+    d = torch.from_numpy(data).cuda()
+    o = torch.from_numpy(offs).cuda()
+    n = len(reqs)
+    for withhold in (3, 0):
+        cuda.tt_debug_lookback(tok.h, 2000, withhold)
+        ids = torch.full((len(data),), -7, dtype=torch.int32, device="cuda")
+        io = torch.full((n + 1,), 5, dtype=torch.int64, device="cuda")
+        for _ in range(2):                                    # capture, then replay
+            cuda.tt_encode_batch_bounded(tok.h, d, o, n, len(data), ids, io)
+            assert tok.status() == (cuda.TT_ERR_TIMEOUT, -1)
+            assert io.cpu().tolist() == [0] * (n + 1)
+            assert bool((ids == -7).all())
+        starts, po = tok.pretokenize(d, o)
+        assert tok.status() == (cuda.TT_ERR_TIMEOUT, -1)
+        assert po.cpu().tolist() == [0] * (n + 1)
+    cuda.tt_debug_lookback(tok.h, 0, -1)
+    got = run_gpu(cuda, tok, data, offs)
+    ref = oracle.Oracle(merges, vb, vo, 1).run(data, offs)
+    assert got["status"] == 0
+    errs = compare_segmented(ref["piece_starts"], ref["piece_offsets"], got["piece_starts"], got["piece_offsets"],
+                             "pieces")
+    errs += compare_segmented(ref["ids"], ref["id_offsets"], got["ids"], got["id_offsets"], "ids")
+    assert not errs, "\n".join(errs)
+    with pytest.raises(cuda.TokTierError):
+        cuda.tt_debug_lookback(tok.h, -1, -1)
+    tok.close()
+
+
 def test_decreasing_offsets_are_rejected_by_status(cuda, vocabs):
     merges, vb, vo = vocabs["small1"]
     tok = cuda.Tokenizer(merges, vb, vo, 1)
