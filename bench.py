@@ -1,26 +1,39 @@
-"""Benchmark: exact full tokenization of 1M-char requests on one GB300.
+"""Benchmark: exact full tokenization on one GB300.
 
-Metric: full-tokenization input GB/s and p50 ms per 1M-char request
-(fresh-sample protocol: every timed step encodes a different seeded
-1,000,000-char mixed-UTF-8 transcript once, after warm-up on other seeds;
-inputs are resident in HBM and L2 is flushed between steps).
+Metric: full-tokenization input GB/s (batched) and p50 ms per 1M-char
+request.  `value` is the batched half on the 64-request rebuild burst
+(burst_64_loguniform, ~17.6 MB): every step is one call that encodes the
+whole batch, inputs resident in HBM, L2 flushed between steps.  The latency
+half is measured on 1,000,000-char mixed-UTF-8 requests under the
+fresh-sample protocol (every timed request a different seeded sample, each
+encoded once after warm-up on other seeds).
 
 One JSON line on stdout (rank 0).  Keys beyond the base contract:
-  p50_ms / p99_ms   per-request device time over the timed steps
-  e2e               the same requests through tt_encode_host (host buffers,
-                    copies and the wait inside the timed region)
-  roofline          the dominant kernel: algorithmic bytes / measured time
-                    against the measured HBM copy bandwidth
-  cpu_baseline      the CPU oracle on the host cores (a bounded sample)
-  batched_gbs       the 64-request rebuild burst (~20 MB) as one call
-  deepseek_batched_gbs  the same batch shape of kana/CJK-mixed text in the
-                    deepseek-style family, as one call
+  p50_ms_per_1m_char_request / p99_...   the latency half (single_1m_mixed)
+  latency_1m          its protocol, steady state and small requests
+  per_request_alone   each burst request encoded alone: p50 / p99 ms
+  o200k_batched       the 256-request o200k-style batch (~58 MB) as one call
+  adversarial_4_4m    the 4.4M-char adversarial request: p50 / p99 ms
+  tiny_ascii_64k      the 64 KB request on its own 4,096-merge vocabulary
+  e2e                 the burst through tt_encode_host (pinned host buffers,
+                      copies and the wait inside the timed region)
+  roofline            the dominant kernel: (B + 4T + 16 per request) of the
+                      batch / its measured launch time, against the measured
+                      HBM copy bandwidth; `path` the same bytes over whole
+                      calls, per workload
+  cpu_baseline        the CPU oracle on the host cores: a thread pool over
+                      the burst and the o200k-style batch, pinned to one NUMA
+                      node, and one thread on a 1M-char request
+  deepseek_batched    the burst's shape of kana/CJK-mixed text in the
+                      deepseek-style family, as one call
 
---impl reference times the CPU oracle on the same workload and metric.
-Under torchrun (N > 1) every rank encodes its own requests (replicas; the
-requests are independent, so there is no collective on the data path).
+--impl reference times the CPU oracle (a thread pool over the host cores)
+on the same workload and metric.  Under torchrun (N > 1) every rank encodes
+its own copy of the batch (replicas: requests are independent, so there is
+no collective on the data path).
 """
 import argparse
+import glob
 import json
 import os
 import statistics
@@ -34,7 +47,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "single_1m_mixed"
+WORKLOAD = "burst_64_loguniform"          # the batched half of the metric
+LATENCY_WORKLOAD = "single_1m_mixed"      # the p50-per-1M-char half
 METRIC = "full-tokenization input GB/s (batched) and p50 ms per 1M-char request"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 256 << 20          # > 129 MB of L2
@@ -43,8 +57,8 @@ L2_FLUSH_BYTES = 256 << 20          # > 129 MB of L2
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=32)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-families", action="store_true", help="skip the deepseek-style batch line")
@@ -61,8 +75,8 @@ def dist_env():
 
 
 def rank_seeds(rank, steps, warmup):
-    """The request seeds a rank times and warms up on: every rank its own,
-    none shared between ranks or between warm-up and timed steps."""
+    """The 1M-char request seeds a rank times and warms up on: every rank its
+    own, none shared between ranks or between warm-up and timed steps."""
     return ([1 + rank * 10_000 + i for i in range(steps)],
             [100_001 + rank * 10_000 + i for i in range(warmup)])
 
@@ -83,13 +97,75 @@ def combine_ranks(device_s, nbytes, world, device):
 
 def requests_for(seeds):
     from exact_bpe_tokenization_gb300 import synth
-    return [synth.workload(WORKLOAD, seed=s)[0] for s in seeds]
+    return [synth.workload(LATENCY_WORKLOAD, seed=s)[0] for s in seeds]
 
 
-def vocab():
+def vocab(name=WORKLOAD):
     from exact_bpe_tokenization_gb300 import synth
-    W = synth.WORKLOADS[WORKLOAD]
+    W = synth.WORKLOADS[name]
     return synth.make_vocab(*W["vocab"]), W["family"]
+
+
+FAMILY_NAMES = {1: "cl100k-style", 2: "o200k-style", 3: "deepseek-style"}
+
+
+def line_config(data_bytes, n_requests, family, n_merges):
+    """The `config` of both arms' lines: the workload and nothing about the
+    implementation, so that the two lines describe the same work."""
+    return {"workload": WORKLOAD, "requests_per_step": n_requests, "bytes_per_step": int(data_bytes),
+            "pattern_family": FAMILY_NAMES[family], "merges": int(n_merges)}
+
+
+def parse_cpulist(text):
+    out = []
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        if "-" in part:
+            a, b = part.split("-")
+            out.extend(range(int(a), int(b) + 1))
+        else:
+            out.append(int(part))
+    return out
+
+
+def numa_placement():
+    """The host cores to run the CPU oracle on: those this process may use,
+    restricted to the NUMA node that holds most of them (the pages pin their
+    CPU comparators to NUMA nodes).  Returns (cores, description)."""
+    allowed = set(os.sched_getaffinity(0))
+    nodes = {}
+    for path in glob.glob("/sys/devices/system/node/node[0-9]*"):
+        try:
+            with open(os.path.join(path, "cpulist")) as f:
+                cpus = [c for c in parse_cpulist(f.read()) if c in allowed]
+        except (OSError, ValueError):
+            continue
+        if cpus:
+            nodes[int(path.rsplit("node", 1)[1])] = cpus
+    if not nodes:
+        return sorted(allowed), {"numa_node": None, "nodes_with_allowed_cores": [],
+                                 "placement": "no NUMA information: all %d allowed cores" % len(allowed)}
+    node = max(sorted(nodes), key=lambda k: len(nodes[k]))
+    return nodes[node], {"numa_node": node, "nodes_with_allowed_cores": sorted(nodes),
+                         "placement": "threads pinned to the %d allowed cores of NUMA node %d "
+                                      "(sched_setaffinity); inputs generated after pinning (first touch)"
+                                      % (len(nodes[node]), node)}
+
+
+class pinned_to:
+    """Run a block with this process's CPU affinity set to `cores`."""
+
+    def __init__(self, cores):
+        self.cores = set(cores)
+
+    def __enter__(self):
+        self.old = os.sched_getaffinity(0)
+        os.sched_setaffinity(0, self.cores)
+        return self
+
+    def __exit__(self, *exc):
+        os.sched_setaffinity(0, self.old)
 
 
 class ClockSampler:
@@ -231,47 +307,13 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
-def piece_classes(binding, tok, d_in, d_off, ids, vocab_offsets, cap, dev):
-    """Pieces of one request (from the pre-tokenizer test hook) split by the
-    execution unit that encodes them, with their bytes and token counts (IDs
-    are mapped back to pieces through the byte lengths of their tokens)."""
-    import torch
-    starts, po = tok.pretokenize(d_in, d_off)
-    torch.cuda.synchronize(dev)
-    n = int(po[-1].item())
-    st = starts[:n].cpu().numpy() - int(d_off[0].item())
-    total = int(d_off[-1].item() - d_off[0].item())
-    lens = np.diff(np.append(st, total))
-    tok_len = np.diff(np.asarray(vocab_offsets))[ids]
-    ends = np.cumsum(tok_len)                     # byte end of every token
-    piece_of_token = np.searchsorted(np.cumsum(lens), ends, side="left")
-    tokens = np.bincount(piece_of_token, minlength=n)
-    out = {}
-    for name, lo, hi in (("small", 1, 16), ("mid", 17, 256), ("long", 257, 1 << 40)):
-        sel = (lens >= lo) & (lens <= hi)
-        out[name] = {"pieces": int(sel.sum()), "bytes": int(lens[sel].sum()), "tokens": int(tokens[sel].sum())}
-    out["all"] = {"pieces": n, "bytes": total, "tokens": int(len(ids))}
-    return out
-
-
-def alg_bytes(kernel, c):
-    """Algorithmic bytes of one launch: what a kernel must read and write at
-    minimum for the pieces and tokens it handles (intermediate traffic such
-    as hash-table gathers is not credited)."""
-    a = c["all"]
-    if kernel == "k_prepass":
-        return a["bytes"]                                     # the batch bytes, read once
-    if kernel == "k_pretok":
-        return a["bytes"] + 4 * a["pieces"]                   # bytes in, int32 piece starts out
-    cls = {"k_bpe_warp": ["small", "mid"], "k_bpe_long": ["long"]}.get(kernel)
-    if cls:
-        p = sum(c[k]["pieces"] for k in cls)
-        return sum(c[k]["bytes"] + 4 * c[k]["tokens"] for k in cls) + 12 * p   # bytes + starts in, IDs + count out
-    if kernel == "k_idscan":
-        return 8 * ((a["pieces"] + 511) // 512) + 4          # chunk totals in, chunk offsets and the ID count out
-    if kernel == "k_ids":
-        return 8 * a["pieces"] + 8 * a["tokens"] + 16        # counts + starts in, IDs in and out, 2 offsets out
-    return a["bytes"] + 4 * a["tokens"]
+def alg_bytes(n_bytes, n_tokens, n_requests):
+    """Algorithmic bytes of a batch (per request: UTF-8 bytes in, 4 bytes
+    per int32 ID out, 16 bytes of offsets), summed over its requests.  Every
+    kernel launch of an encode processes the whole batch, so this is also
+    the per-launch figure.  Intermediate traffic (classes, piece tables, hash
+    gathers) is not credited."""
+    return int(n_bytes) + 4 * int(n_tokens) + 16 * int(n_requests)
 
 
 def recorded_traffic(kernel, workload, key="dram_bytes_per_launch"):
@@ -313,27 +355,42 @@ def issue_roofline(kernel, workload, launch_ms, sm_mhz):
             "warp_inst_per_launch": inst, "peak_from": "152 SMs x 4 schedulers x 1 warp-inst/cycle x SM clock"}
 
 
-def cpu_baseline(merges_vocab, family, seeds):
-    """The oracle as it stands on the host cores: one request per core."""
-    import oracle
-    merges, vb, vo = merges_vocab
-    o = oracle.Oracle(merges, vb, vo, family)
-    reqs = requests_for(seeds)
+def oracle_gbs(o, reqs, threads):
+    """One oracle run over a batch: (GB/s of input, seconds, tokens)."""
     from exact_bpe_tokenization_gb300 import synth
     data, offs = synth.batch(reqs)
-    cores = os.cpu_count() or 1
     t = time.perf_counter()
-    o.run(data, offs, threads=cores, pieces=False)
+    r = o.run(data, offs, threads=threads, pieces=False)
     dt = time.perf_counter() - t
-    # single-thread latency of one request
-    d1, o1 = synth.batch(reqs[:1])
-    t = time.perf_counter()
-    o.run(d1, o1, threads=1, pieces=False)
-    one = time.perf_counter() - t
-    return {"value": len(data) / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "%d requests of 1,000,000 chars (seeds %d..%d), one request per core" % (
-                len(reqs), seeds[0], seeds[-1]),
-            "ms_per_request_1thread": one * 1e3}
+    return len(data) / dt / 1e9, dt, int(r["id_offsets"][-1])
+
+
+def cpu_baseline(merges_vocab, family, seeds):
+    """The oracle as it stands on the host cores, pinned to one NUMA node: a
+    thread pool (one request per thread at a time) over the burst and over
+    the o200k-style batch, and one thread on a 1M-char request."""
+    import oracle
+    from exact_bpe_tokenization_gb300 import synth
+    cores, numa = numa_placement()
+    merges, vb, vo = merges_vocab
+    out = {"unit": UNIT, "cores": len(cores), "kind": "oracle", "numa": numa,
+           "host_cores_online": os.cpu_count()}
+    with pinned_to(cores):
+        o = oracle.Oracle(merges, vb, vo, family)
+        gbs, dt, _ = oracle_gbs(o, synth.workload(WORKLOAD), len(cores))
+        out.update(value=gbs, sample="the whole %s batch once (%d requests), %d threads" % (
+            WORKLOAD, 64, len(cores)), seconds=dt)
+        one = requests_for(seeds[:1])
+        _, dt1, _ = oracle_gbs(o, one, 1)
+        out["ms_per_1m_char_request_1thread"] = dt1 * 1e3
+        o.close()
+        (m4, v4, o4), f4 = vocab("o200k_256_lognormal")
+        o = oracle.Oracle(m4, v4, o4, f4)
+        g4, d4, _ = oracle_gbs(o, synth.workload("o200k_256_lognormal"), len(cores))
+        out["o200k_batched"] = {"value": g4, "unit": UNIT, "seconds": d4, "threads": len(cores),
+                                "sample": "the whole o200k_256_lognormal batch once (256 requests)"}
+        o.close()
+    return out
 
 
 def run_reference(args):
@@ -341,35 +398,63 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    (merges, vb, vo), family = vocab()
-    o = oracle.Oracle(merges, vb, vo, family)
     from exact_bpe_tokenization_gb300 import synth
-    warm = requests_for(range(1001, 1001 + args.warmup))
-    for r in warm:
-        d, off = synth.batch([r])
-        o.run(d, off, threads=1, pieces=False)
-    reqs = requests_for(range(1, 1 + args.steps))
-    times, nbytes = [], 0
-    for r in reqs:
-        d, off = synth.batch([r])
-        t = time.perf_counter()
-        o.run(d, off, threads=1, pieces=False)
-        times.append(time.perf_counter() - t)
-        nbytes += len(d)
+    cores, numa = numa_placement()
+    (merges, vb, vo), family = vocab()
+    with pinned_to(cores):
+        reqs = synth.workload(WORKLOAD)
+        data, offs = synth.batch(reqs)
+        o = oracle.Oracle(merges, vb, vo, family)
+        for _ in range(args.warmup):
+            o.run(data, offs, threads=len(cores), pieces=False)
+        times = []
+        for _ in range(args.steps):
+            t = time.perf_counter()
+            o.run(data, offs, threads=len(cores), pieces=False)
+            times.append(time.perf_counter() - t)
+        lat = []
+        for r in requests_for(range(1, 4)):          # the latency half: one thread per request
+            d1, o1 = synth.batch([r])
+            t = time.perf_counter()
+            o.run(d1, o1, threads=1, pieces=False)
+            lat.append((time.perf_counter() - t) * 1e3)
     total = sum(times)
-    value = nbytes / total / 1e9
+    value = len(data) * args.steps / total / 1e9
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
             "impl": "reference",
-            "p50_ms": float(np.percentile(np.array(times) * 1e3, 50)),
-            "p99_ms": float(np.percentile(np.array(times) * 1e3, 99)),
-            "config": {"workload": WORKLOAD, "requests_per_step": 1, "chars_per_request": 1_000_000,
-                       "protocol": "fresh sample: each step a different seeded request, CPU oracle, 1 thread"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": "%d requests of 1,000,000 chars, one per step" % args.steps},
+            "config": line_config(len(data), len(reqs), family, len(merges)),
+            "protocol": "each step the whole batch through the CPU oracle, a thread pool over the host cores of one "
+                        "NUMA node (one request per thread at a time)",
+            "p50_ms_per_1m_char_request": float(np.percentile(lat, 50)),
+            "p99_ms_per_1m_char_request": float(np.percentile(lat, 99)),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(cores), "kind": "oracle", "numa": numa,
+                             "sample": "%d steps of the whole %s batch (%d requests, %d bytes)" % (
+                                 args.steps, WORKLOAD, len(reqs), len(data))},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def device_times(stream, flush, call, n, warm=1):
+    """Device time in ms of each of n calls (after `warm` untimed ones), one
+    call at a time between CUDA events on `stream`, L2 flushed before each."""
+    import torch
+    out = []
+    for k in range(warm + n):
+        flush.fill_(k)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        call()
+        e.record(stream)
+        e.synchronize()
+        if k >= warm:
+            out.append(s.elapsed_time(e))
+    return out
+
+
+def pct(xs, q):
+    return float(np.percentile(np.asarray(xs, dtype=np.float64), q))
 
 
 def run_ours(args):
@@ -390,30 +475,27 @@ def run_ours(args):
 
     (merges, vb, vo), family = vocab()
     tok = binding.Tokenizer(merges, vb, vo, family)
-    # each rank gets its own seeds (replicas of the same protocol)
-    seeds, warm_seeds = rank_seeds(rank, args.steps, args.warmup)
-    host = [np.frombuffer(r, dtype=np.uint8) for r in requests_for(seeds)]
-    warm = [np.frombuffer(r, dtype=np.uint8) for r in requests_for(warm_seeds)]
-    cap = max(len(h) for h in host + warm)
-    dev_in = [torch.from_numpy(h.copy()).to(dev) for h in host]
-    dev_warm = [torch.from_numpy(h.copy()).to(dev) for h in warm]
-    offs = [torch.tensor([0, len(h)], dtype=torch.int64, device=dev) for h in host]
-    offs_warm = [torch.tensor([0, len(h)], dtype=torch.int64, device=dev) for h in warm]
-    out_ids = torch.empty(cap, dtype=torch.int32, device=dev)
-    out_off = torch.empty(2, dtype=torch.int64, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
-    def encode(d, o):
-        binding.tt_encode_batch_bounded(tok.h, d, o, 1, cap, out_ids, out_off, stream)
+    # ---------------- the batched half: the whole burst as one call per step
+    reqs = synth.workload(WORKLOAD)
+    data, bo = synth.batch(reqs)
+    n = len(reqs)
+    d = torch.from_numpy(data).to(dev)
+    o = torch.from_numpy(bo).to(dev)
+    ids = torch.empty(len(data), dtype=torch.int32, device=dev)
+    io = torch.empty(n + 1, dtype=torch.int64, device=dev)
 
-    for d, o in zip(dev_warm, offs_warm):
-        encode(d, o)
-        flush.fill_(1)
+    def encode():
+        binding.tt_encode_batch_bounded(tok.h, d, o, n, len(data), ids, io, stream)
+
+    for k in range(args.warmup):
+        flush.fill_(k)
+        encode()
     torch.cuda.synchronize(dev)
     status, _ = tok.status()
     assert status == 0, binding.status_string(status)
-
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     launches0 = binding.tt_launch_count(tok.h)
@@ -425,197 +507,238 @@ def run_ours(args):
         for i in range(args.steps):
             flush.fill_(i)                       # evict the previous step's data from L2
             starts[i].record(stream)
-            encode(dev_in[i], offs[i])
+            encode()
             ends[i].record(stream)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
     launches = binding.tt_launch_count(tok.h) - launches0
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    nbytes = sum(len(h) for h in host)
-    device_s = sum(step_ms) / 1e3
-    device_s, nbytes_all = combine_ranks(device_s, nbytes, world, dev)
+    device_s, nbytes_all = combine_ranks(sum(step_ms) / 1e3, len(data) * args.steps, world, dev)
     status, _ = tok.status()
     assert status == 0, binding.status_string(status)
-    # tokens of the last step (for the e2e byte counts)
-    tokens = int(out_off[1].item())
+    tokens = int(io[-1].item())
+    clocks = nclk.summary() if nclk.sm else clk.summary()
 
-    # per-kernel times: a second pass over the same steps with an event
-    # around every kernel (direct launches), L2 flushed between steps
+    # per-kernel times over the same steps: events around every kernel
+    # (direct launches, one kernel at a time), L2 flushed before each step
     binding.tt_profile(tok.h, 1)
     for i in range(args.steps):
         flush.fill_(i)
-        encode(dev_in[i], offs[i])
+        encode()
     prof = binding.tt_profile_read(tok.h)
     binding.tt_profile(tok.h, 0)
 
-    # steady state: one request encoded 200 times back to back, tables and
-    # input hot in L2 (no flush), each replay timed on its own
+    # end to end through host buffers: the batch in pinned host memory before
+    # each timed call, its IDs and offsets written back into pinned host memory
+    pin_in = torch.empty(len(data), dtype=torch.uint8, pin_memory=True)
+    pin_in.numpy()[:] = data
+    pin_ids = torch.empty(len(data), dtype=torch.int32, pin_memory=True)
+    pin_io = torch.empty(n + 1, dtype=torch.int64, pin_memory=True)
+    in_np, ids_np, io_np = pin_in.numpy(), pin_ids.numpy(), pin_io.numpy()
+    e2e_t = []
+    for i in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        st = binding.tt_encode_host(tok.h, in_np, bo, ids_np, io_np, stream)
+        if i >= args.warmup:
+            e2e_t.append(time.perf_counter() - t)
+        assert st == 0, binding.status_string(st)
+    assert int(io_np[-1]) == tokens
+
+    def per_request_alone(h, rq, dd, bb):
+        """Every request of a batch encoded alone (n = 1): device ms, L2
+        flushed before each call, after one untimed call."""
+        out_i = torch.empty(int(max(bb[1:] - bb[:-1])) + 1, dtype=torch.int32, device=dev)
+        out_o = torch.empty(2, dtype=torch.int64, device=dev)
+        times = []
+        for r in range(len(rq)):
+            dr = dd[int(bb[r]):int(bb[r + 1])]
+            orr = torch.tensor([0, int(bb[r + 1] - bb[r])], dtype=torch.int64, device=dev)
+            times += device_times(stream, flush, lambda: binding.tt_encode_batch_bounded(
+                h, dr, orr, 1, len(dr), out_i, out_o, stream), 1)
+        return {"p50_ms": pct(times, 50), "p99_ms": pct(times, 99), "requests": len(times)}
+
+    burst_alone = per_request_alone(tok.h, reqs, d, bo)
+
+    # ---------------- the latency half: 1M-char requests, fresh sample
+    seeds, warm_seeds = rank_seeds(rank, args.steps, args.warmup)
+    host = [np.frombuffer(r, dtype=np.uint8) for r in requests_for(seeds)]
+    warm = [np.frombuffer(r, dtype=np.uint8) for r in requests_for(warm_seeds)]
+    cap = max(len(h) for h in host + warm)
+    dev_in = [torch.from_numpy(h.copy()).to(dev) for h in host]
+    offs1 = [torch.tensor([0, len(h)], dtype=torch.int64, device=dev) for h in host + warm]
+    out1 = torch.empty(cap, dtype=torch.int32, device=dev)
+    io1 = torch.zeros((len(host), 2), dtype=torch.int64, device=dev)
+    for k, h in enumerate(warm):
+        dw = torch.from_numpy(h.copy()).to(dev)
+        flush.fill_(k)
+        binding.tt_encode_batch_bounded(tok.h, dw, offs1[len(host) + k], 1, cap, out1, io1[0], stream)
+    lat = []
+    for i in range(len(host)):
+        lat += device_times(stream, flush, lambda: binding.tt_encode_batch_bounded(
+            tok.h, dev_in[i], offs1[i], 1, cap, out1, io1[i], stream), 1, warm=0)
+    status, _ = tok.status()
+    assert status == 0, binding.status_string(status)
+    lat_tokens = io1[:, 1].cpu().numpy()
+    lat_bytes = np.array([len(h) for h in host])
+    binding.tt_profile(tok.h, 1)
+    for i in range(len(host)):
+        flush.fill_(i)
+        binding.tt_encode_batch_bounded(tok.h, dev_in[i], offs1[i], 1, cap, out1, io1[i], stream)
+    prof1 = binding.tt_profile_read(tok.h)
+    binding.tt_profile(tok.h, 0)
+    # steady state: one request replayed back to back, tables and input hot in L2
     ss = []
     for i in range(203):
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record(stream)
-        encode(dev_in[0], offs[0])
+        binding.tt_encode_batch_bounded(tok.h, dev_in[0], offs1[0], 1, cap, out1, io1[0], stream)
         s1.record(stream)
         s1.synchronize()
         if i >= 3:
             ss.append(s0.elapsed_time(s1))
+    # a 1,000-char request (the paper's Figure 10 starts at 1K chars)
+    t1k = synth.transcript(5, 1000, synth.PROFILE_MIXED)
+    d1k = torch.from_numpy(np.frombuffer(t1k, dtype=np.uint8).copy()).to(dev)
+    o1k = torch.tensor([0, len(t1k)], dtype=torch.int64, device=dev)
+    small = device_times(stream, flush, lambda: binding.tt_encode_batch_bounded(
+        tok.h, d1k, o1k, 1, len(t1k), out1, io1[0], stream), 50)
 
-    # small requests (the paper's Figure 10 quotes 1K chars): device time of a
-    # 1,000-char request and of the 64 KB tiny configuration, 50 calls each
-    # after one untimed call, L2 flushed before each
-    small = {}
-    for label, text in (("1k_chars", synth.transcript(5, 1000, synth.PROFILE_MIXED)),
-                        ("tiny_ascii_64k", synth.workload("tiny_ascii_64k")[0])):
-        dsm = torch.from_numpy(np.frombuffer(text, dtype=np.uint8).copy()).to(dev)
-        osm = torch.tensor([0, len(text)], dtype=torch.int64, device=dev)
-        tsm = []
-        for k in range(51):
-            flush.fill_(k)
-            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s0.record(stream)
-            binding.tt_encode_batch_bounded(tok.h, dsm, osm, 1, len(text), out_ids, out_off, stream)
-            s1.record(stream)
-            s1.synchronize()
-            if k:
-                tsm.append(s0.elapsed_time(s1))
-        small[label] = {"bytes": len(text), "p50_ms": float(np.percentile(tsm, 50)),
-                        "p99_ms": float(np.percentile(tsm, 99)), "vocab": "the main line's 100,000 merges"}
+    # ---------------- the other configurations
+    def single(name, h, calls=20):
+        """p50 / p99 device ms of one named single-request workload."""
+        text = synth.workload(name)[0]
+        ds = torch.from_numpy(np.frombuffer(text, dtype=np.uint8).copy()).to(dev)
+        os_ = torch.tensor([0, len(text)], dtype=torch.int64, device=dev)
+        oi = torch.empty(len(text), dtype=torch.int32, device=dev)
+        oo = torch.empty(2, dtype=torch.int64, device=dev)
+        t = device_times(stream, flush, lambda: binding.tt_encode_batch_bounded(
+            h, ds, os_, 1, len(text), oi, oo, stream), calls, warm=2)
+        st, _ = binding.tt_get_status(h, stream)
+        nt = int(oo[1].item())
+        return {"workload": name, "bytes": len(text), "tokens": nt, "p50_ms": pct(t, 50), "p99_ms": pct(t, 99),
+                "calls": calls, "status": st, "path_alg_bytes": alg_bytes(len(text), nt, 1)}
 
-    # end to end through host buffers (copies and the wait inside): each
-    # step's request sits in pinned host memory before the timed call, and
-    # its IDs come back into pinned host memory
-    pin_in = []
-    for h in host:
-        t_in = torch.empty(len(h), dtype=torch.uint8, pin_memory=True)
-        t_in.numpy()[:] = np.frombuffer(h, dtype=np.uint8)
-        pin_in.append(t_in)
-    pin_ids = torch.empty(max(len(h) for h in host) + 1, dtype=torch.int32, pin_memory=True)
-    pin_io = torch.empty(2, dtype=torch.int64, pin_memory=True)
-    ids_np, io_np = pin_ids.numpy(), pin_io.numpy()
-    e2e_t, h2d, d2h, e2e_tokens = [], 0, 0, []
-    for i, h in enumerate(host):
-        o_np = np.array([0, len(h)], dtype=np.int64)
-        t = time.perf_counter()
-        st = binding.tt_encode_host(tok.h, pin_in[i].numpy(), o_np, ids_np, io_np, stream)
-        e2e_t.append(time.perf_counter() - t)
-        assert st == 0
-        ids = ids_np[:int(io_np[-1])].copy()
-        e2e_tokens.append(int(io_np[-1]))
-        h2d += len(h) + o_np.nbytes
-        d2h += ids.nbytes + io_np.nbytes
+    def batched(name, h, calls=20):
+        """One named multi-request workload as one call: median of `calls`,
+        L2 flushed before each; and every request encoded alone."""
+        rq = synth.workload(name)
+        db, bb = synth.batch(rq)
+        dd = torch.from_numpy(db).to(dev)
+        oo = torch.from_numpy(bb).to(dev)
+        bi = torch.empty(len(db), dtype=torch.int32, device=dev)
+        bio = torch.empty(len(bb), dtype=torch.int64, device=dev)
+        t = device_times(stream, flush, lambda: binding.tt_encode_batch_bounded(
+            h, dd, oo, len(rq), len(db), bi, bio, stream), calls, warm=3)
+        st, _ = binding.tt_get_status(h, stream)
+        nt = int(bio[-1].item())
+        med = statistics.median(t)
+        return {"workload": name, "requests": len(rq), "bytes": len(db), "tokens": nt,
+                "value": len(db) / (med / 1e3) / 1e9, "unit": UNIT, "ms_median": med, "ms_p99": pct(t, 99),
+                "calls": calls, "status": st, "per_request_alone": per_request_alone(h, rq, dd, bb),
+                "path_alg_bytes": alg_bytes(len(db), nt, len(rq))}
+
+    others = {}
+    try:
+        others["adversarial_4_4m"] = single("adversarial_4_4m", tok.h)
+    except Exception as exc:  # reported, never fatal to the main line
+        others["adversarial_4_4m"] = {"error": str(exc)}
+    try:
+        (m0, v0, o0), f0 = vocab("tiny_ascii_64k")
+        t0k = binding.Tokenizer(m0, v0, o0, f0)
+        others["tiny_ascii_64k"] = dict(single("tiny_ascii_64k", t0k.h, 50), merges=len(m0))
+        t0k.close()
+    except Exception as exc:
+        others["tiny_ascii_64k"] = {"error": str(exc)}
+    try:
+        (m4, v4, o4), f4 = vocab("o200k_256_lognormal")
+        t4 = binding.Tokenizer(m4, v4, o4, f4)
+        others["o200k_batched"] = dict(batched("o200k_256_lognormal", t4.h), merges=len(m4),
+                                       pattern_family=FAMILY_NAMES[f4])
+        t4.close()
+    except Exception as exc:
+        others["o200k_batched"] = {"error": str(exc)}
+    if not args.no_families:
+        try:
+            (md, vd, od), fd = vocab("deepseek_64_loguniform")
+            td = binding.Tokenizer(md, vd, od, fd)
+            others["deepseek_batched"] = dict(batched("deepseek_64_loguniform", td.h), merges=len(md),
+                                              pattern_family=FAMILY_NAMES[fd])
+            td.close()
+        except Exception as exc:
+            others["deepseek_batched"] = {"error": str(exc)}
 
     if rank != 0:
+        tok.close()
         if world > 1:
             dist.barrier()
             dist.destroy_process_group()
         return
 
     peak, peak_kind = measured_peak_gbs()
-    per_kernel = {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]} for k, v in prof.items() if v[1]}
-    dominant = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_launch"])
-    # algorithmic bytes of the dominant kernel for the last step's request
-    last_ids = ids                                 # host IDs of the last e2e request (same input as step K)
-    classes = piece_classes(binding, tok, dev_in[-1], offs[-1], last_ids, vo, cap, dev)
-    flush.fill_(0)
-    binding.tt_profile(tok.h, 1)
-    encode(dev_in[-1], offs[-1])
-    last_prof = binding.tt_profile_read(tok.h)
-    binding.tt_profile(tok.h, 0)
-    dom_ms = last_prof[dominant][0] / max(last_prof[dominant][1], 1)
-    alg = alg_bytes(dominant, classes)
-    achieved = alg / (dom_ms / 1e3) / 1e9
-    mean_req_bytes = nbytes / args.steps
-    p_ms = np.array(step_ms)
-    p50_s = float(np.percentile(p_ms, 50)) / 1e3
-    path_alg = mean_req_bytes + 4 * (sum(e2e_tokens) / len(e2e_tokens)) + 16
+    per_kernel = {k: v[0] / max(v[1], 1) for k, v in prof.items() if v[1]}
+    dominant = max(per_kernel, key=per_kernel.get)
+    dom_ms = per_kernel[dominant]
+    alg = alg_bytes(len(data), tokens, n)
+    med_ms = statistics.median(step_ms)
+    lat_alg = float(np.mean(lat_bytes + 4 * lat_tokens + 16))
+    path = {WORKLOAD: {"alg_bytes": alg, "ms": med_ms, "frac": alg / (peak * 1e9 * med_ms / 1e3),
+                       "over": "median step"},
+            LATENCY_WORKLOAD: {"alg_bytes": lat_alg, "ms": pct(lat, 50),
+                               "frac": lat_alg / (peak * 1e9 * pct(lat, 50) / 1e3), "over": "p50 request"}}
+    for key in ("o200k_batched", "adversarial_4_4m"):
+        r = others.get(key, {})
+        ms = r.get("ms_median", r.get("p50_ms"))
+        if ms:
+            path[r["workload"]] = {"alg_bytes": r["path_alg_bytes"], "ms": ms,
+                                   "frac": r["path_alg_bytes"] / (peak * 1e9 * ms / 1e3),
+                                   "over": "median call" if "ms_median" in r else "p50 request"}
     line = {
         "metric": METRIC, "value": nbytes_all / device_s / 1e9, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": device_s / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
         "data": "synthetic",
-        "p50_ms": float(np.percentile(p_ms, 50)), "p99_ms": float(np.percentile(p_ms, 99)),
-        "config": {"workload": WORKLOAD, "requests_per_step": 1, "chars_per_request": 1_000_000,
-                   "bytes_per_request": mean_req_bytes, "pattern_family": "cl100k-style", "merges": len(merges),
-                   "protocol": "fresh sample: each step a different seeded request, graph replay, "
-                               "inputs resident in HBM",
-                   "l2": "flushed between steps by a 256 MiB write", "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "config": line_config(len(data), n, family, len(merges)),
+        "protocol": "each step one tt_encode_batch_bounded call over the whole batch (graph replay), inputs "
+                    "resident in HBM; L2 flushed between steps by a 256 MiB write; %s" % (
+                        "replicas: every rank encodes its own copy" if world > 1 else "1 GPU"),
+        "tokens_per_step": tokens,
+        "p50_ms_per_1m_char_request": pct(lat, 50),
+        "p99_ms_per_1m_char_request": pct(lat, 99),
         "gpu_launches": launches,
         "wall_s_timed_loop": wall,
-        "clocks": nclk.summary() if nclk.sm else clk.summary(),
-        "e2e": {"value": nbytes / sum(e2e_t) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d / args.steps,
-                "d2h_bytes_per_step": d2h / args.steps, "p50_ms": float(np.percentile(np.array(e2e_t) * 1e3, 50)),
-                "api": "tt_encode_host (pinned host buffers)"},
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
+        "clocks": clocks,
+        "e2e": {"value": len(data) * len(e2e_t) / sum(e2e_t) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": int(data.nbytes + bo.nbytes), "d2h_bytes_per_step": int(4 * tokens + bo.nbytes),
+                "p50_ms": pct(np.array(e2e_t) * 1e3, 50), "api": "tt_encode_host (pinned host buffers)"},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": alg / (dom_ms / 1e3) / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": alg / (dom_ms / 1e3) / 1e9 / peak, "peak_kind": peak_kind,
                      "traffic": recorded_traffic(dominant, WORKLOAD),
-                     "issue": issue_roofline(dominant, WORKLOAD, dom_ms,
-                                             (nclk.summary() if nclk.sm else clk.summary()).get("sm_mhz")),
                      "alg_bytes_per_launch": alg, "launch_ms": dom_ms,
-                     "path": {"alg_bytes_per_request": path_alg, "frac": path_alg / (peak * 1e9 * p50_s),
-                              "definition": "UTF-8 in + 4 bytes per ID out + 16 bytes of offsets, over the p50 "
-                                            "request time, against the same peak"},
-                     "timing": "CUDA events around the kernel on its stream, L2 flushed before the launch",
-                     "pieces": classes},
-        "kernels_ms_per_launch": {k: round(v["ms_per_launch"], 5) for k, v in per_kernel.items()},
-        "small_requests": small,
-        "steady_state": {"p50_ms": float(np.percentile(ss, 50)), "p99_ms": float(np.percentile(ss, 99)),
-                         "protocol": "one 1M-char request, 200 graph replays back to back, no L2 flush"},
+                     "definition": "per request: UTF-8 bytes in + 4 bytes per ID out + 16 bytes of offsets, "
+                                   "summed over the batch (every launch processes the whole batch), over the "
+                                   "dominant kernel's mean launch time",
+                     "issue": issue_roofline(dominant, WORKLOAD, dom_ms, clocks.get("sm_mhz")),
+                     "timing": "CUDA events around each kernel on its stream over the same steps, L2 flushed "
+                               "before each step",
+                     "path": path},
+        "kernels_ms_per_launch": {k: round(v, 5) for k, v in per_kernel.items()},
+        "per_request_alone": burst_alone,
+        "latency_1m": {"workload": LATENCY_WORKLOAD, "requests": len(lat), "p50_ms": pct(lat, 50),
+                       "p99_ms": pct(lat, 99), "mean_bytes": float(lat_bytes.mean()),
+                       "mean_tokens": float(lat_tokens.mean()),
+                       "protocol": "fresh sample: each timed request a different seeded sample, encoded once "
+                                   "after warm-up on other seeds; L2 flushed before each",
+                       "kernels_ms_per_launch": {k: round(v[0] / max(v[1], 1), 5) for k, v in prof1.items()
+                                                 if v[1]},
+                       "steady_state": {"p50_ms": pct(ss, 50), "p99_ms": pct(ss, 99),
+                                        "protocol": "one request, 200 graph replays back to back, no L2 flush"},
+                       "request_1k_chars": {"bytes": len(t1k), "p50_ms": pct(small, 50), "p99_ms": pct(small, 99)}},
     }
-    def batched(name, h):
-        """One named multi-request workload as one call: median of 50 calls,
-        L2 flushed before each; and every request encoded alone (after one
-        untimed call), for per-request p50 / p99."""
-        reqs = synth.workload(name)
-        data, bo = synth.batch(reqs)
-        d = torch.from_numpy(data).to(dev)
-        o = torch.from_numpy(bo).to(dev)
-        bi = torch.empty(len(data), dtype=torch.int32, device=dev)
-        bio = torch.empty(len(bo), dtype=torch.int64, device=dev)
-        for _ in range(3):
-            binding.tt_encode_batch_bounded(h, d, o, len(reqs), len(data), bi, bio, stream)
-        alone = []                                 # (each size bucket has its own workspace and graph)
-        for r in range(len(reqs)):
-            dr = d[int(bo[r]):int(bo[r + 1])]
-            orr = torch.tensor([0, int(bo[r + 1] - bo[r])], dtype=torch.int64, device=dev)
-            for k in range(2):
-                flush.fill_(k)
-                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                s.record(stream)
-                binding.tt_encode_batch_bounded(h, dr, orr, 1, len(dr), bi, bio, stream)
-                e.record(stream)
-                e.synchronize()
-            alone.append(s.elapsed_time(e))
-        ts = []
-        for i in range(50):
-            flush.fill_(i)
-            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s.record(stream)
-            binding.tt_encode_batch_bounded(h, d, o, len(reqs), len(data), bi, bio, stream)
-            e.record(stream)
-            e.synchronize()
-            ts.append(s.elapsed_time(e))
-        st, _ = binding.tt_get_status(h, stream)
-        return {"workload": name, "bytes": len(data), "value": len(data) / (statistics.median(ts) / 1e3) / 1e9,
-                "unit": UNIT, "ms_median": statistics.median(ts), "calls": len(ts), "status": st,
-                "per_request_alone": {"p50_ms": float(np.percentile(alone, 50)),
-                                      "p99_ms": float(np.percentile(alone, 99)), "requests": len(alone)}}
-
-    # the batched burst (~20 MB, 64 requests) as one call, for the batched part of the metric
-    try:
-        line["batched_gbs"] = batched("burst_64_loguniform", tok.h)
-    except Exception as exc:  # reported, never fatal to the main line
-        line["batched_gbs"] = {"error": str(exc)}
-    # the same shape of batch in the deepseek-style family (kana/CJK-mixed text)
-    if not args.no_families:
-        try:
-            Wd = synth.WORKLOADS["deepseek_64_loguniform"]
-            dtok = binding.Tokenizer(*synth.make_vocab(*Wd["vocab"]), Wd["family"])
-            line["deepseek_batched_gbs"] = batched("deepseek_64_loguniform", dtok.h)
-            dtok.close()
-        except Exception as exc:  # reported, never fatal to the main line
-            line["deepseek_batched_gbs"] = {"error": str(exc)}
+    line.update(others)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline((merges, vb, vo), family, list(range(1, 25)))
+        line["cpu_baseline"] = cpu_baseline((merges, vb, vo), family, seeds)
     print(json.dumps(line), flush=True)
     tok.close()
     if world > 1:
