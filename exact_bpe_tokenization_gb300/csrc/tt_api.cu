@@ -182,20 +182,22 @@ static tt_status upload_vocab(tt_tokenizer *h, const uint8_t *lb, const int64_t 
     voff[(size_t)i + 1] = (int32_t)bytes.size();
   }
   const uint64_t vcap = next_pow2((uint64_t)std::max<int64_t>(2 * (h->n_vocab + n), 1024));
-  std::vector<uint64_t> vtab(vcap, 0);
+  std::vector<uint4> vtab(vcap, make_uint4(0, 0, 0, 0));
   auto insert = [&](int64_t id) {
     const int len = voff[(size_t)id + 1] - voff[(size_t)id];
-    const uint64_t hh = hash_bytes(bytes.data() + voff[(size_t)id], len);
-    uint64_t sl = hh & (vcap - 1);
-    while (vtab[sl] != 0) sl = (sl + 1) & (vcap - 1);
-    vtab[sl] = ((uint64_t)vocab_fp(hh) << 32) | ((uint64_t)len << 20) | (uint64_t)id;
+    const uint8_t *b = bytes.data() + voff[(size_t)id];
+    uint64_t sl = hash_bytes(b, len) & (vcap - 1);
+    while (vtab[sl].w != 0) sl = (sl + 1) & (vcap - 1);
+    uint32_t e[4];
+    vocab_entry(b, len, (int)id, e);
+    vtab[sl] = make_uint4(e[0], e[1], e[2], e[3]);
   };
   for (int64_t k = 0; k < n; ++k) insert(ids[k]);
   for (int64_t i = 0; i < h->n_vocab; ++i) insert(i);
   void *p;
   tt_status s;
-  if ((s = upload(h, vtab.data(), vtab.size() * 8, &p)) != TT_OK) return s;
-  h->T.vocab_tab = (const uint64_t *)p;
+  if ((s = upload(h, vtab.data(), vtab.size() * sizeof(uint4), &p)) != TT_OK) return s;
+  h->T.vocab_tab = (const uint4 *)p;
   h->T.vocab_mask = (uint32_t)(vcap - 1);
   if ((s = upload(h, bytes.data(), bytes.size(), &p)) != TT_OK) return s;
   h->T.vbytes = (const uint8_t *)p;
@@ -293,6 +295,25 @@ extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, con
   h->T.pair_mask = (uint32_t)(pcap - 1);
   if ((s = upload(h, result.data(), result.size() * 4, &p)) != TT_OK) return fail(s);
   h->T.merge_result = (const int32_t *)p;
+  // ---- the staged table of the lowest ranks (shared memory of the warp BPE kernel)
+  {
+    const int64_t hot_k = std::min<int64_t>(n_merges, HOT_MAX);
+    std::vector<uint64_t> hot(HOT_SLOTS, HOT_EMPTY);
+    std::vector<int32_t> hot_res(HOT_MAX, 0);
+    for (int64_t k = 0; k < hot_k; ++k) {
+      const uint32_t l = (uint32_t)merge_pairs[2 * k], r = (uint32_t)merge_pairs[2 * k + 1];
+      uint32_t sl = hot_slot(l, r);
+      while (hot[sl] != HOT_EMPTY) sl = (sl + 1) & (HOT_SLOTS - 1);
+      hot[sl] = hot_key(l, r) | (uint64_t)k;
+      hot_res[(size_t)k] = result[(size_t)k];
+    }
+    if ((s = upload(h, hot.data(), hot.size() * 8, &p)) != TT_OK) return fail(s);
+    h->T.hot_tab = (const uint64_t *)p;
+    if ((s = upload(h, hot_res.data(), hot_res.size() * 4, &p)) != TT_OK) return fail(s);
+    h->T.hot_res = (const int32_t *)p;
+    h->T.hot_k = (int32_t)hot_k;
+    h->T.n_merges = (int32_t)n_merges;
+  }
   if ((s = upload_vocab(h, nullptr, nullptr, nullptr, 0)) != TT_OK) return fail(s);
   if ((s = upload(h, byte_id.data(), 256 * 4, &p)) != TT_OK) return fail(s);
   h->T.byte_id = (const int32_t *)p;

@@ -45,9 +45,13 @@ __device__ __forceinline__ void set_status(DevStatus *st, int code) { atomicCAS(
 
 // ------------------------------------------------------------ tables
 // pair table entry (16 bytes): {left, right, rank, result}; empty: left = ~0
-// vocab table entry: fp << 32 | len << 20 | id ; empty = 0
+// whole-piece (vocabulary) table entry (16 bytes): the token's first
+// VOCAB_INLINE bytes (little-endian words x, y, z, zero padded) and
+// w = len << 20 | id; empty: w = 0 (no token is empty).  A probe of a piece
+// of at most VOCAB_INLINE bytes reads one entry per slot and nothing else.
 constexpr uint32_t PAIR_EMPTY = 0xFFFFFFFFu;
 constexpr int MAX_VOCAB_BITS = 20;
+constexpr int VOCAB_INLINE = 12;
 constexpr int MAX_RANK_BITS = 24;
 
 struct Tables {
@@ -55,8 +59,12 @@ struct Tables {
   const uint8_t *cls2;        // block * 256 + (cp & 255) -> raw kind (K_*)
   const uint4 *pair_tab;       // {left, right, rank, result}
   uint32_t pair_mask;
+  const uint64_t *hot_tab;     // [HOT_SLOTS] the staged table of the HOT_MAX lowest ranks (see below)
+  const int32_t *hot_res;      // [HOT_MAX] merge result of each staged rank
+  int32_t hot_k;               // merges staged: min(HOT_MAX, merges)
+  int32_t n_merges;
   const int32_t *merge_result;
-  const uint64_t *vocab_tab;
+  const uint4 *vocab_tab;
   uint32_t vocab_mask;
   const uint8_t *vbytes;
   const int32_t *voff;
@@ -73,6 +81,19 @@ struct Tables {
 constexpr int LIT_MAX_LEN = 255;       // bytes of one literal
 constexpr int LIT_MAX_COUNT = 4095;    // literals (12-bit index)
 enum : uint8_t { LIT_SEG = 1, LIT_INNER = 2 };   // per-byte marks of taken literals
+
+// The staged pair table: the merges of the HOT_MAX lowest ranks (those most
+// rounds take) in an open-addressing table of HOT_SLOTS 8-byte entries
+// left << 44 | right << 24 | rank (load factor <= 1/2, linear probing; empty
+// = all ones, which no entry equals since rank < 2^24 - 1), copied into
+// shared memory by every CTA of the warp BPE kernel.
+constexpr int HOT_BITS = 13;
+constexpr int HOT_SLOTS = 1 << HOT_BITS;
+constexpr int HOT_MAX = HOT_SLOTS / 2;
+constexpr uint64_t HOT_EMPTY = ~0ull;
+static_assert(HOT_SLOTS >= 2 * HOT_MAX, "load factor <= 1/2");
+TT_HD uint32_t hot_slot(uint32_t l, uint32_t r) { return (l * 0x9E3779B1u ^ r * 0x85EBCA77u) >> (32 - HOT_BITS); }
+TT_HD uint64_t hot_key(uint32_t l, uint32_t r) { return ((uint64_t)l << 44) | ((uint64_t)r << 24); }
 
 TT_HD uint64_t mix64(uint64_t x) {
   x ^= x >> 33; x *= 0xff51afd7ed558ccdull;
@@ -108,7 +129,12 @@ TT_HD uint64_t hash_bytes(const uint8_t *b, int len) {
   }
   return bh.fin();
 }
-TT_HD uint32_t vocab_fp(uint64_t h) { uint32_t f = (uint32_t)(h >> 32); return f ? f : 1u; }
+// the whole-piece table entry of a token (len >= 1)
+TT_HD void vocab_entry(const uint8_t *b, int len, int id, uint32_t out[4]) {
+  out[0] = out[1] = out[2] = 0;
+  for (int i = 0; i < len && i < VOCAB_INLINE; ++i) out[i / 4] |= (uint32_t)b[i] << (8 * (i % 4));
+  out[3] = ((uint32_t)len << MAX_VOCAB_BITS) | (uint32_t)id;
+}
 
 #if defined(__CUDACC__)
 // (rank, result) of the pair (l, r); rank -1 if (l, r) is not a merge
@@ -137,13 +163,6 @@ __device__ __forceinline__ uint64_t load8(const uint8_t *p, int avail) {
   return v;
 }
 
-// hash_bytes() of len bytes at p (global memory), from 8-byte loads
-__device__ __forceinline__ uint64_t hash_global(const uint8_t *p, int len) {
-  ByteHash bh;
-  bh.init(len);
-  for (int i = 0; i < len; i += 8) bh.word(load8(p + i, len - i));
-  return bh.fin();
-}
 
 // ------------------------------------------------------------ memory order
 __device__ __forceinline__ int ld_acquire(const int *p) {
