@@ -295,25 +295,6 @@ extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, con
   h->T.pair_mask = (uint32_t)(pcap - 1);
   if ((s = upload(h, result.data(), result.size() * 4, &p)) != TT_OK) return fail(s);
   h->T.merge_result = (const int32_t *)p;
-  // ---- the staged table of the lowest ranks (shared memory of the warp BPE kernel)
-  {
-    const int64_t hot_k = std::min<int64_t>(n_merges, HOT_MAX);
-    std::vector<uint64_t> hot(HOT_SLOTS, HOT_EMPTY);
-    std::vector<int32_t> hot_res(HOT_MAX, 0);
-    for (int64_t k = 0; k < hot_k; ++k) {
-      const uint32_t l = (uint32_t)merge_pairs[2 * k], r = (uint32_t)merge_pairs[2 * k + 1];
-      uint32_t sl = hot_slot(l, r);
-      while (hot[sl] != HOT_EMPTY) sl = (sl + 1) & (HOT_SLOTS - 1);
-      hot[sl] = hot_key(l, r) | (uint64_t)k;
-      hot_res[(size_t)k] = result[(size_t)k];
-    }
-    if ((s = upload(h, hot.data(), hot.size() * 8, &p)) != TT_OK) return fail(s);
-    h->T.hot_tab = (const uint64_t *)p;
-    if ((s = upload(h, hot_res.data(), hot_res.size() * 4, &p)) != TT_OK) return fail(s);
-    h->T.hot_res = (const int32_t *)p;
-    h->T.hot_k = (int32_t)hot_k;
-    h->T.n_merges = (int32_t)n_merges;
-  }
   if ((s = upload_vocab(h, nullptr, nullptr, nullptr, 0)) != TT_OK) return fail(s);
   if ((s = upload(h, byte_id.data(), 256 * 4, &p)) != TT_OK) return fail(s);
   h->T.byte_id = (const int32_t *)p;

@@ -71,48 +71,6 @@ __device__ __forceinline__ uint32_t pair_slot(const Tables &T, int l, int r) {
   return (uint32_t)pair_hash((uint32_t)l, (uint32_t)r) & T.pair_mask;
 }
 
-// ---------------------------------------------------------------- rank codes
-// The merge loops of the warp kernel carry, per adjacent pair, a rank code:
-// 2 * rank for a merge, RC_NONE for a pair that is no merge, and H.unk =
-// 2 * hot_k - 1 for a pair the staged table (shared memory) lacks that has
-// not been looked up in the global table yet -- a merge of rank >= hot_k, or
-// none.  H.unk sorts above every staged rank and below every other one, so
-// a round's minimum code is exact unless it is H.unk; then the unknown pairs
-// are looked up in the global table, all at once, and the round starts over.
-// While the round's rank is staged (code < H.k2), the pairs a merge creates
-// are looked up in shared memory only: an absent one gets H.unk.  Once the
-// round's rank is above the staged ones, so are those of every pair a merge
-// creates (a well-ordered list), and they go to the global table directly --
-// so a piece resolves its unknown pairs at most once.  When every merge is
-// staged, a pair missing from the table is no merge: H.unk = RC_NONE.
-constexpr int RC_NONE = INT_MAX;
-struct HotView {
-  const uint64_t *slots;   // shared memory, HOT_SLOTS entries
-  const int32_t *res;      // shared memory, HOT_MAX results
-  int unk;                 // code of an unknown pair (RC_NONE when every merge is staged)
-  int k2;                  // codes below k2 are staged ranks
-};
-
-// (code, result) of the pair (l, r) in the staged table
-__device__ __forceinline__ int2 hot_lookup(const HotView &H, int l, int r) {
-  const uint64_t key = hot_key((uint32_t)l, (uint32_t)r);
-  uint32_t s = hot_slot((uint32_t)l, (uint32_t)r);
-  for (;;) {
-    const uint64_t e = H.slots[s];
-    if (e == HOT_EMPTY) return make_int2(H.unk, 0);
-    if ((e & ~0xFFFFFFull) == key) {
-      const int k = (int)(e & 0xFFFFFFu);
-      return make_int2(2 * k, H.res[k]);
-    }
-    s = (s + 1) & (HOT_SLOTS - 1);
-  }
-}
-__device__ __forceinline__ int2 code_of(int2 pr) { return make_int2(pr.x < 0 ? RC_NONE : 2 * pr.x, pr.y); }
-// (code, result) of a pair made by a merge of code rc
-__device__ __forceinline__ int2 pair_code(const Tables &T, const HotView &H, int rc, int l, int r) {
-  return rc < H.k2 ? hot_lookup(H, l, r) : code_of(pair_lookup(T, l, r));
-}
-
 // Round merging of up to 32 / G pieces of at most G bytes at once, G lanes
 // per piece and one symbol per lane: lane p of a group holds the symbol that
 // starts at byte p (while alive), the rank and result of the pair it starts
@@ -124,8 +82,7 @@ __device__ __forceinline__ int2 pair_code(const Tables &T, const HotView &H, int
 // part; a group with len 0 idles.  Writes the group's IDs to out[0..] and
 // returns their count (on every lane of the group).
 template <int G>
-__device__ __forceinline__ int bpe_lanes(const Tables &T, const HotView &H, const uint8_t *bytes, int len,
-                                         int32_t *out) {
+__device__ __forceinline__ int bpe_lanes(const Tables &T, const uint8_t *bytes, int len, int32_t *out) {
   constexpr unsigned FULL = 0xffffffffu;
   constexpr unsigned GM = G == 32 ? FULL : ((1u << G) - 1);
   const int lane = threadIdx.x & 31;
@@ -134,52 +91,38 @@ __device__ __forceinline__ int bpe_lanes(const Tables &T, const HotView &H, cons
   bool alive = p < len;
   int tok = alive ? __ldg(&T.byte_id[__ldg(bytes + p)]) : -1;
   const int tn0 = __shfl_down_sync(FULL, tok, 1);
-  int rank = RC_NONE, res = 0;
+  int rank = INT_MAX, res = 0;
   if (p + 1 < len) {
-    const int2 pr = hot_lookup(H, tok, tn0);
-    rank = pr.x;
+    const int2 pr = pair_lookup(T, tok, tn0);
+    rank = rank_or_max(pr.x);
     res = pr.y;
   }
-  // each round of a group unlinks at least one symbol, or resolves its
-  // unknown pairs (at most once): len <= G rounds
-  for (int round = 0; round < G; ++round) {
+  for (int round = 0; round < G; ++round) {   // each round unlinks at least one symbol
     int r = rank;
 #pragma unroll
     for (int d = G / 2; d >= 1; d >>= 1) r = min(r, __shfl_xor_sync(FULL, r, d));
-    if (__all_sync(FULL, r == RC_NONE)) break;
-    const bool resolve = r != RC_NONE && r == H.unk;   // the same on every lane of a group
-    if (__any_sync(FULL, resolve)) {           // such groups look their unknown pairs up and merge nothing
-      const unsigned am = (__ballot_sync(FULL, alive) >> sh) & GM;
-      const unsigned hi = am & above_me;
-      const int tn = __shfl_sync(FULL, tok, sh + (hi ? __ffs(hi) - 1 : p));
-      if (resolve && alive && rank == H.unk) { // (an unknown pair has a right neighbour)
-        const int2 pr = code_of(pair_lookup(T, tok, tn));
-        rank = pr.x;
-        res = pr.y;
-      }
-      if (resolve) r = RC_NONE;
-    }
+    if (__all_sync(FULL, r == INT_MAX)) break;
     for (int step = 0; step < G; ++step) {
       const unsigned am = (__ballot_sync(FULL, alive) >> sh) & GM;
       const unsigned lo = am & below;
       const int pvl = lo ? 31 - __clz(lo) : -1;
-      const bool hit = alive && rank == r && r != RC_NONE;
+      const bool hit = alive && rank == r && r != INT_MAX;
       const unsigned hm = (__ballot_sync(FULL, hit) >> sh) & GM;
       const bool sel = hit && !(pvl >= 0 && ((hm >> pvl) & 1u));
       const unsigned sm = (__ballot_sync(FULL, sel) >> sh) & GM;
       const bool pending = hit && !sel;
       if (sel) tok = res;
-      if (alive && pvl >= 0 && ((sm >> pvl) & 1u)) { alive = false; rank = RC_NONE; }
+      if (alive && pvl >= 0 && ((sm >> pvl) & 1u)) { alive = false; rank = INT_MAX; }
       const unsigned am2 = (__ballot_sync(FULL, alive) >> sh) & GM;
       const unsigned hi = am2 & above_me;
       const int nxl = hi ? __ffs(hi) - 1 : -1;
       const int tn = __shfl_sync(FULL, tok, sh + (nxl < 0 ? p : nxl));
       if (alive && (sel || (nxl >= 0 && ((sm >> nxl) & 1u)))) {
         if (nxl < 0) {
-          rank = RC_NONE;
+          rank = INT_MAX;
         } else {
-          const int2 pr = pair_code(T, H, r, tok, tn);
-          rank = pr.x;
+          const int2 pr = pair_lookup(T, tok, tn);
+          rank = rank_or_max(pr.x);
           res = pr.y;
         }
       }
@@ -226,8 +169,8 @@ __device__ __forceinline__ void put_count(const Work &W, int k, int c) {
   if (c) atomicAdd(&W.ids_agg[k / IDS_CHUNK], c);
 }
 
-__device__ __forceinline__ void small_chunk(const Tables &T, const HotView &H, const Work &W, const uint8_t *g,
-                                            int64_t total, int np, int kb) {
+__device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, const uint8_t *g, int64_t total,
+                                            int np, int kb) {
   const int lane = threadIdx.x & 31;
   const int k = kb + lane;
   int32_t s = 0;
@@ -276,7 +219,7 @@ __device__ __forceinline__ void small_chunk(const Tables &T, const HotView &H, c
     const int ps = __shfl_sync(0xffffffffu, s, src < 0 ? la : src);
     int pl = __shfl_sync(0xffffffffu, len, src < 0 ? la : src);
     if (src < 0) pl = 0;
-    const int cnt = bpe_lanes<16>(T, H, g + ps, pl, W.scratch + ps);
+    const int cnt = bpe_lanes<16>(T, g + ps, pl, W.scratch + ps);
     if ((lane & 15) == 0 && src >= 0) { W.n_ids[kb + src] = cnt; mine += cnt; }
   }
   // the chunk's pieces of at most SMALL_MAX bytes, all in one ID chunk
@@ -285,84 +228,61 @@ __device__ __forceinline__ void small_chunk(const Tables &T, const HotView &H, c
   if (lane == 0 && mine) atomicAdd(&W.ids_agg[kb / IDS_CHUNK], mine);
 }
 
-// Look up, in the global table, the pairs with an unknown code among
-// positions base, base + stride, ... (NS of them) of a linked list: first
-// probes of all of them in flight together.
-template <int NS>
-__device__ __forceinline__ void resolve_unknown(const Tables &T, const HotView &H, int n, int base, int stride,
-                                                const int32_t *tok, int32_t *rank, int32_t *res, const int16_t *nx) {
-  uint4 ent[NS];
-  uint32_t sl[NS];
-  int lt[NS], rt[NS];
-  bool v[NS];
-#pragma unroll
-  for (int k = 0; k < NS; ++k) {
-    const int p = base + stride * k;
-    v[k] = p < n && rank[p] == H.unk;            // (an unknown pair has a right neighbour)
-    lt[k] = v[k] ? tok[p] : 0;
-    rt[k] = v[k] ? tok[nx[p]] : 0;
-    sl[k] = pair_slot(T, lt[k], rt[k]);
-    ent[k] = v[k] ? __ldg(&T.pair_tab[sl[k]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-  }
-#pragma unroll
-  for (int k = 0; k < NS; ++k) {
-    if (v[k]) {
-      const int p = base + stride * k;
-      const int2 pr = code_of(pair_finish(T, ent[k], sl[k], lt[k], rt[k]));
-      rank[p] = pr.x;
-      res[p] = pr.y;
-    }
-  }
-}
-
 // The linked-list rounds of one piece of n bytes (32 < n <= 32 * NS) in the
 // warp's shared arrays, NS positions per lane (lane l owns l, l + 32, ...);
-// writes the IDs to out and returns their count.  The codes of a lane's own
+// writes the IDs to out and returns their count.  The ranks of a lane's own
 // positions are read once per step into registers.
 template <int NS>
-__device__ __forceinline__ int list_rounds(const Tables &T, const HotView &H, const uint8_t *b, int n, int32_t *out,
-                                           int32_t *tok, int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
+__device__ __forceinline__ int list_rounds(const Tables &T, const uint8_t *b, int n, int32_t *out, int32_t *tok,
+                                           int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
   const int lane = threadIdx.x & 31;
   const unsigned lt_mask = (1u << lane) - 1;
 #pragma unroll
   for (int k = 0; k < NS; ++k) {
     const int p = lane + 32 * k;
     tok[p] = p < n ? __ldg(&T.byte_id[__ldg(b + p)]) : -1;
-    rank[p] = RC_NONE;
+    rank[p] = INT_MAX;
     nx[p] = (int16_t)(p + 1);
     pv[p] = (int16_t)(p - 1);
   }
   __syncwarp();
-  // initial pair codes from the staged table
+  // initial pair lookups, first probes of all slots in flight together
+  {
+    uint4 ent[NS];
+    uint32_t sl[NS];
+    int lt[NS], rt[NS];
 #pragma unroll
-  for (int k = 0; k < NS; ++k) {
-    const int p = lane + 32 * k;
-    if (p + 1 < n) {
-      const int2 pr = hot_lookup(H, tok[p], tok[p + 1]);
-      rank[p] = pr.x;
-      res[p] = pr.y;
+    for (int k = 0; k < NS; ++k) {
+      const int p = lane + 32 * k;
+      const bool v = p + 1 < n;
+      lt[k] = v ? tok[p] : 0;
+      rt[k] = v ? tok[p + 1] : 0;
+      sl[k] = pair_slot(T, lt[k], rt[k]);
+      ent[k] = v ? __ldg(&T.pair_tab[sl[k]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      const int p = lane + 32 * k;
+      if (p + 1 < n) {
+        const int2 pr = pair_finish(T, ent[k], sl[k], lt[k], rt[k]);
+        rank[p] = rank_or_max(pr.x);
+        res[p] = pr.y;
+      }
     }
   }
   __syncwarp();
-  // each round unlinks at least one symbol, or resolves the unknown pairs
-  // (at most once): n rounds suffice
-  for (int round = 0; round < n; ++round) {
+  for (int round = 0; round < n; ++round) {   // each round unlinks at least one symbol
     int rr[NS];
-    int lm = RC_NONE;
+    int lm = INT_MAX;
 #pragma unroll
     for (int k = 0; k < NS; ++k) {
       rr[k] = rank[lane + 32 * k];
       lm = min(lm, rr[k]);
     }
     const int r = __reduce_min_sync(0xffffffffu, lm);
-    if (r == RC_NONE) break;
-    if (r == H.unk) {
-      resolve_unknown<NS>(T, H, n, lane, 32, tok, rank, res, nx);
-      __syncwarp();
-      continue;
-    }
+    if (r == INT_MAX) break;
     for (int step = 0; step < n; ++step) {
-      if (step > 0) {                         // codes changed in the previous step
+      if (step > 0) {                         // ranks changed in the previous step
 #pragma unroll
         for (int k = 0; k < NS; ++k) rr[k] = rank[lane + 32 * k];
       }
@@ -382,47 +302,29 @@ __device__ __forceinline__ int list_rounds(const Tables &T, const HotView &H, co
         const int q = nx[p], nq = nx[q];
         tok[p] = res[p];
         tok[q] = -1;
-        rank[q] = RC_NONE;
-        rank[p] = RC_NONE;
+        rank[q] = INT_MAX;
+        rank[p] = INT_MAX;
         nx[p] = (int16_t)nq;
         if (nq < n) pv[nq] = (int16_t)p;
       }
       __syncwarp();
-      if (r < H.k2) {                         // staged rank: the new pairs from shared memory
-        for (uint32_t m = sel; m; m &= m - 1) {
-          const int p = lane + 32 * (__ffs(m) - 1);
-          const int a = pv[p], c = nx[p];
-          const int tp = tok[p];
-          if (a >= 0) {
-            const int2 pr = hot_lookup(H, tok[a], tp);
-            rank[a] = pr.x;
-            res[a] = pr.y;
-          }
-          if (c < n) {
-            const int2 pr = hot_lookup(H, tp, tok[c]);
-            rank[p] = pr.x;
-            res[p] = pr.y;
-          }
+      for (uint32_t m = sel; m; m &= m - 1) {
+        const int p = lane + 32 * (__ffs(m) - 1);
+        const int a = pv[p], c = nx[p];
+        const int tp = tok[p];
+        const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
+        const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
+        const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+        const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+        if (a >= 0) {
+          const int2 pr = pair_finish(T, ea, sa, ta, tp);
+          rank[a] = rank_or_max(pr.x);
+          res[a] = pr.y;
         }
-      } else {                                // from the global table, both probes in flight together
-        for (uint32_t m = sel; m; m &= m - 1) {
-          const int p = lane + 32 * (__ffs(m) - 1);
-          const int a = pv[p], c = nx[p];
-          const int tp = tok[p];
-          const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
-          const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
-          const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-          const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-          if (a >= 0) {
-            const int2 pr = code_of(pair_finish(T, ea, sa, ta, tp));
-            rank[a] = pr.x;
-            res[a] = pr.y;
-          }
-          if (c < n) {
-            const int2 pr = code_of(pair_finish(T, ec, sc, tp, tc));
-            rank[p] = pr.x;
-            res[p] = pr.y;
-          }
+        if (c < n) {
+          const int2 pr = pair_finish(T, ec, sc, tp, tc);
+          rank[p] = rank_or_max(pr.x);
+          res[p] = pr.y;
         }
       }
       __syncwarp();
@@ -453,8 +355,8 @@ __device__ __forceinline__ int list_rounds(const Tables &T, const HotView &H, co
 // NS: positions per lane (pieces of at most G * NS bytes).
 constexpr int PAIR_MAX = MID_MAX / 2;
 template <int G, int NS>
-__device__ __forceinline__ int group_rounds(const Tables &T, const HotView &H, const uint8_t *b, int n, int32_t *out,
-                                            int32_t *tok, int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
+__device__ __forceinline__ int group_rounds(const Tables &T, const uint8_t *b, int n, int32_t *out, int32_t *tok,
+                                            int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
   static_assert(G * NS <= MID_MAX * G / 32, "a group's share of the arrays");
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int SHARE = MID_MAX * G / 32;
@@ -464,39 +366,47 @@ __device__ __forceinline__ int group_rounds(const Tables &T, const HotView &H, c
   for (int k = 0; k < NS; ++k) {
     const int p = hl + G * k;
     tok[p] = p < n ? __ldg(&T.byte_id[__ldg(b + p)]) : -1;
-    rank[p] = RC_NONE;
+    rank[p] = INT_MAX;
     nx[p] = (int16_t)(p + 1);
     pv[p] = (int16_t)(p - 1);
   }
   __syncwarp();
 #pragma unroll
-  for (int k = 0; k < NS; ++k) {              // initial pair codes from the staged table
-    const int p = hl + G * k;
-    if (p + 1 < n) {
-      const int2 pr = hot_lookup(H, tok[p], tok[p + 1]);
-      rank[p] = pr.x;
-      res[p] = pr.y;
+  for (int k0 = 0; k0 < NS; k0 += 4) {        // initial lookups, four first probes in flight at a time
+    uint4 ent[4];
+    uint32_t sl[4];
+    int lt[4], rt[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int p = hl + G * (k0 + k);
+      const bool v = k0 + k < NS && p + 1 < n;
+      lt[k] = v ? tok[p] : 0;
+      rt[k] = v ? tok[p + 1] : 0;
+      sl[k] = pair_slot(T, lt[k], rt[k]);
+      ent[k] = v ? __ldg(&T.pair_tab[sl[k]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int p = hl + G * (k0 + k);
+      if (k0 + k < NS && p + 1 < n) {
+        const int2 pr = pair_finish(T, ent[k], sl[k], lt[k], rt[k]);
+        rank[p] = rank_or_max(pr.x);
+        res[p] = pr.y;
+      }
     }
   }
   __syncwarp();
-  // a group's round unlinks at least one symbol or resolves its unknown
-  // pairs (at most once): n <= SHARE rounds
-  for (int round = 0; round < SHARE; ++round) {
+  for (int round = 0; round < SHARE; ++round) {      // a group with pairs unlinks at least one symbol a round
     int rr[NS];
-    int r = RC_NONE;
+    int r = INT_MAX;
 #pragma unroll
     for (int k = 0; k < NS; ++k) {
       rr[k] = rank[hl + G * k];
       r = min(r, rr[k]);
     }
 #pragma unroll
-    for (int d = G / 2; d >= 1; d >>= 1) r = min(r, __shfl_xor_sync(FULL, r, d));   // my group's lowest code
-    if (__all_sync(FULL, r == RC_NONE)) break;
-    if (r != RC_NONE && r == H.unk) {         // this group looks its unknown pairs up and merges nothing
-      resolve_unknown<NS>(T, H, n, hl, G, tok, rank, res, nx);
-      r = RC_NONE;
-    }
-    __syncwarp();
+    for (int d = G / 2; d >= 1; d >>= 1) r = min(r, __shfl_xor_sync(FULL, r, d));   // my group's lowest rank
+    if (__all_sync(FULL, r == INT_MAX)) break;
     for (int step = 0; step < SHARE; ++step) {      // (a bound the same on every lane: the loop holds warp votes)
       if (step > 0) {
 #pragma unroll
@@ -506,7 +416,7 @@ __device__ __forceinline__ int group_rounds(const Tables &T, const HotView &H, c
       bool left = false;
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
-        if (r != RC_NONE && rr[k] == r) {
+        if (r != INT_MAX && rr[k] == r) {
           const int q = pv[hl + G * k];
           if (q < 0 || rank[q] != r) sel |= 1u << k;
           else left = true;
@@ -518,47 +428,29 @@ __device__ __forceinline__ int group_rounds(const Tables &T, const HotView &H, c
         const int q = nx[p], nq = nx[q];
         tok[p] = res[p];
         tok[q] = -1;
-        rank[q] = RC_NONE;
-        rank[p] = RC_NONE;
+        rank[q] = INT_MAX;
+        rank[p] = INT_MAX;
         nx[p] = (int16_t)nq;
         if (nq < n) pv[nq] = (int16_t)p;
       }
       __syncwarp();
-      if (r < H.k2) {                         // staged rank: the new pairs from shared memory
-        for (uint32_t m = sel; m; m &= m - 1) {
-          const int p = hl + G * (__ffs(m) - 1);
-          const int a = pv[p], c = nx[p];
-          const int tp = tok[p];
-          if (a >= 0) {
-            const int2 pr = hot_lookup(H, tok[a], tp);
-            rank[a] = pr.x;
-            res[a] = pr.y;
-          }
-          if (c < n) {
-            const int2 pr = hot_lookup(H, tp, tok[c]);
-            rank[p] = pr.x;
-            res[p] = pr.y;
-          }
+      for (uint32_t m = sel; m; m &= m - 1) {
+        const int p = hl + G * (__ffs(m) - 1);
+        const int a = pv[p], c = nx[p];
+        const int tp = tok[p];
+        const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
+        const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
+        const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+        const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+        if (a >= 0) {
+          const int2 pr = pair_finish(T, ea, sa, ta, tp);
+          rank[a] = rank_or_max(pr.x);
+          res[a] = pr.y;
         }
-      } else {
-        for (uint32_t m = sel; m; m &= m - 1) {
-          const int p = hl + G * (__ffs(m) - 1);
-          const int a = pv[p], c = nx[p];
-          const int tp = tok[p];
-          const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
-          const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
-          const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-          const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-          if (a >= 0) {
-            const int2 pr = code_of(pair_finish(T, ea, sa, ta, tp));
-            rank[a] = pr.x;
-            res[a] = pr.y;
-          }
-          if (c < n) {
-            const int2 pr = code_of(pair_finish(T, ec, sc, tp, tc));
-            rank[p] = pr.x;
-            res[p] = pr.y;
-          }
+        if (c < n) {
+          const int2 pr = pair_finish(T, ec, sc, tp, tc);
+          rank[p] = rank_or_max(pr.x);
+          res[p] = pr.y;
         }
       }
       __syncwarp();
@@ -583,9 +475,9 @@ __device__ __forceinline__ int group_rounds(const Tables &T, const HotView &H, c
 // first .. first + 32 / G - 1 of a list of n_list pieces (past n_list: none): each
 // group probes its piece whole, then the misses merge side by side.
 template <int G, int NS>
-__device__ __forceinline__ void mid_group(const Tables &T, const HotView &H, const Work &W, const uint8_t *g,
-                                          const int32_t *list, int first, int n_list, int32_t *tok, int32_t *rank,
-                                          int32_t *res, int16_t *nx, int16_t *pv) {
+__device__ __forceinline__ void mid_group(const Tables &T, const Work &W, const uint8_t *g, const int32_t *list,
+                                          int first, int n_list, int32_t *tok, int32_t *rank, int32_t *res,
+                                          int16_t *nx, int16_t *pv) {
   const int lane = threadIdx.x & 31, grp = lane / G, gl = lane % G;
   const int pc = first + grp < n_list ? __ldcg(&list[first + grp]) : -1;
   int32_t s = 0;
@@ -603,14 +495,13 @@ __device__ __forceinline__ void mid_group(const Tables &T, const HotView &H, con
     n = 0;                                    // this group idles
   }
   const int off = grp * (MID_MAX * G / 32);
-  const int cnt = group_rounds<G, NS>(T, H, b, n, W.scratch + s, tok + off, rank + off, res + off, nx + off,
-                                      pv + off);
+  const int cnt = group_rounds<G, NS>(T, b, n, W.scratch + s, tok + off, rank + off, res + off, nx + off, pv + off);
   if (gl == 0 && n > 0) put_count(W, pc, cnt);
   __syncwarp();
 }
 
-__device__ __forceinline__ void mid_piece(const Tables &T, const HotView &H, const Work &W, const uint8_t *g, int pc,
-                                          int32_t *tok, int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
+__device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const uint8_t *g, int pc, int32_t *tok,
+                                          int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
   const int lane = threadIdx.x & 31;
   const int32_t s = __ldcg(&W.piece_start[pc]);
   const int32_t e = __ldcg(&W.piece_start[pc + 1]) & 0x7FFFFFFF;
@@ -626,19 +517,19 @@ __device__ __forceinline__ void mid_piece(const Tables &T, const HotView &H, con
     }
   }
   if (n <= 32) {                              // one symbol per lane, state in registers
-    const int cnt = bpe_lanes<32>(T, H, b, n, W.scratch + s);
+    const int cnt = bpe_lanes<32>(T, b, n, W.scratch + s);
     if (lane == 0) put_count(W, pc, cnt);
     return;
   }
   int cnt;
   switch ((n + 31) >> 5) {                    // 2 .. MID_MAX / 32 positions per lane
-    case 2: cnt = list_rounds<2>(T, H, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
-    case 3: cnt = list_rounds<3>(T, H, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
-    case 4: cnt = list_rounds<4>(T, H, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
-    case 5: cnt = list_rounds<5>(T, H, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
-    case 6: cnt = list_rounds<6>(T, H, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
-    case 7: cnt = list_rounds<7>(T, H, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
-    default: cnt = list_rounds<8>(T, H, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    case 2: cnt = list_rounds<2>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    case 3: cnt = list_rounds<3>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    case 4: cnt = list_rounds<4>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    case 5: cnt = list_rounds<5>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    case 6: cnt = list_rounds<6>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    case 7: cnt = list_rounds<7>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
+    default: cnt = list_rounds<8>(T, b, n, W.scratch + s, tok, rank, res, nx, pv); break;
   }
   if (lane == 0) put_count(W, pc, cnt);
   __syncwarp();
@@ -648,42 +539,17 @@ __device__ __forceinline__ void mid_piece(const Tables &T, const HotView &H, con
 // whose longest merge chains set its latency: pairing even the short pieces
 // measured slower there), 1 those of 17..48 bytes, 2 those of 17..48 and of
 // 49..128 bytes (batches).
-// The kernel's shared memory: the staged pair table, then each warp's merge
-// arrays (a piece of up to MID_MAX bytes: token, -1 once unlinked; code of
-// (p, next); its merge result; the list links).
-struct WarpArrays {
-  int32_t tok[MID_MAX], rank[MID_MAX], res[MID_MAX];
-  int16_t nx[MID_MAX], pv[MID_MAX];
-};
-constexpr size_t BPE_WARP_SMEM = HOT_SLOTS * sizeof(uint64_t) + HOT_MAX * sizeof(int32_t) +
-                                 WARP_KERNEL_WARPS * sizeof(WarpArrays);
-static_assert((HOT_SLOTS * sizeof(uint64_t) + HOT_MAX * sizeof(int32_t)) % 16 == 0, "16-byte copies");
-
 template <int PAIRS>
 __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_warp(Tables T, Work W) {
-  extern __shared__ __align__(16) unsigned char bpe_smem[];
-  uint64_t *hot_slots = reinterpret_cast<uint64_t *>(bpe_smem);
-  int32_t *hot_res = reinterpret_cast<int32_t *>(hot_slots + HOT_SLOTS);
-  WarpArrays *wa = reinterpret_cast<WarpArrays *>(hot_res + HOT_MAX);
+  __shared__ int32_t s_tok[WARP_KERNEL_WARPS][MID_MAX];   // token, -1 once unlinked
+  __shared__ int32_t s_rank[WARP_KERNEL_WARPS][MID_MAX];  // rank of (p, next), INT_MAX if none
+  __shared__ int32_t s_res[WARP_KERNEL_WARPS][MID_MAX];   // its merge result
+  __shared__ int16_t s_nx[WARP_KERNEL_WARPS][MID_MAX];
+  __shared__ int16_t s_pv[WARP_KERNEL_WARPS][MID_MAX];
   const CallArgs A = *W.args;
   if (A.n <= 0) return;
   int64_t base, total;
   if (!batch_extent(A, base, total) || call_timed_out(W)) return;
-  // stage the pair table of the lowest ranks (16-byte copies by every thread)
-  {
-    constexpr int N16 = (int)((HOT_SLOTS * sizeof(uint64_t) + HOT_MAX * sizeof(int32_t)) / 16);
-    constexpr int NT16 = (int)(HOT_SLOTS * sizeof(uint64_t) / 16);
-    uint4 *dst = reinterpret_cast<uint4 *>(bpe_smem);
-    const uint4 *ts = reinterpret_cast<const uint4 *>(T.hot_tab);
-    const uint4 *rs = reinterpret_cast<const uint4 *>(T.hot_res);
-    for (int i = threadIdx.x; i < N16; i += BPE_WARP_THREADS) dst[i] = i < NT16 ? __ldg(ts + i) : __ldg(rs + i - NT16);
-  }
-  __syncthreads();
-  HotView H;
-  H.slots = hot_slots;
-  H.res = hot_res;
-  H.unk = T.hot_k == T.n_merges ? RC_NONE : 2 * T.hot_k - 1;
-  H.k2 = 2 * T.hot_k;
   const int np = __ldcg(&W.counters[3]);
   const int c0 = __ldcg(&W.counters[mid_bucket_counter(0)]), c1 = __ldcg(&W.counters[mid_bucket_counter(1)]);
   const int c2 = __ldcg(&W.counters[mid_bucket_counter(2)]);
@@ -703,18 +569,18 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
     gi = __shfl_sync(0xffffffffu, gi, 0);
     if (gi >= nwork) break;
     if (PAIRS >= 2 && gi >= c0 && gi < t1) {     // pieces of 49..128 bytes, two a ticket
-      mid_group<16, PAIR_MAX / 16>(T, H, W, g, W.long_list + lcap, 2 * (gi - c0), c1, wa[warp].tok, wa[warp].rank,
-                                   wa[warp].res, wa[warp].nx, wa[warp].pv);
+      mid_group<16, PAIR_MAX / 16>(T, W, g, W.long_list + lcap, 2 * (gi - c0), c1, s_tok[warp], s_rank[warp],
+                                   s_res[warp], s_nx[warp], s_pv[warp]);
     } else if (PAIRS >= 1 && gi >= t2) {         // pieces of 17..48 bytes, GROUP2 a ticket
-      mid_group<32 / GROUP2, (48 * GROUP2 + 31) / 32>(T, H, W, g, W.long_list + 2 * lcap, GROUP2 * (gi - t2), c2,
-                                                      wa[warp].tok, wa[warp].rank, wa[warp].res, wa[warp].nx,
-                                                      wa[warp].pv);
+      mid_group<32 / GROUP2, (48 * GROUP2 + 31) / 32>(T, W, g, W.long_list + 2 * lcap, GROUP2 * (gi - t2), c2,
+                                                      s_tok[warp], s_rank[warp], s_res[warp], s_nx[warp],
+                                                      s_pv[warp]);
     } else if (gi < t1 || gi >= t2) {
       const int64_t slot = gi < c0 ? gi : gi < t1 ? lcap + (gi - c0) : 2 * lcap + (gi - t2);
-      mid_piece(T, H, W, g, __ldcg(&W.long_list[slot]), wa[warp].tok, wa[warp].rank, wa[warp].res, wa[warp].nx,
-                wa[warp].pv);
+      mid_piece(T, W, g, __ldcg(&W.long_list[slot]), s_tok[warp], s_rank[warp], s_res[warp], s_nx[warp],
+                s_pv[warp]);
     } else {
-      small_chunk(T, H, W, g, total, np, (gi - t1) * SMALL_CHUNK);
+      small_chunk(T, W, g, total, np, (gi - t1) * SMALL_CHUNK);
     }
   }
 }
@@ -1238,8 +1104,8 @@ __global__ void k_hook_offsets(Work W) {
 }
 
 void launch_bpe_warp(const Tables &T, const Work &W, int grid, cudaStream_t s) {
-  if (W.cap_bytes > PAIR_MIN_CAP_BYTES) k_bpe_warp<2><<<grid, BPE_WARP_THREADS, BPE_WARP_SMEM, s>>>(T, W);
-  else k_bpe_warp<0><<<grid, BPE_WARP_THREADS, BPE_WARP_SMEM, s>>>(T, W);
+  if (W.cap_bytes > PAIR_MIN_CAP_BYTES) k_bpe_warp<2><<<grid, BPE_WARP_THREADS, 0, s>>>(T, W);
+  else k_bpe_warp<0><<<grid, BPE_WARP_THREADS, 0, s>>>(T, W);
 }
 void launch_bpe_long(const Tables &T, const Work &W, int grid, cudaStream_t s) {
   k_bpe_long<<<grid, BPE_LONG_THREADS, LONG_SMEM_BYTES, s>>>(T, W);
@@ -1251,12 +1117,7 @@ void launch_hook_pieces(const Work &W, int grid, cudaStream_t s) { k_hook_pieces
 void launch_hook_offsets(const Work &W, int grid, cudaStream_t s) { k_hook_offsets<<<grid, 256, 0, s>>>(W); }
 
 cudaError_t bpe_configure() {
-  cudaError_t e = cudaFuncSetAttribute(k_bpe_long, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LONG_SMEM_BYTES);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_bpe_warp<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BPE_WARP_SMEM);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_bpe_warp<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BPE_WARP_SMEM);
-  return e;
+  return cudaFuncSetAttribute(k_bpe_long, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LONG_SMEM_BYTES);
 }
 
 }  // namespace tt

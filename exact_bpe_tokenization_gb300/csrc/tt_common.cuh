@@ -59,10 +59,6 @@ struct Tables {
   const uint8_t *cls2;        // block * 256 + (cp & 255) -> raw kind (K_*)
   const uint4 *pair_tab;       // {left, right, rank, result}
   uint32_t pair_mask;
-  const uint64_t *hot_tab;     // [HOT_SLOTS] the staged table of the HOT_MAX lowest ranks (see below)
-  const int32_t *hot_res;      // [HOT_MAX] merge result of each staged rank
-  int32_t hot_k;               // merges staged: min(HOT_MAX, merges)
-  int32_t n_merges;
   const int32_t *merge_result;
   const uint4 *vocab_tab;
   uint32_t vocab_mask;
@@ -81,19 +77,6 @@ struct Tables {
 constexpr int LIT_MAX_LEN = 255;       // bytes of one literal
 constexpr int LIT_MAX_COUNT = 4095;    // literals (12-bit index)
 enum : uint8_t { LIT_SEG = 1, LIT_INNER = 2 };   // per-byte marks of taken literals
-
-// The staged pair table: the merges of the HOT_MAX lowest ranks (those most
-// rounds take) in an open-addressing table of HOT_SLOTS 8-byte entries
-// left << 44 | right << 24 | rank (load factor <= 1/2, linear probing; empty
-// = all ones, which no entry equals since rank < 2^24 - 1), copied into
-// shared memory by every CTA of the warp BPE kernel.
-constexpr int HOT_BITS = 13;
-constexpr int HOT_SLOTS = 1 << HOT_BITS;
-constexpr int HOT_MAX = HOT_SLOTS / 2;
-constexpr uint64_t HOT_EMPTY = ~0ull;
-static_assert(HOT_SLOTS >= 2 * HOT_MAX, "load factor <= 1/2");
-TT_HD uint32_t hot_slot(uint32_t l, uint32_t r) { return (l * 0x9E3779B1u ^ r * 0x85EBCA77u) >> (32 - HOT_BITS); }
-TT_HD uint64_t hot_key(uint32_t l, uint32_t r) { return ((uint64_t)l << 44) | ((uint64_t)r << 24); }
 
 TT_HD uint64_t mix64(uint64_t x) {
   x ^= x >> 33; x *= 0xff51afd7ed558ccdull;

@@ -22,9 +22,8 @@ void launch_hook_pre(const Work &W, cudaStream_t s);
 void launch_hook_pieces(const Work &W, int grid, cudaStream_t s);
 void launch_hook_offsets(const Work &W, int grid, cudaStream_t s);
 
-constexpr int BPE_WARP_THREADS = 1024;
-constexpr int BPE_WARP_CTAS_PER_SM = 1;   // 64 registers, 208 KB shared memory (the staged pair table and
-                                          // each warp's merge arrays)
+constexpr int BPE_WARP_THREADS = 256;
+constexpr int BPE_WARP_CTAS_PER_SM = 4;   // all resident: 64 registers, 32 KB shared memory each
 constexpr int BPE_LONG_THREADS = 512;
 constexpr int IDS_THREADS = 256;
 
