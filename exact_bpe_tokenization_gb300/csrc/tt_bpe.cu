@@ -169,8 +169,117 @@ __device__ __forceinline__ void put_count(const Work &W, int k, int c) {
   if (c) atomicAdd(&W.ids_agg[k / IDS_CHUNK], c);
 }
 
-__device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, const uint8_t *g, int64_t total,
-                                            int np, int kb) {
+// ---------------------------------------------------------------- short misses
+// A short piece that is no token is merged by one lane on its own: the
+// pieces of a warp's short-piece chunks that miss the whole-piece table
+// queue up in the warp's MissQueue, and every 32 of them are merged side by
+// side, one per lane.  A lane holds its piece as a compact array of packed
+// words -- rank of the pair the position starts << 40 | that pair's merge
+// result << 20 | token, with RANK_NIL for no pair or no merge -- in the
+// warp's shared arrays, word i of lane l at v[32 * i + l] (conflict-free).
+// A round: the lowest rank r over the array; one pass that merges every
+// leftmost non-overlapping occurrence of r and compacts; then lookups of the
+// pairs next to a merge, four first probes in flight at a time.
+constexpr uint32_t RANK_NIL = 0xFFFFFFu;   // no rank: 2^24 - 1 is above every rank
+constexpr int MISS_QUEUE = 2 * 32;          // < 32 left over plus one chunk's 32
+struct MissQueue {
+  int32_t piece[MISS_QUEUE], start[MISS_QUEUE];
+  uint8_t len[MISS_QUEUE];
+};
+__device__ __forceinline__ uint64_t pack_pos(uint32_t rank, uint32_t res, uint32_t tok) {
+  return ((uint64_t)rank << 40) | ((uint64_t)res << 20) | tok;
+}
+__device__ __forceinline__ uint32_t pos_rank(uint64_t w) { return (uint32_t)(w >> 40); }
+__device__ __forceinline__ uint32_t pos_res(uint64_t w) { return (uint32_t)(w >> 20) & 0xFFFFFu; }
+__device__ __forceinline__ uint32_t pos_tok(uint64_t w) { return (uint32_t)w & 0xFFFFFu; }
+
+// the rank and result of the pairs (i, i + 1) for the set bits i of need
+__device__ __forceinline__ void seq_lookups(const Tables &T, uint64_t *v, uint32_t need) {
+  const int lane = threadIdx.x & 31;
+  while (need) {
+    int at[4];
+    uint32_t sl[4], l[4], r[4];
+    uint4 e[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      at[q] = need ? __ffs(need) - 1 : -1;
+      need &= need - 1;
+      l[q] = r[q] = 0;
+      sl[q] = 0;
+      e[q] = make_uint4(PAIR_EMPTY, 0, 0, 0);
+      if (at[q] >= 0) {
+        l[q] = pos_tok(v[32 * at[q] + lane]);
+        r[q] = pos_tok(v[32 * (at[q] + 1) + lane]);
+        sl[q] = pair_slot(T, (int)l[q], (int)r[q]);
+        e[q] = __ldg(&T.pair_tab[sl[q]]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (at[q] >= 0) {
+        const int2 pr = pair_finish(T, e[q], sl[q], (int)l[q], (int)r[q]);
+        v[32 * at[q] + lane] = pr.x < 0 ? pack_pos(RANK_NIL, 0, l[q]) : pack_pos((uint32_t)pr.x, (uint32_t)pr.y, l[q]);
+      }
+    }
+  }
+}
+
+// BPE of the n <= SMALL_MAX bytes at b by this lane alone: writes the IDs to
+// out and returns their count.
+__device__ __forceinline__ int seq_bpe(const Tables &T, const uint8_t *b, int n, uint64_t *v, int32_t *out) {
+  const int lane = threadIdx.x & 31;
+  for (int i = 0; i < n; ++i) v[32 * i + lane] = pack_pos(RANK_NIL, 0, (uint32_t)__ldg(&T.byte_id[__ldg(b + i)]));
+  int m = n;
+  seq_lookups(T, v, n > 1 ? (1u << (n - 1)) - 1 : 0u);
+  for (int round = 0; round < n; ++round) {   // each round merges at least one pair
+    uint32_t r = RANK_NIL;
+    for (int i = 0; i + 1 < m; ++i) r = min(r, pos_rank(v[32 * i + lane]));
+    if (r == RANK_NIL) break;
+    // merge every leftmost non-overlapping occurrence of r, compacting; the
+    // pairs a merge touches are looked up again
+    int w = 0;
+    uint32_t need = 0;
+    for (int i = 0; i < m; ++w) {
+      const uint64_t x = v[32 * i + lane];
+      if (i + 1 < m && pos_rank(x) == r) {
+        v[32 * w + lane] = pack_pos(RANK_NIL, 0, pos_res(x));
+        need |= (1u << w) | (w ? 1u << (w - 1) : 0u);
+        i += 2;
+      } else {
+        v[32 * w + lane] = x;
+        i += 1;
+      }
+    }
+    m = w;
+    seq_lookups(T, v, need & ((1u << (m - 1)) - 1));   // no pair starts at the last position
+  }
+  for (int i = 0; i < m; ++i) out[i] = (int32_t)pos_tok(v[32 * i + lane]);
+  return m;
+}
+
+// Merge the first cnt (<= 32) queued misses, one per lane.
+__device__ __forceinline__ void run_misses(const Tables &T, const Work &W, const uint8_t *g, const MissQueue &Q,
+                                           int cnt, uint64_t *v) {
+  const int lane = threadIdx.x & 31;
+  if (lane < cnt) {
+    const int k = Q.piece[lane], s = Q.start[lane];
+    const int c = seq_bpe(T, g + s, Q.len[lane], v, W.scratch + s);
+    W.n_ids[k] = c;
+    atomicAdd(&W.ids_agg[k / IDS_CHUNK], c);
+  }
+  __syncwarp();
+}
+
+// One chunk of 32 consecutive pieces: each lane tries the whole-piece
+// shortcut for its piece of at most SMALL_MAX bytes (longer ones are listed
+// by k_pretok) and the misses join the warp's queue.  QUEUE: 32 queued
+// misses are merged as soon as they are there (batches: full warps); else a
+// chunk's misses are merged at once (a single request, whose latency a
+// queue's leftovers at the end of the kernel would lengthen).  qn: the
+// queue's length (warp-uniform).
+template <bool QUEUE>
+__device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, const uint8_t *g, int64_t total, int np,
+                                            int kb, MissQueue &Q, int &qn, uint64_t *v) {
   const int lane = threadIdx.x & 31;
   const int k = kb + lane;
   int32_t s = 0;
@@ -187,7 +296,7 @@ __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, cons
       if (len <= 0 || e > total) {
         W.n_ids[k] = 0;
         set_status(W.status, ST_INVALID_ARG);
-      } else if (len <= SMALL_MAX) {            // longer: listed by k_pretok
+      } else if (len <= SMALL_MAX) {
         const int id = len <= T.max_tok_len ? vocab_probe(T, g + s, len) : -1;
         if (id >= 0) {
           W.scratch[s] = id;
@@ -199,33 +308,32 @@ __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, cons
       }
     }
   }
-  // misses in order of length, longest first, so that the two pieces of a
-  // pair need similar numbers of rounds
-  const unsigned all_miss = __ballot_sync(0xffffffffu, miss);
-  unsigned mm = 0;
-  int len_at = SMALL_MAX + 1;
-  for (unsigned rest = all_miss; rest || mm;) {
-    while (__popc(mm) < 2 && rest) {            // refill from the next shorter length
-      --len_at;
-      const unsigned b = __ballot_sync(0xffffffffu, miss && len == len_at);
-      mm |= b;
-      rest &= ~b;
-    }
-    const int la = __ffs(mm) - 1;
-    mm &= mm - 1;
-    const int lb = mm ? __ffs(mm) - 1 : -1;
-    if (mm) mm &= mm - 1;
-    const int src = lane < 16 ? la : lb;
-    const int ps = __shfl_sync(0xffffffffu, s, src < 0 ? la : src);
-    int pl = __shfl_sync(0xffffffffu, len, src < 0 ? la : src);
-    if (src < 0) pl = 0;
-    const int cnt = bpe_lanes<16>(T, g + ps, pl, W.scratch + ps);
-    if ((lane & 15) == 0 && src >= 0) { W.n_ids[kb + src] = cnt; mine += cnt; }
-  }
-  // the chunk's pieces of at most SMALL_MAX bytes, all in one ID chunk
+  // the hits' counts, all in one ID chunk
 #pragma unroll
   for (int d = 16; d; d >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, d);
   if (lane == 0 && mine) atomicAdd(&W.ids_agg[kb / IDS_CHUNK], mine);
+  const unsigned mm = __ballot_sync(0xffffffffu, miss);
+  if (miss) {
+    const int at = qn + __popc(mm & ((1u << lane) - 1));
+    Q.piece[at] = k;
+    Q.start[at] = s;
+    Q.len[at] = (uint8_t)len;
+  }
+  qn += __popc(mm);
+  __syncwarp();
+  if (!QUEUE) {
+    if (qn) run_misses(T, W, g, Q, qn, v);
+    qn = 0;
+  } else if (qn >= 32) {
+    run_misses(T, W, g, Q, 32, v);
+    const bool mv = lane < qn - 32;             // move the rest to the front
+    int rk = 0, rs = 0, rl = 0;
+    if (mv) { rk = Q.piece[32 + lane]; rs = Q.start[32 + lane]; rl = Q.len[32 + lane]; }
+    __syncwarp();
+    if (mv) { Q.piece[lane] = rk; Q.start[lane] = rs; Q.len[lane] = (uint8_t)rl; }
+    __syncwarp();
+    qn -= 32;
+  }
 }
 
 // The linked-list rounds of one piece of n bytes (32 < n <= 32 * NS) in the
@@ -539,13 +647,19 @@ __device__ __forceinline__ void mid_piece(const Tables &T, const Work &W, const 
 // whose longest merge chains set its latency: pairing even the short pieces
 // measured slower there), 1 those of 17..48 bytes, 2 those of 17..48 and of
 // 49..128 bytes (batches).
+// Each warp's merge arrays (a listed piece of up to MID_MAX bytes: token,
+// -1 once unlinked; rank of (p, next), INT_MAX if none; its merge result;
+// the list links), which also hold the packed words of 32 short misses.
+struct __align__(16) WarpArrays {
+  int32_t tok[MID_MAX], rank[MID_MAX], res[MID_MAX];
+  int16_t nx[MID_MAX], pv[MID_MAX];
+};
+static_assert(sizeof(WarpArrays) >= 32 * SMALL_MAX * sizeof(uint64_t), "room for 32 short misses");
+
 template <int PAIRS>
 __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_warp(Tables T, Work W) {
-  __shared__ int32_t s_tok[WARP_KERNEL_WARPS][MID_MAX];   // token, -1 once unlinked
-  __shared__ int32_t s_rank[WARP_KERNEL_WARPS][MID_MAX];  // rank of (p, next), INT_MAX if none
-  __shared__ int32_t s_res[WARP_KERNEL_WARPS][MID_MAX];   // its merge result
-  __shared__ int16_t s_nx[WARP_KERNEL_WARPS][MID_MAX];
-  __shared__ int16_t s_pv[WARP_KERNEL_WARPS][MID_MAX];
+  __shared__ WarpArrays wa[WARP_KERNEL_WARPS];
+  __shared__ MissQueue mq[WARP_KERNEL_WARPS];
   const CallArgs A = *W.args;
   if (A.n <= 0) return;
   int64_t base, total;
@@ -563,26 +677,29 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
   const int64_t lcap = list_cap(W.cap_bytes);
   const uint8_t *g = A.utf8 + base;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t *s_tok = wa[warp].tok, *s_rank = wa[warp].rank, *s_res = wa[warp].res;
+  int16_t *s_nx = wa[warp].nx, *s_pv = wa[warp].pv;
+  uint64_t *v = reinterpret_cast<uint64_t *>(&wa[warp]);
+  int qn = 0;                                   // queued short misses (warp-uniform)
   for (;;) {
     int gi = 0;
     if (lane == 0) gi = atomicAdd(&W.counters[9], 1);
     gi = __shfl_sync(0xffffffffu, gi, 0);
     if (gi >= nwork) break;
     if (PAIRS >= 2 && gi >= c0 && gi < t1) {     // pieces of 49..128 bytes, two a ticket
-      mid_group<16, PAIR_MAX / 16>(T, W, g, W.long_list + lcap, 2 * (gi - c0), c1, s_tok[warp], s_rank[warp],
-                                   s_res[warp], s_nx[warp], s_pv[warp]);
+      mid_group<16, PAIR_MAX / 16>(T, W, g, W.long_list + lcap, 2 * (gi - c0), c1, s_tok, s_rank, s_res, s_nx,
+                                   s_pv);
     } else if (PAIRS >= 1 && gi >= t2) {         // pieces of 17..48 bytes, GROUP2 a ticket
       mid_group<32 / GROUP2, (48 * GROUP2 + 31) / 32>(T, W, g, W.long_list + 2 * lcap, GROUP2 * (gi - t2), c2,
-                                                      s_tok[warp], s_rank[warp], s_res[warp], s_nx[warp],
-                                                      s_pv[warp]);
+                                                      s_tok, s_rank, s_res, s_nx, s_pv);
     } else if (gi < t1 || gi >= t2) {
       const int64_t slot = gi < c0 ? gi : gi < t1 ? lcap + (gi - c0) : 2 * lcap + (gi - t2);
-      mid_piece(T, W, g, __ldcg(&W.long_list[slot]), s_tok[warp], s_rank[warp], s_res[warp], s_nx[warp],
-                s_pv[warp]);
+      mid_piece(T, W, g, __ldcg(&W.long_list[slot]), s_tok, s_rank, s_res, s_nx, s_pv);
     } else {
-      small_chunk(T, W, g, total, np, (gi - t1) * SMALL_CHUNK);
+      small_chunk<PAIRS >= 1>(T, W, g, total, np, (gi - t1) * SMALL_CHUNK, mq[warp], qn, v);
     }
   }
+  if (qn) run_misses(T, W, g, mq[warp], qn, v);   // the warp's last queued misses
 }
 
 // ---------------------------------------------------------------- long
