@@ -415,12 +415,11 @@ template <int NT>
 struct PretokSmem {
   WinSmem<NT> w;
   uint8_t chain[WIN];
-  uint8_t rq8[WIN];          // reverse-query results per tile char: rq_ws | rq_up << 2
   uint16_t dagg[NT][3];  // scan values of chars whose predicate waits for the barrier
-  S2 s2_tmp[NT / 32];
+  S2 s2_tmp[NT / 32];        // (holds the family's scan state: S2, or the smaller S2L)
   int2 i2_tmp[NT / 32];
   int i_tmp[NT / 32];
-  S2 s2_prefix;
+  S2 s2_prefix;              // (likewise)
   int2 s1c;                  // mark-resolution carry (o200k)
   int rqc;                   // reverse-query carry
   int tile;
@@ -504,6 +503,40 @@ struct Slider {
   }
 };
 
+// The forward-scan state of a family: the 12-byte S2L for the families
+// without a case rule, the full S2 for the o200k-style one.
+template <int FAM> struct ScanOf { using T = S2L; };
+template <> struct ScanOf<FAM_O200K> { using T = S2; };
+__device__ __forceinline__ S2 st_identity(const S2 *) { return s2_identity(); }
+__device__ __forceinline__ S2L st_identity(const S2L *) { return s2l_identity(); }
+__device__ __forceinline__ S2 st_combine(const S2 &a, const S2 &b) { return s2_combine(a, b); }
+__device__ __forceinline__ S2L st_combine(const S2L &a, const S2L &b) { return s2l_combine(a, b); }
+
+// The reverse queries of char j of the tile (pos in [ts, te)), asked only
+// where a rule reads them: the first rq_ws event (low byte, if want_ws) and
+// rq_up event (high byte, if want_up) among the tile's chars after j, else
+// the tile's carry (the first event in the tiles after it).
+template <class WS>
+__device__ __forceinline__ int rq_after(int fam, const WS &S, int64_t ws, int64_t te, int j, int carry, bool want_ws,
+                                        bool want_up) {
+  int lo = want_ws ? 0xFF : 0, hi = want_up ? 0xFF : 0;   // 0xFF: still searching
+  for (int k = j + 1; k < S.nch && (lo == 0xFF || hi == 0xFF); ++k) {
+    const uint32_t c = S.ci[k];
+    if (ws + ci_lead(c) >= te) break;
+    if (lo == 0xFF) {
+      const uint8_t e = rq_ws_event(fam, ci_rs(c), ci_raw(c), ci_cp8(c));
+      if (e != 0xFF) lo = e;
+    }
+    if (hi == 0xFF) {
+      const uint8_t e = rq_up_event(ci_rs(c), ci_raw(c));
+      if (e != 0xFF) hi = e;
+    }
+  }
+  if (lo == 0xFF) lo = carry & 0xFF;
+  if (hi == 0xFF) hi = (carry >> 8) & 0xFF;
+  return lo | (hi << 8);
+}
+
 template <int FAM, int NT>
 __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work W) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -581,70 +614,63 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
 
   // --- forward scan (scan 2) over chars with pos in [ts - 16, te); the
   // published aggregate covers the shifted tile [ts - 16, te - 16)
+  using ST = typename ScanOf<FAM>::T;
+  ST *st_tmp = reinterpret_cast<ST *>(P.s2_tmp);
+  ST *st_agg = reinterpret_cast<ST *>(W.s2_agg), *st_inc = reinterpret_cast<ST *>(W.s2_inc);
+  const ST st_id = st_identity((const ST *)nullptr);
   const int64_t s2_lo = ts - S2_SHIFT, s2_pub_hi = t == ntiles - 1 ? INT64_MAX : te - S2_SHIFT;
   int jlo = c0, jhi = c1;                       // my chars with pos in [s2_lo, te)
   while (jlo < jhi && ws + S.lead(jlo) < s2_lo) ++jlo;
   while (jhi > jlo && ws + S.lead(jhi - 1) >= te) --jhi;
-  S2 agg_all = s2_identity(), agg_pub = s2_identity();
+  ST agg_all = st_id, agg_pub = st_id;
   bool pub_done = false;
-  if (jlo < jhi) {
-    Slider w;
-    w.start(S, ws, jlo);
-    for (int j = jlo;;) {
-      if (!pub_done && w.pos >= s2_pub_hi) { agg_pub = agg_all; pub_done = true; }
-      if (!s2_trivial(fam, w.b)) agg_all = s2_combine(agg_all, s2_element(fam, w.b, w.pos, w.p1, w.p2));
-      if (++j >= jhi) break;
-      w.step(S, ws, j);
+  if constexpr (FAM == FAM_O200K) {
+    if (jlo < jhi) {
+      Slider w;
+      w.start(S, ws, jlo);
+      for (int j = jlo;;) {
+        if (!pub_done && w.pos >= s2_pub_hi) { agg_pub = agg_all; pub_done = true; }
+        if (!s2_trivial(fam, w.b)) agg_all = s2_combine(agg_all, s2_element(fam, w.b, w.pos, w.p1, w.p2));
+        if (++j >= jhi) break;
+        w.step(S, ws, j);
+      }
+    }
+  } else {
+    // only digits and blanks contribute, and their elements read nothing
+    // but their own kind, code point and position and their predecessor's kind
+    for (int j = jlo; j < jhi; ++j) {
+      const uint32_t c = S.ci[j];
+      const int32_t pos = (int32_t)(ws + ci_lead(c));
+      if (!pub_done && pos >= s2_pub_hi) { agg_pub = agg_all; pub_done = true; }
+      const uint8_t e0 = ci_eff(c);
+      if (e0 == K_NUM || e0 == K_WS) {
+        const uint8_t e1 = (ci_rs(c) || j == 0) ? (uint8_t)K_NONE : ci_eff(S.ci[j - 1]);
+        agg_all = s2l_combine(agg_all, s2l_element(e0, e1, ci_cp8(c), pos));
+      }
     }
   }
   if (!pub_done) agg_pub = agg_all;
-  auto comb = [](const S2 &a, const S2 &b) { return s2_combine(a, b); };
-  S2 tile_pub;
-  block_exclusive_scan<NT>(agg_pub, comb, s2_identity(), P.s2_tmp, &tile_pub);
-  // publish now: the successors' look-back runs while this tile answers its
-  // reverse queries
-  if (tid == 0 && t != W.withhold_tile) lookback_publish(t, tile_pub, W.s2_agg, W.s2_inc, W.s2_flag);
-  const S2 my_ex = block_exclusive_scan<NT>(agg_all, comb, s2_identity(), P.s2_tmp, (S2 *)nullptr);
-
-  // --- reverse queries over the tile's chars: first event strictly after j
-  auto first = [](int a, int b) {
-    const int lo = (a & 0xFF) != 0xFF ? (a & 0xFF) : (b & 0xFF);
-    const int hi = (a >> 8) != 0xFF ? (a >> 8) : (b >> 8);
-    return lo | (hi << 8);
-  };
-  {
-    int rq_first = 0xFFFF;
-    for (int j = c0; j < c1; ++j) {
-      const int64_t pos = ws + S.lead(j);
-      if (pos < ts || pos >= te) continue;
-      const uint8_t ew = rq_ws_event(fam, S.rs(j), S.raw(j), S.cp8(j));
-      const uint8_t eu = rq_up_event(S.rs(j), S.raw(j));
-      if ((rq_first & 0xFF) == 0xFF && ew != 0xFF) rq_first = (rq_first & 0xFF00) | ew;
-      if ((rq_first >> 8) == 0xFF && eu != 0xFF) rq_first = (rq_first & 0x00FF) | (eu << 8);
-    }
-    int after = first(block_exclusive_suffix<NT>(rq_first, first, 0xFFFF, P.i_tmp, (int *)nullptr), P.rqc);
-    for (int j = c1 - 1; j >= c0; --j) {
-      const int64_t pos = ws + S.lead(j);
-      if (pos < ts || pos >= te) continue;
-      P.rq8[j] = (uint8_t)((after & 0x3) | (((after >> 8) & 0x3) << 2));
-      const uint8_t ew = rq_ws_event(fam, S.rs(j), S.raw(j), S.cp8(j));
-      const uint8_t eu = rq_up_event(S.rs(j), S.raw(j));
-      if (ew != 0xFF) after = (after & 0xFF00) | ew;
-      if (eu != 0xFF) after = (after & 0x00FF) | (eu << 8);
-    }
-  }
-
+  auto comb = [](const ST &a, const ST &b) { return st_combine(a, b); };
+  ST tile_pub;
+  block_exclusive_scan<NT>(agg_pub, comb, st_id, st_tmp, &tile_pub);
+  // publish now: the successors' look-back runs while this tile scans its
+  // own chars
+  if (tid == 0 && t != W.withhold_tile) lookback_publish(t, tile_pub, st_agg, st_inc, W.s2_flag);
+  const ST my_ex = block_exclusive_scan<NT>(agg_all, comb, st_id, st_tmp, (ST *)nullptr);
   if (tid < 32) {
-    const S2 pre = warp_lookback(t, tile_pub, comb, s2_identity(), W.s2_agg, W.s2_inc, W.s2_flag, W.status,
+    const ST pre = warp_lookback(t, tile_pub, comb, st_id, st_agg, st_inc, W.s2_flag, W.status,
                                  &W.counters[CTR_TIMEOUT], W.spin_limit, true, t == W.withhold_tile);
-    if (tid == 0) P.s2_prefix = pre;
+    if (tid == 0) *reinterpret_cast<ST *>(&P.s2_prefix) = pre;
   }
   __syncthreads();
-  S2 before = s2_combine(P.s2_prefix, my_ex);
+  ST before = st_combine(*reinterpret_cast<const ST *>(&P.s2_prefix), my_ex);
 
   // --- walk: per-char scan values and the predicate.  o200k chars whose
   // contraction lookback reaches the previous thread's chars wait for the
   // barrier (their chain states are written by that thread in this walk).
+  // The reverse queries (is a later CR/LF in this blank run; is the rest of
+  // this letter run upper case) are answered only for the chars whose rule
+  // reads them.
   uint32_t starts = 0, placeholder = 0, deferred = 0;   // bit (j - c0) for my chars (<= PT_BYTES)
   const bool filter = __ldcg(&W.counters[5]) != 0;
   auto decide = [&](int j, const Nbr &nb, const Aggs &a, int64_t pos) {
@@ -658,29 +684,45 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
     }
     if (st) starts |= 1u << (j - c0);
   };
-  for (int j = c0; j < jlo; ++j) P.chain[j] = 1;
-  for (int j = jhi; j < c1; ++j) P.chain[j] = 1;
+  if constexpr (FAM == FAM_O200K) {
+    for (int j = c0; j < jlo; ++j) P.chain[j] = 1;
+    for (int j = jhi; j < c1; ++j) P.chain[j] = 1;
+  }
   if (jlo < jhi) {
     Slider w;
     w.start(S, ws, jlo);
     // chain states of the three chars before jlo (valid for o200k only where
     // they belong to this thread; other cases are deferred below)
-    bool l1 = jlo >= 1 ? P.chain[jlo - 1] != 0 : true, l2 = jlo >= 2 ? P.chain[jlo - 2] != 0 : true;
-    bool l3 = jlo >= 3 ? P.chain[jlo - 3] != 0 : true;
+    bool l1 = true, l2 = true, l3 = true;
+    if constexpr (FAM == FAM_O200K) {
+      l1 = jlo >= 1 ? P.chain[jlo - 1] != 0 : true;
+      l2 = jlo >= 2 ? P.chain[jlo - 2] != 0 : true;
+      l3 = jlo >= 3 ? P.chain[jlo - 3] != 0 : true;
+    }
     for (int j = jlo;;) {
-      const S2 after = s2_trivial(fam, w.b) ? before : s2_combine(before, s2_element(fam, w.b, w.pos, w.p1, w.p2));
-      Aggs a;
-      bool ch;
-      s2_values(before, after, w.pos, a, ch);
-      before = after;
-      if (fam == FAM_O200K) P.chain[j] = ch ? 1 : 0;
+      Aggs a{};
+      bool ch = true;
+      if constexpr (FAM == FAM_O200K) {
+        const S2 after = s2_trivial(fam, w.b) ? before : s2_combine(before, s2_element(fam, w.b, w.pos, w.p1, w.p2));
+        s2_values(before, after, w.pos, a, ch);
+        before = after;
+        P.chain[j] = ch ? 1 : 0;
+      } else if (w.b.e0 == K_NUM || w.b.e0 == K_WS) {   // the only chars whose rules read scan values
+        const S2L after = s2l_combine(before, s2l_element(w.b.e0, w.b.e1, w.b.c0, w.pos));
+        s2l_values(before, after, w.pos, a);
+        before = after;
+      }
       if (w.pos >= ts) {
-        const uint8_t q = P.rq8[j];
-        a.rq_ws = q & 3;
-        a.rq_up = (q >> 2) & 3;
         const Nbr &nb = w.b;
+        const bool want_ws = nb.e0 == K_WS && is_crlf(nb.c1);
+        const bool want_up = FAM == FAM_O200K && nb.e0 == K_LU && nb.e1 == K_LB;
+        if (want_ws || want_up) {
+          const int q = rq_after(fam, S, ws, te, j, P.rqc, want_ws, want_up);
+          a.rq_ws = (uint8_t)(q & 0x3);
+          a.rq_up = (uint8_t)((q >> 8) & 0x3);
+        }
         // (chain states are read only next to an apostrophe: c0 with l1, c2 with l2, c3 with l3)
-        if (fam == FAM_O200K && j < c0 + 3 &&
+        if (FAM == FAM_O200K && j < c0 + 3 &&
             (nb.c0 == '\'' || nb.c1 == '\'' || nb.c2 == '\'' || nb.c3 == '\'')) {
           deferred |= 1u << (j - c0);
           P.dagg[tid][j - c0] = (uint16_t)(a.nidx3 | (a.w_start << 2) | (a.w_prev_other << 3) |

@@ -324,6 +324,52 @@ TT_HD void s2_values(const S2 &before, const S2 &after, int32_t pos, Aggs &a, bo
   chain_after = chain_apply(after.chain, true) != 0;
 }
 
+// The forward aggregates of the families without a case rule (cl100k- and
+// deepseek-style): S2 without its o200k fields, in 12 bytes.
+struct S2L {
+  int32_t wst, ncw;        // as in S2
+  uint32_t num;            // number runs: bit 2 = a reset happened, bits 0..1 = count since it (mod 3)
+};
+TT_HD S2L s2l_identity() {
+  S2L r;
+  r.wst = r.ncw = -1;
+  r.num = 0;
+  return r;
+}
+TT_HD S2L s2l_combine(const S2L &a, const S2L &b) {
+  S2L r;
+  r.wst = max32(a.wst, b.wst);
+  r.ncw = max32(a.ncw, b.ncw);
+  if (b.num & 4u) {
+    r.num = b.num;
+  } else {
+    const uint32_t c = (a.num & 3u) + (b.num & 3u);
+    r.num = (a.num & 4u) | (c >= 3u ? c - 3u : c);
+  }
+  return r;
+}
+// the element of char i from its effective kind e0, its predecessor's e1
+// (K_NONE at a request start), its code point c0 and byte position pos;
+// the identity unless i is a digit or a blank
+TT_HD S2L s2l_element(uint8_t e0, uint8_t e1, uint32_t c0, int32_t pos) {
+  S2L r = s2l_identity();
+  if (e0 == K_NUM) r.num = (e1 != K_NUM ? 4u : 0u) | 1u;
+  if (e0 == K_WS) {
+    if (e1 != K_WS) r.wst = pos * 2 + (e1 == K_OTHER ? 1 : 0);
+    if (!is_crlf(c0)) r.ncw = pos;
+  }
+  return r;
+}
+// the aggregates s2_values gives, from S2L states (no case rule, chain true)
+TT_HD void s2l_values(const S2L &before, const S2L &after, int32_t pos, Aggs &a) {
+  a.nidx3 = (int)(((after.num & 3u) + 2u) % 3u);
+  const int32_t s = after.wst >> 1;
+  a.w_start = s == pos;
+  a.w_prev_other = (after.wst & 1) != 0;
+  a.w_ncw_before = before.ncw >= s;
+  a.case_prev = 0;
+}
+
 // deepseek-style segments: 0 the rest, 1 digits, 2 kana / CJK ideographs
 // (raw kinds; an added-token literal's inner chars are never cut)
 TT_HD int ds_segment_class(uint8_t raw) {

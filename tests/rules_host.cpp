@@ -67,8 +67,11 @@ extern "C" void rules_host_starts(int fam, const uint32_t *cp, const uint8_t *ra
     if (ew != 0xFF) cw = ew;
     if (eu != 0xFF) cu = eu;
   }
-  // forward scan (scan 2), sequential; chain states go into chain[] as we go
+  // forward scan (scan 2), sequential; chain states go into chain[] as we go.
+  // The families without a case rule use the 12-byte state, as the kernels
+  // do; both forms are run and must give the same aggregates.
   S2 before = s2_identity();
+  S2L lbefore = s2l_identity();
   for (int64_t j = 0; j < n; ++j) {
     Nbr b = nbr(j);
     const S2 after = s2_trivial(fam, b) ? before
@@ -78,6 +81,16 @@ extern "C" void rules_host_starts(int fam, const uint32_t *cp, const uint8_t *ra
     s2_values(before, after, (int32_t)j, a, ch);
     chain[j] = ch;
     before = after;
+    if (fam != FAM_O200K) {
+      const S2L lafter = s2l_combine(lbefore, s2l_element(b.e0, b.e1, b.c0, (int32_t)j));
+      Aggs la;
+      s2l_values(lbefore, lafter, (int32_t)j, la);
+      lbefore = lafter;
+      if (b.e0 == K_NUM && la.nidx3 != a.nidx3) { start[j] = 2; continue; }          // 2: the forms disagree
+      if (b.e0 == K_WS && (la.w_start != a.w_start || la.w_prev_other != a.w_prev_other ||
+                           la.w_ncw_before != a.w_ncw_before)) { start[j] = 2; continue; }
+      a = la;
+    }
     a.rq_ws = rq_ws[j];
     a.rq_up = rq_up[j];
     start[j] = piece_start(fam, b, a) ? 1 : 0;
