@@ -254,3 +254,29 @@ def all_strings(alphabet, max_len):
     for _ in range(max_len):
         cur = [s + a for s in cur for a in alphabet]
         yield from cur
+
+
+def family_pieces_chunk(args):
+    """(family, strings) -> the AST matcher's pieces of each string; a
+    worker for process pools (each process builds its own AST from the frozen
+    class table).  family 3 runs the deepseek-style splitters in sequence."""
+    family, strings = args
+    import oracle
+    masks = oracle.class_table()
+    if family == 3:
+        asts = deepseek_asts(masks)
+        return [split_sequence(asts, s) for s in strings]
+    ast = family_ast(family, masks)
+    return [brute_pieces(ast, s) for s in strings]
+
+
+def pieces_in_pool(family, strings, chunk=4096):
+    """family_pieces_chunk over many strings, in a pool of spawned processes."""
+    import multiprocessing
+    import os
+    parts = [(family, strings[i:i + chunk]) for i in range(0, len(strings), chunk)]
+    with multiprocessing.get_context("spawn").Pool(min(8, os.cpu_count() or 1)) as pool:
+        out = []
+        for r in pool.map(family_pieces_chunk, parts):
+            out.extend(r)
+    return out

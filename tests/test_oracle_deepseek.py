@@ -36,6 +36,21 @@ def test_brute_force_splitters_short_strings(alpha, masks):
         assert g == brute.split_sequence(asts, s), repr(s)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("alpha", [
+    ["a", "1", " ", "\n", "日", "か", "・"],     # letters, digit groups, blanks, kana / ideographs, middle dot
+    ["s", "'", "2", "\t", "ー", ".", "x"],      # contractions, digits, tab look-ahead, long-vowel sign, other
+])
+def test_brute_force_splitters_all_strings_up_to_6(alpha):
+    """The three AST splitters run one after another, on every string of
+    length <= 6 over a 7-symbol alphabet (137,256 strings)."""
+    strings = list(brute.all_strings(alpha, 6))
+    want = brute.pieces_in_pool(FAM, strings)
+    got = oracle_pieces_batch(oracle.pretokenizer(FAM), strings)
+    bad = [s for s, g, w in zip(strings, got, want) if g != w]
+    assert not bad, [repr(s) for s in bad[:10]]
+
+
 @pytest.mark.skipif(not HAVE_REGEX, reason="regex engine not installed")
 def test_regex_engine_splitters_all_strings_up_to_5():
     import regex

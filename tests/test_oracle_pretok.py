@@ -50,6 +50,31 @@ def test_brute_force_matcher_short_strings(family, alphabet, masks):
         assert g == brute.brute_pieces(ast, s), repr(s)
 
 
+# Seven symbols each, so that every string of length <= 6 (137,256 of them)
+# goes through the independent AST matcher in seconds.
+AST6 = [
+    (1, ["a", "s", "1", " ", "\n", "'", "."]),       # contractions, digit groups, blank runs, newline absorption
+    (1, ["r", "e", "'", " ", "\t", "\r", "é"]),       # two-letter contractions, tab / CR look-ahead, a 2-byte letter
+    (2, ["s", "T", "'", "a", "\u0301", " ", "."]),     # case splits, a combining mark, contraction suffixes
+    (2, ["B", "b", "か", "1", "\n", "'", "\U0001F642"]),  # caseless letters, digits, newline, a 4-byte symbol
+]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("family,alpha", AST6)
+def test_brute_force_matcher_all_strings_up_to_6(family, alpha):
+    """Independent AST backtracking matcher on every string of length <= 6
+    over a 7-symbol alphabet that holds the hazards of the family (§3.1:
+    digit grouping, whitespace look-ahead, newline absorption; §4.1: case,
+    marks, contractions)."""
+    strings = list(brute.all_strings(alpha, 6))
+    assert len(strings) == 137256
+    want = brute.pieces_in_pool(family, strings)
+    got = oracle_pieces_batch(oracle.pretokenizer(family), strings)
+    bad = [s for s, g, w in zip(strings, got, want) if g != w]
+    assert not bad, [repr(s) for s in bad[:10]]
+
+
 @pytest.mark.skipif(not HAVE_REGEX, reason="regex engine not installed")
 @pytest.mark.parametrize("family,alphabet", [(1, 1), (2, 2), (2, 3)])
 def test_regex_engine_all_strings_up_to_6(family, alphabet):
