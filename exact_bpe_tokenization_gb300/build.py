@@ -3,6 +3,8 @@
 Steps: turn the frozen character-class range file into a C include (checked
 against its recorded SHA-256), compile every CUDA source for sm_103a in
 parallel, link one shared library next to this file.  No cmake; nvcc only.
+build(trace=True) builds the tracing variant instead (-DTT_TRACE, its own
+objects and libtoktier_trace.so; see trace_bpe.py).
 """
 import hashlib
 import os
@@ -16,6 +18,7 @@ REPO = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(REPO, "_build", "toktier-" + platform.machine())
 LIB = os.path.join(HERE, "libtoktier.so")
+TRACE_LIB = os.path.join(HERE, "libtoktier_trace.so")
 SOURCES = ["tt_api.cu", "tt_pretok.cu", "tt_bpe.cu", "tt_literals.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
@@ -80,19 +83,22 @@ def elf_matches_host(path):
     return want is None or struct.unpack("<H", head[18:20])[0] == want
 
 
-def build(force=False, verbose=False):
+def build(force=False, verbose=False, trace=False):
     gen_dir = os.path.join(BUILD, "gen")
     inc = gen_class_include(gen_dir)
+    obj_dir = BUILD + "-trace" if trace else BUILD
+    lib_path = TRACE_LIB if trace else LIB
+    extra = ["-DTT_TRACE"] if trace else []
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers += [inc, os.path.join(REPO, "include", "toktier.h")]
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(obj_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + headers):
-            jobs.append([nvcc()] + ARCH + NVCC_FLAGS + ["-I", gen_dir, "-I", CSRC, "-c", s, "-o", o])
-    os.makedirs(BUILD, exist_ok=True)
+            jobs.append([nvcc()] + ARCH + NVCC_FLAGS + extra + ["-I", gen_dir, "-I", CSRC, "-c", s, "-o", o])
+    os.makedirs(obj_dir, exist_ok=True)
 
     def run(cmd):
         if verbose:
@@ -106,11 +112,11 @@ def build(force=False, verbose=False):
         for out in ex.map(run, jobs):
             if verbose and out.strip():
                 print(out)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".%d.tmp" % os.getpid()
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + ".%d.tmp" % os.getpid()
         run([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -530,7 +530,7 @@ static int grid_long(const Workspace *w) {
 // Enqueue the kernels of one encode on `stream`.  Untimed, the BPE of the
 // huge pieces (k_bpe_long) runs on a second stream beside the warp kernel
 // (k_bpe_warp, every other piece), forked after k_pretok and joined before
-// k_ids; under capture these become two parallel graph branches.  Timed
+// k_idscan; under capture these become two parallel graph branches.  Timed
 // (profiling), every kernel runs in turn on `stream` between events.
 static tt_status enqueue_encode(tt_tokenizer *h, Workspace *w, cudaStream_t stream, bool timed) {
   const Tables &T = h->T;

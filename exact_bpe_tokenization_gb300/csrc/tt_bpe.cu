@@ -26,6 +26,39 @@
 
 namespace tt {
 
+#ifdef TT_TRACE
+// ---------------------------------------------------------------- trace builds
+// A library built with -DTT_TRACE (libtoktier_trace.so, never the product
+// library) records one entry per ticket of the warp BPE kernel: the
+// globaltimer (ns) at its start and end, its kind (0: a piece of 129..256
+// bytes, 1: pieces of 49..128 bytes, 2: a chunk of short pieces with the
+// misses merged during it, 3: pieces of 17..48 bytes, 4: a warp's last queued
+// misses), its pieces, the longest of them and the most merge rounds the
+// warp ran for one of them.  tt_trace_read (trace builds only) copies the
+// records out and starts a new trace.
+constexpr int TRACE_CAP = 1 << 20;
+struct TraceRec {
+  unsigned long long t0, t1;
+  int kind, pieces, max_len, rounds;
+};
+__device__ TraceRec tt_trace_rec[TRACE_CAP];
+__device__ int tt_trace_n;
+__shared__ int tt_trace_rounds[BPE_WARP_THREADS / 32];
+__device__ __forceinline__ unsigned long long trace_clock() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// a round of a warp-synchronous merge loop (counted once, by lane 0)
+#define TT_TRACE_ROUND() \
+  do { if ((threadIdx.x & 31) == 0) ++tt_trace_rounds[threadIdx.x >> 5]; } while (0)
+// the rounds one lane took on its own
+#define TT_TRACE_LANE_ROUNDS(r) atomicMax(&tt_trace_rounds[threadIdx.x >> 5], (r))
+#else
+#define TT_TRACE_ROUND() ((void)0)
+#define TT_TRACE_LANE_ROUNDS(r) ((void)0)
+#endif
+
 // whole-piece vocabulary probe of len bytes at b (global memory): the hash
 // of 8-byte words, then entries whose inline bytes and length match; only a
 // token longer than VOCAB_INLINE bytes compares its remaining bytes in the
@@ -98,6 +131,7 @@ __device__ __forceinline__ int bpe_lanes(const Tables &T, const uint8_t *bytes, 
     res = pr.y;
   }
   for (int round = 0; round < G; ++round) {   // each round unlinks at least one symbol
+    TT_TRACE_ROUND();
     int r = rank;
 #pragma unroll
     for (int d = G / 2; d >= 1; d >>= 1) r = min(r, __shfl_xor_sync(FULL, r, d));
@@ -155,6 +189,7 @@ __device__ __forceinline__ int bpe_lanes(const Tables &T, const uint8_t *bytes, 
 // of a run from its left end: the leftmost non-overlapping set.  Pairs made
 // by a merge rank above r (well-ordered list), so they never join a run.
 constexpr int WARP_KERNEL_WARPS = BPE_WARP_THREADS / 32;
+
 // workspaces above this size (batches; the single request stays below) pair
 // the pieces of 49..128 bytes
 constexpr int64_t PAIR_MIN_CAP_BYTES = 4ll << 20;
@@ -231,10 +266,12 @@ __device__ __forceinline__ int seq_bpe(const Tables &T, const uint8_t *b, int n,
   for (int i = 0; i < n; ++i) v[32 * i + lane] = pack_pos(RANK_NIL, 0, (uint32_t)__ldg(&T.byte_id[__ldg(b + i)]));
   int m = n;
   seq_lookups(T, v, n > 1 ? (1u << (n - 1)) - 1 : 0u);
+  int rounds = 0;
   for (int round = 0; round < n; ++round) {   // each round merges at least one pair
     uint32_t r = RANK_NIL;
     for (int i = 0; i + 1 < m; ++i) r = min(r, pos_rank(v[32 * i + lane]));
     if (r == RANK_NIL) break;
+    ++rounds;
     // merge every leftmost non-overlapping occurrence of r, compacting; the
     // pairs a merge touches are looked up again
     int w = 0;
@@ -253,6 +290,8 @@ __device__ __forceinline__ int seq_bpe(const Tables &T, const uint8_t *b, int n,
     m = w;
     seq_lookups(T, v, need & ((1u << (m - 1)) - 1));   // no pair starts at the last position
   }
+  TT_TRACE_LANE_ROUNDS(rounds);
+  (void)rounds;
   for (int i = 0; i < m; ++i) out[i] = (int32_t)pos_tok(v[32 * i + lane]);
   return m;
 }
@@ -380,6 +419,7 @@ __device__ __forceinline__ int list_rounds(const Tables &T, const uint8_t *b, in
   }
   __syncwarp();
   for (int round = 0; round < n; ++round) {   // each round unlinks at least one symbol
+    TT_TRACE_ROUND();
     int rr[NS];
     int lm = INT_MAX;
 #pragma unroll
@@ -505,6 +545,7 @@ __device__ __forceinline__ int group_rounds(const Tables &T, const uint8_t *b, i
   }
   __syncwarp();
   for (int round = 0; round < SHARE; ++round) {      // a group with pairs unlinks at least one symbol a round
+    TT_TRACE_ROUND();
     int rr[NS];
     int r = INT_MAX;
 #pragma unroll
@@ -667,13 +708,13 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
   const int np = __ldcg(&W.counters[3]);
   const int c0 = __ldcg(&W.counters[mid_bucket_counter(0)]), c1 = __ldcg(&W.counters[mid_bucket_counter(1)]);
   const int c2 = __ldcg(&W.counters[mid_bucket_counter(2)]);
-  // ticket order, longest expected work first: listed pieces of 49..256
-  // bytes, chunks of short pieces, listed pieces of 17..48 bytes.  In
-  // workspaces beyond the single-request size the pieces of 49..128 bytes go
-  // two to a ticket (pair_rounds)
-  // (GROUP2 pieces of 17..48 bytes a ticket when paired)
+  // ticket order, the longest work a ticket first: listed pieces of
+  // 129..256 and 49..128 bytes, listed pieces of 17..48 bytes, then the
+  // chunks of short pieces (the shortest tickets, which even out the end of
+  // the kernel).  In batches the pieces of 49..128 bytes go two to a ticket
+  // and those of 17..48 bytes GROUP2 to a ticket.
   const int tb1 = PAIRS >= 2 ? (c1 + 1) / 2 : c1, tb2 = PAIRS >= 1 ? (c2 + GROUP2 - 1) / GROUP2 : c2;
-  const int t1 = c0 + tb1, t2 = t1 + (np + SMALL_CHUNK - 1) / SMALL_CHUNK, nwork = t2 + tb2;
+  const int t1 = c0 + tb1, t2 = t1 + tb2, nwork = t2 + (np + SMALL_CHUNK - 1) / SMALL_CHUNK;
   const int64_t lcap = list_cap(W.cap_bytes);
   const uint8_t *g = A.utf8 + base;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -686,21 +727,78 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
     if (lane == 0) gi = atomicAdd(&W.counters[9], 1);
     gi = __shfl_sync(0xffffffffu, gi, 0);
     if (gi >= nwork) break;
+#ifdef TT_TRACE
+    if (lane == 0) tt_trace_rounds[warp] = 0;
+    __syncwarp();
+    const unsigned long long tr0 = trace_clock();
+#endif
     if (PAIRS >= 2 && gi >= c0 && gi < t1) {     // pieces of 49..128 bytes, two a ticket
       mid_group<16, PAIR_MAX / 16>(T, W, g, W.long_list + lcap, 2 * (gi - c0), c1, s_tok, s_rank, s_res, s_nx,
                                    s_pv);
-    } else if (PAIRS >= 1 && gi >= t2) {         // pieces of 17..48 bytes, GROUP2 a ticket
-      mid_group<32 / GROUP2, (48 * GROUP2 + 31) / 32>(T, W, g, W.long_list + 2 * lcap, GROUP2 * (gi - t2), c2,
+    } else if (PAIRS >= 1 && gi >= t1 && gi < t2) {   // pieces of 17..48 bytes, GROUP2 a ticket
+      mid_group<32 / GROUP2, (48 * GROUP2 + 31) / 32>(T, W, g, W.long_list + 2 * lcap, GROUP2 * (gi - t1), c2,
                                                       s_tok, s_rank, s_res, s_nx, s_pv);
-    } else if (gi < t1 || gi >= t2) {
-      const int64_t slot = gi < c0 ? gi : gi < t1 ? lcap + (gi - c0) : 2 * lcap + (gi - t2);
+    } else if (gi < t2) {
+      const int64_t slot = gi < c0 ? gi : gi < t1 ? lcap + (gi - c0) : 2 * lcap + (gi - t1);
       mid_piece(T, W, g, __ldcg(&W.long_list[slot]), s_tok, s_rank, s_res, s_nx, s_pv);
     } else {
-      small_chunk<PAIRS >= 1>(T, W, g, total, np, (gi - t1) * SMALL_CHUNK, mq[warp], qn, v);
+      small_chunk<PAIRS >= 1>(T, W, g, total, np, (gi - t2) * SMALL_CHUNK, mq[warp], qn, v);
     }
+#ifdef TT_TRACE
+    __syncwarp();
+    if (lane == 0) {
+      // the ticket's list entries (kinds 0, 1, 3) or chunk (kind 2)
+      const int kind = gi < c0 ? 0 : gi < t1 ? 1 : gi < t2 ? 3 : 2;
+      int first = 0, cnt = 1;
+      const int32_t *list = W.long_list;
+      if (kind == 0) first = gi;
+      if (kind == 1) { list += lcap; first = PAIRS >= 2 ? 2 * (gi - c0) : gi - c0; cnt = min(PAIRS >= 2 ? 2 : 1, c1 - first); }
+      if (kind == 3) { list += 2 * lcap; first = PAIRS >= 1 ? GROUP2 * (gi - t1) : gi - t1; cnt = min(PAIRS >= 1 ? GROUP2 : 1, c2 - first); }
+      int max_len = 0;
+      if (kind == 2) {
+        cnt = min(SMALL_CHUNK, np - (gi - t2) * SMALL_CHUNK);
+        max_len = SMALL_MAX;
+      } else {
+        for (int q = 0; q < cnt; ++q) {
+          const int pc = __ldcg(&list[first + q]);
+          max_len = max(max_len, (__ldcg(&W.piece_start[pc + 1]) & 0x7FFFFFFF) - __ldcg(&W.piece_start[pc]));
+        }
+      }
+      const int at = atomicAdd(&tt_trace_n, 1);
+      if (at < TRACE_CAP) tt_trace_rec[at] = TraceRec{tr0, trace_clock(), kind, cnt, max_len, tt_trace_rounds[warp]};
+    }
+#endif
   }
+#ifdef TT_TRACE
+  if (lane == 0) tt_trace_rounds[warp] = 0;
+  __syncwarp();
+  const unsigned long long tr1 = trace_clock();
+#endif
   if (qn) run_misses(T, W, g, mq[warp], qn, v);   // the warp's last queued misses
+#ifdef TT_TRACE
+  __syncwarp();
+  if (lane == 0 && qn) {
+    const int at = atomicAdd(&tt_trace_n, 1);
+    if (at < TRACE_CAP) tt_trace_rec[at] = TraceRec{tr1, trace_clock(), 4, qn, SMALL_MAX, tt_trace_rounds[warp]};
+  }
+#endif
 }
+
+#ifdef TT_TRACE
+// Trace builds only: copy up to cap records (struct TraceRec, 32 bytes each)
+// of the traced kernels since the last call into out, return how many there
+// were, and start a new trace.
+extern "C" int tt_trace_read(void *out, int cap) {
+  int n = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(&n, tt_trace_n, sizeof(int)) != cudaSuccess) return -1;
+  const int k = n < cap ? n : cap;
+  if (k > 0 && cudaMemcpyFromSymbol(out, tt_trace_rec, (size_t)k * sizeof(TraceRec)) != cudaSuccess) return -1;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(tt_trace_n, &zero, sizeof(int)) != cudaSuccess) return -1;
+  return n;
+}
+#endif
 
 // ---------------------------------------------------------------- long
 // Block per piece.  Thread t owns a contiguous segment of the current token
