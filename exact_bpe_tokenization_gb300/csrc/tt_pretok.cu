@@ -684,11 +684,45 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
     }
     if (st) starts |= 1u << (j - c0);
   };
+  // cl100k-style tiles of 16 bytes a thread (batches): inside a letter run or
+  // a run of "other" chars no rule starts a piece (a letter run's only inner
+  // starts follow an apostrophe two or three chars back), and such chars add
+  // nothing to the scan; they are passed over reading their own and their
+  // predecessor's words, and every other char builds its neighbourhood where
+  // it stands.  Elsewhere the neighbourhood slides along the thread's chars:
+  // on text with short runs (glued kana/CJK text) or 8 bytes a thread, the
+  // lanes of a warp rarely all pass over the same step, and rebuilding a
+  // neighbourhood costs more than sliding it.
+  constexpr bool RUN_SKIP = FAM == FAM_CL100K && NT == 256;
   if constexpr (FAM == FAM_O200K) {
     for (int j = c0; j < jlo; ++j) P.chain[j] = 1;
     for (int j = jhi; j < c1; ++j) P.chain[j] = 1;
+  } else if constexpr (RUN_SKIP) {
+    for (int j = jlo; j < jhi; ++j) {
+      const uint32_t c = S.ci[j];
+      const uint8_t e0 = ci_eff(c);
+      if (!ci_rs(c) && j > 0 && (is_letter(e0) || e0 == K_OTHER)) {
+        const uint8_t e1 = ci_eff(S.ci[j - 1]);
+        if (e0 == K_OTHER ? e1 == K_OTHER
+                          : (is_letter(e1) && !(j >= 2 && ci_cp8(S.ci[j - 2]) == '\'') &&
+                             !(j >= 3 && ci_cp8(S.ci[j - 3]) == '\'')))
+          continue;
+      }
+      const Nbr nb = make_nbr(S, nullptr, j);
+      const int32_t pos = (int32_t)(ws + ci_lead(c));
+      Aggs a{};
+      if (e0 == K_NUM || e0 == K_WS) {
+        const S2L after = s2l_combine(before, s2l_element(e0, nb.e1, nb.c0, pos));
+        s2l_values(before, after, pos, a);
+        before = after;
+      }
+      if (pos >= ts) {
+        if (e0 == K_WS && is_crlf(nb.c1)) a.rq_ws = (uint8_t)(rq_after(fam, S, ws, te, j, P.rqc, true, false) & 0x3);
+        decide(j, nb, a, pos);
+      }
+    }
   }
-  if (jlo < jhi) {
+  if (!RUN_SKIP && jlo < jhi) {
     Slider w;
     w.start(S, ws, jlo);
     // chain states of the three chars before jlo (valid for o200k only where
