@@ -231,49 +231,80 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
     }
   }
 
-  // --- UTF-8 validation of the tile's bytes (RFC 3629, per request).  ASCII
-  // bytes are always valid, so only the others are visited.
+  // --- UTF-8 validation of the tile's bytes (RFC 3629, per request).  Each
+  // thread checks, in one pass over its bytes, the sequences that start among
+  // them: continuation bytes at its start that a lead before them claims are
+  // passed over (that lead's thread checks them), and a sequence open at its
+  // last byte is completed by reading on (at most three bytes).  A request
+  // is rejected for a lead whose sequence is malformed, cut by a request
+  // start or by the batch end, and for a continuation byte no lead claims or
+  // a byte no sequence starts with -- as a byte-by-byte check would find.
+  // Threads with only ASCII bytes in the tile have nothing to check.
   uint32_t hi = 0;
 #pragma unroll
   for (int q = 0; q < PT_BYTES / 4; ++q) hi |= top_bits4(wd[q]) << (4 * q);
-  for (uint32_t m = hi & in_tile; m; m &= m - 1) {
-    const int i = PT_BYTES * tid + __ffs(m) - 1;
-    const int64_t x = ws + i;
-    const uint8_t b = S.bytes[i];
-    bool bad = false;
-    if (b < 0xC0) {                    // continuation: claimed by a lead <= 3 bytes back?
-      bad = true;
-      if (!S.rsb[i]) {
-        for (int d = 1; d <= 3; ++d) {
-          const int q = i - d;
-          if (ws + q < 0) break;
-          const uint8_t bq = S.bytes[q];
-          if ((bq & 0xC0) == 0x80) { if (S.rsb[q]) break; continue; }
-          const int L = (bq >= 0xC2 && bq <= 0xDF) ? 2 : (bq >= 0xE0 && bq <= 0xEF) ? 3 : (bq >= 0xF0 && bq <= 0xF4) ? 4 : 1;
-          bad = L <= d;
-          break;
-        }
-      }
-    } else if (b >= 0xC2 && b <= 0xF4) {
-      const int L = b <= 0xDF ? 2 : b <= 0xEF ? 3 : 4;
-      for (int q = 1; q < L && !bad; ++q)
-        bad = x + q >= total || S.rsb[i + q] || (S.bytes[i + q] & 0xC0) != 0x80;
-      if (!bad) {
-        const uint8_t b1 = S.bytes[i + 1];
-        if ((b == 0xE0 && b1 < 0xA0) || (b == 0xED && b1 > 0x9F) || (b == 0xF0 && b1 < 0x90) || (b == 0xF4 && b1 > 0x8F))
-          bad = true;
-      }
-    } else {
-      bad = true;
-    }
-    if (bad) {
-      // request containing x: last r with offs[r] <= base + x
-      const int64_t r = lower_bound64(A.offs, A.n + 1, base + x + 1) - 1;
+  if (hi & in_tile) {
+    auto reject = [&](int i) {               // the request holding window byte i
+      const int64_t r = lower_bound64(A.offs, A.n + 1, base + ws + i + 1) - 1;
       if (r >= 0 && r < A.n) {
         W.bad[r] = 1;
         atomicMin(&W.status->bad_request, (unsigned long long)r);
         set_status(W.status, ST_INVALID_UTF8);
         atomicExch(&W.counters[5], 1);
+      }
+    };
+    const int f = PT_BYTES * tid + (__ffs(in_tile) - 1);      // my first byte in the tile
+    const int e = PT_BYTES * tid + (32 - __clz(in_tile));     // past my last one
+    int p = f;
+    {
+      // the nearest non-continuation byte before f (at most 3 back, not
+      // across a request start or the batch start) and the bytes from f on
+      // that it claims, if it is a lead
+      int reach = 0;
+      for (int d = 1; d <= 3; ++d) {
+        const int q = f - d;
+        if (ws + q < 0) break;
+        const uint8_t bq = S.bytes[q];
+        if ((bq & 0xC0) == 0x80) {
+          if (S.rsb[q]) break;
+          continue;
+        }
+        reach = ((bq >= 0xC2 && bq <= 0xDF) ? 2 : (bq >= 0xE0 && bq <= 0xEF) ? 3 : (bq >= 0xF0 && bq <= 0xF4) ? 4 : 1) - d;
+        break;
+      }
+      for (; reach > 0 && p < e && (S.bytes[p] & 0xC0) == 0x80 && !S.rsb[p]; --reach) ++p;
+    }
+    int need = 0, lead = -1;                 // continuation bytes the open sequence still needs, its lead
+    uint32_t lo = 0x80, top = 0xBF;          // the range of its next byte
+    for (; p < e || need > 0; ++p) {
+      const uint32_t b = S.bytes[p];
+      if (need > 0) {
+        if (!S.rsb[p] && ws + p < total && b >= lo && b <= top) {
+          --need;
+          lo = 0x80;
+          top = 0xBF;
+          continue;
+        }
+        reject(lead);                        // malformed, or cut by a request start or the batch end
+        need = 0;
+        if (p >= e) break;                   // (past my bytes: another thread checks this one)
+      }
+      if (b < 0x80) continue;
+      lead = p;
+      if (b >= 0xC2 && b <= 0xDF) {
+        need = 1;
+        lo = 0x80;
+        top = 0xBF;
+      } else if (b >= 0xE0 && b <= 0xEF) {
+        need = 2;
+        lo = b == 0xE0 ? 0xA0 : 0x80;        // no overlong three-byte form
+        top = b == 0xED ? 0x9F : 0xBF;       // no surrogate
+      } else if (b >= 0xF0 && b <= 0xF4) {
+        need = 3;
+        lo = b == 0xF0 ? 0x90 : 0x80;        // no overlong four-byte form
+        top = b == 0xF4 ? 0x8F : 0xBF;       // nothing past U+10FFFF
+      } else {
+        reject(p);                           // a continuation no lead claims, or C0, C1, F5..FF
       }
     }
   }
