@@ -295,6 +295,45 @@ extern "C" tt_status tt_create(const int32_t *merge_pairs, int64_t n_merges, con
   h->T.pair_mask = (uint32_t)(pcap - 1);
   if ((s = upload(h, result.data(), result.size() * 4, &p)) != TT_OK) return fail(s);
   h->T.merge_result = (const int32_t *)p;
+  // ---- context table: per (token, side, byte) the lowest rank of a merge
+  // that can take the token from that side (load factor <= 1/4)
+  {
+    std::unordered_map<uint32_t, uint32_t> lowest;
+    lowest.reserve((size_t)n_merges * 2);
+    for (int64_t k = 0; k < n_merges; ++k) {
+      const uint32_t l = (uint32_t)merge_pairs[2 * k], r = (uint32_t)merge_pairs[2 * k + 1];
+      const uint8_t last_l = vocab_bytes[vocab_offsets[l + 1] - 1], first_r = vocab_bytes[vocab_offsets[r]];
+      lowest.emplace(ctx_key(r, 0, last_l), (uint32_t)k);    // ranks ascend with k: the first is the lowest
+      lowest.emplace(ctx_key(l, 1, first_r), (uint32_t)k);
+    }
+    const uint64_t ccap = next_pow2((uint64_t)std::max<size_t>(4 * lowest.size(), 1024));
+    std::vector<uint2> ctab(ccap, make_uint2(CTX_EMPTY, 0));
+    for (const auto &kv : lowest) {
+      uint64_t sl = ctx_hash(kv.first) & (ccap - 1);
+      while (ctab[sl].x != CTX_EMPTY) sl = (sl + 1) & (ccap - 1);
+      ctab[sl] = make_uint2(kv.first, kv.second);
+    }
+    if ((s = upload(h, ctab.data(), ctab.size() * sizeof(uint2), &p)) != TT_OK) return fail(s);
+    h->T.ctx_tab = (const uint2 *)p;
+    h->T.ctx_mask = (uint32_t)(ccap - 1);
+    // the byte tokens' pairs and context entries, indexed directly
+    std::vector<int2> bpair(65536, make_int2(-1, -1));
+    std::vector<int32_t> bctx(2 * 65536, INT32_MAX);
+    for (int b0 = 0; b0 < 256; ++b0) {
+      for (int b1 = 0; b1 < 256; ++b1) {
+        auto it = pairs.find(pair_key((uint32_t)byte_id[b0], (uint32_t)byte_id[b1]));
+        if (it != pairs.end()) bpair[b0 << 8 | b1] = make_int2((int)it->second, result[it->second]);
+        for (uint32_t side = 0; side < 2; ++side) {
+          auto jt = lowest.find(ctx_key((uint32_t)byte_id[b0], side, (uint32_t)b1));
+          if (jt != lowest.end()) bctx[side << 16 | b0 << 8 | b1] = (int32_t)jt->second;
+        }
+      }
+    }
+    if ((s = upload(h, bpair.data(), bpair.size() * sizeof(int2), &p)) != TT_OK) return fail(s);
+    h->T.bpair = (const int2 *)p;
+    if ((s = upload(h, bctx.data(), bctx.size() * sizeof(int32_t), &p)) != TT_OK) return fail(s);
+    h->T.bctx = (const int32_t *)p;
+  }
   if ((s = upload_vocab(h, nullptr, nullptr, nullptr, 0)) != TT_OK) return fail(s);
   if ((s = upload(h, byte_id.data(), 256 * 4, &p)) != TT_OK) return fail(s);
   h->T.byte_id = (const int32_t *)p;

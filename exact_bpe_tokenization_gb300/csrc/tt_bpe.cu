@@ -104,6 +104,74 @@ __device__ __forceinline__ uint32_t pair_slot(const Tables &T, int l, int r) {
   return (uint32_t)pair_hash((uint32_t)l, (uint32_t)r) & T.pair_mask;
 }
 
+// ---------------------------------------------------------------- safe pairs
+// Merges out of rank order, exact.  A pair x.y of rank q is safe when no
+// merge of lower rank can take either token first: no merge (X, x) below q
+// has X ending with the text byte before x, and no merge (y, Z) below q has
+// Z starting with the byte after y (the context table).  Rank-ordered BPE
+// then makes exactly this merge at rank q whatever it does elsewhere before,
+// and every pair its result forms ranks above q (a merge's operands are made
+// by lower ranks), so the pair can merge in any round.  A round merges the
+// occurrences of the lowest rank r of all pairs (leftmost non-overlapping,
+// as before) and every safe pair.  None of these overlap: two adjacent pairs
+// are never both safe (each would need the other's rank to be the higher),
+// and a safe pair of rank q >= r beside an occurrence of r would have a
+// token that the merge of rank r can take.  A pair's key is 2 * rank + 1 if
+// it is safe, 2 * rank if not, INT_MAX if it is no merge: the round minimum
+// is the lowest rank's key.
+__device__ __forceinline__ bool key_safe(int k) { return (k & 1) && k != INT_MAX; }
+
+__device__ __forceinline__ uint32_t ctx_slot(const Tables &T, uint32_t key) { return ctx_hash(key) & T.ctx_mask; }
+// the rest of a context lookup whose first probe e (slot s) is loaded:
+// the lowest rank stored for key, INT_MAX if none
+__device__ __forceinline__ int ctx_finish(const Tables &T, uint2 e, uint32_t s, uint32_t key) {
+  for (;;) {
+    if (e.x == key) return (int)e.y;
+    if (e.x == CTX_EMPTY) return INT_MAX;
+    s = (s + 1) & T.ctx_mask;
+    e = __ldg(&T.ctx_tab[s]);
+  }
+}
+// First probes of the pair (l, r) and of its two context entries, all in
+// flight together; pb / nb: the text byte before l / after r, -1 at the
+// piece's edge (nothing there can take the token).
+struct PairProbe {
+  uint4 e;
+  uint2 el, er;
+  uint32_t s, sl, sr;
+};
+__device__ __forceinline__ void probe_pair(const Tables &T, bool v, int l, int r, int pb, int nb, PairProbe &P) {
+  P.s = pair_slot(T, l, r);
+  P.sl = ctx_slot(T, ctx_key((uint32_t)l, 0, (uint32_t)pb & 255u));
+  P.sr = ctx_slot(T, ctx_key((uint32_t)r, 1, (uint32_t)nb & 255u));
+  P.e = v ? __ldg(&T.pair_tab[P.s]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+  P.el = v && pb >= 0 ? __ldg(&T.ctx_tab[P.sl]) : make_uint2(CTX_EMPTY, 0);
+  P.er = v && nb >= 0 ? __ldg(&T.ctx_tab[P.sr]) : make_uint2(CTX_EMPTY, 0);
+}
+// the pair's key (INT_MAX: no merge) and its merge result
+__device__ __forceinline__ int probed_key(const Tables &T, const PairProbe &P, int l, int r, int pb, int nb,
+                                          int &res) {
+  const int2 pr = pair_finish(T, P.e, P.s, l, r);
+  res = pr.y;
+  if (pr.x < 0) return INT_MAX;
+  const bool safe = (pb < 0 || ctx_finish(T, P.el, P.sl, ctx_key((uint32_t)l, 0, (uint32_t)pb)) > pr.x) &&
+                    (nb < 0 || ctx_finish(T, P.er, P.sr, ctx_key((uint32_t)r, 1, (uint32_t)nb)) > pr.x);
+  return 2 * pr.x + (safe ? 1 : 0);
+}
+// The key and result of the pair of byte tokens b0.b1 (the bytes at p and
+// p + 1 of a piece), with the bytes pb before and nb after them (-1: the
+// piece's edge), from the direct tables.
+__device__ __forceinline__ int byte_pair_key(const Tables &T, int b0, int b1, int pb, int nb, int &res) {
+  const int2 pr = __ldg(&T.bpair[b0 << 8 | b1]);
+  const int cl = pb >= 0 ? __ldg(&T.bctx[b0 << 8 | pb]) : INT_MAX;
+  const int cr = nb >= 0 ? __ldg(&T.bctx[65536 | b1 << 8 | nb]) : INT_MAX;
+  res = pr.y;
+  if (pr.x < 0) return INT_MAX;
+  return 2 * pr.x + (cl > pr.x && cr > pr.x ? 1 : 0);
+}
+// the text byte at i of a piece of n bytes, -1 outside it
+__device__ __forceinline__ int byte_at(const uint8_t *b, int i, int n) { return i >= 0 && i < n ? (int)__ldg(b + i) : -1; }
+
 // Round merging of up to 32 / G pieces of at most G bytes at once, G lanes
 // per piece and one symbol per lane: lane p of a group holds the symbol that
 // starts at byte p (while alive), the rank and result of the pair it starts
@@ -123,13 +191,10 @@ __device__ __forceinline__ int bpe_lanes(const Tables &T, const uint8_t *bytes, 
   const unsigned below = (1u << p) - 1, above_me = ~((2u << p) - 1);
   bool alive = p < len;
   int tok = alive ? __ldg(&T.byte_id[__ldg(bytes + p)]) : -1;
-  const int tn0 = __shfl_down_sync(FULL, tok, 1);
-  int rank = INT_MAX, res = 0;
-  if (p + 1 < len) {
-    const int2 pr = pair_lookup(T, tok, tn0);
-    rank = rank_or_max(pr.x);
-    res = pr.y;
-  }
+  int rank = INT_MAX, res = 0;                 // the key of my pair (2 * rank + safe) and its result
+  if (p + 1 < len)                            // a pair of byte tokens: the direct tables
+    rank = byte_pair_key(T, __ldg(bytes + p), __ldg(bytes + p + 1), byte_at(bytes, p - 1, len),
+                         byte_at(bytes, p + 2, len), res);
   for (int round = 0; round < G; ++round) {   // each round unlinks at least one symbol
     TT_TRACE_ROUND();
     int r = rank;
@@ -140,9 +205,10 @@ __device__ __forceinline__ int bpe_lanes(const Tables &T, const uint8_t *bytes, 
       const unsigned am = (__ballot_sync(FULL, alive) >> sh) & GM;
       const unsigned lo = am & below;
       const int pvl = lo ? 31 - __clz(lo) : -1;
-      const bool hit = alive && rank == r && r != INT_MAX;
+      const bool safe = alive && key_safe(rank);
+      const bool hit = alive && !safe && rank == r && r != INT_MAX;
       const unsigned hm = (__ballot_sync(FULL, hit) >> sh) & GM;
-      const bool sel = hit && !(pvl >= 0 && ((hm >> pvl) & 1u));
+      const bool sel = safe || (hit && !(pvl >= 0 && ((hm >> pvl) & 1u)));
       const unsigned sm = (__ballot_sync(FULL, sel) >> sh) & GM;
       const bool pending = hit && !sel;
       if (sel) tok = res;
@@ -156,7 +222,7 @@ __device__ __forceinline__ int bpe_lanes(const Tables &T, const uint8_t *bytes, 
           rank = INT_MAX;
         } else {
           const int2 pr = pair_lookup(T, tok, tn);
-          rank = rank_or_max(pr.x);
+          rank = pr.x < 0 ? INT_MAX : 2 * pr.x;
           res = pr.y;
         }
       }
@@ -209,12 +275,16 @@ __device__ __forceinline__ void put_count(const Work &W, int k, int c) {
 // pieces of a warp's short-piece chunks that miss the whole-piece table
 // queue up in the warp's MissQueue, and every 32 of them are merged side by
 // side, one per lane.  A lane holds its piece as a compact array of packed
-// words -- rank of the pair the position starts << 40 | that pair's merge
+// words -- key of the pair the position starts << 40 | that pair's merge
 // result << 20 | token, with RANK_NIL for no pair or no merge -- in the
 // warp's shared arrays, word i of lane l at v[32 * i + l] (conflict-free).
-// A round: the lowest rank r over the array; one pass that merges every
-// leftmost non-overlapping occurrence of r and compacts; then lookups of the
-// pairs next to a merge, four first probes in flight at a time.
+// Keys as in the linked lists (2 * rank + safe), the safe bit found only for
+// the first pairs, from the direct tables (for pieces this short, context
+// probes at every lookup cost more than the rounds they save).  A round: the
+// lowest key r over the array; one pass that merges every leftmost
+// non-overlapping occurrence of r and every safe pair, and compacts; then
+// lookups of the pairs next to a merge, four first probes in flight at a
+// time.
 constexpr uint32_t RANK_NIL = 0xFFFFFFu;   // no rank: 2^24 - 1 is above every rank
 constexpr int MISS_QUEUE = 2 * 32;          // < 32 left over plus one chunk's 32
 struct MissQueue {
@@ -253,7 +323,7 @@ __device__ __forceinline__ void seq_lookups(const Tables &T, uint64_t *v, uint32
     for (int q = 0; q < 4; ++q) {
       if (at[q] >= 0) {
         const int2 pr = pair_finish(T, e[q], sl[q], (int)l[q], (int)r[q]);
-        v[32 * at[q] + lane] = pr.x < 0 ? pack_pos(RANK_NIL, 0, l[q]) : pack_pos((uint32_t)pr.x, (uint32_t)pr.y, l[q]);
+        v[32 * at[q] + lane] = pr.x < 0 ? pack_pos(RANK_NIL, 0, l[q]) : pack_pos(2u * (uint32_t)pr.x, (uint32_t)pr.y, l[q]);
       }
     }
   }
@@ -263,9 +333,18 @@ __device__ __forceinline__ void seq_lookups(const Tables &T, uint64_t *v, uint32
 // out and returns their count.
 __device__ __forceinline__ int seq_bpe(const Tables &T, const uint8_t *b, int n, uint64_t *v, int32_t *out) {
   const int lane = threadIdx.x & 31;
-  for (int i = 0; i < n; ++i) v[32 * i + lane] = pack_pos(RANK_NIL, 0, (uint32_t)__ldg(&T.byte_id[__ldg(b + i)]));
+  // the first pairs are pairs of byte tokens (the direct tables, keys with
+  // the safe bit); later lookups leave it clear
+  int bp = -1, b0 = __ldg(b), b1 = n > 1 ? __ldg(b + 1) : -1;
+  for (int i = 0; i < n; ++i) {
+    const int b2 = i + 2 < n ? __ldg(b + i + 2) : -1;
+    int rs = 0;
+    const int key = b1 >= 0 ? byte_pair_key(T, b0, b1, bp, b2, rs) : INT_MAX;
+    const uint32_t t = (uint32_t)__ldg(&T.byte_id[b0]);
+    v[32 * i + lane] = key == INT_MAX ? pack_pos(RANK_NIL, 0, t) : pack_pos((uint32_t)key, (uint32_t)rs, t);
+    bp = b0; b0 = b1; b1 = b2;
+  }
   int m = n;
-  seq_lookups(T, v, n > 1 ? (1u << (n - 1)) - 1 : 0u);
   int rounds = 0;
   for (int round = 0; round < n; ++round) {   // each round merges at least one pair
     uint32_t r = RANK_NIL;
@@ -278,7 +357,8 @@ __device__ __forceinline__ int seq_bpe(const Tables &T, const uint8_t *b, int n,
     uint32_t need = 0;
     for (int i = 0; i < m; ++w) {
       const uint64_t x = v[32 * i + lane];
-      if (i + 1 < m && pos_rank(x) == r) {
+      const uint32_t k = pos_rank(x);
+      if (i + 1 < m && (k == r || ((k & 1) && k != RANK_NIL))) {
         v[32 * w + lane] = pack_pos(RANK_NIL, 0, pos_res(x));
         need |= (1u << w) | (w ? 1u << (w - 1) : 0u);
         i += 2;
@@ -375,6 +455,31 @@ __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, cons
   }
 }
 
+// After a merge at position p of a linked list over a piece of n bytes at b:
+// the keys and results of the pairs (a, p) and (p, c) beside it, all their
+// probes in flight together.
+__device__ __forceinline__ void relink_lookups(const Tables &T, const uint8_t *b, int n, int p, const int32_t *tok,
+                                               int32_t *rank, int32_t *res, const int16_t *nx, const int16_t *pv) {
+  const int a = pv[p], c = nx[p];
+  const int tp = tok[p];
+  const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
+  const int e = c < n ? nx[c] : n;
+  const int pba = a >= 0 ? byte_at(b, a - 1, n) : -1, nba = byte_at(b, c, n);   // around (a, p)
+  const int pbc = byte_at(b, p - 1, n), nbc = c < n ? byte_at(b, e, n) : -1;      // around (p, c)
+  PairProbe Pa, Pc;
+  probe_pair(T, a >= 0, ta, tp, pba, nba, Pa);
+  probe_pair(T, c < n, tp, tc, pbc, nbc, Pc);
+  int rs;
+  if (a >= 0) {
+    rank[a] = probed_key(T, Pa, ta, tp, pba, nba, rs);
+    res[a] = rs;
+  }
+  if (c < n) {
+    rank[p] = probed_key(T, Pc, tp, tc, pbc, nbc, rs);
+    res[p] = rs;
+  }
+}
+
 // The linked-list rounds of one piece of n bytes (32 < n <= 32 * NS) in the
 // warp's shared arrays, NS positions per lane (lane l owns l, l + 32, ...);
 // writes the IDs to out and returns their count.  The ranks of a lane's own
@@ -393,28 +498,14 @@ __device__ __forceinline__ int list_rounds(const Tables &T, const uint8_t *b, in
     pv[p] = (int16_t)(p - 1);
   }
   __syncwarp();
-  // initial pair lookups, first probes of all slots in flight together
-  {
-    uint4 ent[NS];
-    uint32_t sl[NS];
-    int lt[NS], rt[NS];
+  // initial pair lookups (pairs of byte tokens: the direct tables)
 #pragma unroll
-    for (int k = 0; k < NS; ++k) {
-      const int p = lane + 32 * k;
-      const bool v = p + 1 < n;
-      lt[k] = v ? tok[p] : 0;
-      rt[k] = v ? tok[p + 1] : 0;
-      sl[k] = pair_slot(T, lt[k], rt[k]);
-      ent[k] = v ? __ldg(&T.pair_tab[sl[k]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-    }
-#pragma unroll
-    for (int k = 0; k < NS; ++k) {
-      const int p = lane + 32 * k;
-      if (p + 1 < n) {
-        const int2 pr = pair_finish(T, ent[k], sl[k], lt[k], rt[k]);
-        rank[p] = rank_or_max(pr.x);
-        res[p] = pr.y;
-      }
+  for (int k = 0; k < NS; ++k) {
+    const int p = lane + 32 * k;
+    if (p + 1 < n) {
+      int rs;
+      rank[p] = byte_pair_key(T, __ldg(b + p), __ldg(b + p + 1), byte_at(b, p - 1, n), byte_at(b, p + 2, n), rs);
+      res[p] = rs;
     }
   }
   __syncwarp();
@@ -438,7 +529,9 @@ __device__ __forceinline__ int list_rounds(const Tables &T, const uint8_t *b, in
       bool left = false;
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
-        if (rr[k] == r) {
+        if (key_safe(rr[k])) {
+          sel |= 1u << k;
+        } else if (rr[k] == r) {
           const int q = pv[lane + 32 * k];
           if (q < 0 || rank[q] != r) sel |= 1u << k;
           else left = true;
@@ -458,22 +551,7 @@ __device__ __forceinline__ int list_rounds(const Tables &T, const uint8_t *b, in
       __syncwarp();
       for (uint32_t m = sel; m; m &= m - 1) {
         const int p = lane + 32 * (__ffs(m) - 1);
-        const int a = pv[p], c = nx[p];
-        const int tp = tok[p];
-        const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
-        const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
-        const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-        const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-        if (a >= 0) {
-          const int2 pr = pair_finish(T, ea, sa, ta, tp);
-          rank[a] = rank_or_max(pr.x);
-          res[a] = pr.y;
-        }
-        if (c < n) {
-          const int2 pr = pair_finish(T, ec, sc, tp, tc);
-          rank[p] = rank_or_max(pr.x);
-          res[p] = pr.y;
-        }
+        relink_lookups(T, b, n, p, tok, rank, res, nx, pv);
       }
       __syncwarp();
       if (!__any_sync(0xffffffffu, left)) break;
@@ -520,27 +598,12 @@ __device__ __forceinline__ int group_rounds(const Tables &T, const uint8_t *b, i
   }
   __syncwarp();
 #pragma unroll
-  for (int k0 = 0; k0 < NS; k0 += 4) {        // initial lookups, four first probes in flight at a time
-    uint4 ent[4];
-    uint32_t sl[4];
-    int lt[4], rt[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int p = hl + G * (k0 + k);
-      const bool v = k0 + k < NS && p + 1 < n;
-      lt[k] = v ? tok[p] : 0;
-      rt[k] = v ? tok[p + 1] : 0;
-      sl[k] = pair_slot(T, lt[k], rt[k]);
-      ent[k] = v ? __ldg(&T.pair_tab[sl[k]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int p = hl + G * (k0 + k);
-      if (k0 + k < NS && p + 1 < n) {
-        const int2 pr = pair_finish(T, ent[k], sl[k], lt[k], rt[k]);
-        rank[p] = rank_or_max(pr.x);
-        res[p] = pr.y;
-      }
+  for (int k = 0; k < NS; ++k) {              // initial lookups (pairs of byte tokens: the direct tables)
+    const int p = hl + G * k;
+    if (p + 1 < n) {
+      int rs;
+      rank[p] = byte_pair_key(T, __ldg(b + p), __ldg(b + p + 1), byte_at(b, p - 1, n), byte_at(b, p + 2, n), rs);
+      res[p] = rs;
     }
   }
   __syncwarp();
@@ -565,7 +628,9 @@ __device__ __forceinline__ int group_rounds(const Tables &T, const uint8_t *b, i
       bool left = false;
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
-        if (r != INT_MAX && rr[k] == r) {
+        if (key_safe(rr[k])) {
+          sel |= 1u << k;
+        } else if (r != INT_MAX && rr[k] == r) {
           const int q = pv[hl + G * k];
           if (q < 0 || rank[q] != r) sel |= 1u << k;
           else left = true;
@@ -585,22 +650,7 @@ __device__ __forceinline__ int group_rounds(const Tables &T, const uint8_t *b, i
       __syncwarp();
       for (uint32_t m = sel; m; m &= m - 1) {
         const int p = hl + G * (__ffs(m) - 1);
-        const int a = pv[p], c = nx[p];
-        const int tp = tok[p];
-        const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
-        const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
-        const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-        const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-        if (a >= 0) {
-          const int2 pr = pair_finish(T, ea, sa, ta, tp);
-          rank[a] = rank_or_max(pr.x);
-          res[a] = pr.y;
-        }
-        if (c < n) {
-          const int2 pr = pair_finish(T, ec, sc, tp, tc);
-          rank[p] = rank_or_max(pr.x);
-          res[p] = pr.y;
-        }
+        relink_lookups(T, b, n, p, tok, rank, res, nx, pv);
       }
       __syncwarp();
       if (!__any_sync(FULL, left)) break;

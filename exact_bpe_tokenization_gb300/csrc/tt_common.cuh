@@ -65,6 +65,14 @@ struct Tables {
   const uint8_t *vbytes;
   const int32_t *voff;
   const int32_t *byte_id;     // [256]
+  const uint2 *ctx_tab;       // {ctx_key, lowest rank}: see ctx_key
+  uint32_t ctx_mask;
+  // the same for the byte tokens, indexed directly (a piece's first lookups):
+  // bpair[b0 << 8 | b1] = {rank or -1, result} of the pair of byte tokens,
+  // bctx[side << 16 | b << 8 | c] = the context table's entry for the byte
+  // token b (INT_MAX: none)
+  const int2 *bpair;
+  const int32_t *bctx;
   int32_t max_tok_len;
   int32_t family;
   // added-token literals (n_lit == 0: none)
@@ -95,6 +103,21 @@ TT_HD uint32_t pair_hash(uint32_t l, uint32_t r) {
   return h;
 }
 TT_HD uint64_t pair_key(uint32_t l, uint32_t r) { return ((uint64_t)l << MAX_VOCAB_BITS) | r; }
+
+// Context table of the out-of-order merges: for a token t and a byte c,
+// side 0 holds the lowest rank of a merge (X, t) whose X ends with byte c
+// (one that can take t from the left when c precedes it in the text), side
+// 1 the lowest rank of a merge (t, Z) whose Z starts with byte c (one that
+// can take t from the right when c follows it); no entry: no such merge.
+constexpr uint32_t CTX_EMPTY = 0xFFFFFFFFu;
+TT_HD uint32_t ctx_key(uint32_t t, uint32_t side, uint32_t c) { return (t << 9) | (side << 8) | c; }
+TT_HD uint32_t ctx_hash(uint32_t k) {
+  k *= 0x9E3779B1u;
+  k ^= k >> 16;
+  k *= 0x85EBCA77u;
+  k ^= k >> 13;
+  return k;
+}
 
 // hash of a byte string, 8 bytes at a time (little-endian words, zero padded)
 struct ByteHash {

@@ -166,6 +166,28 @@ def test_pieces_merged_two_to_a_warp_in_large_batches(cuda, vocabs):
     check(cuda, vocabs["c1"], 1, reqs + [filler] + reqs[::-1])
 
 
+@pytest.mark.parametrize("large", [False, True])
+def test_out_of_order_merges_on_small_alphabets(cuda, large):
+    """Letter pieces of 17..90 chars over two- and three-symbol alphabets
+    (ASCII letters, a 2-byte and a 3-byte letter), runs of one letter among
+    them, with a vocabulary of 3,000 merges trained on the same text: merges
+    overlap and most pairs have a lower-ranked rival on one side, so merging
+    a pair out of rank order when some lower-ranked merge could still take
+    one of its tokens would change the IDs.  large: a batch beyond 4 MiB
+    (pieces two and four to a warp)."""
+    rng = random.Random(5)
+    words = []
+    for _ in range(3000):
+        alpha = rng.choice(["ab", "abc", "ab日", "aé", "a"])
+        words.append("".join(rng.choice(alpha) for _ in range(rng.randint(17, 90))))
+    reqs = [" ".join(words[i:i + 30]) for i in range(0, len(words), 30)]
+    merges = synth.train_merges(" ".join(reqs).encode(), 3000)
+    vb, vo = synth.vocab_from_merges(merges)
+    if large:
+        reqs = reqs * 28
+    check(cuda, (merges, vb, vo), 1, reqs)
+
+
 # ------------------------------------------------------------ edge cases
 def test_empty_and_degenerate_batches(cuda, vocabs):
     merges, vb, vo = vocabs["small1"]
