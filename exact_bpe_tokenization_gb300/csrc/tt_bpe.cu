@@ -868,7 +868,8 @@ __device__ __forceinline__ int cached_rank(const Tables &T, int l, int r, int &c
 // Pieces of up to LONG_SMEM_MAX bytes run the warp kernel's linked-list
 // rounds with the whole block: the list lives in dynamic shared memory
 // (thread t owns positions t, t + NT, ...), the round minimum is a block
-// reduction, and each merge step costs three barriers and one lookup.
+// reduction, and each merge step costs three barriers and one lookup; safe
+// pairs merge in any round, as in the warp rounds.
 constexpr int LONG_SMEM_MAX = 8192;
 constexpr size_t LONG_SMEM_BYTES = (size_t)LONG_SMEM_MAX * (4 + 4 + 4 + 2 + 2);
 static_assert(LONG_SMEM_MAX / BPE_LONG_THREADS <= 32, "slot mask is 32 bits");
@@ -891,27 +892,12 @@ __device__ void bpe_block_list(const Tables &T, const Work &W, const uint8_t *b,
     pv[p] = (int16_t)(p - 1);
   }
   __syncthreads();
-  for (int k0 = 0; k0 < nslot; k0 += 4) {
-    uint4 ent[4];
-    uint32_t sl[4];
-    int lt[4], rt[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int p = tid + NT * (k0 + j);
-      const bool v = k0 + j < nslot && p + 1 < n;
-      lt[j] = v ? tok[p] : 0;
-      rt[j] = v ? tok[p + 1] : 0;
-      sl[j] = pair_slot(T, lt[j], rt[j]);
-      ent[j] = v ? __ldg(&T.pair_tab[sl[j]]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int p = tid + NT * (k0 + j);
-      if (k0 + j < nslot && p + 1 < n) {
-        const int2 pr = pair_finish(T, ent[j], sl[j], lt[j], rt[j]);
-        rank[p] = rank_or_max(pr.x);
-        res[p] = pr.y;
-      }
+  for (int k = 0; k < nslot; ++k) {            // first lookups: pairs of byte tokens, the direct tables
+    const int p = tid + NT * k;
+    if (p + 1 < n) {
+      int rs;
+      rank[p] = byte_pair_key(T, __ldg(b + p), __ldg(b + p + 1), byte_at(b, p - 1, n), byte_at(b, p + 2, n), rs);
+      res[p] = rs;
     }
   }
   __syncthreads();
@@ -928,7 +914,10 @@ __device__ void bpe_block_list(const Tables &T, const Work &W, const uint8_t *b,
       bool pending = false;
       for (int k = 0; k < nslot; ++k) {
         const int p = tid + NT * k;
-        if (rank[p] == r) {
+        const int key = rank[p];
+        if (key_safe(key)) {
+          sel |= 1u << k;
+        } else if (key == r) {
           const int q = pv[p];
           if (q < 0 || rank[q] != r) sel |= 1u << k;
           else pending = true;
@@ -946,25 +935,7 @@ __device__ void bpe_block_list(const Tables &T, const Work &W, const uint8_t *b,
         if (nq < n) pv[nq] = (int16_t)p;
       }
       __syncthreads();
-      for (uint32_t m = sel; m; m &= m - 1) {
-        const int p = tid + NT * (__ffs(m) - 1);
-        const int a = pv[p], c = nx[p];
-        const int tp = tok[p];
-        const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
-        const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
-        const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-        const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
-        if (a >= 0) {
-          const int2 pr = pair_finish(T, ea, sa, ta, tp);
-          rank[a] = rank_or_max(pr.x);
-          res[a] = pr.y;
-        }
-        if (c < n) {
-          const int2 pr = pair_finish(T, ec, sc, tp, tc);
-          rank[p] = rank_or_max(pr.x);
-          res[p] = pr.y;
-        }
-      }
+      for (uint32_t m = sel; m; m &= m - 1) relink_lookups(T, b, n, tid + NT * (__ffs(m) - 1), tok, rank, res, nx, pv);
       if (!__syncthreads_or(pending)) break;
     }
   }
