@@ -457,12 +457,30 @@ __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, cons
 
 // After a merge at position p of a linked list over a piece of n bytes at b:
 // the keys and results of the pairs (a, p) and (p, c) beside it, all their
-// probes in flight together.
+// probes in flight together.  CTX: test safety (else the keys say "not
+// safe", which is always exact).
+template <bool CTX = true>
 __device__ __forceinline__ void relink_lookups(const Tables &T, const uint8_t *b, int n, int p, const int32_t *tok,
                                                int32_t *rank, int32_t *res, const int16_t *nx, const int16_t *pv) {
   const int a = pv[p], c = nx[p];
   const int tp = tok[p];
   const int ta = a >= 0 ? tok[a] : 0, tc = c < n ? tok[c] : 0;
+  if (!CTX) {
+    const uint32_t sa = pair_slot(T, ta, tp), sc = pair_slot(T, tp, tc);
+    const uint4 ea = a >= 0 ? __ldg(&T.pair_tab[sa]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+    const uint4 ec = c < n ? __ldg(&T.pair_tab[sc]) : make_uint4(PAIR_EMPTY, 0, 0, 0);
+    if (a >= 0) {
+      const int2 pr = pair_finish(T, ea, sa, ta, tp);
+      rank[a] = pr.x < 0 ? INT_MAX : 2 * pr.x;
+      res[a] = pr.y;
+    }
+    if (c < n) {
+      const int2 pr = pair_finish(T, ec, sc, tp, tc);
+      rank[p] = pr.x < 0 ? INT_MAX : 2 * pr.x;
+      res[p] = pr.y;
+    }
+    return;
+  }
   const int e = c < n ? nx[c] : n;
   const int pba = a >= 0 ? byte_at(b, a - 1, n) : -1, nba = byte_at(b, c, n);   // around (a, p)
   const int pbc = byte_at(b, p - 1, n), nbc = c < n ? byte_at(b, e, n) : -1;      // around (p, c)
@@ -578,9 +596,14 @@ __device__ __forceinline__ int list_rounds(const Tables &T, const uint8_t *b, in
 // group passes its own piece (n = 0: none) and gets its IDs' count.  For
 // batches, where warps are the scarce resource: a round's instructions serve
 // several pieces.
-// NS: positions per lane (pieces of at most G * NS bytes).
+// NS: positions per lane (pieces of at most G * NS bytes).  CTX: the
+// lookups after a merge test safety (groups of 16 lanes); the groups of 8
+// lanes (pieces of 17..48 bytes, four a warp) find it for their first pairs
+// only, which measured faster for them (burst k_bpe_warp 0.468 -> 0.447 ms,
+// o200k-style batch 1.59 -> 1.56 ms) and slower for the groups of 16 (0.468
+// -> 0.526 ms).
 constexpr int PAIR_MAX = MID_MAX / 2;
-template <int G, int NS>
+template <int G, int NS, bool CTX = (G >= 16)>
 __device__ __forceinline__ int group_rounds(const Tables &T, const uint8_t *b, int n, int32_t *out, int32_t *tok,
                                             int32_t *rank, int32_t *res, int16_t *nx, int16_t *pv) {
   static_assert(G * NS <= MID_MAX * G / 32, "a group's share of the arrays");
@@ -650,7 +673,7 @@ __device__ __forceinline__ int group_rounds(const Tables &T, const uint8_t *b, i
       __syncwarp();
       for (uint32_t m = sel; m; m &= m - 1) {
         const int p = hl + G * (__ffs(m) - 1);
-        relink_lookups(T, b, n, p, tok, rank, res, nx, pv);
+        relink_lookups<CTX>(T, b, n, p, tok, rank, res, nx, pv);
       }
       __syncwarp();
       if (!__any_sync(FULL, left)) break;
