@@ -389,69 +389,72 @@ __device__ __forceinline__ void run_misses(const Tables &T, const Work &W, const
   __syncwarp();
 }
 
-// One chunk of 32 consecutive pieces: each lane tries the whole-piece
-// shortcut for its piece of at most SMALL_MAX bytes (longer ones are listed
-// by k_pretok) and the misses join the warp's queue.  QUEUE: 32 queued
-// misses are merged as soon as they are there (batches: full warps); else a
-// chunk's misses are merged at once (a single request, whose latency a
-// queue's leftovers at the end of the kernel would lengthen).  qn: the
-// queue's length (warp-uniform).
+// R chunks of 32 consecutive pieces from kb on: each lane tries the
+// whole-piece shortcut for its piece of at most SMALL_MAX bytes (longer ones
+// are listed by k_pretok) and the misses join the warp's queue; 32 queued
+// misses are merged as soon as they are there.  QUEUE: the rest stay queued
+// (batches: full warps); else they are merged at the end of the ticket (a
+// single request, whose latency a queue's leftovers at the end of the
+// kernel would lengthen).  qn: the queue's length (warp-uniform).
 template <bool QUEUE>
 __device__ __forceinline__ void small_chunk(const Tables &T, const Work &W, const uint8_t *g, int64_t total, int np,
-                                            int kb, MissQueue &Q, int &qn, uint64_t *v) {
+                                            int kb, int R, MissQueue &Q, int &qn, uint64_t *v) {
   const int lane = threadIdx.x & 31;
-  const int k = kb + lane;
-  int32_t s = 0;
-  int len = 0;
-  bool miss = false;
-  int mine = 0;                                 // IDs this lane wrote counts for
-  if (k < np) {
-    s = __ldcg(&W.piece_start[k]);
-    if (s < 0) {
-      W.n_ids[k] = 0;                                                  // rejected request
-    } else {
-      const int32_t e = __ldcg(&W.piece_start[k + 1]) & 0x7FFFFFFF;
-      len = e - s;
-      if (len <= 0 || e > total) {
-        W.n_ids[k] = 0;
-        set_status(W.status, ST_INVALID_ARG);
-      } else if (len <= SMALL_MAX) {
-        const int id = len <= T.max_tok_len ? vocab_probe(T, g + s, len) : -1;
-        if (id >= 0) {
-          W.scratch[s] = id;
-          W.n_ids[k] = 1;
-          mine = 1;
-        } else {
-          miss = true;
+  for (int r = 0; r < R; ++r) {
+    const int k = kb + 32 * r + lane;
+    int32_t s = 0;
+    int len = 0;
+    bool miss = false;
+    int mine = 0;                               // IDs this lane wrote counts for
+    if (k < np) {
+      s = __ldcg(&W.piece_start[k]);
+      if (s < 0) {
+        W.n_ids[k] = 0;                                                // rejected request
+      } else {
+        const int32_t e = __ldcg(&W.piece_start[k + 1]) & 0x7FFFFFFF;
+        len = e - s;
+        if (len <= 0 || e > total) {
+          W.n_ids[k] = 0;
+          set_status(W.status, ST_INVALID_ARG);
+        } else if (len <= SMALL_MAX) {
+          const int id = len <= T.max_tok_len ? vocab_probe(T, g + s, len) : -1;
+          if (id >= 0) {
+            W.scratch[s] = id;
+            W.n_ids[k] = 1;
+            mine = 1;
+          } else {
+            miss = true;
+          }
         }
       }
     }
-  }
-  // the hits' counts, all in one ID chunk
+    // the hits' counts, all in one ID chunk
 #pragma unroll
-  for (int d = 16; d; d >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, d);
-  if (lane == 0 && mine) atomicAdd(&W.ids_agg[kb / IDS_CHUNK], mine);
-  const unsigned mm = __ballot_sync(0xffffffffu, miss);
-  if (miss) {
-    const int at = qn + __popc(mm & ((1u << lane) - 1));
-    Q.piece[at] = k;
-    Q.start[at] = s;
-    Q.len[at] = (uint8_t)len;
+    for (int d = 16; d; d >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, d);
+    if (lane == 0 && mine) atomicAdd(&W.ids_agg[kb / IDS_CHUNK], mine);
+    const unsigned mm = __ballot_sync(0xffffffffu, miss);
+    if (miss) {
+      const int at = qn + __popc(mm & ((1u << lane) - 1));
+      Q.piece[at] = k;
+      Q.start[at] = s;
+      Q.len[at] = (uint8_t)len;
+    }
+    qn += __popc(mm);
+    __syncwarp();
+    if (qn >= 32) {
+      run_misses(T, W, g, Q, 32, v);
+      const bool mv = lane < qn - 32;           // move the rest to the front
+      int rk = 0, rs = 0, rl = 0;
+      if (mv) { rk = Q.piece[32 + lane]; rs = Q.start[32 + lane]; rl = Q.len[32 + lane]; }
+      __syncwarp();
+      if (mv) { Q.piece[lane] = rk; Q.start[lane] = rs; Q.len[lane] = (uint8_t)rl; }
+      __syncwarp();
+      qn -= 32;
+    }
   }
-  qn += __popc(mm);
-  __syncwarp();
-  if (!QUEUE) {
-    if (qn) run_misses(T, W, g, Q, qn, v);
+  if (!QUEUE && qn) {
+    run_misses(T, W, g, Q, qn, v);
     qn = 0;
-  } else if (qn >= 32) {
-    run_misses(T, W, g, Q, 32, v);
-    const bool mv = lane < qn - 32;             // move the rest to the front
-    int rk = 0, rs = 0, rl = 0;
-    if (mv) { rk = Q.piece[32 + lane]; rs = Q.start[32 + lane]; rl = Q.len[32 + lane]; }
-    __syncwarp();
-    if (mv) { Q.piece[lane] = rk; Q.start[lane] = rs; Q.len[lane] = (uint8_t)rl; }
-    __syncwarp();
-    qn -= 32;
   }
 }
 
@@ -787,7 +790,13 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
   // the kernel).  In batches the pieces of 49..128 bytes go two to a ticket
   // and those of 17..48 bytes GROUP2 to a ticket.
   const int tb1 = PAIRS >= 2 ? (c1 + 1) / 2 : c1, tb2 = PAIRS >= 1 ? (c2 + GROUP2 - 1) / GROUP2 : c2;
-  const int t1 = c0 + tb1, t2 = t1 + tb2, nwork = t2 + (np + SMALL_CHUNK - 1) / SMALL_CHUNK;
+  // a single request with more chunks of short pieces than the grid has
+  // warps takes two chunks a ticket (their misses merged together: fuller
+  // lanes, 1M-char request 0.087 -> 0.078 ms); a smaller one keeps one
+  // chunk a ticket for more tickets in flight
+  const int R = PAIRS == 0 && (int64_t)np > (int64_t)SMALL_CHUNK * gridDim.x * (blockDim.x / 32) ? 2 : 1;
+  const int CH = SMALL_CHUNK * R;
+  const int t1 = c0 + tb1, t2 = t1 + tb2, nwork = t2 + (np + CH - 1) / CH;
   const int64_t lcap = list_cap(W.cap_bytes);
   const uint8_t *g = A.utf8 + base;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -815,7 +824,7 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
       const int64_t slot = gi < c0 ? gi : gi < t1 ? lcap + (gi - c0) : 2 * lcap + (gi - t1);
       mid_piece(T, W, g, __ldcg(&W.long_list[slot]), s_tok, s_rank, s_res, s_nx, s_pv);
     } else {
-      small_chunk<PAIRS >= 1>(T, W, g, total, np, (gi - t2) * SMALL_CHUNK, mq[warp], qn, v);
+      small_chunk<PAIRS >= 1>(T, W, g, total, np, (gi - t2) * CH, R, mq[warp], qn, v);
     }
 #ifdef TT_TRACE
     __syncwarp();
@@ -829,7 +838,7 @@ __global__ void __launch_bounds__(BPE_WARP_THREADS, BPE_WARP_CTAS_PER_SM) k_bpe_
       if (kind == 3) { list += 2 * lcap; first = PAIRS >= 1 ? GROUP2 * (gi - t1) : gi - t1; cnt = min(PAIRS >= 1 ? GROUP2 : 1, c2 - first); }
       int max_len = 0;
       if (kind == 2) {
-        cnt = min(SMALL_CHUNK, np - (gi - t2) * SMALL_CHUNK);
+        cnt = min(CH, np - (gi - t2) * CH);
         max_len = SMALL_MAX;
       } else {
         for (int q = 0; q < cnt; ++q) {
