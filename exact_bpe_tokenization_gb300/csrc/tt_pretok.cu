@@ -732,14 +732,34 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
     for (int j = jlo; j < jhi; ++j) {
       const uint32_t c = S.ci[j];
       const uint8_t e0 = ci_eff(c);
-      if (!ci_rs(c) && j > 0 && (is_letter(e0) || e0 == K_OTHER)) {
-        const uint8_t e1 = ci_eff(S.ci[j - 1]);
+      const bool rs = ci_rs(c);
+      uint8_t e1 = K_NONE;
+      uint32_t c1 = 0;
+      if (!rs && j > 0) {
+        const uint32_t w1 = S.ci[j - 1];
+        e1 = ci_eff(w1);
+        c1 = ci_cp8(w1);
+      }
+      if (!rs && j > 0 && (is_letter(e0) || e0 == K_OTHER)) {
         if (e0 == K_OTHER ? e1 == K_OTHER
                           : (is_letter(e1) && !(j >= 2 && ci_cp8(S.ci[j - 2]) == '\'') &&
                              !(j >= 3 && ci_cp8(S.ci[j - 3]) == '\'')))
           continue;
       }
-      const Nbr nb = make_nbr(S, nullptr, j);
+      // the near fields suffice except for a letter after an "other" char or a letter
+      Nbr nb;
+      if (needs_far_nbr(e0, e1)) {
+        nb = make_nbr(S, nullptr, j);
+      } else {
+        nb.e0 = e0; nb.c0 = ci_cp8(c); nb.rs = rs; nb.e1 = e1; nb.c1 = c1;
+        nb.e2 = nb.e3 = nb.e4 = K_NONE; nb.c2 = nb.c3 = nb.c4 = 0;
+        nb.en1 = nb.en2 = K_NONE; nb.cn1 = nb.cn2 = 0;
+        nb.l1 = nb.l2 = nb.l3 = true;
+        if (j + 1 < S.nch) {
+          const uint32_t w = S.ci[j + 1];
+          if (!ci_rs(w)) { nb.en1 = ci_eff(w); nb.cn1 = ci_cp8(w); }
+        }
+      }
       const int32_t pos = (int32_t)(ws + ci_lead(c));
       Aggs a{};
       if (e0 == K_NUM || e0 == K_WS) {

@@ -188,6 +188,13 @@ TT_HD bool piece_start(int fam, const Nbr &n, const Aggs &a) {
   return false;
 }
 
+// The families without a case rule: the predicate reads of a char's
+// neighbourhood only rs, e0, e1, c0, c1, en1 and cn1, except for a letter
+// after an "other" char (the optional-prefix rule reads e2 and c2) or after
+// a letter (the contraction rules read two to four chars back).  Where this
+// is false, a neighbourhood holding just those fields decides exactly.
+TT_HD bool needs_far_nbr(uint8_t e0, uint8_t e1) { return is_letter(e0) && (e1 == K_OTHER || is_letter(e1)); }
+
 // ---------------------------------------------------------------- events
 // o200k mark resolution ("scan 1"), on raw kinds.  An other/mark stretch
 // starts at j; a trigger at j switches the rest of its stretch to "other".

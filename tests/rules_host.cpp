@@ -94,6 +94,16 @@ extern "C" void rules_host_starts(int fam, const uint32_t *cp, const uint8_t *ra
     a.rq_ws = rq_ws[j];
     a.rq_up = rq_up[j];
     start[j] = piece_start(fam, b, a) ? 1 : 0;
+    if (fam != FAM_O200K && !needs_far_nbr(b.e0, b.e1)) {
+      // the near fields alone decide: every other field scrambled
+      Nbr nb = b;
+      nb.e2 = nb.e3 = nb.e4 = (uint8_t)((j * 7 + 3) % 8);
+      nb.c2 = nb.c3 = nb.c4 = (j & 1) ? (uint32_t)'\'' : (uint32_t)' ';
+      nb.en2 = (uint8_t)((j * 5 + 1) % 8);
+      nb.cn2 = (j & 2) ? (uint32_t)'s' : (uint32_t)'\n';
+      nb.l1 = nb.l2 = nb.l3 = (j & 4) != 0;
+      if ((piece_start(fam, nb, a) ? 1 : 0) != start[j]) start[j] = 3;   // 3: the near fields do not decide
+    }
   }
 }
 

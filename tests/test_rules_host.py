@@ -86,6 +86,7 @@ def rule_starts(lib, family, kinds, strings):
     # 2 marks a char where the 12-byte scan state of the families without a
     # case rule and the general 20-byte one give different aggregates
     assert not (out == 2).any(), "the two forms of the forward scan disagree"
+    assert not (out == 3).any(), "a char decided from its near neighbourhood alone differs"
     res, k = [], 0
     for s in strings:
         n = len(s)
