@@ -773,7 +773,50 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
       }
     }
   }
-  if (!RUN_SKIP && jlo < jhi) {
+  if constexpr (FAM != FAM_O200K && !RUN_SKIP) {
+    // the other tiles of the families without a case rule: the near fields
+    // (own, predecessor's, successor's word) slide along the thread's chars
+    // with the code points two and three back; a letter after a letter
+    // starts nothing unless an apostrophe is two or three back, and a letter
+    // after an "other" char or an apostrophe builds the rest
+    if (jlo < jhi) {
+      uint32_t w0 = S.ci[jlo];
+      uint32_t wp = jlo > 0 ? S.ci[jlo - 1] : 0;
+      uint32_t cp2 = jlo > 1 ? ci_cp8(S.ci[jlo - 2]) : 0, cp3 = jlo > 2 ? ci_cp8(S.ci[jlo - 3]) : 0;
+      for (int j = jlo; j < jhi; ++j) {
+        const uint32_t wn = j + 1 < S.nch ? S.ci[j + 1] : (1u << 29);   // past the window: a request start
+        const bool rs = ci_rs(w0);
+        Nbr nb;
+        nb.e0 = ci_eff(w0); nb.c0 = ci_cp8(w0); nb.rs = rs;
+        const bool in_p = !rs && j > 0, in_n = !ci_rs(wn);
+        nb.e1 = in_p ? ci_eff(wp) : (uint8_t)K_NONE;
+        nb.c1 = in_p ? ci_cp8(wp) : 0;
+        nb.en1 = in_n ? ci_eff(wn) : (uint8_t)K_NONE;
+        nb.cn1 = in_n ? ci_cp8(wn) : 0;
+        nb.e2 = nb.e3 = nb.e4 = K_NONE; nb.c2 = nb.c3 = nb.c4 = 0;
+        nb.en2 = K_NONE; nb.cn2 = 0;
+        nb.l1 = nb.l2 = nb.l3 = true;
+        const int32_t pos = (int32_t)(ws + ci_lead(w0));
+        Aggs a{};
+        if (nb.e0 == K_NUM || nb.e0 == K_WS) {   // the only chars whose rules read scan values
+          const S2L after = s2l_combine(before, s2l_element(nb.e0, nb.e1, nb.c0, pos));
+          s2l_values(before, after, pos, a);
+          before = after;
+        }
+        const bool inner = is_letter(nb.e0) && is_letter(nb.e1) && cp2 != '\'' && cp3 != '\'';
+        if (pos >= ts && !inner) {
+          if (needs_far_nbr(nb.e0, nb.e1)) nb = make_nbr(S, nullptr, j);
+          if (nb.e0 == K_WS && is_crlf(nb.c1)) a.rq_ws = (uint8_t)(rq_after(fam, S, ws, te, j, P.rqc, true, false) & 0x3);
+          decide(j, nb, a, pos);
+        }
+        cp3 = cp2;
+        cp2 = ci_cp8(wp);
+        wp = w0;
+        w0 = wn;
+      }
+    }
+  }
+  if (FAM == FAM_O200K && jlo < jhi) {
     Slider w;
     w.start(S, ws, jlo);
     // chain states of the three chars before jlo (valid for o200k only where
