@@ -6,19 +6,23 @@
 // vocabulary entry is emitted as that one ID (the whole-piece shortcut).
 // Otherwise merging proceeds in rounds: the lowest rank present among
 // adjacent pairs names one pair, and every leftmost non-overlapping
-// occurrence of it is merged in one sweep; only pairs next to a merge are
-// looked up again.  With a well-ordered merge list (checked when the handle
-// is created) a round equals that many single leftmost merges.
+// occurrence of it is merged in one sweep, together with every safe pair
+// (one that no merge of lower rank can take a token from: see "safe pairs"
+// below); only pairs next to a merge are looked up again.  With a
+// well-ordered merge list (checked when the handle is created) the result
+// equals merging the lowest-ranked leftmost pair one at a time.
 //
-// Execution units by piece length: up to 16 bytes a thread per piece for
-// the whole-piece probe and 16 lanes per piece for merging (state in
-// registers), a warp per piece up to 256 bytes (registers up to 32 bytes,
-// else a linked list in shared memory), a 512-thread block per longer piece
-// (a linked list in shared memory up to 8 KiB, else global ping-pong
-// buffers).  IDs land in a byte-indexed scratch array, and each piece's ID
-// count is also added into its 512-piece chunk's total; k_idscan (one CTA)
-// scans the chunk totals, and k_ids scans each chunk's counts on its own,
-// writes the final contiguous IDs and each request's ID offset.
+// Execution units by piece length: a lane per piece of up to 16 bytes for
+// the whole-piece probe, a miss merged by one lane (in batches, 32 queued
+// misses side by side); a warp per piece of up to 256 bytes (in batches the
+// pieces of 17..48 bytes four to a warp and of 49..128 bytes two to a warp;
+// for a single request, one symbol a lane in registers up to 32 bytes, else
+// a linked list in shared memory); a 512-thread block per longer piece (a
+// linked list in shared memory up to 8 KiB, else global ping-pong buffers).
+// IDs land in a byte-indexed scratch array, and each piece's ID count is
+// also added into its 512-piece chunk's total; k_idscan (one CTA) scans the
+// chunk totals, and k_ids scans each chunk's counts on its own, writes the
+// final contiguous IDs and each request's ID offset.
 #include <limits.h>
 
 #include "tt_common.cuh"
