@@ -1,9 +1,11 @@
 """Pins of the oracle's piece encoder E (TokTier §4.2: rank-ordered merges
 per piece; the ignore_merges whole-piece shortcut) against things other than
 itself: the textbook definition on every short string, hand-worked results,
-the zero-merge closed form, losslessness and the fixpoint property, and the
+the zero-merge closed form, losslessness and the fixpoint property, the
 round-equivalence the GPU schedule relies on (with the counterexample that
-shows why the vocabulary must be well-ordered)."""
+shows why the vocabulary must be well-ordered), and the equivalence of the
+GPU's rounds with safe pairs merged early (with a planted mistake that the
+comparison catches)."""
 import random
 
 import numpy as np
@@ -141,6 +143,117 @@ def test_round_equivalence_needs_well_ordering():
     ranks, results, _ = tables(m, toks)
     assert o.encode_bytes(b"abab", plain=True) == [257, Bc]
     assert round_parallel(b"abab", ranks, results) == [256, 256]
+
+
+def safe_rounds(b, merges, toks, ranks, results, wrong_minimum=False):
+    """The rounds with safe pairs that the warp and block BPE run.  A pair
+    x.y of rank q is safe when no merge of lower rank can take x from the left
+    (a merge (X, x) whose X ends with the text byte before x) or y from the
+    right (a merge (y, Z) whose Z starts with the byte after y).  A round
+    merges every safe pair and the leftmost non-overlapping occurrences of
+    the lowest rank of all pairs.  wrong_minimum: take the round minimum over
+    the pairs that are not safe only (a planted mistake)."""
+    take_left, take_right = {}, {}
+    for k, (l, r) in enumerate(merges.tolist()):
+        take_left.setdefault((r, toks[l][-1]), k)
+        take_right.setdefault((l, toks[r][0]), k)
+    ids, start = list(b), list(range(len(b)))
+    while True:
+        n = len(ids)
+        rs = [ranks.get((ids[i], ids[i + 1])) for i in range(n - 1)]
+        if all(r is None for r in rs):
+            return ids
+        safe = []
+        for i in range(n - 1):
+            q = rs[i]
+            end = start[i + 2] if i + 2 < n else len(b)
+            before = b[start[i] - 1] if start[i] > 0 else None
+            after = b[end] if end < len(b) else None
+            safe.append(q is not None and
+                        (before is None or take_left.get((ids[i], before), q + 1) > q) and
+                        (after is None or take_right.get((ids[i + 1], after), q + 1) > q))
+        pool = [r for i, r in enumerate(rs) if r is not None and not (wrong_minimum and safe[i])]
+        r = min(pool) if pool else None
+        sel = list(safe)
+        i = 0
+        while i < n - 1:
+            if not safe[i] and rs[i] is not None and rs[i] == r:
+                if wrong_minimum and ((i > 0 and sel[i - 1]) or (i + 2 < n and sel[i + 1])):
+                    i += 1
+                    continue
+                sel[i] = True
+                i += 2
+            else:
+                i += 1
+        assert not any(sel[i] and sel[i + 1] for i in range(n - 2)), "merges overlap"
+        out, i = [], 0
+        while i < n:
+            if i + 1 < n and sel[i]:
+                out.append(results[(ids[i], ids[i + 1])])
+                i += 2
+            else:
+                out.append(ids[i])
+                i += 1
+        ids, start = out, _starts(out, toks)
+
+
+def _starts(ids, toks):
+    st, x = [], 0
+    for t in ids:
+        st.append(x)
+        x += len(toks[t])
+    return st
+
+
+def small_alphabet_case():
+    """Letter runs over two- and three-symbol alphabets with a vocabulary of
+    3,000 merges trained on the same text: many overlapping merges."""
+    rng = random.Random(5)
+    words = []
+    for _ in range(600):
+        alpha = rng.choice(["ab", "abc", "ab\u65e5", "a\u00e9", "a"])
+        words.append("".join(rng.choice(alpha) for _ in range(rng.randint(17, 90))))
+    text = " ".join(words)
+    merges = synth.train_merges(text.encode(), 3000)
+    vb, vo = synth.vocab_from_merges(merges)
+    toks = [bytes(vb[vo[i]:vo[i + 1]]) for i in range(len(vo) - 1)]
+    return merges, vb, vo, toks, [w.encode() for w in words]
+
+
+def test_safe_pair_rounds_equal_sequential_merging(hand, small_vocabs):
+    """Merging safe pairs out of rank order (the GPU rounds) gives the
+    sequential result: every string of length <= 6 over 'abcd' with the
+    hand-made vocabulary, 2,000 pieces of generated text with 8,000 merges,
+    and small-alphabet letter runs with a vocabulary trained on them."""
+    o, m, toks = hand
+    ranks, results, _ = tables(m, toks)
+    for s in brute.all_strings("abcd", 6):
+        assert safe_rounds(s.encode(), m, toks, ranks, results) == o.encode_bytes(s.encode(), plain=True), s
+    m, vb, vo = small_vocabs[1]
+    toks = [bytes(vb[vo[i]:vo[i + 1]]) for i in range(len(vo) - 1)]
+    ranks, results, _ = tables(m, toks)
+    o = oracle.Oracle(m, vb, vo, 1)
+    text = synth.transcript(11, 60000, 1).decode()
+    pieces = oracle.pretokenizer(1).pieces(text)
+    for p in random.Random(4).sample(pieces, 2000):
+        b = p.encode()
+        assert safe_rounds(b, m, toks, ranks, results) == o.encode_bytes(b, plain=True), p
+    m, vb, vo, toks, words = small_alphabet_case()
+    ranks, results, _ = tables(m, toks)
+    o = oracle.Oracle(m, vb, vo, 1)
+    for w in words:
+        assert safe_rounds(w, m, toks, ranks, results) == o.encode_bytes(w, plain=True), w
+
+
+def test_safe_pair_rounds_planted_minimum_mistake_is_caught():
+    """The comparison above discriminates: taking the round minimum over the
+    pairs that are not safe lets a lower-ranked safe pair lose a token to a
+    merge it precedes, and changes the result of some small-alphabet run."""
+    m, vb, vo, toks, words = small_alphabet_case()
+    ranks, results, _ = tables(m, toks)
+    o = oracle.Oracle(m, vb, vo, 1)
+    assert any(safe_rounds(w, m, toks, ranks, results, wrong_minimum=True) != o.encode_bytes(w, plain=True)
+               for w in words)
 
 
 def test_seam_example():
