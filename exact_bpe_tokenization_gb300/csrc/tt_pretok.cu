@@ -606,31 +606,50 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 3 : 5) k_pretok(Tables T, Work
 
   // --- effective kinds (o200k: resolve marks with a max-scan entering at ts - 32)
   if (fam == FAM_O200K) {
+    // (each pass slides the previous, own and next words along the thread's
+    // chars: one shared-memory load a char)
+    constexpr uint32_t PAST = 1u << 29;      // past the window's chars: reads as a request start
     int2 v = make_int2(-1, -1);
-    for (int j = c0; j < c1; ++j) {
-      const int64_t pos = ws + S.lead(j);
-      if (pos < ts - S1_SHIFT) continue;
-      const bool in_prev = !S.rs(j) && j > 0;
-      const uint8_t rp = in_prev ? S.raw(j - 1) : K_NONE;
-      const uint32_t cpp = in_prev ? S.cp8(j - 1) : 0;
-      const uint8_t rn = (j + 1 < S.nch && !S.rs(j + 1)) ? S.raw(j + 1) : K_NONE;
-      if (region_start(S.raw(j), rp)) v.x = (int)pos;
-      if (trigger(S.raw(j), rp, cpp, rn)) v.y = (int)pos;
+    if (c0 < c1) {
+      uint32_t wp = c0 > 0 ? S.ci[c0 - 1] : 0, w0 = S.ci[c0];
+      for (int j = c0; j < c1; ++j) {
+        const uint32_t wn = j + 1 < S.nch ? S.ci[j + 1] : PAST;
+        const int64_t pos = ws + ci_lead(w0);
+        if (pos >= ts - S1_SHIFT) {
+          const bool in_prev = !ci_rs(w0) && j > 0;
+          const uint8_t rp = in_prev ? ci_raw(wp) : K_NONE;
+          const uint32_t cpp = in_prev ? ci_cp8(wp) : 0;
+          const uint8_t rn = !ci_rs(wn) ? ci_raw(wn) : K_NONE;
+          if (region_start(ci_raw(w0), rp)) v.x = (int)pos;
+          if (trigger(ci_raw(w0), rp, cpp, rn)) v.y = (int)pos;
+        }
+        wp = w0;
+        w0 = wn;
+      }
     }
     auto mx = [](int2 a, int2 b) { return make_int2(max(a.x, b.x), max(a.y, b.y)); };
     int2 ex = block_exclusive_scan<NT>(v, mx, make_int2(-1, -1), P.i2_tmp, (int2 *)nullptr);
     int2 run = mx(P.s1c, ex);
-    for (int j = c0; j < c1; ++j) {
-      const int64_t pos = ws + S.lead(j);
-      if (pos < ts - S1_SHIFT) { S.set_eff(j, effective(fam, S.raw(j), false)); continue; }
-      const bool in_prev = !S.rs(j) && j > 0;
-      const uint8_t rp = in_prev ? S.raw(j - 1) : K_NONE;
-      const uint32_t cpp = in_prev ? S.cp8(j - 1) : 0;
-      const uint8_t rn = (j + 1 < S.nch && !S.rs(j + 1)) ? S.raw(j + 1) : K_NONE;
-      if (region_start(S.raw(j), rp)) run.x = (int)pos;
-      if (trigger(S.raw(j), rp, cpp, rn)) run.y = (int)pos;
-      const bool mark_other = S.raw(j) == K_MARK && run.x >= 0 && run.y >= run.x;
-      S.set_eff(j, effective(fam, S.raw(j), mark_other));
+    if (c0 < c1) {
+      uint32_t wp = c0 > 0 ? S.ci[c0 - 1] : 0, w0 = S.ci[c0];
+      for (int j = c0; j < c1; ++j) {
+        const uint32_t wn = j + 1 < S.nch ? S.ci[j + 1] : PAST;
+        const int64_t pos = ws + ci_lead(w0);
+        const uint8_t r0 = ci_raw(w0);
+        bool mark_other = false;
+        if (pos >= ts - S1_SHIFT) {
+          const bool in_prev = !ci_rs(w0) && j > 0;
+          const uint8_t rp = in_prev ? ci_raw(wp) : K_NONE;
+          const uint32_t cpp = in_prev ? ci_cp8(wp) : 0;
+          const uint8_t rn = !ci_rs(wn) ? ci_raw(wn) : K_NONE;
+          if (region_start(r0, rp)) run.x = (int)pos;
+          if (trigger(r0, rp, cpp, rn)) run.y = (int)pos;
+          mark_other = r0 == K_MARK && run.x >= 0 && run.y >= run.x;
+        }
+        S.ci[j] = (w0 & ~(0xFu << 25)) | ((uint32_t)effective(fam, r0, mark_other) << 25);
+        wp = w0;
+        w0 = wn;
+      }
     }
   } else {
     for (int j = c0; j < c1; ++j) {
