@@ -70,6 +70,24 @@ struct ByteWin {
   int r0, r1;
 };
 
+// The first index i in [0, n) with a[i] >= v (n if none), a ascending, by
+// one whole warp: each step splits the interval into 32 parts and one load a
+// lane finds the part holding the answer (two steps for up to 1,024
+// requests, instead of one dependent load per halving).
+__device__ __forceinline__ int64_t warp_lower_bound64(const int64_t *a, int64_t n, int64_t v) {
+  const int lane = threadIdx.x & 31;
+  int64_t lo = 0, hi = n;                   // the answer lies in [lo, hi]
+  while (lo < hi) {
+    const int64_t step = (hi - lo + 31) / 32;
+    const int64_t idx = lo + (int64_t)(lane + 1) * step - 1;   // last index of part lane
+    const bool less = idx < hi && __ldg(&a[idx]) < v;
+    const int k = __popc(__ballot_sync(0xffffffffu, less));     // parts wholly below v (a prefix)
+    lo += (int64_t)k * step;                // every index below is < v
+    hi = min(hi, lo + step - 1);            // part k's last index (if tested) is >= v
+  }
+  return lo;
+}
+
 __device__ __forceinline__ int64_t lower_bound64(const int64_t *a, int64_t n, int64_t v) {
   int64_t lo = 0, hi = n;
   while (lo < hi) {
@@ -107,7 +125,10 @@ __device__ __forceinline__ uint32_t decode_at(const WS &S, int64_t ws, int64_t t
 
 // Load the bytes of the window [ws, ws + WIN) and mark request starts.  All
 // threads participate.  src: where to read the batch (NULL: A.utf8).
-template <int NT, class WS>
+// WARP_SEARCH: warps 0 and 1 find the window's request range (the pre-pass,
+// whose tiles wait on it); else thread 0 bisects (the pre-tokenizer, whose
+// batch variant keeps its register count lower that way).
+template <int NT, class WS, bool WARP_SEARCH = false>
 __device__ void load_bytes(const Tables &T, const CallArgs &A, int64_t base, int64_t total, int64_t ws, WS &S,
                            const uint8_t *src = nullptr) {
   constexpr int PT_BYTES = WIN / NT;
@@ -129,11 +150,17 @@ __device__ void load_bytes(const Tables &T, const CallArgs &A, int64_t base, int
   for (int k = 0; k < PT_BYTES; ++k) S.rsb[PT_BYTES * tid + k] = 0;
   if (tid < 8) { S.bytes[WIN + tid] = 0; S.rsb[WIN + tid] = 0; }
   if (tid < 128) S.ascii[tid] = __ldg(&T.cls2[(uint32_t)__ldg(&T.cls1[0]) * 256u + tid]);
-  if (tid == 0) {
-    const int64_t lo = ws < 0 ? 0 : ws;
-    const int64_t hi = ws + WIN < total ? ws + WIN : total;
-    S.r0 = (int)lower_bound64(A.offs, A.n, base + lo);
-    S.r1 = (int)lower_bound64(A.offs, A.n, base + hi);
+  const int64_t wlo = ws < 0 ? 0 : ws;
+  const int64_t whi = ws + WIN < total ? ws + WIN : total;
+  if constexpr (WARP_SEARCH) {
+    if (tid < 64) {
+      const int r = (int)warp_lower_bound64(A.offs, A.n, base + (tid < 32 ? wlo : whi));
+      if (tid == 0) S.r0 = r;
+      if (tid == 32) S.r1 = r;
+    }
+  } else if (tid == 0) {
+    S.r0 = (int)lower_bound64(A.offs, A.n, base + wlo);
+    S.r1 = (int)lower_bound64(A.offs, A.n, base + whi);
   }
   __syncthreads();
   for (int r = S.r0 + tid; r < S.r1; r += NT) {
@@ -210,7 +237,7 @@ __global__ void __launch_bounds__(NT) k_prepass(Tables T, Work W) {
     W.ids_agg[c] = 0;
   // bytes and request starts suffice: the few chars the summaries look at
   // are decoded where they are met
-  load_bytes<NT>(T, A, base, total, ws, S, A.utf8_src);
+  load_bytes<NT, ByteWin, true>(T, A, base, total, ws, S, A.utf8_src);
   // this thread's bytes as words, and which of them lie in the tile
   uint32_t wd[PT_BYTES / 4];
 #pragma unroll
