@@ -93,8 +93,6 @@ __device__ __forceinline__ int vocab_probe(const Tables &T, const uint8_t *b, in
   }
 }
 
-__device__ __forceinline__ int rank_or_max(int r) { return r < 0 ? INT_MAX : r; }
-
 // the rest of a pair lookup whose first probe e (slot s) is already loaded
 __device__ __forceinline__ int2 pair_finish(const Tables &T, uint4 e, uint32_t s, int l, int r) {
   for (;;) {
