@@ -37,3 +37,18 @@ def concat_requests(strings):
     offs = np.zeros(len(bs) + 1, dtype=np.int64)
     np.cumsum([len(b) for b in bs], out=offs[1:])
     return b"".join(bs), offs
+
+
+def permute_vocab(merges, vb, vo, seed):
+    """The same vocabulary under a random renumbering of all its token IDs
+    (byte tokens included): returns (merges, vocab_bytes, vocab_offsets,
+    perm) with old ID i renamed perm[i].  Rank order is unchanged."""
+    n = len(vo) - 1
+    perm = np.random.default_rng(seed).permutation(n).astype(np.int64)
+    inv = np.empty(n, dtype=np.int64)
+    inv[perm] = np.arange(n)
+    toks = [bytes(vb[vo[inv[j]]:vo[inv[j] + 1]]) for j in range(n)]
+    offs = np.zeros(n + 1, dtype=np.int64)
+    np.cumsum([len(t) for t in toks], out=offs[1:])
+    m = perm[np.asarray(merges, dtype=np.int64)].astype(np.int32)
+    return m, np.frombuffer(b"".join(toks), dtype=np.uint8).copy(), offs, perm

@@ -188,6 +188,21 @@ def test_out_of_order_merges_on_small_alphabets(cuda, large):
     check(cuda, (merges, vb, vo), 1, reqs)
 
 
+@pytest.mark.parametrize("large", [False, True])
+def test_renumbered_token_ids(cuda, vocabs, large):
+    """The 100K-merge vocabulary with every token ID renumbered at random
+    (byte tokens included): the byte-to-token map, the direct byte-pair and
+    context tables and the hashed tables must all go through IDs, never
+    assume that byte b is token b.  large: a batch beyond 4 MiB."""
+    from conftest import permute_vocab
+    m, vb, vo = vocabs["c1"]
+    pm, pvb, pvo, _ = permute_vocab(m, vb, vo, 8)
+    reqs = [synth.transcript(40 + i, 20000, synth.PROFILE_MIXED) for i in range(8)]
+    if large:
+        reqs.append(synth.transcript(49, 3_500_000, synth.PROFILE_MIXED))
+    check(cuda, (pm, pvb, pvo), 1, reqs)
+
+
 # ------------------------------------------------------------ edge cases
 def test_empty_and_degenerate_batches(cuda, vocabs):
     merges, vb, vo = vocabs["small1"]

@@ -256,6 +256,17 @@ def test_safe_pair_rounds_planted_minimum_mistake_is_caught():
                for w in words)
 
 
+def test_renumbered_token_ids(small_vocabs):
+    """Token IDs are names: renumbering every ID (byte tokens included, the
+    rank order kept) renames the output and changes nothing else."""
+    from conftest import permute_vocab
+    m, vb, vo = small_vocabs[1]
+    pm, pvb, pvo, perm = permute_vocab(m, vb, vo, 21)
+    o, po = oracle.Oracle(m, vb, vo, 1), oracle.Oracle(pm, pvb, pvo, 1)
+    text = synth.transcript(13, 40000, 1)
+    assert po.encode(text) == [int(perm[i]) for i in o.encode(text)]
+
+
 def test_seam_example():
     """tok(A) || tok(B) != tok(A || B) with A = ' pipe', B = 'line' on a
     vocabulary that holds ' pipe', 'line' and ' pipeline' (TokTier §3.1,
